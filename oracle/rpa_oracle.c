@@ -1,0 +1,256 @@
+/*
+ * rpa_oracle.c -- plain, slow, fp64 CPU oracle for ragged paged attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header or constant table with the CUDA
+ * library.
+ *
+ * What it computes is the plain definition the "ragged_paged.zig" page
+ * reaches with its blockwise online softmax (sections flashAttention and run):
+ * for every sequence s, every query token i of s and every query head qh,
+ *
+ *   kv head      h   = qh / G,  G = num_q_heads / num_kv_heads     (GQA group)
+ *   position     p   = kv_len - q_len + i                      (row_ids)
+ *   key j        K_j = dec(kv_pages[page_indices[s, j/ps], j%ps, 2h,   :]) * k_scale
+ *   value j      V_j = dec(kv_pages[page_indices[s, j/ps], j%ps, 2h+1, :]) * v_scale
+ *   logit        x_j = sm_scale * <q_i, K_j>,  then cap*tanh(x_j/cap) if soft_cap
+ *   allowed(j)   j < kv_len, and (not causal or j <= p),
+ *                and (no window or not (p - sliding_window >= j))
+ *   o            = sum_j w_j V_j / sum_j w_j,  w_j = exp(x_j - max x) on allowed j
+ *
+ * Readings where the page is silent or literal-but-quirky (kept in one place):
+ *  - masked keys get weight exactly 0 (the page adds mask_value, whose exp
+ *    underflows to 0 whenever a row has an allowed key);
+ *  - keys j >= kv_len are always excluded, also when not causal;
+ *  - a row with no allowed key is 0 (the page's l_safe guard);
+ *  - dequant is exact fp64 x*scale (the page rounds it to the q dtype);
+ *  - tokens not covered by [cu_q_lens[0], cu_q_lens[num_seqs]) are 0.
+ *
+ * Decoders follow the formats' definitions: bf16 is the top half of an IEEE
+ * binary32; e4m3fn has bias 7, 3 mantissa bits, subnormals, no infinities,
+ * S.1111.111 = NaN, max 448.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+typedef struct {
+    int64_t num_q_tokens, num_q_heads, num_kv_heads, head_dim;
+    int64_t total_num_pages, page_size, max_num_seqs, pages_per_seq;
+    int32_t kv_is_fp8; /* 0: bf16 K/V bits, 1: fp8 e4m3fn bytes */
+    int32_t is_causal;
+    double sm_scale;
+    int32_t has_soft_cap;
+    int32_t has_k_scale;
+    double soft_cap;
+    double k_scale;
+    int32_t has_v_scale;
+    int32_t has_sliding_window;
+    double v_scale;
+    int64_t sliding_window;
+} OracleCfg;
+
+enum { OR_OK = 0, OR_INVALID_ARG = 1, OR_BAD_PAGE_INDEX = 4, OR_BAD_LENGTHS = 5 };
+
+/* bf16: the 16 stored bits are the upper half of an IEEE-754 binary32. */
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* fp8 e4m3fn (OCP FP8): 1 sign, 4 exponent (bias 7), 3 mantissa bits. */
+double oracle_e4m3_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xF;
+    int m = b & 0x7;
+    double v;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, 1 - 7); /* subnormal */
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Mask of the page (flashAttention): a key is dropped when it is past the
+ * sequence, when causal and j > p, or when p - sliding_window >= j. */
+static int key_allowed(const OracleCfg* c, int64_t kv_len, int64_t p, int64_t j) {
+    if (j >= kv_len) return 0;
+    if (c->is_causal && j > p) return 0;
+    if (c->has_sliding_window && p - c->sliding_window >= j) return 0;
+    return 1;
+}
+
+static double kv_elem(const OracleCfg* c, const void* kv, int64_t page, int64_t slot,
+                      int64_t comb_head, int64_t d) {
+    int64_t idx = ((page * c->page_size + slot) * (2 * c->num_kv_heads) + comb_head) * c->head_dim + d;
+    if (c->kv_is_fp8) return oracle_e4m3_to_f64(((const uint8_t*)kv)[idx]);
+    return oracle_bf16_to_f64(((const uint16_t*)kv)[idx]);
+}
+
+/* Lengths / page-table validity, stated as the preconditions of the method.
+ * Returns OR_OK, OR_BAD_LENGTHS or OR_BAD_PAGE_INDEX (lengths checked first). */
+int rpa_oracle_validate(const OracleCfg* c, const int32_t* kv_lens, const int32_t* page_indices,
+                        const int32_t* cu_q_lens, int32_t num_seqs) {
+    if (num_seqs < 0 || num_seqs > c->max_num_seqs) return OR_BAD_LENGTHS;
+    if (cu_q_lens[0] < 0) return OR_BAD_LENGTHS;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int64_t q0 = cu_q_lens[s], q1 = cu_q_lens[s + 1], kl = kv_lens[s];
+        if (q1 < q0) return OR_BAD_LENGTHS;
+        if (kl < 0 || kl > c->pages_per_seq * c->page_size) return OR_BAD_LENGTHS;
+        if (q1 - q0 > kl) return OR_BAD_LENGTHS;
+    }
+    if (cu_q_lens[num_seqs] > c->num_q_tokens) return OR_BAD_LENGTHS;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        int64_t kl = kv_lens[s];
+        int64_t np = (kl + c->page_size - 1) / c->page_size;
+        for (int64_t j = 0; j < np; ++j) {
+            int32_t pg = page_indices[(int64_t)s * c->pages_per_seq + j];
+            if (pg < 0 || pg >= c->total_num_pages) return OR_BAD_PAGE_INDEX;
+        }
+    }
+    return OR_OK;
+}
+
+/* One output row: query token t (of sequence s, local index i), query head qh.
+ * scratch holds kv_len doubles. */
+static void one_row(const OracleCfg* c, const uint16_t* q, const void* kv, const int32_t* kv_lens,
+                    const int32_t* page_indices, const int32_t* cu_q_lens, int32_t s, int64_t t,
+                    int64_t qh, double* out, double* x) {
+    const int64_t D = c->head_dim;
+    const int64_t G = c->num_q_heads / c->num_kv_heads;
+    const int64_t h = qh / G;
+    const int64_t q_len = (int64_t)cu_q_lens[s + 1] - cu_q_lens[s];
+    const int64_t kv_len = kv_lens[s];
+    const int64_t i = t - cu_q_lens[s];
+    const int64_t p = kv_len - q_len + i;
+    const double ks = c->has_k_scale ? c->k_scale : 1.0;
+    const double vs = c->has_v_scale ? c->v_scale : 1.0;
+    const uint16_t* qrow = q + (t * c->num_q_heads + qh) * D;
+
+    for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
+    double xmax = -INFINITY;
+    int any = 0;
+    for (int64_t j = 0; j < kv_len; ++j) {
+        if (!key_allowed(c, kv_len, p, j)) continue;
+        int64_t page = page_indices[(int64_t)s * c->pages_per_seq + j / c->page_size];
+        int64_t slot = j % c->page_size;
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; ++d)
+            dot += oracle_bf16_to_f64(qrow[d]) * (kv_elem(c, kv, page, slot, 2 * h, d) * ks);
+        double xj = c->sm_scale * dot;
+        if (c->has_soft_cap) xj = c->soft_cap * tanh(xj / c->soft_cap);
+        x[j] = xj;
+        if (!any || xj > xmax) xmax = xj;
+        any = 1;
+    }
+    if (!any) return; /* no allowed key: row is 0 */
+    double denom = 0.0;
+    for (int64_t j = 0; j < kv_len; ++j) {
+        if (!key_allowed(c, kv_len, p, j)) continue;
+        double w = exp(x[j] - xmax);
+        denom += w;
+        int64_t page = page_indices[(int64_t)s * c->pages_per_seq + j / c->page_size];
+        int64_t slot = j % c->page_size;
+        for (int64_t d = 0; d < D; ++d) out[d] += w * (kv_elem(c, kv, page, slot, 2 * h + 1, d) * vs);
+    }
+    for (int64_t d = 0; d < D; ++d) out[d] /= denom;
+}
+
+static int32_t seq_of_token(const int32_t* cu_q_lens, int32_t num_seqs, int64_t t) {
+    /* Last s with cu_q_lens[s] <= t < cu_q_lens[s+1]; -1 if none. */
+    for (int32_t s = 0; s < num_seqs; ++s)
+        if (t >= cu_q_lens[s] && t < cu_q_lens[s + 1]) return s;
+    return -1;
+}
+
+typedef struct {
+    const OracleCfg* c;
+    const uint16_t* q;
+    const void* kv;
+    const int32_t* kv_lens;
+    const int32_t* page_indices;
+    const int32_t* cu_q_lens;
+    int32_t num_seqs;
+    const int64_t* rows; /* (token, q head) pairs, or NULL for all rows */
+    int64_t nrows;
+    double* out;
+    int64_t next;
+    int64_t max_kv;
+} Job;
+
+static void* worker(void* arg) {
+    Job* jb = (Job*)arg;
+    const OracleCfg* c = jb->c;
+    const int64_t D = c->head_dim;
+    double* x = (double*)malloc(sizeof(double) * (size_t)(jb->max_kv > 0 ? jb->max_kv : 1));
+    for (;;) {
+        int64_t r = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
+        if (r >= jb->nrows) break;
+        int64_t t, qh;
+        if (jb->rows) {
+            t = jb->rows[2 * r];
+            qh = jb->rows[2 * r + 1];
+        } else {
+            t = r / c->num_q_heads;
+            qh = r % c->num_q_heads;
+        }
+        double* o = jb->out + r * D;
+        int32_t s = seq_of_token(jb->cu_q_lens, jb->num_seqs, t);
+        if (s < 0) {
+            for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+            continue;
+        }
+        one_row(c, jb->q, jb->kv, jb->kv_lens, jb->page_indices, jb->cu_q_lens, s, t, qh, o, x);
+    }
+    free(x);
+    return NULL;
+}
+
+static int run_job(Job* jb, int nthreads) {
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    jb->max_kv = 0;
+    for (int32_t s = 0; s < jb->num_seqs; ++s)
+        if (jb->kv_lens[s] > jb->max_kv) jb->max_kv = jb->kv_lens[s];
+    pthread_t th[256];
+    int started = 0;
+    for (int k = 0; k < nthreads; ++k) {
+        if (pthread_create(&th[k], NULL, worker, jb) != 0) break;
+        ++started;
+    }
+    if (started == 0) worker(jb);
+    for (int k = 0; k < started; ++k) pthread_join(th[k], NULL);
+    return started > 0 ? started : 1;
+}
+
+/* All rows: out[num_q_tokens, num_q_heads, head_dim] in fp64.
+ * Returns the number of threads used, or -code on invalid input. */
+int rpa_oracle_forward(const OracleCfg* c, const uint16_t* q, const void* kv_pages,
+                       const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
+                       int32_t num_seqs, double* out, int nthreads) {
+    if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return -OR_INVALID_ARG;
+    int v = rpa_oracle_validate(c, kv_lens, page_indices, cu_q_lens, num_seqs);
+    if (v) return -v;
+    Job jb = {c, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, NULL,
+              c->num_q_tokens * c->num_q_heads, out, 0, 0};
+    return run_job(&jb, nthreads);
+}
+
+/* Selected rows only: rows = nrows (token, q head) int64 pairs; out[nrows, head_dim]. */
+int rpa_oracle_rows(const OracleCfg* c, const uint16_t* q, const void* kv_pages, const int32_t* kv_lens,
+                    const int32_t* page_indices, const int32_t* cu_q_lens, int32_t num_seqs,
+                    const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+    if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return -OR_INVALID_ARG;
+    int v = rpa_oracle_validate(c, kv_lens, page_indices, cu_q_lens, num_seqs);
+    if (v) return -v;
+    Job jb = {c, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, rows, nrows, out, 0, 0};
+    return run_job(&jb, nthreads);
+}

@@ -1,0 +1,291 @@
+"""Seeded synthetic inputs for ragged paged attention.
+
+This module only *draws* inputs: sequence lengths, a shuffled page table,
+queries and the paged K/V cache.  It holds none of the attention arithmetic,
+so both the CUDA path and the CPU oracle can consume the same bytes.
+
+Layouts follow the "ragged_paged.zig" page (kernel arguments of ``run``):
+
+* ``q``            [num_q_tokens, num_q_heads, head_dim]   bf16 bits (uint16)
+* ``kv_pages``     [total_num_pages, page_size, 2*num_kv_heads, head_dim]
+                   bf16 bits (uint16) or fp8 e4m3fn bytes (uint8); combined
+                   head 2h is K of kv head h, 2h+1 is V of kv head h.
+* ``kv_lens``      [max_num_seqs]                 int32
+* ``page_indices`` [max_num_seqs, pages_per_seq]  int32
+* ``cu_q_lens``    [max_num_seqs + 1]             int32
+
+Recipe (fixed, so every run sees the same bytes):
+
+1. ``default_rng([seed, 0])`` draws the lengths, then a permutation of the
+   physical pages, then the page ids of unused page-table entries.
+2. Logical pages of the sequences take the permutation in order (sequence 0's
+   pages first), so physical placement is shuffled.
+3. ``q`` and ``kv_pages`` are filled chunk by chunk (2**22 elements per chunk)
+   from ``default_rng([seed, 1, chunk])`` and ``default_rng([seed, 2, chunk])``.
+   Every element of ``kv_pages`` is drawn, tail slots and unused pages too.
+4. Values are N(0, 1) in float32, rounded to bf16 with round-to-nearest-even.
+   fp8 K/V values are ``clip(N(0,1) / 0.05, -448, 448)`` rounded to e4m3fn.
+"""
+
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+
+MASK_VALUE = -2.38197633e38  # "ragged_paged.zig", Cfg.mask_value default
+CHUNK = 1 << 22
+
+
+@dataclass
+class Problem:
+    """One ragged paged attention call: configuration plus host arrays."""
+
+    num_q_tokens: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    total_num_pages: int
+    page_size: int
+    max_num_seqs: int
+    pages_per_seq: int
+    kv_dtype: str  # "bf16" or "fp8_e4m3"
+    sm_scale: float
+    soft_cap: float | None = None
+    k_scale: float | None = None
+    v_scale: float | None = None
+    is_causal: bool = True
+    sliding_window: int | None = None
+    mask_value: float = MASK_VALUE
+    num_seqs: int = 0
+    q: np.ndarray = field(default=None, repr=False)
+    kv_pages: np.ndarray = field(default=None, repr=False)
+    kv_lens: np.ndarray = field(default=None, repr=False)
+    page_indices: np.ndarray = field(default=None, repr=False)
+    cu_q_lens: np.ndarray = field(default=None, repr=False)
+    name: str = "custom"
+
+    def cfg_dict(self) -> dict:
+        return dict(
+            num_q_tokens=self.num_q_tokens, num_q_heads=self.num_q_heads,
+            num_kv_heads=self.num_kv_heads, head_dim=self.head_dim,
+            total_num_pages=self.total_num_pages, page_size=self.page_size,
+            max_num_seqs=self.max_num_seqs, pages_per_seq=self.pages_per_seq,
+            kv_dtype=self.kv_dtype, sm_scale=self.sm_scale,
+            soft_cap=self.soft_cap, k_scale=self.k_scale, v_scale=self.v_scale,
+            is_causal=self.is_causal, sliding_window=self.sliding_window,
+            mask_value=self.mask_value)
+
+    @property
+    def q_lens(self) -> np.ndarray:
+        cu = self.cu_q_lens[: self.num_seqs + 1].astype(np.int64)
+        return np.diff(cu)
+
+    @property
+    def seq_kv_lens(self) -> np.ndarray:
+        return self.kv_lens[: self.num_seqs].astype(np.int64)
+
+
+# ---------------------------------------------------------------- encoders
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (nearest, ties to even); returns uint16 bits.
+
+    Inputs are finite, so no NaN special case is needed."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).copy()
+    u += ((u >> 16) & np.uint32(1)) + np.uint32(0x7FFF)
+    return (u >> 16).astype(np.uint16)
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 (already within +-448) to fp8 e4m3fn bytes via torch."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------- fills
+def _fill(out_flat: np.ndarray, seed: int, stream: int, kind: str,
+          threads: int | None = None) -> None:
+    n = out_flat.size
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def work(c: int) -> None:
+        lo = c * CHUNK
+        hi = min(n, lo + CHUNK)
+        rng = np.random.default_rng([seed, stream, c])
+        x = rng.standard_normal(hi - lo, dtype=np.float32)
+        if kind == "bf16":
+            out_flat[lo:hi] = f32_to_bf16_bits(x)
+        else:
+            np.clip(x / np.float32(0.05), -448.0, 448.0, out=x)
+            out_flat[lo:hi] = f32_to_e4m3_bits(x)
+
+    threads = threads or min(32, os.cpu_count() or 1)
+    if nchunks <= 1:
+        for c in range(nchunks):
+            work(c)
+        return
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(work, range(nchunks)))
+
+
+def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
+          head_dim: int, page_size: int, pages_per_seq: int | None = None,
+          total_num_pages: int | None = None, kv_dtype: str = "bf16",
+          sm_scale: float | None = None, soft_cap=None, k_scale=None,
+          v_scale=None, is_causal: bool = True, sliding_window=None,
+          max_num_seqs: int | None = None, extra_tokens: int = 0,
+          extra_pages: int = 0, name: str = "custom",
+          rng_lengths: np.random.Generator | None = None) -> Problem:
+    """Build a problem with the given lengths (already drawn by the caller)."""
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    kv_lens_a = np.asarray(kv_lens, dtype=np.int64)
+    S = len(q_lens)
+    assert len(kv_lens_a) == S
+    npages = (kv_lens_a + page_size - 1) // page_size
+    if pages_per_seq is None:
+        pages_per_seq = max(1, int(npages.max()) if S else 1)
+    used = int(npages.sum())
+    if total_num_pages is None:
+        total_num_pages = max(1, used + extra_pages)
+    assert total_num_pages >= used
+    max_num_seqs = max_num_seqs or max(S, 1)
+    T = int(q_lens.sum()) + extra_tokens
+
+    rng = rng_lengths if rng_lengths is not None else np.random.default_rng([seed, 0])
+    perm = rng.permutation(total_num_pages).astype(np.int32)
+    page_indices = rng.integers(0, total_num_pages, size=(max_num_seqs, pages_per_seq),
+                                dtype=np.int64).astype(np.int32)
+    off = 0
+    for s in range(S):
+        n = int(npages[s])
+        page_indices[s, :n] = perm[off: off + n]
+        off += n
+
+    cu = np.zeros(max_num_seqs + 1, dtype=np.int32)
+    cu[1: S + 1] = np.cumsum(q_lens)
+    cu[S + 1:] = cu[S]
+    kvl = np.zeros(max_num_seqs, dtype=np.int32)
+    kvl[:S] = kv_lens_a
+
+    Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
+    q = np.empty((T, Hq, D), dtype=np.uint16)
+    _fill(q.reshape(-1), seed, 1, "bf16")
+    kv_np_dtype = np.uint16 if kv_dtype == "bf16" else np.uint8
+    kv = np.empty((total_num_pages, page_size, 2 * Hkv, D), dtype=kv_np_dtype)
+    _fill(kv.reshape(-1), seed, 2, "bf16" if kv_dtype == "bf16" else "fp8")
+
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    return Problem(
+        num_q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+        total_num_pages=total_num_pages, page_size=page_size,
+        max_num_seqs=max_num_seqs, pages_per_seq=pages_per_seq,
+        kv_dtype=kv_dtype, sm_scale=float(sm_scale), soft_cap=soft_cap,
+        k_scale=k_scale, v_scale=v_scale, is_causal=is_causal,
+        sliding_window=sliding_window, num_seqs=S, q=q, kv_pages=kv,
+        kv_lens=kvl, page_indices=page_indices, cu_q_lens=cu, name=name)
+
+
+# ---------------------------------------------------------------- the five workloads
+WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill")
+
+
+def workload(name: str) -> Problem:
+    """The five named workloads (seeds 0..4)."""
+    if name == "tiny":
+        # 3 sequences, q_lens {1,5,16}, kv_lens {17,40,64}, 16 physical pages.
+        return build(seed=0, q_lens=[1, 5, 16], kv_lens=[17, 40, 64], num_q_heads=4,
+                     num_kv_heads=2, head_dim=64, page_size=16, pages_per_seq=4,
+                     total_num_pages=16, sm_scale=1.0 / 8.0, name=name)
+    if name == "decode":
+        # Llama-3-8B-like decode: 256 x q_len 1, kv_len ~ U[512, 8192].
+        rng = np.random.default_rng([1, 0])
+        kl = rng.integers(512, 8192, size=256, endpoint=True)
+        return build(seed=1, q_lens=np.ones(256, np.int64), kv_lens=kl, num_q_heads=32,
+                     num_kv_heads=8, head_dim=128, page_size=16, pages_per_seq=512,
+                     sm_scale=1.0 / math.sqrt(128), name=name, rng_lengths=rng)
+    if name == "mixed":
+        # 8 chunked-prefill chunks of 512 tokens + 56 decodes (4152 tokens).
+        rng = np.random.default_rng([2, 0])
+        kl_pf = rng.integers(0, 16384, size=8, endpoint=True) + 512
+        kl_dec = rng.integers(1024, 32768, size=56, endpoint=True)
+        ql = np.concatenate([np.full(8, 512), np.ones(56, np.int64)])
+        kl = np.concatenate([kl_pf, kl_dec])
+        return build(seed=2, q_lens=ql, kv_lens=kl, num_q_heads=32, num_kv_heads=8,
+                     head_dim=128, page_size=32, pages_per_seq=1024,
+                     sm_scale=1.0 / math.sqrt(128), name=name, rng_lengths=rng)
+    if name == "fp8_window":
+        # Gemma-2-like knobs with fp8 e4m3 K/V.
+        rng = np.random.default_rng([3, 0])
+        ql = rng.integers(1, 64, size=128, endpoint=True)
+        kl = rng.integers(256, 16384, size=128, endpoint=True)
+        return build(seed=3, q_lens=ql, kv_lens=kl, num_q_heads=16, num_kv_heads=8,
+                     head_dim=256, page_size=16, pages_per_seq=1024, kv_dtype="fp8_e4m3",
+                     sm_scale=1.0 / 16.0, soft_cap=50.0, k_scale=0.05, v_scale=0.05,
+                     sliding_window=4096, name=name, rng_lengths=rng)
+    if name == "long_prefill":
+        # 4 fresh prefills of 8192 tokens, 64 q heads / 8 kv heads.
+        rng = np.random.default_rng([4, 0])
+        return build(seed=4, q_lens=[8192] * 4, kv_lens=[8192] * 4, num_q_heads=64,
+                     num_kv_heads=8, head_dim=128, page_size=64, pages_per_seq=128,
+                     total_num_pages=512, sm_scale=1.0 / math.sqrt(128), name=name,
+                     rng_lengths=rng)
+    raise KeyError(name)
+
+
+def random_small(seed: int, *, num_seqs: int = 3, max_q: int = 9, max_kv: int = 50,
+                 num_q_heads: int = 4, num_kv_heads: int = 2, head_dim: int = 64,
+                 page_size: int = 16, kv_dtype: str = "bf16", decode_only: bool = False,
+                 **knobs) -> Problem:
+    """A small random ragged batch (q_len <= kv_len) for tests."""
+    rng = np.random.default_rng([seed, 0])
+    kl = rng.integers(1, max_kv, size=num_seqs, endpoint=True)
+    if decode_only:
+        ql = np.ones(num_seqs, np.int64)
+    else:
+        ql = np.minimum(rng.integers(1, max_q, size=num_seqs, endpoint=True), kl)
+    return build(seed=seed, q_lens=ql, kv_lens=kl, num_q_heads=num_q_heads,
+                 num_kv_heads=num_kv_heads, head_dim=head_dim, page_size=page_size,
+                 kv_dtype=kv_dtype, rng_lengths=rng, extra_pages=3, **knobs)
+
+
+def algorithmic_work(p: Problem) -> dict:
+    """Algorithmic bytes and FLOPs of one call (keys in the allowed band only).
+
+    bytes = sum_s n_kv(s) * 2*Hkv*D*kv_elt + 2 * T_used*Hq*D*2 + 4*(pages used + 2S + 1)
+    flops = sum_s sum_i 4*Hq*D*n_allowed(s, i)
+    """
+    kv_elt = 2 if p.kv_dtype == "bf16" else 1
+    Hq, Hkv, D = p.num_q_heads, p.num_kv_heads, p.head_dim
+    byts = 0
+    pairs = 0
+    pages = 0
+    sw = p.sliding_window
+    for s in range(p.num_seqs):
+        ql = int(p.cu_q_lens[s + 1] - p.cu_q_lens[s])
+        kl = int(p.kv_lens[s])
+        if ql == 0:
+            continue
+        i = np.arange(ql, dtype=np.int64)
+        pos = kl - ql + i
+        hi = np.minimum(pos + 1, kl) if p.is_causal else np.full(ql, kl)
+        lo = np.maximum(pos - sw + 1, 0) if sw else np.zeros(ql, np.int64)
+        n_allowed = np.maximum(hi - lo, 0)
+        pairs += int(n_allowed.sum())
+        band_lo = int(lo.min())
+        band_hi = int(hi.max())
+        byts += (band_hi - band_lo) * 2 * Hkv * D * kv_elt
+        pages += (kl + p.page_size - 1) // p.page_size
+    t_used = int(p.cu_q_lens[p.num_seqs])
+    byts += 2 * t_used * Hq * D * 2 + 4 * (pages + 2 * p.num_seqs + 1)
+    return dict(bytes=byts, flops=4 * Hq * D * pairs, exps=Hq * pairs,
+                q_tokens=t_used)

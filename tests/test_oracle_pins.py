@@ -1,0 +1,331 @@
+"""Pins for the fp64 oracle, independent of the oracle's own code.
+
+Each pin is chosen so that a plausible slip in the oracle (a dropped scale, an
+off-by-one in the query position, a swapped K/V head, a wrong window edge, a
+mis-decoded fp8 code) fails at least one of them:
+
+* format decoders against numpy / torch casts and the formats' fixed points;
+* brute-force dense attention in numpy (explicit mask matrix, softmax over a
+  dense score matrix) on tiny unpaged inputs scattered into shuffled pages;
+* closed forms: uniform V, a single allowed key, one-key sequences;
+* the softcap identity c*tanh(x/c) = 2c*sigmoid(2x/c) - c of the
+  "from_qwen_ops.rs" page (``capped``) used as an independent formula;
+* invariants: page placement, decode = last prefill row, poisoned tails,
+  sequence order, GQA = MHA with repeated K/V.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rpa_inputs as ri
+from rpa_inputs import Problem
+
+
+# ------------------------------------------------------------------ helpers
+def dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, kv_dtype="bf16", **knobs):
+    """Dense per-sequence K/V/Q drawn here, then scattered into shuffled pages.
+
+    Returns (problem, dense) where dense[s] = (Q [ql,Hq,D], K [kl,Hkv,D], V [kl,Hkv,D])
+    as float64 values of the stored bits (before k/v scales)."""
+    S = len(q_lens)
+    npages = [(k + ps - 1) // ps for k in kv_lens]
+    N = sum(npages) + 2
+    P = max(npages + [1])
+    perm = rng.permutation(N)
+    page_indices = np.zeros((S, P), np.int32)
+    off = 0
+    for s in range(S):
+        page_indices[s, :npages[s]] = perm[off:off + npages[s]]
+        page_indices[s, npages[s]:] = perm[-1]
+        off += npages[s]
+    T = int(sum(q_lens))
+    q = ri.f32_to_bf16_bits(rng.standard_normal((T, Hq, D)).astype(np.float32))
+    if kv_dtype == "bf16":
+        kv = ri.f32_to_bf16_bits(rng.standard_normal((N, ps, 2 * Hkv, D)).astype(np.float32))
+        dec = ri.bf16_bits_to_f32
+    else:
+        x = np.clip(rng.standard_normal((N, ps, 2 * Hkv, D)) / 0.05, -448, 448).astype(np.float32)
+        kv = ri.f32_to_e4m3_bits(x)
+        dec = lambda b: torch.from_numpy(b).view(torch.float8_e4m3fn).float().numpy()
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    prob = Problem(num_q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                   total_num_pages=N, page_size=ps, max_num_seqs=S, pages_per_seq=P,
+                   kv_dtype=kv_dtype, num_seqs=S, q=q, kv_pages=kv,
+                   kv_lens=np.asarray(kv_lens, np.int32), page_indices=page_indices,
+                   cu_q_lens=cu, sm_scale=knobs.pop("sm_scale", 1.0 / math.sqrt(D)), **knobs)
+    qf = ri.bf16_bits_to_f32(q).astype(np.float64)
+    kvf = dec(kv).astype(np.float64)
+    dense = []
+    for s in range(S):
+        kl = kv_lens[s]
+        pg = page_indices[s, np.arange(kl) // ps]
+        slot = np.arange(kl) % ps
+        K = kvf[pg, slot][:, 0::2, :]
+        V = kvf[pg, slot][:, 1::2, :]
+        dense.append((qf[cu[s]:cu[s + 1]], K, V))
+    return prob, dense
+
+
+def brute(prob, dense, capped_form=False):
+    """Dense softmax attention with an explicit mask matrix, fp64."""
+    G = prob.num_q_heads // prob.num_kv_heads
+    ks = prob.k_scale or 1.0
+    vs = prob.v_scale or 1.0
+    out = np.zeros((prob.num_q_tokens, prob.num_q_heads, prob.head_dim))
+    for s, (Q, K, V) in enumerate(dense):
+        ql, kl = Q.shape[0], K.shape[0]
+        q0 = prob.cu_q_lens[s]
+        pos = kl - ql + np.arange(ql)[:, None]
+        col = np.arange(kl)[None, :]
+        allowed = np.ones((ql, kl), bool)
+        if prob.is_causal:
+            allowed &= col <= pos
+        if prob.sliding_window is not None:
+            allowed &= ~(pos - prob.sliding_window >= col)
+        for qh in range(prob.num_q_heads):
+            h = qh // G
+            x = prob.sm_scale * (Q[:, qh, :] @ (K[:, h, :] * ks).T)
+            if prob.soft_cap is not None:
+                c = prob.soft_cap
+                if capped_form:
+                    x = 2 * c / (1 + np.exp(-2 * x / c)) - c
+                else:
+                    x = c * np.tanh(x / c)
+            x = np.where(allowed, x, -np.inf)
+            m = x.max(axis=1, keepdims=True)
+            has = np.isfinite(m)
+            w = np.where(allowed, np.exp(x - np.where(has, m, 0.0)), 0.0)
+            den = w.sum(axis=1, keepdims=True)
+            o = (w @ (V[:, h, :] * vs)) / np.where(den > 0, den, 1.0)
+            out[q0:q0 + ql, qh, :] = o
+    return out
+
+
+def close(a, b, tol=1e-12):
+    scale = max(1.0, float(np.abs(b).max()))
+    err = float(np.abs(a - b).max()) / scale
+    assert err <= tol, err
+
+
+# ------------------------------------------------------------------ decoders
+def test_bf16_decoder_matches_float32_view():
+    for bits in list(range(0, 65536, 7)) + [0x3F80, 0xBF80, 0x7F7F, 0x0001, 0x8000]:
+        ref = float(np.array([bits << 16], np.uint32).view(np.float32)[0])
+        got = oracle.decode_bf16(bits)
+        assert (math.isnan(ref) and math.isnan(got)) or ref == got, bits
+
+
+def test_e4m3_decoder_all_codes():
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double()
+    for code in range(256):
+        got = oracle.decode_e4m3(code)
+        r = float(ref[code])
+        assert (math.isnan(r) and math.isnan(got)) or r == got, code
+    # fixed points of the format: max normal, min subnormal, 1, -1, NaN
+    assert oracle.decode_e4m3(0x7E) == 448.0
+    assert oracle.decode_e4m3(0x01) == 2.0 ** -9
+    assert oracle.decode_e4m3(0x08) == 2.0 ** -6
+    assert oracle.decode_e4m3(0x38) == 1.0
+    assert oracle.decode_e4m3(0xB8) == -1.0
+    assert math.isnan(oracle.decode_e4m3(0x7F)) and math.isnan(oracle.decode_e4m3(0xFF))
+
+
+# ------------------------------------------------------------------ brute force
+CASES = [
+    dict(q_lens=[1, 5, 16], kv_lens=[17, 40, 64], Hq=4, Hkv=2, D=64, ps=16),
+    dict(q_lens=[3, 1, 7, 2], kv_lens=[3, 9, 30, 2], Hq=4, Hkv=4, D=16, ps=4),
+    dict(q_lens=[6, 2], kv_lens=[20, 33], Hq=8, Hkv=2, D=16, ps=8, sliding_window=5),
+    dict(q_lens=[4, 4], kv_lens=[11, 4], Hq=2, Hkv=1, D=16, ps=4, soft_cap=0.7, sm_scale=0.9),
+    dict(q_lens=[5, 1], kv_lens=[9, 13], Hq=4, Hkv=2, D=16, ps=4, is_causal=False),
+    dict(q_lens=[5, 3], kv_lens=[9, 13], Hq=4, Hkv=2, D=16, ps=4, is_causal=False,
+         sliding_window=3),
+    dict(q_lens=[3, 8], kv_lens=[40, 21], Hq=4, Hkv=2, D=32, ps=8, kv_dtype="fp8_e4m3",
+         k_scale=0.05, v_scale=0.07, soft_cap=5.0, sliding_window=9, sm_scale=0.125),
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_oracle_equals_dense_brute_force(case):
+    kw = dict(CASES[case])
+    rng = np.random.default_rng(100 + case)
+    prob, dense = dense_problem(rng, kw.pop("q_lens"), kw.pop("kv_lens"), kw.pop("Hq"),
+                                kw.pop("Hkv"), kw.pop("D"), kw.pop("ps"), **kw)
+    close(oracle.forward(prob), brute(prob, dense))
+
+
+def test_softcap_identity_from_capped_form():
+    rng = np.random.default_rng(7)
+    prob, dense = dense_problem(rng, [4, 9], [12, 30], 4, 2, 32, 8, soft_cap=1.5, sm_scale=1.0)
+    close(oracle.forward(prob), brute(prob, dense, capped_form=True), 1e-12)
+    # with a cap the logits never leave [-cap, cap]: scaling q by 1e3 must not blow up
+    prob.q = ri.f32_to_bf16_bits(ri.bf16_bits_to_f32(prob.q) * 1000)
+    o = oracle.forward(prob)
+    assert np.isfinite(o).all()
+
+
+def test_mask_value_additive_reading():
+    """The page adds mask_value (-2.38e38) to masked logits; in f32 their exp is 0, so
+    the additive mask equals dropping the key whenever a row keeps >= 1 key."""
+    rng = np.random.default_rng(11)
+    prob, dense = dense_problem(rng, [6], [10], 2, 1, 16, 4, sm_scale=0.3)
+    Q, K, V = dense[0]
+    pos = 10 - 6 + np.arange(6)[:, None]
+    masked = np.arange(10)[None, :] > pos
+    x = (prob.sm_scale * (Q[:, 0, :] @ K[:, 0, :].T)).astype(np.float32)
+    x = x + np.where(masked, np.float32(ri.MASK_VALUE), np.float32(0))
+    w = np.exp(x - x.max(axis=1, keepdims=True))
+    o32 = (w @ V[:, 0, :]) / w.sum(axis=1, keepdims=True)
+    assert (w[masked] == 0).all()
+    close(oracle.forward(prob)[:, 0, :], o32, 1e-5)
+
+
+# ------------------------------------------------------------------ closed forms
+def test_uniform_v_gives_v():
+    rng = np.random.default_rng(3)
+    prob, _ = dense_problem(rng, [3, 7], [30, 17], 4, 2, 16, 4, soft_cap=3.0, sliding_window=6)
+    vals = ri.f32_to_bf16_bits(rng.standard_normal((2, 16)).astype(np.float32))
+    prob.kv_pages[:, :, 1, :] = vals[0]
+    prob.kv_pages[:, :, 3, :] = vals[1]
+    o = oracle.forward(prob)
+    v = ri.bf16_bits_to_f32(vals).astype(np.float64)
+    for qh in range(4):
+        close(o[:, qh, :], np.broadcast_to(v[qh // 2], o[:, qh, :].shape), 1e-14)
+
+
+def test_window_one_selects_own_position():
+    """sliding_window = 1 keeps exactly key p = kv_len - q_len + i, so o = V[p]."""
+    rng = np.random.default_rng(4)
+    prob, dense = dense_problem(rng, [4, 1], [9, 6], 2, 1, 16, 4, sliding_window=1)
+    o = oracle.forward(prob)
+    for s, (Q, K, V) in enumerate(dense):
+        ql, kl = Q.shape[0], K.shape[0]
+        for i in range(ql):
+            t = prob.cu_q_lens[s] + i
+            for qh in range(2):
+                close(o[t, qh], V[kl - ql + i, 0], 1e-14)
+
+
+def test_single_key_sequence():
+    rng = np.random.default_rng(5)
+    prob, dense = dense_problem(rng, [1, 1], [1, 1], 4, 2, 16, 4)
+    o = oracle.forward(prob)
+    for s, (Q, K, V) in enumerate(dense):
+        for qh in range(4):
+            close(o[s, qh], V[0, qh // 2], 1e-14)
+
+
+# ------------------------------------------------------------------ invariants
+def test_page_placement_invariance_bit_identical():
+    prob = ri.random_small(21, num_seqs=4, max_q=7, max_kv=60, page_size=8)
+    o1 = oracle.forward(prob)
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(prob.total_num_pages)  # new physical slot of each page
+    kv2 = np.empty_like(prob.kv_pages)
+    kv2[perm] = prob.kv_pages
+    prob.kv_pages = kv2
+    prob.page_indices = perm[prob.page_indices].astype(np.int32)
+    o2 = oracle.forward(prob)
+    assert np.array_equal(o1, o2)
+
+
+def test_decode_equals_last_prefill_row():
+    L = 37
+    pf = ri.build(seed=9, q_lens=[L], kv_lens=[L], num_q_heads=4, num_kv_heads=2, head_dim=32,
+                  page_size=8, sliding_window=20, soft_cap=2.0)
+    o_pf = oracle.forward(pf)
+    dec = ri.build(seed=9, q_lens=[1], kv_lens=[L], num_q_heads=4, num_kv_heads=2, head_dim=32,
+                   page_size=8, sliding_window=20, soft_cap=2.0)
+    dec.kv_pages = pf.kv_pages
+    dec.page_indices = pf.page_indices
+    dec.q = pf.q[L - 1:L].copy()
+    o_dec = oracle.forward(dec)
+    assert np.array_equal(o_dec[0], o_pf[L - 1])
+
+
+def test_tail_and_unused_pages_do_not_matter():
+    prob = ri.random_small(22, num_seqs=3, max_q=5, max_kv=45, page_size=16)
+    o1 = oracle.forward(prob)
+    kvf = prob.kv_pages.copy()
+    ps = prob.page_size
+    used = set()
+    for s in range(prob.num_seqs):
+        kl = int(prob.kv_lens[s])
+        for j in range((kl + ps - 1) // ps):
+            used.add(int(prob.page_indices[s, j]))
+    nan_bits = np.uint16(0x7FC0)
+    for pg in range(prob.total_num_pages):
+        if pg not in used:
+            kvf[pg] = nan_bits
+    for s in range(prob.num_seqs):
+        kl = int(prob.kv_lens[s])
+        if kl % ps:
+            kvf[prob.page_indices[s, kl // ps], kl % ps:] = nan_bits
+    prob.kv_pages = kvf
+    assert np.array_equal(o1, oracle.forward(prob))
+
+
+def test_sequence_order_invariance():
+    prob = ri.random_small(23, num_seqs=4, max_q=6, max_kv=40)
+    o1 = oracle.forward(prob)
+    order = [2, 0, 3, 1]
+    ql = prob.q_lens
+    cu = prob.cu_q_lens
+    q2 = np.concatenate([prob.q[cu[s]:cu[s + 1]] for s in order])
+    prob2 = ri.build(seed=23, q_lens=ql[order], kv_lens=prob.kv_lens[order], num_q_heads=4,
+                     num_kv_heads=2, head_dim=64, page_size=16,
+                     total_num_pages=prob.total_num_pages)
+    prob2.q = q2
+    prob2.kv_pages = prob.kv_pages
+    prob2.page_indices = prob.page_indices[order]
+    o2 = oracle.forward(prob2)
+    o1r = np.concatenate([o1[cu[s]:cu[s + 1]] for s in order])
+    assert np.array_equal(o1r, o2)
+
+
+def test_gqa_equals_mha_with_repeated_kv():
+    prob = ri.random_small(24, num_seqs=3, max_q=5, max_kv=30, num_q_heads=6, num_kv_heads=2,
+                           head_dim=16, page_size=4, soft_cap=4.0)
+    o1 = oracle.forward(prob)
+    G = 3
+    kv = prob.kv_pages  # [N, ps, 2*Hkv, D]
+    k = kv[:, :, 0::2]
+    v = kv[:, :, 1::2]
+    k = np.repeat(k, G, axis=2)
+    v = np.repeat(v, G, axis=2)
+    kv2 = np.empty(kv.shape[:2] + (2 * 6, kv.shape[3]), kv.dtype)
+    kv2[:, :, 0::2] = k
+    kv2[:, :, 1::2] = v
+    prob.kv_pages = kv2
+    prob.num_kv_heads = 6
+    assert np.array_equal(o1, oracle.forward(prob))
+
+
+def test_uncovered_tokens_are_zero():
+    prob = ri.build(seed=25, q_lens=[2, 3], kv_lens=[5, 9], num_q_heads=2, num_kv_heads=1,
+                    head_dim=16, page_size=4, extra_tokens=3)
+    o = oracle.forward(prob)
+    assert (o[5:] == 0).all() and (np.abs(o[:5]).sum() > 0)
+
+
+# ------------------------------------------------------------------ validation
+def test_validation_codes():
+    prob = ri.random_small(26, num_seqs=3)
+    assert oracle.validate(prob) == 0
+    bad = ri.random_small(26, num_seqs=3)
+    bad.page_indices[0, 0] = bad.total_num_pages
+    assert oracle.validate(bad) == 4
+    bad = ri.random_small(26, num_seqs=3)
+    bad.kv_lens[1] = bad.pages_per_seq * bad.page_size + 1
+    assert oracle.validate(bad) == 5
+    bad = ri.random_small(26, num_seqs=3)
+    bad.kv_lens[2] = int(bad.cu_q_lens[3] - bad.cu_q_lens[2]) - 1
+    assert oracle.validate(bad) == 5
+    bad = ri.random_small(26, num_seqs=3)
+    bad.cu_q_lens[2] = bad.cu_q_lens[1] - 1
+    assert oracle.validate(bad) == 5
+    with pytest.raises(oracle.OracleError):
+        oracle.forward(bad)

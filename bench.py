@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Ragged paged attention benchmark (one JSON line on stdout).
+
+A step is one full call of the library -- planner, decode attention, prefill
+attention, split-KV combine -- over one batch of the workload, with inputs
+resident in HBM.  The default workload is the Llama-3-8B-like decode batch:
+256 sequences, q_len 1, kv_len ~ U[512, 8192], 32 q heads / 8 kv heads,
+head_dim 128, page_size 16, bf16 (seeded synthetic data).  Its K/V cache
+(about 4.6 GB) is far larger than L2, so no flush is needed between steps.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--workload NAME] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only reference this project
+has) on the host cores, on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs its own replica of the batch (weak
+scaling, no collective on the data path); rank 0 prints the line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import rpa_inputs as ri  # noqa: E402
+
+METRIC = "ragged paged attn tokens/s; decode HBM GB/s & prefill TFLOP/s vs roofline"
+KERNEL_NAMES = ("planner", "decode_attention", "prefill_attention", "combine")
+KERNEL_SOURCES = {
+    "decode_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_attn_mma.cu",
+                         "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
+    "prefill_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_attn_mma.cu",
+                          "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
+}
+DESCR = {
+    "tiny": "3 seqs q_len {1,5,16} kv_len {17,40,64}, Hq 4 / Hkv 2, D 64, page 16, bf16",
+    "decode": "256 seqs x q_len 1, kv_len~U[512,8192], Hq 32 / Hkv 8, D 128, page 16, bf16",
+    "mixed": "8 prefill chunks x 512 + 56 decodes (4152 tokens), Hq 32 / Hkv 8, D 128, page 32, bf16",
+    "fp8_window": "128 seqs q_len~U{1..64} kv_len~U[256,16384], Hq 16 / Hkv 8, D 256, page 16, "
+                  "fp8 e4m3 K/V, softcap 50, window 4096",
+    "long_prefill": "4 seqs x 8192 fresh prefill, Hq 64 / Hkv 8, D 128, page 64, bf16",
+    "decode_quarter": "64 seqs x q_len 1, kv_len~U[512,8192], Hq 32 / Hkv 8, D 128, page 16, bf16",
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=list(ri.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def sources_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram bytes per launch from profiles/kernel_traffic.txt, if taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
+        return None
+    sha = sources_sha(KERNEL_SOURCES[kernel])
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and \
+                    parts[1] == workload and parts[2] == sha:
+                return float(parts[3])
+    return None
+
+
+class Clocks:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.proc = None
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if uuid:
+                cmd += ["-i", uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(prob, budget_s=12.0, max_reps=8):
+    """The oracle as it stands, on the host cores, over the whole batch or a sample."""
+    import oracle
+
+    T = int(prob.cu_q_lens[prob.num_seqs])
+    rows_all = np.stack(np.meshgrid(np.arange(T), np.arange(prob.num_q_heads), indexing="ij"),
+                        axis=-1).reshape(-1, 2).astype(np.int64)
+    # size the sample from one small probe so the run stays within budget
+    probe = rows_all[: max(1, min(len(rows_all), 64))]
+    t0 = time.perf_counter()
+    _, threads = oracle.rows(prob, probe, return_threads=True)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    n = int(min(len(rows_all), max(prob.num_q_heads, budget_s / max(per_row, 1e-9))))
+    n -= n % prob.num_q_heads or 0
+    n = max(n, prob.num_q_heads)
+    sample = rows_all[:n]
+    done, t0 = 0, time.perf_counter()
+    reps = 0
+    while reps < max_reps:
+        oracle.rows(prob, sample)
+        done += len(sample)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    tokens = done / prob.num_q_heads
+    return {"value": tokens / el, "unit": "tokens/s", "cores": int(threads), "kind": "oracle",
+            "sample": f"first {n // prob.num_q_heads} of {T} query tokens (all {prob.num_q_heads} heads)"
+                      f" x {reps} reps, {el:.1f} s"}
+
+
+def run_reference(args, rank):
+    """--impl reference: the fp64 oracle on the host cores, same metric and workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    prob = ri.workload(args.workload)
+    T = int(prob.cu_q_lens[prob.num_seqs])
+    rows_all = np.stack(np.meshgrid(np.arange(T), np.arange(prob.num_q_heads), indexing="ij"),
+                        axis=-1).reshape(-1, 2).astype(np.int64)
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    t0 = time.perf_counter()
+    _, threads = oracle.rows(prob, rows_all[: prob.num_q_heads], return_threads=True)
+    per_tok = time.perf_counter() - t0
+    budget = 90.0 / (steps + warm)  # whole run within ~1.5 minutes
+    ntok = int(max(1, min(T, budget / max(per_tok, 1e-9))))
+    sample = rows_all[: ntok * prob.num_q_heads]
+    for _ in range(warm):
+        oracle.rows(prob, sample)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.rows(prob, sample)
+    el = time.perf_counter() - t0
+    value = ntok * steps / el
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
+            "warmup": warm, "ms_per_step": el / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                       "sample_tokens_per_step": ntok},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": int(threads), "kind": "oracle",
+                             "sample": f"first {ntok} of {T} query tokens (all heads) per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line, default=float), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    import torch
+
+    import __graft_entry__
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+
+    prob = ri.workload(args.workload)
+    work = ri.algorithmic_work(prob)
+    q = torch.from_numpy(prob.q.view(np.int16)).view(torch.bfloat16).to(dev)
+    if prob.kv_dtype == "bf16":
+        kv = torch.from_numpy(prob.kv_pages.view(np.int16)).view(torch.bfloat16).to(dev)
+    else:
+        kv = torch.from_numpy(prob.kv_pages).to(dev)
+    kvl = torch.from_numpy(prob.kv_lens).to(dev)
+    pi = torch.from_numpy(prob.page_indices).to(dev)
+    cu = torch.from_numpy(prob.cu_q_lens).to(dev)
+    out = torch.empty_like(q)
+    att = RaggedPagedAttention(**prob.cfg_dict())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        att.forward(q, kv, kvl, pi, cu, prob.num_seqs, out=out, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if att.status() != 0:
+        raise SystemExit(f"library status {att.status()} on warm-up")
+
+    K = max(1, args.steps)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+    clocks = Clocks(uuid)
+    time.sleep(0.3)
+    att.profile_begin(K)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    kern = att.profile_read(K)  # [K, 4] ms
+    if dist is not None:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    tokens = work["q_tokens"]
+    value = tokens * K * world / (ms_total / 1e3)
+
+    # dominant kernel and its roofline
+    hbm, tf_burst, tf_sust, src = peaks()
+    mean_k = kern.mean(axis=0)
+    dom = int(np.argmax(mean_k))
+    dom_name = KERNEL_NAMES[dom]
+    if dom_name == "prefill_attention":
+        bound, achieved, peak, unit = "tensor", work["flops"] / (mean_k[dom] * 1e-3) / 1e12, tf_burst, "TFLOP/s"
+    else:
+        bound, achieved, peak, unit = "hbm", work["bytes"] / (mean_k[dom] * 1e-3) / 1e9, hbm, "GB/s"
+    traffic = recorded_traffic(dom_name, args.workload)
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": traffic, "kernel": dom_name, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+            "kernel_ms": float(mean_k[dom]),
+            "algorithmic": {"bytes": work["bytes"], "flops": work["flops"]}}
+
+    # end to end through the public host-buffer entry point
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = q.cpu().pin_memory()
+        hkvl = kvl.cpu().pin_memory()
+        hpi = pi.cpu().pin_memory()
+        hcu = cu.cpu().pin_memory()
+        hout = torch.empty_like(hq).pin_memory()
+        for _ in range(3):
+            att.forward_host(hq, kv, hkvl, hpi, hcu, prob.num_seqs, hout, stream=stream)
+        torch.cuda.synchronize()
+        Ke = args.e2e_steps
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(Ke):
+            att.forward_host(hq, kv, hkvl, hpi, hcu, prob.num_seqs, hout, stream=stream)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        ms_e = a0.elapsed_time(a1)
+        if dist is not None:
+            t = torch.tensor([ms_e], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_e = float(t.item())
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hkvl, hpi, hcu))
+        e2e = {"value": tokens * Ke * world / (ms_e / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
+               "ms_per_step": ms_e / Ke, "steps": Ke}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(prob)
+
+    if rank == 0:
+        kv_gb = prob.kv_pages.nbytes / 1e9
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob.kv_dtype == "bf16" else "bf16/fp8",
+            "data": "synthetic (seeded)",
+            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
+                       "num_seqs": prob.num_seqs, "q_tokens": tokens,
+                       "kv_tokens": int(prob.kv_lens[: prob.num_seqs].sum()),
+                       "l2": f"no flush: inputs larger than L2 (K/V cache {kv_gb:.2f} GB)"
+                       if kv_gb > 0.129 else "inputs fit in L2 (no flush)",
+                       "ranks": world},
+            "step_hbm_gbs": work["bytes"] / (ms_step * 1e-3) / 1e9,
+            "step_tflops": work["flops"] / (ms_step * 1e-3) / 1e12,
+            "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * K, "clocks": clk,
+        }
+        print(json.dumps(line, default=float), flush=True)
+    att.close()
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,172 @@
+/*
+ * rpa.h -- C ABI of the GB300 ragged paged attention library (librpa.so).
+ *
+ * Ragged paged attention is the mixed prefill/decode grouped-query attention
+ * of a serving engine, as defined by the "ragged_paged.zig" page (Cfg, run,
+ * flashAttention):
+ *
+ *   queries of many sequences are packed raggedly into q[num_q_tokens, Hq, D];
+ *   sequence s owns tokens [cu_q_lens[s], cu_q_lens[s+1]) and kv_lens[s] keys;
+ *   its keys live in fixed-size pages of kv_pages[total_num_pages, page_size,
+ *   2*Hkv, D] (combined head 2h = K of kv head h, 2h+1 = V of kv head h),
+ *   logical page j of s being physical page page_indices[s, j].
+ *
+ *   Query token i of s sits at key position p = kv_len - q_len + i.  Query head
+ *   qh reads kv head qh / (Hq/Hkv).  The logit of key j is
+ *   sm_scale * <q, k_scale*K_j>, soft-capped as cap*tanh(x/cap) when a cap is
+ *   set (before masking); key j is masked when j >= kv_len, when causal and
+ *   j > p, or when p - sliding_window >= j.  The output is the softmax-weighted
+ *   sum of v_scale*V_j, cast to the q dtype.
+ *
+ * Conventions for every entry point:
+ *  - All functions return an RpaStatus code (0 = RPA_OK); no C++ exception
+ *    crosses this boundary and no function aborts the process.
+ *  - "device" pointers are CUDA global memory of the device that was current
+ *    at rpa_create; "host" pointers are ordinary (ideally pinned) host memory.
+ *  - The caller owns every tensor.  The handle owns only its workspace.
+ *  - Work is enqueued on the given stream (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and is asynchronous unless stated.
+ */
+#ifndef RPA_H_
+#define RPA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types. q is bf16; K/V are bf16 or fp8 e4m3fn ("ragged_paged.zig",
+ * Cfg.q_dtype / Cfg.kv_dtype). */
+typedef enum RpaDtype { RPA_DT_BF16 = 0, RPA_DT_FP8_E4M3 = 1 } RpaDtype;
+
+typedef enum RpaStatus {
+    RPA_OK = 0,
+    RPA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad configuration value */
+    RPA_ERR_UNSUPPORTED = 2,    /* dtype, head_dim not in {64,128,256}, Hq % Hkv != 0, group > 64 */
+    RPA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
+    RPA_ERR_BAD_PAGE_INDEX = 4, /* device-detected: a used page id outside [0, total_num_pages) */
+    RPA_ERR_BAD_LENGTHS = 5,    /* device-detected: kv_len > pages_per_seq*page_size, q_len > kv_len,
+                                   cu_q_lens decreasing or past num_q_tokens, negative lengths */
+    RPA_ERR_TIMEOUT = 6         /* device-detected: a bounded wait gave up */
+} RpaStatus;
+
+/* Kernel configuration: the shape fields and numeric knobs of the page's Cfg.
+ * The block knobs (num_kv_pages_per_block, num_queries_per_block) are not
+ * exposed: the library picks its own tiles. */
+typedef struct RpaCfg {
+    int64_t num_q_tokens;    /* rows of q and o */
+    int64_t num_q_heads;     /* Hq */
+    int64_t num_kv_heads;    /* Hkv; Hq % Hkv == 0 and Hq/Hkv <= 64 */
+    int64_t head_dim;        /* D in {64, 128, 256} */
+    int64_t total_num_pages; /* physical pages in kv_pages */
+    int64_t page_size;       /* keys per page, >= 1 */
+    int64_t max_num_seqs;    /* rows of kv_lens / page_indices; cu_q_lens has max_num_seqs+1 */
+    int64_t pages_per_seq;   /* columns of page_indices */
+    int64_t sliding_window;  /* used when has_sliding_window; must be >= 1 */
+    int32_t q_dtype;         /* RpaDtype: RPA_DT_BF16 */
+    int32_t kv_dtype;        /* RpaDtype: RPA_DT_BF16 or RPA_DT_FP8_E4M3 */
+    float sm_scale;          /* logit scale, finite */
+    float mask_value;        /* additive mask of the page (default -2.38197633e38); must be
+                                <= -1e30 so that masked keys get weight exactly 0 */
+    float soft_cap;          /* used when has_soft_cap; > 0 */
+    float k_scale;           /* used when has_k_scale; K dequant factor */
+    float v_scale;           /* used when has_v_scale; V dequant factor */
+    int32_t has_soft_cap;
+    int32_t has_k_scale;
+    int32_t has_v_scale;
+    int32_t is_causal;       /* 1 = causal (default of the page) */
+    int32_t has_sliding_window;
+    int32_t reserved;        /* set to 0 */
+} RpaCfg;
+
+typedef struct RpaHandle RpaHandle;
+
+/* Fill *cfg with the page's defaults for the shape fields given: q/kv bf16,
+ * mask_value -2.38197633e38, causal, no softcap, no scales, no window. */
+void rpa_cfg_init(RpaCfg* cfg);
+
+/* Check a configuration on the host only (no CUDA call).  Returns RPA_OK,
+ * RPA_ERR_INVALID_ARG or RPA_ERR_UNSUPPORTED. */
+int rpa_validate_cfg(const RpaCfg* cfg);
+
+/* Validate cfg, then allocate the workspace (plan buffers and split-KV
+ * partials, sized for the worst case of cfg) on the current device.
+ * On success *out receives the handle; on failure *out is NULL. */
+int rpa_create(const RpaCfg* cfg, RpaHandle** out);
+
+/* One ragged paged attention call (the page's kernel call with inputs
+ * kv_lens, page_indices, cu_q_lens, num_seqs, q, kv_pages and output o).
+ *   q            device, [num_q_tokens, Hq, D] bf16, 16-byte aligned
+ *   kv_pages     device, [total_num_pages, page_size, 2*Hkv, D] kv_dtype, 16-byte aligned
+ *   kv_lens      device, int32 [max_num_seqs]
+ *   page_indices device, int32 [max_num_seqs, pages_per_seq], row-major
+ *   cu_q_lens    device, int32 [max_num_seqs + 1]
+ *   num_seqs     host scalar, 0 <= num_seqs <= max_num_seqs (the page passes it
+ *                as a one-element array)
+ *   o            device, [num_q_tokens, Hq, D] bf16, 16-byte aligned, written in
+ *                full: rows of tokens outside [cu_q_lens[0], cu_q_lens[num_seqs])
+ *                are written as 0
+ *   stream       cudaStream_t as void*
+ * Host-detectable errors return at once without enqueuing work.  Lengths and
+ * page ids are checked on the device and set the status read by
+ * rpa_get_status: bad lengths leave every row of o zero; a bad page id is
+ * never dereferenced (its keys read as zero) and leaves the rows of the
+ * sequences that use it unspecified.  Calls on one handle must be serialised
+ * on the GPU (one stream, or ordered streams): they share the workspace. */
+int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t* kv_lens,
+                const int32_t* page_indices, const int32_t* cu_q_lens, int32_t num_seqs,
+                void* o, void* stream);
+
+/* rpa_forward with the per-step inputs and the output in HOST memory: q,
+ * kv_lens, page_indices and cu_q_lens are copied host->device into staging
+ * buffers owned by the handle (allocated on first use), the call runs, and o
+ * is copied back device->host, all on `stream`.  kv_pages stays a device
+ * pointer (the paged cache is resident state).  The host buffers must stay
+ * valid until the stream reaches the end of the call; pinned memory makes
+ * the copies asynchronous. */
+int rpa_forward_host(RpaHandle* h, const void* q_host, const void* kv_pages,
+                     const int32_t* kv_lens_host, const int32_t* page_indices_host,
+                     const int32_t* cu_q_lens_host, int32_t num_seqs, void* o_host,
+                     void* stream);
+
+/* Synchronise `stream` and return the device-side status of the last call
+ * (RPA_OK, RPA_ERR_BAD_PAGE_INDEX, RPA_ERR_BAD_LENGTHS or RPA_ERR_TIMEOUT),
+ * or RPA_ERR_CUDA if the synchronisation failed. */
+int rpa_get_status(RpaHandle* h, void* stream);
+
+/* Work plan of the last call, for tests and tooling.  Synchronises `stream`.
+ * info (host, 16 int32) receives: [0] status, [1] decode items, [2] prefill
+ * items, [3] split-KV combine entries, [4] decode chunk (keys), [5] decode
+ * tile rows, [6] prefill tile rows, [7] partial slots used, [8] planned
+ * units, [9] 1 if units were sorted by cost, [10] resident decode CTAs.  items (host, may be NULL)
+ * receives up to max_items decode items followed by the prefill items, 8
+ * int32 each: seq, kv head, first query token of the sequence's tile (local),
+ * tokens in the tile, first key, end key, partial slot (-1 = direct write),
+ * piece index. */
+int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items, void* stream);
+
+/* Per-kernel timing for benchmarks.  After rpa_profile_begin(h, n) the next n
+ * calls of rpa_forward on h record CUDA events (on their stream) around each
+ * of their four kernels: planner, decode attention, prefill attention,
+ * combine.  rpa_profile_read synchronises on those events and writes, for
+ * each recorded call c < *n_calls, ms[4*c + k] = duration of kernel k in
+ * milliseconds; ms holds max_calls*4 floats (host).  Profiling stops after
+ * n calls or at the next rpa_profile_begin; the events are owned by h. */
+int rpa_profile_begin(RpaHandle* h, int32_t max_calls);
+int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_calls);
+
+/* Free the workspace and the handle (synchronises the device first). NULL is ignored. */
+void rpa_destroy(RpaHandle* h);
+
+/* Static description of a status code. */
+const char* rpa_strerror(int code);
+
+/* ABI version of this header (major*100 + minor). */
+int rpa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RPA_H_ */

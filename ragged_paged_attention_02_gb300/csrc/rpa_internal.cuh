@@ -1,0 +1,200 @@
+// rpa_internal.cuh -- shared definitions of the CUDA side of librpa.
+//
+// Plan layout, kernel parameters and the small PTX helpers (cp.async,
+// ldmatrix, mma.sync, ex2) used by the attention kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/rpa.h"
+
+namespace rpa {
+
+// ---------------------------------------------------------------- plan layout
+// Control block (int32 words) at the start of the workspace.
+enum Ctrl : int {
+    kStatus = 0,
+    kNumDecItems = 1,
+    kNumPfItems = 2,
+    kNumComb = 3,
+    kDecChunk = 4,
+    kDecCounter = 5,
+    kPfCounter = 6,
+    kNumPart = 7,
+    kNumUnits = 8,
+    kSorted = 9,
+    kCovLo = 10,   // first token covered by a sequence
+    kCovHi = 11,   // end of covered tokens
+    kCtrlWords = 32,
+};
+
+// One work item: 8 int32.
+struct Item {
+    int seq, head, tok0, ntok, kv_begin, kv_end, part, piece;
+};
+
+// One split-KV combine entry: rows [0, rows) of (seq, head) merge `pieces`
+// partials starting at slot `part`.
+struct Comb {
+    int seq, head, part, pieces;
+};
+
+constexpr int kDecRows = 16;       // rows of a decode tile (one m16 MMA tile)
+constexpr int kPfRows = 64;        // rows of a prefill tile (4 warps x 16)
+constexpr int kDecWaves = 4;       // target decode items per resident CTA
+constexpr int kMinChunk = 512;     // smallest split-KV piece (keys)
+constexpr int kChunkAlign = 64;    // pieces are multiples of this many keys
+constexpr int kMaxSort = 16384;    // units sorted by cost on the device
+constexpr int kPlanThreads = 1024;
+
+struct PlanParams {
+    const int* kv_lens;
+    const int* cu_q_lens;
+    int num_seqs;
+    int T;           // num_q_tokens
+    int Hkv;
+    int G;           // q heads per kv head
+    int P, ps;       // pages_per_seq, page_size
+    int causal, has_window, window;
+    int dec_rows;    // rows of a decode tile
+    int pf_rows;     // rows of a prefill tile
+    int dec_slots;   // resident decode CTAs
+    int max_units;   // capacity of the unit arrays
+    int max_dec_units, max_pf_units;  // capacities of the two item lists (in units)
+    int max_part;    // capacity of partial slots
+    int max_comb;    // capacity of combine entries
+    int* ctrl;
+    int* seq_scratch;  // [4 * max_num_seqs]
+    int* units;        // [max_units * 8]
+    unsigned long long* keys;  // [max_units] (only used if > kMaxSort)
+    Item* dec_items;
+    Item* pf_items;
+    Comb* comb;
+};
+
+struct AttnParams {
+    const uint8_t* q;
+    const uint8_t* kv;
+    uint8_t* o;
+    const int* kv_lens;
+    const int* page_indices;
+    const int* cu_q_lens;
+    int T, Hq, Hkv, G, D, ps, P, N;
+    int causal, has_window, window, has_cap;
+    float qk_log2;      // sm_scale * k_scale * log2(e)  (no cap)
+    float cap_exp;      // 2 * sm_scale * k_scale / cap * log2(e)
+    float cap_log2;     // cap * log2(e)
+    float v_scale;
+    int* ctrl;
+    const Item* items;
+    int item_count_word;   // ctrl index of the item count
+    int counter_word;      // ctrl index of the work counter
+    float* part_o;         // [max_part, kDecRows, D]
+    float* part_ml;        // [max_part, kDecRows, 2]
+};
+
+struct CombParams {
+    uint8_t* o;
+    const int* cu_q_lens;
+    int num_seqs, T, Hq, G, D;
+    float v_scale;
+    const int* ctrl;
+    const Comb* comb;
+    const float* part_o;
+    const float* part_ml;
+};
+
+// ---------------------------------------------------------------- host launchers
+struct Launch {
+    int grid;
+    cudaStream_t stream;
+};
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
+cudaError_t launch_decode(const AttnParams& p, int fp8, const Launch& l);
+cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l);
+cudaError_t launch_combine(const CombParams& p, const Launch& l);
+// occupancy / attributes (call once per device)
+cudaError_t attn_prepare(int D, int fp8, int* dec_blocks_per_sm, int* pf_blocks_per_sm);
+size_t plan_smem_bytes();
+cudaError_t plan_prepare();
+
+// ---------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    // zero-fill when !valid (src-size 0): nothing is read from src
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// D = A*B + D, m16n8k16, fp32 accumulate; F16 selects f16 operands, else bf16.
+template <bool F16>
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    if constexpr (F16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+            "{%8,%9}, {%0,%1,%2,%3};\n"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// 2^x on the special-function unit (hardware instruction).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Pack two floats into a bf16x2 / f16x2 register (round to nearest even).
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    uint32_t r;
+    if constexpr (F16)
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two e4m3fn bytes -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ void set_status(int* ctrl, int code) {
+    atomicCAS(ctrl + kStatus, 0, code);
+}
+#endif
+
+}  // namespace rpa

@@ -196,7 +196,7 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
 
 
 # ---------------------------------------------------------------- the five workloads
-WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill")
+WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill", "decode_quarter")
 
 
 def workload(name: str) -> Problem:
@@ -211,6 +211,14 @@ def workload(name: str) -> Problem:
         rng = np.random.default_rng([1, 0])
         kl = rng.integers(512, 8192, size=256, endpoint=True)
         return build(seed=1, q_lens=np.ones(256, np.int64), kv_lens=kl, num_q_heads=32,
+                     num_kv_heads=8, head_dim=128, page_size=16, pages_per_seq=512,
+                     sm_scale=1.0 / math.sqrt(128), name=name, rng_lengths=rng)
+    if name == "decode_quarter":
+        # the decode workload's first 64 sequences (same lengths and seeds): a
+        # smaller case for profiler captures (K/V ~1.1 GB, still far above L2)
+        rng = np.random.default_rng([1, 0])
+        kl = rng.integers(512, 8192, size=256, endpoint=True)[:64]
+        return build(seed=1, q_lens=np.ones(64, np.int64), kv_lens=kl, num_q_heads=32,
                      num_kv_heads=8, head_dim=128, page_size=16, pages_per_seq=512,
                      sm_scale=1.0 / math.sqrt(128), name=name, rng_lengths=rng)
     if name == "mixed":

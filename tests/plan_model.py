@@ -1,0 +1,86 @@
+"""Python re-derivation of the device planner's work list (host logic, no GPU).
+
+Written from the planner's stated rules, not from its code: decode-class
+sequences (q_len * G <= decode rows) are cut into key pieces of `chunk` keys,
+prefill-class sequences into query tiles of pf_rows // G tokens; each unit's
+key range is the band its rows can see; units are ordered decode first, then
+by cost (keys) descending, ties by unit index; each unit yields one item per
+kv head.
+"""
+import numpy as np
+
+
+def band(kl, ql, i0, i1, causal, window):
+    p_lo = kl - ql + i0
+    p_hi = kl - ql + i1 - 1
+    hi = min(kl, p_hi + 1) if causal else kl
+    lo = max(0, p_lo - window + 1) if window else 0
+    return lo, max(hi, lo)
+
+
+def plan(prob, dec_slots, dec_rows=16, pf_rows=64, waves=4, min_chunk=512, align=64,
+         max_sort=16384):
+    Hkv = prob.num_kv_heads
+    G = prob.num_q_heads // Hkv
+    Tq = max(1, pf_rows // G)
+    S = prob.num_seqs
+    cu = prob.cu_q_lens.astype(np.int64)
+    kvl = prob.kv_lens.astype(np.int64)
+    win = prob.sliding_window or 0
+    causal = prob.is_causal
+    cls, cnt = [], []
+    total = 0
+    for s in range(S):
+        q0, q1, kl = cu[s], cu[s + 1], kvl[s]
+        ql = q1 - q0
+        if q0 < 0 or ql < 0 or kl < 0 or kl > prob.pages_per_seq * prob.page_size or ql > kl \
+                or q1 > prob.num_q_tokens:
+            return dict(status=5, dec=np.zeros((0, 8), np.int32), pf=np.zeros((0, 8), np.int32))
+        if ql == 0:
+            cls.append(0); cnt.append(0)
+        elif ql * G <= dec_rows:
+            lo, hi = band(kl, ql, 0, ql, causal, win)
+            cls.append(1); cnt.append(hi - lo)
+            total += (hi - lo) * Hkv
+        else:
+            cls.append(2); cnt.append(-(-ql // Tq))
+    target = waves * max(1, dec_slots)
+    chunk = max(-(-total // target), min_chunk)
+    chunk = -(-chunk // align) * align
+    chunk = min(chunk, 1 << 30)
+    units = []  # (cls_bit, cost, desc[8])
+    part = 0
+    for s in range(S):
+        if cls[s] != 1:
+            continue
+        ql = int(cu[s + 1] - cu[s])
+        lo, hi = band(int(kvl[s]), ql, 0, ql, causal, win)
+        pieces = -(-cnt[s] // chunk)
+        base = part if pieces > 1 else -1
+        if pieces > 1:
+            part += pieces * Hkv
+        for k in range(pieces):
+            kb = lo + k * chunk
+            ke = min(hi, kb + chunk)
+            units.append((0, ke - kb, [s, 0, ql, kb, ke, base, k, pieces]))
+    for s in range(S):
+        if cls[s] != 2:
+            continue
+        ql = int(cu[s + 1] - cu[s])
+        for k in range(cnt[s]):
+            t0 = k * Tq
+            nt = min(Tq, ql - t0)
+            lo, hi = band(int(kvl[s]), ql, t0, t0 + nt, causal, win)
+            units.append((1, hi - lo, [s, t0, nt, lo, hi, -1, 0, 1]))
+    n = len(units)
+    order = list(range(n))
+    if n <= max_sort:
+        order.sort(key=lambda u: (units[u][0], 0x7FFFFFFF - units[u][1], u))
+    dec, pf = [], []
+    for u in order:
+        c, _, d = units[u]
+        for h in range(Hkv):
+            item = [d[0], h, d[1], d[2], d[3], d[4], d[5] + h * d[7] + d[6] if d[5] >= 0 else -1, d[6]]
+            (dec if c == 0 else pf).append(item)
+    return dict(status=0, chunk=chunk, sorted=int(n <= max_sort), n_units=n, n_part=part,
+                dec=np.array(dec, np.int32).reshape(-1, 8), pf=np.array(pf, np.int32).reshape(-1, 8))

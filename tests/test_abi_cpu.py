@@ -1,0 +1,78 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+declared in include/rpa.h, and rejects bad configurations on the host."""
+import os
+import re
+
+import pytest
+
+import ragged_paged_attention_02_gb300 as rpa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return rpa.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "rpa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rpa_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert header_functions() == sorted(rpa.EXPORTS)
+
+
+def test_library_exports_every_header_symbol(L):
+    for name in header_functions():
+        assert hasattr(L, name), name
+    assert L.rpa_version() == 100
+
+
+def test_strerror_covers_codes(L):
+    for code in range(7):
+        assert L.rpa_strerror(code).decode() != "unknown status code"
+
+
+BASE = dict(num_q_tokens=22, num_q_heads=4, num_kv_heads=2, head_dim=64, total_num_pages=16,
+            page_size=16, max_num_seqs=3, pages_per_seq=4, sm_scale=0.125)
+
+
+@pytest.mark.parametrize("change,code", [
+    ({}, rpa.RPA_OK),
+    (dict(num_q_heads=6, num_kv_heads=4), rpa.RPA_ERR_UNSUPPORTED),
+    (dict(head_dim=96), rpa.RPA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=130, num_kv_heads=1), rpa.RPA_ERR_UNSUPPORTED),
+    (dict(mask_value=-1.0), rpa.RPA_ERR_UNSUPPORTED),
+    (dict(page_size=0), rpa.RPA_ERR_INVALID_ARG),
+    (dict(total_num_pages=0), rpa.RPA_ERR_INVALID_ARG),
+    (dict(num_q_tokens=-1), rpa.RPA_ERR_INVALID_ARG),
+    (dict(sliding_window=0), rpa.RPA_ERR_INVALID_ARG),
+    (dict(soft_cap=-3.0), rpa.RPA_ERR_INVALID_ARG),
+    (dict(sm_scale=float("nan")), rpa.RPA_ERR_INVALID_ARG),
+    (dict(kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05), rpa.RPA_OK),
+    (dict(pages_per_seq=1 << 20, page_size=1 << 12), rpa.RPA_ERR_INVALID_ARG),
+])
+def test_validate_cfg(L, change, code):
+    cfg = dict(BASE)
+    cfg.update(change)
+    assert rpa.validate_cfg(**cfg) == code
+
+
+def test_null_handle_and_create_out(L):
+    import ctypes
+
+    assert L.rpa_forward(None, None, None, None, None, None, 0, None, None) == rpa.RPA_ERR_INVALID_ARG
+    assert L.rpa_get_status(None, None) == rpa.RPA_ERR_INVALID_ARG
+    c = rpa.make_cfg(**BASE)
+    assert L.rpa_create(ctypes.byref(c), None) == rpa.RPA_ERR_INVALID_ARG
+    bad = rpa.make_cfg(**dict(BASE, head_dim=80))
+    h = ctypes.c_void_p(1)
+    assert L.rpa_create(ctypes.byref(bad), ctypes.byref(h)) == rpa.RPA_ERR_UNSUPPORTED
+    assert not h.value
+    L.rpa_destroy(None)

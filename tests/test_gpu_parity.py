@@ -1,0 +1,227 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerance: |gpu - oracle| <= 2e-2 + 2e-2*|oracle| for bf16 K/V and
+6e-2 + 6e-2*|oracle| for fp8 K/V, element by element.  Small cases compare
+every row; the full-size workloads compare every row the oracle can afford
+(decode) or a seeded sample of rows (the rest), plus whole-output properties.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import rpa_inputs as ri
+from gpu_util import assert_close, o_to_f64, run, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def test_tiny_workload_all_rows():
+    p = ri.workload("tiny")
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, "tiny")
+
+
+SMALL = [
+    # (seed, kwargs) -- several tiles, ragged tails, every knob and head_dim
+    (30, dict(num_seqs=5, max_q=40, max_kv=300, num_q_heads=8, num_kv_heads=2, head_dim=128)),
+    (31, dict(num_seqs=4, max_q=90, max_kv=400, num_q_heads=4, num_kv_heads=4, head_dim=64,
+              page_size=8)),
+    (32, dict(num_seqs=3, max_q=70, max_kv=500, num_q_heads=16, num_kv_heads=8, head_dim=256,
+              page_size=16, soft_cap=50.0, sliding_window=100, sm_scale=1 / 16)),
+    (33, dict(num_seqs=6, max_q=20, max_kv=700, num_q_heads=16, num_kv_heads=8, head_dim=256,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0, sliding_window=300,
+              sm_scale=1 / 16)),
+    (34, dict(num_seqs=5, max_q=50, max_kv=300, num_q_heads=8, num_kv_heads=1, head_dim=128,
+              is_causal=False)),
+    (35, dict(num_seqs=5, max_q=50, max_kv=300, num_q_heads=8, num_kv_heads=2, head_dim=64,
+              is_causal=False, sliding_window=40, soft_cap=5.0)),
+    (36, dict(num_seqs=16, decode_only=True, max_kv=3000, num_q_heads=32, num_kv_heads=8,
+              head_dim=128)),
+    (37, dict(num_seqs=9, decode_only=True, max_kv=2500, num_q_heads=16, num_kv_heads=8,
+              head_dim=128, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07)),
+    (38, dict(num_seqs=4, max_q=30, max_kv=200, num_q_heads=64, num_kv_heads=1, head_dim=64,
+              page_size=64)),
+    (39, dict(num_seqs=7, max_q=12, max_kv=2000, num_q_heads=12, num_kv_heads=3, head_dim=128,
+              page_size=32, kv_dtype="fp8_e4m3", k_scale=0.5, sliding_window=1)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_cases_all_rows(case):
+    seed, kw = SMALL[case]
+    p = ri.random_small(seed, **kw)
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, f"small case {case}")
+
+
+def _sample_rows(p, n, seed):
+    rng = np.random.default_rng(seed)
+    T = int(p.cu_q_lens[p.num_seqs])
+    t = rng.integers(0, T, size=n)
+    # always include the first and last token of every sequence (tails, decode rows)
+    ends = np.concatenate([p.cu_q_lens[:p.num_seqs], p.cu_q_lens[1:p.num_seqs + 1] - 1])
+    t = np.unique(np.concatenate([t, ends[ends >= 0]]))
+    h = rng.integers(0, p.num_q_heads, size=t.size)
+    return np.stack([t, h], axis=1).astype(np.int64)
+
+
+@pytest.mark.parametrize("name,nrows", [("decode", None), ("mixed", 3000), ("fp8_window", 3000),
+                                        ("long_prefill", 1500)])
+def test_full_workloads(name, nrows):
+    p = ri.workload(name)
+    got, st = run(p)
+    assert st == 0
+    assert np.isfinite(got).all()
+    if nrows is None:
+        ref = oracle.forward(p)
+        assert_close(got, ref, p.kv_dtype, name)
+    else:
+        rows = _sample_rows(p, nrows, 1234)
+        ref = oracle.rows(p, rows)
+        assert_close(got[rows[:, 0], rows[:, 1]], ref, p.kv_dtype, name)
+
+
+def test_planner_matches_python_rederivation():
+    from plan_model import plan
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    for name in ("tiny", "mixed"):
+        p = ri.workload(name) if name == "tiny" else ri.random_small(
+            40, num_seqs=60, max_q=300, max_kv=5000, num_q_heads=32, num_kv_heads=8, head_dim=128,
+            sliding_window=777)
+        att = RaggedPagedAttention(**p.cfg_dict())
+        att.forward(*to_dev(p), p.num_seqs)
+        info, items = att.plan()
+        ref = plan(p, int(info[10]))
+        assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
+        assert info[9] == ref["sorted"] and info[7] == ref["n_part"]
+        assert np.array_equal(items[: info[1]], ref["dec"])
+        assert np.array_equal(items[info[1]:], ref["pf"])
+        att.close()
+
+
+def test_page_placement_invariance_bit_identical():
+    p = ri.random_small(41, num_seqs=6, max_q=40, max_kv=900, num_q_heads=8, num_kv_heads=2,
+                        head_dim=128)
+    a, _ = run(p)
+    perm = np.random.default_rng(1).permutation(p.total_num_pages)
+    kv2 = np.empty_like(p.kv_pages)
+    kv2[perm] = p.kv_pages
+    p.kv_pages = kv2
+    p.page_indices = perm[p.page_indices].astype(np.int32)
+    b, _ = run(p)
+    assert np.array_equal(a, b)
+
+
+def test_poisoned_tails_and_unused_pages():
+    p = ri.random_small(42, num_seqs=5, max_q=30, max_kv=500, num_q_heads=8, num_kv_heads=2,
+                        head_dim=128, extra_tokens=0)
+    ref = oracle.forward(p)
+    used = set()
+    ps = p.page_size
+    for s in range(p.num_seqs):
+        kl = int(p.kv_lens[s])
+        used.update(int(x) for x in p.page_indices[s, : (kl + ps - 1) // ps])
+        if kl % ps:
+            p.kv_pages[p.page_indices[s, kl // ps], kl % ps:] = 0x7FC0  # NaN
+    for pg in range(p.total_num_pages):
+        if pg not in used:
+            p.kv_pages[pg] = 0x7F80  # +inf
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, ref, p.kv_dtype, "poisoned")
+
+
+def test_uncovered_tokens_and_padding_rows():
+    p = ri.build(seed=43, q_lens=[3, 0, 17, 1], kv_lens=[40, 9, 200, 1], num_q_heads=8,
+                 num_kv_heads=2, head_dim=64, page_size=16, extra_tokens=5, max_num_seqs=7)
+    import torch
+
+    t = to_dev(p)
+    out = torch.full_like(t[0], 3.0)
+    got, st = run(p, tensors=t, out=out)
+    assert st == 0
+    assert (got[21:] == 0).all()
+    assert_close(got, oracle.forward(p), p.kv_dtype, "padding")
+
+
+def test_zero_sequences_writes_zeros():
+    p = ri.build(seed=44, q_lens=[4], kv_lens=[10], num_q_heads=4, num_kv_heads=2, head_dim=64,
+                 page_size=16)
+    p.num_seqs = 0
+    import torch
+
+    t = to_dev(p)
+    out = torch.full_like(t[0], 7.0)
+    got, st = run(p, tensors=t, out=out)
+    assert st == 0 and (got == 0).all()
+
+
+def test_bad_page_index_sets_status():
+    p = ri.random_small(45, num_seqs=3, max_q=5, max_kv=60)
+    p.page_indices[1, 0] = p.total_num_pages + 5
+    got, st = run(p)
+    assert st == 4
+    assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("mut", ["kv_too_long", "q_gt_kv", "cu_decreasing", "cu_past_T"])
+def test_bad_lengths_set_status_and_zero_output(mut):
+    p = ri.random_small(46, num_seqs=3, max_q=5, max_kv=60)
+    if mut == "kv_too_long":
+        p.kv_lens[0] = p.pages_per_seq * p.page_size + 1
+    elif mut == "q_gt_kv":
+        p.kv_lens[2] = int(p.cu_q_lens[3] - p.cu_q_lens[2]) - 1
+    elif mut == "cu_decreasing":
+        p.cu_q_lens[2] = p.cu_q_lens[1] - 1
+    else:
+        p.cu_q_lens[3] = p.num_q_tokens + 1
+    assert oracle.validate(p) == 5
+    import torch
+
+    t = to_dev(p)
+    out = torch.full_like(t[0], 5.0)
+    got, st = run(p, tensors=t, out=out)
+    assert st == 5 and (got == 0).all()
+
+
+def test_forward_host_equals_forward():
+    p = ri.random_small(47, num_seqs=6, max_q=20, max_kv=700, num_q_heads=8, num_kv_heads=2,
+                        head_dim=128)
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    att = RaggedPagedAttention(**p.cfg_dict())
+    t = to_dev(p)
+    dev_out = o_to_f64(att.forward(*t, p.num_seqs))
+    host = [x.cpu().pin_memory() for x in t]
+    out_h = torch.empty_like(host[0]).pin_memory()
+    att.forward_host(host[0], t[1], host[2], host[3], host[4], p.num_seqs, out_h)
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    assert np.array_equal(dev_out, o_to_f64(out_h))
+    att.close()
+
+
+def test_repeat_calls_are_deterministic():
+    p = ri.random_small(48, num_seqs=10, decode_only=True, max_kv=4000, num_q_heads=32,
+                        num_kv_heads=8, head_dim=128)
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    att = RaggedPagedAttention(**p.cfg_dict())
+    t = to_dev(p)
+    a = o_to_f64(att.forward(*t, p.num_seqs))
+    b = o_to_f64(att.forward(*t, p.num_seqs))
+    assert np.array_equal(a, b)
+    att.close()

@@ -48,7 +48,9 @@ typedef enum RpaStatus {
     RPA_ERR_BAD_PAGE_INDEX = 4, /* device-detected: a used page id outside [0, total_num_pages) */
     RPA_ERR_BAD_LENGTHS = 5,    /* device-detected: kv_len > pages_per_seq*page_size, q_len > kv_len,
                                    cu_q_lens decreasing or past num_q_tokens, negative lengths */
-    RPA_ERR_TIMEOUT = 6         /* device-detected: a bounded wait gave up */
+    RPA_ERR_TIMEOUT = 6,        /* device-detected: a bounded wait gave up */
+    RPA_ERR_NO_ALLOC_LIMIT = 7  /* rpa_forward_noalloc: the configuration's workspace exceeds
+                                   the library's fixed 32 MiB scratch array */
 } RpaStatus;
 
 /* Kernel configuration: the shape fields and numeric knobs of the page's Cfg.
@@ -155,6 +157,34 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
  * n calls or at the next rpa_profile_begin; the events are owned by h. */
 int rpa_profile_begin(RpaHandle* h, int32_t max_calls);
 int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_calls);
+
+/* rpa_forward for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that may not call cudaMalloc/cudaFree where they run attention: serving
+ * engines that hand all device memory to their own arena allocator, code
+ * paths where an allocation's implicit device synchronisation is not
+ * allowed, and plain-C hosts that have no allocator to give the library.
+ *
+ * It takes no handle: the configuration and tensors are those of rpa_create
+ * plus rpa_forward, and the planner, attention and combine kernels are the
+ * same.  Their workspace (plan, work items, split-KV partials) is carved from
+ * one 32 MiB array in the library's own device memory, which every GPU that
+ * loads the library holds until the process exits.  A configuration whose
+ * worst-case workspace exceeds 32 MiB returns RPA_ERR_NO_ALLOC_LIMIT before
+ * anything is enqueued.  Nothing here calls cudaMalloc, cudaFree or any other
+ * allocating routine.
+ *
+ * The first call on each device (with that device current) looks up the
+ * array's device address and sets kernel attributes; make that first call
+ * before any stream capture.  Every call shares the one array and it keeps
+ * the previous call's contents (the call clears what must start at zero), so
+ * calls that overlap on the GPU -- on different streams, or from different
+ * threads -- race and must be serialised by the caller.  The device-side
+ * status (bad lengths or page ids) is not reported by this entry point. */
+int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void* kv_pages,
+                        const int32_t* kv_lens, const int32_t* page_indices,
+                        const int32_t* cu_q_lens, int32_t num_seqs, void* o, void* stream);
 
 /* Free the workspace and the handle (synchronises the device first). NULL is ignored. */
 void rpa_destroy(RpaHandle* h);

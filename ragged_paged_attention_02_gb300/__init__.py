@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     RPA_ERR_BAD_PAGE_INDEX,
     RPA_ERR_CUDA,
     RPA_ERR_INVALID_ARG,
+    RPA_ERR_NO_ALLOC_LIMIT,
     RPA_ERR_TIMEOUT,
     RPA_ERR_UNSUPPORTED,
     RPA_OK,

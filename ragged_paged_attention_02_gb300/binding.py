@@ -23,13 +23,14 @@ RPA_ERR_CUDA = 3
 RPA_ERR_BAD_PAGE_INDEX = 4
 RPA_ERR_BAD_LENGTHS = 5
 RPA_ERR_TIMEOUT = 6
+RPA_ERR_NO_ALLOC_LIMIT = 7
 RPA_DT_BF16 = 0
 RPA_DT_FP8_E4M3 = 1
 
 # every entry point declared in include/rpa.h
 EXPORTS = ("rpa_cfg_init", "rpa_validate_cfg", "rpa_create", "rpa_forward", "rpa_forward_host",
            "rpa_get_status", "rpa_read_plan", "rpa_profile_begin", "rpa_profile_read",
-           "rpa_destroy", "rpa_strerror", "rpa_version")
+           "rpa_forward_noalloc", "rpa_destroy", "rpa_strerror", "rpa_version")
 
 
 class RpaCfg(ctypes.Structure):
@@ -89,6 +90,8 @@ def lib():
         L.rpa_profile_begin.restype = ctypes.c_int
         L.rpa_profile_read.argtypes = [vp, vp, i32, vp]
         L.rpa_profile_read.restype = ctypes.c_int
+        L.rpa_forward_noalloc.argtypes = [ctypes.POINTER(RpaCfg), vp, vp, vp, vp, vp, i32, vp, vp]
+        L.rpa_forward_noalloc.restype = ctypes.c_int
         L.rpa_destroy.argtypes = [vp]
         L.rpa_destroy.restype = None
         L.rpa_strerror.argtypes = [ctypes.c_int]

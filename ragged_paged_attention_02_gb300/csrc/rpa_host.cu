@@ -100,6 +100,7 @@ const char* rpa_strerror(int code) {
         case RPA_ERR_BAD_PAGE_INDEX: return "page index outside [0, total_num_pages)";
         case RPA_ERR_BAD_LENGTHS: return "bad lengths (kv_len > capacity, q_len > kv_len, or cu_q_lens not monotone / past num_q_tokens)";
         case RPA_ERR_TIMEOUT: return "a bounded device wait timed out";
+        case RPA_ERR_NO_ALLOC_LIMIT: return "workspace exceeds the fixed 32 MiB scratch array of rpa_forward_noalloc";
         default: return "unknown status code";
     }
 }

@@ -35,7 +35,7 @@ def test_library_exports_every_header_symbol(L):
 
 
 def test_strerror_covers_codes(L):
-    for code in range(7):
+    for code in range(8):
         assert L.rpa_strerror(code).decode() != "unknown status code"
 
 

@@ -1,0 +1,81 @@
+"""rpa_forward_noalloc: the forward call for callers that cannot allocate.
+
+Serving engines that give all device memory to their own arena allocator, or
+that may not call cudaMalloc/cudaFree (an implicit device synchronisation)
+where attention runs, call this entry point instead of rpa_create +
+rpa_forward.  Its workspace is a fixed 32 MiB array inside the library.  This
+test calls it through the C ABI and checks that two calls in a row give the
+same output as the handle-based rpa_forward, at the tolerance of the other
+parity tests, and that an oversized configuration is refused.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import rpa_inputs as ri
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+
+
+def _noalloc(prob, t, out):
+    import ragged_paged_attention_02_gb300 as rpa
+
+    c = rpa.make_cfg(**prob.cfg_dict())
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    q, kv, kvl, pi, cu = t
+    return rpa.lib().rpa_forward_noalloc(ctypes.byref(c), q.data_ptr(), kv.data_ptr(), kvl.data_ptr(),
+                                         pi.data_ptr(), cu.data_ptr(), int(prob.num_seqs),
+                                         out.data_ptr(), stream)
+
+
+@pytest.mark.parametrize("name", ["tiny", "split_decode", "mixed_small"])
+def test_noalloc_matches_rpa_forward_twice(name):
+    from gpu_util import assert_close, o_to_f64, to_dev
+
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    if name == "tiny":
+        p = ri.workload("tiny")
+    elif name == "split_decode":
+        p = ri.random_small(60, num_seqs=12, decode_only=True, max_kv=6000, num_q_heads=32,
+                            num_kv_heads=8, head_dim=128)
+    else:
+        p = ri.random_small(61, num_seqs=8, max_q=80, max_kv=900, num_q_heads=16, num_kv_heads=8,
+                            head_dim=256, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05,
+                            soft_cap=50.0, sliding_window=300, sm_scale=1 / 16)
+    t = to_dev(p)
+    att = RaggedPagedAttention(**p.cfg_dict())
+    ref = o_to_f64(att.forward(*t, p.num_seqs))
+    assert att.status() == 0
+    att.close()
+    for _ in range(2):
+        out = torch.full_like(t[0], 9.0)
+        assert _noalloc(p, t, out) == 0
+        torch.cuda.synchronize()
+        got = o_to_f64(out)
+        assert_close(got, ref, p.kv_dtype, f"noalloc {name}")
+
+
+def test_noalloc_rejects_oversized_workspace():
+    import ragged_paged_attention_02_gb300 as rpa
+
+    p = ri.workload("tiny")
+    cfg = p.cfg_dict()
+    cfg["max_num_seqs"] = 1 << 21  # work-item lists alone need far more than 32 MiB
+    c = rpa.make_cfg(**cfg)
+    dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
+    r = rpa.lib().rpa_forward_noalloc(ctypes.byref(c), dummy.data_ptr(), dummy.data_ptr(),
+                                      dummy.data_ptr(), dummy.data_ptr(), dummy.data_ptr(), 1,
+                                      dummy.data_ptr(), None)
+    assert r == rpa.RPA_ERR_NO_ALLOC_LIMIT

@@ -1,4 +1,4 @@
-// rpa_attn_mma.cu -- K1 (warp-MMA variant): paged-KV flash attention.
+// rpa_attn_mma.cu -- K1 prefill (warp-MMA): paged-KV flash attention for query tiles.
 //
 // One persistent CTA pulls work items (sequence, kv head, query tile, key
 // range) from the planner's list and runs the blockwise online softmax of the
@@ -26,10 +26,9 @@
 // taken to f16, and the MMAs run in f16; k_scale is folded into the logit
 // scale and v_scale into the epilogue.
 //
-// Two shapes share the code:  decode  (WM=1, WN=4): 16 rows, the 4 warps split
-//                             the keys of each stage, merged at the end;
-//                             prefill (WM=4, WN=1): 64 rows, all warps share
-//                             each stage of keys.
+// The body is written for WM row-warps x WN key-warps; the prefill kernel
+// uses WM=4, WN=1: 64 rows, all warps share each stage of keys.  (WN > 1
+// splits the keys of a stage across warps and merges them at the end.)
 #include "rpa_internal.cuh"
 
 namespace rpa {
@@ -383,11 +382,6 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
 }
 
 // ---------------------------------------------------------------- instantiations
-// decode: 16 rows, 4 warps split the keys of a stage
-template <int D, bool FP8>
-struct DecShape {
-    static constexpr int WM = 1, WN = 4, BK = 16, STAGES = 3;
-};
 // prefill: 64 rows (4 warps), all warps share each stage
 template <int D, bool FP8>
 struct PfShape {
@@ -395,21 +389,12 @@ struct PfShape {
 };
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(128) rpa_decode_attn(const AttnParams p) {
-    using S = DecShape<D, FP8>;
-    attn_body<D, FP8, S::WM, S::WN, S::BK, S::STAGES>(p);
-}
-template <int D, bool FP8>
 __global__ void __launch_bounds__(128) rpa_prefill_attn(const AttnParams p) {
     using S = PfShape<D, FP8>;
     attn_body<D, FP8, S::WM, S::WN, S::BK, S::STAGES>(p);
 }
 template <template <int, bool> class Shape, int D, bool FP8>
 struct KernelOf;
-template <int D, bool FP8>
-struct KernelOf<DecShape, D, FP8> {
-    static constexpr auto fn = rpa_decode_attn<D, FP8>;
-};
 template <int D, bool FP8>
 struct KernelOf<PfShape, D, FP8> {
     static constexpr auto fn = rpa_prefill_attn<D, FP8>;
@@ -462,16 +447,9 @@ cudaError_t dispatch_prepare(int D, int fp8, int* bps) {
 
 }  // namespace
 
-cudaError_t launch_decode(const AttnParams& p, int fp8, const Launch& l) {
-    return dispatch_launch<DecShape>(p.D, fp8, p, l);
-}
 cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l) {
     return dispatch_launch<PfShape>(p.D, fp8, p, l);
 }
-cudaError_t attn_prepare(int D, int fp8, int* dec_bps, int* pf_bps) {
-    cudaError_t e = dispatch_prepare<DecShape>(D, fp8, dec_bps);
-    if (e != cudaSuccess) return e;
-    return dispatch_prepare<PfShape>(D, fp8, pf_bps);
-}
+cudaError_t attn_prepare(int D, int fp8, int* pf_bps) { return dispatch_prepare<PfShape>(D, fp8, pf_bps); }
 
 }  // namespace rpa

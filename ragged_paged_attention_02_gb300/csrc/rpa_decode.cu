@@ -1,0 +1,556 @@
+// rpa_decode.cu -- K1 decode: paged-KV attention for tiles of <= 16 query rows.
+//
+// Decode-class work items (q_len * G <= 16 rows of one kv head, a key range of
+// one sequence) are HBM-bound: every key's K and V rows are read once and
+// used by at most 16 rows.  The kernel is warp-specialised and persistent:
+//
+//   producer warp   pulls items from the planner's list, walks each item's
+//                   keys in stages of 64, and gathers them through the page
+//                   table ("ragged_paged.zig": createKvAsyncCopyDescriptors,
+//                   logical page -> page_indices[s, page]) with bulk tensor
+//                   copies: one copy per (page run, K/V, 128-byte column
+//                   block), K rows of kv head h being combined head 2h and V
+//                   rows 2h+1 of each slot.  The Q tile of an item (G
+//                   consecutive heads of up to 16/G tokens) comes with the
+//                   item's first stage.  A 3-stage mbarrier ring keeps copies
+//                   in flight across item boundaries (the page's next-block
+//                   prefetch, carried across sequences the same way).
+//   4 consumer      each take 16 keys of every stage: S = Q K^T on mma.sync
+//   warps           (fp32), scale / softcap / masks in the log2 domain, online
+//                   softmax, O += P V; at the item's last stage the four
+//                   partial (m, l, O) are merged through shared memory and
+//                   written as bf16 o, or as an fp32 split-KV partial for the
+//                   combine kernel.
+//
+// fp8 e4m3 K/V: stages hold the raw bytes; each consumer warp converts its 16
+// keys to f16 (exact) in its own buffer and runs the MMAs in f16, with
+// k_scale folded into the logit scale and v_scale into the epilogue.
+//
+// Every wait is a bounded mbarrier wait (a global-timer deadline): on expiry
+// the status word gets RPA_ERR_TIMEOUT and the warp returns.
+#include <cuda.h>
+
+#include "rpa_internal.cuh"
+
+namespace rpa {
+
+namespace {
+
+constexpr int kCW = 4;                  // consumer warps
+constexpr int kDecThreads = 32 * (kCW + 1);
+constexpr int kKS = 64;                 // keys per stage (16 per consumer warp)
+constexpr int kNS = 3;                  // stages in the ring
+constexpr int kMetaWords = 16;
+
+// stage meta words
+enum Meta : int {
+    mItem = 0, mSeq, mHead, mQStart, mQl, mKl, mKvBegin, mKvEnd, mPart, mTok0, mNtok, mSt, mNst,
+    mKey0, mStop
+};
+
+template <int D, bool FP8>
+struct DecGeom {
+    static constexpr int E = FP8 ? 1 : 2;          // bytes per K/V element
+    static constexpr int DHQ = D * 2 / 128;        // 128-byte column blocks of a bf16 row
+    static constexpr int DH = FP8 ? 1 : DHQ;       // column blocks per K/V box
+    static constexpr int QB = DHQ * 16 * 128;      // Q area: [DHQ][16 lines][128 B]
+    static constexpr int KVB = kKS * 2 * D * E;    // K/V area of one stage
+    static constexpr int SB = QB + KVB;            // one stage
+    static constexpr int CONV = FP8 ? 16 * D * 4 : 0;  // per-warp f16 buffer (K and V, 16 keys)
+    static constexpr int SMEM = kNS * SB + kCW * CONV + 1024;  // + alignment slack
+    static_assert(QB % 1024 == 0 && KVB % 1024 == 0, "stage alignment");
+    static_assert(kCW * 16 * D * 4 <= (FP8 ? kCW * CONV : KVB), "merge area");
+};
+
+__device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
+    return line * 128u + (((chunk ^ line) & 7u) << 4);
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_constant__ CUtensorMap kvmap,
+                                                               const __grid_constant__ CUtensorMap qmap,
+                                                               const DecParams p) {
+    using Gm = DecGeom<D, FP8>;
+    constexpr bool F16 = FP8;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kNS];
+    __shared__ __align__(8) uint64_t empty_bar[kNS];
+    __shared__ __align__(8) uint64_t merge_bar;
+    __shared__ int meta[kNS][kMetaWords];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const AttnParams& a = p.a;
+    int* ctrl = a.ctrl;
+    const uint64_t tmo = p.timeout_ns;
+    const int n_items = a.ctrl[a.item_count_word];
+    // 1 KiB-aligned base: the 128-byte swizzle pattern follows address bits 7..9
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t smem0 = smem_u32(smem);
+
+    if (tid == 0) {
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&empty_bar[i]), kCW);
+        }
+        mbar_init(smem_u32(&merge_bar), kCW);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kCW) {
+        // =============================== producer ===============================
+        if (p.debug_stall) return;  // test hook: consumers must time out
+        const int BR = p.BR, ps = a.ps;
+        const int boxes = kKS / BR;                       // page runs per stage
+        const int tasks = boxes * (FP8 ? 2 : 2 * Gm::DH);  // copies per stage
+        const uint32_t box_bytes = (uint32_t)BR * (FP8 ? D : 128);  // one copy
+        const int PBB_P = FP8 ? 2 * BR * D : 2 * Gm::DH * BR * 128;   // one page run
+        int s = 0;
+        uint32_t ph = 0;
+        int it = 0;
+        if (lane == 0) it = atomicAdd(ctrl + a.counter_word, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        bool ok = true;
+        while (ok && it < n_items) {
+            const Item item = a.items[it];
+            int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(ctrl + a.counter_word, 1);
+            const int q_start = a.cu_q_lens[item.seq];
+            const int ql = a.cu_q_lens[item.seq + 1] - q_start;
+            const int kl = a.kv_lens[item.seq];
+            const int* ptab = a.page_indices + (size_t)item.seq * a.P;
+            const int key0 = item.kv_begin - (item.kv_begin & (BR - 1));
+            const int nst = (item.kv_end - key0 + kKS - 1) / kKS;
+            // page ids of 32 consecutive logical pages, one per lane
+            int win0 = key0 / ps;
+            int win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
+            for (int st = 0; st < nst && ok; ++st) {
+                const int k_stage = key0 + st * kKS;
+                // make sure the page-id window covers this stage
+                const int lp_last = min(k_stage + kKS - 1, item.kv_end - 1) / ps;
+                if (lp_last - win0 >= 32) {
+                    win0 = k_stage / ps;
+                    win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
+                }
+                if (!mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t st_base = smem0 + s * Gm::SB;
+                const uint32_t kv_base = st_base + Gm::QB;
+                // copy tasks of this stage, lane-strided: (page run b, K/V, column block)
+                auto task = [&](int t, int& x, int& y, uint32_t& dst) -> int {
+                    // 0: nothing to copy, 1: copy, 2: bad page id
+                    const int per = FP8 ? 2 : 2 * Gm::DH;
+                    const int b = t / per, rem = t % per;
+                    const int kv = FP8 ? rem : rem / Gm::DH;
+                    const int dh = FP8 ? 0 : rem % Gm::DH;
+                    const int k0 = k_stage + b * BR;
+                    const int lp = k0 / ps;
+                    const int pg = __shfl_sync(0xffffffffu, win, (lp - win0) & 31);
+                    if (t >= tasks || k0 >= item.kv_end || k0 + BR <= item.kv_begin) return 0;
+                    if ((unsigned)pg >= (unsigned)a.N) return 2;
+                    x = (2 * item.head + kv) * D + dh * 64;
+                    y = pg * ps + (k0 - lp * ps);
+                    dst = kv_base + (uint32_t)(b * PBB_P) +
+                          (FP8 ? (uint32_t)(kv * BR * D) : (uint32_t)((kv * Gm::DH + dh) * BR * 128));
+                    return 1;
+                };
+                int n_mine = 0, bad = 0;
+                for (int t0 = 0; t0 < tasks; t0 += 32) {
+                    int x, y;
+                    uint32_t dst;
+                    const int r = task(t0 + lane, x, y, dst);
+                    n_mine += r == 1;
+                    bad |= r == 2;
+                }
+                const int n_issue = __reduce_add_sync(0xffffffffu, n_mine);
+                if (__any_sync(0xffffffffu, bad)) {
+                    // a page id outside [0, N): never dereferenced; its keys read as zero
+                    if (lane == 0) set_status(ctrl, RPA_ERR_BAD_PAGE_INDEX);
+                    for (int i = lane; i < Gm::KVB / 16; i += 32)
+                        *reinterpret_cast<uint4*>(smem + (kv_base - smem0) + i * 16) = make_uint4(0, 0, 0, 0);
+                    fence_proxy_async_smem();
+                }
+                if (lane == 0) {
+                    int* m = meta[s];
+                    m[mItem] = it;
+                    m[mSeq] = item.seq;
+                    m[mHead] = item.head;
+                    m[mQStart] = q_start;
+                    m[mQl] = ql;
+                    m[mKl] = kl;
+                    m[mKvBegin] = item.kv_begin;
+                    m[mKvEnd] = item.kv_end;
+                    m[mPart] = item.part;
+                    m[mTok0] = item.tok0;
+                    m[mNtok] = item.ntok;
+                    m[mSt] = st;
+                    m[mNst] = nst;
+                    m[mKey0] = k_stage;
+                    m[mStop] = 0;
+                }
+                __syncwarp();
+                const uint32_t fb = smem_u32(&full_bar[s]);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(fb, (uint32_t)n_issue * box_bytes +
+                                                  (st == 0 ? (uint32_t)(Gm::DHQ * p.Tt * a.G * 128) : 0u));
+                __syncwarp();
+                if (st == 0 && lane < Gm::DHQ)
+                    tma_load_3d(st_base + lane * 2048, &qmap, fb, lane * 64, item.head * a.G,
+                                q_start + item.tok0);
+                for (int t0 = 0; t0 < tasks; t0 += 32) {
+                    int x, y;
+                    uint32_t dst;
+                    if (task(t0 + lane, x, y, dst) == 1) tma_load_2d(dst, &kvmap, fb, x, y);
+                }
+                if (++s == kNS) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            it = __shfl_sync(0xffffffffu, nxt, 0);
+        }
+        if (ok && mbar_wait(smem_u32(&empty_bar[s]), ph ^ 1u, ctrl, tmo)) {
+            if (lane == 0) {
+                meta[s][mStop] = 1;
+                mbar_arrive(smem_u32(&full_bar[s]));
+            }
+        } else {
+            // gave up: let the copies already issued land before leaving
+            for (int i = 0; i < kNS; ++i) mbar_wait(smem_u32(&full_bar[i]), 0, ctrl, tmo);
+        }
+        return;
+    }
+
+    // =============================== consumers ===============================
+    const int w = warp;
+    const int G = a.G, Hq = a.Hq;
+    const int BR = p.BR, br_shift = p.br_shift;
+    const uint32_t PBB = FP8 ? (uint32_t)(2 * BR * D) : (uint32_t)(2 * Gm::DH * BR * 128);
+    uint8_t* conv = smem + kNS * Gm::SB + w * Gm::CONV;  // fp8 only
+    int s = 0;
+    uint32_t ph = 0, mph = 0;
+    uint32_t qf[D / 16][4];
+    float o_acc[D / 8][4];
+    float m_r[2], l_r[2];
+    int pos[2];
+    for (;;) {
+        if (!mbar_wait(smem_u32(&full_bar[s]), ph, ctrl, tmo)) return;
+        const int* m = meta[s];
+        if (m[mStop]) return;
+        const int st = m[mSt], nst = m[mNst];
+        const int kv_begin = m[mKvBegin], kv_end = m[mKvEnd];
+        const int kl = m[mKl], ql = m[mQl];
+        const int tok0 = m[mTok0], ntok = m[mNtok];
+        const uint32_t st_base = smem0 + s * Gm::SB;
+        const uint32_t kv_base = st_base + Gm::QB;
+        if (st == 0) {
+            // Q fragments (A operand) for the whole item, from the stage's Q area
+#pragma unroll
+            for (int kd = 0; kd < D / 16; ++kd) {
+                const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int c = 2 * kd + (lane >> 4);
+                const uint32_t line = (uint32_t)((c >> 3) * 16 + r);
+                ldsm_x4(st_base + swz128(line, c & 7), qf[kd][0], qf[kd][1], qf[kd][2], qf[kd][3]);
+                if constexpr (F16) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t v = qf[kd][k];
+                        qf[kd][k] = pack2<true>(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+            m_r[0] = m_r[1] = -INFINITY;
+            l_r[0] = l_r[1] = 0.f;
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) pos[ri] = kl - ql + tok0 + ((lane >> 2) + ri * 8) / G;
+        }
+
+        // ---- this warp's 16 keys: [kw, kw + 16)
+        const int kw = m[mKey0] + 16 * w;
+        const bool any_in = kw < kv_end && kw + 16 > kv_begin;
+        if (any_in) {
+            const bool partial = kw < kv_begin || kw + 16 > kv_end;
+            uint32_t kb, vb;  // bases of row 0 for the ldmatrix address helpers below
+            if constexpr (FP8) {
+                // e4m3 -> f16 into this warp's buffer: [K 16 rows][V 16 rows] of D f16, swizzled
+                for (int i = lane; i < 16 * 2 * (D / 8); i += 32) {
+                    const int row = i / (2 * (D / 8));
+                    const int rem = i % (2 * (D / 8));
+                    const int kv = rem / (D / 8), ch = rem % (D / 8);
+                    const int kk = 16 * w + row;
+                    const int j = kw + row;
+                    uint4 o4 = make_uint4(0, 0, 0, 0);
+                    if (j >= kv_begin && j < kv_end) {
+                        const int b = kk >> br_shift, r = kk & (BR - 1);
+                        const uint8_t* src = smem + (kv_base - smem0) + b * PBB + kv * BR * D + r * D + ch * 8;
+                        const uint2 raw = *reinterpret_cast<const uint2*>(src);
+                        o4.x = e4m3x2_to_f16x2((uint16_t)(raw.x & 0xffff));
+                        o4.y = e4m3x2_to_f16x2((uint16_t)(raw.x >> 16));
+                        o4.z = e4m3x2_to_f16x2((uint16_t)(raw.y & 0xffff));
+                        o4.w = e4m3x2_to_f16x2((uint16_t)(raw.y >> 16));
+                    }
+                    *reinterpret_cast<uint4*>(conv + kv * (16 * D * 2) + row * (D * 2) +
+                                              (((ch ^ row) & 7) | (ch & ~7)) * 16) = o4;
+                }
+                __syncwarp();
+                kb = smem_u32(conv);
+                vb = kb + 16 * D * 2;
+            } else {
+                if (partial) {
+                    // keys of this slice outside [kv_begin, kv_end): V rows to zero
+                    for (int i = lane; i < 16 * Gm::DH * 8; i += 32) {
+                        const int row = i / (Gm::DH * 8);
+                        const int c = i % (Gm::DH * 8);
+                        const int j = kw + row;
+                        if (j >= kv_begin && j < kv_end) continue;
+                        const int kk = 16 * w + row;
+                        const int b = kk >> br_shift, r = kk & (BR - 1);
+                        const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
+                        *reinterpret_cast<uint4*>(smem + (kv_base - smem0) + b * PBB + swz128(line, c & 7)) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                kb = kv_base;
+                vb = kv_base;
+            }
+
+            // ---- S = Q K^T  (16 rows x 16 keys)
+            float sacc[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+            {
+                const int row = (lane & 7) + (lane >> 4) * 8;  // key row of this lane's ldmatrix
+#pragma unroll
+                for (int kd = 0; kd < D / 16; ++kd) {
+                    const int c = 2 * kd + ((lane >> 3) & 1);
+                    uint32_t addr;
+                    if constexpr (FP8) {
+                        addr = kb + row * (D * 2) + ((((c ^ row) & 7) | (c & ~7)) * 16);
+                    } else {
+                        const int kk = 16 * w + row;
+                        const int b = kk >> br_shift, r = kk & (BR - 1);
+                        const uint32_t line = (uint32_t)((c >> 3) * BR + r);
+                        addr = kb + b * PBB + swz128(line, c & 7);
+                    }
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(addr, b0, b1, b2, b3);
+                    mma16816<F16>(sacc[0], qf[kd], b0, b1);
+                    mma16816<F16>(sacc[1], qf[kd], b2, b3);
+                }
+            }
+            // ---- scale, softcap, masks (log2 domain)
+            const bool need_mask = partial || (a.causal && kw + 15 > kl - ql + tok0) ||
+                                   (a.has_window && kw <= kl - ql + tok0 + ntok - 1 - a.window);
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int ri = e >> 1;
+                    float x = sacc[nb][e];
+                    if (a.has_cap) {
+                        const float t = ex2(x * a.cap_exp);
+                        x = a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + t);
+                    } else {
+                        x *= a.qk_log2;
+                    }
+                    if (need_mask) {
+                        const int j = kw + nb * 8 + (lane & 3) * 2 + (e & 1);
+                        const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos[ri]) &&
+                                         (!a.has_window || j > pos[ri] - a.window);
+                        x = okk ? x : -INFINITY;
+                    }
+                    sacc[nb][e] = x;
+                    mx[ri] = fmaxf(mx[ri], x);
+                }
+            }
+            float base[2];
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 1));
+                mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 2));
+                const float m_new = fmaxf(m_r[ri], mx[ri]);
+                base[ri] = m_new == -INFINITY ? 0.f : m_new;
+                const float alpha = ex2(m_r[ri] - base[ri]);
+                m_r[ri] = m_new;
+                l_r[ri] *= alpha;
+#pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    o_acc[nd][2 * ri] *= alpha;
+                    o_acc[nd][2 * ri + 1] *= alpha;
+                }
+            }
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float pe = ex2(sacc[nb][e] - base[e >> 1]);
+                    sacc[nb][e] = pe;
+                    l_r[e >> 1] += pe;
+                }
+            }
+            // ---- O += P V
+            {
+                uint32_t pa[4];
+                pa[0] = pack2<F16>(sacc[0][0], sacc[0][1]);
+                pa[1] = pack2<F16>(sacc[0][2], sacc[0][3]);
+                pa[2] = pack2<F16>(sacc[1][0], sacc[1][1]);
+                pa[3] = pack2<F16>(sacc[1][2], sacc[1][3]);
+                const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+                    const int c = 2 * nd2 + (lane >> 4);
+                    uint32_t addr;
+                    if constexpr (FP8) {
+                        addr = vb + row * (D * 2) + ((((c ^ row) & 7) | (c & ~7)) * 16);
+                    } else {
+                        const int kk = 16 * w + row;
+                        const int b = kk >> br_shift, r = kk & (BR - 1);
+                        const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
+                        addr = vb + b * PBB + swz128(line, c & 7);
+                    }
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(addr, b0, b1, b2, b3);
+                    mma16816<F16>(o_acc[2 * nd2], pa, b0, b1);
+                    mma16816<F16>(o_acc[2 * nd2 + 1], pa, b2, b3);
+                }
+            }
+        }
+
+        const uint32_t eb = smem_u32(&empty_bar[s]);
+        if (st == nst - 1) {
+            // ---- merge the four warps' partials; the stage's own buffers hold them
+            float* red_o = FP8 ? reinterpret_cast<float*>(smem + kNS * Gm::SB)
+                               : reinterpret_cast<float*>(smem + (kv_base - smem0));  // [kCW][16][D]
+            float* red_ml = reinterpret_cast<float*>(smem + (st_base - smem0));        // [kCW][16][2]
+            float lsum[2];
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                lsum[ri] = l_r[ri] + __shfl_xor_sync(0xffffffffu, l_r[ri], 1);
+                lsum[ri] += __shfl_xor_sync(0xffffffffu, lsum[ri], 2);
+            }
+            const uint32_t mb = smem_u32(&merge_bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mb);  // A: every warp is done reading the stage
+            if (!mbar_wait(mb, mph, ctrl, tmo)) return;
+            mph ^= 1u;
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                const int r = (lane >> 2) + ri * 8;
+#pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd)
+                    *reinterpret_cast<float2*>(red_o + (w * 16 + r) * D + nd * 8 + (lane & 3) * 2) =
+                        make_float2(o_acc[nd][2 * ri], o_acc[nd][2 * ri + 1]);
+                if ((lane & 3) == 0) {
+                    red_ml[(w * 16 + r) * 2] = m_r[ri];
+                    red_ml[(w * 16 + r) * 2 + 1] = lsum[ri];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mb);  // B: every partial is in shared memory
+            if (!mbar_wait(mb, mph, ctrl, tmo)) return;
+            mph ^= 1u;
+            const int rows_used = ntok * G;
+            const int part = m[mPart];
+            const int q_start = m[mQStart];
+            const int head = m[mHead];
+            for (int e = w * 32 + lane; e < 16 * (D / 2); e += kCW * 32) {
+                const int r = e / (D / 2);
+                const int c = (e % (D / 2)) * 2;
+                if (r >= rows_used) break;
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < kCW; ++ww) M = fmaxf(M, red_ml[(ww * 16 + r) * 2]);
+                float L = 0.f, o0 = 0.f, o1 = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int ww = 0; ww < kCW; ++ww) {
+                        const float sc = ex2(red_ml[(ww * 16 + r) * 2] - M);
+                        L += sc * red_ml[(ww * 16 + r) * 2 + 1];
+                        const float2 v = *reinterpret_cast<const float2*>(red_o + (ww * 16 + r) * D + c);
+                        o0 += sc * v.x;
+                        o1 += sc * v.y;
+                    }
+                }
+                if (part < 0) {
+                    const float inv = L > 0.f ? a.v_scale / L : 0.f;
+                    const int t = q_start + tok0 + r / G;
+                    const int qh = head * G + r % G;
+                    *reinterpret_cast<uint32_t*>(a.o + (((size_t)t * Hq + qh) * D + c) * 2) =
+                        pack2<false>(o0 * inv, o1 * inv);
+                } else {
+                    *reinterpret_cast<float2*>(a.part_o + ((size_t)part * kDecRows + r) * D + c) =
+                        make_float2(o0, o1);
+                    if (c == 0)
+                        *reinterpret_cast<float2*>(a.part_ml + ((size_t)part * kDecRows + r) * 2) =
+                            make_float2(M, L);
+                }
+            }
+            fence_proxy_async_smem();  // the stage will be refilled by bulk copies
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eb);
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eb);
+        }
+        if (++s == kNS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+}
+
+template <int D, bool FP8>
+struct DecKern {
+    using Gm = DecGeom<D, FP8>;
+    static cudaError_t prepare(int* bps) {
+        cudaError_t e = cudaFuncSetAttribute(rpa_decode_attn<D, FP8>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_decode_attn<D, FP8>, kDecThreads,
+                                                             Gm::SMEM);
+    }
+    static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p,
+                              const Launch& l) {
+        rpa_decode_attn<D, FP8><<<l.grid, kDecThreads, Gm::SMEM, l.stream>>>(kvm, qm, p);
+        return cudaGetLastError();
+    }
+};
+
+}  // namespace
+
+cudaError_t decode_prepare(int D, int fp8, int* bps) {
+    if (fp8) {
+        if (D == 64) return DecKern<64, true>::prepare(bps);
+        if (D == 128) return DecKern<128, true>::prepare(bps);
+        if (D == 256) return DecKern<256, true>::prepare(bps);
+    } else {
+        if (D == 64) return DecKern<64, false>::prepare(bps);
+        if (D == 128) return DecKern<128, false>::prepare(bps);
+        if (D == 256) return DecKern<256, false>::prepare(bps);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int fp8,
+                              const Launch& l) {
+    const int D = p.a.D;
+    if (fp8) {
+        if (D == 64) return DecKern<64, true>::launch(kvm, qm, p, l);
+        if (D == 128) return DecKern<128, true>::launch(kvm, qm, p, l);
+        if (D == 256) return DecKern<256, true>::launch(kvm, qm, p, l);
+    } else {
+        if (D == 64) return DecKern<64, false>::launch(kvm, qm, p, l);
+        if (D == 128) return DecKern<128, false>::launch(kvm, qm, p, l);
+        if (D == 256) return DecKern<256, false>::launch(kvm, qm, p, l);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rpa

@@ -17,6 +17,10 @@
 using namespace rpa;
 
 struct RpaHandle {
+    CUtensorMap kvmap;   // decode gather descriptors, re-encoded when the pointers change
+    CUtensorMap qmap;
+    const void* kvmap_ptr;
+    const void* qmap_ptr;
     RpaCfg cfg;
     int device;
     int sms;
@@ -25,6 +29,9 @@ struct RpaHandle {
     int max_dec_units, max_pf_units, max_units, max_part, max_comb;
     float qk_log2, cap_exp, cap_log2, v_scale;
     int window;
+    int BR, br_shift, Tt;
+    int debug_stall;
+    unsigned long long timeout_ns;
     void* ws;
     size_t ws_bytes;
     int* ctrl;
@@ -145,6 +152,7 @@ int rpa_validate_cfg(const RpaCfg* c) {
     if (c->num_q_heads % c->num_kv_heads) return RPA_ERR_UNSUPPORTED;
     if (c->num_q_heads / c->num_kv_heads > kPfRows) return RPA_ERR_UNSUPPORTED;
     if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return RPA_ERR_UNSUPPORTED;
+    if (c->page_size % 4) return RPA_ERR_UNSUPPORTED;  // page runs of the gather are >= 4 slots
     if (c->q_dtype != RPA_DT_BF16) return RPA_ERR_UNSUPPORTED;
     if (c->kv_dtype != RPA_DT_BF16 && c->kv_dtype != RPA_DT_FP8_E4M3) return RPA_ERR_UNSUPPORTED;
     // masked keys get weight exactly 0 only if the additive mask value is huge and negative
@@ -171,10 +179,24 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     h->cap_log2 = c.has_soft_cap ? (float)(c.soft_cap * kLog2e) : 0.f;
     h->v_scale = c.has_v_scale ? c.v_scale : 1.f;
     h->window = c.has_sliding_window ? (int)(c.sliding_window > 0x7fffffff ? 0x7fffffff : c.sliding_window) : 0;
+    h->BR = 64;
+    while ((int)(c.page_size % h->BR)) h->BR >>= 1;
+    h->br_shift = 0;
+    while ((1 << h->br_shift) < h->BR) ++h->br_shift;
+    h->Tt = h->G <= kDecRows ? kDecRows / h->G : 1;
+    {
+        // test hooks: a producer that issues nothing, and the bound of every device wait
+        const char* e = getenv("RPA_DEBUG_STALL_PRODUCER");
+        h->debug_stall = (e && e[0] == '1') ? 1 : 0;
+        const char* t = getenv("RPA_DEBUG_TIMEOUT_MS");
+        const long long ms = t ? atoll(t) : 1000;
+        h->timeout_ns = (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
+    }
 
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-        plan_prepare() != cudaSuccess || attn_prepare(h->D, h->fp8, &h->dec_bps, &h->pf_bps) != cudaSuccess) {
+        plan_prepare() != cudaSuccess || attn_prepare(h->D, h->fp8, &h->pf_bps) != cudaSuccess ||
+        decode_prepare(h->D, h->fp8, &h->dec_bps) != cudaSuccess) {
         cudaGetLastError();
         delete h;
         return RPA_ERR_CUDA;
@@ -301,16 +323,39 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     ap.part_o = h->part_o;
     ap.part_ml = h->part_ml;
 
-    ap.items = h->dec_items;
-    ap.item_count_word = kNumDecItems;
-    ap.counter_word = kDecCounter;
-    if (launch_decode(ap, h->fp8, Launch{h->sms * h->dec_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    if (c.num_q_tokens > 0) {
+        if (h->kvmap_ptr != kv_pages) {
+            if (encode_kv_map(&h->kvmap, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
+                              (int)c.num_kv_heads, h->D, h->BR) != 0)
+                return RPA_ERR_INVALID_ARG;
+            h->kvmap_ptr = kv_pages;
+        }
+        if (h->qmap_ptr != q) {
+            if (encode_q_map(&h->qmap, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G, h->Tt) != 0)
+                return RPA_ERR_INVALID_ARG;
+            h->qmap_ptr = q;
+        }
+        DecParams dp;
+        dp.a = ap;
+        dp.a.items = h->dec_items;
+        dp.a.item_count_word = kNumDecItems;
+        dp.a.counter_word = kDecCounter;
+        dp.BR = h->BR;
+        dp.br_shift = h->br_shift;
+        dp.Tt = h->Tt;
+        dp.debug_stall = h->debug_stall;
+        dp.timeout_ns = h->timeout_ns;
+        if (launch_decode_tma(h->kvmap, h->qmap, dp, h->fp8, Launch{h->sms * h->dec_bps, st}) != cudaSuccess)
+            return RPA_ERR_CUDA;
+    }
     if (ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return RPA_ERR_CUDA;
 
-    ap.items = h->pf_items;
-    ap.item_count_word = kNumPfItems;
-    ap.counter_word = kPfCounter;
-    if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    if (c.num_q_tokens > 0) {
+        ap.items = h->pf_items;
+        ap.item_count_word = kNumPfItems;
+        ap.counter_word = kPfCounter;
+        if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    }
     if (ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return RPA_ERR_CUDA;
 
     CombParams cp;

@@ -4,6 +4,7 @@
 // ldmatrix, mma.sync, ex2) used by the attention kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -94,6 +95,15 @@ struct AttnParams {
     float* part_ml;        // [max_part, kDecRows, 2]
 };
 
+struct DecParams {
+    AttnParams a;
+    int BR;                 // keys per copied page run: gcd(page_size, 64), >= 4
+    int br_shift;           // log2(BR)
+    int Tt;                 // query tokens per Q copy: 16 / G
+    int debug_stall;        // test hook: the producer issues nothing
+    unsigned long long timeout_ns;  // bound of every mbarrier wait
+};
+
 struct CombParams {
     uint8_t* o;
     const int* cu_q_lens;
@@ -111,11 +121,16 @@ struct Launch {
     cudaStream_t stream;
 };
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
-cudaError_t launch_decode(const AttnParams& p, int fp8, const Launch& l);
 cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l);
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
+cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int fp8,
+                              const Launch& l);
+cudaError_t decode_prepare(int D, int fp8, int* blocks_per_sm);
+// tensor maps for the decode gather (host; no allocation)
+int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR);
+int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt);
 // occupancy / attributes (call once per device)
-cudaError_t attn_prepare(int D, int fp8, int* dec_blocks_per_sm, int* pf_blocks_per_sm);
+cudaError_t attn_prepare(int D, int fp8, int* pf_blocks_per_sm);
 size_t plan_smem_bytes();
 cudaError_t plan_prepare();
 
@@ -194,6 +209,71 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
 
 __device__ __forceinline__ void set_status(int* ctrl, int code) {
     atomicCAS(ctrl + kStatus, 0, code);
+}
+
+// ---- mbarrier, bulk tensor copies, timer
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Wait for the phase of `parity` to complete, giving up after timeout_ns:
+// then the status word gets RPA_ERR_TIMEOUT and false is returned.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* ctrl,
+                                          uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > timeout_ns) {
+            set_status(ctrl, RPA_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// 2-D / 3-D tiled tensor copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int x, int y,
+                                            int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
+        : "memory");
 }
 #endif
 

@@ -61,7 +61,7 @@ int setup(int dev, int D, int fp8, void** scratch, int* dec_bps, int* pf_bps) {
     const int di = d_index(D);
     if (!g_ready[dev][di][fp8]) {
         int a = 0, b = 0;
-        if (attn_prepare(D, fp8, &a, &b) != cudaSuccess) {
+        if (decode_prepare(D, fp8, &a) != cudaSuccess || attn_prepare(D, fp8, &b) != cudaSuccess) {
             cudaGetLastError();
             return RPA_ERR_CUDA;
         }
@@ -198,14 +198,31 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     ap.ctrl = ctrl;
     ap.part_o = part_o;
     ap.part_ml = part_ml;
-    ap.items = dec_items;
-    ap.item_count_word = kNumDecItems;
-    ap.counter_word = kDecCounter;
-    if (launch_decode(ap, fp8, Launch{(int)dec_slots, st}) != cudaSuccess) return RPA_ERR_CUDA;
-    ap.items = pf_items;
-    ap.item_count_word = kNumPfItems;
-    ap.counter_word = kPfCounter;
-    if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    if (c.num_q_tokens > 0) {
+        int BR = 64, br_shift = 0;
+        while ((int)(c.page_size % BR)) BR >>= 1;
+        while ((1 << br_shift) < BR) ++br_shift;
+        const int Tt = G <= kDecRows ? kDecRows / G : 1;
+        CUtensorMap kvm, qm;  // descriptors are encoded on the host stack
+        if (encode_kv_map(&kvm, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0 ||
+            encode_q_map(&qm, q, c.num_q_tokens, (int)c.num_q_heads, D, G, Tt) != 0)
+            return RPA_ERR_INVALID_ARG;
+        DecParams dp;
+        dp.a = ap;
+        dp.a.items = dec_items;
+        dp.a.item_count_word = kNumDecItems;
+        dp.a.counter_word = kDecCounter;
+        dp.BR = BR;
+        dp.br_shift = br_shift;
+        dp.Tt = Tt;
+        dp.debug_stall = 0;
+        dp.timeout_ns = 1000000000ull;
+        if (launch_decode_tma(kvm, qm, dp, fp8, Launch{(int)dec_slots, st}) != cudaSuccess) return RPA_ERR_CUDA;
+        ap.items = pf_items;
+        ap.item_count_word = kNumPfItems;
+        ap.counter_word = kPfCounter;
+        if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    }
 
     CombParams cp;
     cp.o = static_cast<uint8_t*>(o);

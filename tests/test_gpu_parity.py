@@ -225,3 +225,24 @@ def test_repeat_calls_are_deterministic():
     b = o_to_f64(att.forward(*t, p.num_seqs))
     assert np.array_equal(a, b)
     att.close()
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
+    """The decode producer is told to issue nothing (test hook read at rpa_create): every
+    consumer wait must expire after its bound, set RPA_ERR_TIMEOUT and return."""
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    p = ri.random_small(49, num_seqs=4, decode_only=True, max_kv=300, num_q_heads=8,
+                        num_kv_heads=2, head_dim=128)
+    monkeypatch.setenv("RPA_DEBUG_STALL_PRODUCER", "1")
+    monkeypatch.setenv("RPA_DEBUG_TIMEOUT_MS", "50")
+    att = RaggedPagedAttention(**p.cfg_dict())
+    monkeypatch.delenv("RPA_DEBUG_STALL_PRODUCER")
+    monkeypatch.delenv("RPA_DEBUG_TIMEOUT_MS")
+    t = to_dev(p)
+    att.forward(*t, p.num_seqs)
+    assert att.status() == 6
+    att.close()
+    got, st = run(p, tensors=t)  # a fresh handle on the same context works
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, "after timeout")

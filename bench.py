@@ -37,7 +37,7 @@ import rpa_inputs as ri  # noqa: E402
 METRIC = "ragged paged attn tokens/s; decode HBM GB/s & prefill TFLOP/s vs roofline"
 KERNEL_NAMES = ("planner", "decode_attention", "prefill_attention", "combine")
 KERNEL_SOURCES = {
-    "decode_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_attn_mma.cu",
+    "decode_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_decode.cu",
                          "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
     "prefill_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_attn_mma.cu",
                           "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],

@@ -19,8 +19,11 @@ using namespace rpa;
 struct RpaHandle {
     CUtensorMap kvmap;   // decode gather descriptors, re-encoded when the pointers change
     CUtensorMap qmap;
+    CUtensorMap qmap_pf;  // Q tiles of the tensor-memory prefill kernel
     const void* kvmap_ptr;
     const void* qmap_ptr;
+    int tc;               // prefill on tcgen05 (bf16 K/V, head_dim 64 or 128)
+    int pf_rows;          // rows of a prefill tile (128 with tcgen05, else 64)
     RpaCfg cfg;
     int device;
     int sms;
@@ -184,6 +187,8 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     h->br_shift = 0;
     while ((1 << h->br_shift) < h->BR) ++h->br_shift;
     h->Tt = h->G <= kDecRows ? kDecRows / h->G : 1;
+    h->tc = (!h->fp8 && (h->D == 64 || h->D == 128)) ? 1 : 0;
+    h->pf_rows = h->tc ? kTcRows : kPfRows;
     {
         // test hooks: a producer that issues nothing, and the bound of every device wait
         const char* e = getenv("RPA_DEBUG_STALL_PRODUCER");
@@ -195,7 +200,8 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
 
     if (cudaGetDevice(&h->device) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-        plan_prepare() != cudaSuccess || attn_prepare(h->D, h->fp8, &h->pf_bps) != cudaSuccess ||
+        plan_prepare() != cudaSuccess ||
+        (h->tc ? prefill_tc_prepare(h->D, &h->pf_bps) : attn_prepare(h->D, h->fp8, &h->pf_bps)) != cudaSuccess ||
         decode_prepare(h->D, h->fp8, &h->dec_bps) != cudaSuccess) {
         cudaGetLastError();
         delete h;
@@ -206,7 +212,7 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
 
     // worst-case capacities (see the planner's chunk rule)
     const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
-    const int64_t Tq = kPfRows / h->G;
+    const int64_t Tq = h->pf_rows / h->G;
     const int64_t dec_slots = (int64_t)h->sms * h->dec_bps;
     h->max_dec_units = (int)(S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1);
     h->max_pf_units = (int)((c.num_q_tokens + Tq - 1) / Tq + S + 1);
@@ -276,7 +282,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.has_window = c.has_sliding_window ? 1 : 0;
     pp.window = h->window;
     pp.dec_rows = kDecRows;
-    pp.pf_rows = kPfRows;
+    pp.pf_rows = h->pf_rows;
     pp.dec_slots = h->sms * h->dec_bps;
     pp.max_units = h->max_units;
     pp.max_dec_units = h->max_dec_units;
@@ -331,7 +337,9 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
             h->kvmap_ptr = kv_pages;
         }
         if (h->qmap_ptr != q) {
-            if (encode_q_map(&h->qmap, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G, h->Tt) != 0)
+            if (encode_q_map(&h->qmap, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G, h->Tt) != 0 ||
+                (h->tc && encode_q_map(&h->qmap_pf, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G,
+                                       kTcRows / h->G) != 0))
                 return RPA_ERR_INVALID_ARG;
             h->qmap_ptr = q;
         }
@@ -354,7 +362,17 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
         ap.items = h->pf_items;
         ap.item_count_word = kNumPfItems;
         ap.counter_word = kPfCounter;
-        if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+        if (h->tc) {
+            TcParams tp;
+            tp.a = ap;
+            tp.BR = h->BR;
+            tp.Tq = kTcRows / h->G;
+            tp.timeout_ns = h->timeout_ns;
+            if (launch_prefill_tc(h->kvmap, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
+                return RPA_ERR_CUDA;
+        } else if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) {
+            return RPA_ERR_CUDA;
+        }
     }
     if (ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return RPA_ERR_CUDA;
 
@@ -483,7 +501,7 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[3] = ctrl[kNumComb];
     info[4] = ctrl[kDecChunk];
     info[5] = kDecRows;
-    info[6] = kPfRows;
+    info[6] = h->pf_rows;
     info[7] = ctrl[kNumPart];
     info[8] = ctrl[kNumUnits];
     info[9] = ctrl[kSorted];

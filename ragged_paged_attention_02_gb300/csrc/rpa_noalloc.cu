@@ -61,7 +61,9 @@ int setup(int dev, int D, int fp8, void** scratch, int* dec_bps, int* pf_bps) {
     const int di = d_index(D);
     if (!g_ready[dev][di][fp8]) {
         int a = 0, b = 0;
-        if (decode_prepare(D, fp8, &a) != cudaSuccess || attn_prepare(D, fp8, &b) != cudaSuccess) {
+        const bool tc = !fp8 && (D == 64 || D == 128);
+        if (decode_prepare(D, fp8, &a) != cudaSuccess ||
+            (tc ? prefill_tc_prepare(D, &b) : attn_prepare(D, fp8, &b)) != cudaSuccess) {
             cudaGetLastError();
             return RPA_ERR_CUDA;
         }
@@ -107,7 +109,9 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
 
     // worst-case capacities, the same rule as rpa_create's workspace
     const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
-    const int64_t Tq = kPfRows / G;
+    const bool tc = !fp8 && (D == 64 || D == 128);
+    const int pf_rows = tc ? kTcRows : kPfRows;
+    const int64_t Tq = pf_rows / G;
     const int64_t dec_slots = (int64_t)sms * dec_bps;
     const int64_t max_dec_units = S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1;
     const int64_t max_pf_units = (c.num_q_tokens + Tq - 1) / Tq + S + 1;
@@ -156,7 +160,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     pp.has_window = c.has_sliding_window ? 1 : 0;
     pp.window = window;
     pp.dec_rows = kDecRows;
-    pp.pf_rows = kPfRows;
+    pp.pf_rows = pf_rows;
     pp.dec_slots = (int)dec_slots;
     pp.max_units = (int)max_units;
     pp.max_dec_units = (int)max_dec_units;
@@ -203,9 +207,10 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
         while ((int)(c.page_size % BR)) BR >>= 1;
         while ((1 << br_shift) < BR) ++br_shift;
         const int Tt = G <= kDecRows ? kDecRows / G : 1;
-        CUtensorMap kvm, qm;  // descriptors are encoded on the host stack
+        CUtensorMap kvm, qm, qm_pf;  // descriptors are encoded on the host stack
         if (encode_kv_map(&kvm, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0 ||
-            encode_q_map(&qm, q, c.num_q_tokens, (int)c.num_q_heads, D, G, Tt) != 0)
+            encode_q_map(&qm, q, c.num_q_tokens, (int)c.num_q_heads, D, G, Tt) != 0 ||
+            (tc && encode_q_map(&qm_pf, q, c.num_q_tokens, (int)c.num_q_heads, D, G, kTcRows / G) != 0))
             return RPA_ERR_INVALID_ARG;
         DecParams dp;
         dp.a = ap;
@@ -221,7 +226,16 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
         ap.items = pf_items;
         ap.item_count_word = kNumPfItems;
         ap.counter_word = kPfCounter;
-        if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+        if (tc) {
+            TcParams tp;
+            tp.a = ap;
+            tp.BR = BR;
+            tp.Tq = kTcRows / G;
+            tp.timeout_ns = 1000000000ull;
+            if (launch_prefill_tc(kvm, qm_pf, tp, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+        } else if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) {
+            return RPA_ERR_CUDA;
+        }
     }
 
     CombParams cp;

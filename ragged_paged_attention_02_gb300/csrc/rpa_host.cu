@@ -6,6 +6,7 @@
 // caller's stream.  No call synchronises except rpa_get_status,
 // rpa_read_plan and rpa_destroy.
 #include <math.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -23,7 +24,7 @@ struct RpaHandle {
     const void* kvmap_ptr;
     const void* qmap_ptr;
     int tc;               // prefill on tcgen05 (bf16 K/V, head_dim 64 or 128)
-    int pf_rows;          // rows of a prefill tile (128 with tcgen05, else 64)
+    int pf_tokens;        // query tokens of a prefill tile (2 x 128-row tcgen05 tiles, else 64 rows)
     RpaCfg cfg;
     int device;
     int sms;
@@ -188,7 +189,7 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     while ((1 << h->br_shift) < h->BR) ++h->br_shift;
     h->Tt = h->G <= kDecRows ? kDecRows / h->G : 1;
     h->tc = (!h->fp8 && (h->D == 64 || h->D == 128)) ? 1 : 0;
-    h->pf_rows = h->tc ? kTcRows : kPfRows;
+    h->pf_tokens = h->tc ? 2 * (kTcRows / h->G) : (kPfRows / h->G > 0 ? kPfRows / h->G : 1);
     {
         // test hooks: a producer that issues nothing, and the bound of every device wait
         const char* e = getenv("RPA_DEBUG_STALL_PRODUCER");
@@ -198,21 +199,33 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
         h->timeout_ns = (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
     }
 
-    if (cudaGetDevice(&h->device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
-        plan_prepare() != cudaSuccess ||
-        (h->tc ? prefill_tc_prepare(h->D, &h->pf_bps) : attn_prepare(h->D, h->fp8, &h->pf_bps)) != cudaSuccess ||
-        decode_prepare(h->D, h->fp8, &h->dec_bps) != cudaSuccess) {
-        cudaGetLastError();
-        delete h;
-        return RPA_ERR_CUDA;
+    {
+        // RPA_DEBUG=1 names the set-up step that failed (stderr)
+        const char* dbg = getenv("RPA_DEBUG");
+        const bool verbose = dbg && dbg[0] == '1';
+        cudaError_t e = cudaSuccess;
+        const char* step = "";
+        if ((e = cudaGetDevice(&h->device)) != cudaSuccess) step = "cudaGetDevice";
+        else if ((e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess)
+            step = "multiprocessor count";
+        else if ((e = plan_prepare()) != cudaSuccess) step = "planner attributes";
+        else if ((e = h->tc ? prefill_tc_prepare(h->D, &h->pf_bps) : attn_prepare(h->D, h->fp8, &h->pf_bps)) !=
+                 cudaSuccess)
+            step = "prefill kernel attributes";
+        else if ((e = decode_prepare(h->D, h->fp8, &h->dec_bps)) != cudaSuccess) step = "decode kernel attributes";
+        else if (h->pf_bps < 1) step = "prefill kernel cannot be resident";
+        else if (h->dec_bps < 1) step = "decode kernel cannot be resident";
+        if (step[0]) {
+            if (verbose) fprintf(stderr, "rpa_create: %s failed: %s\n", step, cudaGetErrorString(e));
+            cudaGetLastError();
+            delete h;
+            return RPA_ERR_CUDA;
+        }
     }
-    if (h->dec_bps < 1) h->dec_bps = 1;
-    if (h->pf_bps < 1) h->pf_bps = 1;
 
     // worst-case capacities (see the planner's chunk rule)
     const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
-    const int64_t Tq = h->pf_rows / h->G;
+    const int64_t Tq = h->pf_tokens;
     const int64_t dec_slots = (int64_t)h->sms * h->dec_bps;
     h->max_dec_units = (int)(S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1);
     h->max_pf_units = (int)((c.num_q_tokens + Tq - 1) / Tq + S + 1);
@@ -282,7 +295,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.has_window = c.has_sliding_window ? 1 : 0;
     pp.window = h->window;
     pp.dec_rows = kDecRows;
-    pp.pf_rows = h->pf_rows;
+    pp.pf_tokens = h->pf_tokens;
     pp.dec_slots = h->sms * h->dec_bps;
     pp.max_units = h->max_units;
     pp.max_dec_units = h->max_dec_units;
@@ -366,7 +379,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
             TcParams tp;
             tp.a = ap;
             tp.BR = h->BR;
-            tp.Tq = kTcRows / h->G;
+            tp.Tq = h->pf_tokens;
             tp.timeout_ns = h->timeout_ns;
             if (launch_prefill_tc(h->kvmap, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
                 return RPA_ERR_CUDA;
@@ -501,7 +514,7 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[3] = ctrl[kNumComb];
     info[4] = ctrl[kDecChunk];
     info[5] = kDecRows;
-    info[6] = h->pf_rows;
+    info[6] = h->pf_tokens;
     info[7] = ctrl[kNumPart];
     info[8] = ctrl[kNumUnits];
     info[9] = ctrl[kSorted];

@@ -110,8 +110,8 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     // worst-case capacities, the same rule as rpa_create's workspace
     const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
     const bool tc = !fp8 && (D == 64 || D == 128);
-    const int pf_rows = tc ? kTcRows : kPfRows;
-    const int64_t Tq = pf_rows / G;
+    const int pf_tokens = tc ? 2 * (kTcRows / G) : (kPfRows / G > 0 ? kPfRows / G : 1);
+    const int64_t Tq = pf_tokens;
     const int64_t dec_slots = (int64_t)sms * dec_bps;
     const int64_t max_dec_units = S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1;
     const int64_t max_pf_units = (c.num_q_tokens + Tq - 1) / Tq + S + 1;
@@ -160,7 +160,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     pp.has_window = c.has_sliding_window ? 1 : 0;
     pp.window = window;
     pp.dec_rows = kDecRows;
-    pp.pf_rows = pf_rows;
+    pp.pf_tokens = pf_tokens;
     pp.dec_slots = (int)dec_slots;
     pp.max_units = (int)max_units;
     pp.max_dec_units = (int)max_dec_units;
@@ -230,7 +230,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
             TcParams tp;
             tp.a = ap;
             tp.BR = BR;
-            tp.Tq = kTcRows / G;
+            tp.Tq = pf_tokens;
             tp.timeout_ns = 1000000000ull;
             if (launch_prefill_tc(kvm, qm_pf, tp, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
         } else if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) {

@@ -12,8 +12,10 @@
 //    (split-KV; partial results are merged by the combine kernel);
 //  * prefill-class sequences become units (sequence, query tile);
 //  * each unit expands to one item per kv head;
-//  * units are sorted by cost (keys to visit), longest first, so that the
-//    persistent kernels finish together; ties keep unit order.
+//  * decode units are sorted by cost (keys to visit), longest first, so that
+//    the persistent kernel finishes together; prefill units are sorted by
+//    sequence, then cost, so that the CTAs running at any moment share one
+//    sequence's K/V in L2; ties keep unit order.
 //
 // The key range of a unit is the band its rows can see (page: flashAttention
 // row_ids / col_ids masks): causal rows end at position p, windowed rows start
@@ -89,7 +91,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     int* s_pend = s_dend + p.num_seqs + 1;
     int* s_part = s_pend + p.num_seqs + 1;
     int* s_comb = s_part + p.num_seqs + 1;
-    const int Tq = max(1, p.pf_rows / p.G);  // query tokens per prefill tile
+    const int Tq = max(1, p.pf_tokens);  // query tokens per prefill tile
 
     if (tid == 0) {
         s_bad = 0;
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     __syncthreads();
 
     // ---- 4. unit descriptors and sort keys
-    const bool do_sort = n_units <= kMaxSort;
+    const bool do_sort = n_units <= kMaxSort && S < 65536;  // key fields: unit < 2^16, seq < 2^16
     for (int u = tid; u < n_units; u += blockDim.x) {
         int d[8];
         int cost;
@@ -227,8 +229,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         dst[0] = make_int4(d[0], d[1], d[2], d[3]);
         dst[1] = make_int4(d[4], d[5], d[6], d[7]);
         if (do_sort)
-            s_keys[u] = ((unsigned long long)cls_bit << 63) |
-                        ((unsigned long long)(0x7FFFFFFF - cost) << 32) | (unsigned long long)u;
+            s_keys[u] = cls_bit == 0
+                            ? ((unsigned long long)(0x7FFFFFFF - cost) << 32) | (unsigned long long)u
+                            : (1ull << 63) | ((unsigned long long)d[0] << 47) |
+                                  ((unsigned long long)(0x7FFFFFFF - cost) << 16) | (unsigned long long)u;
     }
 
     // ---- 5. bitonic sort of the keys (ascending: decode first, then cost descending)
@@ -258,7 +262,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
 
     // ---- 6. items (one per kv head) in sorted unit order
     for (int r = tid; r < n_units; r += blockDim.x) {
-        const int u = do_sort ? (int)(s_keys[r] & 0xFFFFFFFFull) : r;
+        // unit index: low 32 bits of a decode key, low 16 bits of a prefill key
+        const unsigned long long key = do_sort ? s_keys[r] : 0ull;
+        const int u = !do_sort ? r : (int)((key >> 63) ? (key & 0xFFFFull) : (key & 0xFFFFFFFFull));
         const int4* src = reinterpret_cast<const int4*>(p.units + (size_t)u * 8);
         const int4 a = src[0], b = src[1];
         const bool is_dec = r < n_dec;

@@ -1,32 +1,36 @@
 // rpa_prefill_tc.cu -- K1 prefill on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// One persistent CTA per SM takes prefill work items: 128 query rows of one kv
-// head (Tq = 128 / G tokens x the G query heads of the group, packed as the
-// "ragged_paged.zig" page packs its q block into [Tq*G, D]) against a key
-// range of one sequence.  Roles:
+// One persistent CTA per SM takes prefill work items: up to 256 query rows of
+// one kv head, as two 128-row tiles A and B (each Tq = 128 / G tokens x the G
+// query heads of the group, packed the way the "ragged_paged.zig" page packs
+// its q block into [Tq*G, D]), against a key range of one sequence.  Both
+// tiles share every K/V tile, which halves the K/V traffic per FLOP.  Roles:
 //
-//   producer warp   gathers the Q tile and, per 128-key tile, the K and V rows
-//                   through the page table with bulk tensor copies (page runs
-//                   of the page's createKvAsyncCopyDescriptors), into a
-//                   2-stage ring; 128-byte swizzle, K-major rows.
-//   MMA warp        one thread issues S = Q K^T (M=128, N=128, K=16 steps,
-//                   both operands from shared memory) into one of two TMEM
-//                   S buffers, and O += P V with P read from TMEM and V
-//                   used MN-major from shared memory; completion is signalled
-//                   with tcgen05.commit on mbarriers.
-//   4 softmax warps thread r owns TMEM lane r (query row r): it loads its S
-//                   row, applies scale / softcap / masks (flashAttention's
-//                   row_ids/col_ids masks) in the log2 domain, keeps the
-//                   running max m and sum l, writes P in bf16 over its S row,
-//                   and rescales its O row only when the max grows by more than
-//                   2^8 (the result is the same: every P and l use the same
-//                   stale max).  At the item's end it normalises O by l and
+//   producer warp   gathers the two Q tiles and, per 128-key tile, the K and V
+//                   rows through the page table with bulk tensor copies (page
+//                   runs of the page's createKvAsyncCopyDescriptors) into a
+//                   2-stage ring; 128-byte swizzle, rows K-major.
+//   MMA warp        one thread issues, per key tile j,
+//                     S_A = Q_A K_j^T, S_B = Q_B K_j^T   (both operands in smem)
+//                     O_A += P_A V_j, O_B += P_B V_j     (P from TMEM, V MN-major)
+//                   in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) so that the
+//                   tensor cores run one tile's MMAs while the other tile's
+//                   softmax works; completion is signalled by tcgen05.commit.
+//   2 x 4 softmax   warp group A (warps 0-3) owns S_A/O_A, group B (warps 4-7)
+//   warps           S_B/O_B; thread r of a group owns TMEM lane r (one query
+//                   row): it loads its S row, applies scale / softcap / masks
+//                   (flashAttention's row_ids/col_ids masks) in the log2 domain,
+//                   keeps the running max m and sum l, writes P in bf16 over its
+//                   S row, and rescales its O row only when the max grows by more
+//                   than 2^8 (every P and l use the same stale max, so the result
+//                   is unchanged).  At the item's end it normalises O by l and
 //                   stores bf16 o.
 //
 // Keys of a tile outside the item's [kv_begin, kv_end) are masked in S and
-// their V rows are zeroed in shared memory before the PV MMA (tail slots of a
-// page may hold any bits; the page zeroes K/V past kv_len the same way).
-// All waits are bounded; on expiry the status word gets RPA_ERR_TIMEOUT.
+// their V rows are zeroed in shared memory (by group A, before PV_A) since
+// tail slots of a page may hold any bits; the page zeroes K/V past kv_len the
+// same way.  All waits are bounded; on expiry the status word gets
+// RPA_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "rpa_internal.cuh"
@@ -38,7 +42,8 @@ namespace {
 constexpr int kM = kTcRows;      // query rows per tile = TMEM lanes
 constexpr int kBN = 128;         // keys per K/V tile
 constexpr int kNS = 2;           // K/V stages
-constexpr int kThreads = 192;    // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kThreads = 320;    // warps 0-7 softmax (A: 0-3, B: 4-7), 8 producer, 9 MMA
+constexpr int kProducer = 8, kMma = 9;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;  // rescale O when the row max grows by more than 2^8
 
@@ -47,14 +52,16 @@ enum TcMeta : int { tSeq = 0, tHead, tQStart, tQl, tKl, tKvBegin, tKvEnd, tTok0,
 template <int D>
 struct TcGeom {
     static constexpr int CB = D / 64;                // 128-byte column blocks of a row
-    static constexpr int QBYTES = CB * kM * 128;     // one Q slot
+    static constexpr int QTILE = CB * kM * 128;      // one 128-row Q tile
     static constexpr int KBYTES = CB * kBN * 128;    // K (or V) of one stage
     static constexpr int STAGE = 2 * KBYTES;
-    static constexpr int DATA = 2 * QBYTES + kNS * STAGE;
-    // keep one CTA per SM: it owns all 512 TMEM columns
+    static constexpr int DATA = 2 * QTILE + kNS * STAGE;
+    // one CTA per SM: it owns all 512 TMEM columns
     static constexpr int SMEM = (DATA + 1024) > 120 * 1024 ? (DATA + 1024) : 120 * 1024;
-    static constexpr int TM_S0 = 0, TM_S1 = kBN, TM_O = 2 * kBN;
-    static_assert(2 * kBN + D <= kTmemCols, "TMEM budget");
+    // TMEM columns: S_A, S_B, O_A, O_B
+    __host__ __device__ static constexpr uint32_t TM_S(int x) { return (uint32_t)(x * kBN); }
+    __host__ __device__ static constexpr uint32_t TM_O(int x) { return (uint32_t)(2 * kBN + x * D); }
+    static_assert(2 * kBN + 2 * D <= kTmemCols, "TMEM budget");
 };
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
@@ -65,12 +72,12 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                                                               const TcParams p) {
     using Gm = TcGeom<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t q_full[2], q_empty[2], meta_free[2];
+    __shared__ __align__(8) uint64_t q_full, q_empty, meta_free;
     __shared__ __align__(8) uint64_t kv_full[kNS], kv_empty[kNS];
-    __shared__ __align__(8) uint64_t s_full[2], p_full[2];
-    __shared__ __align__(8) uint64_t pv_done, o_full, o_free;
+    __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done[2];
+    __shared__ __align__(8) uint64_t o_full, o_free;
     __shared__ uint32_t tmem_base_sh;
-    __shared__ int meta[2][16];
+    __shared__ int meta[16];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const AttnParams& a = p.a;
@@ -79,39 +86,39 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     const int n_items = a.ctrl[a.item_count_word];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t smem0 = smem_u32(smem);
-    const uint32_t q_base = smem0;                         // 2 Q slots
-    const uint32_t kv_base = smem0 + 2 * Gm::QBYTES;       // kNS stages of [K | V]
+    const uint32_t q_base = smem0;                       // Q_A, Q_B
+    const uint32_t kv_base = smem0 + 2 * Gm::QTILE;      // kNS stages of [K | V]
 
     if (tid == 0) {
+        mbar_init(smem_u32(&q_full), 1);
+        mbar_init(smem_u32(&q_empty), 1);
+        mbar_init(smem_u32(&meta_free), 8);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(smem_u32(&q_full[i]), 1);
-            mbar_init(smem_u32(&q_empty[i]), 1);
-            mbar_init(smem_u32(&meta_free[i]), 4);
             mbar_init(smem_u32(&s_full[i]), 1);
             mbar_init(smem_u32(&p_full[i]), 4);
+            mbar_init(smem_u32(&pv_done[i]), 1);
         }
         for (int i = 0; i < kNS; ++i) {
             mbar_init(smem_u32(&kv_full[i]), 1);
             mbar_init(smem_u32(&kv_empty[i]), 1);
         }
-        mbar_init(smem_u32(&pv_done), 1);
         mbar_init(smem_u32(&o_full), 1);
-        mbar_init(smem_u32(&o_free), 4);
+        mbar_init(smem_u32(&o_free), 8);
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    if (warp == kMma) tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
-    if (warp == 4) {
+    if (warp == kProducer) {
         // =============================== producer ===============================
-        const int BR = p.BR, ps = a.ps, G = a.G;
+        const int BR = p.BR, ps = a.ps, G = a.G, Th = p.Tq / 2;  // tokens per Q tile
         const int tasks = (kBN / BR) * 2 * Gm::CB;
         const uint32_t box_bytes = (uint32_t)BR * 128u;
-        const uint32_t q_bytes = (uint32_t)(Gm::CB * G * p.Tq * 128);
-        int qs = 0, s = 0;
+        const uint32_t q_bytes = (uint32_t)(2 * Gm::CB * G * Th * 128);
+        int s = 0;
         uint32_t qph = 0, ph = 0;
         bool ok = true;
         int it = 0;
@@ -119,16 +126,13 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
         it = __shfl_sync(0xffffffffu, it, 0);
         for (;;) {
             const bool stop = it >= n_items;
-            // a Q slot (and its meta) for the next item, or for the stop mark
-            if (!mbar_wait(smem_u32(&q_empty[qs]), qph ^ 1u, ctrl, tmo) ||
-                !mbar_wait(smem_u32(&meta_free[qs]), qph ^ 1u, ctrl, tmo)) {
-                ok = false;
+            if (!mbar_wait(smem_u32(&q_empty), qph ^ 1u, ctrl, tmo) ||
+                !mbar_wait(smem_u32(&meta_free), qph ^ 1u, ctrl, tmo))
                 break;
-            }
             if (stop) {
                 if (lane == 0) {
-                    meta[qs][tStop] = 1;
-                    mbar_arrive(smem_u32(&q_full[qs]));
+                    meta[tStop] = 1;
+                    mbar_arrive(smem_u32(&q_full));
                 }
                 break;
             }
@@ -142,31 +146,31 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
             const int key0 = item.kv_begin - (item.kv_begin & (BR - 1));
             const int nt = (item.kv_end - key0 + kBN - 1) / kBN;
             if (lane == 0) {
-                int* m = meta[qs];
-                m[tSeq] = item.seq;
-                m[tHead] = item.head;
-                m[tQStart] = q_start;
-                m[tQl] = ql;
-                m[tKl] = kl;
-                m[tKvBegin] = item.kv_begin;
-                m[tKvEnd] = item.kv_end;
-                m[tTok0] = item.tok0;
-                m[tNtok] = item.ntok;
-                m[tNt] = nt;
-                m[tKey0] = key0;
-                m[tStop] = 0;
+                meta[tSeq] = item.seq;
+                meta[tHead] = item.head;
+                meta[tQStart] = q_start;
+                meta[tQl] = ql;
+                meta[tKl] = kl;
+                meta[tKvBegin] = item.kv_begin;
+                meta[tKvEnd] = item.kv_end;
+                meta[tTok0] = item.tok0;
+                meta[tNtok] = item.ntok;
+                meta[tNt] = nt;
+                meta[tKey0] = key0;
+                meta[tStop] = 0;
             }
             __syncwarp();
-            const uint32_t qfb = smem_u32(&q_full[qs]);
-            if (lane == 0) mbar_arrive_expect_tx(qfb, q_bytes);
+            const uint32_t qfb = smem_u32(&q_full);
+            // tile B only when it has tokens: a box wholly past the last query token is not copied
+            const int q_tiles = item.ntok > Th ? 2 : 1;
+            if (lane == 0) mbar_arrive_expect_tx(qfb, q_bytes / 2 * q_tiles);
             __syncwarp();
-            if (lane < Gm::CB)
-                tma_load_3d(q_base + qs * Gm::QBYTES + lane * (kM * 128), &qmap, qfb, lane * 64, item.head * G,
-                            q_start + item.tok0);
-            if (++qs == 2) {
-                qs = 0;
-                qph ^= 1u;
+            if (lane < q_tiles * Gm::CB) {
+                const int tile = lane / Gm::CB, cb = lane % Gm::CB;
+                tma_load_3d(q_base + tile * Gm::QTILE + cb * (kM * 128), &qmap, qfb, cb * 64, item.head * G,
+                            q_start + item.tok0 + tile * Th);
             }
+            qph ^= 1u;
             int win0 = key0 / ps;
             int win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
             for (int t = 0; t < nt && ok; ++t) {
@@ -228,108 +232,127 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
             if (!ok) break;
             it = __shfl_sync(0xffffffffu, nxt, 0);
         }
-        (void)ok;
-    } else if (warp == 5) {
+    } else if (warp == kMma) {
         // =============================== MMA issuer ===============================
         if (lane == 0) {
             constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kBN, 0, 0);
             constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
-            int qs = 0, s = 0;
+            int s = 0;
             uint32_t qph = 0, ph = 0;
-            uint32_t g = 0;        // tiles issued so far (all items): S buffer g & 1
-            uint32_t items = 0;    // items finished
+            uint32_t j_all = 0;   // key tiles issued so far (all items): phase of s_full / p_full / pv_done
+            uint32_t items = 0;   // items finished
             bool ok = true;
-            // PV of tile gg (stage ss) of the current item; first = first tile of the item
-            auto issue_pv = [&](uint32_t gg, int ss, bool first) -> bool {
-                const int b = gg & 1;
-                if (!mbar_wait(smem_u32(&p_full[b]), (gg >> 1) & 1u, ctrl, tmo)) return false;
-                if (first && items > 0 && !mbar_wait(smem_u32(&o_free), (items - 1) & 1u, ctrl, tmo)) return false;
+            auto issue_qk = [&](int x, int ss) {
+                const uint32_t qsl = q_base + x * Gm::QTILE;
+                const uint32_t kst = kv_base + ss * Gm::STAGE;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t qoff = (uint32_t)((kk >> 2) * (kM * 128) + (kk & 3) * 32);
+                    const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
+                    umma_ss(tmem + Gm::TM_S(x), umma_sdesc(qsl + qoff, 16, 1024), umma_sdesc(kst + koff, 16, 1024),
+                            idesc_qk, kk > 0 ? 1 : 0);
+                }
+                umma_commit(smem_u32(&s_full[x]));
+            };
+            auto issue_pv = [&](int x, int ss, uint32_t jj, bool first) -> bool {
+                if (!mbar_wait(smem_u32(&p_full[x]), jj & 1u, ctrl, tmo)) return false;
                 tc_fence_after();
                 const uint32_t vst = kv_base + ss * Gm::STAGE + Gm::KBYTES;
 #pragma unroll
                 for (int kk = 0; kk < kBN / 16; ++kk) {
                     const uint64_t bdesc = umma_sdesc(vst + kk * 16 * 128, kBN * 128, 1024);
-                    umma_ts(tmem + Gm::TM_O, tmem + (b ? Gm::TM_S1 : Gm::TM_S0) + kk * 8, bdesc, idesc_pv,
+                    umma_ts(tmem + Gm::TM_O(x), tmem + Gm::TM_S(x) + kk * 8, bdesc, idesc_pv,
                             (!first || kk > 0) ? 1 : 0);
                 }
-                umma_commit(smem_u32(&kv_empty[ss]));
-                umma_commit(smem_u32(&pv_done));
+                umma_commit(smem_u32(&pv_done[x]));
                 return true;
             };
             for (;;) {
-                if (!mbar_wait(smem_u32(&q_full[qs]), qph, ctrl, tmo)) break;
-                if (meta[qs][tStop]) break;
-                const int nt = meta[qs][tNt];
+                if (!mbar_wait(smem_u32(&q_full), qph, ctrl, tmo)) break;
+                if (meta[tStop]) break;
+                const int nt = meta[tNt];
+                qph ^= 1u;
                 tc_fence_after();
-                const uint32_t qsl = q_base + qs * Gm::QBYTES;
-                int prev_s = 0;
-                for (int t = 0; t < nt && ok; ++t) {
-                    if (!mbar_wait(smem_u32(&kv_full[s]), ph, ctrl, tmo)) {
+                if (!mbar_wait(smem_u32(&kv_full[s]), ph, ctrl, tmo)) break;
+                tc_fence_after();
+                issue_qk(0, s);
+                issue_qk(1, s);
+                if (nt == 1) umma_commit(smem_u32(&q_empty));
+                for (int t = 0; t < nt; ++t) {
+                    const uint32_t jj = j_all + t;
+                    const int cur = s;
+                    int nxt_s = s + 1;
+                    uint32_t nxt_ph = ph;
+                    if (nxt_s == kNS) {
+                        nxt_s = 0;
+                        nxt_ph ^= 1u;
+                    }
+                    const bool more = t + 1 < nt;
+                    // O_A / O_B are overwritten by this item's first PV: the previous epilogue must be done
+                    if (t == 0 && items > 0 && !mbar_wait(smem_u32(&o_free), (items - 1) & 1u, ctrl, tmo)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const int b = g & 1;
-                    const uint32_t kst = kv_base + s * Gm::STAGE;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)((kk >> 2) * (kM * 128) + (kk & 3) * 32);
-                        const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
-                        umma_ss(tmem + (b ? Gm::TM_S1 : Gm::TM_S0), umma_sdesc(qsl + off, 16, 1024),
-                                umma_sdesc(kst + koff, 16, 1024), idesc_qk, kk > 0 ? 1 : 0);
-                    }
-                    umma_commit(smem_u32(&s_full[b]));
-                    if (t == nt - 1) umma_commit(smem_u32(&q_empty[qs]));
-                    if (t > 0 && !issue_pv(g - 1, prev_s, t == 1)) {
+                    if (!issue_pv(0, cur, jj, t == 0)) {
                         ok = false;
                         break;
                     }
-                    prev_s = s;
-                    ++g;
-                    if (++s == kNS) {
-                        s = 0;
-                        ph ^= 1u;
+                    if (more) {
+                        if (!mbar_wait(smem_u32(&kv_full[nxt_s]), nxt_ph, ctrl, tmo)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_qk(0, nxt_s);
                     }
+                    if (!issue_pv(1, cur, jj, t == 0)) {
+                        ok = false;
+                        break;
+                    }
+                    umma_commit(smem_u32(&kv_empty[cur]));
+                    if (more) {
+                        issue_qk(1, nxt_s);
+                        if (t + 2 == nt) umma_commit(smem_u32(&q_empty));
+                    }
+                    s = nxt_s;
+                    ph = nxt_ph;
                 }
-                if (!ok || !issue_pv(g - 1, prev_s, nt == 1)) break;
+                if (!ok) break;
+                j_all += nt;
                 umma_commit(smem_u32(&o_full));
                 ++items;
-                if (++qs == 2) {
-                    qs = 0;
-                    qph ^= 1u;
-                }
             }
         }
         __syncwarp();
     } else {
-        // =============================== softmax warps ===============================
-        const int r = tid;  // TMEM lane == query row of the tile
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        const int G = a.G, Hq = a.Hq;
-        int qs = 0, s = 0;
+        // =============================== softmax warp groups ===============================
+        const int x = warp >> 2;           // 0: tile A, 1: tile B
+        const int r = tid & 127;           // TMEM lane == row of this tile
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const int G = a.G, Hq = a.Hq, Th = p.Tq / 2;
+        int s = 0;
         uint32_t qph = 0, ph = 0;
-        uint32_t g = 0, items = 0;
+        uint32_t j_all = 0, items = 0;
         for (;;) {
-            if (!mbar_wait(smem_u32(&q_full[qs]), qph, ctrl, tmo)) break;
-            const int* mm = meta[qs];
-            const int stop = mm[tStop];
-            const int head = mm[tHead], q_start = mm[tQStart], ql = mm[tQl], kl = mm[tKl];
-            const int kv_begin = mm[tKvBegin], kv_end = mm[tKvEnd], tok0 = mm[tTok0], ntok = mm[tNtok];
-            const int nt = mm[tNt], key0 = mm[tKey0];
+            if (!mbar_wait(smem_u32(&q_full), qph, ctrl, tmo)) break;
+            const int stop = meta[tStop];
+            const int head = meta[tHead], q_start = meta[tQStart], ql = meta[tQl], kl = meta[tKl];
+            const int kv_begin = meta[tKvBegin], kv_end = meta[tKvEnd], tok0 = meta[tTok0];
+            const int ntok = meta[tNtok], nt = meta[tNt], key0 = meta[tKey0];
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&meta_free[qs]));
+            if (lane == 0) mbar_arrive(smem_u32(&meta_free));
             if (stop) break;
-            if (++qs == 2) {
-                qs = 0;
-                qph ^= 1u;
-            }
-            const int pos = kl - ql + tok0 + r / G;  // key position of this row
-            const int pos_lo = kl - ql + tok0, pos_hi = kl - ql + tok0 + ntok - 1;
+            qph ^= 1u;
+            // this tile's tokens: [tok0 + x*Th, tok0 + x*Th + ntx)
+            const int ttok0 = tok0 + x * Th;
+            const int ntx = max(0, min(Th, ntok - x * Th));
+            const int pos = kl - ql + ttok0 + r / G;  // key position of this row
+            const int pos_lo = kl - ql + ttok0, pos_hi = kl - ql + ttok0 + max(ntx, 1) - 1;
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             for (int t = 0; t < nt; ++t) {
-                const int b = g & 1;
-                if (!mbar_wait(smem_u32(&s_full[b]), (g >> 1) & 1u, ctrl, tmo)) {
+                const uint32_t jj = j_all + t;
+                if (!mbar_wait(smem_u32(&s_full[x]), jj & 1u, ctrl, tmo)) {
                     ok = false;
                     break;
                 }
@@ -338,69 +361,81 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 const bool partial = k_lo < kv_begin || k_lo + kBN > kv_end;
                 const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
                                        (a.has_window && k_lo <= pos_hi - a.window);
-                const uint32_t scol = b ? Gm::TM_S1 : Gm::TM_S0;
-                float x[kBN];
-#pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) tmem_ld32(lane_addr + scol + c * 32, reinterpret_cast<uint32_t*>(x) + c * 32);
-                tmem_ld_wait();
+                const uint32_t scol = Gm::TM_S(x);
+                // pass 1: row max of the transformed logits; masked or capped values are
+                // written back to TMEM so that pass 2 only exponentiates
+                const bool rewrite = need_mask || a.has_cap;
                 float mt = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < kBN; ++i) {
-                    float v = x[i];
-                    if (a.has_cap) {
-                        const float e = ex2(v * a.cap_exp);
-                        v = a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + e);
-                    } else {
-                        v *= a.qk_log2;
-                    }
-                    if (need_mask) {
-                        const int j = k_lo + i;
-                        const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos) &&
-                                         (!a.has_window || j > pos - a.window);
-                        v = okk ? v : -INFINITY;
-                    }
-                    x[i] = v;
-                    mt = fmaxf(mt, v);
-                }
-                const bool need = mt > m_run + kRescaleLog2;  // false when mt == -inf
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = fmaxf(m_run, mt);
-                    const float alpha = m_run == -INFINITY ? 0.f : ex2(m_run - m_new);
-                    if (t > 0) {
-                        // O holds this item's PVs up to tile g-1: wait for it, then scale in place
-                        if (!mbar_wait(smem_u32(&pv_done), (g - 1) & 1u, ctrl, tmo)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
 #pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
-                            uint32_t ov[32];
-                            tmem_ld32(lane_addr + Gm::TM_O + c * 32, ov);
-                            tmem_ld_wait();
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t sv[32];
+                    tmem_ld32(lane_addr + scol + c * 32, sv);
+                    tmem_ld_wait();
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                            tmem_st32(lane_addr + Gm::TM_O + c * 32, ov);
+                    for (int i = 0; i < 32; ++i) {
+                        float v = __uint_as_float(sv[i]);
+                        if (a.has_cap) {
+                            const float e = ex2(v * a.cap_exp);
+                            v = a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + e);
+                        } else {
+                            v *= a.qk_log2;
                         }
-                        tmem_st_wait();
+                        if (need_mask) {
+                            const int j = k_lo + c * 32 + i;
+                            const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos) &&
+                                             (!a.has_window || j > pos - a.window);
+                            v = okk ? v : -INFINITY;
+                        }
+                        mt = fmaxf(mt, v);
+                        sv[i] = __float_as_uint(v);
                     }
-                    l_run *= alpha;
-                    m_run = m_new;
+                    if (rewrite) tmem_st32(lane_addr + scol + c * 32, sv);
                 }
-                const float base = m_run == -INFINITY ? 0.f : m_run;
-                uint32_t pk[kBN / 2];
+                if (rewrite) tmem_st_wait();
+                // lazy rescale: move the running max only when it grows by more than 2^8
+                const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);  // false if mt == -inf
+                const float m_new = need ? fmaxf(m_run, mt) : m_run;
+                const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
+                const float base = m_new == -INFINITY ? 0.f : m_new;
+                // pass 2: p = 2^(x - base) in bf16 over the consumed S columns (P[i] at column i/2)
+                const float mul = rewrite ? 1.f : a.qk_log2;
+                float lsum = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t sv[32], pk[16];
+                    tmem_ld32(lane_addr + scol + c * 32, sv);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < kBN / 2; ++i) {
-                    const float p0 = ex2(x[2 * i] - base);
-                    const float p1 = ex2(x[2 * i + 1] - base);
-                    l_run += p0 + p1;
-                    pk[i] = pack2<false>(p0, p1);
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), mul, -base));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), mul, -base));
+                        lsum += p0 + p1;
+                        pk[i] = pack2<false>(p0, p1);
+                    }
+                    tmem_st16(lane_addr + scol + c * 16, pk);
                 }
+                l_run = l_run * alpha + lsum;
+                m_run = m_new;
+                if (need && t > 0) {
+                    // O holds this item's PVs up to tile t-1: wait for them, then scale in place
+                    if (!mbar_wait(smem_u32(&pv_done[x]), (jj - 1) & 1u, ctrl, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_addr + Gm::TM_O(x) + c * 32, ov);
+                        tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < kBN / 64; ++c) tmem_st32(lane_addr + scol + c * 32, pk + c * 32);
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(lane_addr + Gm::TM_O(x) + c * 32, ov);
+                    }
+                }
                 tmem_st_wait();
-                if (partial) {
-                    // zero the V rows of keys outside [kv_begin, kv_end) once this stage has landed
+                if (partial && x == 0) {
+                    // zero the V rows of keys outside [kv_begin, kv_end) once the stage has landed
                     if (!mbar_wait(smem_u32(&kv_full[s]), ph, ctrl, tmo)) {
                         ok = false;
                         break;
@@ -417,26 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&p_full[b]));
-                ++g;
+                if (lane == 0) mbar_arrive(smem_u32(&p_full[x]));
                 if (++s == kNS) {
                     s = 0;
                     ph ^= 1u;
                 }
             }
             if (!ok) break;
+            j_all += nt;
             // ---- epilogue: o = O * v_scale / l
             if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
             tc_fence_after();
-            const int rows_used = ntok * G;
+            const int rows_used = ntx * G;
             const float inv = l_run > 0.f ? a.v_scale / l_run : 0.f;
-            const int t_tok = q_start + tok0 + r / G;
+            const int t_tok = q_start + ttok0 + r / G;
             const int qh = head * G + r % G;
             uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
-                tmem_ld32(lane_addr + Gm::TM_O + c * 32, ov);
+                tmem_ld32(lane_addr + Gm::TM_O(x) + c * 32, ov);
                 tmem_ld_wait();
                 if (r < rows_used) {
 #pragma unroll
@@ -458,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kMma) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }

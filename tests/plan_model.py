@@ -2,10 +2,10 @@
 
 Written from the planner's stated rules, not from its code: decode-class
 sequences (q_len * G <= decode rows) are cut into key pieces of `chunk` keys,
-prefill-class sequences into query tiles of pf_rows // G tokens; each unit's
-key range is the band its rows can see; units are ordered decode first, then
-by cost (keys) descending, ties by unit index; each unit yields one item per
-kv head.
+prefill-class sequences into query tiles of pf_tokens tokens; each unit's
+key range is the band its rows can see; units are ordered decode first (by
+cost descending), then prefill (by sequence, then cost descending), ties by
+unit index; each unit yields one item per kv head.
 """
 import numpy as np
 
@@ -18,11 +18,11 @@ def band(kl, ql, i0, i1, causal, window):
     return lo, max(hi, lo)
 
 
-def plan(prob, dec_slots, dec_rows=16, pf_rows=64, waves=4, min_chunk=512, align=64,
+def plan(prob, dec_slots, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, align=64,
          max_sort=16384):
     Hkv = prob.num_kv_heads
     G = prob.num_q_heads // Hkv
-    Tq = max(1, pf_rows // G)
+    Tq = max(1, pf_tokens if pf_tokens is not None else 64 // G)
     S = prob.num_seqs
     cu = prob.cu_q_lens.astype(np.int64)
     kvl = prob.kv_lens.astype(np.int64)
@@ -74,13 +74,16 @@ def plan(prob, dec_slots, dec_rows=16, pf_rows=64, waves=4, min_chunk=512, align
             units.append((1, hi - lo, [s, t0, nt, lo, hi, -1, 0, 1]))
     n = len(units)
     order = list(range(n))
-    if n <= max_sort:
-        order.sort(key=lambda u: (units[u][0], 0x7FFFFFFF - units[u][1], u))
+    if n <= max_sort and S < 65536:
+        def key(u):
+            c, cost, d = units[u]
+            return (0, 0x7FFFFFFF - cost, 0, u) if c == 0 else (1, d[0], 0x7FFFFFFF - cost, u)
+        order.sort(key=key)
     dec, pf = [], []
     for u in order:
         c, _, d = units[u]
         for h in range(Hkv):
             item = [d[0], h, d[1], d[2], d[3], d[4], d[5] + h * d[7] + d[6] if d[5] >= 0 else -1, d[6]]
             (dec if c == 0 else pf).append(item)
-    return dict(status=0, chunk=chunk, sorted=int(n <= max_sort), n_units=n, n_part=part,
+    return dict(status=0, chunk=chunk, sorted=int(n <= max_sort and S < 65536), n_units=n, n_part=part,
                 dec=np.array(dec, np.int32).reshape(-1, 8), pf=np.array(pf, np.int32).reshape(-1, 8))

@@ -104,7 +104,7 @@ def test_planner_matches_python_rederivation():
         att = RaggedPagedAttention(**p.cfg_dict())
         att.forward(*to_dev(p), p.num_seqs)
         info, items = att.plan()
-        ref = plan(p, int(info[10]), pf_rows=int(info[6]))
+        ref = plan(p, int(info[10]), pf_tokens=int(info[6]))
         assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
         assert info[9] == ref["sorted"] and info[7] == ref["n_part"]
         assert np.array_equal(items[: info[1]], ref["dec"])

@@ -366,32 +366,41 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 // written back to TMEM so that pass 2 only exponentiates
                 const bool rewrite = need_mask || a.has_cap;
                 float mt = -INFINITY;
+                if (!rewrite) {
+                    // interior tile, no cap: the max of the scaled logits (four independent chains)
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t sv[32];
-                    tmem_ld32(lane_addr + scol + c * 32, sv);
-                    tmem_ld_wait();
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(lane_addr + scol + c * 32, sv);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float v = __uint_as_float(sv[i]);
-                        if (a.has_cap) {
-                            const float e = ex2(v * a.cap_exp);
-                            v = a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + e);
-                        } else {
-                            v *= a.qk_log2;
-                        }
-                        if (need_mask) {
+                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sv[i]) * a.qk_log2);
+                    }
+                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                } else {
+                    const bool cap = a.has_cap;
+#pragma unroll 1
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(lane_addr + scol + c * 32, sv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float v = __uint_as_float(sv[i]);
+                            v = cap ? a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + ex2(v * a.cap_exp))
+                                    : v * a.qk_log2;
                             const int j = k_lo + c * 32 + i;
                             const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos) &&
                                              (!a.has_window || j > pos - a.window);
-                            v = okk ? v : -INFINITY;
+                            v = (okk || !need_mask) ? v : -INFINITY;
+                            mt = fmaxf(mt, v);
+                            sv[i] = __float_as_uint(v);
                         }
-                        mt = fmaxf(mt, v);
-                        sv[i] = __float_as_uint(v);
+                        tmem_st32(lane_addr + scol + c * 32, sv);
                     }
-                    if (rewrite) tmem_st32(lane_addr + scol + c * 32, sv);
+                    tmem_st_wait();
                 }
-                if (rewrite) tmem_st_wait();
                 // lazy rescale: move the running max only when it grows by more than 2^8
                 const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);  // false if mt == -inf
                 const float m_new = need ? fmaxf(m_run, mt) : m_run;
@@ -399,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 const float base = m_new == -INFINITY ? 0.f : m_new;
                 // pass 2: p = 2^(x - base) in bf16 over the consumed S columns (P[i] at column i/2)
                 const float mul = rewrite ? 1.f : a.qk_log2;
-                float lsum = 0.f;
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t sv[32], pk[16];
@@ -409,11 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                     for (int i = 0; i < 16; ++i) {
                         const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), mul, -base));
                         const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), mul, -base));
-                        lsum += p0 + p1;
+                        ls4[i & 3] += p0 + p1;
                         pk[i] = pack2<false>(p0, p1);
                     }
                     tmem_st16(lane_addr + scol + c * 16, pk);
                 }
+                const float lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
                 l_run = l_run * alpha + lsum;
                 m_run = m_new;
                 if (need && t > 0) {

@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=list(ri.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--all", action="store_true",
+                    help="one line per workload (tiny excluded), no CPU baseline or e2e")
     return ap.parse_args()
 
 
@@ -289,20 +291,31 @@ def main():
     tokens = work["q_tokens"]
     value = tokens * K * world / (ms_total / 1e3)
 
-    # dominant kernel and its roofline
+    # per-kernel roofline: each attention kernel is charged with its own sequences' work,
+    # bound by whichever of HBM bytes / tensor FLOPs takes longer at peak
     hbm, tf_burst, tf_sust, src = peaks()
     mean_k = kern.mean(axis=0)
-    dom = int(np.argmax(mean_k))
-    dom_name = KERNEL_NAMES[dom]
-    if dom_name == "prefill_attention":
-        bound, achieved, peak, unit = "tensor", work["flops"] / (mean_k[dom] * 1e-3) / 1e12, tf_burst, "TFLOP/s"
-    else:
-        bound, achieved, peak, unit = "hbm", work["bytes"] / (mean_k[dom] * 1e-3) / 1e9, hbm, "GB/s"
-    traffic = recorded_traffic(dom_name, args.workload)
-    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-            "traffic": traffic, "kernel": dom_name, "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
-            "kernel_ms": float(mean_k[dom]),
-            "algorithmic": {"bytes": work["bytes"], "flops": work["flops"]}}
+
+    def kernel_roof(name, ms):
+        w = work["decode" if name == "decode_attention" else "prefill"]
+        t_hbm = w["bytes"] / (hbm * 1e9)
+        t_tc = w["flops"] / (tf_burst * 1e12)
+        if t_tc > t_hbm:
+            bound, achieved, peak, unit, key = "tensor", w["flops"] / (ms * 1e-3) / 1e12, tf_burst, "TFLOP/s", "bf16_tflops"
+        else:
+            bound, achieved, peak, unit, key = "hbm", w["bytes"] / (ms * 1e-3) / 1e9, hbm, "GB/s", "hbm_gbs"
+        return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": recorded_traffic(name, args.workload), "kernel": name,
+                "peak_source": f"{src} ({key})", "kernel_ms": float(ms),
+                "algorithmic": {"bytes": w["bytes"], "flops": w["flops"]}}
+
+    attn = [i for i, n in enumerate(KERNEL_NAMES) if n.endswith("_attention")]
+    dom = max(attn, key=lambda i: mean_k[i])
+    roof = kernel_roof(KERNEL_NAMES[dom], mean_k[dom])
+    kroofs = {KERNEL_NAMES[i]: kernel_roof(KERNEL_NAMES[i], mean_k[i]) for i in attn
+              if work["decode" if KERNEL_NAMES[i] == "decode_attention" else "prefill"]["bytes"] > 0}
+    # the whole step against the combined roofline time max(bytes / BW, FLOPs / peak)
+    t_star = max(work["bytes"] / (hbm * 1e9), work["flops"] / (tf_burst * 1e12))
 
     # end to end through the public host-buffer entry point
     e2e = None
@@ -352,6 +365,8 @@ def main():
                        "ranks": world},
             "step_hbm_gbs": work["bytes"] / (ms_step * 1e-3) / 1e9,
             "step_tflops": work["flops"] / (ms_step * 1e-3) / 1e12,
+            "step_roofline_frac": t_star / (ms_step * 1e-3),
+            "kernel_rooflines": kroofs,
             "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 4 * K, "clocks": clk,
@@ -363,4 +378,11 @@ def main():
 
 
 if __name__ == "__main__":
-    main()
+    a0 = parse()
+    if a0.all and a0.impl == "ours":
+        for w in ("decode", "mixed", "fp8_window", "long_prefill"):
+            sys.argv = [sys.argv[0], "--workload", w, "--steps", str(a0.steps), "--warmup",
+                        str(a0.warmup), "--no-cpu-baseline", "--e2e-steps", "0"]
+            main()
+    else:
+        main()

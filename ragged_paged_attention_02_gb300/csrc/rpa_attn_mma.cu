@@ -72,6 +72,9 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wm = warp % WM, wn = warp / WM;
+    pdl_trigger();
+    pdl_wait();  // the planner's items are complete from here on
+    if ((int)blockIdx.x >= p.ctrl[kPfCtas]) return;  // SMs left to the decode kernel
     const int n_items = p.ctrl[p.item_count_word];
     const int G = p.G, Hq = p.Hq, ps = p.ps;
     const size_t kv_slot_stride = (size_t)2 * p.Hkv * D * kKvElt;
@@ -412,8 +415,7 @@ struct Kern {
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, C::kThreads, C::kSmem);
     }
     static cudaError_t launch(const AttnParams& p, const Launch& l) {
-        fn<<<l.grid, C::kThreads, C::kSmem, l.stream>>>(p);
-        return cudaGetLastError();
+        return launch_pdl(fn, l.grid, C::kThreads, C::kSmem, l.stream, p);
     }
 };
 

@@ -18,6 +18,7 @@ namespace rpa {
 namespace {
 
 __global__ void __launch_bounds__(256) rpa_combine_kernel(const CombParams p) {
+    pdl_wait();  // the attention kernels' partials are complete from here on
     const int n_comb = p.ctrl[kNumComb];
     const int D = p.D, G = p.G, Hq = p.Hq;
     for (int e = blockIdx.x; e < n_comb; e += gridDim.x) {
@@ -67,8 +68,7 @@ __global__ void __launch_bounds__(256) rpa_combine_kernel(const CombParams p) {
 }  // namespace
 
 cudaError_t launch_combine(const CombParams& p, const Launch& l) {
-    rpa_combine_kernel<<<l.grid, 256, 0, l.stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(rpa_combine_kernel, l.grid, 256, 0, l.stream, p);
 }
 
 }  // namespace rpa

@@ -82,7 +82,6 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
     const AttnParams& a = p.a;
     int* ctrl = a.ctrl;
     const uint64_t tmo = p.timeout_ns;
-    const int n_items = a.ctrl[a.item_count_word];
     // 1 KiB-aligned base: the 128-byte swizzle pattern follows address bits 7..9
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t smem0 = smem_u32(smem);
@@ -96,6 +95,10 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_trigger();
+    pdl_wait();  // the planner's items are complete from here on
+    if ((int)blockIdx.x >= a.ctrl[kDecCtas]) return;  // SMs left to the prefill kernel
+    const int n_items = a.ctrl[a.item_count_word];
 
     if (warp == kCW) {
         // =============================== producer ===============================
@@ -518,8 +521,7 @@ struct DecKern {
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p,
                               const Launch& l) {
-        rpa_decode_attn<D, FP8><<<l.grid, kDecThreads, Gm::SMEM, l.stream>>>(kvm, qm, p);
-        return cudaGetLastError();
+        return launch_pdl(rpa_decode_attn<D, FP8>, l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 

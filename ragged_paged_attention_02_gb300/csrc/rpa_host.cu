@@ -53,6 +53,11 @@ struct RpaHandle {
     cudaEvent_t* prof_ev;   // [prof_cap][5]
     int prof_cap;
     int prof_used;
+    // decode and prefill run concurrently: decode on a second stream forked after the planner
+    int concurrent;
+    cudaStream_t side;
+    cudaEvent_t ev_plan, ev_dec;
+    int force_pf_sms, force_dec_sms;  // tuning hooks (environment, read at rpa_create)
 };
 
 namespace {
@@ -197,6 +202,13 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
         const char* t = getenv("RPA_DEBUG_TIMEOUT_MS");
         const long long ms = t ? atoll(t) : 1000;
         h->timeout_ns = (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
+        // tuning hooks: run decode and prefill one after the other, or fix the SM split
+        const char* ser = getenv("RPA_SERIAL");
+        h->concurrent = (ser && ser[0] == '1') ? 0 : 1;
+        const char* fp = getenv("RPA_DEBUG_PF_SMS");
+        h->force_pf_sms = fp ? atoi(fp) : 0;
+        const char* fd = getenv("RPA_DEBUG_DEC_SMS");
+        h->force_dec_sms = fd ? atoi(fd) : 0;
     }
 
     {
@@ -245,6 +257,16 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     h->ws_bytes = off;
     if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
+        delete h;
+        return RPA_ERR_CUDA;
+    }
+    if (h->concurrent && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+                          cudaEventCreateWithFlags(&h->ev_plan, cudaEventDisableTiming) != cudaSuccess ||
+                          cudaEventCreateWithFlags(&h->ev_dec, cudaEventDisableTiming) != cudaSuccess)) {
+        cudaGetLastError();
+        if (h->ev_plan) cudaEventDestroy(h->ev_plan);
+        if (h->side) cudaStreamDestroy(h->side);
+        cudaFree(h->ws);
         delete h;
         return RPA_ERR_CUDA;
     }
@@ -297,6 +319,18 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.dec_rows = kDecRows;
     pp.pf_tokens = h->pf_tokens;
     pp.dec_slots = h->sms * h->dec_bps;
+    pp.concurrent = h->concurrent;
+    pp.n_sms = h->sms;
+    pp.dec_bps = h->dec_bps;
+    pp.pf_bps = h->pf_bps;
+    pp.pf_mma_rows = h->tc ? 2 * kTcRows : kPfRows;
+    pp.D = h->D;
+    pp.kv_elt = h->fp8 ? 1 : 2;
+    pp.pf_sm_gflops = h->tc ? kPfSmGflopsTc : kPfSmGflopsMma;
+    pp.dec_sm_gbs = kDecSmGBs;
+    pp.hbm_gbs = kHbmGBs;
+    pp.force_pf_sms = h->force_pf_sms;
+    pp.force_dec_sms = h->force_dec_sms;
     pp.max_units = h->max_units;
     pp.max_dec_units = h->max_dec_units;
     pp.max_pf_units = h->max_pf_units;
@@ -342,6 +376,12 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     ap.part_o = h->part_o;
     ap.part_ml = h->part_ml;
 
+    cudaStream_t dst = st;  // stream of the decode kernel
+    if (h->concurrent) {
+        if (cudaEventRecord(h->ev_plan, st) != cudaSuccess || cudaStreamWaitEvent(h->side, h->ev_plan, 0) != cudaSuccess)
+            return RPA_ERR_CUDA;
+        dst = h->side;
+    }
     if (c.num_q_tokens > 0) {
         if (h->kvmap_ptr != kv_pages) {
             if (encode_kv_map(&h->kvmap, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
@@ -366,10 +406,11 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
         dp.Tt = h->Tt;
         dp.debug_stall = h->debug_stall;
         dp.timeout_ns = h->timeout_ns;
-        if (launch_decode_tma(h->kvmap, h->qmap, dp, h->fp8, Launch{h->sms * h->dec_bps, st}) != cudaSuccess)
+        if (launch_decode_tma(h->kvmap, h->qmap, dp, h->fp8, Launch{h->sms * h->dec_bps, dst}) != cudaSuccess)
             return RPA_ERR_CUDA;
     }
-    if (ev[2] && cudaEventRecord(ev[2], st) != cudaSuccess) return RPA_ERR_CUDA;
+    if (ev[2] && cudaEventRecord(ev[2], dst) != cudaSuccess) return RPA_ERR_CUDA;
+    if (h->concurrent && cudaEventRecord(h->ev_dec, dst) != cudaSuccess) return RPA_ERR_CUDA;
 
     if (c.num_q_tokens > 0) {
         ap.items = h->pf_items;
@@ -388,6 +429,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
         }
     }
     if (ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return RPA_ERR_CUDA;
+    if (h->concurrent && cudaStreamWaitEvent(st, h->ev_dec, 0) != cudaSuccess) return RPA_ERR_CUDA;
 
     CombParams cp;
     cp.o = static_cast<uint8_t*>(o);
@@ -436,9 +478,13 @@ int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_call
     const int n = h->prof_used < max_calls ? h->prof_used : max_calls;
     for (int c = 0; c < n; ++c) {
         if (cudaEventSynchronize(h->prof_ev[c * 5 + 4]) != cudaSuccess) return RPA_ERR_CUDA;
+        // events: 0 start, 1 planner done, 2 decode done, 3 prefill done, 4 combine done;
+        // with concurrent decode / prefill both are timed from the planner's end
+        static const int from_ser[4] = {0, 1, 2, 3}, from_con[4] = {0, 1, 1, 3};
+        const int* from = h->concurrent ? from_con : from_ser;
         for (int k = 0; k < 4; ++k) {
             float t = 0.f;
-            if (cudaEventElapsedTime(&t, h->prof_ev[c * 5 + k], h->prof_ev[c * 5 + k + 1]) != cudaSuccess)
+            if (cudaEventElapsedTime(&t, h->prof_ev[c * 5 + from[k]], h->prof_ev[c * 5 + k + 1]) != cudaSuccess)
                 return RPA_ERR_CUDA;
             ms[c * 4 + k] = t;
         }
@@ -518,7 +564,12 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[7] = ctrl[kNumPart];
     info[8] = ctrl[kNumUnits];
     info[9] = ctrl[kSorted];
-    info[10] = h->sms * h->dec_bps;
+    info[10] = ctrl[kDecCtas];
+    info[11] = ctrl[kPfCtas];
+    info[12] = h->sms;
+    info[13] = h->dec_bps;
+    info[14] = h->pf_bps;
+    info[15] = h->concurrent;
     if (items && max_items > 0) {
         const int64_t nd = ctrl[kNumDecItems] < max_items ? ctrl[kNumDecItems] : max_items;
         const int64_t np = ctrl[kNumPfItems] < max_items - nd ? ctrl[kNumPfItems] : max_items - nd;
@@ -533,6 +584,9 @@ void rpa_destroy(RpaHandle* h) {
     if (!h) return;
     DeviceGuard g(h->device);
     prof_free(h);
+    if (h->ev_dec) cudaEventDestroy(h->ev_dec);
+    if (h->ev_plan) cudaEventDestroy(h->ev_plan);
+    if (h->side) cudaStreamDestroy(h->side);
     if (h->stage) cudaFree(h->stage);
     if (h->ws) cudaFree(h->ws);
     delete h;

@@ -27,6 +27,8 @@ enum Ctrl : int {
     kSorted = 9,
     kCovLo = 10,   // first token covered by a sequence
     kCovHi = 11,   // end of covered tokens
+    kPfCtas = 12,  // prefill CTAs that take work (the rest exit at once)
+    kDecCtas = 13, // decode CTAs that take work
     kCtrlWords = 32,
 };
 
@@ -46,8 +48,15 @@ constexpr int kPfRows = 64;        // rows of a prefill tile (4 warps x 16)
 constexpr int kDecWaves = 4;       // target decode items per resident CTA
 constexpr int kMinChunk = 512;     // smallest split-KV piece (keys)
 constexpr int kChunkAlign = 64;    // pieces are multiples of this many keys
-constexpr int kMaxSort = 16384;    // units sorted by cost on the device
+constexpr int kMaxSort = 8192;     // units sorted by cost on the device
+constexpr int kSeqSmem = 4096;     // sequences whose plan scratch fits in shared memory
 constexpr int kPlanThreads = 1024;
+// rates of the SM-split model (planner): FLOP/ns of one SM on prefill, B/ns one SM can
+// stream in the decode kernel, and HBM B/ns
+constexpr int kPfSmGflopsTc = 7600;
+constexpr int kPfSmGflopsMma = 800;
+constexpr int kDecSmGBs = 70;
+constexpr int kHbmGBs = 6700;
 
 struct PlanParams {
     const int* kv_lens;
@@ -60,7 +69,17 @@ struct PlanParams {
     int causal, has_window, window;
     int dec_rows;    // rows of a decode tile
     int pf_tokens;   // query tokens of a prefill tile
-    int dec_slots;   // resident decode CTAs
+    int dec_slots;   // resident decode CTAs (all SMs)
+    // SM split between the decode and prefill kernels when they run concurrently
+    int concurrent;      // 1: the two kernels run at the same time on disjoint SMs
+    int n_sms, dec_bps, pf_bps;  // SMs, resident CTAs per SM of each kernel
+    int pf_mma_rows;     // MMA rows per prefill unit (tile padding included)
+    int D, kv_elt;
+    int pf_sm_gflops;    // prefill FLOP rate of one SM (FLOP/ns)
+    int dec_sm_gbs;      // decode bytes one SM can stream (B/ns)
+    int hbm_gbs;         // HBM bandwidth (B/ns)
+    int force_pf_sms;    // > 0: tuning hook, prefill SMs when both classes have work
+    int force_dec_sms;   // > 0: tuning hook, decode SMs
     int max_units;   // capacity of the unit arrays
     int max_dec_units, max_pf_units;  // capacities of the two item lists (in units)
     int max_part;    // capacity of partial slots
@@ -127,6 +146,21 @@ struct Launch {
     int grid;
     cudaStream_t stream;
 };
+// Launch with programmatic stream serialisation (the kernel calls pdl_wait()).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern k, int grid, int block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, args...);
+}
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
 cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l);
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
@@ -216,6 +250,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
     return r;
 }
+
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialisation attribute may start before its predecessor in the
+// stream ends; it must call pdl_wait() before touching anything the
+// predecessor writes.  pdl_trigger() lets the next kernel start early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 __device__ __forceinline__ void set_status(int* ctrl, int code) {
     atomicCAS(ctrl + kStatus, 0, code);

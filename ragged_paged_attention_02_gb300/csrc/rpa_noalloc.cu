@@ -162,6 +162,18 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     pp.dec_rows = kDecRows;
     pp.pf_tokens = pf_tokens;
     pp.dec_slots = (int)dec_slots;
+    pp.concurrent = 0;  // one stream: decode and prefill run one after the other on all SMs
+    pp.n_sms = sms;
+    pp.dec_bps = dec_bps;
+    pp.pf_bps = pf_bps;
+    pp.pf_mma_rows = tc ? 2 * kTcRows : kPfRows;
+    pp.D = D;
+    pp.kv_elt = fp8 ? 1 : 2;
+    pp.pf_sm_gflops = tc ? kPfSmGflopsTc : kPfSmGflopsMma;
+    pp.dec_sm_gbs = kDecSmGBs;
+    pp.hbm_gbs = kHbmGBs;
+    pp.force_pf_sms = 0;
+    pp.force_dec_sms = 0;
     pp.max_units = (int)max_units;
     pp.max_dec_units = (int)max_dec_units;
     pp.max_pf_units = (int)max_pf_units;

@@ -35,31 +35,51 @@ __device__ __forceinline__ void key_band(int kl, int ql, int i0, int i1, const P
     if (hi < lo) hi = lo;
 }
 
-// Exclusive scan of one int per thread over the whole block; *total gets the sum.
-__device__ int block_scan(int v, int* s_warp, int* total) {
+// Exclusive scan of four ints per thread over the whole block (one pass for
+// all four); *total gets the sums.  s_warp holds 33 int4.
+__device__ int4 block_scan4(int4 v, int4* s_warp, int4* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    int x = v;
+    int4 x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        int4 y;
+        y.x = __shfl_up_sync(0xffffffffu, x.x, o);
+        y.y = __shfl_up_sync(0xffffffffu, x.y, o);
+        y.z = __shfl_up_sync(0xffffffffu, x.z, o);
+        y.w = __shfl_up_sync(0xffffffffu, x.w, o);
+        if (lane >= o) {
+            x.x += y.x;
+            x.y += y.y;
+            x.z += y.z;
+            x.w += y.w;
+        }
     }
     if (lane == 31) s_warp[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        int w = lane < nwarps ? s_warp[lane] : 0;
-        int ww = w;
+        const int4 w = lane < nwarps ? s_warp[lane] : make_int4(0, 0, 0, 0);
+        int4 ww = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int y = __shfl_up_sync(0xffffffffu, ww, o);
-            if (lane >= o) ww += y;
+            int4 y;
+            y.x = __shfl_up_sync(0xffffffffu, ww.x, o);
+            y.y = __shfl_up_sync(0xffffffffu, ww.y, o);
+            y.z = __shfl_up_sync(0xffffffffu, ww.z, o);
+            y.w = __shfl_up_sync(0xffffffffu, ww.w, o);
+            if (lane >= o) {
+                ww.x += y.x;
+                ww.y += y.y;
+                ww.z += y.z;
+                ww.w += y.w;
+            }
         }
-        s_warp[lane] = ww - w;
+        s_warp[lane] = make_int4(ww.x - w.x, ww.y - w.y, ww.z - w.z, ww.w - w.w);
         if (lane == 31) s_warp[32] = ww;
     }
     __syncthreads();
-    const int r = x - v + s_warp[warp];
+    const int4 base = s_warp[warp];
+    const int4 r = make_int4(x.x - v.x + base.x, x.y - v.y + base.y, x.z - v.z + base.z, x.w - v.w + base.w);
     *total = s_warp[32];
     __syncthreads();
     return r;
@@ -77,25 +97,31 @@ __device__ __forceinline__ int upper_seq(const int* ends, int n, int u) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p) {
-    extern __shared__ unsigned long long s_keys[];  // kMaxSort
-    __shared__ int s_warp[33];
+    extern __shared__ __align__(16) unsigned long long s_keys[];  // kMaxSort keys, then sequence scratch
+    __shared__ int4 s_warp[33];
     __shared__ int s_bad;
     __shared__ unsigned long long s_total;
+    __shared__ unsigned long long s_pf_keys;  // sum over prefill units of the keys they visit
+    __shared__ int s_split[2];                // prefill CTAs, decode CTAs
     const int tid = threadIdx.x;
     const int S = p.num_seqs;
     int* ctrl = p.ctrl;
-    // per-sequence scratch: class, count, decode/prefill unit end, partial offset, combine offset
-    int* s_cls = p.seq_scratch;
-    int* s_cnt = s_cls + p.num_seqs + 1;
-    int* s_dend = s_cnt + p.num_seqs + 1;
-    int* s_pend = s_dend + p.num_seqs + 1;
-    int* s_part = s_pend + p.num_seqs + 1;
-    int* s_comb = s_part + p.num_seqs + 1;
+    pdl_trigger();  // the attention kernels may start their prologue now
+    // per-sequence scratch (shared memory when it fits): class, count, decode / prefill
+    // unit ends, partial offset, combine offset
+    int* seq_base = S <= kSeqSmem ? reinterpret_cast<int*>(s_keys + kMaxSort) : p.seq_scratch;
+    int* s_cls = seq_base;
+    int* s_cnt = s_cls + S + 1;
+    int* s_dend = s_cnt + S + 1;
+    int* s_pend = s_dend + S + 1;
+    int* s_part = s_pend + S + 1;
+    int* s_comb = s_part + S + 1;
     const int Tq = max(1, p.pf_tokens);  // query tokens per prefill tile
 
     if (tid == 0) {
         s_bad = 0;
         s_total = 0ull;
+        s_pf_keys = 0ull;
     }
     __syncthreads();
 
@@ -117,6 +143,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             } else {
                 cls = 2;
                 cnt = (ql + Tq - 1) / Tq;
+                unsigned long long keys = 0;
+                for (int k = 0; k < cnt; ++k) {
+                    int lo, hi;
+                    key_band(kl, ql, k * Tq, min(ql, (k + 1) * Tq), p, lo, hi);
+                    keys += (unsigned long long)(hi - lo);
+                }
+                atomicAdd(&s_pf_keys, keys);
             }
         }
         s_cls[s] = cls;
@@ -131,10 +164,39 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         return;
     }
 
-    // ---- 2. split-KV chunk for decode units
+    // ---- 2. SMs for each kernel, then the split-KV chunk for decode units
+    if (tid == 0) {
+        int pf_sms = p.n_sms, dec_sms = p.n_sms;
+        const unsigned long long dec_bytes = s_total * (unsigned long long)(2 * p.D * p.kv_elt);
+        const unsigned long long pf_flops =
+            s_pf_keys * (unsigned long long)p.Hkv * (unsigned long long)p.pf_mma_rows * (unsigned long long)(4 * p.D);
+        if (p.concurrent && dec_bytes > 0 && pf_flops > 0) {
+            // minimise max(prefill time, decode time) over the prefill SM count (times in ns)
+            unsigned long long best = ~0ull;
+            int best_x = 1;
+            for (int x = 1; x < p.n_sms; ++x) {
+                const unsigned long long tp = pf_flops / ((unsigned long long)x * p.pf_sm_gflops);
+                const unsigned long long bw =
+                    min((unsigned long long)p.hbm_gbs, (unsigned long long)(p.n_sms - x) * p.dec_sm_gbs);
+                const unsigned long long td = dec_bytes / bw;
+                const unsigned long long c = tp > td ? tp : td;
+                if (c < best) {
+                    best = c;
+                    best_x = x;
+                }
+            }
+            if (p.force_pf_sms > 0) best_x = min(p.force_pf_sms, p.n_sms - 1);
+            pf_sms = best_x;
+            dec_sms = p.n_sms - best_x;
+        }
+        if (p.force_dec_sms > 0) dec_sms = min(p.force_dec_sms, p.n_sms);
+        s_split[0] = pf_sms * p.pf_bps;
+        s_split[1] = dec_sms * p.dec_bps;
+    }
+    __syncthreads();
     int chunk;
     {
-        const unsigned long long target = (unsigned long long)kDecWaves * (unsigned long long)max(1, p.dec_slots);
+        const unsigned long long target = (unsigned long long)kDecWaves * (unsigned long long)max(1, s_split[1]);
         unsigned long long c = (s_total + target - 1) / target;
         if (c < (unsigned long long)kMinChunk) c = kMinChunk;
         c = (c + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
@@ -159,25 +221,18 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 pu = cnt;
             }
         }
-        int tot;
-        const int od = block_scan(du, s_warp, &tot);
-        const int td = tot;
-        const int op = block_scan(pu, s_warp, &tot);
-        const int tp = tot;
-        const int oa = block_scan(pa, s_warp, &tot);
-        const int ta = tot;
-        const int oc = block_scan(cb, s_warp, &tot);
-        const int tc = tot;
+        int4 tot;
+        const int4 off = block_scan4(make_int4(du, pu, pa, cb), s_warp, &tot);
         if (s < S) {
-            s_dend[s] = carry_d + od + du;
-            s_pend[s] = carry_p + op + pu;
-            s_part[s] = carry_part + oa;
-            s_comb[s] = carry_comb + oc;
+            s_dend[s] = carry_d + off.x + du;
+            s_pend[s] = carry_p + off.y + pu;
+            s_part[s] = carry_part + off.z;
+            s_comb[s] = carry_comb + off.w;
         }
-        carry_d += td;
-        carry_p += tp;
-        carry_part += ta;
-        carry_comb += tc;
+        carry_d += tot.x;
+        carry_p += tot.y;
+        carry_part += tot.z;
+        carry_comb += tot.w;
     }
     const int n_dec = carry_d, n_pf = carry_p, n_units = n_dec + n_pf;
     if (n_units > p.max_units || n_dec > p.max_dec_units || n_pf > p.max_pf_units ||
@@ -236,13 +291,14 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
 
     // ---- 5. bitonic sort of the keys (ascending: decode first, then cost descending)
-    int n2 = 1;
+    int n2 = 32;
     while (n2 < n_units) n2 <<= 1;
     if (do_sort) {
         for (int i = n_units + tid; i < n2; i += blockDim.x) s_keys[i] = ~0ull;
         __syncthreads();
         for (int k = 2; k <= n2; k <<= 1) {
-            for (int j = k >> 1; j > 0; j >>= 1) {
+            // strides >= 32: pairs in different warps, through shared memory
+            for (int j = k >> 1; j >= 32; j >>= 1) {
                 for (int i = tid; i < n2; i += blockDim.x) {
                     const int ixj = i ^ j;
                     if (ixj > i) {
@@ -256,6 +312,19 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 }
                 __syncthreads();
             }
+            // strides < 32: both keys of a pair sit in one warp, exchanged by shuffles
+            for (int i = tid; i < n2; i += blockDim.x) {
+                unsigned long long v = s_keys[i];
+                const bool up = (i & k) == 0;
+                for (int j = min(k >> 1, 16); j > 0; j >>= 1) {
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+                    const bool lower = (i & j) == 0;
+                    const unsigned long long lo = v < o ? v : o, hi = v < o ? o : v;
+                    v = (lower == up) ? lo : hi;
+                }
+                s_keys[i] = v;
+            }
+            __syncthreads();
         }
     }
     __syncthreads();
@@ -308,13 +377,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         ctrl[kSorted] = do_sort ? 1 : 0;
         ctrl[kCovLo] = S > 0 ? p.cu_q_lens[0] : 0;
         ctrl[kCovHi] = S > 0 ? p.cu_q_lens[S] : 0;
+        ctrl[kPfCtas] = s_split[0];
+        ctrl[kDecCtas] = s_split[1];
         ctrl[kStatus] = 0;
     }
 }
 
 }  // namespace
 
-size_t plan_smem_bytes() { return sizeof(unsigned long long) * kMaxSort; }
+size_t plan_smem_bytes() { return sizeof(unsigned long long) * kMaxSort + sizeof(int) * 6 * (kSeqSmem + 1); }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem) {
     rpa_plan_kernel<<<1, kPlanThreads, smem, st>>>(p);

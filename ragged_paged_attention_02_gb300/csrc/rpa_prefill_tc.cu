@@ -83,7 +83,6 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     const AttnParams& a = p.a;
     int* ctrl = a.ctrl;
     const uint64_t tmo = p.timeout_ns;
-    const int n_items = a.ctrl[a.item_count_word];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t smem0 = smem_u32(smem);
     const uint32_t q_base = smem0;                       // Q_A, Q_B
@@ -111,8 +110,13 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
+    pdl_trigger();
+    pdl_wait();  // the planner's items are complete from here on
+    const int n_items = a.ctrl[a.item_count_word];
+    const bool active = (int)blockIdx.x < a.ctrl[kPfCtas];  // otherwise SMs left to the decode kernel
 
-    if (warp == kProducer) {
+    if (!active) {
+    } else if (warp == kProducer) {
         // =============================== producer ===============================
         const int BR = p.BR, ps = a.ps, G = a.G, Th = p.Tq / 2;  // tokens per Q tile
         const int tasks = (kBN / BR) * 2 * Gm::CB;
@@ -518,8 +522,7 @@ struct TcKern {
         return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_prefill_tc<D>, kThreads, Gm::SMEM);
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
-        rpa_prefill_tc<D><<<l.grid, kThreads, Gm::SMEM, l.stream>>>(kvm, qm, p);
-        return cudaGetLastError();
+        return launch_pdl(rpa_prefill_tc<D>, l.grid, kThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 

@@ -266,18 +266,21 @@ def random_small(seed: int, *, num_seqs: int = 3, max_q: int = 9, max_kv: int = 
                  kv_dtype=kv_dtype, rng_lengths=rng, extra_pages=3, **knobs)
 
 
-def algorithmic_work(p: Problem) -> dict:
+def algorithmic_work(p: Problem, decode_rows: int = 16) -> dict:
     """Algorithmic bytes and FLOPs of one call (keys in the allowed band only).
 
     bytes = sum_s n_kv(s) * 2*Hkv*D*kv_elt + 2 * T_used*Hq*D*2 + 4*(pages used + 2S + 1)
     flops = sum_s sum_i 4*Hq*D*n_allowed(s, i)
+
+    The same sums split by sequence class are returned as ``decode`` and
+    ``prefill`` (a sequence is decode-class when q_len * G <= decode_rows),
+    so that each attention kernel is charged with the work it does.
     """
     kv_elt = 2 if p.kv_dtype == "bf16" else 1
     Hq, Hkv, D = p.num_q_heads, p.num_kv_heads, p.head_dim
-    byts = 0
-    pairs = 0
-    pages = 0
+    G = Hq // Hkv
     sw = p.sliding_window
+    part = {"decode": [0, 0, 0, 0], "prefill": [0, 0, 0, 0]}  # bytes, pairs, pages, tokens
     for s in range(p.num_seqs):
         ql = int(p.cu_q_lens[s + 1] - p.cu_q_lens[s])
         kl = int(p.kv_lens[s])
@@ -288,12 +291,16 @@ def algorithmic_work(p: Problem) -> dict:
         hi = np.minimum(pos + 1, kl) if p.is_causal else np.full(ql, kl)
         lo = np.maximum(pos - sw + 1, 0) if sw else np.zeros(ql, np.int64)
         n_allowed = np.maximum(hi - lo, 0)
-        pairs += int(n_allowed.sum())
-        band_lo = int(lo.min())
-        band_hi = int(hi.max())
-        byts += (band_hi - band_lo) * 2 * Hkv * D * kv_elt
-        pages += (kl + p.page_size - 1) // p.page_size
+        c = part["decode" if ql * G <= decode_rows else "prefill"]
+        c[0] += (int(hi.max()) - int(lo.min())) * 2 * Hkv * D * kv_elt + 2 * ql * Hq * D * 2
+        c[1] += int(n_allowed.sum())
+        c[2] += (kl + p.page_size - 1) // p.page_size
+        c[3] += ql
+    out = {}
+    for k, (b, pairs, pages, toks) in part.items():
+        out[k] = dict(bytes=b + 4 * pages, flops=4 * Hq * D * pairs, q_tokens=toks)
     t_used = int(p.cu_q_lens[p.num_seqs])
-    byts += 2 * t_used * Hq * D * 2 + 4 * (pages + 2 * p.num_seqs + 1)
-    return dict(bytes=byts, flops=4 * Hq * D * pairs, exps=Hq * pairs,
-                q_tokens=t_used)
+    byts = out["decode"]["bytes"] + out["prefill"]["bytes"] + 4 * (2 * p.num_seqs + 1)
+    pairs = (out["decode"]["flops"] + out["prefill"]["flops"]) // (4 * Hq * D)
+    return dict(bytes=byts, flops=4 * Hq * D * pairs, exps=Hq * pairs, q_tokens=t_used,
+                decode=out["decode"], prefill=out["prefill"])

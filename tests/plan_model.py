@@ -18,8 +18,39 @@ def band(kl, ql, i0, i1, causal, window):
     return lo, max(hi, lo)
 
 
-def plan(prob, dec_slots, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, align=64,
-         max_sort=16384):
+# rates of the SM-split model (FLOP/ns per SM on prefill, B/ns per SM decode, HBM B/ns)
+PF_SM_GFLOPS_TC, PF_SM_GFLOPS_MMA, DEC_SM_GBS, HBM_GBS = 7600, 800, 70, 6700
+
+
+def split(prob, dec_keyheads, pf_keys, n_sms, dec_bps, pf_bps, concurrent, force_pf=0, force_dec=0):
+    """(prefill CTAs, decode CTAs): minimise max(prefill time, decode time) over the
+    prefill SM count, integer nanoseconds, first minimum wins."""
+    tc = prob.kv_dtype == "bf16" and prob.head_dim in (64, 128)
+    D, Hkv = prob.head_dim, prob.num_kv_heads
+    kv_elt = 2 if prob.kv_dtype == "bf16" else 1
+    pf_rows = 256 if tc else 64
+    rate = PF_SM_GFLOPS_TC if tc else PF_SM_GFLOPS_MMA
+    dec_bytes = dec_keyheads * 2 * D * kv_elt
+    pf_flops = pf_keys * Hkv * pf_rows * 4 * D
+    pf_sms = dec_sms = n_sms
+    if concurrent and dec_bytes > 0 and pf_flops > 0:
+        best, best_x = None, 1
+        for x in range(1, n_sms):
+            tp = pf_flops // (x * rate)
+            td = dec_bytes // min(HBM_GBS, (n_sms - x) * DEC_SM_GBS)
+            c = max(tp, td)
+            if best is None or c < best:
+                best, best_x = c, x
+        if force_pf > 0:
+            best_x = min(force_pf, n_sms - 1)
+        pf_sms, dec_sms = best_x, n_sms - best_x
+    if force_dec > 0:
+        dec_sms = min(force_dec, n_sms)
+    return pf_sms * pf_bps, dec_sms * dec_bps
+
+
+def plan(prob, dec_slots=None, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, align=64,
+         max_sort=8192, n_sms=None, dec_bps=None, pf_bps=1, concurrent=False):
     Hkv = prob.num_kv_heads
     G = prob.num_q_heads // Hkv
     Tq = max(1, pf_tokens if pf_tokens is not None else 64 // G)
@@ -30,6 +61,7 @@ def plan(prob, dec_slots, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, a
     causal = prob.is_causal
     cls, cnt = [], []
     total = 0
+    pf_keys = 0
     for s in range(S):
         q0, q1, kl = cu[s], cu[s + 1], kvl[s]
         ql = q1 - q0
@@ -44,7 +76,14 @@ def plan(prob, dec_slots, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, a
             total += (hi - lo) * Hkv
         else:
             cls.append(2); cnt.append(-(-ql // Tq))
-    target = waves * max(1, dec_slots)
+            for k in range(cnt[-1]):
+                lo, hi = band(kl, ql, k * Tq, min(ql, (k + 1) * Tq), causal, win)
+                pf_keys += hi - lo
+    if n_sms is not None:
+        pf_ctas, dec_ctas = split(prob, total, pf_keys, n_sms, dec_bps, pf_bps, concurrent)
+    else:
+        pf_ctas, dec_ctas = None, dec_slots
+    target = waves * max(1, dec_ctas)
     chunk = max(-(-total // target), min_chunk)
     chunk = -(-chunk // align) * align
     chunk = min(chunk, 1 << 30)
@@ -86,4 +125,5 @@ def plan(prob, dec_slots, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, a
             item = [d[0], h, d[1], d[2], d[3], d[4], d[5] + h * d[7] + d[6] if d[5] >= 0 else -1, d[6]]
             (dec if c == 0 else pf).append(item)
     return dict(status=0, chunk=chunk, sorted=int(n <= max_sort and S < 65536), n_units=n, n_part=part,
+                pf_ctas=pf_ctas, dec_ctas=dec_ctas,
                 dec=np.array(dec, np.int32).reshape(-1, 8), pf=np.array(pf, np.int32).reshape(-1, 8))

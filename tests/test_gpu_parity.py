@@ -104,8 +104,10 @@ def test_planner_matches_python_rederivation():
         att = RaggedPagedAttention(**p.cfg_dict())
         att.forward(*to_dev(p), p.num_seqs)
         info, items = att.plan()
-        ref = plan(p, int(info[10]), pf_tokens=int(info[6]))
+        ref = plan(p, pf_tokens=int(info[6]), n_sms=int(info[12]), dec_bps=int(info[13]),
+                   pf_bps=int(info[14]), concurrent=bool(info[15]))
         assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
+        assert info[10] == ref["dec_ctas"] and info[11] == ref["pf_ctas"]
         assert info[9] == ref["sorted"] and info[7] == ref["n_part"]
         assert np.array_equal(items[: info[1]], ref["dec"])
         assert np.array_equal(items[info[1]:], ref["pf"])

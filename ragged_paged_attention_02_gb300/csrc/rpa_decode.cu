@@ -104,10 +104,8 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
         // =============================== producer ===============================
         if (p.debug_stall) return;  // test hook: consumers must time out
         const int BR = p.BR, ps = a.ps;
-        const int boxes = kKS / BR;                       // page runs per stage
-        const int tasks = boxes * (FP8 ? 2 : 2 * Gm::DH);  // copies per stage
-        const uint32_t box_bytes = (uint32_t)BR * (FP8 ? D : 128);  // one copy
-        const int PBB_P = FP8 ? 2 * BR * D : 2 * Gm::DH * BR * 128;   // one page run
+        const int runs = kKS / BR;  // page runs per stage, one bulk copy each (K and V of the head)
+        const uint32_t run_bytes = FP8 ? (uint32_t)(2 * BR * D) : (uint32_t)(2 * Gm::DH * BR * 128);
         int s = 0;
         uint32_t ph = 0;
         int it = 0;
@@ -141,34 +139,14 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                 }
                 const uint32_t st_base = smem0 + s * Gm::SB;
                 const uint32_t kv_base = st_base + Gm::QB;
-                // copy tasks of this stage, lane-strided: (page run b, K/V, column block)
-                auto task = [&](int t, int& x, int& y, uint32_t& dst) -> int {
-                    // 0: nothing to copy, 1: copy, 2: bad page id
-                    const int per = FP8 ? 2 : 2 * Gm::DH;
-                    const int b = t / per, rem = t % per;
-                    const int kv = FP8 ? rem : rem / Gm::DH;
-                    const int dh = FP8 ? 0 : rem % Gm::DH;
-                    const int k0 = k_stage + b * BR;
-                    const int lp = k0 / ps;
-                    const int pg = __shfl_sync(0xffffffffu, win, (lp - win0) & 31);
-                    if (t >= tasks || k0 >= item.kv_end || k0 + BR <= item.kv_begin) return 0;
-                    if ((unsigned)pg >= (unsigned)a.N) return 2;
-                    x = (2 * item.head + kv) * D + dh * 64;
-                    y = pg * ps + (k0 - lp * ps);
-                    dst = kv_base + (uint32_t)(b * PBB_P) +
-                          (FP8 ? (uint32_t)(kv * BR * D) : (uint32_t)((kv * Gm::DH + dh) * BR * 128));
-                    return 1;
-                };
-                int n_mine = 0, bad = 0;
-                for (int t0 = 0; t0 < tasks; t0 += 32) {
-                    int x, y;
-                    uint32_t dst;
-                    const int r = task(t0 + lane, x, y, dst);
-                    n_mine += r == 1;
-                    bad |= r == 2;
-                }
-                const int n_issue = __reduce_add_sync(0xffffffffu, n_mine);
-                if (__any_sync(0xffffffffu, bad)) {
+                // lane r < runs copies page run r of this stage (BR keys of one page)
+                const int k0 = k_stage + lane * BR;
+                const int lp = k0 / ps;
+                const int pg = __shfl_sync(0xffffffffu, win, (lp - win0) & 31);
+                const bool want = lane < runs && k0 < item.kv_end && k0 + BR > item.kv_begin;
+                const bool good = (unsigned)pg < (unsigned)a.N;
+                const int n_issue = __popc(__ballot_sync(0xffffffffu, want && good));
+                if (__any_sync(0xffffffffu, want && !good)) {
                     // a page id outside [0, N): never dereferenced; its keys read as zero
                     if (lane == 0) set_status(ctrl, RPA_ERR_BAD_PAGE_INDEX);
                     for (int i = lane; i < Gm::KVB / 16; i += 32)
@@ -196,17 +174,15 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                 __syncwarp();
                 const uint32_t fb = smem_u32(&full_bar[s]);
                 if (lane == 0)
-                    mbar_arrive_expect_tx(fb, (uint32_t)n_issue * box_bytes +
+                    mbar_arrive_expect_tx(fb, (uint32_t)n_issue * run_bytes +
                                                   (st == 0 ? (uint32_t)(Gm::DHQ * p.Tt * a.G * 128) : 0u));
                 __syncwarp();
                 if (st == 0 && lane < Gm::DHQ)
                     tma_load_3d(st_base + lane * 2048, &qmap, fb, lane * 64, item.head * a.G,
                                 q_start + item.tok0);
-                for (int t0 = 0; t0 < tasks; t0 += 32) {
-                    int x, y;
-                    uint32_t dst;
-                    if (task(t0 + lane, x, y, dst) == 1) tma_load_2d(dst, &kvmap, fb, x, y);
-                }
+                if (want && good)
+                    tma_load_3d(kv_base + (uint32_t)lane * run_bytes, &kvmap, fb, 0, pg * ps + (k0 - lp * ps),
+                                FP8 ? 2 * item.head : 2 * item.head * Gm::DH);
                 if (++s == kNS) {
                     s = 0;
                     ph ^= 1u;

@@ -18,7 +18,8 @@
 using namespace rpa;
 
 struct RpaHandle {
-    CUtensorMap kvmap;   // decode gather descriptors, re-encoded when the pointers change
+    CUtensorMap kvmap;   // decode gather: one copy per page run (K and V of a head)
+    CUtensorMap kvmap_pf;  // tensor-memory prefill gather: one copy per (page run, K/V, column block)
     CUtensorMap qmap;
     CUtensorMap qmap_pf;  // Q tiles of the tensor-memory prefill kernel
     const void* kvmap_ptr;
@@ -384,8 +385,10 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     }
     if (c.num_q_tokens > 0) {
         if (h->kvmap_ptr != kv_pages) {
-            if (encode_kv_map(&h->kvmap, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
-                              (int)c.num_kv_heads, h->D, h->BR) != 0)
+            if (encode_kv_map_runs(&h->kvmap, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
+                                   (int)c.num_kv_heads, h->D, h->BR) != 0 ||
+                (h->tc && encode_kv_map(&h->kvmap_pf, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
+                                        (int)c.num_kv_heads, h->D, h->BR) != 0))
                 return RPA_ERR_INVALID_ARG;
             h->kvmap_ptr = kv_pages;
         }
@@ -422,7 +425,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
             tp.BR = h->BR;
             tp.Tq = h->pf_tokens;
             tp.timeout_ns = h->timeout_ns;
-            if (launch_prefill_tc(h->kvmap, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
+            if (launch_prefill_tc(h->kvmap_pf, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
                 return RPA_ERR_CUDA;
         } else if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) {
             return RPA_ERR_CUDA;

@@ -173,6 +173,7 @@ constexpr int kTcRows = 128;  // rows of a tensor-memory prefill tile
 // tensor maps for the decode gather (host; no allocation)
 int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR);
 int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt);
+int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR);
 // occupancy / attributes (call once per device)
 cudaError_t attn_prepare(int D, int fp8, int* pf_blocks_per_sm);
 size_t plan_smem_bytes();

@@ -219,8 +219,9 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
         while ((int)(c.page_size % BR)) BR >>= 1;
         while ((1 << br_shift) < BR) ++br_shift;
         const int Tt = G <= kDecRows ? kDecRows / G : 1;
-        CUtensorMap kvm, qm, qm_pf;  // descriptors are encoded on the host stack
-        if (encode_kv_map(&kvm, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0 ||
+        CUtensorMap kvm, kvm_pf, qm, qm_pf;  // descriptors are encoded on the host stack
+        if (encode_kv_map_runs(&kvm, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0 ||
+            (tc && encode_kv_map(&kvm_pf, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0) ||
             encode_q_map(&qm, q, c.num_q_tokens, (int)c.num_q_heads, D, G, Tt) != 0 ||
             (tc && encode_q_map(&qm_pf, q, c.num_q_tokens, (int)c.num_q_heads, D, G, kTcRows / G) != 0))
             return RPA_ERR_INVALID_ARG;
@@ -244,7 +245,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
             tp.BR = BR;
             tp.Tq = pf_tokens;
             tp.timeout_ns = 1000000000ull;
-            if (launch_prefill_tc(kvm, qm_pf, tp, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+            if (launch_prefill_tc(kvm_pf, qm_pf, tp, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
         } else if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) {
             return RPA_ERR_CUDA;
         }

@@ -55,6 +55,36 @@ int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, 
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
+// K/V pages viewed as a 3-D tensor for the decode gather: (row elements of one
+// 128-byte column block, slots, column blocks of a slot row).  One box = BR
+// slots of kv head h: its K column blocks then its V column blocks, landing in
+// shared memory as [2*D/64][BR][128 B] (bf16, 128-byte swizzle); for fp8 the
+// box is (D bytes, BR slots, K and V) landing as [2][BR][D] (no swizzle).
+// The slot dimension comes before the column-block dimension so that the BR
+// rows of one column block are consecutive 128-byte lines.
+int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR) {
+    EncodeTiledFn fn = encoder();
+    if (!fn) return -1;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r;
+    if (fp8) {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(N * ps), (cuuint64_t)(2 * Hkv)};
+        const cuuint64_t strides[2] = {(cuuint64_t)(2 * Hkv * D), (cuuint64_t)D};
+        const cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)BR, 2u};
+        r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(kv), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[3] = {64u, (cuuint64_t)(N * ps), (cuuint64_t)(2 * Hkv * D / 64)};
+        const cuuint64_t strides[2] = {(cuuint64_t)(2 * Hkv * D * 2), 128u};
+        const cuuint32_t box[3] = {64u, (cuuint32_t)BR, (cuuint32_t)(2 * D / 64)};
+        r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
 // q viewed as (D, Hq, T): one box = 64 elements x the G heads of a kv group x
 // Tt tokens, 128-byte swizzle; tokens past T read as zero.
 int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt) {

@@ -205,7 +205,8 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
         h->timeout_ns = (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
         // tuning hooks: run decode and prefill one after the other, or fix the SM split
         const char* ser = getenv("RPA_SERIAL");
-        h->concurrent = (ser && ser[0] == '1') ? 0 : 1;
+        // the SM-split model is calibrated for the tensor-memory prefill kernel only
+        h->concurrent = (ser && ser[0] == '1') || !h->tc ? 0 : 1;
         const char* fp = getenv("RPA_DEBUG_PF_SMS");
         h->force_pf_sms = fp ? atoi(fp) : 0;
         const char* fd = getenv("RPA_DEBUG_DEC_SMS");

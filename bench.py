@@ -40,6 +40,7 @@ KERNEL_SOURCES = {
     "decode_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_decode.cu",
                          "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
     "prefill_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_prefill_tc.cu",
+                          "ragged_paged_attention_02_gb300/csrc/rpa_prefill_tc8.cu",
                           "ragged_paged_attention_02_gb300/csrc/rpa_attn_mma.cu",
                           "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
 }

@@ -25,7 +25,8 @@ struct RpaHandle {
     const void* kvmap_ptr;
     const void* qmap_ptr;
     int tc;               // prefill on tcgen05 (bf16 K/V, head_dim 64 or 128)
-    int pf_tokens;        // query tokens of a prefill tile (2 x 128-row tcgen05 tiles, else 64 rows)
+    int tc8;              // prefill on tcgen05 with fp8 K/V converted in shared memory (head_dim 128 or 256)
+    int pf_tokens;        // query tokens of a prefill item (2 x 128 rows for tc, 128 rows for tc8, else 64)
     RpaCfg cfg;
     int device;
     int sms;
@@ -195,7 +196,10 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     while ((1 << h->br_shift) < h->BR) ++h->br_shift;
     h->Tt = h->G <= kDecRows ? kDecRows / h->G : 1;
     h->tc = (!h->fp8 && (h->D == 64 || h->D == 128)) ? 1 : 0;
-    h->pf_tokens = h->tc ? 2 * (kTcRows / h->G) : (kPfRows / h->G > 0 ? kPfRows / h->G : 1);
+    h->tc8 = (h->fp8 && (h->D == 128 || h->D == 256)) ? 1 : 0;
+    h->pf_tokens = h->tc    ? 2 * (kTcRows / h->G)
+                   : h->tc8 ? kTcRows / h->G
+                            : (kPfRows / h->G > 0 ? kPfRows / h->G : 1);
     {
         // test hooks: a producer that issues nothing, and the bound of every device wait
         const char* e = getenv("RPA_DEBUG_STALL_PRODUCER");
@@ -223,8 +227,9 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
         else if ((e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess)
             step = "multiprocessor count";
         else if ((e = plan_prepare()) != cudaSuccess) step = "planner attributes";
-        else if ((e = h->tc ? prefill_tc_prepare(h->D, &h->pf_bps) : attn_prepare(h->D, h->fp8, &h->pf_bps)) !=
-                 cudaSuccess)
+        else if ((e = h->tc    ? prefill_tc_prepare(h->D, &h->pf_bps)
+                      : h->tc8 ? prefill_tc8_prepare(h->D, &h->pf_bps)
+                               : attn_prepare(h->D, h->fp8, &h->pf_bps)) != cudaSuccess)
             step = "prefill kernel attributes";
         else if ((e = decode_prepare(h->D, h->fp8, &h->dec_bps)) != cudaSuccess) step = "decode kernel attributes";
         else if (h->pf_bps < 1) step = "prefill kernel cannot be resident";
@@ -325,10 +330,10 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.n_sms = h->sms;
     pp.dec_bps = h->dec_bps;
     pp.pf_bps = h->pf_bps;
-    pp.pf_mma_rows = h->tc ? 2 * kTcRows : kPfRows;
+    pp.pf_mma_rows = h->tc ? 2 * kTcRows : h->tc8 ? kTcRows : kPfRows;
     pp.D = h->D;
     pp.kv_elt = h->fp8 ? 1 : 2;
-    pp.pf_sm_gflops = h->tc ? kPfSmGflopsTc : kPfSmGflopsMma;
+    pp.pf_sm_gflops = (h->tc || h->tc8) ? kPfSmGflopsTc : kPfSmGflopsMma;
     pp.dec_sm_gbs = kDecSmGBs;
     pp.hbm_gbs = kHbmGBs;
     pp.force_pf_sms = h->force_pf_sms;
@@ -395,8 +400,8 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
         }
         if (h->qmap_ptr != q) {
             if (encode_q_map(&h->qmap, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G, h->Tt) != 0 ||
-                (h->tc && encode_q_map(&h->qmap_pf, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G,
-                                       kTcRows / h->G) != 0))
+                ((h->tc || h->tc8) && encode_q_map(&h->qmap_pf, q, c.num_q_tokens, (int)c.num_q_heads, h->D,
+                                                   h->G, kTcRows / h->G) != 0))
                 return RPA_ERR_INVALID_ARG;
             h->qmap_ptr = q;
         }
@@ -427,6 +432,15 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
             tp.Tq = h->pf_tokens;
             tp.timeout_ns = h->timeout_ns;
             if (launch_prefill_tc(h->kvmap_pf, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
+                return RPA_ERR_CUDA;
+        } else if (h->tc8) {
+            // the fp8 kernel copies whole page runs (K and V of the head) with the decode gather's map
+            TcParams tp;
+            tp.a = ap;
+            tp.BR = h->BR;
+            tp.Tq = h->pf_tokens;
+            tp.timeout_ns = h->timeout_ns;
+            if (launch_prefill_tc8(h->kvmap, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
                 return RPA_ERR_CUDA;
         } else if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) {
             return RPA_ERR_CUDA;

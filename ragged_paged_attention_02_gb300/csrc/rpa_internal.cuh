@@ -169,6 +169,9 @@ cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, con
 cudaError_t decode_prepare(int D, int fp8, int* blocks_per_sm);
 cudaError_t launch_prefill_tc(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l);
 cudaError_t prefill_tc_prepare(int D, int* blocks_per_sm);
+cudaError_t launch_prefill_tc8(const CUtensorMap& kvm_runs, const CUtensorMap& qm, const TcParams& p,
+                               const Launch& l);
+cudaError_t prefill_tc8_prepare(int D, int* blocks_per_sm);
 constexpr int kTcRows = 128;  // rows of a tensor-memory prefill tile
 // tensor maps for the decode gather (host; no allocation)
 int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR);
@@ -344,6 +347,14 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t lbo, uin
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, int a_mn, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Instruction descriptor, kind::f16 with f16 A and B (fp32 accumulator).
+__host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem),

@@ -62,8 +62,10 @@ int setup(int dev, int D, int fp8, void** scratch, int* dec_bps, int* pf_bps) {
     if (!g_ready[dev][di][fp8]) {
         int a = 0, b = 0;
         const bool tc = !fp8 && (D == 64 || D == 128);
+        const bool tc8 = fp8 && (D == 128 || D == 256);
         if (decode_prepare(D, fp8, &a) != cudaSuccess ||
-            (tc ? prefill_tc_prepare(D, &b) : attn_prepare(D, fp8, &b)) != cudaSuccess) {
+            (tc ? prefill_tc_prepare(D, &b) : tc8 ? prefill_tc8_prepare(D, &b) : attn_prepare(D, fp8, &b)) !=
+                cudaSuccess) {
             cudaGetLastError();
             return RPA_ERR_CUDA;
         }
@@ -110,7 +112,8 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     // worst-case capacities, the same rule as rpa_create's workspace
     const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
     const bool tc = !fp8 && (D == 64 || D == 128);
-    const int pf_tokens = tc ? 2 * (kTcRows / G) : (kPfRows / G > 0 ? kPfRows / G : 1);
+    const bool tc8 = fp8 && (D == 128 || D == 256);
+    const int pf_tokens = tc ? 2 * (kTcRows / G) : tc8 ? kTcRows / G : (kPfRows / G > 0 ? kPfRows / G : 1);
     const int64_t Tq = pf_tokens;
     const int64_t dec_slots = (int64_t)sms * dec_bps;
     const int64_t max_dec_units = S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1;
@@ -166,10 +169,10 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     pp.n_sms = sms;
     pp.dec_bps = dec_bps;
     pp.pf_bps = pf_bps;
-    pp.pf_mma_rows = tc ? 2 * kTcRows : kPfRows;
+    pp.pf_mma_rows = tc ? 2 * kTcRows : tc8 ? kTcRows : kPfRows;
     pp.D = D;
     pp.kv_elt = fp8 ? 1 : 2;
-    pp.pf_sm_gflops = tc ? kPfSmGflopsTc : kPfSmGflopsMma;
+    pp.pf_sm_gflops = (tc || tc8) ? kPfSmGflopsTc : kPfSmGflopsMma;
     pp.dec_sm_gbs = kDecSmGBs;
     pp.hbm_gbs = kHbmGBs;
     pp.force_pf_sms = 0;
@@ -223,7 +226,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
         if (encode_kv_map_runs(&kvm, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0 ||
             (tc && encode_kv_map(&kvm_pf, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0) ||
             encode_q_map(&qm, q, c.num_q_tokens, (int)c.num_q_heads, D, G, Tt) != 0 ||
-            (tc && encode_q_map(&qm_pf, q, c.num_q_tokens, (int)c.num_q_heads, D, G, kTcRows / G) != 0))
+            ((tc || tc8) && encode_q_map(&qm_pf, q, c.num_q_tokens, (int)c.num_q_heads, D, G, kTcRows / G) != 0))
             return RPA_ERR_INVALID_ARG;
         DecParams dp;
         dp.a = ap;
@@ -246,6 +249,13 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
             tp.Tq = pf_tokens;
             tp.timeout_ns = 1000000000ull;
             if (launch_prefill_tc(kvm_pf, qm_pf, tp, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
+        } else if (tc8) {
+            TcParams tp;
+            tp.a = ap;
+            tp.BR = BR;
+            tp.Tq = pf_tokens;
+            tp.timeout_ns = 1000000000ull;
+            if (launch_prefill_tc8(kvm, qm_pf, tp, Launch{sms * pf_bps, st}) != cudaSuccess) return RPA_ERR_CUDA;
         } else if (launch_prefill(ap, fp8, Launch{sms * pf_bps, st}) != cudaSuccess) {
             return RPA_ERR_CUDA;
         }

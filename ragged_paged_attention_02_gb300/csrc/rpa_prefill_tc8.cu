@@ -1,0 +1,585 @@
+// rpa_prefill_tc8.cu -- K1 prefill for fp8 e4m3 K/V on the tcgen05 tensor cores.
+//
+// One persistent CTA per SM takes prefill work items of up to 128 query rows
+// of one kv head (Tq = 128 / G tokens x the G query heads of the group, packed
+// as the "ragged_paged.zig" page packs its q block into [Tq*G, D]) against a
+// key range of one sequence, in tiles of 64 keys.  The page dequantises with
+// k.astype(f32) * k_scale -> q dtype; here the e4m3 values are converted
+// exactly to f16, both MMAs run in f16 with fp32 accumulation, k_scale is
+// folded into the logit scale and v_scale into the epilogue.  Roles:
+//
+//   producer warp    Q tile (bf16) into a staging buffer, then per 64-key tile
+//                    the raw fp8 K/V rows of each page run (one bulk tensor
+//                    copy per run: K and V of the head) into a 2-slot ring.
+//   4 converter      Q: bf16 -> f16 into TMEM (the A operand of S = Q K^T);
+//   warps            K and V: e4m3 -> f16 into double-buffered, 128-byte
+//                    swizzled tiles (K-major), keys outside the item's
+//                    [kv_begin, kv_end) written as zero (the page zeroes K/V
+//                    past kv_len; tail slots may hold any bits).
+//   MMA warp         S = Q K^T (A from TMEM, B from smem) into one of two TMEM
+//                    S buffers; O += P V (P from TMEM over S, V MN-major).
+//   4 softmax warps  thread r owns TMEM lane r (query row r): scale / softcap /
+//                    masks in the log2 domain, running max and sum, P in f16,
+//                    lazy O rescale (max grows by more than 2^8), epilogue.
+//
+// TMEM: Q (D/2 columns of packed f16 pairs), S0, S1 (64 each), O (D) -- 512
+// columns at D = 256.  All waits are bounded; on expiry the status word gets
+// RPA_ERR_TIMEOUT.
+#include <cuda.h>
+
+#include "rpa_internal.cuh"
+
+namespace rpa {
+
+namespace {
+
+constexpr int kM = kTcRows;   // query rows per tile = TMEM lanes
+constexpr int kBN = 64;       // keys per K/V tile
+constexpr int kThreads = 320; // warps 0-3 softmax, 4-7 convert, 8 producer, 9 MMA
+constexpr int kProducer = 8, kMma = 9;
+constexpr int kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.f;
+
+enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, eNtok, eNt, eKey0, eStop };
+
+template <int D>
+struct G8 {
+    static constexpr int CB = D / 64;                  // 128-byte column blocks of a 16-bit row
+    static constexpr int ROUNDS = D / 128;             // Q staging rounds (two column blocks each)
+    static constexpr int QSTAGE = 2 * kM * 128;        // Q staging: 2 column blocks x 128 rows
+    static constexpr int RAW = kBN * 2 * D;            // one raw fp8 stage (K and V)
+    static constexpr int T16 = CB * kBN * 128;         // one f16 K (or V) tile
+    static constexpr int DATA = QSTAGE + 2 * RAW + 4 * T16;
+    static constexpr int SMEM = DATA + 1024;
+    static constexpr uint32_t TM_Q = 0;                // Q: D/2 columns
+    static constexpr uint32_t TM_S0 = D / 2, TM_S1 = D / 2 + kBN;
+    static constexpr uint32_t TM_O = D / 2 + 2 * kBN;  // O: D columns
+    static_assert(D / 2 + 2 * kBN + D <= kTmemCols, "TMEM budget");
+    static_assert(DATA + 1024 <= 227 * 1024, "shared memory budget");
+};
+
+__device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// e4m3 x 8 (two words) -> f16 x 8 (uint4)
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 b) {
+    uint4 o;
+    o.x = e4m3x2_to_f16x2((uint16_t)(b.x & 0xffff));
+    o.y = e4m3x2_to_f16x2((uint16_t)(b.x >> 16));
+    o.z = e4m3x2_to_f16x2((uint16_t)(b.y & 0xffff));
+    o.w = e4m3x2_to_f16x2((uint16_t)(b.y >> 16));
+    return o;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_constant__ CUtensorMap kvmap,
+                                                               const __grid_constant__ CUtensorMap qmap,
+                                                               const TcParams p) {
+    using Gm = G8<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t meta_full[2], meta_free[2];
+    __shared__ __align__(8) uint64_t q_full, q_empty, q_ready, qt_free;
+    __shared__ __align__(8) uint64_t raw_full[2], raw_empty[2];
+    __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
+    __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done, o_full, o_free;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int meta[2][16];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const AttnParams& a = p.a;
+    int* ctrl = a.ctrl;
+    const uint64_t tmo = p.timeout_ns;
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t smem0 = smem_u32(smem);
+    const uint32_t q_stage = smem0;                                 // Q staging (bf16)
+    const uint32_t raw_base = q_stage + Gm::QSTAGE;                 // 2 raw fp8 stages
+    const uint32_t k16_base = raw_base + 2 * Gm::RAW;               // 2 f16 K tiles
+    const uint32_t v16_base = k16_base + 2 * Gm::T16;               // 2 f16 V tiles
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&meta_full[i]), 1);
+            mbar_init(smem_u32(&meta_free[i]), 9);  // 4 softmax + 4 converter warps + MMA thread
+            mbar_init(smem_u32(&raw_full[i]), 1);
+            mbar_init(smem_u32(&raw_empty[i]), 4);
+            mbar_init(smem_u32(&k_full[i]), 4);
+            mbar_init(smem_u32(&k_empty[i]), 1);
+            mbar_init(smem_u32(&v_full[i]), 4);
+            mbar_init(smem_u32(&v_empty[i]), 1);
+            mbar_init(smem_u32(&s_full[i]), 1);
+            mbar_init(smem_u32(&p_full[i]), 4);
+        }
+        mbar_init(smem_u32(&q_full), 1);
+        mbar_init(smem_u32(&q_empty), 4);
+        mbar_init(smem_u32(&q_ready), 4);
+        mbar_init(smem_u32(&qt_free), 1);
+        mbar_init(smem_u32(&pv_done), 1);
+        mbar_init(smem_u32(&o_full), 1);
+        mbar_init(smem_u32(&o_free), 4);
+        fence_mbar_init();
+    }
+    if (warp == kMma) tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    pdl_trigger();
+    pdl_wait();  // the planner's items are complete from here on
+    const int n_items = a.ctrl[a.item_count_word];
+    const bool active = (int)blockIdx.x < a.ctrl[kPfCtas];
+
+    if (!active) {
+    } else if (warp == kProducer) {
+        // =============================== producer ===============================
+        const int BR = p.BR, ps = a.ps, G = a.G, Tq = p.Tq;
+        const int runs = kBN / BR;
+        const uint32_t run_bytes = (uint32_t)(2 * BR * D);
+        const uint32_t q_round_bytes = (uint32_t)(2 * G * Tq * 128);
+        int s = 0, ms = 0;
+        uint32_t ph = 0, mph = 0, qph = 0;
+        bool ok = true;
+        int it = 0;
+        if (lane == 0) it = atomicAdd(ctrl + a.counter_word, 1);
+        it = __shfl_sync(0xffffffffu, it, 0);
+        for (;;) {
+            if (!mbar_wait(smem_u32(&meta_free[ms]), mph ^ 1u, ctrl, tmo)) break;
+            if (it >= n_items) {
+                if (lane == 0) {
+                    meta[ms][eStop] = 1;
+                    mbar_arrive(smem_u32(&meta_full[ms]));
+                }
+                break;
+            }
+            const Item item = a.items[it];
+            int nxt = 0;
+            if (lane == 0) nxt = atomicAdd(ctrl + a.counter_word, 1);
+            const int q_start = a.cu_q_lens[item.seq];
+            const int ql = a.cu_q_lens[item.seq + 1] - q_start;
+            const int kl = a.kv_lens[item.seq];
+            const int* ptab = a.page_indices + (size_t)item.seq * a.P;
+            const int key0 = item.kv_begin - (item.kv_begin & (BR - 1));
+            const int nt = (item.kv_end - key0 + kBN - 1) / kBN;
+            if (lane == 0) {
+                int* m = meta[ms];
+                m[eSeq] = item.seq;
+                m[eHead] = item.head;
+                m[eQStart] = q_start;
+                m[eQl] = ql;
+                m[eKl] = kl;
+                m[eKvBegin] = item.kv_begin;
+                m[eKvEnd] = item.kv_end;
+                m[eTok0] = item.tok0;
+                m[eNtok] = item.ntok;
+                m[eNt] = nt;
+                m[eKey0] = key0;
+                m[eStop] = 0;
+                mbar_arrive(smem_u32(&meta_full[ms]));
+            }
+            if (++ms == 2) {
+                ms = 0;
+                mph ^= 1u;
+            }
+            // Q: two column blocks per round through the staging buffer
+            for (int rd = 0; rd < Gm::ROUNDS && ok; ++rd) {
+                if (!mbar_wait(smem_u32(&q_empty), qph ^ 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t qfb = smem_u32(&q_full);
+                if (lane == 0) mbar_arrive_expect_tx(qfb, q_round_bytes);
+                __syncwarp();
+                if (lane < 2)
+                    tma_load_3d(q_stage + lane * (kM * 128), &qmap, qfb, (2 * rd + lane) * 64, item.head * G,
+                                q_start + item.tok0);
+                qph ^= 1u;
+            }
+            int win0 = key0 / ps;
+            int win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
+            for (int t = 0; t < nt && ok; ++t) {
+                const int k_tile = key0 + t * kBN;
+                const int lp_last = min(k_tile + kBN - 1, item.kv_end - 1) / ps;
+                if (lp_last - win0 >= 32) {
+                    win0 = k_tile / ps;
+                    win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
+                }
+                if (!mbar_wait(smem_u32(&raw_empty[s]), ph ^ 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t stage = raw_base + s * Gm::RAW;
+                const int k0 = k_tile + lane * BR;
+                const int lp = k0 / ps;
+                const int pg = __shfl_sync(0xffffffffu, win, (lp - win0) & 31);
+                const bool want = lane < runs && k0 < item.kv_end && k0 + BR > item.kv_begin;
+                const bool good = (unsigned)pg < (unsigned)a.N;
+                const int n_issue = __popc(__ballot_sync(0xffffffffu, want && good));
+                if (__any_sync(0xffffffffu, want && !good) && lane == 0) set_status(ctrl, RPA_ERR_BAD_PAGE_INDEX);
+                const uint32_t fb = smem_u32(&raw_full[s]);
+                if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_issue * run_bytes);
+                __syncwarp();
+                if (want && good)
+                    tma_load_3d(stage + (uint32_t)lane * run_bytes, &kvmap, fb, 0, pg * ps + (k0 - lp * ps),
+                                2 * item.head);
+                if (++s == 2) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            it = __shfl_sync(0xffffffffu, nxt, 0);
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // =============================== converters ===============================
+        const int cw = warp - 4;             // converter warp 0..3
+        const int r = tid - 128;             // TMEM lane (query row) for the Q conversion
+        const uint32_t lane_addr = tmem + ((uint32_t)(cw * 32) << 16);
+        const int BR = p.BR;
+        int s = 0, ms = 0;
+        uint32_t ph = 0, mph = 0, qph = 0;
+        uint32_t tg = 0, items = 0;  // tiles (all items) and items converted
+        for (;;) {
+            if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
+            const int* mm = meta[ms];
+            const int stop = mm[eStop], kv_begin = mm[eKvBegin], kv_end = mm[eKvEnd], nt = mm[eNt],
+                      key0 = mm[eKey0];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&meta_free[ms]));
+            if (stop) break;
+            if (++ms == 2) {
+                ms = 0;
+                mph ^= 1u;
+            }
+            // ---- Q: bf16 staging -> f16 TMEM columns (thread r owns query row r)
+            if (items > 0 && !mbar_wait(smem_u32(&qt_free), (items - 1) & 1u, ctrl, tmo)) break;
+            bool ok = true;
+            for (int rd = 0; rd < Gm::ROUNDS; ++rd) {
+                if (!mbar_wait(smem_u32(&q_full), qph, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                qph ^= 1u;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t qv[32];
+                    const uint8_t* row = smem + (q_stage - smem0) + half * (kM * 128) + r * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(row + (((c ^ r) & 7) << 4));
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            qv[4 * c + k] = pack2<true>(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xffff0000u));
+                    }
+                    tmem_st32(lane_addr + Gm::TM_Q + (2 * rd + half) * 32, qv);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&q_empty));
+            }
+            if (!ok) break;
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&q_ready));
+            // ---- K / V tiles: this warp converts keys [16cw, 16cw + 16) of each tile, one row per pass
+            for (int t = 0; t < nt; ++t, ++tg) {
+                const int b2 = tg & 1;
+                const uint32_t par = (tg >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&raw_full[s]), ph, ctrl, tmo) ||
+                    !mbar_wait(smem_u32(&k_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* raw = smem + (raw_base - smem0) + s * Gm::RAW;
+                const int k_lo = key0 + t * kBN;
+#pragma unroll 1
+                for (int kv = 0; kv < 2; ++kv) {
+                    if (kv == 1 && !mbar_wait(smem_u32(&v_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* dst = smem + ((kv ? v16_base : k16_base) - smem0) + b2 * Gm::T16;
+                    // a lane converts 8 consecutive elements: D / 8 lanes per key row, 32 / (D / 8) rows a pass
+                    constexpr int LPR = D / 8, RPP = 32 / LPR;
+                    const int e = lane % LPR, cb = e >> 3, c = e & 7;
+#pragma unroll 4
+                    for (int kr = lane / LPR; kr < 16; kr += RPP) {
+                        const int key = 16 * cw + kr;  // key row of the tile
+                        const int j = k_lo + key;
+                        uint4 o = make_uint4(0, 0, 0, 0);
+                        if (j >= kv_begin && j < kv_end) {
+                            const int bb = key / BR, rr = key - bb * BR;
+                            const uint2 v8 = *reinterpret_cast<const uint2*>(raw + bb * (2 * BR * D) + kv * BR * D +
+                                                                             rr * D + e * 8);
+                            o = e4m3x8_to_f16x8(v8);
+                        }
+                        const int line = cb * kBN + key;
+                        put_u4(dst + line * 128 + (((c ^ line) & 7) << 4), o);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(kv ? &v_full[b2] : &k_full[b2]));
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&raw_empty[s]));
+                if (++s == 2) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            ++items;
+        }
+    } else if (warp == kMma) {
+        // =============================== MMA issuer ===============================
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = umma_idesc_f16(kM, kBN, 0, 0);
+            constexpr uint32_t idesc_pv = umma_idesc_f16(kM, D, 0, 1);
+            int ms = 0;
+            uint32_t mph = 0;
+            uint32_t tg = 0, items = 0;
+            bool ok = true;
+            auto issue_pv = [&](uint32_t g, bool first) -> bool {
+                const int b2 = g & 1;
+                const uint32_t par = (g >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&p_full[b2]), par, ctrl, tmo) ||
+                    !mbar_wait(smem_u32(&v_full[b2]), par, ctrl, tmo))
+                    return false;
+                if (first && items > 0 && !mbar_wait(smem_u32(&o_free), (items - 1) & 1u, ctrl, tmo)) return false;
+                tc_fence_after();
+                const uint32_t vt = v16_base + b2 * Gm::T16;
+                const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk) {
+                    const uint64_t bdesc = umma_sdesc(vt + kk * 16 * 128, kBN * 128, 1024);
+                    umma_ts(tmem + Gm::TM_O, tmem + scol + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1 : 0);
+                }
+                umma_commit(smem_u32(&v_empty[b2]));
+                umma_commit(smem_u32(&pv_done));
+                return true;
+            };
+            for (;;) {
+                if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
+                const int stop = meta[ms][eStop], nt = meta[ms][eNt];
+                mbar_arrive(smem_u32(&meta_free[ms]));
+                if (stop) break;
+                if (++ms == 2) {
+                    ms = 0;
+                    mph ^= 1u;
+                }
+                if (!mbar_wait(smem_u32(&q_ready), items & 1u, ctrl, tmo)) break;
+                tc_fence_after();
+                const uint32_t g0 = tg;
+                for (int t = 0; t < nt; ++t, ++tg) {
+                    const int b2 = tg & 1;
+                    if (!mbar_wait(smem_u32(&k_full[b2]), (tg >> 1) & 1u, ctrl, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t kt = k16_base + b2 * Gm::T16;
+                    const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
+                        umma_ts(tmem + scol, tmem + Gm::TM_Q + kk * 8, umma_sdesc(kt + koff, 16, 1024), idesc_qk,
+                                kk > 0 ? 1 : 0);
+                    }
+                    umma_commit(smem_u32(&s_full[b2]));
+                    umma_commit(smem_u32(&k_empty[b2]));
+                    if (t == nt - 1) umma_commit(smem_u32(&qt_free));
+                    if (t > 0 && !issue_pv(tg - 1, t == 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok || !issue_pv(tg - 1, tg - 1 == g0)) break;
+                umma_commit(smem_u32(&o_full));
+                ++items;
+            }
+        }
+        __syncwarp();
+    } else {
+        // =============================== softmax warps ===============================
+        const int r = tid;  // TMEM lane == query row
+        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        const int G = a.G, Hq = a.Hq;
+        int ms = 0;
+        uint32_t mph = 0, tg = 0, items = 0;
+        for (;;) {
+            if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
+            const int* mm = meta[ms];
+            const int stop = mm[eStop];
+            const int head = mm[eHead], q_start = mm[eQStart], ql = mm[eQl], kl = mm[eKl];
+            const int kv_begin = mm[eKvBegin], kv_end = mm[eKvEnd], tok0 = mm[eTok0];
+            const int ntok = mm[eNtok], nt = mm[eNt], key0 = mm[eKey0];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&meta_free[ms]));
+            if (stop) break;
+            if (++ms == 2) {
+                ms = 0;
+                mph ^= 1u;
+            }
+            const int pos = kl - ql + tok0 + r / G;
+            const int pos_lo = kl - ql + tok0, pos_hi = kl - ql + tok0 + ntok - 1;
+            float m_run = -INFINITY, l_run = 0.f;
+            bool ok = true;
+            for (int t = 0; t < nt; ++t, ++tg) {
+                const int b2 = tg & 1;
+                if (!mbar_wait(smem_u32(&s_full[b2]), (tg >> 1) & 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int k_lo = key0 + t * kBN;
+                const bool partial = k_lo < kv_begin || k_lo + kBN > kv_end;
+                const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
+                                       (a.has_window && k_lo <= pos_hi - a.window);
+                const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+                const bool rewrite = need_mask || a.has_cap;
+                float mt = -INFINITY;
+                if (!rewrite) {
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(lane_addr + scol + c * 32, sv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sv[i]) * a.qk_log2);
+                    }
+                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                } else {
+                    const bool cap = a.has_cap;
+#pragma unroll 1
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t sv[32];
+                        tmem_ld32(lane_addr + scol + c * 32, sv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float v = __uint_as_float(sv[i]);
+                            v = cap ? a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + ex2(v * a.cap_exp))
+                                    : v * a.qk_log2;
+                            const int j = k_lo + c * 32 + i;
+                            const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos) &&
+                                             (!a.has_window || j > pos - a.window);
+                            v = (okk || !need_mask) ? v : -INFINITY;
+                            mt = fmaxf(mt, v);
+                            sv[i] = __float_as_uint(v);
+                        }
+                        tmem_st32(lane_addr + scol + c * 32, sv);
+                    }
+                    tmem_st_wait();
+                }
+                const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
+                const float m_new = need ? fmaxf(m_run, mt) : m_run;
+                const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
+                const float base = m_new == -INFINITY ? 0.f : m_new;
+                const float mul = rewrite ? 1.f : a.qk_log2;
+                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int c = 0; c < kBN / 32; ++c) {
+                    uint32_t sv[32], pk[16];
+                    tmem_ld32(lane_addr + scol + c * 32, sv);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), mul, -base));
+                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), mul, -base));
+                        ls4[i & 3] += p0 + p1;
+                        pk[i] = pack2<true>(p0, p1);
+                    }
+                    tmem_st16(lane_addr + scol + c * 16, pk);
+                }
+                l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+                m_run = m_new;
+                if (need && t > 0) {
+                    if (!mbar_wait(smem_u32(&pv_done), (tg - 1) & 1u, ctrl, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(lane_addr + Gm::TM_O + c * 32, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(lane_addr + Gm::TM_O + c * 32, ov);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
+            }
+            if (!ok) break;
+            // ---- epilogue: o = O * v_scale / l
+            if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
+            tc_fence_after();
+            const int rows_used = ntok * G;
+            const float inv = l_run > 0.f ? a.v_scale / l_run : 0.f;
+            const int t_tok = q_start + tok0 + r / G;
+            const int qh = head * G + r % G;
+            uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2);
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(lane_addr + Gm::TM_O + c * 32, ov);
+                tmem_ld_wait();
+                if (r < rows_used) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 w;
+                        w.x = pack2<false>(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
+                        w.y = pack2<false>(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
+                        w.z = pack2<false>(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
+                        w.w = pack2<false>(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
+                        put_u4(orow + c * 64 + i * 16, w);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&o_free));
+            ++items;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D>
+struct Tc8Kern {
+    using Gm = G8<D>;
+    static cudaError_t prepare(int* bps) {
+        cudaError_t e =
+            cudaFuncSetAttribute(rpa_prefill_tc8<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+        if (e != cudaSuccess) return e;
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_prefill_tc8<D>, kThreads, Gm::SMEM);
+    }
+    static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
+        return launch_pdl(rpa_prefill_tc8<D>, l.grid, kThreads, Gm::SMEM, l.stream, kvm, qm, p);
+    }
+};
+
+}  // namespace
+
+cudaError_t prefill_tc8_prepare(int D, int* bps) {
+    if (D == 128) return Tc8Kern<128>::prepare(bps);
+    if (D == 256) return Tc8Kern<256>::prepare(bps);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_tc8(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
+    if (p.a.D == 128) return Tc8Kern<128>::launch(kvm, qm, p, l);
+    if (p.a.D == 256) return Tc8Kern<256>::launch(kvm, qm, p, l);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rpa

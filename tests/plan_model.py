@@ -28,8 +28,9 @@ def split(prob, dec_keyheads, pf_keys, n_sms, dec_bps, pf_bps, concurrent, force
     tc = prob.kv_dtype == "bf16" and prob.head_dim in (64, 128)
     D, Hkv = prob.head_dim, prob.num_kv_heads
     kv_elt = 2 if prob.kv_dtype == "bf16" else 1
-    pf_rows = 256 if tc else 64
-    rate = PF_SM_GFLOPS_TC if tc else PF_SM_GFLOPS_MMA
+    tc8 = prob.kv_dtype != "bf16" and prob.head_dim in (128, 256)
+    pf_rows = 256 if tc else 128 if tc8 else 64
+    rate = PF_SM_GFLOPS_TC if (tc or tc8) else PF_SM_GFLOPS_MMA
     dec_bytes = dec_keyheads * 2 * D * kv_elt
     pf_flops = pf_keys * Hkv * pf_rows * 4 * D
     pf_sms = dec_sms = n_sms

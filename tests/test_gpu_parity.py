@@ -54,6 +54,13 @@ SMALL = [
               page_size=64)),
     (39, dict(num_seqs=7, max_q=12, max_kv=2000, num_q_heads=12, num_kv_heads=3, head_dim=128,
               page_size=32, kv_dtype="fp8_e4m3", k_scale=0.5, sliding_window=1)),
+    # fp8 prefill on the tensor-memory kernel: page runs of 64 / 8 keys, G = 8, 1 and 3
+    (40, dict(num_seqs=4, max_q=300, max_kv=900, num_q_heads=16, num_kv_heads=2, head_dim=128,
+              page_size=64, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, is_causal=False)),
+    (41, dict(num_seqs=3, max_q=200, max_kv=600, num_q_heads=4, num_kv_heads=4, head_dim=256,
+              page_size=8, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.2, sm_scale=1 / 16)),
+    (42, dict(num_seqs=5, max_q=100, max_kv=400, num_q_heads=6, num_kv_heads=2, head_dim=128,
+              page_size=16, kv_dtype="fp8_e4m3", k_scale=0.05, soft_cap=30.0, sliding_window=150)),
 ]
 
 
@@ -127,20 +134,24 @@ def test_page_placement_invariance_bit_identical():
     assert np.array_equal(a, b)
 
 
-def test_poisoned_tails_and_unused_pages():
-    p = ri.random_small(42, num_seqs=5, max_q=30, max_kv=500, num_q_heads=8, num_kv_heads=2,
-                        head_dim=128, extra_tokens=0)
+@pytest.mark.parametrize("kv_dtype,head_dim", [("bf16", 128), ("fp8_e4m3", 128), ("fp8_e4m3", 256)])
+def test_poisoned_tails_and_unused_pages(kv_dtype, head_dim):
+    extra = {} if kv_dtype == "bf16" else dict(k_scale=0.05, v_scale=0.05)
+    p = ri.random_small(42, num_seqs=5, max_q=130, max_kv=500, num_q_heads=8, num_kv_heads=2,
+                        head_dim=head_dim, extra_tokens=0, kv_dtype=kv_dtype, **extra)
     ref = oracle.forward(p)
     used = set()
     ps = p.page_size
+    # bf16: NaN in the tails, +inf in unused pages; e4m3fn has no inf, NaN is 0x7F
+    nan, inf = (0x7FC0, 0x7F80) if kv_dtype == "bf16" else (0x7F, 0x7F)
     for s in range(p.num_seqs):
         kl = int(p.kv_lens[s])
         used.update(int(x) for x in p.page_indices[s, : (kl + ps - 1) // ps])
         if kl % ps:
-            p.kv_pages[p.page_indices[s, kl // ps], kl % ps:] = 0x7FC0  # NaN
+            p.kv_pages[p.page_indices[s, kl // ps], kl % ps:] = nan
     for pg in range(p.total_num_pages):
         if pg not in used:
-            p.kv_pages[pg] = 0x7F80  # +inf
+            p.kv_pages[pg] = inf
     got, st = run(p)
     assert st == 0
     assert_close(got, ref, p.kv_dtype, "poisoned")

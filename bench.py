@@ -52,6 +52,8 @@ DESCR = {
                   "fp8 e4m3 K/V, softcap 50, window 4096",
     "long_prefill": "4 seqs x 8192 fresh prefill, Hq 64 / Hkv 8, D 128, page 64, bf16",
     "decode_quarter": "64 seqs x q_len 1, kv_len~U[512,8192], Hq 32 / Hkv 8, D 128, page 16, bf16",
+    "fp8_window_quarter": "the first 32 seqs of fp8_window (q_len~U{1..64} kv_len~U[256,16384]), "
+                          "Hq 16 / Hkv 8, D 256, page 16, fp8 e4m3 K/V, softcap 50, window 4096",
 }
 
 

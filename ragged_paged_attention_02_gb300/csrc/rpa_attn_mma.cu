@@ -242,7 +242,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
                     float x = sacc[nb][e];
                     if (p.has_cap) {
                         const float t = ex2(x * p.cap_exp);
-                        x = p.cap_log2 - 2.f * p.cap_log2 * __frcp_rn(1.f + t);
+                        x = p.cap_log2 - 2.f * p.cap_log2 * rcp_approx(1.f + t);
                     } else {
                         x *= p.qk_log2;
                     }

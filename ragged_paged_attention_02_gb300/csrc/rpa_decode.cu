@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                     float x = sacc[nb][e];
                     if (a.has_cap) {
                         const float t = ex2(x * a.cap_exp);
-                        x = a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + t);
+                        x = a.cap_log2 - 2.f * a.cap_log2 * rcp_approx(1.f + t);
                     } else {
                         x *= a.qk_log2;
                     }

@@ -237,6 +237,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// 1/x on the special-function unit (hardware instruction, flush-to-zero).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Pack two floats into a bf16x2 / f16x2 register (round to nearest even).
 template <bool F16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {

@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             float v = __uint_as_float(sv[i]);
-                            v = cap ? a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + ex2(v * a.cap_exp))
+                            v = cap ? a.cap_log2 - 2.f * a.cap_log2 * rcp_approx(1.f + ex2(v * a.cap_exp))
                                     : v * a.qk_log2;
                             const int j = k_lo + c * 32 + i;
                             const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos) &&

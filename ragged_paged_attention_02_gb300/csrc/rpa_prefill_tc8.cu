@@ -60,14 +60,43 @@ struct G8 {
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// e4m3 x 8 (two words) -> f16 x 8 (uint4)
+// e4m3 byte b = s eeee mmm  ->  the f16 with bits s 0eeee mmm0000000, whose value is exactly
+// e4m3(b) / 2^8 for every finite b, normal or subnormal (both formats put the exponent bias
+// so that moving the field moves the value by 2^(15 - 7)); the factor is taken back in the
+// logit scale and the output scale.  Integer ops only: the special-function pipe stays free
+// for the softmax.  An e4m3 NaN (s 1111 111) maps to 480 / 2^8 instead of NaN.
+constexpr float kKvUnscale = 256.f;
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel) {
+    const uint32_t u = __byte_perm(w, 0u, sel);  // the two bytes in the low byte of each half
+    const uint32_t t = u << 7;                   // eeee mmm at bits 7..13, s at bit 14
+    return t + (t & 0x40004000u);                // s carried from bit 14 up to bit 15
+}
 __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 b) {
     uint4 o;
-    o.x = e4m3x2_to_f16x2((uint16_t)(b.x & 0xffff));
-    o.y = e4m3x2_to_f16x2((uint16_t)(b.x >> 16));
-    o.z = e4m3x2_to_f16x2((uint16_t)(b.y & 0xffff));
-    o.w = e4m3x2_to_f16x2((uint16_t)(b.y >> 16));
+    o.x = e4m3x2_to_f16x2_scaled(b.x, 0x4140u);
+    o.y = e4m3x2_to_f16x2_scaled(b.x, 0x4342u);
+    o.z = e4m3x2_to_f16x2_scaled(b.y, 0x4140u);
+    o.w = e4m3x2_to_f16x2_scaled(b.y, 0x4342u);
     return o;
+}
+
+// Logits of one 64-key tile in the log2 domain, in place: scale (or soft cap), then
+// keys outside [lo, hi] of the tile to -inf; returns the row max.
+template <bool CAP, bool MASK>
+__device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl, float cape, int lo, int hi) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int i = 0; i < kBN; ++i) {
+        float v = __uint_as_float(sv[i]);
+        if constexpr (CAP)
+            v = capl - 2.f * capl * rcp_approx(1.f + ex2(v * cape));  // cap * tanh(x / cap), log2 domain
+        else
+            v *= qk;
+        if constexpr (MASK) v = (i >= lo && i <= hi) ? v : -INFINITY;
+        m4[i & 3] = fmaxf(m4[i & 3], v);
+        sv[i] = __float_as_uint(v);
+    }
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
 template <int D>
@@ -232,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
         const int cw = warp - 4;             // converter warp 0..3
         const int r = tid - 128;             // TMEM lane (query row) for the Q conversion
         const uint32_t lane_addr = tmem + ((uint32_t)(cw * 32) << 16);
-        const int BR = p.BR;
+        const int BR = p.BR, brs = __ffs(BR) - 1;
         int s = 0, ms = 0;
         uint32_t ph = 0, mph = 0, qph = 0;
         uint32_t tg = 0, items = 0;  // tiles (all items) and items converted
@@ -297,22 +326,38 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                         break;
                     }
                     uint8_t* dst = smem + ((kv ? v16_base : k16_base) - smem0) + b2 * Gm::T16;
-                    // a lane converts 8 consecutive elements: D / 8 lanes per key row, 32 / (D / 8) rows a pass
-                    constexpr int LPR = D / 8, RPP = 32 / LPR;
-                    const int e = lane % LPR, cb = e >> 3, c = e & 7;
-#pragma unroll 4
-                    for (int kr = lane / LPR; kr < 16; kr += RPP) {
-                        const int key = 16 * cw + kr;  // key row of the tile
+                    // a lane converts 16 consecutive bytes of a key row: D / 16 lanes per row, RPP rows a
+                    // pass; all loads first, then convert and store
+                    constexpr int LPR = D / 16, RPP = 32 / LPR, NP = 16 / RPP;
+                    const int e = lane % LPR, r0 = lane / LPR;
+                    uint4 v[NP];
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        const int key = 16 * cw + r0 + i * RPP;
+                        v[i] = *reinterpret_cast<const uint4*>(raw + (key >> brs) * (2 * BR * D) + kv * BR * D +
+                                                               (key & (BR - 1)) * D + e * 16);
+                    }
+                    // the 16 elements are two 16-byte f16 chunks 2e, 2e+1 of column block e / 4; lanes of
+                    // odd (e / 4) store their second chunk first so that each store of 8 lanes covers
+                    // all 32 banks
+                    const bool sw = (e >> 2) & 1;
+                    const int cb = e >> 2, c0 = (2 * e) & 7;
+#pragma unroll
+                    for (int i = 0; i < NP; ++i) {
+                        const int key = 16 * cw + r0 + i * RPP;
                         const int j = k_lo + key;
-                        uint4 o = make_uint4(0, 0, 0, 0);
-                        if (j >= kv_begin && j < kv_end) {
-                            const int bb = key / BR, rr = key - bb * BR;
-                            const uint2 v8 = *reinterpret_cast<const uint2*>(raw + bb * (2 * BR * D) + kv * BR * D +
-                                                                             rr * D + e * 8);
-                            o = e4m3x8_to_f16x8(v8);
+                        const bool in = j >= kv_begin && j < kv_end;
+                        const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
+                        const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
+                        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+                        if (in) {
+                            o0 = e4m3x8_to_f16x8(make_uint2(a0, a1));
+                            o1 = e4m3x8_to_f16x8(make_uint2(b0, b1));
                         }
                         const int line = cb * kBN + key;
-                        put_u4(dst + line * 128 + (((c ^ line) & 7) << 4), o);
+                        uint8_t* row = dst + line * 128;
+                        put_u4(row + ((((c0 + (sw ? 1 : 0)) ^ line) & 7) << 4), o0);
+                        put_u4(row + ((((c0 + (sw ? 0 : 1)) ^ line) & 7) << 4), o1);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -403,6 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
         const int r = tid;  // TMEM lane == query row
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
         const int G = a.G, Hq = a.Hq;
+        // K and V tiles hold the e4m3 values divided by 2^8 (see e4m3x4_to_f16x4)
+        const float qk = a.qk_log2 * kKvUnscale, cape = a.cap_exp * kKvUnscale, capl = a.cap_log2;
         int ms = 0;
         uint32_t mph = 0, tg = 0, items = 0;
         for (;;) {
@@ -435,62 +482,40 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                 const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
                                        (a.has_window && k_lo <= pos_hi - a.window);
                 const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
-                const bool rewrite = need_mask || a.has_cap;
-                float mt = -INFINITY;
-                if (!rewrite) {
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-                    for (int c = 0; c < kBN / 32; ++c) {
-                        uint32_t sv[32];
-                        tmem_ld32(lane_addr + scol + c * 32, sv);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sv[i]) * a.qk_log2);
-                    }
-                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                // one load of the row's 64 logits; transform, mask and max in registers
+                uint32_t sv[kBN];
+                tmem_ld32(lane_addr + scol, sv);
+                tmem_ld32(lane_addr + scol + 32, sv + 32);
+                tmem_ld_wait();
+                float mt;
+                if (need_mask) {
+                    // keys allowed for this row: [lo, hi] relative to the tile
+                    int lo = kv_begin, hi = kv_end - 1;
+                    if (a.has_window) lo = max(lo, pos - a.window + 1);
+                    if (a.causal) hi = min(hi, pos);
+                    lo -= k_lo;
+                    hi -= k_lo;
+                    mt = a.has_cap ? tile_logits<true, true>(sv, qk, capl, cape, lo, hi)
+                                   : tile_logits<false, true>(sv, qk, capl, cape, lo, hi);
                 } else {
-                    const bool cap = a.has_cap;
-#pragma unroll 1
-                    for (int c = 0; c < kBN / 32; ++c) {
-                        uint32_t sv[32];
-                        tmem_ld32(lane_addr + scol + c * 32, sv);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            float v = __uint_as_float(sv[i]);
-                            v = cap ? a.cap_log2 - 2.f * a.cap_log2 * __frcp_rn(1.f + ex2(v * a.cap_exp))
-                                    : v * a.qk_log2;
-                            const int j = k_lo + c * 32 + i;
-                            const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos) &&
-                                             (!a.has_window || j > pos - a.window);
-                            v = (okk || !need_mask) ? v : -INFINITY;
-                            mt = fmaxf(mt, v);
-                            sv[i] = __float_as_uint(v);
-                        }
-                        tmem_st32(lane_addr + scol + c * 32, sv);
-                    }
-                    tmem_st_wait();
+                    mt = a.has_cap ? tile_logits<true, false>(sv, qk, capl, cape, 0, 0)
+                                   : tile_logits<false, false>(sv, qk, capl, cape, 0, 0);
                 }
                 const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
                 const float m_new = need ? fmaxf(m_run, mt) : m_run;
                 const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
                 const float base = m_new == -INFINITY ? 0.f : m_new;
-                const float mul = rewrite ? 1.f : a.qk_log2;
+                // P = 2^(x - base) in f16 over the first 32 S columns (P[i] at column i/2)
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t sv[32], pk[16];
-                    tmem_ld32(lane_addr + scol + c * 32, sv);
-                    tmem_ld_wait();
+                uint32_t pk[kBN / 2];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), mul, -base));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), mul, -base));
-                        ls4[i & 3] += p0 + p1;
-                        pk[i] = pack2<true>(p0, p1);
-                    }
-                    tmem_st16(lane_addr + scol + c * 16, pk);
+                for (int i = 0; i < kBN / 2; ++i) {
+                    const float p0 = ex2(__uint_as_float(sv[2 * i]) - base);
+                    const float p1 = ex2(__uint_as_float(sv[2 * i + 1]) - base);
+                    ls4[i & 3] += p0 + p1;
+                    pk[i] = pack2<true>(p0, p1);
                 }
+                tmem_st32(lane_addr + scol, pk);
                 l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
                 m_run = m_new;
                 if (need && t > 0) {
@@ -519,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
             if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
             tc_fence_after();
             const int rows_used = ntok * G;
-            const float inv = l_run > 0.f ? a.v_scale / l_run : 0.f;
+            const float inv = l_run > 0.f ? a.v_scale * kKvUnscale / l_run : 0.f;
             const int t_tok = q_start + tok0 + r / G;
             const int qh = head * G + r % G;
             uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2);

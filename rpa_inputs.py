@@ -196,7 +196,8 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
 
 
 # ---------------------------------------------------------------- the five workloads
-WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill", "decode_quarter")
+WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill", "decode_quarter",
+             "fp8_window_quarter")
 
 
 def workload(name: str) -> Problem:
@@ -236,6 +237,16 @@ def workload(name: str) -> Problem:
         rng = np.random.default_rng([3, 0])
         ql = rng.integers(1, 64, size=128, endpoint=True)
         kl = rng.integers(256, 16384, size=128, endpoint=True)
+        return build(seed=3, q_lens=ql, kv_lens=kl, num_q_heads=16, num_kv_heads=8,
+                     head_dim=256, page_size=16, pages_per_seq=1024, kv_dtype="fp8_e4m3",
+                     sm_scale=1.0 / 16.0, soft_cap=50.0, k_scale=0.05, v_scale=0.05,
+                     sliding_window=4096, name=name, rng_lengths=rng)
+    if name == "fp8_window_quarter":
+        # the fp8_window workload's first 32 sequences (same lengths and seeds): a
+        # smaller case for profiler captures (K/V ~1.2 GB, still far above L2)
+        rng = np.random.default_rng([3, 0])
+        ql = rng.integers(1, 64, size=128, endpoint=True)[:32]
+        kl = rng.integers(256, 16384, size=128, endpoint=True)[:32]
         return build(seed=3, q_lens=ql, kv_lens=kl, num_q_heads=16, num_kv_heads=8,
                      head_dim=256, page_size=16, pages_per_seq=1024, kv_dtype="fp8_e4m3",
                      sm_scale=1.0 / 16.0, soft_cap=50.0, k_scale=0.05, v_scale=0.05,

@@ -255,25 +255,46 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
             const bool partial = kw < kv_begin || kw + 16 > kv_end;
             uint32_t kb, vb;  // bases of row 0 for the ldmatrix address helpers below
             if constexpr (FP8) {
-                // e4m3 -> f16 into this warp's buffer: [K 16 rows][V 16 rows] of D f16, swizzled
-                for (int i = lane; i < 16 * 2 * (D / 8); i += 32) {
-                    const int row = i / (2 * (D / 8));
-                    const int rem = i % (2 * (D / 8));
-                    const int kv = rem / (D / 8), ch = rem % (D / 8);
-                    const int kk = 16 * w + row;
-                    const int j = kw + row;
-                    uint4 o4 = make_uint4(0, 0, 0, 0);
-                    if (j >= kv_begin && j < kv_end) {
+                // e4m3 -> f16 into this warp's buffer: [K 16 rows][V 16 rows] of D f16, swizzled.
+                // A lane converts 16 consecutive bytes of one (row, K/V) unit; loads are issued
+                // in batches before any conversion so that shared-memory latency overlaps.
+                constexpr int LPR = D / 16, UPP = 32 / LPR, NPASS = 32 / UPP, BATCH = D == 256 ? 2 : 4;
+                static_assert(NPASS % BATCH == 0, "conversion passes");
+                const int e = lane % LPR, u0 = lane / LPR;
+                // lanes of odd (e / 4) store their second 16-byte chunk first: each 8-lane store
+                // phase then covers all 32 banks
+                const bool sw = (e >> 2) & 1;
+#pragma unroll
+                for (int pb = 0; pb < NPASS; pb += BATCH) {
+                    uint4 v[BATCH];
+#pragma unroll
+                    for (int i = 0; i < BATCH; ++i) {
+                        const int u = u0 + (pb + i) * UPP;  // unit: K rows 0..15, then V rows 0..15
+                        const int kv = u >> 4, row = u & 15;
+                        const int kk = 16 * w + row;
                         const int b = kk >> br_shift, r = kk & (BR - 1);
-                        const uint8_t* src = smem + (kv_base - smem0) + b * PBB + kv * BR * D + r * D + ch * 8;
-                        const uint2 raw = *reinterpret_cast<const uint2*>(src);
-                        o4.x = e4m3x2_to_f16x2((uint16_t)(raw.x & 0xffff));
-                        o4.y = e4m3x2_to_f16x2((uint16_t)(raw.x >> 16));
-                        o4.z = e4m3x2_to_f16x2((uint16_t)(raw.y & 0xffff));
-                        o4.w = e4m3x2_to_f16x2((uint16_t)(raw.y >> 16));
+                        v[i] = *reinterpret_cast<const uint4*>(smem + (kv_base - smem0) + b * PBB + kv * BR * D +
+                                                               r * D + e * 16);
                     }
-                    *reinterpret_cast<uint4*>(conv + kv * (16 * D * 2) + row * (D * 2) +
-                                              (((ch ^ row) & 7) | (ch & ~7)) * 16) = o4;
+#pragma unroll
+                    for (int i = 0; i < BATCH; ++i) {
+                        const int u = u0 + (pb + i) * UPP;
+                        const int kv = u >> 4, row = u & 15;
+                        const int j = kw + row;
+                        const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
+                        const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
+                        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+                        if (j >= kv_begin && j < kv_end) {
+                            o0 = make_uint4(e4m3x2_to_f16x2((uint16_t)(a0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(a0 >> 16)),
+                                            e4m3x2_to_f16x2((uint16_t)(a1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(a1 >> 16)));
+                            o1 = make_uint4(e4m3x2_to_f16x2((uint16_t)(b0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(b0 >> 16)),
+                                            e4m3x2_to_f16x2((uint16_t)(b1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(b1 >> 16)));
+                        }
+                        uint8_t* rowp = conv + kv * (16 * D * 2) + row * (D * 2);
+                        const int c1 = 2 * e + (sw ? 1 : 0), c2 = 2 * e + (sw ? 0 : 1);
+                        *reinterpret_cast<uint4*>(rowp + (((c1 ^ row) & 7) | (c1 & ~7)) * 16) = o0;
+                        *reinterpret_cast<uint4*>(rowp + (((c2 ^ row) & 7) | (c2 & ~7)) * 16) = o1;
+                    }
                 }
                 __syncwarp();
                 kb = smem_u32(conv);

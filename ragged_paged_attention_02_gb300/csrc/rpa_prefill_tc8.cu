@@ -35,8 +35,12 @@ namespace {
 
 constexpr int kM = kTcRows;   // query rows per tile = TMEM lanes
 constexpr int kBN = 64;       // keys per K/V tile
-constexpr int kThreads = 320; // warps 0-3 softmax, 4-7 convert, 8 producer, 9 MMA
-constexpr int kProducer = 8, kMma = 9;
+// warps 0-7 softmax (two per TMEM lane quadrant, one per half of the key tile), 8-11 convert,
+// 12 producer, 13 MMA
+constexpr int kThreads = 448;
+constexpr int kConv0 = 8, kProducer = 12, kMma = 13;
+// 4 warps share an SM sub-partition's 16384 registers: at most 128 a thread (launch bound 512)
+constexpr int kRegBoundThreads = 512;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -45,8 +49,8 @@ enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, 
 template <int D>
 struct G8 {
     static constexpr int CB = D / 64;                  // 128-byte column blocks of a 16-bit row
-    static constexpr int ROUNDS = D / 128;             // Q staging rounds (two column blocks each)
-    static constexpr int QSTAGE = 2 * kM * 128;        // Q staging: 2 column blocks x 128 rows
+    static constexpr int ROUNDS = D / 64;              // Q staging rounds (one column block each)
+    static constexpr int QSTAGE = kM * 128;            // Q staging: one column block x 128 rows
     static constexpr int RAW = kBN * 2 * D;            // one raw fp8 stage (K and V)
     static constexpr int T16 = CB * kBN * 128;         // one f16 K (or V) tile
     static constexpr int DATA = QSTAGE + 2 * RAW + 4 * T16;
@@ -55,7 +59,7 @@ struct G8 {
     static constexpr uint32_t TM_S0 = D / 2, TM_S1 = D / 2 + kBN;
     static constexpr uint32_t TM_O = D / 2 + 2 * kBN;  // O: D columns
     static_assert(D / 2 + 2 * kBN + D <= kTmemCols, "TMEM budget");
-    static_assert(DATA + 1024 <= 227 * 1024, "shared memory budget");
+    static_assert(DATA + 1024 + 4096 <= 227 * 1024, "shared memory budget (dynamic + static)");
 };
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
@@ -80,13 +84,63 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 b) {
     return o;
 }
 
-// Logits of one 64-key tile in the log2 domain, in place: scale (or soft cap), then
-// keys outside [lo, hi] of the tile to -inf; returns the row max.
-template <bool CAP, bool MASK>
+// e4m3 x 8 -> f16 x 8 with the hardware conversion (exact values)
+__device__ __forceinline__ uint4 e4m3x8_to_f16x8_hw(uint32_t w0, uint32_t w1) {
+    return make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
+                      e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
+}
+
+// One converter warp's 16 key rows (16 cw .. 16 cw + 15) of one half (K or V) of a raw stage
+// ([run][K | V][BR rows][D bytes]; `raw` points at the half's first run) into a 128-byte
+// swizzled f16 tile [D / 64][64 rows][128 B].  Keys outside [kv_begin, kv_end) become zero.
+// HW: exact hardware conversion, else the integer placement (value / 2^8).  A lane converts 16
+// consecutive bytes of a row (D / 16 lanes a row, RPP rows a pass); all loads are issued first.
+template <int D, bool HW>
+__device__ __forceinline__ void convert_rows(const uint8_t* raw, uint8_t* dst, int cw, int lane, int brs, int k_lo,
+                                             int kv_begin, int kv_end) {
+    constexpr int LPR = D / 16, RPP = 32 / LPR, NP = 16 / RPP;
+    const int BR = 1 << brs;
+    const int e = lane % LPR, r0 = lane / LPR;
+    uint4 v[NP];
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const int key = 16 * cw + r0 + i * RPP;
+        v[i] = *reinterpret_cast<const uint4*>(raw + (key >> brs) * (2 * BR * D) + (key & (BR - 1)) * D + e * 16);
+    }
+    // the 16 elements are f16 chunks 2e, 2e+1 of column block e / 4; lanes of odd (e / 4) store
+    // their second chunk first so that each store of 8 lanes covers all 32 banks
+    const bool sw = (e >> 2) & 1;
+    const int cb = e >> 2, c0 = (2 * e) & 7;
+#pragma unroll
+    for (int i = 0; i < NP; ++i) {
+        const int key = 16 * cw + r0 + i * RPP;
+        const int j = k_lo + key;
+        const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
+        const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
+        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+        if (j >= kv_begin && j < kv_end) {
+            if constexpr (HW) {
+                o0 = e4m3x8_to_f16x8_hw(a0, a1);
+                o1 = e4m3x8_to_f16x8_hw(b0, b1);
+            } else {
+                o0 = e4m3x8_to_f16x8(make_uint2(a0, a1));
+                o1 = e4m3x8_to_f16x8(make_uint2(b0, b1));
+            }
+        }
+        const int line = cb * kBN + key;
+        uint8_t* row = dst + line * 128;
+        put_u4(row + ((((c0 + (sw ? 1 : 0)) ^ line) & 7) << 4), o0);
+        put_u4(row + ((((c0 + (sw ? 0 : 1)) ^ line) & 7) << 4), o1);
+    }
+}
+
+// Logits of N keys of a row in the log2 domain, in place: scale (or soft cap), then keys
+// outside [lo, hi] (relative to the first) to -inf; returns their max.
+template <bool CAP, bool MASK, int N>
 __device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl, float cape, int lo, int hi) {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-    for (int i = 0; i < kBN; ++i) {
+    for (int i = 0; i < N; ++i) {
         float v = __uint_as_float(sv[i]);
         if constexpr (CAP)
             v = capl - 2.f * capl * rcp_approx(1.f + ex2(v * cape));  // cap * tanh(x / cap), log2 domain
@@ -100,7 +154,7 @@ __device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl,
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_constant__ CUtensorMap kvmap,
+__global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __grid_constant__ CUtensorMap kvmap,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const TcParams p) {
     using Gm = G8<D>;
@@ -110,6 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
     __shared__ __align__(8) uint64_t raw_full[2], raw_empty[2];
     __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
     __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done, o_full, o_free;
+    __shared__ __align__(8) uint64_t xchg[4];  // per lane quadrant: the two softmax warps' row maxima / sums
+    __shared__ float xm[2][2][kM];             // [tile parity][key half][row] partial row maxima
+    __shared__ float xl[2][kM];                // [key half][row] partial row sums
     __shared__ uint32_t tmem_base_sh;
     __shared__ int meta[2][16];
 
@@ -127,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&meta_full[i]), 1);
-            mbar_init(smem_u32(&meta_free[i]), 9);  // 4 softmax + 4 converter warps + MMA thread
+            mbar_init(smem_u32(&meta_free[i]), 13);  // 8 softmax + 4 converter warps + MMA thread
             mbar_init(smem_u32(&raw_full[i]), 1);
             mbar_init(smem_u32(&raw_empty[i]), 4);
             mbar_init(smem_u32(&k_full[i]), 4);
@@ -135,15 +192,16 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
             mbar_init(smem_u32(&v_full[i]), 4);
             mbar_init(smem_u32(&v_empty[i]), 1);
             mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&p_full[i]), 4);
+            mbar_init(smem_u32(&p_full[i]), 8);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 64);
         mbar_init(smem_u32(&q_full), 1);
         mbar_init(smem_u32(&q_empty), 4);
         mbar_init(smem_u32(&q_ready), 4);
         mbar_init(smem_u32(&qt_free), 1);
         mbar_init(smem_u32(&pv_done), 1);
         mbar_init(smem_u32(&o_full), 1);
-        mbar_init(smem_u32(&o_free), 4);
+        mbar_init(smem_u32(&o_free), 8);
         fence_mbar_init();
     }
     if (warp == kMma) tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
@@ -162,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
         const int BR = p.BR, ps = a.ps, G = a.G, Tq = p.Tq;
         const int runs = kBN / BR;
         const uint32_t run_bytes = (uint32_t)(2 * BR * D);
-        const uint32_t q_round_bytes = (uint32_t)(2 * G * Tq * 128);
+        const uint32_t q_round_bytes = (uint32_t)(G * Tq * 128);
         int s = 0, ms = 0;
         uint32_t ph = 0, mph = 0, qph = 0;
         bool ok = true;
@@ -207,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                 ms = 0;
                 mph ^= 1u;
             }
-            // Q: two column blocks per round through the staging buffer
+            // Q: one column block per round through the staging buffer
             for (int rd = 0; rd < Gm::ROUNDS && ok; ++rd) {
                 if (!mbar_wait(smem_u32(&q_empty), qph ^ 1u, ctrl, tmo)) {
                     ok = false;
@@ -216,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                 const uint32_t qfb = smem_u32(&q_full);
                 if (lane == 0) mbar_arrive_expect_tx(qfb, q_round_bytes);
                 __syncwarp();
-                if (lane < 2)
-                    tma_load_3d(q_stage + lane * (kM * 128), &qmap, qfb, (2 * rd + lane) * 64, item.head * G,
+                if (lane == 0)
+                    tma_load_3d(q_stage, &qmap, qfb, rd * 64, item.head * G,
                                 q_start + item.tok0);
                 qph ^= 1u;
             }
@@ -256,10 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
             if (!ok) break;
             it = __shfl_sync(0xffffffffu, nxt, 0);
         }
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= kConv0 && warp < kConv0 + 4) {
         // =============================== converters ===============================
-        const int cw = warp - 4;             // converter warp 0..3
-        const int r = tid - 128;             // TMEM lane (query row) for the Q conversion
+        const int cw = warp - kConv0;        // converter warp 0..3 == its TMEM lane quadrant
+        const int r = tid - kConv0 * 32;     // TMEM lane (query row) for the Q conversion
         const uint32_t lane_addr = tmem + ((uint32_t)(cw * 32) << 16);
         const int BR = p.BR, brs = __ffs(BR) - 1;
         int s = 0, ms = 0;
@@ -286,10 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                     break;
                 }
                 qph ^= 1u;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
+                {
                     uint32_t qv[32];
-                    const uint8_t* row = smem + (q_stage - smem0) + half * (kM * 128) + r * 128;
+                    const uint8_t* row = smem + (q_stage - smem0) + r * 128;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const uint4 w = *reinterpret_cast<const uint4*>(row + (((c ^ r) & 7) << 4));
@@ -298,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                         for (int k = 0; k < 4; ++k)
                             qv[4 * c + k] = pack2<true>(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xffff0000u));
                     }
-                    tmem_st32(lane_addr + Gm::TM_Q + (2 * rd + half) * 32, qv);
+                    tmem_st32(lane_addr + Gm::TM_Q + rd * 32, qv);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&q_empty));
@@ -308,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&q_ready));
-            // ---- K / V tiles: this warp converts keys [16cw, 16cw + 16) of each tile, one row per pass
+            // ---- K / V tiles: this warp converts keys [16cw, 16cw + 16) of each tile
             for (int t = 0; t < nt; ++t, ++tg) {
                 const int b2 = tg & 1;
                 const uint32_t par = (tg >> 1) & 1u;
@@ -319,51 +376,22 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                 }
                 const uint8_t* raw = smem + (raw_base - smem0) + s * Gm::RAW;
                 const int k_lo = key0 + t * kBN;
-#pragma unroll 1
-                for (int kv = 0; kv < 2; ++kv) {
-                    if (kv == 1 && !mbar_wait(smem_u32(&v_empty[b2]), par ^ 1u, ctrl, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* dst = smem + ((kv ? v16_base : k16_base) - smem0) + b2 * Gm::T16;
-                    // a lane converts 16 consecutive bytes of a key row: D / 16 lanes per row, RPP rows a
-                    // pass; all loads first, then convert and store
-                    constexpr int LPR = D / 16, RPP = 32 / LPR, NP = 16 / RPP;
-                    const int e = lane % LPR, r0 = lane / LPR;
-                    uint4 v[NP];
-#pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        const int key = 16 * cw + r0 + i * RPP;
-                        v[i] = *reinterpret_cast<const uint4*>(raw + (key >> brs) * (2 * BR * D) + kv * BR * D +
-                                                               (key & (BR - 1)) * D + e * 16);
-                    }
-                    // the 16 elements are two 16-byte f16 chunks 2e, 2e+1 of column block e / 4; lanes of
-                    // odd (e / 4) store their second chunk first so that each store of 8 lanes covers
-                    // all 32 banks
-                    const bool sw = (e >> 2) & 1;
-                    const int cb = e >> 2, c0 = (2 * e) & 7;
-#pragma unroll
-                    for (int i = 0; i < NP; ++i) {
-                        const int key = 16 * cw + r0 + i * RPP;
-                        const int j = k_lo + key;
-                        const bool in = j >= kv_begin && j < kv_end;
-                        const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
-                        const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
-                        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                        if (in) {
-                            o0 = e4m3x8_to_f16x8(make_uint2(a0, a1));
-                            o1 = e4m3x8_to_f16x8(make_uint2(b0, b1));
-                        }
-                        const int line = cb * kBN + key;
-                        uint8_t* row = dst + line * 128;
-                        put_u4(row + ((((c0 + (sw ? 1 : 0)) ^ line) & 7) << 4), o0);
-                        put_u4(row + ((((c0 + (sw ? 0 : 1)) ^ line) & 7) << 4), o1);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(kv ? &v_full[b2] : &k_full[b2]));
+                // K exactly (hardware conversion), then V as value / 2^8 (integer placement): the
+                // two halves load the special-function and the integer pipes about evenly
+                convert_rows<D, true>(raw, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, brs, k_lo, kv_begin,
+                                      kv_end);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&k_full[b2]));
+                if (!mbar_wait(smem_u32(&v_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+                convert_rows<D, false>(raw + BR * D, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, brs, k_lo,
+                                       kv_begin, kv_end);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&v_full[b2]));
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&raw_empty[s]));
                 if (++s == 2) {
@@ -445,13 +473,20 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
         __syncwarp();
     } else {
         // =============================== softmax warps ===============================
-        const int r = tid;  // TMEM lane == query row
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+        // warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key half w / 4 of every tile
+        // (32 logits a row); the two warps of a quadrant exchange row maxima every tile and row
+        // sums at the item's end through shared memory and the quadrant's xchg barrier
+        const int q4 = warp & 3, half = warp >> 2;
+        const int r = q4 * 32 + lane;  // TMEM lane == query row
+        const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
+        const uint32_t xb = smem_u32(&xchg[q4]);
+        constexpr int HC = kBN / 2;  // logits of a row this thread owns
+        constexpr int HO = D / 2;    // O columns this thread owns
         const int G = a.G, Hq = a.Hq;
-        // K and V tiles hold the e4m3 values divided by 2^8 (see e4m3x4_to_f16x4)
-        const float qk = a.qk_log2 * kKvUnscale, cape = a.cap_exp * kKvUnscale, capl = a.cap_log2;
+        // K tiles hold the exact values, V tiles the values divided by 2^8 (see convert_rows)
+        const float qk = a.qk_log2, capl = a.cap_log2, cape = a.cap_exp;
         int ms = 0;
-        uint32_t mph = 0, tg = 0, items = 0;
+        uint32_t mph = 0, tg = 0, items = 0, xph = 0;
         for (;;) {
             if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
             const int* mm = meta[ms];
@@ -481,57 +516,66 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                 const bool partial = k_lo < kv_begin || k_lo + kBN > kv_end;
                 const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
                                        (a.has_window && k_lo <= pos_hi - a.window);
-                const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
-                // one load of the row's 64 logits; transform, mask and max in registers
-                uint32_t sv[kBN];
+                const uint32_t scol = (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * HC;
+                // this half's 32 logits of the row; transform, mask and max in registers
+                uint32_t sv[HC];
                 tmem_ld32(lane_addr + scol, sv);
-                tmem_ld32(lane_addr + scol + 32, sv + 32);
                 tmem_ld_wait();
-                float mt;
+                float mh;
                 if (need_mask) {
-                    // keys allowed for this row: [lo, hi] relative to the tile
+                    // keys allowed for this row: [lo, hi] relative to the half's first key
                     int lo = kv_begin, hi = kv_end - 1;
                     if (a.has_window) lo = max(lo, pos - a.window + 1);
                     if (a.causal) hi = min(hi, pos);
-                    lo -= k_lo;
-                    hi -= k_lo;
-                    mt = a.has_cap ? tile_logits<true, true>(sv, qk, capl, cape, lo, hi)
-                                   : tile_logits<false, true>(sv, qk, capl, cape, lo, hi);
+                    lo -= k_lo + half * HC;
+                    hi -= k_lo + half * HC;
+                    mh = a.has_cap ? tile_logits<true, true, HC>(sv, qk, capl, cape, lo, hi)
+                                   : tile_logits<false, true, HC>(sv, qk, capl, cape, lo, hi);
                 } else {
-                    mt = a.has_cap ? tile_logits<true, false>(sv, qk, capl, cape, 0, 0)
-                                   : tile_logits<false, false>(sv, qk, capl, cape, 0, 0);
+                    mh = a.has_cap ? tile_logits<true, false, HC>(sv, qk, capl, cape, 0, 0)
+                                   : tile_logits<false, false, HC>(sv, qk, capl, cape, 0, 0);
                 }
+                // row max over both halves
+                xm[tg & 1][half][r] = mh;
+                mbar_arrive(xb);
+                if (!mbar_wait(xb, xph, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                xph ^= 1u;
+                const float mt = fmaxf(mh, xm[tg & 1][half ^ 1][r]);
                 const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
                 const float m_new = need ? fmaxf(m_run, mt) : m_run;
                 const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
                 const float base = m_new == -INFINITY ? 0.f : m_new;
-                // P = 2^(x - base) in f16 over the first 32 S columns (P[i] at column i/2)
+                // P = 2^(x - base) in f16 over this half's first 16 S columns (P[i] at column i/2)
                 float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-                uint32_t pk[kBN / 2];
+                uint32_t pk[HC / 2];
 #pragma unroll
-                for (int i = 0; i < kBN / 2; ++i) {
+                for (int i = 0; i < HC / 2; ++i) {
                     const float p0 = ex2(__uint_as_float(sv[2 * i]) - base);
                     const float p1 = ex2(__uint_as_float(sv[2 * i + 1]) - base);
                     ls4[i & 3] += p0 + p1;
                     pk[i] = pack2<true>(p0, p1);
                 }
-                tmem_st32(lane_addr + scol, pk);
+                tmem_st16(lane_addr + (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * (HC / 2), pk);
                 l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
                 m_run = m_new;
                 if (need && t > 0) {
+                    // this warp's half of the O row holds the item's PVs up to tile t-1
                     if (!mbar_wait(smem_u32(&pv_done), (tg - 1) & 1u, ctrl, tmo)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
+                    for (int c = 0; c < HO / 32; ++c) {
                         uint32_t ov[32];
-                        tmem_ld32(lane_addr + Gm::TM_O + c * 32, ov);
+                        tmem_ld32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(lane_addr + Gm::TM_O + c * 32, ov);
+                        tmem_st32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
                     }
                 }
                 tmem_st_wait();
@@ -540,18 +584,23 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc8(const __grid_cons
                 if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
             }
             if (!ok) break;
-            // ---- epilogue: o = O * v_scale / l
+            // ---- epilogue: o = O * v_scale / l, this warp's half of the row
+            xl[half][r] = l_run;
+            mbar_arrive(xb);
+            if (!mbar_wait(xb, xph, ctrl, tmo)) break;
+            xph ^= 1u;
+            const float l_row = l_run + xl[half ^ 1][r];
             if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
             tc_fence_after();
             const int rows_used = ntok * G;
-            const float inv = l_run > 0.f ? a.v_scale * kKvUnscale / l_run : 0.f;
+            const float inv = l_row > 0.f ? a.v_scale * kKvUnscale / l_row : 0.f;
             const int t_tok = q_start + tok0 + r / G;
             const int qh = head * G + r % G;
-            uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2);
+            uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2) + half * HO * 2;
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < HO / 32; ++c) {
                 uint32_t ov[32];
-                tmem_ld32(lane_addr + Gm::TM_O + c * 32, ov);
+                tmem_ld32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
                 tmem_ld_wait();
                 if (r < rows_used) {
 #pragma unroll

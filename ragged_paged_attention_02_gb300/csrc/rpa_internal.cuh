@@ -244,6 +244,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
     return y;
 }
 
+// tanh(x) on the special-function unit (hardware approximation, relative error about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Pack two floats into a bf16x2 / f16x2 register (round to nearest even).
 template <bool F16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {

@@ -137,13 +137,13 @@ __device__ __forceinline__ void convert_rows(const uint8_t* raw, uint8_t* dst, i
 // Logits of N keys of a row in the log2 domain, in place: scale (or soft cap), then keys
 // outside [lo, hi] (relative to the first) to -inf; returns their max.
 template <bool CAP, bool MASK, int N>
-__device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl, float cape, int lo, int hi) {
+__device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl, float capt, int lo, int hi) {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int i = 0; i < N; ++i) {
         float v = __uint_as_float(sv[i]);
         if constexpr (CAP)
-            v = capl - 2.f * capl * rcp_approx(1.f + ex2(v * cape));  // cap * tanh(x / cap), log2 domain
+            v = capl * tanh_approx(v * capt);  // cap * tanh(x / cap), log2 domain
         else
             v *= qk;
         if constexpr (MASK) v = (i >= lo && i <= hi) ? v : -INFINITY;
@@ -483,8 +483,11 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
         constexpr int HC = kBN / 2;  // logits of a row this thread owns
         constexpr int HO = D / 2;    // O columns this thread owns
         const int G = a.G, Hq = a.Hq;
-        // K tiles hold the exact values, V tiles the values divided by 2^8 (see convert_rows)
-        const float qk = a.qk_log2, capl = a.cap_log2, cape = a.cap_exp;
+        // K tiles hold the exact values, V tiles the values divided by 2^8 (see convert_rows).
+        // Soft cap: cap log2(e) tanh(s sm_scale k_scale / cap) with the hardware tanh (relative
+        // error about 2^-11, the order of the f16 rounding of P); its argument factor is
+        // cap_exp / (2 log2(e)).
+        const float qk = a.qk_log2, capl = a.cap_log2, cape = a.cap_exp * (0.5f / 1.4426950408889634f);
         int ms = 0;
         uint32_t mph = 0, tg = 0, items = 0, xph = 0;
         for (;;) {
@@ -503,6 +506,9 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             }
             const int pos = kl - ql + tok0 + r / G;
             const int pos_lo = kl - ql + tok0, pos_hi = kl - ql + tok0 + ntok - 1;
+            // a quadrant whose 32 rows are all past the item's rows computes nothing: its P and
+            // O rows are never stored (it still takes part in the barriers, in order)
+            const bool idle = q4 * 32 >= ntok * G;
             float m_run = -INFINITY, l_run = 0.f;
             bool ok = true;
             for (int t = 0; t < nt; ++t, ++tg) {
@@ -512,6 +518,11 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     break;
                 }
                 tc_fence_after();
+                if (idle) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
+                    continue;
+                }
                 const int k_lo = key0 + t * kBN;
                 const bool partial = k_lo < kv_begin || k_lo + kBN > kv_end;
                 const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
@@ -584,6 +595,13 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
             }
             if (!ok) break;
+            if (idle) {
+                if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&o_free));
+                ++items;
+                continue;
+            }
             // ---- epilogue: o = O * v_scale / l, this warp's half of the row
             xl[half][r] = l_run;
             mbar_arrive(xb);

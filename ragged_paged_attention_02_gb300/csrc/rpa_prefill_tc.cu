@@ -371,17 +371,28 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 const bool rewrite = need_mask || a.has_cap;
                 float mt = -INFINITY;
                 if (!rewrite) {
-                    // interior tile, no cap: the max of the scaled logits (four independent chains)
+                    // interior tile, no cap: the extreme raw logit times the scale (the max for a
+                    // positive scale, the min for a negative one); three-input max/min, four chains
+                    const bool pos_scale = a.qk_log2 >= 0.f;
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    float n4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
 #pragma unroll 1
                     for (int c = 0; c < kBN / 32; ++c) {
                         uint32_t sv[32];
                         tmem_ld32(lane_addr + scol + c * 32, sv);
                         tmem_ld_wait();
+                        if (pos_scale) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], __uint_as_float(sv[i]) * a.qk_log2);
+                            for (int i = 0; i < 16; ++i)
+                                m4[i & 3] = fmax3(m4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                n4[i & 3] = fmin3(n4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+                        }
                     }
-                    mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    mt = pos_scale ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.qk_log2
+                                   : fminf(fminf(n4[0], n4[1]), fminf(n4[2], n4[3])) * a.qk_log2;
                 } else {
                     const bool cap = a.has_cap;
 #pragma unroll 1
@@ -412,7 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 const float base = m_new == -INFINITY ? 0.f : m_new;
                 // pass 2: p = 2^(x - base) in bf16 over the consumed S columns (P[i] at column i/2)
                 const float mul = rewrite ? 1.f : a.qk_log2;
-                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                // x * mul - base and the running sums on pairs of lanes (f32x2)
+                const uint64_t mul2 = f32x2(mul, mul), nbase2 = f32x2(-base, -base);
+                uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll 1
                 for (int c = 0; c < kBN / 32; ++c) {
                     uint32_t sv[32], pk[16];
@@ -420,14 +433,20 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float p0 = ex2(fmaf(__uint_as_float(sv[2 * i]), mul, -base));
-                        const float p1 = ex2(fmaf(__uint_as_float(sv[2 * i + 1]), mul, -base));
-                        ls4[i & 3] += p0 + p1;
+                        float x0, x1;
+                        f32x2_split(ffma2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), mul2, nbase2),
+                                    x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        const uint64_t pp = f32x2(p0, p1);
+                        ls2[i & 1] = fadd2(ls2[i & 1], pp);
                         pk[i] = pack2<false>(p0, p1);
                     }
                     tmem_st16(lane_addr + scol + c * 16, pk);
                 }
-                const float lsum = (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+                float la, lb, lc, ld;
+                f32x2_split(ls2[0], la, lb);
+                f32x2_split(ls2[1], lc, ld);
+                const float lsum = (la + lb) + (lc + ld);
                 l_run = l_run * alpha + lsum;
                 m_run = m_new;
                 if (need && t > 0) {

@@ -139,16 +139,25 @@ __device__ __forceinline__ void convert_rows(const uint8_t* raw, uint8_t* dst, i
 template <bool CAP, bool MASK, int N>
 __device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl, float capt, int lo, int hi) {
     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    const uint64_t qk2 = f32x2(qk, qk), capl2 = f32x2(capl, capl), capt2 = f32x2(capt, capt);
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        float v = __uint_as_float(sv[i]);
-        if constexpr (CAP)
-            v = capl * tanh_approx(v * capt);  // cap * tanh(x / cap), log2 domain
-        else
-            v *= qk;
-        if constexpr (MASK) v = (i >= lo && i <= hi) ? v : -INFINITY;
-        m4[i & 3] = fmaxf(m4[i & 3], v);
-        sv[i] = __float_as_uint(v);
+    for (int i = 0; i < N; i += 2) {
+        uint64_t v2 = f32x2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+        float v0, v1;
+        if constexpr (CAP) {
+            // cap * tanh(x / cap), log2 domain
+            f32x2_split(fmul2(v2, capt2), v0, v1);
+            f32x2_split(fmul2(f32x2(tanh_approx(v0), tanh_approx(v1)), capl2), v0, v1);
+        } else {
+            f32x2_split(fmul2(v2, qk2), v0, v1);
+        }
+        if constexpr (MASK) {
+            v0 = (i >= lo && i <= hi) ? v0 : -INFINITY;
+            v1 = (i + 1 >= lo && i + 1 <= hi) ? v1 : -INFINITY;
+        }
+        m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], v0, v1);
+        sv[i] = __float_as_uint(v0);
+        sv[i + 1] = __float_as_uint(v1);
     }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
@@ -560,17 +569,23 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
                 const float base = m_new == -INFINITY ? 0.f : m_new;
                 // P = 2^(x - base) in f16 over this half's first 16 S columns (P[i] at column i/2)
-                float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+                // x - base and the running sums on pairs of lanes (f32x2)
+                const uint64_t nbase2 = f32x2(-base, -base);
+                uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
                 uint32_t pk[HC / 2];
 #pragma unroll
                 for (int i = 0; i < HC / 2; ++i) {
-                    const float p0 = ex2(__uint_as_float(sv[2 * i]) - base);
-                    const float p1 = ex2(__uint_as_float(sv[2 * i + 1]) - base);
-                    ls4[i & 3] += p0 + p1;
+                    float x0, x1;
+                    f32x2_split(fadd2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), nbase2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
                     pk[i] = pack2<true>(p0, p1);
                 }
                 tmem_st16(lane_addr + (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * (HC / 2), pk);
-                l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
+                float la, lb, lc, ld;
+                f32x2_split(ls2[0], la, lb);
+                f32x2_split(ls2[1], lc, ld);
+                l_run = l_run * alpha + ((la + lb) + (lc + ld));
                 m_run = m_new;
                 if (need && t > 0) {
                     // this warp's half of the O row holds the item's PVs up to tile t-1

@@ -66,6 +66,19 @@ struct TcGeom {
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
+// p = 2^(x * mul - base) for the 32 logits of one S chunk: bf16 pairs into pk, sums into ls2
+__device__ __forceinline__ void exp_chunk(const uint32_t* sv, uint64_t mul2, uint64_t nbase2, uint64_t* ls2,
+                                          uint32_t* pk) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float x0, x1;
+        f32x2_split(ffma2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), mul2, nbase2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
+        pk[i] = pack2<false>(p0, p1);
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_constant__ CUtensorMap kvmap,
                                                               const __grid_constant__ CUtensorMap qmap,
@@ -370,29 +383,59 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 // written back to TMEM so that pass 2 only exponentiates
                 const bool rewrite = need_mask || a.has_cap;
                 float mt = -INFINITY;
+                uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+                bool need;
+                float alpha, m_new;
                 if (!rewrite) {
-                    // interior tile, no cap: the extreme raw logit times the scale (the max for a
-                    // positive scale, the min for a negative one); three-input max/min, four chains
+                    // interior tile, no cap.  Pass 1: the extreme raw logit times the scale (the max
+                    // for a positive scale, the min for a negative one), chunks 2, 3 then 0, 1, two
+                    // loads in flight; chunks 0 and 1 stay in registers for pass 2
                     const bool pos_scale = a.qk_log2 >= 0.f;
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                     float n4[4] = {INFINITY, INFINITY, INFINITY, INFINITY};
-#pragma unroll 1
-                    for (int c = 0; c < kBN / 32; ++c) {
-                        uint32_t sv[32];
-                        tmem_ld32(lane_addr + scol + c * 32, sv);
+                    uint32_t sa[32], sb[32];
+#pragma unroll
+                    for (int h = 1; h >= 0; --h) {
+                        tmem_ld32(lane_addr + scol + (2 * h) * 32, sa);
+                        tmem_ld32(lane_addr + scol + (2 * h + 1) * 32, sb);
                         tmem_ld_wait();
                         if (pos_scale) {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                m4[i & 3] = fmax3(m4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+                            for (int i = 0; i < 16; ++i) {
+                                m4[i & 3] = fmax3(m4[i & 3], __uint_as_float(sa[2 * i]), __uint_as_float(sa[2 * i + 1]));
+                                m4[(i + 2) & 3] = fmax3(m4[(i + 2) & 3], __uint_as_float(sb[2 * i]), __uint_as_float(sb[2 * i + 1]));
+                            }
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                n4[i & 3] = fmin3(n4[i & 3], __uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1]));
+                            for (int i = 0; i < 16; ++i) {
+                                n4[i & 3] = fmin3(n4[i & 3], __uint_as_float(sa[2 * i]), __uint_as_float(sa[2 * i + 1]));
+                                n4[(i + 2) & 3] = fmin3(n4[(i + 2) & 3], __uint_as_float(sb[2 * i]), __uint_as_float(sb[2 * i + 1]));
+                            }
                         }
                     }
                     mt = pos_scale ? fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.qk_log2
                                    : fminf(fminf(n4[0], n4[1]), fminf(n4[2], n4[3])) * a.qk_log2;
+                    // lazy rescale: move the running max only when it grows by more than 2^8
+                    need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);  // false if mt == -inf
+                    m_new = need ? fmaxf(m_run, mt) : m_run;
+                    alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
+                    const float base = m_new == -INFINITY ? 0.f : m_new;
+                    // pass 2: P = 2^(x - base) in bf16 over the consumed S columns (P[i] at column
+                    // i/2): chunks 0 and 1 from registers (their P lands in columns 0-31, S chunk 0),
+                    // chunks 2 and 3 reloaded while chunk 1 is exponentiated
+                    const uint64_t mul2 = f32x2(a.qk_log2, a.qk_log2), nbase2 = f32x2(-base, -base);
+                    uint32_t pk[16];
+                    exp_chunk(sa, mul2, nbase2, ls2, pk);
+                    tmem_st16(lane_addr + scol, pk);
+                    tmem_ld32(lane_addr + scol + 64, sa);
+                    exp_chunk(sb, mul2, nbase2, ls2, pk);
+                    tmem_st16(lane_addr + scol + 16, pk);
+                    tmem_ld32(lane_addr + scol + 96, sb);
+                    tmem_ld_wait();
+                    exp_chunk(sa, mul2, nbase2, ls2, pk);
+                    tmem_st16(lane_addr + scol + 32, pk);
+                    exp_chunk(sb, mul2, nbase2, ls2, pk);
+                    tmem_st16(lane_addr + scol + 48, pk);
                 } else {
                     const bool cap = a.has_cap;
 #pragma unroll 1
@@ -415,33 +458,20 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                         tmem_st32(lane_addr + scol + c * 32, sv);
                     }
                     tmem_st_wait();
-                }
-                // lazy rescale: move the running max only when it grows by more than 2^8
-                const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);  // false if mt == -inf
-                const float m_new = need ? fmaxf(m_run, mt) : m_run;
-                const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
-                const float base = m_new == -INFINITY ? 0.f : m_new;
-                // pass 2: p = 2^(x - base) in bf16 over the consumed S columns (P[i] at column i/2)
-                const float mul = rewrite ? 1.f : a.qk_log2;
-                // x * mul - base and the running sums on pairs of lanes (f32x2)
-                const uint64_t mul2 = f32x2(mul, mul), nbase2 = f32x2(-base, -base);
-                uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+                    need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
+                    m_new = need ? fmaxf(m_run, mt) : m_run;
+                    alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
+                    const float base = m_new == -INFINITY ? 0.f : m_new;
+                    // pass 2 over the rewritten (already scaled and masked) logits
+                    const uint64_t mul2 = f32x2(1.f, 1.f), nbase2 = f32x2(-base, -base);
 #pragma unroll 1
-                for (int c = 0; c < kBN / 32; ++c) {
-                    uint32_t sv[32], pk[16];
-                    tmem_ld32(lane_addr + scol + c * 32, sv);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        f32x2_split(ffma2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), mul2, nbase2),
-                                    x0, x1);
-                        const float p0 = ex2(x0), p1 = ex2(x1);
-                        const uint64_t pp = f32x2(p0, p1);
-                        ls2[i & 1] = fadd2(ls2[i & 1], pp);
-                        pk[i] = pack2<false>(p0, p1);
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        uint32_t sv[32], pk[16];
+                        tmem_ld32(lane_addr + scol + c * 32, sv);
+                        tmem_ld_wait();
+                        exp_chunk(sv, mul2, nbase2, ls2, pk);
+                        tmem_st16(lane_addr + scol + c * 16, pk);
                     }
-                    tmem_st16(lane_addr + scol + c * 16, pk);
                 }
                 float la, lb, lc, ld;
                 f32x2_split(ls2[0], la, lb);

@@ -52,10 +52,12 @@ constexpr int kMaxSort = 8192;     // units sorted by cost on the device
 constexpr int kSeqSmem = 4096;     // sequences whose plan scratch fits in shared memory
 constexpr int kPlanThreads = 1024;
 // rates of the SM-split model (planner): FLOP/ns of one SM on prefill, B/ns one SM can
-// stream in the decode kernel, and HBM B/ns
-constexpr int kPfSmGflopsTc = 7600;
+// stream in the decode kernel, and HBM B/ns.  The first two are the rates measured with
+// both kernels running at once (chunked prefill of 512 tokens beside long decodes, D 128):
+// lower than either kernel alone, which shares no SMs, L2 or HBM bandwidth.
+constexpr int kPfSmGflopsTc = 6800;
 constexpr int kPfSmGflopsMma = 800;
-constexpr int kDecSmGBs = 70;
+constexpr int kDecSmGBs = 64;
 constexpr int kHbmGBs = 6700;
 
 struct PlanParams {

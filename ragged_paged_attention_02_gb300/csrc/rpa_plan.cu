@@ -144,12 +144,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 cls = 2;
                 cnt = (ql + Tq - 1) / Tq;
                 unsigned long long keys = 0;
+                int wmax = 0;
                 for (int k = 0; k < cnt; ++k) {
                     int lo, hi;
                     key_band(kl, ql, k * Tq, min(ql, (k + 1) * Tq), p, lo, hi);
                     keys += (unsigned long long)(hi - lo);
+                    wmax = max(wmax, hi - lo);
                 }
                 atomicAdd(&s_pf_keys, keys);
+                s_comb[s] = wmax;  // the sequence's heaviest unit (sort weight); combine offsets are decode-only
             }
         }
         s_cls[s] = cls;
@@ -226,8 +229,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         if (s < S) {
             s_dend[s] = carry_d + off.x + du;
             s_pend[s] = carry_p + off.y + pu;
-            s_part[s] = carry_part + off.z;
-            s_comb[s] = carry_comb + off.w;
+            if (s_cls[s] != 2) {  // partial and combine offsets are read for decode sequences only
+                s_part[s] = carry_part + off.z;
+                s_comb[s] = carry_comb + off.w;
+            }
         }
         carry_d += tot.x;
         carry_p += tot.y;
@@ -250,7 +255,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     const bool do_sort = n_units <= kMaxSort && S < 65536;  // key fields: unit < 2^16, seq < 2^16
     for (int u = tid; u < n_units; u += blockDim.x) {
         int d[8];
-        int cost;
+        int cost, wseq = 0;
         int cls_bit;
         if (u < n_dec) {
             const int s = upper_seq(s_dend, S, u);
@@ -278,16 +283,23 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             d[0] = s; d[1] = t0; d[2] = nt; d[3] = lo; d[4] = hi;
             d[5] = -1; d[6] = 0; d[7] = 1;
             cost = hi - lo;
+            wseq = s_comb[s];
             cls_bit = 1;
         }
         int4* dst = reinterpret_cast<int4*>(p.units + (size_t)u * 8);
         dst[0] = make_int4(d[0], d[1], d[2], d[3]);
         dst[1] = make_int4(d[4], d[5], d[6], d[7]);
+        // decode: cost descending.  Prefill: sequences by their heaviest unit descending (the
+        // longest work starts first), a sequence's units together (its K/V stays in L2), then
+        // cost descending; weights and costs in 16-key buckets.  Fields: class 1 | weight 16 |
+        // sequence 18 | cost 16 | unit 13 (units < 8192, sequences < 65536 when sorting).
         if (do_sort)
             s_keys[u] = cls_bit == 0
                             ? ((unsigned long long)(0x7FFFFFFF - cost) << 32) | (unsigned long long)u
-                            : (1ull << 63) | ((unsigned long long)d[0] << 47) |
-                                  ((unsigned long long)(0x7FFFFFFF - cost) << 16) | (unsigned long long)u;
+                            : (1ull << 63) | ((unsigned long long)(0xFFFF - min(wseq >> 4, 0xFFFF)) << 47) |
+                                  ((unsigned long long)d[0] << 29) |
+                                  ((unsigned long long)(0xFFFF - min(cost >> 4, 0xFFFF)) << 13) |
+                                  (unsigned long long)u;
     }
 
     // ---- 5. bitonic sort of the keys (ascending: decode first, then cost descending)
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     for (int r = tid; r < n_units; r += blockDim.x) {
         // unit index: low 32 bits of a decode key, low 16 bits of a prefill key
         const unsigned long long key = do_sort ? s_keys[r] : 0ull;
-        const int u = !do_sort ? r : (int)((key >> 63) ? (key & 0xFFFFull) : (key & 0xFFFFFFFFull));
+        const int u = !do_sort ? r : (int)((key >> 63) ? (key & 0x1FFFull) : (key & 0xFFFFFFFFull));
         const int4* src = reinterpret_cast<const int4*>(p.units + (size_t)u * 8);
         const int4 a = src[0], b = src[1];
         const bool is_dec = r < n_dec;

@@ -4,8 +4,9 @@ Written from the planner's stated rules, not from its code: decode-class
 sequences (q_len * G <= decode rows) are cut into key pieces of `chunk` keys,
 prefill-class sequences into query tiles of pf_tokens tokens; each unit's
 key range is the band its rows can see; units are ordered decode first (by
-cost descending), then prefill (by sequence, then cost descending), ties by
-unit index; each unit yields one item per kv head.
+cost descending), then prefill (sequences by their heaviest unit descending,
+a sequence's units together, then cost descending; weights and costs in
+16-key buckets), ties by unit index; each unit yields one item per kv head.
 """
 import numpy as np
 
@@ -19,7 +20,7 @@ def band(kl, ql, i0, i1, causal, window):
 
 
 # rates of the SM-split model (FLOP/ns per SM on prefill, B/ns per SM decode, HBM B/ns)
-PF_SM_GFLOPS_TC, PF_SM_GFLOPS_MMA, DEC_SM_GBS, HBM_GBS = 7600, 800, 70, 6700
+PF_SM_GFLOPS_TC, PF_SM_GFLOPS_MMA, DEC_SM_GBS, HBM_GBS = 6800, 800, 64, 6700
 
 
 def split(prob, dec_keyheads, pf_keys, n_sms, dec_bps, pf_bps, concurrent, force_pf=0, force_dec=0):
@@ -103,6 +104,7 @@ def plan(prob, dec_slots=None, dec_rows=16, pf_tokens=None, waves=4, min_chunk=5
             kb = lo + k * chunk
             ke = min(hi, kb + chunk)
             units.append((0, ke - kb, [s, 0, ql, kb, ke, base, k, pieces]))
+    weight = {}
     for s in range(S):
         if cls[s] != 2:
             continue
@@ -112,12 +114,17 @@ def plan(prob, dec_slots=None, dec_rows=16, pf_tokens=None, waves=4, min_chunk=5
             nt = min(Tq, ql - t0)
             lo, hi = band(int(kvl[s]), ql, t0, t0 + nt, causal, win)
             units.append((1, hi - lo, [s, t0, nt, lo, hi, -1, 0, 1]))
+            weight[s] = max(weight.get(s, 0), hi - lo)
     n = len(units)
     order = list(range(n))
     if n <= max_sort and S < 65536:
+        # decode: cost descending; prefill: sequences by heaviest unit descending, a sequence's
+        # units together, then cost descending (weights and costs in 16-key buckets); ties by unit
         def key(u):
             c, cost, d = units[u]
-            return (0, 0x7FFFFFFF - cost, 0, u) if c == 0 else (1, d[0], 0x7FFFFFFF - cost, u)
+            if c == 0:
+                return (0, 0x7FFFFFFF - cost, 0, 0, u)
+            return (1, 0xFFFF - min(weight[d[0]] >> 4, 0xFFFF), d[0], 0xFFFF - min(cost >> 4, 0xFFFF), u)
         order.sort(key=key)
     dec, pf = [], []
     for u in order:

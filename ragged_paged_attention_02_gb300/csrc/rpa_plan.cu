@@ -13,9 +13,10 @@
 //  * prefill-class sequences become units (sequence, query tile);
 //  * each unit expands to one item per kv head;
 //  * decode units are sorted by cost (keys to visit), longest first, so that
-//    the persistent kernel finishes together; prefill units are sorted by
-//    sequence, then cost, so that the CTAs running at any moment share one
-//    sequence's K/V in L2; ties keep unit order.
+//    the persistent kernel finishes together; prefill sequences are ordered by
+//    their heaviest unit, longest first, and a sequence's units stay together
+//    (by cost) so that the CTAs running at any moment share one sequence's K/V
+//    in L2; ties keep unit order.
 //
 // The key range of a unit is the band its rows can see (page: flashAttention
 // row_ids / col_ids masks): causal rows end at position p, windowed rows start
@@ -85,6 +86,39 @@ __device__ int4 block_scan4(int4 v, int4* s_warp, int4* total) {
     return r;
 }
 
+// Sum of one 64-bit value per thread over the block (all threads get it).  s_red holds 32.
+__device__ unsigned long long block_sum64(unsigned long long v, unsigned long long* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    unsigned long long t = lane < nwarps ? s_red[lane] : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    __syncthreads();
+    return t;
+}
+// Minimum of one 64-bit value per thread over the block (all threads get it).  s_red holds 32.
+__device__ unsigned long long block_min64(unsigned long long v, unsigned long long* s_red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w < v ? w : v;
+    }
+    if (lane == 0) s_red[warp] = v;
+    __syncthreads();
+    unsigned long long t = lane < nwarps ? s_red[lane] : ~0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long w = __shfl_xor_sync(0xffffffffu, t, o);
+        t = w < t ? w : t;
+    }
+    __syncthreads();
+    return t;
+}
+
 // first s in [0, n) with ends[s] > u (ends non-decreasing, ends[n-1] > u)
 __device__ __forceinline__ int upper_seq(const int* ends, int n, int u) {
     int lo = 0, hi = n - 1;
@@ -99,9 +133,8 @@ __device__ __forceinline__ int upper_seq(const int* ends, int n, int u) {
 __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p) {
     extern __shared__ __align__(16) unsigned long long s_keys[];  // kMaxSort keys, then sequence scratch
     __shared__ int4 s_warp[33];
+    __shared__ unsigned long long s_red[32];
     __shared__ int s_bad;
-    __shared__ unsigned long long s_total;
-    __shared__ unsigned long long s_pf_keys;  // sum over prefill units of the keys they visit
     __shared__ int s_split[2];                // prefill CTAs, decode CTAs
     const int tid = threadIdx.x;
     const int S = p.num_seqs;
@@ -118,14 +151,12 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     int* s_comb = s_part + S + 1;
     const int Tq = max(1, p.pf_tokens);  // query tokens per prefill tile
 
-    if (tid == 0) {
-        s_bad = 0;
-        s_total = 0ull;
-        s_pf_keys = 0ull;
-    }
+    if (tid == 0) s_bad = 0;
     __syncthreads();
 
-    // ---- 1. validate and classify each sequence
+    // ---- 1. validate and classify each sequence; per-thread sums of decode (key, kv head)
+    // pairs and of the keys prefill units visit, reduced over the block below
+    unsigned long long my_total = 0ull, my_pf_keys = 0ull;
     for (int s = tid; s < S; s += blockDim.x) {
         const int q0 = p.cu_q_lens[s], q1 = p.cu_q_lens[s + 1], kl = p.kv_lens[s];
         const int ql = q1 - q0;
@@ -139,7 +170,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 key_band(kl, ql, 0, ql, p, lo, hi);
                 cls = 1;
                 cnt = hi - lo;
-                atomicAdd(&s_total, (unsigned long long)cnt * (unsigned long long)p.Hkv);
+                my_total += (unsigned long long)cnt * (unsigned long long)p.Hkv;
             } else {
                 cls = 2;
                 cnt = (ql + Tq - 1) / Tq;
@@ -151,7 +182,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                     keys += (unsigned long long)(hi - lo);
                     wmax = max(wmax, hi - lo);
                 }
-                atomicAdd(&s_pf_keys, keys);
+                my_pf_keys += keys;
                 s_comb[s] = wmax;  // the sequence's heaviest unit (sort weight); combine offsets are decode-only
             }
         }
@@ -167,34 +198,42 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         return;
     }
 
+    const unsigned long long s_total = block_sum64(my_total, s_red);
+    const unsigned long long s_pf_keys = block_sum64(my_pf_keys, s_red);
+
     // ---- 2. SMs for each kernel, then the split-KV chunk for decode units
-    if (tid == 0) {
-        int pf_sms = p.n_sms, dec_sms = p.n_sms;
+    {
         const unsigned long long dec_bytes = s_total * (unsigned long long)(2 * p.D * p.kv_elt);
         const unsigned long long pf_flops =
             s_pf_keys * (unsigned long long)p.Hkv * (unsigned long long)p.pf_mma_rows * (unsigned long long)(4 * p.D);
-        if (p.concurrent && dec_bytes > 0 && pf_flops > 0) {
-            // minimise max(prefill time, decode time) over the prefill SM count (times in ns)
-            unsigned long long best = ~0ull;
-            int best_x = 1;
-            for (int x = 1; x < p.n_sms; ++x) {
+        const bool both = p.concurrent && dec_bytes > 0 && pf_flops > 0;
+        // minimise max(prefill time, decode time) over the prefill SM count x (times in ns; one
+        // x per thread, the first minimum wins: (time << 16 | x) is unique and orders that way)
+        unsigned long long mine = ~0ull;
+        if (both) {
+            for (int x = 1 + tid; x < p.n_sms; x += blockDim.x) {
                 const unsigned long long tp = pf_flops / ((unsigned long long)x * p.pf_sm_gflops);
                 const unsigned long long bw =
                     min((unsigned long long)p.hbm_gbs, (unsigned long long)(p.n_sms - x) * p.dec_sm_gbs);
                 const unsigned long long td = dec_bytes / bw;
                 const unsigned long long c = tp > td ? tp : td;
-                if (c < best) {
-                    best = c;
-                    best_x = x;
-                }
+                const unsigned long long k = (min(c, (1ull << 47) - 1) << 16) | (unsigned long long)x;
+                mine = k < mine ? k : mine;
             }
-            if (p.force_pf_sms > 0) best_x = min(p.force_pf_sms, p.n_sms - 1);
-            pf_sms = best_x;
-            dec_sms = p.n_sms - best_x;
         }
-        if (p.force_dec_sms > 0) dec_sms = min(p.force_dec_sms, p.n_sms);
-        s_split[0] = pf_sms * p.pf_bps;
-        s_split[1] = dec_sms * p.dec_bps;
+        const unsigned long long best = block_min64(mine, s_red);
+        if (tid == 0) {
+            int pf_sms = p.n_sms, dec_sms = p.n_sms;
+            if (both) {
+                int best_x = (int)(best & 0xFFFFull);
+                if (p.force_pf_sms > 0) best_x = min(p.force_pf_sms, p.n_sms - 1);
+                pf_sms = best_x;
+                dec_sms = p.n_sms - best_x;
+            }
+            if (p.force_dec_sms > 0) dec_sms = min(p.force_dec_sms, p.n_sms);
+            s_split[0] = pf_sms * p.pf_bps;
+            s_split[1] = dec_sms * p.dec_bps;
+        }
     }
     __syncthreads();
     int chunk;
@@ -341,27 +380,21 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
     __syncthreads();
 
-    // ---- 6. items (one per kv head) in sorted unit order
-    for (int r = tid; r < n_units; r += blockDim.x) {
-        // unit index: low 32 bits of a decode key, low 16 bits of a prefill key
+    // ---- 6. items (one per kv head) in sorted unit order; consecutive threads write
+    // consecutive items (coalesced 16-byte stores)
+    for (int idx = tid; idx < n_units * p.Hkv; idx += blockDim.x) {
+        const int r = idx / p.Hkv, h = idx - r * p.Hkv;
+        // unit index: low 32 bits of a decode key, low 13 bits of a prefill key
         const unsigned long long key = do_sort ? s_keys[r] : 0ull;
         const int u = !do_sort ? r : (int)((key >> 63) ? (key & 0x1FFFull) : (key & 0xFFFFFFFFull));
         const int4* src = reinterpret_cast<const int4*>(p.units + (size_t)u * 8);
         const int4 a = src[0], b = src[1];
         const bool is_dec = r < n_dec;
         Item* dst = is_dec ? p.dec_items + (size_t)r * p.Hkv : p.pf_items + (size_t)(r - n_dec) * p.Hkv;
-        for (int h = 0; h < p.Hkv; ++h) {
-            Item it;
-            it.seq = a.x;
-            it.head = h;
-            it.tok0 = a.y;
-            it.ntok = a.z;
-            it.kv_begin = a.w;
-            it.kv_end = b.x;
-            it.part = b.y >= 0 ? b.y + h * b.w + b.z : -1;
-            it.piece = b.z;
-            dst[h] = it;
-        }
+        int4* d4 = reinterpret_cast<int4*>(dst + h);
+        // Item: seq, head, tok0, ntok | kv_begin, kv_end, part, piece
+        d4[0] = make_int4(a.x, h, a.y, a.z);
+        d4[1] = make_int4(a.w, b.x, b.y >= 0 ? b.y + h * b.w + b.z : -1, b.z);
     }
     // ---- 7. combine entries of split decode sequences
     for (int s = tid; s < S; s += blockDim.x) {

@@ -320,10 +320,14 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                 vb = kv_base;
             }
 
-            // ---- S = Q K^T  (16 rows x 16 keys)
-            float sacc[2][4];
+            // ---- S = Q K^T  (16 rows x 16 keys); even and odd k-steps accumulate separately
+            // (two independent MMA chains per n-block), summed at the end
+            float sacc[2][4], sodd[2][4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+            for (int i = 0; i < 2; ++i) {
+                sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+                sodd[i][0] = sodd[i][1] = sodd[i][2] = sodd[i][3] = 0.f;
+            }
             {
                 const int row = (lane & 7) + (lane >> 4) * 8;  // key row of this lane's ldmatrix
 #pragma unroll
@@ -340,9 +344,13 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                     }
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-                    mma16816<F16>(sacc[0], qf[kd], b0, b1);
-                    mma16816<F16>(sacc[1], qf[kd], b2, b3);
+                    mma16816<F16>((kd & 1) ? sodd[0] : sacc[0], qf[kd], b0, b1);
+                    mma16816<F16>((kd & 1) ? sodd[1] : sacc[1], qf[kd], b2, b3);
                 }
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[i][e] += sodd[i][e];
             }
             // ---- scale, softcap, masks (log2 domain)
             const bool need_mask = partial || (a.causal && kw + 15 > kl - ql + tok0) ||
@@ -370,22 +378,32 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                     mx[ri] = fmaxf(mx[ri], x);
                 }
             }
+            // lazy rescale: the running max moves only when some row's max grows by more than
+            // 2^8 (P and l use the same stale max, so the result is unchanged; P stays <= 2^8)
             float base[2];
 #pragma unroll
             for (int ri = 0; ri < 2; ++ri) {
                 mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 1));
                 mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 2));
-                const float m_new = fmaxf(m_r[ri], mx[ri]);
-                base[ri] = m_new == -INFINITY ? 0.f : m_new;
-                const float alpha = ex2(m_r[ri] - base[ri]);
-                m_r[ri] = m_new;
-                l_r[ri] *= alpha;
+            }
+            const bool need = __any_sync(0xffffffffu, mx[0] > m_r[0] + 8.f || mx[1] > m_r[1] + 8.f);
+            if (need) {
 #pragma unroll
-                for (int nd = 0; nd < D / 8; ++nd) {
-                    o_acc[nd][2 * ri] *= alpha;
-                    o_acc[nd][2 * ri + 1] *= alpha;
+                for (int ri = 0; ri < 2; ++ri) {
+                    const float m_new = fmaxf(m_r[ri], mx[ri]);
+                    const float b = m_new == -INFINITY ? 0.f : m_new;
+                    const float alpha = m_r[ri] == -INFINITY ? 0.f : ex2(m_r[ri] - b);
+                    m_r[ri] = m_new;
+                    l_r[ri] *= alpha;
+#pragma unroll
+                    for (int nd = 0; nd < D / 8; ++nd) {
+                        o_acc[nd][2 * ri] *= alpha;
+                        o_acc[nd][2 * ri + 1] *= alpha;
+                    }
                 }
             }
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) base[ri] = m_r[ri] == -INFINITY ? 0.f : m_r[ri];
 #pragma unroll
             for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll

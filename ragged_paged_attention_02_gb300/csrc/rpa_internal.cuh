@@ -55,9 +55,9 @@ constexpr int kPlanThreads = 1024;
 // stream in the decode kernel, and HBM B/ns.  The first two are the rates measured with
 // both kernels running at once (chunked prefill of 512 tokens beside long decodes, D 128):
 // lower than either kernel alone, which shares no SMs, L2 or HBM bandwidth.
-constexpr int kPfSmGflopsTc = 6800;
+constexpr int kPfSmGflopsTc = 6500;
 constexpr int kPfSmGflopsMma = 800;
-constexpr int kDecSmGBs = 64;
+constexpr int kDecSmGBs = 68;
 constexpr int kHbmGBs = 6700;
 
 struct PlanParams {

@@ -35,12 +35,14 @@ namespace {
 
 constexpr int kM = kTcRows;   // query rows per tile = TMEM lanes
 constexpr int kBN = 64;       // keys per K/V tile
-// warps 0-7 softmax (two per TMEM lane quadrant, one per half of the key tile), 8-11 convert,
-// 12 producer, 13 MMA
-constexpr int kThreads = 448;
-constexpr int kConv0 = 8, kProducer = 12, kMma = 13;
-// 4 warps share an SM sub-partition's 16384 registers: at most 128 a thread (launch bound 512)
-constexpr int kRegBoundThreads = 512;
+// warps 0-7 softmax (two per TMEM lane quadrant, one per half of the key tile), 8-15 convert
+// (8 key rows of a tile each; 8-11 also convert Q, one TMEM lane quadrant each), 16 producer,
+// 17 MMA
+constexpr int kThreads = 576;
+constexpr int kConv0 = 8, kNConv = 8, kProducer = 16, kMma = 17;
+constexpr int kConvRows = kBN / kNConv;  // key rows of a tile per converter warp
+// 5 warps share an SM sub-partition's 16384 registers: at most 96 a thread (launch bound 640)
+constexpr int kRegBoundThreads = 640;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
@@ -90,7 +92,7 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8_hw(uint32_t w0, uint32_t w1) {
                       e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
 }
 
-// One converter warp's 16 key rows (16 cw .. 16 cw + 15) of one half (K or V) of a raw stage
+// One converter warp's key rows (kConvRows cw .. + kConvRows - 1) of one half (K or V) of a raw stage
 // ([run][K | V][BR rows][D bytes]; `raw` points at the half's first run) into a 128-byte
 // swizzled f16 tile [D / 64][64 rows][128 B].  Keys outside [kv_begin, kv_end) become zero.
 // HW: exact hardware conversion, else the integer placement (value / 2^8).  A lane converts 16
@@ -98,13 +100,13 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8_hw(uint32_t w0, uint32_t w1) {
 template <int D, bool HW>
 __device__ __forceinline__ void convert_rows(const uint8_t* raw, uint8_t* dst, int cw, int lane, int brs, int k_lo,
                                              int kv_begin, int kv_end) {
-    constexpr int LPR = D / 16, RPP = 32 / LPR, NP = 16 / RPP;
+    constexpr int LPR = D / 16, RPP = 32 / LPR, NP = kConvRows / RPP;
     const int BR = 1 << brs;
     const int e = lane % LPR, r0 = lane / LPR;
     uint4 v[NP];
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-        const int key = 16 * cw + r0 + i * RPP;
+        const int key = kConvRows * cw + r0 + i * RPP;
         v[i] = *reinterpret_cast<const uint4*>(raw + (key >> brs) * (2 * BR * D) + (key & (BR - 1)) * D + e * 16);
     }
     // the 16 elements are f16 chunks 2e, 2e+1 of column block e / 4; lanes of odd (e / 4) store
@@ -113,7 +115,7 @@ __device__ __forceinline__ void convert_rows(const uint8_t* raw, uint8_t* dst, i
     const int cb = e >> 2, c0 = (2 * e) & 7;
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
-        const int key = 16 * cw + r0 + i * RPP;
+        const int key = kConvRows * cw + r0 + i * RPP;
         const int j = k_lo + key;
         const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
         const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
@@ -193,12 +195,12 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&meta_full[i]), 1);
-            mbar_init(smem_u32(&meta_free[i]), 13);  // 8 softmax + 4 converter warps + MMA thread
+            mbar_init(smem_u32(&meta_free[i]), 17);  // 8 softmax + 8 converter warps + MMA thread
             mbar_init(smem_u32(&raw_full[i]), 1);
-            mbar_init(smem_u32(&raw_empty[i]), 4);
-            mbar_init(smem_u32(&k_full[i]), 4);
+            mbar_init(smem_u32(&raw_empty[i]), kNConv);
+            mbar_init(smem_u32(&k_full[i]), kNConv);
             mbar_init(smem_u32(&k_empty[i]), 1);
-            mbar_init(smem_u32(&v_full[i]), 4);
+            mbar_init(smem_u32(&v_full[i]), kNConv);
             mbar_init(smem_u32(&v_empty[i]), 1);
             mbar_init(smem_u32(&s_full[i]), 1);
             mbar_init(smem_u32(&p_full[i]), 8);
@@ -323,11 +325,12 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             if (!ok) break;
             it = __shfl_sync(0xffffffffu, nxt, 0);
         }
-    } else if (warp >= kConv0 && warp < kConv0 + 4) {
+    } else if (warp >= kConv0 && warp < kConv0 + kNConv) {
         // =============================== converters ===============================
-        const int cw = warp - kConv0;        // converter warp 0..3 == its TMEM lane quadrant
-        const int r = tid - kConv0 * 32;     // TMEM lane (query row) for the Q conversion
-        const uint32_t lane_addr = tmem + ((uint32_t)(cw * 32) << 16);
+        const int cw = warp - kConv0;        // converter warp 0..7; 0..3 also convert Q
+        const bool qconv = cw < 4;           // its TMEM lane quadrant is cw (warp % 4)
+        const int r = (cw & 3) * 32 + lane;  // TMEM lane (query row) for the Q conversion
+        const uint32_t lane_addr = tmem + ((uint32_t)((cw & 3) * 32) << 16);
         const int BR = p.BR, brs = __ffs(BR) - 1;
         int s = 0, ms = 0;
         uint32_t ph = 0, mph = 0, qph = 0;
@@ -345,9 +348,9 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 mph ^= 1u;
             }
             // ---- Q: bf16 staging -> f16 TMEM columns (thread r owns query row r)
-            if (items > 0 && !mbar_wait(smem_u32(&qt_free), (items - 1) & 1u, ctrl, tmo)) break;
+            if (qconv && items > 0 && !mbar_wait(smem_u32(&qt_free), (items - 1) & 1u, ctrl, tmo)) break;
             bool ok = true;
-            for (int rd = 0; rd < Gm::ROUNDS; ++rd) {
+            for (int rd = 0; rd < (qconv ? Gm::ROUNDS : 0); ++rd) {
                 if (!mbar_wait(smem_u32(&q_full), qph, ctrl, tmo)) {
                     ok = false;
                     break;
@@ -370,11 +373,13 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 if (lane == 0) mbar_arrive(smem_u32(&q_empty));
             }
             if (!ok) break;
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&q_ready));
-            // ---- K / V tiles: this warp converts keys [16cw, 16cw + 16) of each tile
+            if (qconv) {
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&q_ready));
+            }
+            // ---- K / V tiles: this warp converts keys [kConvRows cw, kConvRows (cw + 1)) of each tile
             for (int t = 0; t < nt; ++t, ++tg) {
                 const int b2 = tg & 1;
                 const uint32_t par = (tg >> 1) & 1u;

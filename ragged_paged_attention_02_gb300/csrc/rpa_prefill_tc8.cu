@@ -425,25 +425,11 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             uint32_t mph = 0;
             uint32_t tg = 0, items = 0;
             bool ok = true;
-            auto issue_pv = [&](uint32_t g, bool first) -> bool {
-                const int b2 = g & 1;
-                const uint32_t par = (g >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&p_full[b2]), par, ctrl, tmo) ||
-                    !mbar_wait(smem_u32(&v_full[b2]), par, ctrl, tmo))
-                    return false;
-                if (first && items > 0 && !mbar_wait(smem_u32(&o_free), (items - 1) & 1u, ctrl, tmo)) return false;
-                tc_fence_after();
-                const uint32_t vt = v16_base + b2 * Gm::T16;
-                const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t bdesc = umma_sdesc(vt + kk * 16 * 128, kBN * 128, 1024);
-                    umma_ts(tmem + Gm::TM_O, tmem + scol + kk * 8, bdesc, idesc_pv, (!first || kk > 0) ? 1 : 0);
-                }
-                umma_commit(smem_u32(&v_empty[b2]));
-                umma_commit(smem_u32(&pv_done));
-                return true;
-            };
+            // Per item, QK(t) and PV(t) are issued as soon as their inputs are ready, in either
+            // order: QK(t) needs K(t) converted and PV(t-2) issued (it overwrites S(t % 2), which
+            // PV(t-2) reads; the tensor pipe runs in issue order); PV(t) needs P(t), V(t) and, for
+            // the item's first PV, the previous epilogue done with O.  Readiness is polled without
+            // blocking; a poll that sees nothing ready for longer than the wait bound gives up.
             for (;;) {
                 if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
                 const int stop = meta[ms][eStop], nt = meta[ms][eNt];
@@ -455,31 +441,70 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 }
                 if (!mbar_wait(smem_u32(&q_ready), items & 1u, ctrl, tmo)) break;
                 tc_fence_after();
-                const uint32_t g0 = tg;
-                for (int t = 0; t < nt; ++t, ++tg) {
-                    const int b2 = tg & 1;
-                    if (!mbar_wait(smem_u32(&k_full[b2]), (tg >> 1) & 1u, ctrl, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t kt = k16_base + b2 * Gm::T16;
-                    const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+                int tq = 0, tp = 0;  // next QK and next PV of this item
+                uint64_t t_idle = 0;
+                int idle = 0;
+                while (tp < nt) {
+                    bool did = false;
+                    if (tq < nt && tq <= tp + 1) {
+                        const uint32_t g = tg + tq;
+                        const int b2 = g & 1;
+                        if (mbar_test(smem_u32(&k_full[b2]), (g >> 1) & 1u)) {
+                            tc_fence_after();
+                            const uint32_t kt = k16_base + b2 * Gm::T16;
+                            const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
-                        umma_ts(tmem + scol, tmem + Gm::TM_Q + kk * 8, umma_sdesc(kt + koff, 16, 1024), idesc_qk,
-                                kk > 0 ? 1 : 0);
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
+                                umma_ts(tmem + scol, tmem + Gm::TM_Q + kk * 8, umma_sdesc(kt + koff, 16, 1024),
+                                        idesc_qk, kk > 0 ? 1 : 0);
+                            }
+                            umma_commit(smem_u32(&s_full[b2]));
+                            umma_commit(smem_u32(&k_empty[b2]));
+                            if (tq == nt - 1) umma_commit(smem_u32(&qt_free));
+                            ++tq;
+                            did = true;
+                        }
                     }
-                    umma_commit(smem_u32(&s_full[b2]));
-                    umma_commit(smem_u32(&k_empty[b2]));
-                    if (t == nt - 1) umma_commit(smem_u32(&qt_free));
-                    if (t > 0 && !issue_pv(tg - 1, t == 1)) {
-                        ok = false;
-                        break;
+                    if (tp < tq) {
+                        const uint32_t g = tg + tp;
+                        const int b2 = g & 1;
+                        const uint32_t par = (g >> 1) & 1u;
+                        const bool first = tp == 0;
+                        if (mbar_test(smem_u32(&p_full[b2]), par) && mbar_test(smem_u32(&v_full[b2]), par) &&
+                            (!first || items == 0 || mbar_test(smem_u32(&o_free), (items - 1) & 1u))) {
+                            tc_fence_after();
+                            const uint32_t vt = v16_base + b2 * Gm::T16;
+                            const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+#pragma unroll
+                            for (int kk = 0; kk < kBN / 16; ++kk) {
+                                const uint64_t bdesc = umma_sdesc(vt + kk * 16 * 128, kBN * 128, 1024);
+                                umma_ts(tmem + Gm::TM_O, tmem + scol + kk * 8, bdesc, idesc_pv,
+                                        (!first || kk > 0) ? 1 : 0);
+                            }
+                            umma_commit(smem_u32(&v_empty[b2]));
+                            umma_commit(smem_u32(&pv_done));
+                            ++tp;
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        idle = 0;
+                        t_idle = 0;
+                    } else if (++idle >= 64) {
+                        idle = 0;
+                        const uint64_t now = global_ns();
+                        if (t_idle == 0) {
+                            t_idle = now;
+                        } else if (now - t_idle > tmo) {
+                            set_status(ctrl, RPA_ERR_TIMEOUT);
+                            ok = false;
+                            break;
+                        }
                     }
                 }
-                if (!ok || !issue_pv(tg - 1, tg - 1 == g0)) break;
+                if (!ok) break;
+                tg += nt;
                 umma_commit(smem_u32(&o_full));
                 ++items;
             }

@@ -143,7 +143,8 @@ int rpa_get_status(RpaHandle* h, void* stream);
  * tile rows, [6] query tokens per prefill tile, [7] partial slots used, [8] planned
  * units, [9] 1 if units were sorted by cost, [10] decode CTAs given work, [11]
  * prefill CTAs given work, [12] SMs, [13] / [14] resident decode / prefill
- * CTAs per SM, [15] 1 if decode and prefill ran concurrently.  items (host, may be NULL)
+ * CTAs per SM, [15] bit 0: decode and prefill ran concurrently, bit 1: decode units were
+ * items of the prefill kernel (fp8 K/V on tensor memory).  items (host, may be NULL)
  * receives up to max_items decode items followed by the prefill items, 8
  * int32 each: seq, kv head, first query token of the sequence's tile (local),
  * tokens in the tile, first key, end key, partial slot (-1 = direct write),

@@ -247,8 +247,10 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     const int64_t Tq = h->pf_tokens;
     const int64_t dec_slots = (int64_t)h->sms * h->dec_bps;
     h->max_dec_units = (int)(S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1);
-    h->max_pf_units = (int)((c.num_q_tokens + Tq - 1) / Tq + S + 1);
-    h->max_units = h->max_dec_units + h->max_pf_units;
+    const int pf_only_units = (int)((c.num_q_tokens + Tq - 1) / Tq + S + 1);
+    h->max_units = h->max_dec_units + pf_only_units;
+    // with fp8 K/V on tensor memory, decode units are items of the prefill kernel too
+    h->max_pf_units = h->tc8 ? h->max_units : pf_only_units;
     h->max_part = (int)(h->max_dec_units * Hkv);
     h->max_comb = (int)(S * Hkv);
 
@@ -331,6 +333,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.dec_bps = h->dec_bps;
     pp.pf_bps = h->pf_bps;
     pp.pf_mma_rows = h->tc ? 2 * kTcRows : h->tc8 ? kTcRows : kPfRows;
+    pp.dec_on_pf = h->tc8;
     pp.D = h->D;
     pp.kv_elt = h->fp8 ? 1 : 2;
     pp.pf_sm_gflops = (h->tc || h->tc8) ? kPfSmGflopsTc : kPfSmGflopsMma;
@@ -587,7 +590,7 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[12] = h->sms;
     info[13] = h->dec_bps;
     info[14] = h->pf_bps;
-    info[15] = h->concurrent;
+    info[15] = h->concurrent | (h->tc8 << 1);
     if (items && max_items > 0) {
         const int64_t nd = ctrl[kNumDecItems] < max_items ? ctrl[kNumDecItems] : max_items;
         const int64_t np = ctrl[kNumPfItems] < max_items - nd ? ctrl[kNumPfItems] : max_items - nd;

@@ -76,6 +76,7 @@ struct PlanParams {
     int concurrent;      // 1: the two kernels run at the same time on disjoint SMs
     int n_sms, dec_bps, pf_bps;  // SMs, resident CTAs per SM of each kernel
     int pf_mma_rows;     // MMA rows per prefill unit (tile padding included)
+    int dec_on_pf;       // 1: decode units become items of the prefill kernel (no decode kernel work)
     int D, kv_elt;
     int pf_sm_gflops;    // prefill FLOP rate of one SM (FLOP/ns)
     int dec_sm_gbs;      // decode bytes one SM can stream (B/ns)

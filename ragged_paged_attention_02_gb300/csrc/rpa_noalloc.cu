@@ -117,8 +117,9 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     const int64_t Tq = pf_tokens;
     const int64_t dec_slots = (int64_t)sms * dec_bps;
     const int64_t max_dec_units = S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1;
-    const int64_t max_pf_units = (c.num_q_tokens + Tq - 1) / Tq + S + 1;
-    const int64_t max_units = max_dec_units + max_pf_units;
+    const int64_t pf_only_units = (c.num_q_tokens + Tq - 1) / Tq + S + 1;
+    const int64_t max_units = max_dec_units + pf_only_units;
+    const int64_t max_pf_units = tc8 ? max_units : pf_only_units;
     const int64_t max_part = max_dec_units * Hkv;
     const int64_t max_comb = S * Hkv;
     size_t off = 0;
@@ -170,6 +171,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     pp.dec_bps = dec_bps;
     pp.pf_bps = pf_bps;
     pp.pf_mma_rows = tc ? 2 * kTcRows : tc8 ? kTcRows : kPfRows;
+    pp.dec_on_pf = tc8 ? 1 : 0;
     pp.D = D;
     pp.kv_elt = fp8 ? 1 : 2;
     pp.pf_sm_gflops = (tc || tc8) ? kPfSmGflopsTc : kPfSmGflopsMma;

@@ -238,7 +238,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     __syncthreads();
     int chunk;
     {
-        const unsigned long long target = (unsigned long long)kDecWaves * (unsigned long long)max(1, s_split[1]);
+        // pieces for about kDecWaves items per CTA of the kernel that runs them
+        const int dec_ctas = p.dec_on_pf ? s_split[0] : s_split[1];
+        const unsigned long long target = (unsigned long long)kDecWaves * (unsigned long long)max(1, dec_ctas);
         unsigned long long c = (s_total + target - 1) / target;
         if (c < (unsigned long long)kMinChunk) c = kMinChunk;
         c = (c + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         carry_comb += tot.w;
     }
     const int n_dec = carry_d, n_pf = carry_p, n_units = n_dec + n_pf;
-    if (n_units > p.max_units || n_dec > p.max_dec_units || n_pf > p.max_pf_units ||
+    if (n_units > p.max_units || n_dec > p.max_dec_units || (p.dec_on_pf ? n_units : n_pf) > p.max_pf_units ||
         carry_part > p.max_part || carry_comb > p.max_comb) {
         // cannot happen with the create-time sizing; refuse rather than overflow
         if (tid == 0) {
@@ -389,8 +391,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         const int u = !do_sort ? r : (int)((key >> 63) ? (key & 0x1FFFull) : (key & 0xFFFFFFFFull));
         const int4* src = reinterpret_cast<const int4*>(p.units + (size_t)u * 8);
         const int4 a = src[0], b = src[1];
-        const bool is_dec = r < n_dec;
-        Item* dst = is_dec ? p.dec_items + (size_t)r * p.Hkv : p.pf_items + (size_t)(r - n_dec) * p.Hkv;
+        // decode units come first; with dec_on_pf they lead the prefill kernel's list instead
+        const bool is_dec = r < n_dec && !p.dec_on_pf;
+        Item* dst = is_dec ? p.dec_items + (size_t)r * p.Hkv
+                           : p.pf_items + (size_t)(p.dec_on_pf ? r : r - n_dec) * p.Hkv;
         int4* d4 = reinterpret_cast<int4*>(dst + h);
         // Item: seq, head, tok0, ntok | kv_begin, kv_end, part, piece
         d4[0] = make_int4(a.x, h, a.y, a.z);
@@ -411,8 +415,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         }
     }
     if (tid == 0) {
-        ctrl[kNumDecItems] = n_dec * p.Hkv;
-        ctrl[kNumPfItems] = n_pf * p.Hkv;
+        ctrl[kNumDecItems] = p.dec_on_pf ? 0 : n_dec * p.Hkv;
+        ctrl[kNumPfItems] = (p.dec_on_pf ? n_units : n_pf) * p.Hkv;
         ctrl[kNumComb] = carry_comb;
         ctrl[kDecChunk] = chunk;
         ctrl[kDecCounter] = 0;

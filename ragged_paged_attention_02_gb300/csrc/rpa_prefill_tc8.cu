@@ -46,7 +46,7 @@ constexpr int kRegBoundThreads = 640;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 
-enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, eNtok, eNt, eKey0, eStop };
+enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, eNtok, eNt, eKey0, eStop, ePart };
 
 template <int D>
 struct G8 {
@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 m[eNtok] = item.ntok;
                 m[eNt] = nt;
                 m[eKey0] = key0;
+                m[ePart] = item.part;
                 m[eStop] = 0;
                 mbar_arrive(smem_u32(&meta_full[ms]));
             }
@@ -535,7 +536,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             const int stop = mm[eStop];
             const int head = mm[eHead], q_start = mm[eQStart], ql = mm[eQl], kl = mm[eKl];
             const int kv_begin = mm[eKvBegin], kv_end = mm[eKvEnd], tok0 = mm[eTok0];
-            const int ntok = mm[eNtok], nt = mm[eNt], key0 = mm[eKey0];
+            const int ntok = mm[eNtok], nt = mm[eNt], key0 = mm[eKey0], part = mm[ePart];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&meta_free[ms]));
             if (stop) break;
@@ -656,6 +657,36 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
             tc_fence_after();
             const int rows_used = ntok * G;
+            if (part >= 0) {
+                // a split-KV piece of a decode-class sequence (rows_used <= 16): the unnormalised
+                // O (V tiles hold values / 2^8), the running max (log2 domain) and the row sum go
+                // to partial slot `part`, merged by the combine kernel
+                // (tensor-memory loads are warp-collective: every lane loads, live rows store)
+                float* prow = a.part_o + ((size_t)part * kDecRows + r) * D + half * HO;
+#pragma unroll 1
+                for (int c = 0; c < HO / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
+                    tmem_ld_wait();
+                    if (r < rows_used) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            *reinterpret_cast<float4*>(prow + c * 32 + 4 * i) =
+                                make_float4(__uint_as_float(ov[4 * i]) * kKvUnscale,
+                                            __uint_as_float(ov[4 * i + 1]) * kKvUnscale,
+                                            __uint_as_float(ov[4 * i + 2]) * kKvUnscale,
+                                            __uint_as_float(ov[4 * i + 3]) * kKvUnscale);
+                    }
+                }
+                if (half == 0 && r < rows_used)
+                    *reinterpret_cast<float2*>(a.part_ml + ((size_t)part * kDecRows + r) * 2) =
+                        make_float2(m_run, l_row);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&o_free));
+                ++items;
+                continue;
+            }
             const float inv = l_row > 0.f ? a.v_scale * kKvUnscale / l_row : 0.f;
             const int t_tok = q_start + tok0 + r / G;
             const int qh = head * G + r % G;

@@ -52,7 +52,9 @@ def split(prob, dec_keyheads, pf_keys, n_sms, dec_bps, pf_bps, concurrent, force
 
 
 def plan(prob, dec_slots=None, dec_rows=16, pf_tokens=None, waves=4, min_chunk=512, align=64,
-         max_sort=8192, n_sms=None, dec_bps=None, pf_bps=1, concurrent=False):
+         max_sort=8192, n_sms=None, dec_bps=None, pf_bps=1, concurrent=False, dec_on_pf=False):
+    """dec_on_pf: decode units become items of the prefill kernel (leading its list) and their
+    key pieces are sized for the prefill kernel's CTAs."""
     Hkv = prob.num_kv_heads
     G = prob.num_q_heads // Hkv
     Tq = max(1, pf_tokens if pf_tokens is not None else 64 // G)
@@ -85,7 +87,7 @@ def plan(prob, dec_slots=None, dec_rows=16, pf_tokens=None, waves=4, min_chunk=5
         pf_ctas, dec_ctas = split(prob, total, pf_keys, n_sms, dec_bps, pf_bps, concurrent)
     else:
         pf_ctas, dec_ctas = None, dec_slots
-    target = waves * max(1, dec_ctas)
+    target = waves * max(1, pf_ctas if dec_on_pf else dec_ctas)
     chunk = max(-(-total // target), min_chunk)
     chunk = -(-chunk // align) * align
     chunk = min(chunk, 1 << 30)
@@ -131,7 +133,7 @@ def plan(prob, dec_slots=None, dec_rows=16, pf_tokens=None, waves=4, min_chunk=5
         c, _, d = units[u]
         for h in range(Hkv):
             item = [d[0], h, d[1], d[2], d[3], d[4], d[5] + h * d[7] + d[6] if d[5] >= 0 else -1, d[6]]
-            (dec if c == 0 else pf).append(item)
+            (dec if c == 0 and not dec_on_pf else pf).append(item)
     return dict(status=0, chunk=chunk, sorted=int(n <= max_sort and S < 65536), n_units=n, n_part=part,
                 pf_ctas=pf_ctas, dec_ctas=dec_ctas,
                 dec=np.array(dec, np.int32).reshape(-1, 8), pf=np.array(pf, np.int32).reshape(-1, 8))

@@ -104,15 +104,21 @@ def test_planner_matches_python_rederivation():
     from plan_model import plan
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
-    for name in ("tiny", "mixed"):
-        p = ri.workload(name) if name == "tiny" else ri.random_small(
-            40, num_seqs=60, max_q=300, max_kv=5000, num_q_heads=32, num_kv_heads=8, head_dim=128,
-            sliding_window=777)
+    for name in ("tiny", "mixed", "fp8"):
+        if name == "tiny":
+            p = ri.workload(name)
+        elif name == "mixed":
+            p = ri.random_small(40, num_seqs=60, max_q=300, max_kv=5000, num_q_heads=32, num_kv_heads=8,
+                                head_dim=128, sliding_window=777)
+        else:  # fp8 K/V on tensor memory: decode units become prefill-kernel items
+            p = ri.random_small(41, num_seqs=50, max_q=60, max_kv=6000, num_q_heads=16, num_kv_heads=8,
+                                head_dim=256, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05,
+                                sliding_window=2000)
         att = RaggedPagedAttention(**p.cfg_dict())
         att.forward(*to_dev(p), p.num_seqs)
         info, items = att.plan()
         ref = plan(p, pf_tokens=int(info[6]), n_sms=int(info[12]), dec_bps=int(info[13]),
-                   pf_bps=int(info[14]), concurrent=bool(info[15]))
+                   pf_bps=int(info[14]), concurrent=bool(info[15] & 1), dec_on_pf=bool(info[15] & 2))
         assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
         assert info[10] == ref["dec_ctas"] and info[11] == ref["pf_ctas"]
         assert info[9] == ref["sorted"] and info[7] == ref["n_part"]

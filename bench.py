@@ -300,6 +300,13 @@ def main():
     hbm, tf_burst, tf_sust, src = peaks()
     mean_k = kern.mean(axis=0)
 
+    # with fp8 K/V on tensor memory the prefill kernel also runs the decode-class units
+    # (rpa_read_plan info[15] bit 1): charge it with both classes' work
+    if int(att.plan(max_items=1)[0][15]) & 2:
+        d, pf = work["decode"], work["prefill"]
+        work["prefill"] = {k: d[k] + pf[k] for k in pf}
+        work["decode"] = {k: 0 for k in d}
+
     def kernel_roof(name, ms):
         w = work["decode" if name == "decode_attention" else "prefill"]
         t_hbm = w["bytes"] / (hbm * 1e9)

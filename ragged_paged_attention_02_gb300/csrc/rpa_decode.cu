@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
         const int BR = p.BR, ps = a.ps;
         const int runs = kKS / BR;  // page runs per stage, one bulk copy each (K and V of the head)
         const uint32_t run_bytes = FP8 ? (uint32_t)(2 * BR * D) : (uint32_t)(2 * Gm::DH * BR * 128);
+        const uint64_t pol_stream = l2_policy_evict_first();
         int s = 0;
         uint32_t ph = 0;
         int it = 0;
@@ -180,9 +181,11 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                 if (st == 0 && lane < Gm::DHQ)
                     tma_load_3d(st_base + lane * 2048, &qmap, fb, lane * 64, item.head * a.G,
                                 q_start + item.tok0);
+                // decode K/V is read once: evict it first, so that it does not push out of L2 the
+                // K/V a concurrent prefill re-reads
                 if (want && good)
-                    tma_load_3d(kv_base + (uint32_t)lane * run_bytes, &kvmap, fb, 0, pg * ps + (k0 - lp * ps),
-                                FP8 ? 2 * item.head : 2 * item.head * Gm::DH);
+                    tma_load_3d_hint(kv_base + (uint32_t)lane * run_bytes, &kvmap, fb, 0, pg * ps + (k0 - lp * ps),
+                                     FP8 ? 2 * item.head : 2 * item.head * Gm::DH, pol_stream);
                 if (++s == kNS) {
                     s = 0;
                     ph ^= 1u;

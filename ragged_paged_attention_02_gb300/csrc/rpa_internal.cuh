@@ -395,6 +395,36 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
         : "memory");
 }
 
+// L2 cache policies for bulk copies: evict-first for data read once (streamed K/V), evict-last
+// for data several CTAs re-read from L2.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+// 3-D tiled tensor copy global -> shared with an L2 cache policy.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* map, uint32_t bar, int x, int y, int z,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;\n" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, uint32_t bar, int x, int y,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;\n" ::"r"(dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y), "l"(pol)
+        : "memory");
+}
+
 // ---- tcgen05 (5th-generation tensor cores, tensor memory)
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), descriptor version 1, 128-byte swizzle.

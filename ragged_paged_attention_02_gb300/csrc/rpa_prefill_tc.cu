@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
         const int BR = p.BR, ps = a.ps, G = a.G, Th = p.Tq / 2;  // tokens per Q tile
         const int tasks = (kBN / BR) * 2 * Gm::CB;
         const uint32_t box_bytes = (uint32_t)BR * 128u;
+        const uint64_t pol_keep = l2_policy_evict_last();
         const uint32_t q_bytes = (uint32_t)(2 * Gm::CB * G * Th * 128);
         int s = 0;
         uint32_t qph = 0, ph = 0;
@@ -236,10 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 const uint32_t fb = smem_u32(&kv_full[s]);
                 if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_issue * box_bytes);
                 __syncwarp();
+                // a sequence's K/V is re-read from L2 by the CTAs running its other query tiles
                 for (int t0 = 0; t0 < tasks; t0 += 32) {
                     int x, y;
                     uint32_t dst;
-                    if (task(t0 + lane, x, y, dst) == 1) tma_load_2d(dst, &kvmap, fb, x, y);
+                    if (task(t0 + lane, x, y, dst) == 1) tma_load_2d_hint(dst, &kvmap, fb, x, y, pol_keep);
                 }
                 if (++s == kNS) {
                     s = 0;

@@ -300,9 +300,13 @@ def main():
     hbm, tf_burst, tf_sust, src = peaks()
     mean_k = kern.mean(axis=0)
 
-    # with fp8 K/V on tensor memory the prefill kernel also runs the decode-class units
-    # (rpa_read_plan info[15] bit 1): charge it with both classes' work
-    if int(att.plan(max_items=1)[0][15]) & 2:
+    # the decode class is the library's (rpa_read_plan info[5]: rows of a decode tile); with fp8
+    # K/V on tensor memory the prefill kernel also runs the decode-class units (info[15] bit 1):
+    # charge it with both classes' work
+    info = att.plan(max_items=1)[0]
+    if int(info[5]) != 16:
+        work = ri.algorithmic_work(prob, decode_rows=int(info[5]))
+    if int(info[15]) & 2:
         d, pf = work["decode"], work["prefill"]
         work["prefill"] = {k: d[k] + pf[k] for k in pf}
         work["decode"] = {k: 0 for k in d}

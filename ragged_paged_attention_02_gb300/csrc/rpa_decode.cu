@@ -1,4 +1,4 @@
-// rpa_decode.cu -- K1 decode: paged-KV attention for tiles of <= 16 query rows.
+// rpa_decode.cu -- K1 decode: paged-KV attention for tiles of <= 16 (or <= 8) query rows.
 //
 // Decode-class work items (q_len * G <= 16 rows of one kv head, a key range of
 // one sequence) are HBM-bound: every key's K and V rows are read once and
@@ -22,6 +22,10 @@
 //                   written as bf16 o, or as an fp32 split-KV partial for the
 //                   combine kernel.
 //
+// Tiles of at most 8 rows (bf16 K/V, G <= 8; the common decode case) put the
+// keys on the MMA's M side instead: S^T = K Q^T and O^T += V^T P^T, half the
+// MMAs and accumulator registers of a 16-row tile, three CTAs per SM.
+//
 // fp8 e4m3 K/V: stages hold the raw bytes; each consumer warp converts its 16
 // keys to f16 (exact) in its own buffer and runs the MMAs in f16, with
 // k_scale folded into the logit scale and v_scale into the epilogue.
@@ -39,7 +43,7 @@ namespace {
 constexpr int kCW = 4;                  // consumer warps
 constexpr int kDecThreads = 32 * (kCW + 1);
 constexpr int kKS = 64;                 // keys per stage (16 per consumer warp)
-constexpr int kNS = 3;                  // stages in the ring
+// stages in the ring: 3 for 16-row tiles (2 CTAs/SM), 2 for 8-row tiles (3 CTAs/SM)
 constexpr int kMetaWords = 16;
 
 // stage meta words
@@ -48,29 +52,36 @@ enum Meta : int {
     mKey0, mStop
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, int ROWS>
 struct DecGeom {
+    static constexpr int NS = ROWS == 8 ? 2 : 3;   // stages in the ring
     static constexpr int E = FP8 ? 1 : 2;          // bytes per K/V element
     static constexpr int DHQ = D * 2 / 128;        // 128-byte column blocks of a bf16 row
     static constexpr int DH = FP8 ? 1 : DHQ;       // column blocks per K/V box
-    static constexpr int QB = DHQ * 16 * 128;      // Q area: [DHQ][16 lines][128 B]
+    static constexpr int QB = DHQ * ROWS * 128;    // Q area: [DHQ][ROWS lines][128 B]
     static constexpr int KVB = kKS * 2 * D * E;    // K/V area of one stage
     static constexpr int SB = QB + KVB;            // one stage
     static constexpr int CONV = FP8 ? 16 * D * 4 : 0;  // per-warp f16 buffer (K and V, 16 keys)
-    static constexpr int SMEM = kNS * SB + kCW * CONV + 1024;  // + alignment slack
+    static constexpr int SMEM = NS * SB + kCW * CONV + 1024;  // + alignment slack
     static_assert(QB % 1024 == 0 && KVB % 1024 == 0, "stage alignment");
-    static_assert(kCW * 16 * D * 4 <= (FP8 ? kCW * CONV : KVB), "merge area");
+    static_assert(kCW * ROWS * D * 4 <= (FP8 ? kCW * CONV : KVB), "merge area");
+    static_assert(ROWS == 16 || !FP8, "8-row tiles are bf16 only");
 };
 
 __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
     return line * 128u + (((chunk ^ line) & 7u) << 4);
 }
 
-template <int D, bool FP8>
-__global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_constant__ CUtensorMap kvmap,
-                                                               const __grid_constant__ CUtensorMap qmap,
-                                                               const DecParams p) {
-    using Gm = DecGeom<D, FP8>;
+// resident CTAs per SM the register allocation is sized for (shared memory allows 2 at D <= 128,
+// 3 with 8-row tiles; D = 256 fits one)
+template <int D, int ROWS>
+constexpr int dec_min_blocks() { return D > 128 ? 1 : ROWS == 8 ? 3 : 2; }
+
+template <int D, bool FP8, int ROWS>
+__global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_decode_attn(
+    const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap, const DecParams p) {
+    using Gm = DecGeom<D, FP8, ROWS>;
+    constexpr int kNS = Gm::NS;
     constexpr bool F16 = FP8;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kNS];
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
                                                   (st == 0 ? (uint32_t)(Gm::DHQ * p.Tt * a.G * 128) : 0u));
                 __syncwarp();
                 if (st == 0 && lane < Gm::DHQ)
-                    tma_load_3d(st_base + lane * 2048, &qmap, fb, lane * 64, item.head * a.G,
+                    tma_load_3d(st_base + lane * (ROWS * 128), &qmap, fb, lane * 64, item.head * a.G,
                                 q_start + item.tok0);
                 // decode K/V is read once: evict it first, so that it does not push out of L2 the
                 // K/V a concurrent prefill re-reads
@@ -205,6 +216,7 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
         return;
     }
 
+    if constexpr (ROWS == 16) {
     // =============================== consumers ===============================
     const int w = warp;
     const int G = a.G, Hq = a.Hq;
@@ -525,50 +537,312 @@ __global__ void __launch_bounds__(kDecThreads) rpa_decode_attn(const __grid_cons
             ph ^= 1u;
         }
     }
+    } else {
+    // ====================== consumers, tiles of <= 8 rows: keys on the MMA's M side ======================
+    // S^T = K Q^T with A = 16 keys x 16 d of the stage (ldmatrix) and B = Q^T (16 d x 8 rows, registers,
+    // loaded once per item); O^T += V^T P^T with A = 16 d x 16 keys (ldmatrix.trans) and B = P^T (16 keys
+    // x 8 rows, built from S^T's accumulators with four shuffles).  Half the MMAs of a 16-row tile and
+    // half its accumulator registers.  Thread (g = lane / 4, q = lane % 4) holds rows 2q and 2q + 1 of
+    // keys g and g + 8 (S^T), and of d = 16 mt + g and + 8 (O^T, m-tile mt).
+    const int w = warp;
+    const int G = a.G, Hq = a.Hq;
+    const int BR = p.BR, br_shift = p.br_shift;
+    const uint32_t PBB = (uint32_t)(2 * Gm::DH * BR * 128);
+    const int g = lane >> 2, q = lane & 3;
+    int s = 0;
+    uint32_t ph = 0, mph = 0;
+    uint32_t qt[D / 16][2];
+    float o_acc[D / 16][4];
+    float m_r[2], l_r[2];
+    int pos[2];  // kv positions of rows 2q, 2q + 1
+    for (;;) {
+        if (!mbar_wait(smem_u32(&full_bar[s]), ph, ctrl, tmo)) return;
+        const int* m = meta[s];
+        if (m[mStop]) return;
+        const int st = m[mSt], nst = m[mNst];
+        const int kv_begin = m[mKvBegin], kv_end = m[mKvEnd];
+        const int kl = m[mKl], ql = m[mQl];
+        const int tok0 = m[mTok0], ntok = m[mNtok];
+        const uint32_t st_base = smem0 + s * Gm::SB;
+        const uint32_t kv_base = st_base + Gm::QB;
+        if (st == 0) {
+            // Q^T fragments (B operand) for the whole item: rows 0-7 of the stage's Q area, two
+            // k-steps per ldmatrix.x4 (matrix i: d chunk 2 kd + i)
+#pragma unroll
+            for (int kd = 0; kd < D / 16; kd += 2) {
+                const int c = 2 * kd + (lane >> 3);
+                const uint32_t line = (uint32_t)((c >> 3) * ROWS + (lane & 7));
+                ldsm_x4(st_base + swz128(line, c & 7), qt[kd][0], qt[kd][1], qt[kd + 1][0], qt[kd + 1][1]);
+            }
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+            m_r[0] = m_r[1] = -INFINITY;
+            l_r[0] = l_r[1] = 0.f;
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) pos[ri] = kl - ql + tok0 + (2 * q + ri) / G;
+        }
+
+        // ---- this warp's 16 keys: [kw, kw + 16)
+        const int kw = m[mKey0] + 16 * w;
+        const bool any_in = kw < kv_end && kw + 16 > kv_begin;
+        if (any_in) {
+            const bool partial = kw < kv_begin || kw + 16 > kv_end;
+            if (partial) {
+                // keys of this slice outside [kv_begin, kv_end): V rows to zero
+                for (int i = lane; i < 16 * Gm::DH * 8; i += 32) {
+                    const int row = i / (Gm::DH * 8);
+                    const int c = i % (Gm::DH * 8);
+                    const int j = kw + row;
+                    if (j >= kv_begin && j < kv_end) continue;
+                    const int kk = 16 * w + row;
+                    const int b = kk >> br_shift, r = kk & (BR - 1);
+                    const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
+                    *reinterpret_cast<uint4*>(smem + (kv_base - smem0) + b * PBB + swz128(line, c & 7)) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+
+            // ---- S^T = K Q^T  (16 keys x 8 rows); even and odd k-steps in two MMA chains
+            float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sodd[4] = {0.f, 0.f, 0.f, 0.f};
+            {
+                // A matrices: keys 0-7 / 8-15 (lane bit 3) of d chunk 2 kd / 2 kd + 1 (lane bit 4)
+                const int kk = 16 * w + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int b = kk >> br_shift, r = kk & (BR - 1);
+#pragma unroll
+                for (int kd = 0; kd < D / 16; ++kd) {
+                    const int c = 2 * kd + (lane >> 4);
+                    const uint32_t line = (uint32_t)((c >> 3) * BR + r);
+                    uint32_t af[4];
+                    ldsm_x4(kv_base + b * PBB + swz128(line, c & 7), af[0], af[1], af[2], af[3]);
+                    mma16816<false>((kd & 1) ? sodd : sacc, af, qt[kd][0], qt[kd][1]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+            }
+            // ---- scale, softcap, masks (log2 domain); sacc[e]: key g + 8 (e >> 1), row 2q + (e & 1)
+            const bool need_mask = partial || (a.causal && kw + 15 > kl - ql + tok0) ||
+                                   (a.has_window && kw <= kl - ql + tok0 + ntok - 1 - a.window);
+            float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int ri = e & 1;
+                float x = sacc[e];
+                if (a.has_cap) {
+                    const float t = ex2(x * a.cap_exp);
+                    x = a.cap_log2 - 2.f * a.cap_log2 * rcp_approx(1.f + t);
+                } else {
+                    x *= a.qk_log2;
+                }
+                if (need_mask) {
+                    const int j = kw + g + 8 * (e >> 1);
+                    const bool okk = j >= kv_begin && j < kv_end && (!a.causal || j <= pos[ri]) &&
+                                     (!a.has_window || j > pos[ri] - a.window);
+                    x = okk ? x : -INFINITY;
+                }
+                sacc[e] = x;
+                mx[ri] = fmaxf(mx[ri], x);
+            }
+            // row max over the warp's 16 keys: the eight lanes of a row differ in lane bits 2-4
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 4));
+                mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 8));
+                mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 16));
+            }
+            // lazy rescale: the running max moves only when some row's max grows by more than 2^8
+            const bool need = __any_sync(0xffffffffu, mx[0] > m_r[0] + 8.f || mx[1] > m_r[1] + 8.f);
+            if (need) {
+#pragma unroll
+                for (int ri = 0; ri < 2; ++ri) {
+                    const float m_new = fmaxf(m_r[ri], mx[ri]);
+                    const float bse = m_new == -INFINITY ? 0.f : m_new;
+                    const float alpha = m_r[ri] == -INFINITY ? 0.f : ex2(m_r[ri] - bse);
+                    m_r[ri] = m_new;
+                    l_r[ri] *= alpha;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        o_acc[mt][ri] *= alpha;
+                        o_acc[mt][ri + 2] *= alpha;
+                    }
+                }
+            }
+            float base[2];
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) base[ri] = m_r[ri] == -INFINITY ? 0.f : m_r[ri];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float pe = ex2(sacc[e] - base[e & 1]);
+                sacc[e] = pe;
+                l_r[e & 1] += pe;
+            }
+            // ---- P^T as the B operand: b0 = P[key 2q, 2q + 1][row g], b1 = P[key 2q + 8, 2q + 9][row g].
+            // P[key k][row n] (k < 8) sits in lane 4k + n/2, element n % 2 (keys 8-15: elements 2, 3).
+            uint32_t pb0, pb1;
+            {
+                const uint32_t w01 = pack2<false>(sacc[0], sacc[1]);  // key g:     rows 2q, 2q + 1
+                const uint32_t w23 = pack2<false>(sacc[2], sacc[3]);  // key g + 8: rows 2q, 2q + 1
+                const int src0 = 8 * q + (g >> 1), src1 = src0 + 4;   // lanes of keys 2q, 2q + 1
+                const uint32_t x0 = __shfl_sync(0xffffffffu, w01, src0);
+                const uint32_t x1 = __shfl_sync(0xffffffffu, w01, src1);
+                const uint32_t y0 = __shfl_sync(0xffffffffu, w23, src0);
+                const uint32_t y1 = __shfl_sync(0xffffffffu, w23, src1);
+                const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;  // row g's half of each word
+                pb0 = __byte_perm(x0, x1, sel);
+                pb1 = __byte_perm(y0, y1, sel);
+            }
+            // ---- O^T += V^T P^T: A matrices: d chunk 2 mt / 2 mt + 1 (lane bit 3) of keys 0-7 / 8-15
+            // (lane bit 4), transposed
+            {
+                const int kk = 16 * w + (lane & 7) + (lane >> 4) * 8;
+                const int b = kk >> br_shift, r = kk & (BR - 1);
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+                    const int c = 2 * mt + ((lane >> 3) & 1);
+                    const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
+                    uint32_t af[4];
+                    ldsm_x4_t(kv_base + b * PBB + swz128(line, c & 7), af[0], af[1], af[2], af[3]);
+                    mma16816<false>(o_acc[mt], af, pb0, pb1);
+                }
+            }
+        }
+
+        const uint32_t eb = smem_u32(&empty_bar[s]);
+        if (st == nst - 1) {
+            // ---- merge the four warps' partials; the stage's own buffers hold them
+            float* red_o = reinterpret_cast<float*>(smem + (kv_base - smem0));  // [kCW][ROWS][D]
+            float* red_ml = reinterpret_cast<float*>(smem + (st_base - smem0)); // [kCW][ROWS][2]
+            float lsum[2];
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                lsum[ri] = l_r[ri] + __shfl_xor_sync(0xffffffffu, l_r[ri], 4);
+                lsum[ri] += __shfl_xor_sync(0xffffffffu, lsum[ri], 8);
+                lsum[ri] += __shfl_xor_sync(0xffffffffu, lsum[ri], 16);
+            }
+            const uint32_t mb = smem_u32(&merge_bar);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mb);  // A: every warp is done reading the stage
+            if (!mbar_wait(mb, mph, ctrl, tmo)) return;
+            mph ^= 1u;
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    red_o[(w * ROWS + 2 * q + (e & 1)) * D + 16 * mt + g + 8 * (e >> 1)] = o_acc[mt][e];
+            if (g == 0) {
+#pragma unroll
+                for (int ri = 0; ri < 2; ++ri) {
+                    red_ml[(w * ROWS + 2 * q + ri) * 2] = m_r[ri];
+                    red_ml[(w * ROWS + 2 * q + ri) * 2 + 1] = lsum[ri];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(mb);  // B: every partial is in shared memory
+            if (!mbar_wait(mb, mph, ctrl, tmo)) return;
+            mph ^= 1u;
+            const int rows_used = ntok * G;
+            const int part = m[mPart];
+            const int q_start = m[mQStart];
+            const int head = m[mHead];
+            for (int e = w * 32 + lane; e < ROWS * (D / 2); e += kCW * 32) {
+                const int r = e / (D / 2);
+                const int c = (e % (D / 2)) * 2;
+                if (r >= rows_used) break;
+                float M = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < kCW; ++ww) M = fmaxf(M, red_ml[(ww * ROWS + r) * 2]);
+                float L = 0.f, o0 = 0.f, o1 = 0.f;
+                if (M != -INFINITY) {
+#pragma unroll
+                    for (int ww = 0; ww < kCW; ++ww) {
+                        const float sc = ex2(red_ml[(ww * ROWS + r) * 2] - M);
+                        L += sc * red_ml[(ww * ROWS + r) * 2 + 1];
+                        const float2 v = *reinterpret_cast<const float2*>(red_o + (ww * ROWS + r) * D + c);
+                        o0 += sc * v.x;
+                        o1 += sc * v.y;
+                    }
+                }
+                if (part < 0) {
+                    const float inv = L > 0.f ? a.v_scale / L : 0.f;
+                    const int t = q_start + tok0 + r / G;
+                    const int qh = head * G + r % G;
+                    *reinterpret_cast<uint32_t*>(a.o + (((size_t)t * Hq + qh) * D + c) * 2) =
+                        pack2<false>(o0 * inv, o1 * inv);
+                } else {
+                    *reinterpret_cast<float2*>(a.part_o + ((size_t)part * kDecRows + r) * D + c) =
+                        make_float2(o0, o1);
+                    if (c == 0)
+                        *reinterpret_cast<float2*>(a.part_ml + ((size_t)part * kDecRows + r) * 2) =
+                            make_float2(M, L);
+                }
+            }
+            fence_proxy_async_smem();  // the stage will be refilled by bulk copies
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eb);
+        } else {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(eb);
+        }
+        if (++s == kNS) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int ROWS>
 struct DecKern {
-    using Gm = DecGeom<D, FP8>;
+    using Gm = DecGeom<D, FP8, ROWS>;
     static cudaError_t prepare(int* bps) {
-        cudaError_t e = cudaFuncSetAttribute(rpa_decode_attn<D, FP8>,
+        cudaError_t e = cudaFuncSetAttribute(rpa_decode_attn<D, FP8, ROWS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_decode_attn<D, FP8>, kDecThreads,
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_decode_attn<D, FP8, ROWS>, kDecThreads,
                                                              Gm::SMEM);
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p,
                               const Launch& l) {
-        return launch_pdl(rpa_decode_attn<D, FP8>, l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
+        return launch_pdl(rpa_decode_attn<D, FP8, ROWS>, l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 
 }  // namespace
 
-cudaError_t decode_prepare(int D, int fp8, int* bps) {
+cudaError_t decode_prepare(int D, int fp8, int rows, int* bps) {
     if (fp8) {
-        if (D == 64) return DecKern<64, true>::prepare(bps);
-        if (D == 128) return DecKern<128, true>::prepare(bps);
-        if (D == 256) return DecKern<256, true>::prepare(bps);
+        if (rows != 16) return cudaErrorInvalidValue;
+        if (D == 64) return DecKern<64, true, 16>::prepare(bps);
+        if (D == 128) return DecKern<128, true, 16>::prepare(bps);
+        if (D == 256) return DecKern<256, true, 16>::prepare(bps);
+    } else if (rows == 8) {
+        if (D == 64) return DecKern<64, false, 8>::prepare(bps);
+        if (D == 128) return DecKern<128, false, 8>::prepare(bps);
+        if (D == 256) return DecKern<256, false, 8>::prepare(bps);
     } else {
-        if (D == 64) return DecKern<64, false>::prepare(bps);
-        if (D == 128) return DecKern<128, false>::prepare(bps);
-        if (D == 256) return DecKern<256, false>::prepare(bps);
+        if (D == 64) return DecKern<64, false, 16>::prepare(bps);
+        if (D == 128) return DecKern<128, false, 16>::prepare(bps);
+        if (D == 256) return DecKern<256, false, 16>::prepare(bps);
     }
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int fp8,
-                              const Launch& l) {
-    const int D = p.a.D;
+                              int rows, const Launch& l) {
     if (fp8) {
-        if (D == 64) return DecKern<64, true>::launch(kvm, qm, p, l);
-        if (D == 128) return DecKern<128, true>::launch(kvm, qm, p, l);
-        if (D == 256) return DecKern<256, true>::launch(kvm, qm, p, l);
+        if (rows != 16) return cudaErrorInvalidValue;
+        if (p.a.D == 64) return DecKern<64, true, 16>::launch(kvm, qm, p, l);
+        if (p.a.D == 128) return DecKern<128, true, 16>::launch(kvm, qm, p, l);
+        if (p.a.D == 256) return DecKern<256, true, 16>::launch(kvm, qm, p, l);
+    } else if (rows == 8) {
+        if (p.a.D == 64) return DecKern<64, false, 8>::launch(kvm, qm, p, l);
+        if (p.a.D == 128) return DecKern<128, false, 8>::launch(kvm, qm, p, l);
+        if (p.a.D == 256) return DecKern<256, false, 8>::launch(kvm, qm, p, l);
     } else {
-        if (D == 64) return DecKern<64, false>::launch(kvm, qm, p, l);
-        if (D == 128) return DecKern<128, false>::launch(kvm, qm, p, l);
-        if (D == 256) return DecKern<256, false>::launch(kvm, qm, p, l);
+        if (p.a.D == 64) return DecKern<64, false, 16>::launch(kvm, qm, p, l);
+        if (p.a.D == 128) return DecKern<128, false, 16>::launch(kvm, qm, p, l);
+        if (p.a.D == 256) return DecKern<256, false, 16>::launch(kvm, qm, p, l);
     }
     return cudaErrorInvalidValue;
 }

@@ -36,6 +36,7 @@ struct RpaHandle {
     float qk_log2, cap_exp, cap_log2, v_scale;
     int window;
     int BR, br_shift, Tt;
+    int dec_rows;         // query rows of a decode tile: 8 (bf16, G <= 8) or 16
     int debug_stall;
     unsigned long long timeout_ns;
     void* ws;
@@ -194,7 +195,9 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     while ((int)(c.page_size % h->BR)) h->BR >>= 1;
     h->br_shift = 0;
     while ((1 << h->br_shift) < h->BR) ++h->br_shift;
-    h->Tt = h->G <= kDecRows ? kDecRows / h->G : 1;
+    // 8-row decode tiles (keys on the MMA's M side) whenever a group fits: bf16 K/V, G <= 8
+    h->dec_rows = (!h->fp8 && h->G <= 8) ? 8 : kDecRows;
+    h->Tt = h->G <= h->dec_rows ? h->dec_rows / h->G : 1;
     h->tc = (!h->fp8 && (h->D == 64 || h->D == 128)) ? 1 : 0;
     h->tc8 = (h->fp8 && (h->D == 128 || h->D == 256)) ? 1 : 0;
     h->pf_tokens = h->tc    ? 2 * (kTcRows / h->G)
@@ -231,7 +234,8 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
                       : h->tc8 ? prefill_tc8_prepare(h->D, &h->pf_bps)
                                : attn_prepare(h->D, h->fp8, &h->pf_bps)) != cudaSuccess)
             step = "prefill kernel attributes";
-        else if ((e = decode_prepare(h->D, h->fp8, &h->dec_bps)) != cudaSuccess) step = "decode kernel attributes";
+        else if ((e = decode_prepare(h->D, h->fp8, h->dec_rows, &h->dec_bps)) != cudaSuccess)
+            step = "decode kernel attributes";
         else if (h->pf_bps < 1) step = "prefill kernel cannot be resident";
         else if (h->dec_bps < 1) step = "decode kernel cannot be resident";
         if (step[0]) {
@@ -325,7 +329,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.causal = c.is_causal ? 1 : 0;
     pp.has_window = c.has_sliding_window ? 1 : 0;
     pp.window = h->window;
-    pp.dec_rows = kDecRows;
+    pp.dec_rows = h->dec_rows;
     pp.pf_tokens = h->pf_tokens;
     pp.dec_slots = h->sms * h->dec_bps;
     pp.concurrent = h->concurrent;
@@ -418,7 +422,8 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
         dp.Tt = h->Tt;
         dp.debug_stall = h->debug_stall;
         dp.timeout_ns = h->timeout_ns;
-        if (launch_decode_tma(h->kvmap, h->qmap, dp, h->fp8, Launch{h->sms * h->dec_bps, dst}) != cudaSuccess)
+        if (launch_decode_tma(h->kvmap, h->qmap, dp, h->fp8, h->dec_rows, Launch{h->sms * h->dec_bps, dst}) !=
+            cudaSuccess)
             return RPA_ERR_CUDA;
     }
     if (ev[2] && cudaEventRecord(ev[2], dst) != cudaSuccess) return RPA_ERR_CUDA;
@@ -580,7 +585,7 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[2] = ctrl[kNumPfItems];
     info[3] = ctrl[kNumComb];
     info[4] = ctrl[kDecChunk];
-    info[5] = kDecRows;
+    info[5] = h->dec_rows;
     info[6] = h->pf_tokens;
     info[7] = ctrl[kNumPart];
     info[8] = ctrl[kNumUnits];

@@ -57,7 +57,7 @@ constexpr int kPlanThreads = 1024;
 // lower than either kernel alone, which shares no SMs, L2 or HBM bandwidth.
 constexpr int kPfSmGflopsTc = 6500;
 constexpr int kPfSmGflopsMma = 800;
-constexpr int kDecSmGBs = 68;
+constexpr int kDecSmGBs = 78;
 constexpr int kHbmGBs = 6700;
 
 struct PlanParams {
@@ -167,9 +167,10 @@ cudaError_t launch_pdl(Kern k, int grid, int block, size_t smem, cudaStream_t st
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
 cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l);
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
+// rows: query rows of a decode tile, 16 (any) or 8 (bf16 K/V, G <= 8: keys on the MMA's M side)
 cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int fp8,
-                              const Launch& l);
-cudaError_t decode_prepare(int D, int fp8, int* blocks_per_sm);
+                              int rows, const Launch& l);
+cudaError_t decode_prepare(int D, int fp8, int rows, int* blocks_per_sm);
 cudaError_t launch_prefill_tc(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l);
 cudaError_t prefill_tc_prepare(int D, int* blocks_per_sm);
 cudaError_t launch_prefill_tc8(const CUtensorMap& kvm_runs, const CUtensorMap& qm, const TcParams& p,

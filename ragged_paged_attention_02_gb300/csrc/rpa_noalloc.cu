@@ -28,9 +28,9 @@ static __device__ __align__(256) unsigned char g_rpa_scratch[kNoAllocScratchByte
 
 std::mutex g_mu;
 void* g_scratch_dev[kMaxDevices];
-int g_dec_bps[kMaxDevices][3][2];  // [device][D: 64,128,256][fp8]
-int g_pf_bps[kMaxDevices][3][2];
-bool g_ready[kMaxDevices][3][2];
+int g_dec_bps[kMaxDevices][3][2][2];  // [device][D: 64,128,256][fp8][8-row decode tiles]
+int g_pf_bps[kMaxDevices][3][2][2];
+bool g_ready[kMaxDevices][3][2][2];
 bool g_plan_ready[kMaxDevices];
 
 int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
@@ -40,7 +40,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // Once per device (and per head size / K/V type for the kernel attributes),
 // with that device current: fetch the scratch array's device address and set
 // the kernels' shared-memory limits.  None of this allocates.
-int setup(int dev, int D, int fp8, void** scratch, int* dec_bps, int* pf_bps) {
+int setup(int dev, int D, int fp8, int dec_rows, void** scratch, int* dec_bps, int* pf_bps) {
     if (dev < 0 || dev >= kMaxDevices) return RPA_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_scratch_dev[dev]) {
@@ -58,24 +58,24 @@ int setup(int dev, int D, int fp8, void** scratch, int* dec_bps, int* pf_bps) {
         }
         g_plan_ready[dev] = true;
     }
-    const int di = d_index(D);
-    if (!g_ready[dev][di][fp8]) {
+    const int di = d_index(D), r8 = dec_rows == 8 ? 1 : 0;
+    if (!g_ready[dev][di][fp8][r8]) {
         int a = 0, b = 0;
         const bool tc = !fp8 && (D == 64 || D == 128);
         const bool tc8 = fp8 && (D == 128 || D == 256);
-        if (decode_prepare(D, fp8, &a) != cudaSuccess ||
+        if (decode_prepare(D, fp8, dec_rows, &a) != cudaSuccess ||
             (tc ? prefill_tc_prepare(D, &b) : tc8 ? prefill_tc8_prepare(D, &b) : attn_prepare(D, fp8, &b)) !=
                 cudaSuccess) {
             cudaGetLastError();
             return RPA_ERR_CUDA;
         }
-        g_dec_bps[dev][di][fp8] = a < 1 ? 1 : a;
-        g_pf_bps[dev][di][fp8] = b < 1 ? 1 : b;
-        g_ready[dev][di][fp8] = true;
+        g_dec_bps[dev][di][fp8][r8] = a < 1 ? 1 : a;
+        g_pf_bps[dev][di][fp8][r8] = b < 1 ? 1 : b;
+        g_ready[dev][di][fp8][r8] = true;
     }
     *scratch = g_scratch_dev[dev];
-    *dec_bps = g_dec_bps[dev][di][fp8];
-    *pf_bps = g_pf_bps[dev][di][fp8];
+    *dec_bps = g_dec_bps[dev][di][fp8][r8];
+    *pf_bps = g_pf_bps[dev][di][fp8][r8];
     return RPA_OK;
 }
 
@@ -106,7 +106,8 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     }
     void* scratch = nullptr;
     int dec_bps = 1, pf_bps = 1;
-    const int su = setup(dev, D, fp8, &scratch, &dec_bps, &pf_bps);
+    const int dec_rows = (!fp8 && G <= 8) ? 8 : kDecRows;  // the same rule as rpa_create
+    const int su = setup(dev, D, fp8, dec_rows, &scratch, &dec_bps, &pf_bps);
     if (su != RPA_OK) return su;
 
     // worst-case capacities, the same rule as rpa_create's workspace
@@ -163,7 +164,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     pp.causal = c.is_causal ? 1 : 0;
     pp.has_window = c.has_sliding_window ? 1 : 0;
     pp.window = window;
-    pp.dec_rows = kDecRows;
+    pp.dec_rows = dec_rows;
     pp.pf_tokens = pf_tokens;
     pp.dec_slots = (int)dec_slots;
     pp.concurrent = 0;  // one stream: decode and prefill run one after the other on all SMs
@@ -223,7 +224,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
         int BR = 64, br_shift = 0;
         while ((int)(c.page_size % BR)) BR >>= 1;
         while ((1 << br_shift) < BR) ++br_shift;
-        const int Tt = G <= kDecRows ? kDecRows / G : 1;
+        const int Tt = G <= dec_rows ? dec_rows / G : 1;
         CUtensorMap kvm, kvm_pf, qm, qm_pf;  // descriptors are encoded on the host stack
         if (encode_kv_map_runs(&kvm, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0 ||
             (tc && encode_kv_map(&kvm_pf, kv_pages, fp8, c.total_num_pages, (int)c.page_size, (int)Hkv, D, BR) != 0) ||
@@ -240,7 +241,8 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
         dp.Tt = Tt;
         dp.debug_stall = 0;
         dp.timeout_ns = 1000000000ull;
-        if (launch_decode_tma(kvm, qm, dp, fp8, Launch{(int)dec_slots, st}) != cudaSuccess) return RPA_ERR_CUDA;
+        if (launch_decode_tma(kvm, qm, dp, fp8, dec_rows, Launch{(int)dec_slots, st}) != cudaSuccess)
+            return RPA_ERR_CUDA;
         ap.items = pf_items;
         ap.item_count_word = kNumPfItems;
         ap.counter_word = kPfCounter;

@@ -20,7 +20,7 @@ def band(kl, ql, i0, i1, causal, window):
 
 
 # rates of the SM-split model (FLOP/ns per SM on prefill, B/ns per SM decode, HBM B/ns)
-PF_SM_GFLOPS_TC, PF_SM_GFLOPS_MMA, DEC_SM_GBS, HBM_GBS = 6500, 800, 68, 6700
+PF_SM_GFLOPS_TC, PF_SM_GFLOPS_MMA, DEC_SM_GBS, HBM_GBS = 6500, 800, 78, 6700
 
 
 def split(prob, dec_keyheads, pf_keys, n_sms, dec_bps, pf_bps, concurrent, force_pf=0, force_dec=0):

@@ -117,7 +117,7 @@ def test_planner_matches_python_rederivation():
         att = RaggedPagedAttention(**p.cfg_dict())
         att.forward(*to_dev(p), p.num_seqs)
         info, items = att.plan()
-        ref = plan(p, pf_tokens=int(info[6]), n_sms=int(info[12]), dec_bps=int(info[13]),
+        ref = plan(p, dec_rows=int(info[5]), pf_tokens=int(info[6]), n_sms=int(info[12]), dec_bps=int(info[13]),
                    pf_bps=int(info[14]), concurrent=bool(info[15] & 1), dec_on_pf=bool(info[15] & 2))
         assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
         assert info[10] == ref["dec_ctas"] and info[11] == ref["pf_ctas"]

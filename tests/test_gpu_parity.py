@@ -61,6 +61,15 @@ SMALL = [
               page_size=8, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.2, sm_scale=1 / 16)),
     (42, dict(num_seqs=5, max_q=100, max_kv=400, num_q_heads=6, num_kv_heads=2, head_dim=128,
               page_size=16, kv_dtype="fp8_e4m3", k_scale=0.05, soft_cap=30.0, sliding_window=150)),
+    # decode tiles of <= 8 rows (keys on the MMA's M side): G = 8 / 1 / 3 at the 8-row class
+    # boundary, D 64 / 256 / 128, long keys split across CTAs; and 16-row tiles for G = 16
+    (43, dict(num_seqs=12, decode_only=True, max_kv=5000, num_q_heads=16, num_kv_heads=2, head_dim=64,
+              page_size=32)),
+    (44, dict(num_seqs=10, max_q=12, max_kv=3000, num_q_heads=4, num_kv_heads=4, head_dim=256,
+              page_size=8, sliding_window=700)),
+    (45, dict(num_seqs=9, max_q=3, max_kv=4000, num_q_heads=9, num_kv_heads=3, head_dim=128,
+              soft_cap=20.0, is_causal=False)),
+    (46, dict(num_seqs=8, decode_only=True, max_kv=4000, num_q_heads=32, num_kv_heads=2, head_dim=128)),
 ]
 
 

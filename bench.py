@@ -214,11 +214,45 @@ def run_reference(args, rank):
     print(json.dumps(line, default=float), flush=True)
 
 
+def rank_layout():
+    """(world size, rank, local rank) as torch.distributed.run exports them; 1, 0, 0 alone."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_ranks(world):
+    """Join the process group when launched as several ranks (NCCL on GPUs, gloo on the CPU).
+
+    The ranks are independent replicas: the group carries only the barriers around the timed
+    region and the max-reduction of its length, never attention data."""
+    if world <= 1:
+        return None
+    import torch
+    import torch.distributed as dist
+
+    dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return dist
+
+
+def max_over_ranks(ms, dist, device):
+    """The job's elapsed time: the largest of the ranks' own (the job ends with its slowest)."""
+    if dist is None:
+        return float(ms)
+    import torch
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, steps, world, ms_total):
+    """Whole-job query tokens per second: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * steps * world / (ms_total / 1e3)
+
+
 def main():
     args = parse()
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = rank_layout()
     if args.impl == "reference":
         run_reference(args, rank)
         return
@@ -227,11 +261,7 @@ def main():
     import __graft_entry__
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dist = init_ranks(world)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if rank == 0 or world == 1:
@@ -287,13 +317,10 @@ def main():
     clk = clocks.stop()
     ms_total = e0.elapsed_time(e1)
     kern = att.profile_read(K)  # [K, 4] ms
-    if dist is not None:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist, dev)
     ms_step = ms_total / K
     tokens = work["q_tokens"]
-    value = tokens * K * world / (ms_total / 1e3)
+    value = job_throughput(tokens, K, world, ms_total)
 
     # per-kernel roofline: each attention kernel is charged with its own sequences' work,
     # bound by whichever of HBM bytes / tensor FLOPs takes longer at peak
@@ -351,13 +378,9 @@ def main():
             att.forward_host(hq, kv, hkvl, hpi, hcu, prob.num_seqs, hout, stream=stream)
         a1.record(stream)
         torch.cuda.synchronize()
-        ms_e = a0.elapsed_time(a1)
-        if dist is not None:
-            t = torch.tensor([ms_e], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_e = float(t.item())
+        ms_e = max_over_ranks(a0.elapsed_time(a1), dist, dev)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hkvl, hpi, hcu))
-        e2e = {"value": tokens * Ke * world / (ms_e / 1e3), "unit": "tokens/s",
+        e2e = {"value": job_throughput(tokens, Ke, world, ms_e), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
                "ms_per_step": ms_e / Ke, "steps": Ke}
 

@@ -261,28 +261,35 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
             uint32_t j_all = 0;   // key tiles issued so far (all items): phase of s_full / p_full / pv_done
             uint32_t items = 0;   // items finished
             bool ok = true;
+            // descriptors are formed once per call and offset per MMA in their low (address) half:
+            // the MMA thread shares its sub-partition with two softmax warps, so each MMA costs it
+            // only a few issue slots
             auto issue_qk = [&](int x, int ss) {
-                const uint32_t qsl = q_base + x * Gm::QTILE;
-                const uint32_t kst = kv_base + ss * Gm::STAGE;
+                const uint64_t qd = umma_sdesc(q_base + x * Gm::QTILE, 16, 1024);
+                const uint64_t kd = umma_sdesc(kv_base + ss * Gm::STAGE, 16, 1024);
+                const uint32_t qd_lo = (uint32_t)qd, qd_hi = (uint32_t)(qd >> 32);
+                const uint32_t kd_lo = (uint32_t)kd, kd_hi = (uint32_t)(kd >> 32);
+                const uint32_t sd = tmem + Gm::TM_S(x);
+                umma_ss_c<0>(sd, qd_lo, qd_hi, kd_lo, kd_hi, idesc_qk);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t qoff = (uint32_t)((kk >> 2) * (kM * 128) + (kk & 3) * 32);
-                    const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
-                    umma_ss(tmem + Gm::TM_S(x), umma_sdesc(qsl + qoff, 16, 1024), umma_sdesc(kst + koff, 16, 1024),
-                            idesc_qk, kk > 0 ? 1 : 0);
-                }
+                for (int kk = 1; kk < D / 16; ++kk)
+                    umma_ss_c<1>(sd, qd_lo + ((kk >> 2) * (kM * 128) + (kk & 3) * 32) / 16, qd_hi,
+                                 kd_lo + ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) / 16, kd_hi, idesc_qk);
                 umma_commit(smem_u32(&s_full[x]));
             };
             auto issue_pv = [&](int x, int ss, uint32_t jj, bool first) -> bool {
                 if (!mbar_wait(smem_u32(&p_full[x]), jj & 1u, ctrl, tmo)) return false;
                 tc_fence_after();
-                const uint32_t vst = kv_base + ss * Gm::STAGE + Gm::KBYTES;
+                const uint64_t vd = umma_sdesc(kv_base + ss * Gm::STAGE + Gm::KBYTES, kBN * 128, 1024);
+                const uint32_t vd_lo = (uint32_t)vd, vd_hi = (uint32_t)(vd >> 32);
+                const uint32_t od = tmem + Gm::TM_O(x), pa = tmem + Gm::TM_S(x);
+                if (first)
+                    umma_ts_c<0>(od, pa, vd_lo, vd_hi, idesc_pv);
+                else
+                    umma_ts_c<1>(od, pa, vd_lo, vd_hi, idesc_pv);
 #pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk) {
-                    const uint64_t bdesc = umma_sdesc(vst + kk * 16 * 128, kBN * 128, 1024);
-                    umma_ts(tmem + Gm::TM_O(x), tmem + Gm::TM_S(x) + kk * 8, bdesc, idesc_pv,
-                            (!first || kk > 0) ? 1 : 0);
-                }
+                for (int kk = 1; kk < kBN / 16; ++kk)
+                    umma_ts_c<1>(od, pa + kk * 8, vd_lo + kk * 16 * 128 / 16, vd_hi, idesc_pv);
                 umma_commit(smem_u32(&pv_done[x]));
                 return true;
             };

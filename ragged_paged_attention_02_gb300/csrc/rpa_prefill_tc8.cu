@@ -11,21 +11,28 @@
 //   producer warp    Q tile (bf16) into a staging buffer, then per 64-key tile
 //                    the raw fp8 K/V rows of each page run (one bulk tensor
 //                    copy per run: K and V of the head) into a 2-slot ring.
-//   4 converter      Q: bf16 -> f16 into TMEM (the A operand of S = Q K^T);
-//   warps            K and V: e4m3 -> f16 into double-buffered, 128-byte
-//                    swizzled tiles (K-major), keys outside the item's
-//                    [kv_begin, kv_end) written as zero (the page zeroes K/V
-//                    past kv_len; tail slots may hold any bits).
+//   8 converter      Q (warps on lane quadrants 0-3): bf16 -> f16 into TMEM
+//   warps            (the A operand of S = Q K^T).  K and V: each warp takes 8
+//                    key rows of a tile into registers (the ring slot goes
+//                    straight back to the producer), then e4m3 -> f16 into
+//                    double-buffered, 128-byte swizzled tiles (K-major), keys
+//                    outside the item's [kv_begin, kv_end) written as zero
+//                    (the page zeroes K/V past kv_len; tail slots may hold any
+//                    bits).
 //   MMA warp         S = Q K^T (A from TMEM, B from smem) into one of two TMEM
 //                    S buffers; O += P V (P from TMEM over S, V MN-major).
-//   4 softmax warps  thread r owns TMEM lane r (query row r): scale / softcap /
-//                    masks in the log2 domain, running max and sum, P in f16,
-//                    lazy O rescale (max grows by more than 2^8), epilogue.
+//   8 softmax warps  two per TMEM lane quadrant, one per half of the key tile:
+//                    scale / softcap / masks in the log2 domain, running max
+//                    and sum, P in f16, lazy O rescale (max grows by more than
+//                    2^8), epilogue.  Items of at most 64 rows hold each query
+//                    row in 2, 4 or 8 TMEM lanes that split the keys.
 //
 // TMEM: Q (D/2 columns of packed f16 pairs), S0, S1 (64 each), O (D) -- 512
 // columns at D = 256.  All waits are bounded; on expiry the status word gets
 // RPA_ERR_TIMEOUT.
 #include <cuda.h>
+
+#include <type_traits>
 
 #include "rpa_internal.cuh"
 
@@ -45,6 +52,7 @@ constexpr int kConvRows = kBN / kNConv;  // key rows of a tile per converter war
 constexpr int kRegBoundThreads = 640;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
+constexpr uint32_t kIssueNapNs = 100;  // longest suspension of the MMA thread's idle wait
 
 enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, eNtok, eNt, eKey0, eStop, ePart };
 
@@ -92,30 +100,39 @@ __device__ __forceinline__ uint4 e4m3x8_to_f16x8_hw(uint32_t w0, uint32_t w1) {
                       e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
 }
 
-// One converter warp's key rows (kConvRows cw .. + kConvRows - 1) of one half (K or V) of a raw stage
-// ([run][K | V][BR rows][D bytes]; `raw` points at the half's first run) into a 128-byte
-// swizzled f16 tile [D / 64][64 rows][128 B].  Keys outside [kv_begin, kv_end) become zero.
-// HW: exact hardware conversion, else the integer placement (value / 2^8).  A lane converts 16
-// consecutive bytes of a row (D / 16 lanes a row, RPP rows a pass); all loads are issued first.
-template <int D, bool HW>
-__device__ __forceinline__ void convert_rows(const uint8_t* raw, uint8_t* dst, int cw, int lane, int brs, int k_lo,
-                                             int kv_begin, int kv_end) {
-    constexpr int LPR = D / 16, RPP = 32 / LPR, NP = kConvRows / RPP;
+// One converter warp's key rows (kConvRows cw .. + kConvRows - 1) of one half (K or V) of a raw
+// stage ([run][K | V][BR rows][D bytes]; `raw` points at the half's first run): a lane takes 16
+// consecutive bytes of a row (D / 16 lanes a row, RPP rows a pass, NP passes).
+template <int D>
+struct ConvLanes {
+    static constexpr int LPR = D / 16, RPP = 32 / LPR, NP = kConvRows / RPP;
+};
+template <int D>
+__device__ __forceinline__ void load_rows(const uint8_t* raw, int cw, int lane, int brs, uint4* v) {
+    using C = ConvLanes<D>;
     const int BR = 1 << brs;
-    const int e = lane % LPR, r0 = lane / LPR;
-    uint4 v[NP];
+    const int e = lane % C::LPR, r0 = lane / C::LPR;
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
-        const int key = kConvRows * cw + r0 + i * RPP;
+    for (int i = 0; i < C::NP; ++i) {
+        const int key = kConvRows * cw + r0 + i * C::RPP;
         v[i] = *reinterpret_cast<const uint4*>(raw + (key >> brs) * (2 * BR * D) + (key & (BR - 1)) * D + e * 16);
     }
+}
+// ... and those rows, converted, into a 128-byte swizzled f16 tile [D / 64][64 rows][128 B]; keys
+// outside [kv_begin, kv_end) become zero.  HW: exact hardware conversion, else the integer
+// placement (value / 2^8).
+template <int D, bool HW>
+__device__ __forceinline__ void store_rows(const uint4* v, uint8_t* dst, int cw, int lane, int k_lo, int kv_begin,
+                                           int kv_end) {
+    using C = ConvLanes<D>;
+    const int e = lane % C::LPR, r0 = lane / C::LPR;
     // the 16 elements are f16 chunks 2e, 2e+1 of column block e / 4; lanes of odd (e / 4) store
     // their second chunk first so that each store of 8 lanes covers all 32 banks
     const bool sw = (e >> 2) & 1;
     const int cb = e >> 2, c0 = (2 * e) & 7;
 #pragma unroll
-    for (int i = 0; i < NP; ++i) {
-        const int key = kConvRows * cw + r0 + i * RPP;
+    for (int i = 0; i < C::NP; ++i) {
+        const int key = kConvRows * cw + r0 + i * C::RPP;
         const int j = k_lo + key;
         const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
         const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
@@ -162,6 +179,31 @@ __device__ __forceinline__ float tile_logits(uint32_t* sv, float qk, float capl,
         sv[i + 1] = __float_as_uint(v1);
     }
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// Copies of each query row in a 128-row tile (a power of two; see the softmax warps)
+__device__ __forceinline__ int row_copies(int rows) { return rows <= 16 ? 8 : rows <= 32 ? 4 : rows <= 64 ? 2 : 1; }
+
+// The N = 32 / F logits of copy c among a lane's 32: kv[i] = sv[c N + i]
+template <int F>
+__device__ __forceinline__ void pick_keys(const uint32_t* sv, int c, uint32_t* kv) {
+    constexpr int N = 32 / F;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        uint32_t x = sv[i];
+#pragma unroll
+        for (int k = 1; k < F; ++k) x = c == k ? sv[k * N + i] : x;
+        kv[i] = x;
+    }
+}
+
+// Sum of a row's copies (lanes l, l ^ R, l ^ 2R, ...) of 32 O columns, in every lane
+__device__ __forceinline__ void add_copies(uint32_t* ov, int R) {
+    for (int x = R; x < 32; x <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            ov[i] = __float_as_uint(__uint_as_float(ov[i]) + __uint_as_float(__shfl_xor_sync(0xffffffffu, ov[i], x)));
+    }
 }
 
 template <int D>
@@ -328,9 +370,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
         }
     } else if (warp >= kConv0 && warp < kConv0 + kNConv) {
         // =============================== converters ===============================
-        const int cw = warp - kConv0;        // converter warp 0..7; 0..3 also convert Q
-        const bool qconv = cw < 4;           // its TMEM lane quadrant is cw (warp % 4)
-        const int r = (cw & 3) * 32 + lane;  // TMEM lane (query row) for the Q conversion
+        const int cw = warp - kConv0;  // converter warp 0..7; 0..3 also convert Q
+        const bool qconv = cw < 4;     // its TMEM lane quadrant is cw (warp % 4)
         const uint32_t lane_addr = tmem + ((uint32_t)((cw & 3) * 32) << 16);
         const int BR = p.BR, brs = __ffs(BR) - 1;
         int s = 0, ms = 0;
@@ -340,7 +381,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
             const int* mm = meta[ms];
             const int stop = mm[eStop], kv_begin = mm[eKvBegin], kv_end = mm[eKvEnd], nt = mm[eNt],
-                      key0 = mm[eKey0];
+                      key0 = mm[eKey0], ntok = mm[eNtok];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&meta_free[ms]));
             if (stop) break;
@@ -348,7 +389,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 ms = 0;
                 mph ^= 1u;
             }
-            // ---- Q: bf16 staging -> f16 TMEM columns (thread r owns query row r)
+            // ---- Q: bf16 staging -> f16 TMEM columns; TMEM lane (cw & 3) 32 + lane holds query
+            // row (cw & 3) R + lane % R (R = 32 / copies of each row)
+            const int R = 32 / row_copies(ntok * a.G);
+            const int r = (cw & 3) * R + lane % R;
             if (qconv && items > 0 && !mbar_wait(smem_u32(&qt_free), (items - 1) & 1u, ctrl, tmo)) break;
             bool ok = true;
             for (int rd = 0; rd < (qconv ? Gm::ROUNDS : 0); ++rd) {
@@ -384,17 +428,30 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             for (int t = 0; t < nt; ++t, ++tg) {
                 const int b2 = tg & 1;
                 const uint32_t par = (tg >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&raw_full[s]), ph, ctrl, tmo) ||
-                    !mbar_wait(smem_u32(&k_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                if (!mbar_wait(smem_u32(&raw_full[s]), ph, ctrl, tmo)) {
                     ok = false;
                     break;
                 }
+                // the warp's K and V rows of the stage into registers, and the stage straight back
+                // to the producer: the next copy starts while this tile is being converted
                 const uint8_t* raw = smem + (raw_base - smem0) + s * Gm::RAW;
+                uint4 kr[ConvLanes<D>::NP], vr[ConvLanes<D>::NP];
+                load_rows<D>(raw, cw, lane, brs, kr);
+                load_rows<D>(raw + BR * D, cw, lane, brs, vr);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&raw_empty[s]));
+                if (++s == 2) {
+                    s = 0;
+                    ph ^= 1u;
+                }
                 const int k_lo = key0 + t * kBN;
                 // K exactly (hardware conversion), then V as value / 2^8 (integer placement): the
                 // two halves load the special-function and the integer pipes about evenly
-                convert_rows<D, true>(raw, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, brs, k_lo, kv_begin,
-                                      kv_end);
+                if (!mbar_wait(smem_u32(&k_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                    ok = false;
+                    break;
+                }
+                store_rows<D, true>(kr, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&k_full[b2]));
@@ -402,17 +459,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     ok = false;
                     break;
                 }
-                convert_rows<D, false>(raw + BR * D, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, brs, k_lo,
-                                       kv_begin, kv_end);
+                store_rows<D, false>(vr, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&v_full[b2]));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&raw_empty[s]));
-                if (++s == 2) {
-                    s = 0;
-                    ph ^= 1u;
-                }
             }
             if (!ok) break;
             ++items;
@@ -452,14 +502,14 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const int b2 = g & 1;
                         if (mbar_test(smem_u32(&k_full[b2]), (g >> 1) & 1u)) {
                             tc_fence_after();
-                            const uint32_t kt = k16_base + b2 * Gm::T16;
-                            const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+                            const uint64_t kd = umma_sdesc(k16_base + b2 * Gm::T16, 16, 1024);
+                            const uint32_t kd_lo = (uint32_t)kd, kd_hi = (uint32_t)(kd >> 32);
+                            const uint32_t sd = tmem + (b2 ? Gm::TM_S1 : Gm::TM_S0), qa = tmem + Gm::TM_Q;
+                            umma_ts_c<0>(sd, qa, kd_lo, kd_hi, idesc_qk);
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t koff = (uint32_t)((kk >> 2) * (kBN * 128) + (kk & 3) * 32);
-                                umma_ts(tmem + scol, tmem + Gm::TM_Q + kk * 8, umma_sdesc(kt + koff, 16, 1024),
-                                        idesc_qk, kk > 0 ? 1 : 0);
-                            }
+                            for (int kk = 1; kk < D / 16; ++kk)
+                                umma_ts_c<1>(sd, qa + kk * 8, kd_lo + ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) / 16, kd_hi,
+                                             idesc_qk);
                             umma_commit(smem_u32(&s_full[b2]));
                             umma_commit(smem_u32(&k_empty[b2]));
                             if (tq == nt - 1) umma_commit(smem_u32(&qt_free));
@@ -475,14 +525,16 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         if (mbar_test(smem_u32(&p_full[b2]), par) && mbar_test(smem_u32(&v_full[b2]), par) &&
                             (!first || items == 0 || mbar_test(smem_u32(&o_free), (items - 1) & 1u))) {
                             tc_fence_after();
-                            const uint32_t vt = v16_base + b2 * Gm::T16;
-                            const uint32_t scol = b2 ? Gm::TM_S1 : Gm::TM_S0;
+                            const uint64_t vd = umma_sdesc(v16_base + b2 * Gm::T16, kBN * 128, 1024);
+                            const uint32_t vd_lo = (uint32_t)vd, vd_hi = (uint32_t)(vd >> 32);
+                            const uint32_t od = tmem + Gm::TM_O, pa = tmem + (b2 ? Gm::TM_S1 : Gm::TM_S0);
+                            if (first)
+                                umma_ts_c<0>(od, pa, vd_lo, vd_hi, idesc_pv);
+                            else
+                                umma_ts_c<1>(od, pa, vd_lo, vd_hi, idesc_pv);
 #pragma unroll
-                            for (int kk = 0; kk < kBN / 16; ++kk) {
-                                const uint64_t bdesc = umma_sdesc(vt + kk * 16 * 128, kBN * 128, 1024);
-                                umma_ts(tmem + Gm::TM_O, tmem + scol + kk * 8, bdesc, idesc_pv,
-                                        (!first || kk > 0) ? 1 : 0);
-                            }
+                            for (int kk = 1; kk < kBN / 16; ++kk)
+                                umma_ts_c<1>(od, pa + kk * 8, vd_lo + kk * 16 * 128 / 16, vd_hi, idesc_pv);
                             umma_commit(smem_u32(&v_empty[b2]));
                             umma_commit(smem_u32(&pv_done));
                             ++tp;
@@ -492,7 +544,23 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     if (did) {
                         idle = 0;
                         t_idle = 0;
-                    } else if (++idle >= 64) {
+                        continue;
+                    }
+                    // nothing ready: sleep briefly on a barrier the next PV or QK waits for (the two
+                    // in turn when both wait), which leaves the sub-partition's issue slots to the
+                    // softmax and converter warps
+                    {
+                        const uint32_t gp = tg + tp, gq = tg + tq;
+                        const uint32_t pp = (gp >> 1) & 1u;
+                        const bool qk_next = tq < nt && tq <= tp + 1 && (tp >= tq || (idle & 1));
+                        if (qk_next)
+                            mbar_try_wait_for(smem_u32(&k_full[gq & 1]), (gq >> 1) & 1u, kIssueNapNs);
+                        else if (tp < tq && !mbar_test(smem_u32(&p_full[gp & 1]), pp))
+                            mbar_try_wait_for(smem_u32(&p_full[gp & 1]), pp, kIssueNapNs);
+                        else if (tp < tq)
+                            mbar_try_wait_for(smem_u32(&v_full[gp & 1]), pp, kIssueNapNs);
+                    }
+                    if (++idle >= 4) {
                         idle = 0;
                         const uint64_t now = global_ns();
                         if (t_idle == 0) {
@@ -513,15 +581,22 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
         __syncwarp();
     } else {
         // =============================== softmax warps ===============================
-        // warp w owns TMEM lanes 32 (w % 4) .. + 31 (query rows) and key half w / 4 of every tile
-        // (32 logits a row); the two warps of a quadrant exchange row maxima every tile and row
-        // sums at the item's end through shared memory and the quadrant's xchg barrier
+        // warp w serves TMEM lanes 32 (w % 4) .. + 31 and key half w / 4 of every tile (32
+        // logits a lane); the two warps of a quadrant exchange row maxima every tile and row sums
+        // at the item's end through shared memory and the quadrant's xchg barrier.
+        // Row copies: an item of at most 64 (32, 16) rows holds each query row in F = 2 (4, 8)
+        // lanes of a quadrant (lane l: row q R + l % R, copy c = l / R, R = 32 / F; the Q
+        // converters place them so).  Copy c takes keys c n .. c n + n - 1 (n = 32 / F) of the
+        // warp's half and leaves P zero in the others, so that each copy's O row sums its own keys;
+        // the epilogue adds the copies (lanes l ^ R, l ^ 2R, ...).  The tensor pipe computes 128
+        // rows whatever the item's count: copies turn rows that would idle into a split of the
+        // exponentials across all four sub-partitions.
         const int q4 = warp & 3, half = warp >> 2;
-        const int r = q4 * 32 + lane;  // TMEM lane == query row
+        const int L = q4 * 32 + lane;  // TMEM lane
         const uint32_t lane_addr = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t xb = smem_u32(&xchg[q4]);
-        constexpr int HC = kBN / 2;  // logits of a row this thread owns
-        constexpr int HO = D / 2;    // O columns this thread owns
+        constexpr int HC = kBN / 2;  // logits of a lane's row in this warp's half of a tile
+        constexpr int HO = D / 2;    // O columns this warp owns
         const int G = a.G, Hq = a.Hq;
         // K tiles hold the exact values, V tiles the values divided by 2^8 (see convert_rows).
         // Soft cap: cap log2(e) tanh(s sm_scale k_scale / cap) with the hardware tanh (relative
@@ -544,101 +619,116 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 ms = 0;
                 mph ^= 1u;
             }
+            const int rows_used = ntok * G;
+            const int R = 32 / row_copies(rows_used);
+            const int c = lane / R;           // copy
+            const int r = q4 * R + lane % R;  // query row
             const int pos = kl - ql + tok0 + r / G;
             const int pos_lo = kl - ql + tok0, pos_hi = kl - ql + tok0 + ntok - 1;
-            // a quadrant whose 32 rows are all past the item's rows computes nothing: its P and
-            // O rows are never stored (it still takes part in the barriers, in order)
-            const bool idle = q4 * 32 >= ntok * G;
+            // a quadrant whose rows are all past the item's rows computes nothing: its P and O
+            // rows are never stored (it still takes part in the barriers, in order)
+            const bool idle = q4 * R >= rows_used;
             float m_run = -INFINITY, l_run = 0.f;
-            bool ok = true;
-            for (int t = 0; t < nt; ++t, ++tg) {
-                const int b2 = tg & 1;
-                if (!mbar_wait(smem_u32(&s_full[b2]), (tg >> 1) & 1u, ctrl, tmo)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (idle) {
+            // the item's tiles with F copies of each row (n = 32 / F logits a lane)
+            auto run_tiles = [&](auto fc) -> bool {
+                constexpr int F = decltype(fc)::value, NK = HC / F;
+                for (int t = 0; t < nt; ++t, ++tg) {
+                    const int b2 = tg & 1;
+                    if (!mbar_wait(smem_u32(&s_full[b2]), (tg >> 1) & 1u, ctrl, tmo)) return false;
+                    tc_fence_after();
+                    if (idle) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
+                        continue;
+                    }
+                    const int k_lo = key0 + t * kBN;
+                    const bool partial = k_lo < kv_begin || k_lo + kBN > kv_end;
+                    const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
+                                           (a.has_window && k_lo <= pos_hi - a.window);
+                    const uint32_t scol = (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * HC;
+                    // this half's 32 logits of the lane's row, then the copy's NK of them
+                    uint32_t sv[HC];
+                    tmem_ld32(lane_addr + scol, sv);
+                    tmem_ld_wait();
+                    uint32_t kv[NK];
+                    pick_keys<F>(sv, c, kv);
+                    float mh;
+                    if (need_mask) {
+                        // keys allowed for this row: [lo, hi] relative to the copy's first key
+                        int lo = kv_begin, hi = kv_end - 1;
+                        if (a.has_window) lo = max(lo, pos - a.window + 1);
+                        if (a.causal) hi = min(hi, pos);
+                        const int k_first = k_lo + half * HC + c * NK;
+                        lo -= k_first;
+                        hi -= k_first;
+                        mh = a.has_cap ? tile_logits<true, true, NK>(kv, qk, capl, cape, lo, hi)
+                                       : tile_logits<false, true, NK>(kv, qk, capl, cape, lo, hi);
+                    } else {
+                        mh = a.has_cap ? tile_logits<true, false, NK>(kv, qk, capl, cape, 0, 0)
+                                       : tile_logits<false, false, NK>(kv, qk, capl, cape, 0, 0);
+                    }
+                    // row max over the copies, then over both halves
+#pragma unroll
+                    for (int x = 32 / F; x < 32; x <<= 1) mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, x));
+                    xm[tg & 1][half][L] = mh;
+                    mbar_arrive(xb);
+                    if (!mbar_wait(xb, xph, ctrl, tmo)) return false;
+                    xph ^= 1u;
+                    const float mt = fmaxf(mh, xm[tg & 1][half ^ 1][L]);
+                    const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
+                    const float m_new = need ? fmaxf(m_run, mt) : m_run;
+                    const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
+                    const float base = m_new == -INFINITY ? 0.f : m_new;
+                    // P = 2^(x - base) in f16; x - base and the running sums on pairs (f32x2)
+                    const uint64_t nbase2 = f32x2(-base, -base);
+                    uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+                    uint32_t own[NK / 2];
+#pragma unroll
+                    for (int i = 0; i < NK / 2; ++i) {
+                        float x0, x1;
+                        f32x2_split(fadd2(f32x2(__uint_as_float(kv[2 * i]), __uint_as_float(kv[2 * i + 1])), nbase2),
+                                    x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
+                        own[i] = pack2<true>(p0, p1);
+                    }
+                    // the half's 16 P columns (P[i] at column i / 2): the copy's own, zero elsewhere
+                    uint32_t pk[HC / 2];
+#pragma unroll
+                    for (int k = 0; k < HC / 2; ++k) pk[k] = (F == 1 || k / (NK / 2) == c) ? own[k % (NK / 2)] : 0u;
+                    tmem_st16(lane_addr + (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * (HC / 2), pk);
+                    float la, lb, lc, ld;
+                    f32x2_split(ls2[0], la, lb);
+                    f32x2_split(ls2[1], lc, ld);
+                    l_run = l_run * alpha + ((la + lb) + (lc + ld));
+                    m_run = m_new;
+                    if (need && t > 0) {
+                        // this warp's half of the O row holds the item's PVs up to tile t-1
+                        if (!mbar_wait(smem_u32(&pv_done), (tg - 1) & 1u, ctrl, tmo)) return false;
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < HO / 32; ++cc) {
+                            uint32_t ov[32];
+                            tmem_ld32(lane_addr + Gm::TM_O + half * HO + cc * 32, ov);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                            tmem_st32(lane_addr + Gm::TM_O + half * HO + cc * 32, ov);
+                        }
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
-                    continue;
                 }
-                const int k_lo = key0 + t * kBN;
-                const bool partial = k_lo < kv_begin || k_lo + kBN > kv_end;
-                const bool need_mask = partial || (a.causal && k_lo + kBN - 1 > pos_lo) ||
-                                       (a.has_window && k_lo <= pos_hi - a.window);
-                const uint32_t scol = (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * HC;
-                // this half's 32 logits of the row; transform, mask and max in registers
-                uint32_t sv[HC];
-                tmem_ld32(lane_addr + scol, sv);
-                tmem_ld_wait();
-                float mh;
-                if (need_mask) {
-                    // keys allowed for this row: [lo, hi] relative to the half's first key
-                    int lo = kv_begin, hi = kv_end - 1;
-                    if (a.has_window) lo = max(lo, pos - a.window + 1);
-                    if (a.causal) hi = min(hi, pos);
-                    lo -= k_lo + half * HC;
-                    hi -= k_lo + half * HC;
-                    mh = a.has_cap ? tile_logits<true, true, HC>(sv, qk, capl, cape, lo, hi)
-                                   : tile_logits<false, true, HC>(sv, qk, capl, cape, lo, hi);
-                } else {
-                    mh = a.has_cap ? tile_logits<true, false, HC>(sv, qk, capl, cape, 0, 0)
-                                   : tile_logits<false, false, HC>(sv, qk, capl, cape, 0, 0);
-                }
-                // row max over both halves
-                xm[tg & 1][half][r] = mh;
-                mbar_arrive(xb);
-                if (!mbar_wait(xb, xph, ctrl, tmo)) {
-                    ok = false;
-                    break;
-                }
-                xph ^= 1u;
-                const float mt = fmaxf(mh, xm[tg & 1][half ^ 1][r]);
-                const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
-                const float m_new = need ? fmaxf(m_run, mt) : m_run;
-                const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
-                const float base = m_new == -INFINITY ? 0.f : m_new;
-                // P = 2^(x - base) in f16 over this half's first 16 S columns (P[i] at column i/2)
-                // x - base and the running sums on pairs of lanes (f32x2)
-                const uint64_t nbase2 = f32x2(-base, -base);
-                uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
-                uint32_t pk[HC / 2];
-#pragma unroll
-                for (int i = 0; i < HC / 2; ++i) {
-                    float x0, x1;
-                    f32x2_split(fadd2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), nbase2), x0, x1);
-                    const float p0 = ex2(x0), p1 = ex2(x1);
-                    ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
-                    pk[i] = pack2<true>(p0, p1);
-                }
-                tmem_st16(lane_addr + (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * (HC / 2), pk);
-                float la, lb, lc, ld;
-                f32x2_split(ls2[0], la, lb);
-                f32x2_split(ls2[1], lc, ld);
-                l_run = l_run * alpha + ((la + lb) + (lc + ld));
-                m_run = m_new;
-                if (need && t > 0) {
-                    // this warp's half of the O row holds the item's PVs up to tile t-1
-                    if (!mbar_wait(smem_u32(&pv_done), (tg - 1) & 1u, ctrl, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c = 0; c < HO / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
-                    }
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
+                return true;
+            };
+            bool ok;
+            switch (R) {
+                case 32: ok = run_tiles(std::integral_constant<int, 1>{}); break;
+                case 16: ok = run_tiles(std::integral_constant<int, 2>{}); break;
+                case 8: ok = run_tiles(std::integral_constant<int, 4>{}); break;
+                default: ok = run_tiles(std::integral_constant<int, 8>{}); break;
             }
             if (!ok) break;
             if (idle) {
@@ -648,37 +738,40 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 ++items;
                 continue;
             }
-            // ---- epilogue: o = O * v_scale / l, this warp's half of the row
-            xl[half][r] = l_run;
+            // ---- epilogue: o = O * v_scale / l, this warp's half of the row, the copies added
+            for (int x = R; x < 32; x <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
+            xl[half][L] = l_run;
             mbar_arrive(xb);
             if (!mbar_wait(xb, xph, ctrl, tmo)) break;
             xph ^= 1u;
-            const float l_row = l_run + xl[half ^ 1][r];
+            const float l_row = l_run + xl[half ^ 1][L];
             if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
             tc_fence_after();
-            const int rows_used = ntok * G;
+            // tensor-memory loads and shuffles are warp-collective: every lane takes part, the
+            // first copy of each live row stores
+            const bool store = c == 0 && r < rows_used;
             if (part >= 0) {
                 // a split-KV piece of a decode-class sequence (rows_used <= 16): the unnormalised
                 // O (V tiles hold values / 2^8), the running max (log2 domain) and the row sum go
                 // to partial slot `part`, merged by the combine kernel
-                // (tensor-memory loads are warp-collective: every lane loads, live rows store)
                 float* prow = a.part_o + ((size_t)part * kDecRows + r) * D + half * HO;
 #pragma unroll 1
-                for (int c = 0; c < HO / 32; ++c) {
+                for (int cc = 0; cc < HO / 32; ++cc) {
                     uint32_t ov[32];
-                    tmem_ld32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
+                    tmem_ld32(lane_addr + Gm::TM_O + half * HO + cc * 32, ov);
                     tmem_ld_wait();
-                    if (r < rows_used) {
+                    add_copies(ov, R);
+                    if (store) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            *reinterpret_cast<float4*>(prow + c * 32 + 4 * i) =
+                            *reinterpret_cast<float4*>(prow + cc * 32 + 4 * i) =
                                 make_float4(__uint_as_float(ov[4 * i]) * kKvUnscale,
                                             __uint_as_float(ov[4 * i + 1]) * kKvUnscale,
                                             __uint_as_float(ov[4 * i + 2]) * kKvUnscale,
                                             __uint_as_float(ov[4 * i + 3]) * kKvUnscale);
                     }
                 }
-                if (half == 0 && r < rows_used)
+                if (half == 0 && store)
                     *reinterpret_cast<float2*>(a.part_ml + ((size_t)part * kDecRows + r) * 2) =
                         make_float2(m_run, l_row);
                 tc_fence_before();
@@ -692,11 +785,12 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             const int qh = head * G + r % G;
             uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2) + half * HO * 2;
 #pragma unroll 1
-            for (int c = 0; c < HO / 32; ++c) {
+            for (int cc = 0; cc < HO / 32; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(lane_addr + Gm::TM_O + half * HO + c * 32, ov);
+                tmem_ld32(lane_addr + Gm::TM_O + half * HO + cc * 32, ov);
                 tmem_ld_wait();
-                if (r < rows_used) {
+                add_copies(ov, R);
+                if (store) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         uint4 w;
@@ -704,7 +798,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         w.y = pack2<false>(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
                         w.z = pack2<false>(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
                         w.w = pack2<false>(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
-                        put_u4(orow + c * 64 + i * 16, w);
+                        put_u4(orow + cc * 64 + i * 16, w);
                     }
                 }
             }

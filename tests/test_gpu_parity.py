@@ -70,6 +70,13 @@ SMALL = [
     (45, dict(num_seqs=9, max_q=3, max_kv=4000, num_q_heads=9, num_kv_heads=3, head_dim=128,
               soft_cap=20.0, is_causal=False)),
     (46, dict(num_seqs=8, decode_only=True, max_kv=4000, num_q_heads=32, num_kv_heads=2, head_dim=128)),
+    # fp8 tensor-memory prefill with 8 / 4 / 2 / 1 copies of each query row (items of <= 16, 32,
+    # 64 and 128 rows): G = 2 at D 256 with soft cap and window, G = 4 at D 128
+    (47, dict(num_seqs=14, max_q=64, max_kv=1500, num_q_heads=16, num_kv_heads=8, head_dim=256,
+              page_size=16, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0,
+              sliding_window=400, sm_scale=1 / 16)),
+    (48, dict(num_seqs=10, max_q=40, max_kv=1200, num_q_heads=16, num_kv_heads=4, head_dim=128,
+              page_size=32, kv_dtype="fp8_e4m3", k_scale=0.08, v_scale=0.1)),
 ]
 
 

@@ -346,10 +346,18 @@ def main():
             bound, achieved, peak, unit, key = "tensor", w["flops"] / (ms * 1e-3) / 1e12, tf_burst, "TFLOP/s", "bf16_tflops"
         else:
             bound, achieved, peak, unit, key = "hbm", w["bytes"] / (ms * 1e-3) / 1e9, hbm, "GB/s", "hbm_gbs"
-        return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": recorded_traffic(name, args.workload), "kernel": name,
-                "peak_source": f"{src} ({key})", "kernel_ms": float(ms),
-                "algorithmic": {"bytes": w["bytes"], "flops": w["flops"]}}
+        r = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+             "traffic": recorded_traffic(name, args.workload), "kernel": name,
+             "peak_source": f"{src} ({key})", "kernel_ms": float(ms),
+             "algorithmic": {"bytes": w["bytes"], "flops": w["flops"]}}
+        if int(info[15]) & 1:
+            # decode and prefill ran at once on disjoint SMs: the kernel's share of the chip's peak
+            per_sm = int(info[13] if name == "decode_attention" else info[14])
+            ctas = int(info[10] if name == "decode_attention" else info[11])
+            sms = min(int(info[12]), -(-ctas // max(per_sm, 1)))
+            r["sms"] = sms
+            r["frac_of_sm_share"] = achieved / (peak * sms / max(int(info[12]), 1)) if sms else None
+        return r
 
     attn = [i for i, n in enumerate(KERNEL_NAMES) if n.endswith("_attention")]
     dom = max(attn, key=lambda i: mean_k[i])

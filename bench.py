@@ -350,8 +350,9 @@ def main():
              "traffic": recorded_traffic(name, args.workload), "kernel": name,
              "peak_source": f"{src} ({key})", "kernel_ms": float(ms),
              "algorithmic": {"bytes": w["bytes"], "flops": w["flops"]}}
-        if int(info[15]) & 1:
-            # decode and prefill ran at once on disjoint SMs: the kernel's share of the chip's peak
+        if int(info[15]) & 1 and bound == "tensor":
+            # decode and prefill ran at once on disjoint SMs: the kernel's share of the chip's tensor peak
+            # (HBM bandwidth is shared, not split by SMs)
             per_sm = int(info[13] if name == "decode_attention" else info[14])
             ctas = int(info[10] if name == "decode_attention" else info[11])
             sms = min(int(info[12]), -(-ctas // max(per_sm, 1)))

@@ -192,6 +192,24 @@ def test_uncovered_tokens_and_padding_rows():
     assert_close(got, oracle.forward(p), p.kv_dtype, "padding")
 
 
+@pytest.mark.parametrize("kv_dtype,head_dim,q_lens", [
+    ("bf16", 128, [1, 37, 5, 300]),
+    ("fp8_e4m3", 256, [1, 37, 5, 130]),
+])
+def test_full_page_tables(kv_dtype, head_dim, q_lens):
+    """Sequences whose kv_len is the largest the page table holds (pages_per_seq * page_size):
+    every page slot of their row is used, the last key sits in the last slot of the last page."""
+    ps = 16
+    kv = [1024, 1024, 700, 1024]  # pages_per_seq = 64 from the longest
+    p = ri.build(seed=45, q_lens=q_lens, kv_lens=kv, num_q_heads=16, num_kv_heads=4, head_dim=head_dim,
+                 page_size=ps, kv_dtype=kv_dtype, k_scale=0.05 if kv_dtype != "bf16" else None,
+                 v_scale=0.05 if kv_dtype != "bf16" else None, soft_cap=30.0, sliding_window=600)
+    assert p.pages_per_seq * p.page_size == 1024
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, "full page tables")
+
+
 def test_zero_sequences_writes_zeros():
     p = ri.build(seed=44, q_lens=[4], kv_lens=[10], num_q_heads=4, num_kv_heads=2, head_dim=64,
                  page_size=16)

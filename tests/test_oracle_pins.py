@@ -11,7 +11,7 @@ mis-decoded fp8 code) fails at least one of them:
 * the softcap identity c*tanh(x/c) = 2c*sigmoid(2x/c) - c of the
   "from_qwen_ops.rs" page (``capped``) used as an independent formula;
 * invariants: page placement, decode = last prefill row, poisoned tails,
-  sequence order, GQA = MHA with repeated K/V.
+  sequence order, GQA = MHA with repeated K/V, fp8 scales = pre-scaled bf16 K/V.
 """
 
 import math
@@ -329,3 +329,28 @@ def test_validation_codes():
     assert oracle.validate(bad) == 5
     with pytest.raises(oracle.OracleError):
         oracle.forward(bad)
+
+
+def test_scale_folding_equals_prescaled_bf16():
+    """fp8 K/V with k_scale / v_scale equals bf16 K/V holding the decoded values times the scales
+    (up to bf16 rounding of those products): the scales multiply K and V, not Q, O or the logits
+    in some other place."""
+    ks, vs = 0.05, 0.07
+    p8 = ri.random_small(26, num_seqs=3, max_q=6, max_kv=40, num_q_heads=4, num_kv_heads=2, head_dim=32,
+                         page_size=8, kv_dtype="fp8_e4m3", k_scale=ks, v_scale=vs, soft_cap=8.0)
+    o8 = oracle.forward(p8)
+    dec = torch.from_numpy(p8.kv_pages).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    scaled = dec.copy()
+    scaled[:, :, 0::2] *= ks
+    scaled[:, :, 1::2] *= vs
+    pb = ri.random_small(26, num_seqs=3, max_q=6, max_kv=40, num_q_heads=4, num_kv_heads=2, head_dim=32,
+                         page_size=8, soft_cap=8.0)
+    assert np.array_equal(pb.kv_lens, p8.kv_lens) and np.array_equal(pb.cu_q_lens, p8.cu_q_lens)
+    pb.q = p8.q
+    pb.page_indices = p8.page_indices
+    pb.kv_pages = ri.f32_to_bf16_bits(scaled.astype(np.float32))
+    ob = oracle.forward(pb)
+    assert np.abs(o8 - ob).max() <= 1e-2 * max(1.0, np.abs(o8).max())
+    # and dropping either scale is visible
+    p8.k_scale = None
+    assert np.abs(oracle.forward(p8) - o8).max() > 1e-2

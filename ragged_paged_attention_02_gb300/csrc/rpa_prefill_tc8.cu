@@ -215,8 +215,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     __shared__ __align__(8) uint64_t meta_full[2], meta_free[2];
     __shared__ __align__(8) uint64_t q_full, q_empty, q_ready, qt_free;
     __shared__ __align__(8) uint64_t raw_full[2], raw_empty[2];
-    __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2];
-    __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done, o_full, o_free;
+    // per S / f16 buffer b: K converted; QK done (S ready, K buffer free); P and V ready (softmax
+    // and converter warps); PV done (V buffer free, O holds the PV)
+    __shared__ __align__(8) uint64_t k_full[2], qk_done[2], pv_ready[2], pv_done[2];
+    __shared__ __align__(8) uint64_t o_full, o_free;
     __shared__ __align__(8) uint64_t xchg[4];  // per lane quadrant: the two softmax warps' row maxima / sums
     __shared__ float xm[2][2][kM];             // [tile parity][key half][row] partial row maxima
     __shared__ float xl[2][kM];                // [key half][row] partial row sums
@@ -241,18 +243,15 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             mbar_init(smem_u32(&raw_full[i]), 1);
             mbar_init(smem_u32(&raw_empty[i]), kNConv);
             mbar_init(smem_u32(&k_full[i]), kNConv);
-            mbar_init(smem_u32(&k_empty[i]), 1);
-            mbar_init(smem_u32(&v_full[i]), kNConv);
-            mbar_init(smem_u32(&v_empty[i]), 1);
-            mbar_init(smem_u32(&s_full[i]), 1);
-            mbar_init(smem_u32(&p_full[i]), 8);
+            mbar_init(smem_u32(&qk_done[i]), 1);
+            mbar_init(smem_u32(&pv_ready[i]), 8 + kNConv);
+            mbar_init(smem_u32(&pv_done[i]), 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 64);
         mbar_init(smem_u32(&q_full), 1);
         mbar_init(smem_u32(&q_empty), 4);
         mbar_init(smem_u32(&q_ready), 4);
         mbar_init(smem_u32(&qt_free), 1);
-        mbar_init(smem_u32(&pv_done), 1);
         mbar_init(smem_u32(&o_full), 1);
         mbar_init(smem_u32(&o_free), 8);
         fence_mbar_init();
@@ -447,7 +446,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 const int k_lo = key0 + t * kBN;
                 // K exactly (hardware conversion), then V as value / 2^8 (integer placement): the
                 // two halves load the special-function and the integer pipes about evenly
-                if (!mbar_wait(smem_u32(&k_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                if (!mbar_wait(smem_u32(&qk_done[b2]), par ^ 1u, ctrl, tmo)) {
                     ok = false;
                     break;
                 }
@@ -455,14 +454,14 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&k_full[b2]));
-                if (!mbar_wait(smem_u32(&v_empty[b2]), par ^ 1u, ctrl, tmo)) {
+                if (!mbar_wait(smem_u32(&pv_done[b2]), par ^ 1u, ctrl, tmo)) {
                     ok = false;
                     break;
                 }
                 store_rows<D, false>(vr, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&v_full[b2]));
+                if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
             }
             if (!ok) break;
             ++items;
@@ -510,8 +509,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                             for (int kk = 1; kk < D / 16; ++kk)
                                 umma_ts_c<1>(sd, qa + kk * 8, kd_lo + ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) / 16, kd_hi,
                                              idesc_qk);
-                            umma_commit(smem_u32(&s_full[b2]));
-                            umma_commit(smem_u32(&k_empty[b2]));
+                            umma_commit(smem_u32(&qk_done[b2]));
                             if (tq == nt - 1) umma_commit(smem_u32(&qt_free));
                             ++tq;
                             did = true;
@@ -522,7 +520,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const int b2 = g & 1;
                         const uint32_t par = (g >> 1) & 1u;
                         const bool first = tp == 0;
-                        if (mbar_test(smem_u32(&p_full[b2]), par) && mbar_test(smem_u32(&v_full[b2]), par) &&
+                        if (mbar_test(smem_u32(&pv_ready[b2]), par) &&
                             (!first || items == 0 || mbar_test(smem_u32(&o_free), (items - 1) & 1u))) {
                             tc_fence_after();
                             const uint64_t vd = umma_sdesc(v16_base + b2 * Gm::T16, kBN * 128, 1024);
@@ -535,8 +533,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
 #pragma unroll
                             for (int kk = 1; kk < kBN / 16; ++kk)
                                 umma_ts_c<1>(od, pa + kk * 8, vd_lo + kk * 16 * 128 / 16, vd_hi, idesc_pv);
-                            umma_commit(smem_u32(&v_empty[b2]));
-                            umma_commit(smem_u32(&pv_done));
+                            umma_commit(smem_u32(&pv_done[b2]));
                             ++tp;
                             did = true;
                         }
@@ -555,10 +552,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const bool qk_next = tq < nt && tq <= tp + 1 && (tp >= tq || (idle & 1));
                         if (qk_next)
                             mbar_try_wait_for(smem_u32(&k_full[gq & 1]), (gq >> 1) & 1u, kIssueNapNs);
-                        else if (tp < tq && !mbar_test(smem_u32(&p_full[gp & 1]), pp))
-                            mbar_try_wait_for(smem_u32(&p_full[gp & 1]), pp, kIssueNapNs);
                         else if (tp < tq)
-                            mbar_try_wait_for(smem_u32(&v_full[gp & 1]), pp, kIssueNapNs);
+                            mbar_try_wait_for(smem_u32(&pv_ready[gp & 1]), pp, kIssueNapNs);
                     }
                     if (++idle >= 4) {
                         idle = 0;
@@ -634,11 +629,11 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 constexpr int F = decltype(fc)::value, NK = HC / F;
                 for (int t = 0; t < nt; ++t, ++tg) {
                     const int b2 = tg & 1;
-                    if (!mbar_wait(smem_u32(&s_full[b2]), (tg >> 1) & 1u, ctrl, tmo)) return false;
+                    if (!mbar_wait(smem_u32(&qk_done[b2]), (tg >> 1) & 1u, ctrl, tmo)) return false;
                     tc_fence_after();
                     if (idle) {
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
+                        if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
                         continue;
                     }
                     const int k_lo = key0 + t * kBN;
@@ -704,7 +699,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     m_run = m_new;
                     if (need && t > 0) {
                         // this warp's half of the O row holds the item's PVs up to tile t-1
-                        if (!mbar_wait(smem_u32(&pv_done), (tg - 1) & 1u, ctrl, tmo)) return false;
+                        if (!mbar_wait(smem_u32(&pv_done[(tg - 1) & 1]), ((tg - 1) >> 1) & 1u, ctrl, tmo)) return false;
                         tc_fence_after();
 #pragma unroll 1
                         for (int cc = 0; cc < HO / 32; ++cc) {
@@ -719,7 +714,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&p_full[b2]));
+                    if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
                 }
                 return true;
             };

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t q_full, q_empty, meta_free;
     __shared__ __align__(8) uint64_t kv_full[kNS], kv_empty[kNS];
-    __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done[2];
+    __shared__ __align__(8) uint64_t s_full[2], p_full[2];
     __shared__ __align__(8) uint64_t o_full, o_free;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int meta[16];
@@ -108,7 +108,6 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&s_full[i]), 1);
             mbar_init(smem_u32(&p_full[i]), 4);
-            mbar_init(smem_u32(&pv_done[i]), 1);
         }
         for (int i = 0; i < kNS; ++i) {
             mbar_init(smem_u32(&kv_full[i]), 1);
@@ -258,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
             constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
             int s = 0;
             uint32_t qph = 0, ph = 0;
-            uint32_t j_all = 0;   // key tiles issued so far (all items): phase of s_full / p_full / pv_done
+            uint32_t j_all = 0;   // key tiles issued so far (all items): phase of s_full / p_full
             uint32_t items = 0;   // items finished
             bool ok = true;
             // descriptors are formed once per call and offset per MMA in their low (address) half:
@@ -290,7 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
 #pragma unroll
                 for (int kk = 1; kk < kBN / 16; ++kk)
                     umma_ts_c<1>(od, pa + kk * 8, vd_lo + kk * 16 * 128 / 16, vd_hi, idesc_pv);
-                umma_commit(smem_u32(&pv_done[x]));
                 return true;
             };
             for (;;) {
@@ -489,12 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 l_run = l_run * alpha + lsum;
                 m_run = m_new;
                 if (need && t > 0) {
-                    // O holds this item's PVs up to tile t-1: wait for them, then scale in place
-                    if (!mbar_wait(smem_u32(&pv_done[x]), (jj - 1) & 1u, ctrl, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    // O holds this item's PVs up to tile t-1, all complete: the MMA thread issues
+                    // S_x(t) after PV_x(t-1), and a commit (here s_full, waited for above) arrives
+                    // once every MMA issued before it is done.  Scale in place.
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t ov[32];

@@ -74,26 +74,6 @@ struct G8 {
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// e4m3 byte b = s eeee mmm  ->  the f16 with bits s 0eeee mmm0000000, whose value is exactly
-// e4m3(b) / 2^8 for every finite b, normal or subnormal (both formats put the exponent bias
-// so that moving the field moves the value by 2^(15 - 7)); the factor is taken back in the
-// logit scale and the output scale.  Integer ops only: the special-function pipe stays free
-// for the softmax.  An e4m3 NaN (s 1111 111) maps to 480 / 2^8 instead of NaN.
-constexpr float kKvUnscale = 256.f;
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, uint32_t sel) {
-    const uint32_t u = __byte_perm(w, 0u, sel);  // the two bytes in the low byte of each half
-    const uint32_t t = u << 7;                   // eeee mmm at bits 7..13, s at bit 14
-    return t + (t & 0x40004000u);                // s carried from bit 14 up to bit 15
-}
-__device__ __forceinline__ uint4 e4m3x8_to_f16x8(uint2 b) {
-    uint4 o;
-    o.x = e4m3x2_to_f16x2_scaled(b.x, 0x4140u);
-    o.y = e4m3x2_to_f16x2_scaled(b.x, 0x4342u);
-    o.z = e4m3x2_to_f16x2_scaled(b.y, 0x4140u);
-    o.w = e4m3x2_to_f16x2_scaled(b.y, 0x4342u);
-    return o;
-}
-
 // e4m3 x 8 -> f16 x 8 with the hardware conversion (exact values)
 __device__ __forceinline__ uint4 e4m3x8_to_f16x8_hw(uint32_t w0, uint32_t w1) {
     return make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
@@ -118,10 +98,9 @@ __device__ __forceinline__ void load_rows(const uint8_t* raw, int cw, int lane, 
         v[i] = *reinterpret_cast<const uint4*>(raw + (key >> brs) * (2 * BR * D) + (key & (BR - 1)) * D + e * 16);
     }
 }
-// ... and those rows, converted, into a 128-byte swizzled f16 tile [D / 64][64 rows][128 B]; keys
-// outside [kv_begin, kv_end) become zero.  HW: exact hardware conversion, else the integer
-// placement (value / 2^8).
-template <int D, bool HW>
+// ... and those rows, converted exactly to f16, into a 128-byte swizzled tile [D / 64][64 rows]
+// [128 B]; keys outside [kv_begin, kv_end) become zero.
+template <int D>
 __device__ __forceinline__ void store_rows(const uint4* v, uint8_t* dst, int cw, int lane, int k_lo, int kv_begin,
                                            int kv_end) {
     using C = ConvLanes<D>;
@@ -138,13 +117,8 @@ __device__ __forceinline__ void store_rows(const uint4* v, uint8_t* dst, int cw,
         const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
         if (j >= kv_begin && j < kv_end) {
-            if constexpr (HW) {
-                o0 = e4m3x8_to_f16x8_hw(a0, a1);
-                o1 = e4m3x8_to_f16x8_hw(b0, b1);
-            } else {
-                o0 = e4m3x8_to_f16x8(make_uint2(a0, a1));
-                o1 = e4m3x8_to_f16x8(make_uint2(b0, b1));
-            }
+            o0 = e4m3x8_to_f16x8_hw(a0, a1);
+            o1 = e4m3x8_to_f16x8_hw(b0, b1);
         }
         const int line = cb * kBN + key;
         uint8_t* row = dst + line * 128;
@@ -444,13 +418,12 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     ph ^= 1u;
                 }
                 const int k_lo = key0 + t * kBN;
-                // K exactly (hardware conversion), then V as value / 2^8 (integer placement): the
-                // two halves load the special-function and the integer pipes about evenly
+                // K, then V, both converted exactly by the hardware conversion
                 if (!mbar_wait(smem_u32(&qk_done[b2]), par ^ 1u, ctrl, tmo)) {
                     ok = false;
                     break;
                 }
-                store_rows<D, true>(kr, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
+                store_rows<D>(kr, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&k_full[b2]));
@@ -458,7 +431,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     ok = false;
                     break;
                 }
-                store_rows<D, false>(vr, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
+                store_rows<D>(vr, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
@@ -593,7 +566,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
         constexpr int HC = kBN / 2;  // logits of a lane's row in this warp's half of a tile
         constexpr int HO = D / 2;    // O columns this warp owns
         const int G = a.G, Hq = a.Hq;
-        // K tiles hold the exact values, V tiles the values divided by 2^8 (see convert_rows).
+        // K and V tiles hold the exact e4m3 values (the scales act on the logits and the output).
         // Soft cap: cap log2(e) tanh(s sm_scale k_scale / cap) with the hardware tanh (relative
         // error about 2^-11, the order of the f16 rounding of P); its argument factor is
         // cap_exp / (2 log2(e)).
@@ -747,8 +720,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             const bool store = c == 0 && r < rows_used;
             if (part >= 0) {
                 // a split-KV piece of a decode-class sequence (rows_used <= 16): the unnormalised
-                // O (V tiles hold values / 2^8), the running max (log2 domain) and the row sum go
-                // to partial slot `part`, merged by the combine kernel
+                // O, the running max (log2 domain) and the row sum go to partial slot `part`,
+                // merged by the combine kernel
                 float* prow = a.part_o + ((size_t)part * kDecRows + r) * D + half * HO;
 #pragma unroll 1
                 for (int cc = 0; cc < HO / 32; ++cc) {
@@ -760,10 +733,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
                             *reinterpret_cast<float4*>(prow + cc * 32 + 4 * i) =
-                                make_float4(__uint_as_float(ov[4 * i]) * kKvUnscale,
-                                            __uint_as_float(ov[4 * i + 1]) * kKvUnscale,
-                                            __uint_as_float(ov[4 * i + 2]) * kKvUnscale,
-                                            __uint_as_float(ov[4 * i + 3]) * kKvUnscale);
+                                make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]),
+                                            __uint_as_float(ov[4 * i + 2]), __uint_as_float(ov[4 * i + 3]));
                     }
                 }
                 if (half == 0 && store)
@@ -775,7 +746,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 ++items;
                 continue;
             }
-            const float inv = l_row > 0.f ? a.v_scale * kKvUnscale / l_row : 0.f;
+            const float inv = l_row > 0.f ? a.v_scale / l_row : 0.f;
             const int t_tok = q_start + tok0 + r / G;
             const int qh = head * G + r % G;
             uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2) + half * HO * 2;

@@ -163,7 +163,7 @@ int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_call
 
 /* rpa_forward for callers that cannot allocate device memory.
  *
- * The paper has no counterpart to this entry point; it exists for callers
+ * The method has no counterpart to this entry point (it is an API choice); it exists for callers
  * that may not call cudaMalloc/cudaFree where they run attention: serving
  * engines that hand all device memory to their own arena allocator, code
  * paths where an allocation's implicit device synchronisation is not

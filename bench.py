@@ -173,9 +173,18 @@ def cpu_baseline(prob, budget_s=12.0, max_reps=8):
             break
     el = time.perf_counter() - t0
     tokens = done / prob.num_q_heads
+    # the same oracle on one thread, over a smaller sample (a few seconds)
+    n1 = int(min(n, max(prob.num_q_heads, (budget_s / 4) / max(per_row * threads, 1e-9))))
+    n1 -= n1 % prob.num_q_heads or 0
+    n1 = max(n1, prob.num_q_heads)
+    t1 = time.perf_counter()
+    oracle.rows(prob, rows_all[:n1], nthreads=1)
+    el1 = time.perf_counter() - t1
     return {"value": tokens / el, "unit": "tokens/s", "cores": int(threads), "kind": "oracle",
             "sample": f"first {n // prob.num_q_heads} of {T} query tokens (all {prob.num_q_heads} heads)"
-                      f" x {reps} reps, {el:.1f} s"}
+                      f" x {reps} reps, {el:.1f} s",
+            "value_1thread": n1 / prob.num_q_heads / el1,
+            "sample_1thread": f"first {n1 // prob.num_q_heads} query tokens (all heads), {el1:.1f} s"}
 
 
 def run_reference(args, rank):

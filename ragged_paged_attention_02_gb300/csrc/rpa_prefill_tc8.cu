@@ -451,8 +451,11 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             // Per item, QK(t) and PV(t) are issued as soon as their inputs are ready, in either
             // order: QK(t) needs K(t) converted and PV(t-2) issued (it overwrites S(t % 2), which
             // PV(t-2) reads; the tensor pipe runs in issue order); PV(t) needs P(t), V(t) and, for
-            // the item's first PV, the previous epilogue done with O.  Readiness is polled without
-            // blocking; a poll that sees nothing ready for longer than the wait bound gives up.
+            // the item's first PV, the previous epilogue done with O.  Readiness is tested without
+            // blocking; when nothing is ready the thread naps briefly on a pending barrier, and a
+            // thread that sees nothing ready for longer than the wait bound gives up.  Every
+            // barrier test and commit costs this thread tens of cycles in series with the tensor
+            // pipe, so each MMA group uses one readiness barrier and one commit.
             for (;;) {
                 if (!mbar_wait(smem_u32(&meta_full[ms]), mph, ctrl, tmo)) break;
                 const int stop = meta[ms][eStop], nt = meta[ms][eNt];

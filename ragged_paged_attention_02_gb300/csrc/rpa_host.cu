@@ -465,6 +465,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     cp.Hq = (int)c.num_q_heads;
     cp.G = h->G;
     cp.D = h->D;
+    cp.rows_max = h->dec_rows;
     cp.v_scale = h->v_scale;
     cp.ctrl = h->ctrl;
     cp.comb = h->comb;

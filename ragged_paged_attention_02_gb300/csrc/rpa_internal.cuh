@@ -137,6 +137,7 @@ struct CombParams {
     uint8_t* o;
     const int* cu_q_lens;
     int num_seqs, T, Hq, G, D;
+    int rows_max;  // most rows of a combine entry (the decode tile's rows)
     float v_scale;
     const int* ctrl;
     const Comb* comb;

@@ -273,6 +273,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     cp.Hq = (int)c.num_q_heads;
     cp.G = G;
     cp.D = D;
+    cp.rows_max = dec_rows;
     cp.v_scale = ap.v_scale;
     cp.ctrl = ctrl;
     cp.comb = comb;

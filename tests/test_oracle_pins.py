@@ -157,6 +157,29 @@ def test_oracle_equals_dense_brute_force(case):
     close(oracle.forward(prob), brute(prob, dense))
 
 
+@pytest.mark.parametrize("seed", range(24))
+def test_oracle_random_configs_equal_brute_force(seed):
+    """Random small configurations (ragged lengths, GQA factor, page size, causal or not,
+    window, soft cap, bf16 or fp8 with scales) against the dense brute force."""
+    rng = np.random.default_rng([7, seed])
+    S = int(rng.integers(1, 5))
+    q_lens = [int(x) for x in rng.integers(1, 9, size=S)]
+    kv_lens = [int(rng.integers(q, 49)) for q in q_lens]
+    Hkv = int(rng.integers(1, 4))
+    Hq = Hkv * int(rng.choice([1, 2, 4]))
+    D = int(rng.choice([16, 32]))
+    ps = int(rng.choice([4, 8, 16]))
+    kw = dict(is_causal=bool(rng.integers(0, 2)), sm_scale=float(rng.uniform(0.05, 0.5)))
+    if rng.integers(0, 2):
+        kw["sliding_window"] = int(rng.integers(1, 40))
+    if rng.integers(0, 2):
+        kw["soft_cap"] = float(rng.uniform(0.5, 30.0))
+    if rng.integers(0, 2):
+        kw.update(kv_dtype="fp8_e4m3", k_scale=float(rng.uniform(0.01, 0.1)), v_scale=float(rng.uniform(0.01, 0.1)))
+    prob, dense = dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, **kw)
+    close(oracle.forward(prob), brute(prob, dense))
+
+
 def test_softcap_identity_from_capped_form():
     rng = np.random.default_rng(7)
     prob, dense = dense_problem(rng, [4, 9], [12, 30], 4, 2, 32, 8, soft_cap=1.5, sm_scale=1.0)

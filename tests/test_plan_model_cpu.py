@@ -1,6 +1,7 @@
 """Properties of the planner's stated rules (host logic, via the Python model):
 the items of one (sequence, kv head) tile exactly the key band without overlap,
-split pieces respect the chunk, and the capacity bound of the workspace holds."""
+split pieces respect the chunk, and the capacity bound of the workspace holds; for
+16- and 8-row decode tiles, and with decode units run by the prefill kernel."""
 import numpy as np
 import pytest
 
@@ -9,7 +10,8 @@ from plan_model import band, plan
 
 
 @pytest.mark.parametrize("seed", range(6))
-def test_items_cover_the_bands(seed):
+@pytest.mark.parametrize("dec_rows,dec_on_pf", [(16, False), (8, False), (16, True)])
+def test_items_cover_the_bands(seed, dec_rows, dec_on_pf):
     rng = np.random.default_rng(seed)
     S = int(rng.integers(1, 40))
     G = int(rng.choice([1, 2, 4, 8]))
@@ -19,7 +21,7 @@ def test_items_cover_the_bands(seed):
     p = ri.build(seed=seed, q_lens=ql, kv_lens=kl, num_q_heads=2 * G, num_kv_heads=2, head_dim=64,
                  page_size=16, sliding_window=(int(rng.integers(1, 500)) if seed % 2 else None))
     slots = int(rng.integers(1, 300))
-    pl = plan(p, slots)
+    pl = plan(p, slots, dec_rows=dec_rows, dec_on_pf=dec_on_pf, n_sms=152, dec_bps=3, pf_bps=1)
     assert pl["status"] == 0
     items = np.concatenate([pl["dec"], pl["pf"]])
     for s in range(S):
@@ -34,7 +36,7 @@ def test_items_cover_the_bands(seed):
                 lo, hi = band(int(kl[s]), int(ql[s]), int(it[2]), int(it[2] + it[3]), True,
                               p.sliding_window or 0)
                 assert lo <= it[4] < it[5] <= hi
-            dec_like = ql[s] * G <= 16
+            dec_like = ql[s] * G <= dec_rows
             if dec_like:
                 spans = sorted((int(it[4]), int(it[5])) for it in mine)
                 lo, hi = band(int(kl[s]), int(ql[s]), 0, int(ql[s]), True, p.sliding_window or 0)

@@ -57,6 +57,9 @@ BASE = dict(num_q_tokens=22, num_q_heads=4, num_kv_heads=2, head_dim=64, total_n
     (dict(sm_scale=float("nan")), rpa.RPA_ERR_INVALID_ARG),
     (dict(kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05), rpa.RPA_OK),
     (dict(pages_per_seq=1 << 20, page_size=1 << 12), rpa.RPA_ERR_INVALID_ARG),
+    (dict(page_size=6), rpa.RPA_ERR_UNSUPPORTED),  # page runs of the gather are >= 4 slots
+    (dict(page_size=4, pages_per_seq=16), rpa.RPA_OK),
+    (dict(head_dim=256, num_q_heads=16, num_kv_heads=8), rpa.RPA_OK),
 ])
 def test_validate_cfg(L, change, code):
     cfg = dict(BASE)
@@ -76,3 +79,25 @@ def test_null_handle_and_create_out(L):
     assert L.rpa_create(ctypes.byref(bad), ctypes.byref(h)) == rpa.RPA_ERR_UNSUPPORTED
     assert not h.value
     L.rpa_destroy(None)
+
+
+def test_cfg_init_defaults_keep_the_shape(L):
+    """rpa_cfg_init keeps the shape fields and sets the page's defaults for the rest."""
+    import ctypes
+    import math
+
+    from ragged_paged_attention_02_gb300.binding import RPA_DT_BF16, RpaCfg
+
+    c = RpaCfg()
+    c.num_q_tokens, c.num_q_heads, c.num_kv_heads, c.head_dim = 22, 4, 2, 64
+    c.total_num_pages, c.page_size, c.max_num_seqs, c.pages_per_seq = 16, 16, 3, 4
+    c.is_causal, c.soft_cap, c.reserved = 0, 9.0, 5
+    L.rpa_cfg_init(ctypes.byref(c))
+    assert (c.num_q_tokens, c.num_q_heads, c.num_kv_heads, c.head_dim) == (22, 4, 2, 64)
+    assert (c.total_num_pages, c.page_size, c.max_num_seqs, c.pages_per_seq) == (16, 16, 3, 4)
+    assert c.q_dtype == RPA_DT_BF16 and c.kv_dtype == RPA_DT_BF16
+    assert math.isclose(c.sm_scale, 1 / 8, rel_tol=1e-7)
+    assert math.isclose(c.mask_value, -2.38197633e38, rel_tol=1e-7)
+    assert c.is_causal == 1 and c.reserved == 0
+    assert (c.has_soft_cap, c.has_k_scale, c.has_v_scale, c.has_sliding_window) == (0, 0, 0, 0)
+    assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_OK

@@ -232,6 +232,56 @@ def test_window_one_selects_own_position():
                 close(o[t, qh], V[kl - ql + i, 0], 1e-14)
 
 
+@pytest.mark.parametrize("causal,window", [(True, None), (True, 3), (True, 7), (False, None), (False, 4)])
+def test_zero_query_averages_the_allowed_keys(causal, window):
+    """q = 0 makes every logit 0, so o is the plain mean of V over the allowed keys: with the
+    causal mask keys 0..p, with a window of w also j > p - w, without causality all keys (and
+    j > p - w under a window).  Pins both mask edges and the 1 / sum normalisation."""
+    rng = np.random.default_rng(12)
+    prob, dense = dense_problem(rng, [5, 2], [12, 9], 2, 1, 16, 4, is_causal=causal,
+                                sliding_window=window)
+    prob.q = np.zeros_like(prob.q)
+    o = oracle.forward(prob)
+    for s, (Q, K, V) in enumerate(dense):
+        ql, kl = Q.shape[0], K.shape[0]
+        for i in range(ql):
+            p = kl - ql + i
+            lo = 0 if window is None else max(0, p - window + 1)
+            hi = p if causal else kl - 1
+            want = V[lo:hi + 1, 0].mean(axis=0)
+            for qh in range(2):
+                close(o[prob.cu_q_lens[s] + i, qh], want, 1e-13)
+
+
+def test_two_keys_closed_form_weights():
+    """Logits 0 and ln 3 (q = e_0, k_0 = 0, k_1 = 2 e_0, sm_scale = ln 3 / 2) weight V by 1/4 and
+    3/4; with a soft cap c the second logit is c tanh(ln 3 / c)."""
+    D = 16
+    for cap in (None, 0.8):
+        rng = np.random.default_rng(13)
+        prob, dense = dense_problem(rng, [1], [2], 1, 1, D, 4, sm_scale=math.log(3.0) / 2,
+                                    soft_cap=cap)
+        q = np.zeros((1, 1, D), np.float32)
+        q[0, 0, 0] = 1.0
+        prob.q = ri.f32_to_bf16_bits(q)
+        kvb = np.zeros(prob.kv_pages.shape, np.float32)
+        vals = rng.standard_normal((2, D)).astype(np.float32)
+        pg = prob.page_indices[0, 0]
+        kvb[pg, 1, 0, 0] = 2.0           # K of key 1 (key 0 stays 0)
+        kvb[pg, 0, 1, :] = vals[0]       # V of key 0
+        kvb[pg, 1, 1, :] = vals[1]       # V of key 1
+        prob.kv_pages = ri.f32_to_bf16_bits(kvb)
+        v = ri.bf16_bits_to_f32(prob.kv_pages[pg, :2, 1, :]).astype(np.float64)
+        x1 = prob.sm_scale * 2.0  # the oracle computes in fp64 from the configured scale
+        if cap is not None:
+            x1 = cap * math.tanh(x1 / cap)
+        w1 = math.exp(x1) / (1.0 + math.exp(x1))
+        want = (1 - w1) * v[0] + w1 * v[1]
+        close(oracle.forward(prob)[0, 0], want, 1e-13)
+        if cap is None:
+            assert abs(w1 - 0.75) < 1e-6
+
+
 def test_single_key_sequence():
     rng = np.random.default_rng(5)
     prob, dense = dense_problem(rng, [1, 1], [1, 1], 4, 2, 16, 4)

@@ -12,10 +12,14 @@ function of the C file follows the "ragged_paged.zig" page, sections
 walk, GQA head mapping, dequant); see the C file's header for the readings.
 
 Parity pins (tests/test_oracle_pins.py): brute-force dense attention on tiny
-unpaged inputs, closed forms (uniform V, single allowed key, one-key
-sequences), the softcap identity of the "from_qwen_ops.rs" page (``capped``),
-format decoders checked code by code, and the invariants of page placement,
-decode-vs-prefill, tail poisoning, sequence order and GQA repetition.
+unpaged inputs (fixed and random configurations), closed forms (uniform V,
+single allowed key, one-key sequences, zero-query means over the allowed keys,
+two-key weights), the softcap identity of the "from_qwen_ops.rs" page
+(``capped``), format decoders checked code by code, and the invariants of page
+placement, decode-vs-prefill, tail poisoning, sequence order, GQA repetition
+and fp8 scale folding.  tests/test_oracle_mutations.py plants slips in a copy
+of the C source and checks that the pins catch each.  No function is left
+with its parity unpinned.
 """
 
 from __future__ import annotations

@@ -58,3 +58,17 @@ def test_no_gpu_means_an_error_not_a_fallback():
     p = ri.workload("tiny")
     with pytest.raises((RpaError, RuntimeError)):
         RaggedPagedAttention(**p.cfg_dict())
+
+
+def test_kernels_use_no_trap_or_closed_copy_calls():
+    """Failures are reported through the status word, never by trapping the GPU; the batched
+    memcpy calls that faulted GPUs of this class are not used (nor named)."""
+    files = _sources("ragged_paged_attention_02_gb300/**/*.cu", "ragged_paged_attention_02_gb300/**/*.cuh",
+                     "include/*.h", "ragged_paged_attention_02_gb300/**/*.py", "bench.py", "__graft_entry__.py")
+    closed = ["Memcpy" + "BatchAsync", "Memcpy3D" + "BatchAsync"]
+    for f in files:
+        src = open(f).read()
+        assert "__trap" not in src and not re.search(r"\btrap\s*;", src), f
+        assert not re.search(r"(?<![A-Za-z_])assert\s*\(", src) or f.endswith(".py"), f
+        for name in closed:
+            assert name not in src, (f, name)

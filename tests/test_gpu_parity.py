@@ -77,6 +77,11 @@ SMALL = [
               sliding_window=400, sm_scale=1 / 16)),
     (48, dict(num_seqs=10, max_q=40, max_kv=1200, num_q_heads=16, num_kv_heads=4, head_dim=128,
               page_size=32, kv_dtype="fp8_e4m3", k_scale=0.08, v_scale=0.1)),
+    # fp8 K/V at D 64: the mma.sync decode kernel and the warp-MMA prefill
+    (70, dict(num_seqs=8, max_q=40, max_kv=900, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, soft_cap=20.0, sliding_window=300)),
+    (71, dict(num_seqs=10, decode_only=True, max_kv=3000, num_q_heads=8, num_kv_heads=2, head_dim=64,
+              page_size=32, kv_dtype="fp8_e4m3", k_scale=0.08, v_scale=0.05)),
 ]
 
 

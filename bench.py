@@ -270,8 +270,8 @@ def main():
     import __graft_entry__
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
+    torch.cuda.set_device(local_rank)  # before the process group, so NCCL binds this rank's GPU
     dist = init_ranks(world)
-    torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     if rank == 0 or world == 1:
         __graft_entry__.build()

@@ -62,7 +62,7 @@ typedef struct RpaCfg {
     int64_t num_kv_heads;    /* Hkv; Hq % Hkv == 0 and Hq/Hkv <= 64 */
     int64_t head_dim;        /* D in {64, 128, 256} */
     int64_t total_num_pages; /* physical pages in kv_pages */
-    int64_t page_size;       /* keys per page, >= 1 */
+    int64_t page_size;       /* keys per page: a multiple of 4 (others give RPA_ERR_UNSUPPORTED) */
     int64_t max_num_seqs;    /* rows of kv_lens / page_indices; cu_q_lens has max_num_seqs+1 */
     int64_t pages_per_seq;   /* columns of page_indices */
     int64_t sliding_window;  /* used when has_sliding_window; must be >= 1 */

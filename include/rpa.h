@@ -43,7 +43,8 @@ typedef enum RpaDtype { RPA_DT_BF16 = 0, RPA_DT_FP8_E4M3 = 1 } RpaDtype;
 typedef enum RpaStatus {
     RPA_OK = 0,
     RPA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad configuration value */
-    RPA_ERR_UNSUPPORTED = 2,    /* dtype, head_dim not in {64,128,256}, Hq % Hkv != 0, group > 64 */
+    RPA_ERR_UNSUPPORTED = 2,    /* dtype, head_dim not in {64,128,256}, Hq % Hkv != 0, group > 64,
+                                   page_size not a multiple of 4, mask_value above -1e30 */
     RPA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
     RPA_ERR_BAD_PAGE_INDEX = 4, /* device-detected: a used page id outside [0, total_num_pages) */
     RPA_ERR_BAD_LENGTHS = 5,    /* device-detected: kv_len > pages_per_seq*page_size, q_len > kv_len,

@@ -1,0 +1,70 @@
+"""bench.py's host-side helpers on the CPU: the clock record parsed from nvidia-smi samples
+(a stand-in process returns canned lines), the measured-peaks fallback, and the traffic record
+lookup keyed by the kernel sources' hash."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+class _FakeProc:
+    def __init__(self, out):
+        self.out = out
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.out, ""
+
+
+def test_clock_record_median_max_and_reasons(monkeypatch):
+    lines = "\n".join([
+        "2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "2055, 2070, 1200.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "2070, 2070, 1210.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "[N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ])
+    monkeypatch.setattr(bench.subprocess, "Popen", lambda *a, **k: _FakeProc(lines))
+    monkeypatch.setattr(bench.time, "sleep", lambda s: None)
+    c = bench.Clocks("GPU-0")
+    r = c.stop()
+    assert r["sm_mhz"] == 2070.0 and r["sm_max_mhz"] == 2070.0 and r["samples"] == 3
+    assert r["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_record_flags_thermal_slowdown(monkeypatch):
+    lines = "1500, 2070, 1300, 0x20, Not Active, Active, Not Active, Not Active"
+    monkeypatch.setattr(bench.subprocess, "Popen", lambda *a, **k: _FakeProc(lines))
+    monkeypatch.setattr(bench.time, "sleep", lambda s: None)
+    r = bench.Clocks(None).stop()
+    assert r["reasons"] == ["hw_thermal_slowdown"] and r["sm_mhz"] == 1500.0
+
+
+def test_peaks_fallback_and_measured(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == (6800.0, 1900.0, 1700.0, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 6787.2, "bf16_tflops": 1919.3, "bf16_tflops_sustained": 1700.0}))
+    assert bench.peaks() == (6787.2, 1919.3, 1700.0, "measured")
+
+
+def test_recorded_traffic_needs_the_current_sources(tmp_path, monkeypatch):
+    sha = bench.sources_sha(bench.KERNEL_SOURCES["decode_attention"])
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "kernel_traffic.txt").write_text(
+        "# comment\n"
+        f"decode_attention decode {sha} 123456\n"
+        "decode_attention mixed 0000000000000000 999\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # sources_sha reads the kernel files relative to ROOT: keep them readable from the repo
+    monkeypatch.setattr(bench, "sources_sha", lambda names: sha)
+    assert bench.recorded_traffic("decode_attention", "decode") == 123456.0
+    assert bench.recorded_traffic("decode_attention", "fp8_window") is None
+    assert bench.recorded_traffic("combine", "decode") is None

@@ -427,3 +427,17 @@ def test_scale_folding_equals_prescaled_bf16():
     # and dropping either scale is visible
     p8.k_scale = None
     assert np.abs(oracle.forward(p8) - o8).max() > 1e-2
+
+
+def test_rows_equal_forward_bit_for_bit():
+    """oracle.rows (used for the sampled rows of the full-size parity cases and the CPU
+    baseline) computes exactly the rows oracle.forward does, on one thread or several."""
+    prob = ri.random_small(27, num_seqs=4, max_q=12, max_kv=80, num_q_heads=6, num_kv_heads=2,
+                           head_dim=32, page_size=8, soft_cap=10.0, sliding_window=20)
+    full = oracle.forward(prob)
+    T = int(prob.cu_q_lens[prob.num_seqs])
+    rng = np.random.default_rng(5)
+    rows = np.stack([rng.integers(0, T, 40), rng.integers(0, prob.num_q_heads, 40)], axis=1).astype(np.int64)
+    for nthreads in (1, 0):
+        got = oracle.rows(prob, rows, nthreads=nthreads)
+        assert np.array_equal(got, full[rows[:, 0], rows[:, 1]])

@@ -7,6 +7,9 @@ resident in HBM.  The default workload is the Llama-3-8B-like decode batch:
 256 sequences, q_len 1, kv_len ~ U[512, 8192], 32 q heads / 8 kv heads,
 head_dim 128, page_size 16, bf16 (seeded synthetic data).  Its K/V cache
 (about 4.6 GB) is far larger than L2, so no flush is needed between steps.
+The default line also carries, under "workloads", the same measurements of
+the mixed prefill/decode batch, the fp8 K/V windowed batch and the long
+prefill (the metric's prefill TFLOP/s), each timed the same way.
 
   python bench.py [--steps K] [--warmup W] [--gpus N] [--workload NAME] [--impl reference]
 
@@ -68,6 +71,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--all", action="store_true",
                     help="one line per workload (tiny excluded), no CPU baseline or e2e")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="the decode line without the other workloads' measurements")
     return ap.parse_args()
 
 
@@ -259,27 +264,9 @@ def job_throughput(tokens_per_rank, steps, world, ms_total):
     return tokens_per_rank * steps * world / (ms_total / 1e3)
 
 
-def main():
-    args = parse()
-    world, rank, local_rank = rank_layout()
-    if args.impl == "reference":
-        run_reference(args, rank)
-        return
+def upload(prob, dev):
     import torch
 
-    import __graft_entry__
-    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
-
-    torch.cuda.set_device(local_rank)  # before the process group, so NCCL binds this rank's GPU
-    dist = init_ranks(world)
-    dev = torch.device("cuda", local_rank)
-    if rank == 0 or world == 1:
-        __graft_entry__.build()
-    if dist is not None:
-        dist.barrier()
-
-    prob = ri.workload(args.workload)
-    work = ri.algorithmic_work(prob)
     q = torch.from_numpy(prob.q.view(np.int16)).view(torch.bfloat16).to(dev)
     if prob.kv_dtype == "bf16":
         kv = torch.from_numpy(prob.kv_pages.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -288,6 +275,30 @@ def main():
     kvl = torch.from_numpy(prob.kv_lens).to(dev)
     pi = torch.from_numpy(prob.page_indices).to(dev)
     cu = torch.from_numpy(prob.cu_q_lens).to(dev)
+    return q, kv, kvl, pi, cu
+
+
+def gpu_uuid(dev):
+    import torch
+
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        return uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        return None
+
+
+def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
+    """Time `steps` calls of the library on workload `name` (after `warmup` untimed ones) with CUDA
+    events on the launching stream, barrier and synchronise on both sides, max over ranks; per-kernel
+    times from the library's own events; the roofline of each attention kernel and of the step."""
+    import torch
+
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    prob = ri.workload(name)
+    work = ri.algorithmic_work(prob)
+    q, kv, kvl, pi, cu = upload(prob, dev)
     out = torch.empty_like(q)
     att = RaggedPagedAttention(**prob.cfg_dict())
     stream = torch.cuda.current_stream()
@@ -295,20 +306,14 @@ def main():
     def step():
         att.forward(q, kv, kvl, pi, cu, prob.num_seqs, out=out, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         step()
     torch.cuda.synchronize()
     if att.status() != 0:
-        raise SystemExit(f"library status {att.status()} on warm-up")
+        raise SystemExit(f"library status {att.status()} on warm-up ({name})")
 
-    K = max(1, args.steps)
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-    except Exception:
-        uuid = None
-    clocks = Clocks(uuid)
+    K = max(1, steps)
+    clocks = Clocks(gpu_uuid(dev))
     time.sleep(0.3)
     att.profile_begin(K)
     if dist is not None:
@@ -346,9 +351,10 @@ def main():
         d, pf = work["decode"], work["prefill"]
         work["prefill"] = {k: d[k] + pf[k] for k in pf}
         work["decode"] = {k: 0 for k in d}
+    has_work = {"decode_attention": int(info[1]) > 0, "prefill_attention": int(info[2]) > 0}
 
-    def kernel_roof(name, ms):
-        w = work["decode" if name == "decode_attention" else "prefill"]
+    def kernel_roof(kname, ms):
+        w = work["decode" if kname == "decode_attention" else "prefill"]
         t_hbm = w["bytes"] / (hbm * 1e9)
         t_tc = w["flops"] / (tf_burst * 1e12)
         if t_tc > t_hbm:
@@ -356,30 +362,48 @@ def main():
         else:
             bound, achieved, peak, unit, key = "hbm", w["bytes"] / (ms * 1e-3) / 1e9, hbm, "GB/s", "hbm_gbs"
         r = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-             "traffic": recorded_traffic(name, args.workload), "kernel": name,
+             "traffic": recorded_traffic(kname, name), "kernel": kname,
              "peak_source": f"{src} ({key})", "kernel_ms": float(ms),
              "algorithmic": {"bytes": w["bytes"], "flops": w["flops"]}}
-        if int(info[15]) & 1 and bound == "tensor":
+        if int(info[15]) & 1 and bound == "tensor" and all(has_work.values()):
             # decode and prefill ran at once on disjoint SMs: the kernel's share of the chip's tensor peak
             # (HBM bandwidth is shared, not split by SMs)
-            per_sm = int(info[13] if name == "decode_attention" else info[14])
-            ctas = int(info[10] if name == "decode_attention" else info[11])
+            per_sm = int(info[13] if kname == "decode_attention" else info[14])
+            ctas = int(info[10] if kname == "decode_attention" else info[11])
             sms = min(int(info[12]), -(-ctas // max(per_sm, 1)))
             r["sms"] = sms
             r["frac_of_sm_share"] = achieved / (peak * sms / max(int(info[12]), 1)) if sms else None
         return r
 
-    attn = [i for i, n in enumerate(KERNEL_NAMES) if n.endswith("_attention")]
-    dom = max(attn, key=lambda i: mean_k[i])
-    roof = kernel_roof(KERNEL_NAMES[dom], mean_k[dom])
-    kroofs = {KERNEL_NAMES[i]: kernel_roof(KERNEL_NAMES[i], mean_k[i]) for i in attn
-              if work["decode" if KERNEL_NAMES[i] == "decode_attention" else "prefill"]["bytes"] > 0}
+    # the dominant kernel: the longer of the attention kernels that had work (an idle kernel's
+    # span is only its launch)
+    attn = [i for i, n in enumerate(KERNEL_NAMES) if n.endswith("_attention") and has_work[n]]
+    kroofs = {KERNEL_NAMES[i]: kernel_roof(KERNEL_NAMES[i], mean_k[i]) for i in attn}
+    dom = max(attn, key=lambda i: mean_k[i]) if attn else None
+    roof = kroofs[KERNEL_NAMES[dom]] if dom is not None else None
     # the whole step against the combined roofline time max(bytes / BW, FLOPs / peak)
     t_star = max(work["bytes"] / (hbm * 1e9), work["flops"] / (tf_burst * 1e12))
+    kv_gb = prob.kv_pages.nbytes / 1e9
+    res = {
+        "workload": f"{name}: {DESCR[name]}", "value": value, "unit": "tokens/s", "steps": K,
+        "warmup": max(3, warmup), "ms_per_step": ms_step,
+        "dtype": "bf16" if prob.kv_dtype == "bf16" else "f16 (e4m3 K/V converted exactly)",
+        "config": {"workload": f"{name}: {DESCR[name]}", "num_seqs": prob.num_seqs, "q_tokens": tokens,
+                   "kv_tokens": int(prob.kv_lens[: prob.num_seqs].sum()),
+                   "l2": f"no flush: inputs larger than L2 (K/V cache {kv_gb:.2f} GB)"
+                   if kv_gb > 0.129 else f"K/V cache {kv_gb:.3f} GB, about L2-sized (no flush)",
+                   "ranks": world},
+        "step_hbm_gbs": work["bytes"] / (ms_step * 1e-3) / 1e9,
+        "step_tflops": work["flops"] / (ms_step * 1e-3) / 1e12,
+        "step_roofline_frac": t_star / (ms_step * 1e-3),
+        "step_roofline_bound": "hbm" if work["bytes"] / (hbm * 1e9) >= work["flops"] / (tf_burst * 1e12) else "tensor",
+        "kernel_rooflines": kroofs,
+        "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k)},
+        "roofline": roof, "gpu_launches": 4 * K, "clocks": clk,
+    }
 
     # end to end through the public host-buffer entry point
-    e2e = None
-    if args.e2e_steps > 0:
+    if e2e_steps > 0:
         hq = q.cpu().pin_memory()
         hkvl = kvl.cpu().pin_memory()
         hpi = pi.cpu().pin_memory()
@@ -388,7 +412,7 @@ def main():
         for _ in range(3):
             att.forward_host(hq, kv, hkvl, hpi, hcu, prob.num_seqs, hout, stream=stream)
         torch.cuda.synchronize()
-        Ke = args.e2e_steps
+        Ke = e2e_steps
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
@@ -398,37 +422,69 @@ def main():
         torch.cuda.synchronize()
         ms_e = max_over_ranks(a0.elapsed_time(a1), dist, dev)
         h2d = sum(x.numel() * x.element_size() for x in (hq, hkvl, hpi, hcu))
-        e2e = {"value": job_throughput(tokens, Ke, world, ms_e), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
-               "ms_per_step": ms_e / Ke, "steps": Ke}
+        res["e2e"] = {"value": job_throughput(tokens, Ke, world, ms_e), "unit": "tokens/s",
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(hout.numel() * hout.element_size()),
+                      "ms_per_step": ms_e / Ke, "steps": Ke}
+    att.close()
+    del q, kv, kvl, pi, cu, out
+    torch.cuda.empty_cache()
+    return res, prob
+
+
+# the other workloads of the default line: (name, timed steps); each K/V cache is far above L2
+# except long_prefill's (134 MB, about L2-sized)
+SIDE_WORKLOADS = (("mixed", 300), ("fp8_window", 300), ("long_prefill", 100))
+
+
+def main():
+    args = parse()
+    world, rank, local_rank = rank_layout()
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    import torch
+
+    import __graft_entry__
+
+    torch.cuda.set_device(local_rank)  # before the process group, so NCCL binds this rank's GPU
+    dist = init_ranks(world)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if dist is not None:
+        dist.barrier()
+
+    res, prob = measure(args.workload, args.steps, args.warmup, dist, dev, world, e2e_steps=args.e2e_steps)
+    # the default line also carries the other workloads of the metric (prefill TFLOP/s, the mixed
+    # batch, fp8 K/V), each measured the same way; the headline value stays the decode batch's
+    side = {}
+    if not args.no_side_workloads and args.workload == "decode":
+        for name, k in SIDE_WORKLOADS:
+            r, _ = measure(name, min(k, max(1, args.steps)), args.warmup, dist, dev, world)
+            side[name] = {key: r[key] for key in ("value", "unit", "ms_per_step", "steps", "dtype", "config",
+                                                  "step_roofline_frac", "step_roofline_bound", "step_hbm_gbs",
+                                                  "step_tflops", "kernel_rooflines", "kernels_ms", "roofline",
+                                                  "clocks")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(prob)
 
     if rank == 0:
-        kv_gb = prob.kv_pages.nbytes / 1e9
         line = {
-            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if prob.kv_dtype == "bf16" else "f16 (e4m3 K/V converted exactly)",
-            "data": "synthetic (seeded)",
-            "config": {"workload": f"{args.workload}: {DESCR[args.workload]}",
-                       "num_seqs": prob.num_seqs, "q_tokens": tokens,
-                       "kv_tokens": int(prob.kv_lens[: prob.num_seqs].sum()),
-                       "l2": f"no flush: inputs larger than L2 (K/V cache {kv_gb:.2f} GB)"
-                       if kv_gb > 0.129 else "inputs fit in L2 (no flush)",
-                       "ranks": world},
-            "step_hbm_gbs": work["bytes"] / (ms_step * 1e-3) / 1e9,
-            "step_tflops": work["flops"] / (ms_step * 1e-3) / 1e12,
-            "step_roofline_frac": t_star / (ms_step * 1e-3),
-            "kernel_rooflines": kroofs,
-            "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k)},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * K, "clocks": clk,
+            "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": res["steps"],
+            "warmup": res["warmup"], "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": res["dtype"], "data": "synthetic (seeded)",
+            "config": res["config"],
+            "step_hbm_gbs": res["step_hbm_gbs"], "step_tflops": res["step_tflops"],
+            "step_roofline_frac": res["step_roofline_frac"],
+            "kernel_rooflines": res["kernel_rooflines"], "kernels_ms": res["kernels_ms"],
+            "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res.get("e2e"),
+            "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
         }
+        if side:
+            line["workloads"] = side
         print(json.dumps(line, default=float), flush=True)
-    att.close()
     if dist is not None:
         dist.destroy_process_group()
 
@@ -438,7 +494,7 @@ if __name__ == "__main__":
     if a0.all and a0.impl == "ours":
         for w in ("decode", "mixed", "fp8_window", "long_prefill"):
             sys.argv = [sys.argv[0], "--workload", w, "--steps", str(a0.steps), "--warmup",
-                        str(a0.warmup), "--no-cpu-baseline", "--e2e-steps", "0"]
+                        str(a0.warmup), "--no-cpu-baseline", "--e2e-steps", "0", "--no-side-workloads"]
             main()
     else:
         main()

@@ -153,14 +153,40 @@ int rpa_get_status(RpaHandle* h, void* stream);
 int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items, void* stream);
 
 /* Per-kernel timing for benchmarks.  After rpa_profile_begin(h, n) the next n
- * calls of rpa_forward on h record CUDA events (on their stream) around each
- * of their four kernels: planner, decode attention, prefill attention,
- * combine.  rpa_profile_read synchronises on those events and writes, for
- * each recorded call c < *n_calls, ms[4*c + k] = duration of kernel k in
- * milliseconds; ms holds max_calls*4 floats (host).  Profiling stops after
- * n calls or at the next rpa_profile_begin; the events are owned by h. */
+ * calls of rpa_forward on h record CUDA events around each of their four
+ * kernels: planner, decode attention, prefill attention, combine.  Each kernel
+ * is timed on the stream it runs on, from an event recorded just before its
+ * launch (after any wait on the other stream) to one recorded just after it,
+ * so that the two attention kernels are timed correctly also when they run at
+ * once on two streams.  rpa_profile_read synchronises on those events and
+ * writes, for each recorded call c < *n_calls, ms[4*c + k] = duration of
+ * kernel k in milliseconds (a kernel with no work reads as its launch time);
+ * ms holds max_calls*4 floats (host).  Profiling stops after n calls or at the
+ * next rpa_profile_begin; the events are owned by h. */
 int rpa_profile_begin(RpaHandle* h, int32_t max_calls);
 int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_calls);
+
+/* Options of a handle (rpa_set_option).  Production code needs none of them;
+ * the library reads no environment variable. */
+typedef enum RpaOption {
+    RPA_OPT_WAIT_TIMEOUT_MS = 1,   /* bound of every device-side wait, in ms (1 .. 3600000; default
+                                      1000); a wait that runs out sets RPA_ERR_TIMEOUT */
+    RPA_OPT_SERIAL = 2,            /* 1: run decode and prefill attention one after the other on the
+                                      caller's stream instead of concurrently on two streams with an
+                                      SM split (default 0; configurations without the split always
+                                      run serially) */
+    RPA_OPT_PREFILL_SMS = 3,       /* > 0: SMs given to prefill attention when both kernels have
+                                      work and run concurrently (0 = the planner's model; tuning) */
+    RPA_OPT_DECODE_SMS = 4,        /* > 0: SMs given to decode attention (0 = the planner's model) */
+    RPA_OPT_TEST_STALL_PRODUCER = 100  /* test hook, 1: the decode kernel's copy warp issues nothing, so
+                                      that its consumers' bounded waits run out (status
+                                      RPA_ERR_TIMEOUT); the kernel still returns */
+} RpaOption;
+
+/* Set option `option` of h to `value` for the following calls.  Host only.
+ * Returns RPA_OK, or RPA_ERR_INVALID_ARG for an unknown option or a value
+ * outside its range (the option is then unchanged). */
+int rpa_set_option(RpaHandle* h, int32_t option, int64_t value);
 
 /* rpa_forward for callers that cannot allocate device memory.
  *
@@ -185,7 +211,9 @@ int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_call
  * the previous call's contents (the call clears what must start at zero), so
  * calls that overlap on the GPU -- on different streams, or from different
  * threads -- race and must be serialised by the caller.  The device-side
- * status (bad lengths or page ids) is not reported by this entry point. */
+ * status is not reported by this entry point: bad lengths (o all zero), a bad
+ * page id, and a device wait that ran out (after 1 s; o then unspecified)
+ * still return RPA_OK. */
 int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void* kv_pages,
                         const int32_t* kv_lens, const int32_t* page_indices,
                         const int32_t* cu_q_lens, int32_t num_seqs, void* o, void* stream);
@@ -196,7 +224,7 @@ void rpa_destroy(RpaHandle* h);
 /* Static description of a status code. */
 const char* rpa_strerror(int code);
 
-/* ABI version of this header (major*100 + minor). */
+/* ABI version of this header (major*100 + minor): 200. */
 int rpa_version(void);
 
 #ifdef __cplusplus

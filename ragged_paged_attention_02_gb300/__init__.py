@@ -19,6 +19,11 @@ from .binding import (  # noqa: F401
     RPA_ERR_TIMEOUT,
     RPA_ERR_UNSUPPORTED,
     RPA_OK,
+    RPA_OPT_DECODE_SMS,
+    RPA_OPT_PREFILL_SMS,
+    RPA_OPT_SERIAL,
+    RPA_OPT_TEST_STALL_PRODUCER,
+    RPA_OPT_WAIT_TIMEOUT_MS,
     RaggedPagedAttention,
     RpaError,
     lib,

@@ -29,8 +29,14 @@ RPA_DT_FP8_E4M3 = 1
 
 # every entry point declared in include/rpa.h
 EXPORTS = ("rpa_cfg_init", "rpa_validate_cfg", "rpa_create", "rpa_forward", "rpa_forward_host",
-           "rpa_get_status", "rpa_read_plan", "rpa_profile_begin", "rpa_profile_read",
+           "rpa_get_status", "rpa_read_plan", "rpa_profile_begin", "rpa_profile_read", "rpa_set_option",
            "rpa_forward_noalloc", "rpa_destroy", "rpa_strerror", "rpa_version")
+
+RPA_OPT_WAIT_TIMEOUT_MS = 1
+RPA_OPT_SERIAL = 2
+RPA_OPT_PREFILL_SMS = 3
+RPA_OPT_DECODE_SMS = 4
+RPA_OPT_TEST_STALL_PRODUCER = 100
 
 
 class RpaCfg(ctypes.Structure):
@@ -90,6 +96,8 @@ def lib():
         L.rpa_profile_begin.restype = ctypes.c_int
         L.rpa_profile_read.argtypes = [vp, vp, i32, vp]
         L.rpa_profile_read.restype = ctypes.c_int
+        L.rpa_set_option.argtypes = [vp, i32, i64]
+        L.rpa_set_option.restype = ctypes.c_int
         L.rpa_forward_noalloc.argtypes = [ctypes.POINTER(RpaCfg), vp, vp, vp, vp, vp, i32, vp, vp]
         L.rpa_forward_noalloc.restype = ctypes.c_int
         L.rpa_destroy.argtypes = [vp]
@@ -221,6 +229,11 @@ class RaggedPagedAttention:
 
     def status(self, stream=None) -> int:
         return int(lib().rpa_get_status(self._h, _stream_ptr(stream)))
+
+    def set_option(self, option: int, value: int):
+        r = lib().rpa_set_option(self._h, int(option), int(value))
+        if r != RPA_OK:
+            raise RpaError(r, "rpa_set_option")
 
     def profile_begin(self, max_calls: int):
         r = lib().rpa_profile_begin(self._h, int(max_calls))

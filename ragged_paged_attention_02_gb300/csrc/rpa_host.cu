@@ -37,8 +37,8 @@ struct RpaHandle {
     int window;
     int BR, br_shift, Tt;
     int dec_rows;         // query rows of a decode tile: 8 (bf16, G <= 8) or 16
-    int debug_stall;
-    unsigned long long timeout_ns;
+    int debug_stall;      // RPA_OPT_TEST_STALL_PRODUCER
+    unsigned long long timeout_ns;  // RPA_OPT_WAIT_TIMEOUT_MS
     void* ws;
     size_t ws_bytes;
     int* ctrl;
@@ -53,14 +53,16 @@ struct RpaHandle {
     uint8_t* stage;
     size_t stage_bytes;
     // per-kernel timing (rpa_profile_begin / rpa_profile_read)
-    cudaEvent_t* prof_ev;   // [prof_cap][5]
+    cudaEvent_t* prof_ev;   // [prof_cap][kProfEvents]
     int prof_cap;
     int prof_used;
-    // decode and prefill run concurrently: decode on a second stream forked after the planner
-    int concurrent;
+    // decode and prefill may run concurrently: decode on a second stream forked after the planner
+    int can_concurrent;   // the side stream and events exist (tensor-memory bf16 prefill)
+    int serial;           // RPA_OPT_SERIAL: run the two one after the other on the caller's stream
+    int concurrent;       // the mode of the last call
     cudaStream_t side;
     cudaEvent_t ev_plan, ev_dec;
-    int force_pf_sms, force_dec_sms;  // tuning hooks (environment, read at rpa_create)
+    int force_pf_sms, force_dec_sms;  // RPA_OPT_PREFILL_SMS / RPA_OPT_DECODE_SMS
 };
 
 namespace {
@@ -89,15 +91,22 @@ struct DeviceGuard {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
-// event k (0..4) of the call being profiled, or nullptr when not profiling
+// Profile events of one call: each kernel is timed from an event recorded on its own stream
+// just before its launch (after any cross-stream wait) to one recorded just after it.
+enum ProfEvent : int {
+    kEvStart = 0, kEvPlanEnd, kEvDecStart, kEvDecEnd, kEvPfStart, kEvPfEnd, kEvCombStart, kEvCombEnd,
+    kProfEvents
+};
+
+// event k of the call being profiled, or nullptr when not profiling
 cudaEvent_t prof_event(RpaHandle* h, int k) {
     if (!h->prof_ev || h->prof_used >= h->prof_cap) return nullptr;
-    return h->prof_ev[h->prof_used * 5 + k];
+    return h->prof_ev[h->prof_used * kProfEvents + k];
 }
 
 void prof_free(RpaHandle* h) {
     if (!h->prof_ev) return;
-    for (int i = 0; i < h->prof_cap * 5; ++i)
+    for (int i = 0; i < h->prof_cap * kProfEvents; ++i)
         if (h->prof_ev[i]) cudaEventDestroy(h->prof_ev[i]);
     free(h->prof_ev);
     h->prof_ev = nullptr;
@@ -108,7 +117,7 @@ void prof_free(RpaHandle* h) {
 
 extern "C" {
 
-int rpa_version(void) { return 100; }
+int rpa_version(void) { return 200; }
 
 const char* rpa_strerror(int code) {
     switch (code) {
@@ -203,43 +212,23 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
     h->pf_tokens = h->tc    ? 2 * (kTcRows / h->G)
                    : h->tc8 ? kTcRows / h->G
                             : (kPfRows / h->G > 0 ? kPfRows / h->G : 1);
+    h->timeout_ns = 1000000000ull;  // bound of every device wait (RPA_OPT_WAIT_TIMEOUT_MS)
+    // the SM-split model is calibrated for the tensor-memory bf16 prefill kernel only
+    h->can_concurrent = h->tc;
     {
-        // test hooks: a producer that issues nothing, and the bound of every device wait
-        const char* e = getenv("RPA_DEBUG_STALL_PRODUCER");
-        h->debug_stall = (e && e[0] == '1') ? 1 : 0;
-        const char* t = getenv("RPA_DEBUG_TIMEOUT_MS");
-        const long long ms = t ? atoll(t) : 1000;
-        h->timeout_ns = (unsigned long long)(ms > 0 ? ms : 1000) * 1000000ull;
-        // tuning hooks: run decode and prefill one after the other, or fix the SM split
-        const char* ser = getenv("RPA_SERIAL");
-        // the SM-split model is calibrated for the tensor-memory prefill kernel only
-        h->concurrent = (ser && ser[0] == '1') || !h->tc ? 0 : 1;
-        const char* fp = getenv("RPA_DEBUG_PF_SMS");
-        h->force_pf_sms = fp ? atoi(fp) : 0;
-        const char* fd = getenv("RPA_DEBUG_DEC_SMS");
-        h->force_dec_sms = fd ? atoi(fd) : 0;
-    }
-
-    {
-        // RPA_DEBUG=1 names the set-up step that failed (stderr)
-        const char* dbg = getenv("RPA_DEBUG");
-        const bool verbose = dbg && dbg[0] == '1';
         cudaError_t e = cudaSuccess;
-        const char* step = "";
-        if ((e = cudaGetDevice(&h->device)) != cudaSuccess) step = "cudaGetDevice";
+        bool failed = false;
+        if ((e = cudaGetDevice(&h->device)) != cudaSuccess) failed = true;
         else if ((e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device)) != cudaSuccess)
-            step = "multiprocessor count";
-        else if ((e = plan_prepare()) != cudaSuccess) step = "planner attributes";
+            failed = true;
+        else if ((e = plan_prepare()) != cudaSuccess) failed = true;
         else if ((e = h->tc    ? prefill_tc_prepare(h->D, &h->pf_bps)
                       : h->tc8 ? prefill_tc8_prepare(h->D, &h->pf_bps)
                                : attn_prepare(h->D, h->fp8, &h->pf_bps)) != cudaSuccess)
-            step = "prefill kernel attributes";
-        else if ((e = decode_prepare(h->D, h->fp8, h->dec_rows, &h->dec_bps)) != cudaSuccess)
-            step = "decode kernel attributes";
-        else if (h->pf_bps < 1) step = "prefill kernel cannot be resident";
-        else if (h->dec_bps < 1) step = "decode kernel cannot be resident";
-        if (step[0]) {
-            if (verbose) fprintf(stderr, "rpa_create: %s failed: %s\n", step, cudaGetErrorString(e));
+            failed = true;
+        else if ((e = decode_prepare(h->D, h->fp8, h->dec_rows, &h->dec_bps)) != cudaSuccess) failed = true;
+        else if (h->pf_bps < 1 || h->dec_bps < 1) failed = true;  // a kernel cannot be resident
+        if (failed) {
             cudaGetLastError();
             delete h;
             return RPA_ERR_CUDA;
@@ -273,7 +262,7 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out) {
         delete h;
         return RPA_ERR_CUDA;
     }
-    if (h->concurrent && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+    if (h->can_concurrent && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
                           cudaEventCreateWithFlags(&h->ev_plan, cudaEventDisableTiming) != cudaSuccess ||
                           cudaEventCreateWithFlags(&h->ev_dec, cudaEventDisableTiming) != cudaSuccess)) {
         cudaGetLastError();
@@ -316,6 +305,8 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     DeviceGuard g(h->device);
     if (!g.ok) return RPA_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int conc = h->can_concurrent && !h->serial;
+    h->concurrent = conc;
 
     PlanParams pp;
     pp.kv_lens = kv_lens;
@@ -332,7 +323,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.dec_rows = h->dec_rows;
     pp.pf_tokens = h->pf_tokens;
     pp.dec_slots = h->sms * h->dec_bps;
-    pp.concurrent = h->concurrent;
+    pp.concurrent = conc;
     pp.n_sms = h->sms;
     pp.dec_bps = h->dec_bps;
     pp.pf_bps = h->pf_bps;
@@ -357,11 +348,12 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     pp.dec_items = h->dec_items;
     pp.pf_items = h->pf_items;
     pp.comb = h->comb;
-    cudaEvent_t ev[5];
-    for (int k = 0; k < 5; ++k) ev[k] = prof_event(h, k);
-    if (ev[0] && cudaEventRecord(ev[0], st) != cudaSuccess) return RPA_ERR_CUDA;
+    cudaEvent_t ev[kProfEvents];
+    for (int k = 0; k < kProfEvents; ++k) ev[k] = prof_event(h, k);
+    auto rec = [&](int k, cudaStream_t on) { return !ev[k] || cudaEventRecord(ev[k], on) == cudaSuccess; };
+    if (!rec(kEvStart, st)) return RPA_ERR_CUDA;
     if (launch_plan(pp, st, plan_smem_bytes()) != cudaSuccess) return RPA_ERR_CUDA;
-    if (ev[1] && cudaEventRecord(ev[1], st) != cudaSuccess) return RPA_ERR_CUDA;
+    if (!rec(kEvPlanEnd, st)) return RPA_ERR_CUDA;
 
     AttnParams ap;
     ap.q = static_cast<const uint8_t*>(q);
@@ -390,28 +382,51 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     ap.part_o = h->part_o;
     ap.part_ml = h->part_ml;
 
+    // With concurrent decode / prefill the decode kernel runs on the side stream, forked from st
+    // after the planner.  Once forked, every return joins it back (st waits for whatever was
+    // enqueued there), so that no kernel of this call is still writing the workspace when the
+    // caller's stream moves on.
     cudaStream_t dst = st;  // stream of the decode kernel
-    if (h->concurrent) {
+    bool forked = false;
+    auto join = [&]() -> bool {
+        if (!forked) return true;
+        forked = false;
+        return cudaEventRecord(h->ev_dec, h->side) == cudaSuccess &&
+               cudaStreamWaitEvent(st, h->ev_dec, 0) == cudaSuccess;
+    };
+    auto fail = [&](int code) {
+        join();
+        return code;
+    };
+    if (conc) {
         if (cudaEventRecord(h->ev_plan, st) != cudaSuccess || cudaStreamWaitEvent(h->side, h->ev_plan, 0) != cudaSuccess)
             return RPA_ERR_CUDA;
         dst = h->side;
+        forked = true;
     }
     if (c.num_q_tokens > 0) {
         if (h->kvmap_ptr != kv_pages) {
             if (encode_kv_map_runs(&h->kvmap, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
                                    (int)c.num_kv_heads, h->D, h->BR) != 0 ||
                 (h->tc && encode_kv_map(&h->kvmap_pf, kv_pages, h->fp8, c.total_num_pages, (int)c.page_size,
-                                        (int)c.num_kv_heads, h->D, h->BR) != 0))
-                return RPA_ERR_INVALID_ARG;
+                                        (int)c.num_kv_heads, h->D, h->BR) != 0)) {
+                h->kvmap_ptr = nullptr;
+                return fail(RPA_ERR_INVALID_ARG);
+            }
             h->kvmap_ptr = kv_pages;
         }
         if (h->qmap_ptr != q) {
             if (encode_q_map(&h->qmap, q, c.num_q_tokens, (int)c.num_q_heads, h->D, h->G, h->Tt) != 0 ||
                 ((h->tc || h->tc8) && encode_q_map(&h->qmap_pf, q, c.num_q_tokens, (int)c.num_q_heads, h->D,
-                                                   h->G, kTcRows / h->G) != 0))
-                return RPA_ERR_INVALID_ARG;
+                                                   h->G, kTcRows / h->G) != 0)) {
+                h->qmap_ptr = nullptr;
+                return fail(RPA_ERR_INVALID_ARG);
+            }
             h->qmap_ptr = q;
         }
+    }
+    if (!rec(kEvDecStart, dst)) return fail(RPA_ERR_CUDA);
+    if (c.num_q_tokens > 0) {
         DecParams dp;
         dp.a = ap;
         dp.a.items = h->dec_items;
@@ -424,38 +439,32 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
         dp.timeout_ns = h->timeout_ns;
         if (launch_decode_tma(h->kvmap, h->qmap, dp, h->fp8, h->dec_rows, Launch{h->sms * h->dec_bps, dst}) !=
             cudaSuccess)
-            return RPA_ERR_CUDA;
+            return fail(RPA_ERR_CUDA);
     }
-    if (ev[2] && cudaEventRecord(ev[2], dst) != cudaSuccess) return RPA_ERR_CUDA;
-    if (h->concurrent && cudaEventRecord(h->ev_dec, dst) != cudaSuccess) return RPA_ERR_CUDA;
+    if (!rec(kEvDecEnd, dst)) return fail(RPA_ERR_CUDA);
 
+    if (!rec(kEvPfStart, st)) return fail(RPA_ERR_CUDA);
     if (c.num_q_tokens > 0) {
         ap.items = h->pf_items;
         ap.item_count_word = kNumPfItems;
         ap.counter_word = kPfCounter;
-        if (h->tc) {
+        cudaError_t e;
+        if (h->tc || h->tc8) {
             TcParams tp;
             tp.a = ap;
             tp.BR = h->BR;
             tp.Tq = h->pf_tokens;
             tp.timeout_ns = h->timeout_ns;
-            if (launch_prefill_tc(h->kvmap_pf, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
-                return RPA_ERR_CUDA;
-        } else if (h->tc8) {
             // the fp8 kernel copies whole page runs (K and V of the head) with the decode gather's map
-            TcParams tp;
-            tp.a = ap;
-            tp.BR = h->BR;
-            tp.Tq = h->pf_tokens;
-            tp.timeout_ns = h->timeout_ns;
-            if (launch_prefill_tc8(h->kvmap, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st}) != cudaSuccess)
-                return RPA_ERR_CUDA;
-        } else if (launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st}) != cudaSuccess) {
-            return RPA_ERR_CUDA;
+            e = h->tc ? launch_prefill_tc(h->kvmap_pf, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st})
+                      : launch_prefill_tc8(h->kvmap, h->qmap_pf, tp, Launch{h->sms * h->pf_bps, st});
+        } else {
+            e = launch_prefill(ap, h->fp8, Launch{h->sms * h->pf_bps, st});
         }
+        if (e != cudaSuccess) return fail(RPA_ERR_CUDA);
     }
-    if (ev[3] && cudaEventRecord(ev[3], st) != cudaSuccess) return RPA_ERR_CUDA;
-    if (h->concurrent && cudaStreamWaitEvent(st, h->ev_dec, 0) != cudaSuccess) return RPA_ERR_CUDA;
+    if (!rec(kEvPfEnd, st)) return fail(RPA_ERR_CUDA);
+    if (!join()) return RPA_ERR_CUDA;
 
     CombParams cp;
     cp.o = static_cast<uint8_t*>(o);
@@ -471,9 +480,10 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     cp.comb = h->comb;
     cp.part_o = h->part_o;
     cp.part_ml = h->part_ml;
+    if (!rec(kEvCombStart, st)) return RPA_ERR_CUDA;
     if (launch_combine(cp, Launch{h->sms * 2, st}) != cudaSuccess) return RPA_ERR_CUDA;
-    if (ev[4]) {
-        if (cudaEventRecord(ev[4], st) != cudaSuccess) return RPA_ERR_CUDA;
+    if (ev[kEvCombEnd]) {
+        if (cudaEventRecord(ev[kEvCombEnd], st) != cudaSuccess) return RPA_ERR_CUDA;
         ++h->prof_used;
     }
     return RPA_OK;
@@ -485,10 +495,10 @@ int rpa_profile_begin(RpaHandle* h, int32_t max_calls) {
     if (!g.ok) return RPA_ERR_CUDA;
     prof_free(h);
     if (max_calls == 0) return RPA_OK;
-    h->prof_ev = static_cast<cudaEvent_t*>(calloc((size_t)max_calls * 5, sizeof(cudaEvent_t)));
+    h->prof_ev = static_cast<cudaEvent_t*>(calloc((size_t)max_calls * kProfEvents, sizeof(cudaEvent_t)));
     if (!h->prof_ev) return RPA_ERR_INVALID_ARG;
     h->prof_cap = max_calls;
-    for (int i = 0; i < max_calls * 5; ++i) {
+    for (int i = 0; i < max_calls * kProfEvents; ++i) {
         if (cudaEventCreate(&h->prof_ev[i]) != cudaSuccess) {
             cudaGetLastError();
             prof_free(h);
@@ -503,21 +513,45 @@ int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_call
     DeviceGuard g(h->device);
     if (!g.ok) return RPA_ERR_CUDA;
     const int n = h->prof_used < max_calls ? h->prof_used : max_calls;
+    // kernel k runs between events from[k] and to[k] of its call, both on the kernel's own stream
+    static const int from[4] = {kEvStart, kEvDecStart, kEvPfStart, kEvCombStart};
+    static const int to[4] = {kEvPlanEnd, kEvDecEnd, kEvPfEnd, kEvCombEnd};
     for (int c = 0; c < n; ++c) {
-        if (cudaEventSynchronize(h->prof_ev[c * 5 + 4]) != cudaSuccess) return RPA_ERR_CUDA;
-        // events: 0 start, 1 planner done, 2 decode done, 3 prefill done, 4 combine done;
-        // with concurrent decode / prefill both are timed from the planner's end
-        static const int from_ser[4] = {0, 1, 2, 3}, from_con[4] = {0, 1, 1, 3};
-        const int* from = h->concurrent ? from_con : from_ser;
+        cudaEvent_t* e = h->prof_ev + (size_t)c * kProfEvents;
+        if (cudaEventSynchronize(e[kEvCombEnd]) != cudaSuccess) return RPA_ERR_CUDA;
         for (int k = 0; k < 4; ++k) {
             float t = 0.f;
-            if (cudaEventElapsedTime(&t, h->prof_ev[c * 5 + from[k]], h->prof_ev[c * 5 + k + 1]) != cudaSuccess)
-                return RPA_ERR_CUDA;
+            if (cudaEventElapsedTime(&t, e[from[k]], e[to[k]]) != cudaSuccess) return RPA_ERR_CUDA;
             ms[c * 4 + k] = t;
         }
     }
     *n_calls = n;
     return RPA_OK;
+}
+
+int rpa_set_option(RpaHandle* h, int32_t option, int64_t value) {
+    if (!h) return RPA_ERR_INVALID_ARG;
+    switch (option) {
+        case RPA_OPT_WAIT_TIMEOUT_MS:
+            if (value < 1 || value > 3600000) return RPA_ERR_INVALID_ARG;
+            h->timeout_ns = (unsigned long long)value * 1000000ull;
+            return RPA_OK;
+        case RPA_OPT_SERIAL:
+            if (value != 0 && value != 1) return RPA_ERR_INVALID_ARG;
+            h->serial = (int)value;
+            return RPA_OK;
+        case RPA_OPT_PREFILL_SMS:
+        case RPA_OPT_DECODE_SMS:
+            if (value < 0 || value > h->sms) return RPA_ERR_INVALID_ARG;
+            (option == RPA_OPT_PREFILL_SMS ? h->force_pf_sms : h->force_dec_sms) = (int)value;
+            return RPA_OK;
+        case RPA_OPT_TEST_STALL_PRODUCER:
+            if (value != 0 && value != 1) return RPA_ERR_INVALID_ARG;
+            h->debug_stall = (int)value;
+            return RPA_OK;
+        default:
+            return RPA_ERR_INVALID_ARG;
+    }
 }
 
 int rpa_forward_host(RpaHandle* h, const void* q_host, const void* kv_pages, const int32_t* kv_lens_host,

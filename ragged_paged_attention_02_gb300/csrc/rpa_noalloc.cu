@@ -69,8 +69,10 @@ int setup(int dev, int D, int fp8, int dec_rows, void** scratch, int* dec_bps, i
             cudaGetLastError();
             return RPA_ERR_CUDA;
         }
-        g_dec_bps[dev][di][fp8][r8] = a < 1 ? 1 : a;
-        g_pf_bps[dev][di][fp8][r8] = b < 1 ? 1 : b;
+        // a kernel that cannot be resident: refuse before anything is enqueued (as rpa_create does)
+        if (a < 1 || b < 1) return RPA_ERR_CUDA;
+        g_dec_bps[dev][di][fp8][r8] = a;
+        g_pf_bps[dev][di][fp8][r8] = b;
         g_ready[dev][di][fp8][r8] = true;
     }
     *scratch = g_scratch_dev[dev];

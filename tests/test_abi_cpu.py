@@ -31,7 +31,7 @@ def test_header_declares_the_binding_exports():
 def test_library_exports_every_header_symbol(L):
     for name in header_functions():
         assert hasattr(L, name), name
-    assert L.rpa_version() == 100
+    assert L.rpa_version() == 200
 
 
 def test_strerror_covers_codes(L):
@@ -72,6 +72,7 @@ def test_null_handle_and_create_out(L):
 
     assert L.rpa_forward(None, None, None, None, None, None, 0, None, None) == rpa.RPA_ERR_INVALID_ARG
     assert L.rpa_get_status(None, None) == rpa.RPA_ERR_INVALID_ARG
+    assert L.rpa_set_option(None, rpa.RPA_OPT_SERIAL, 1) == rpa.RPA_ERR_INVALID_ARG
     c = rpa.make_cfg(**BASE)
     assert L.rpa_create(ctypes.byref(c), None) == rpa.RPA_ERR_INVALID_ARG
     bad = rpa.make_cfg(**dict(BASE, head_dim=80))

@@ -2,8 +2,9 @@
 
 Tolerance: |gpu - oracle| <= 2e-2 + 2e-2*|oracle| for bf16 K/V and
 6e-2 + 6e-2*|oracle| for fp8 K/V, element by element.  Small cases compare
-every row; the full-size workloads compare every row the oracle can afford
-(decode) or a seeded sample of rows (the rest), plus whole-output properties.
+every row; the full-size workloads compare every row (decode, mixed,
+fp8_window) or a seeded sample of over 8 k rows that holds every query tile's
+first and last row (long_prefill, 2.1 M rows), plus whole-output properties.
 """
 import numpy as np
 import pytest
@@ -82,6 +83,17 @@ SMALL = [
               kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, soft_cap=20.0, sliding_window=300)),
     (71, dict(num_seqs=10, decode_only=True, max_kv=3000, num_q_heads=8, num_kv_heads=2, head_dim=64,
               page_size=32, kv_dtype="fp8_e4m3", k_scale=0.08, v_scale=0.05)),
+    # fp8 K/V with G >= 16 on the tensor-memory kernel: query tiles of 8, 4 and 2 tokens; decode rows
+    # (q_len 1, G 16) as split pieces merged by the combine kernel
+    (72, dict(num_seqs=9, max_q=20, max_kv=3000, num_q_heads=32, num_kv_heads=2, head_dim=128, page_size=16,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05)),
+    (73, dict(num_seqs=7, max_q=10, max_kv=2000, num_q_heads=32, num_kv_heads=1, head_dim=256, page_size=32,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.06, soft_cap=50.0, sliding_window=700,
+              sm_scale=1 / 16)),
+    (74, dict(num_seqs=6, max_q=6, max_kv=1500, num_q_heads=64, num_kv_heads=1, head_dim=128, page_size=16,
+              kv_dtype="fp8_e4m3", k_scale=0.07, v_scale=0.05, is_causal=False)),
+    (75, dict(num_seqs=8, decode_only=True, max_kv=6000, num_q_heads=32, num_kv_heads=2, head_dim=256,
+              page_size=16, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
 ]
 
 
@@ -94,29 +106,44 @@ def test_small_cases_all_rows(case):
     assert_close(got, oracle.forward(p), p.kv_dtype, f"small case {case}")
 
 
-def _sample_rows(p, n, seed):
+def _sample_rows(p, n, seed, tile_tokens):
+    """n random (token, q head) rows, plus, for every query tile of `tile_tokens` tokens of every
+    sequence, its first and last token, each with the first and the last q head of a random kv
+    group (the first and last MMA rows of the tile), and every sequence's first and last token."""
     rng = np.random.default_rng(seed)
+    G = p.num_q_heads // p.num_kv_heads
     T = int(p.cu_q_lens[p.num_seqs])
-    t = rng.integers(0, T, size=n)
-    # always include the first and last token of every sequence (tails, decode rows)
-    ends = np.concatenate([p.cu_q_lens[:p.num_seqs], p.cu_q_lens[1:p.num_seqs + 1] - 1])
-    t = np.unique(np.concatenate([t, ends[ends >= 0]]))
-    h = rng.integers(0, p.num_q_heads, size=t.size)
-    return np.stack([t, h], axis=1).astype(np.int64)
+    toks, heads = [rng.integers(0, T, size=n)], [rng.integers(0, p.num_q_heads, size=n)]
+    for s in range(p.num_seqs):
+        q0, q1 = int(p.cu_q_lens[s]), int(p.cu_q_lens[s + 1])
+        if q1 == q0:
+            continue
+        first = np.arange(q0, q1, tile_tokens)
+        last = np.minimum(first + tile_tokens, q1) - 1
+        for t in (first, last):
+            grp = rng.integers(0, p.num_kv_heads, size=t.size) * G
+            toks += [t, t]
+            heads += [grp, grp + G - 1]
+    rows = np.unique(np.stack([np.concatenate(toks), np.concatenate(heads)], axis=1), axis=0)
+    return rows.astype(np.int64)
 
 
-@pytest.mark.parametrize("name,nrows", [("decode", None), ("mixed", 3000), ("fp8_window", 3000),
-                                        ("long_prefill", 1500)])
-def test_full_workloads(name, nrows):
+@pytest.mark.parametrize("name", ["decode", "mixed", "fp8_window", "long_prefill"])
+def test_full_workloads(name):
+    """The four full-size workloads in the launch configuration the benchmark times.  decode, mixed
+    and fp8_window: every output row against the oracle.  long_prefill (2.1 M rows): a seeded sample
+    of over 8 k rows holding the first and last row of every 128-row query tile."""
     p = ri.workload(name)
     got, st = run(p)
     assert st == 0
     assert np.isfinite(got).all()
-    if nrows is None:
+    if name != "long_prefill":
         ref = oracle.forward(p)
         assert_close(got, ref, p.kv_dtype, name)
     else:
-        rows = _sample_rows(p, nrows, 1234)
+        G = p.num_q_heads // p.num_kv_heads
+        rows = _sample_rows(p, 2000, 1234, tile_tokens=128 // G)
+        assert len(rows) >= 8000
         ref = oracle.rows(p, rows)
         assert_close(got[rows[:, 0], rows[:, 1]], ref, p.kv_dtype, name)
 
@@ -285,22 +312,45 @@ def test_repeat_calls_are_deterministic():
     att.close()
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(monkeypatch):
-    """The decode producer is told to issue nothing (test hook read at rpa_create): every
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The decode kernel's copy warp is told to issue nothing (the handle's test option): every
     consumer wait must expire after its bound, set RPA_ERR_TIMEOUT and return."""
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+    from ragged_paged_attention_02_gb300.binding import RPA_OPT_TEST_STALL_PRODUCER, RPA_OPT_WAIT_TIMEOUT_MS
 
     p = ri.random_small(49, num_seqs=4, decode_only=True, max_kv=300, num_q_heads=8,
                         num_kv_heads=2, head_dim=128)
-    monkeypatch.setenv("RPA_DEBUG_STALL_PRODUCER", "1")
-    monkeypatch.setenv("RPA_DEBUG_TIMEOUT_MS", "50")
     att = RaggedPagedAttention(**p.cfg_dict())
-    monkeypatch.delenv("RPA_DEBUG_STALL_PRODUCER")
-    monkeypatch.delenv("RPA_DEBUG_TIMEOUT_MS")
+    att.set_option(RPA_OPT_TEST_STALL_PRODUCER, 1)
+    att.set_option(RPA_OPT_WAIT_TIMEOUT_MS, 50)
     t = to_dev(p)
     att.forward(*t, p.num_seqs)
     assert att.status() == 6
+    att.set_option(RPA_OPT_TEST_STALL_PRODUCER, 0)
+    att.forward(*t, p.num_seqs)  # the same handle works again once the hook is off
+    assert att.status() == 0
     att.close()
-    got, st = run(p, tensors=t)  # a fresh handle on the same context works
+    got, st = run(p, tensors=t)  # and a fresh handle on the same context
     assert st == 0
     assert_close(got, oracle.forward(p), p.kv_dtype, "after timeout")
+
+
+def test_serial_option_matches_concurrent_bit_for_bit():
+    """RPA_OPT_SERIAL runs decode and prefill one after the other instead of on two streams at
+    once with an SM split; the work items are the same, so the outputs are identical."""
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+    from ragged_paged_attention_02_gb300.binding import RPA_OPT_SERIAL
+
+    p = ri.random_small(50, num_seqs=20, max_q=200, max_kv=3000, num_q_heads=16, num_kv_heads=4,
+                        head_dim=128)
+    att = RaggedPagedAttention(**p.cfg_dict())
+    t = to_dev(p)
+    a = o_to_f64(att.forward(*t, p.num_seqs))
+    info_a = att.plan(max_items=1)[0]
+    att.set_option(RPA_OPT_SERIAL, 1)
+    b = o_to_f64(att.forward(*t, p.num_seqs))
+    info_b = att.plan(max_items=1)[0]
+    assert att.status() == 0
+    assert (info_a[15] & 1) == 1 and (info_b[15] & 1) == 0
+    assert np.array_equal(a, b)
+    att.close()

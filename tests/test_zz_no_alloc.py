@@ -4,9 +4,12 @@ Serving engines that give all device memory to their own arena allocator, or
 that may not call cudaMalloc/cudaFree (an implicit device synchronisation)
 where attention runs, call this entry point instead of rpa_create +
 rpa_forward.  Its workspace is a fixed 32 MiB array inside the library.  This
-test calls it through the C ABI and checks that two calls in a row give the
-same output as the handle-based rpa_forward, at the tolerance of the other
-parity tests, and that an oversized configuration is refused.
+test calls it through the C ABI, twice in a row per case, and checks each
+output against the fp64 oracle and against the handle-based rpa_forward, at
+the tolerance of the other parity tests.  The cases reach every kernel branch
+of the entry point: the bf16 tensor-memory prefill, the warp-MMA prefill (bf16
+D 256), the fp8 tensor-memory prefill, 8- and 16-row decode tiles and split-KV
+pieces.  An oversized configuration is refused.
 """
 import ctypes
 
@@ -39,21 +42,33 @@ def _noalloc(prob, t, out):
                                          out.data_ptr(), stream)
 
 
-@pytest.mark.parametrize("name", ["tiny", "split_decode", "mixed_small"])
-def test_noalloc_matches_rpa_forward_twice(name):
+CASES = {
+    "tiny": None,
+    # 8-row decode tiles, long keys split into pieces (combine kernel)
+    "split_decode": (60, dict(num_seqs=12, decode_only=True, max_kv=6000, num_q_heads=32, num_kv_heads=8,
+                              head_dim=128)),
+    # fp8 K/V at D 256: the fp8 tensor-memory prefill (decode rows as its items too)
+    "fp8_mixed": (61, dict(num_seqs=8, max_q=80, max_kv=900, num_q_heads=16, num_kv_heads=8, head_dim=256,
+                           kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0,
+                           sliding_window=300, sm_scale=1 / 16)),
+    # bf16 at D 256: the warp-MMA prefill
+    "bf16_d256": (62, dict(num_seqs=6, max_q=70, max_kv=800, num_q_heads=8, num_kv_heads=4, head_dim=256,
+                           soft_cap=30.0, sm_scale=1 / 16)),
+    # bf16 with G = 16: 16-row decode tiles beside the bf16 tensor-memory prefill
+    "bf16_g16": (63, dict(num_seqs=10, max_q=30, max_kv=3000, num_q_heads=32, num_kv_heads=2, head_dim=128)),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_matches_oracle_and_rpa_forward_twice(name):
+    import oracle
     from gpu_util import assert_close, o_to_f64, to_dev
 
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
-    if name == "tiny":
-        p = ri.workload("tiny")
-    elif name == "split_decode":
-        p = ri.random_small(60, num_seqs=12, decode_only=True, max_kv=6000, num_q_heads=32,
-                            num_kv_heads=8, head_dim=128)
-    else:
-        p = ri.random_small(61, num_seqs=8, max_q=80, max_kv=900, num_q_heads=16, num_kv_heads=8,
-                            head_dim=256, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05,
-                            soft_cap=50.0, sliding_window=300, sm_scale=1 / 16)
+    case = CASES[name]
+    p = ri.workload("tiny") if case is None else ri.random_small(case[0], **case[1])
+    want = oracle.forward(p)
     t = to_dev(p)
     att = RaggedPagedAttention(**p.cfg_dict())
     ref = o_to_f64(att.forward(*t, p.num_seqs))
@@ -64,7 +79,8 @@ def test_noalloc_matches_rpa_forward_twice(name):
         assert _noalloc(p, t, out) == 0
         torch.cuda.synchronize()
         got = o_to_f64(out)
-        assert_close(got, ref, p.kv_dtype, f"noalloc {name}")
+        assert_close(got, want, p.kv_dtype, f"noalloc {name} vs oracle")
+        assert_close(got, ref, p.kv_dtype, f"noalloc {name} vs rpa_forward")
 
 
 def test_noalloc_rejects_oversized_workspace():

@@ -11,10 +11,15 @@ function of the C file follows the "ragged_paged.zig" page, sections
 ``flashAttention`` (mask, softcap, online softmax, PV) and ``run`` (sequence
 walk, GQA head mapping, dequant); see the C file's header for the readings.
 
+Attention sinks follow the "from_qwen_ops.rs" page (flat_softmax_rows_at,
+``sinks``): one extra logit per query head that starts the row maximum and
+joins the denominator with no value.
+
 Parity pins (tests/test_oracle_pins.py): brute-force dense attention on tiny
-unpaged inputs (fixed and random configurations), closed forms (uniform V,
-single allowed key, one-key sequences, zero-query means over the allowed keys,
-two-key weights), the softcap identity of the "from_qwen_ops.rs" page
+unpaged inputs (fixed and random configurations, with and without sinks),
+closed forms (uniform V, single allowed key, one-key sequences, zero-query
+means over the allowed keys, two-key weights, zero-query means shrunk by a
+sink), the softcap identity of the "from_qwen_ops.rs" page
 (``capped``), format decoders checked code by code, and the invariants of page
 placement, decode-vs-prefill, tail poisoning, sequence order, GQA repetition
 and fp8 scale folding.  tests/test_oracle_mutations.py plants slips in a copy
@@ -50,6 +55,7 @@ class OracleCfg(ctypes.Structure):
         ("soft_cap", ctypes.c_double), ("k_scale", ctypes.c_double),
         ("has_v_scale", ctypes.c_int32), ("has_sliding_window", ctypes.c_int32),
         ("v_scale", ctypes.c_double), ("sliding_window", ctypes.c_int64),
+        ("has_sinks", ctypes.c_int32), ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -100,6 +106,14 @@ def make_cfg(cfg: dict) -> OracleCfg:
     sw = cfg.get("sliding_window")
     c.has_sliding_window = 0 if sw is None else 1
     c.sliding_window = 0 if sw is None else int(sw)
+    sinks = cfg.get("sinks")
+    c.has_sinks = 0 if sinks is None else 1
+    if sinks is not None:
+        # the fp32 values the library reads, widened exactly; kept alive with the structure
+        arr = np.ascontiguousarray(np.asarray(sinks, dtype=np.float32).astype(np.float64))
+        assert arr.shape == (int(cfg["num_q_heads"]),)
+        c._sinks_keep = arr
+        c.sinks = arr.ctypes.data
     return c
 
 

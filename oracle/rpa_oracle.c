@@ -19,6 +19,15 @@
  *                and (no window or not (p - sliding_window >= j))
  *   o            = sum_j w_j V_j / sum_j w_j,  w_j = exp(x_j - max x) on allowed j
  *
+ * Attention sinks (the "from_qwen_ops.rs" page, flat_softmax_rows_at, on
+ * `sinks`): when set, query head qh has one extra logit s_qh that joins its
+ * row's softmax and carries no value: the row maximum starts from s_qh and
+ * exp(s_qh - max) joins the denominator,
+ *   o            = sum_j w_j V_j / (sum_j w_j + exp(s_qh - m)),
+ *   m            = max(s_qh, max x),  w_j = exp(x_j - m).
+ * The sink is a logit of the softmax as it stands: it is neither scaled by
+ * sm_scale nor soft-capped (those act on the q.k products).
+ *
  * Readings where the page is silent or literal-but-quirky (kept in one place):
  *  - masked keys get weight exactly 0 (the page adds mask_value, whose exp
  *    underflows to 0 whenever a row has an allowed key);
@@ -52,6 +61,8 @@ typedef struct {
     int32_t has_sliding_window;
     double v_scale;
     int64_t sliding_window;
+    int32_t has_sinks;
+    const double* sinks; /* [num_q_heads] sink logits when has_sinks */
 } OracleCfg;
 
 enum { OR_OK = 0, OR_INVALID_ARG = 1, OR_BAD_PAGE_INDEX = 4, OR_BAD_LENGTHS = 5 };
@@ -137,6 +148,8 @@ static void one_row(const OracleCfg* c, const uint16_t* q, const void* kv, const
     for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
     double xmax = -INFINITY;
     int any = 0;
+    /* a sink logit starts the row maximum */
+    if (c->has_sinks) xmax = c->sinks[qh];
     for (int64_t j = 0; j < kv_len; ++j) {
         if (!key_allowed(c, kv_len, p, j)) continue;
         int64_t page = page_indices[(int64_t)s * c->pages_per_seq + j / c->page_size];
@@ -147,11 +160,13 @@ static void one_row(const OracleCfg* c, const uint16_t* q, const void* kv, const
         double xj = c->sm_scale * dot;
         if (c->has_soft_cap) xj = c->soft_cap * tanh(xj / c->soft_cap);
         x[j] = xj;
-        if (!any || xj > xmax) xmax = xj;
+        if (xj > xmax) xmax = xj;
         any = 1;
     }
-    if (!any) return; /* no allowed key: row is 0 */
+    if (!any) return; /* no allowed key: row is 0 (with a sink too: its term carries no value) */
     double denom = 0.0;
+    /* the sink's term joins the denominator and takes no value */
+    if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);
     for (int64_t j = 0; j < kv_len; ++j) {
         if (!key_allowed(c, kv_len, p, j)) continue;
         double w = exp(x[j] - xmax);

@@ -25,6 +25,8 @@ Recipe (fixed, so every run sees the same bytes):
    Every element of ``kv_pages`` is drawn, tail slots and unused pages too.
 4. Values are N(0, 1) in float32, rounded to bf16 with round-to-nearest-even.
    fp8 K/V values are ``clip(N(0,1) / 0.05, -448, 448)`` rounded to e4m3fn.
+5. Attention sinks, when asked for, are one float32 logit per query head drawn
+   as N(0, 2^2) from ``default_rng([seed, 3])``.
 """
 
 from __future__ import annotations
@@ -60,6 +62,7 @@ class Problem:
     is_causal: bool = True
     sliding_window: int | None = None
     mask_value: float = MASK_VALUE
+    sinks: np.ndarray | None = field(default=None, repr=False)  # float32 [num_q_heads] sink logits
     num_seqs: int = 0
     q: np.ndarray = field(default=None, repr=False)
     kv_pages: np.ndarray = field(default=None, repr=False)
@@ -77,7 +80,7 @@ class Problem:
             kv_dtype=self.kv_dtype, sm_scale=self.sm_scale,
             soft_cap=self.soft_cap, k_scale=self.k_scale, v_scale=self.v_scale,
             is_causal=self.is_causal, sliding_window=self.sliding_window,
-            mask_value=self.mask_value)
+            mask_value=self.mask_value, sinks=self.sinks)
 
     @property
     def q_lens(self) -> np.ndarray:
@@ -143,9 +146,12 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
           sm_scale: float | None = None, soft_cap=None, k_scale=None,
           v_scale=None, is_causal: bool = True, sliding_window=None,
           max_num_seqs: int | None = None, extra_tokens: int = 0,
-          extra_pages: int = 0, name: str = "custom",
+          extra_pages: int = 0, name: str = "custom", sinks=None,
           rng_lengths: np.random.Generator | None = None) -> Problem:
-    """Build a problem with the given lengths (already drawn by the caller)."""
+    """Build a problem with the given lengths (already drawn by the caller).
+
+    ``sinks``: None (no attention sinks), True (drawn, recipe step 5) or an
+    array of num_q_heads logits."""
     q_lens = np.asarray(q_lens, dtype=np.int64)
     kv_lens_a = np.asarray(kv_lens, dtype=np.int64)
     S = len(q_lens)
@@ -185,13 +191,17 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
 
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
+    if sinks is True:
+        sinks = (np.random.default_rng([seed, 3]).standard_normal(Hq) * 2.0).astype(np.float32)
+    elif sinks is not None:
+        sinks = np.ascontiguousarray(sinks, dtype=np.float32).reshape(Hq)
     return Problem(
         num_q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
         total_num_pages=total_num_pages, page_size=page_size,
         max_num_seqs=max_num_seqs, pages_per_seq=pages_per_seq,
         kv_dtype=kv_dtype, sm_scale=float(sm_scale), soft_cap=soft_cap,
         k_scale=k_scale, v_scale=v_scale, is_causal=is_causal,
-        sliding_window=sliding_window, num_seqs=S, q=q, kv_pages=kv,
+        sliding_window=sliding_window, sinks=sinks, num_seqs=S, q=q, kv_pages=kv,
         kv_lens=kvl, page_indices=page_indices, cu_q_lens=cu, name=name)
 
 

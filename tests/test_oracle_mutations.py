@@ -3,6 +3,7 @@
 denominator, the fp8 decoder), compile it, and check that the pins of test_oracle_pins.py catch
 it.  The mistakes are planted in a temporary copy on the CPU; the oracle itself is untouched."""
 import ctypes
+import math
 import os
 import subprocess
 
@@ -30,6 +31,11 @@ MUTATIONS = [
     ("slot off by one", "int64_t slot = j % c->page_size;", "int64_t slot = (j + 1) % c->page_size;"),
     ("e4m3 subnormal scale", "v = ldexp((double)m / 8.0, 1 - 7); /* subnormal */", "v = ldexp((double)m / 8.0, -7);"),
     ("e4m3 exponent bias", "v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("sink left out of the denominator", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);", ""),
+    ("sink of the wrong head", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);",
+     "if (c->has_sinks) denom += exp(c->sinks[qh / G] - xmax);"),
+    ("sink with the wrong sign", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);",
+     "if (c->has_sinks) denom += exp(-c->sinks[qh] - xmax);"),
 ]
 
 
@@ -40,6 +46,8 @@ def _pin_calls():
     calls += [lambda s=s: pins.test_oracle_random_configs_equal_brute_force(s) for s in range(24)]
     calls += [lambda a=a, w=w: pins.test_zero_query_averages_the_allowed_keys(a, w)
               for a, w in [(True, None), (True, 3), (True, 7), (False, None), (False, 4)]]
+    calls += [lambda v=v: pins.test_zero_query_mean_shrunk_by_a_sink(v) for v in (0.0, math.log(3.0), -2.5)]
+    calls += [pins.test_very_negative_sink_changes_nothing]
     calls += [pins.test_two_keys_closed_form_weights, pins.test_window_one_selects_own_position,
               pins.test_uniform_v_gives_v, pins.test_single_key_sequence,
               pins.test_decode_equals_last_prefill_row, pins.test_gqa_equals_mha_with_repeated_kv,

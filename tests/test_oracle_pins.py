@@ -7,7 +7,11 @@ mis-decoded fp8 code) fails at least one of them:
 * format decoders against numpy / torch casts and the formats' fixed points;
 * brute-force dense attention in numpy (explicit mask matrix, softmax over a
   dense score matrix) on tiny unpaged inputs scattered into shuffled pages;
-* closed forms: uniform V, a single allowed key, one-key sequences;
+* closed forms: uniform V, a single allowed key, one-key sequences, zero-query
+  means, two-key weights, zero-query means shrunk by a sink (n / (n + e^s));
+* attention sinks (the "from_qwen_ops.rs" page, flat_softmax_rows_at): the
+  brute force takes the sink as one more always-allowed column with a zero
+  value row; a very negative sink changes nothing;
 * the softcap identity c*tanh(x/c) = 2c*sigmoid(2x/c) - c of the
   "from_qwen_ops.rs" page (``capped``) used as an independent formula;
 * invariants: page placement, decode = last prefill row, poisoned tails,
@@ -52,6 +56,8 @@ def dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, kv_dtype="bf16", **knobs
         kv = ri.f32_to_e4m3_bits(x)
         dec = lambda b: torch.from_numpy(b).view(torch.float8_e4m3fn).float().numpy()
     cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    if knobs.get("sinks") is not None:
+        knobs["sinks"] = np.asarray(knobs["sinks"], np.float32)
     prob = Problem(num_q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                    total_num_pages=N, page_size=ps, max_num_seqs=S, pages_per_seq=P,
                    kv_dtype=kv_dtype, num_seqs=S, q=q, kv_pages=kv,
@@ -96,11 +102,22 @@ def brute(prob, dense, capped_form=False):
                 else:
                     x = c * np.tanh(x / c)
             x = np.where(allowed, x, -np.inf)
+            Vh = V[:, h, :] * vs
+            if prob.sinks is not None:
+                # the sink as one more column of the score matrix, always allowed, whose value
+                # row is zero
+                x = np.concatenate([x, np.full((ql, 1), float(prob.sinks[qh]))], axis=1)
+                allowed_s = np.concatenate([allowed, np.ones((ql, 1), bool)], axis=1)
+                Vh = np.concatenate([Vh, np.zeros((1, Vh.shape[1]))], axis=0)
+            else:
+                allowed_s = allowed
             m = x.max(axis=1, keepdims=True)
             has = np.isfinite(m)
-            w = np.where(allowed, np.exp(x - np.where(has, m, 0.0)), 0.0)
+            w = np.where(allowed_s, np.exp(x - np.where(has, m, 0.0)), 0.0)
             den = w.sum(axis=1, keepdims=True)
-            o = (w @ (V[:, h, :] * vs)) / np.where(den > 0, den, 1.0)
+            o = (w @ Vh) / np.where(den > 0, den, 1.0)
+            # a row with no allowed key is zero (with a sink too: the sink carries no value)
+            o[~allowed.any(axis=1)] = 0.0
             out[q0:q0 + ql, qh, :] = o
     return out
 
@@ -145,6 +162,12 @@ CASES = [
          sliding_window=3),
     dict(q_lens=[3, 8], kv_lens=[40, 21], Hq=4, Hkv=2, D=32, ps=8, kv_dtype="fp8_e4m3",
          k_scale=0.05, v_scale=0.07, soft_cap=5.0, sliding_window=9, sm_scale=0.125),
+    # attention sinks: plain, with soft cap and window, and sinks far above / below the logits
+    dict(q_lens=[1, 5, 16], kv_lens=[17, 40, 64], Hq=4, Hkv=2, D=64, ps=16,
+         sinks=[0.5, -1.0, 2.0, 0.0]),
+    dict(q_lens=[6, 2], kv_lens=[20, 33], Hq=8, Hkv=2, D=16, ps=8, sliding_window=5, soft_cap=2.0,
+         sinks=[3.0, -3.0, 0.1, 1.7, -0.4, 5.0, 0.0, 1.0]),
+    dict(q_lens=[4, 4], kv_lens=[11, 4], Hq=2, Hkv=1, D=16, ps=4, is_causal=False, sinks=[40.0, -40.0]),
 ]
 
 
@@ -176,6 +199,8 @@ def test_oracle_random_configs_equal_brute_force(seed):
         kw["soft_cap"] = float(rng.uniform(0.5, 30.0))
     if rng.integers(0, 2):
         kw.update(kv_dtype="fp8_e4m3", k_scale=float(rng.uniform(0.01, 0.1)), v_scale=float(rng.uniform(0.01, 0.1)))
+    if rng.integers(0, 2):
+        kw["sinks"] = (rng.standard_normal(Hq) * 2).astype(np.float32)
     prob, dense = dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, **kw)
     close(oracle.forward(prob), brute(prob, dense))
 
@@ -251,6 +276,40 @@ def test_zero_query_averages_the_allowed_keys(causal, window):
             want = V[lo:hi + 1, 0].mean(axis=0)
             for qh in range(2):
                 close(o[prob.cu_q_lens[s] + i, qh], want, 1e-13)
+
+
+@pytest.mark.parametrize("sink", [0.0, math.log(3.0), -2.5])
+def test_zero_query_mean_shrunk_by_a_sink(sink):
+    """q = 0 makes every allowed logit 0, so each allowed key weighs 1 and the sink e^s: o is the
+    mean of V over the n allowed keys times n / (n + e^s) (s = ln 3: n / (n + 3))."""
+    rng = np.random.default_rng(14)
+    Hq = 2
+    prob, dense = dense_problem(rng, [5, 2], [12, 9], Hq, 1, 16, 4, sliding_window=4,
+                                sinks=[sink, 0.0])
+    prob.q = np.zeros_like(prob.q)
+    o = oracle.forward(prob)
+    for s, (Q, K, V) in enumerate(dense):
+        ql, kl = Q.shape[0], K.shape[0]
+        for i in range(ql):
+            p = kl - ql + i
+            lo = max(0, p - 4 + 1)
+            n = p - lo + 1
+            mean = V[lo:p + 1, 0].mean(axis=0)
+            # the sink is stored as fp32: the closed form takes that value
+            for qh, sv in ((0, float(np.float32(sink))), (1, 0.0)):
+                close(o[prob.cu_q_lens[s] + i, qh], mean * n / (n + math.exp(sv)), 1e-13)
+
+
+def test_very_negative_sink_changes_nothing():
+    """A sink far below every logit has weight exp(-1e30) = 0 and does not move the maximum: the
+    output equals the one without sinks, bit for bit."""
+    prob = ri.random_small(28, num_seqs=4, max_q=9, max_kv=60, num_q_heads=4, num_kv_heads=2,
+                           head_dim=32, page_size=8, soft_cap=10.0, sliding_window=20)
+    o1 = oracle.forward(prob)
+    prob.sinks = np.full(4, -1e30, np.float32)
+    assert np.array_equal(o1, oracle.forward(prob))
+    prob.sinks = np.zeros(4, np.float32)
+    assert not np.array_equal(o1, oracle.forward(prob))
 
 
 def test_two_keys_closed_form_weights():

@@ -398,7 +398,10 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
         "step_roofline_frac": t_star / (ms_step * 1e-3),
         "step_roofline_bound": "hbm" if work["bytes"] / (hbm * 1e9) >= work["flops"] / (tf_burst * 1e12) else "tensor",
         "kernel_rooflines": kroofs,
-        "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k)},
+        # an attention kernel with no work is launched all the same; its event span is its wait for
+        # SMs (the other kernel may hold them all), not work, so it is listed as idle instead
+        "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k) if has_work.get(n, True)},
+        "idle_kernels": [n for n in KERNEL_NAMES if not has_work.get(n, True)],
         "roofline": roof, "gpu_launches": 4 * K, "clocks": clk,
     }
 
@@ -463,8 +466,8 @@ def main():
             r, _ = measure(name, min(k, max(1, args.steps)), args.warmup, dist, dev, world)
             side[name] = {key: r[key] for key in ("value", "unit", "ms_per_step", "steps", "dtype", "config",
                                                   "step_roofline_frac", "step_roofline_bound", "step_hbm_gbs",
-                                                  "step_tflops", "kernel_rooflines", "kernels_ms", "roofline",
-                                                  "clocks")}
+                                                  "step_tflops", "kernel_rooflines", "kernels_ms", "idle_kernels",
+                                                  "roofline", "clocks")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -479,6 +482,7 @@ def main():
             "step_hbm_gbs": res["step_hbm_gbs"], "step_tflops": res["step_tflops"],
             "step_roofline_frac": res["step_roofline_frac"],
             "kernel_rooflines": res["kernel_rooflines"], "kernels_ms": res["kernels_ms"],
+            "idle_kernels": res["idle_kernels"],
             "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res.get("e2e"),
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
         }

@@ -80,8 +80,23 @@ typedef struct RpaCfg {
     int32_t has_v_scale;
     int32_t is_causal;       /* 1 = causal (default of the page) */
     int32_t has_sliding_window;
+    int32_t has_sinks;       /* 1: attention sinks, read from `sinks` */
+    int32_t kv_layout;       /* RpaKvLayout: RPA_KV_SPLIT (the page's layout, default) */
     int32_t reserved;        /* set to 0 */
+    int64_t v_head_dim;      /* 0 (V rows are head_dim wide, the page's layout) */
+    const float* sinks;      /* when has_sinks: device, [num_q_heads] fp32, 4-byte aligned; the
+                                sink logit of each query head (the "from_qwen_ops.rs" page,
+                                flat_softmax_rows_at, `sinks`): it starts the row maximum and
+                                exp(sink - max) joins the softmax denominator, carrying no
+                                value.  It is a logit of the softmax as it stands (not scaled by
+                                sm_scale, not soft-capped).  Read by every call on the handle
+                                (or by the rpa_forward_noalloc call given this cfg): it must
+                                stay valid while those calls run. */
 } RpaCfg;
+
+/* K/V page layouts.  RPA_KV_SPLIT: kv_pages[total_num_pages, page_size,
+ * 2*Hkv, D], combined head 2h = K of kv head h, 2h+1 = V (the page's). */
+typedef enum RpaKvLayout { RPA_KV_SPLIT = 0 } RpaKvLayout;
 
 typedef struct RpaHandle RpaHandle;
 

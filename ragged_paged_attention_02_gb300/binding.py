@@ -51,7 +51,9 @@ class RpaCfg(ctypes.Structure):
         ("soft_cap", ctypes.c_float), ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float),
         ("has_soft_cap", ctypes.c_int32), ("has_k_scale", ctypes.c_int32),
         ("has_v_scale", ctypes.c_int32), ("is_causal", ctypes.c_int32),
-        ("has_sliding_window", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("has_sliding_window", ctypes.c_int32), ("has_sinks", ctypes.c_int32),
+        ("kv_layout", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("v_head_dim", ctypes.c_int64), ("sinks", ctypes.c_void_p),
     ]
 
 
@@ -110,10 +112,28 @@ def lib():
     return _lib
 
 
+def _sinks_pointer(sinks, host_ok):
+    """Device address of a float32 [Hq] sink tensor (a torch CUDA tensor, or an int address).
+    A host (numpy) array is taken only where nothing is dereferenced (host-side validation)."""
+    if sinks is None:
+        return None
+    if isinstance(sinks, int):
+        return sinks
+    if isinstance(sinks, np.ndarray):
+        if not host_ok:
+            raise ValueError("sinks must be a CUDA float32 tensor (RaggedPagedAttention converts numpy arrays)")
+        return sinks.ctypes.data
+    import torch
+
+    if not (sinks.is_cuda and sinks.dtype == torch.float32 and sinks.is_contiguous()):
+        raise ValueError("sinks must be a contiguous CUDA float32 tensor [num_q_heads]")
+    return sinks.data_ptr()
+
+
 def make_cfg(*, num_q_tokens, num_q_heads, num_kv_heads, head_dim, total_num_pages, page_size,
              max_num_seqs, pages_per_seq, sm_scale, kv_dtype="bf16", soft_cap=None, k_scale=None,
-             v_scale=None, is_causal=True, sliding_window=None, mask_value=MASK_VALUE,
-             **_ignored) -> RpaCfg:
+             v_scale=None, is_causal=True, sliding_window=None, mask_value=MASK_VALUE, sinks=None,
+             _host_ok=False, **_ignored) -> RpaCfg:
     c = RpaCfg()
     c.num_q_tokens, c.num_q_heads, c.num_kv_heads = int(num_q_tokens), int(num_q_heads), int(num_kv_heads)
     c.head_dim, c.total_num_pages, c.page_size = int(head_dim), int(total_num_pages), int(page_size)
@@ -127,12 +147,14 @@ def make_cfg(*, num_q_tokens, num_q_heads, num_kv_heads, head_dim, total_num_pag
     c.has_v_scale, c.v_scale = (0, 1.0) if v_scale is None else (1, float(v_scale))
     c.is_causal = 1 if is_causal else 0
     c.has_sliding_window, c.sliding_window = (0, 0) if sliding_window is None else (1, int(sliding_window))
+    ptr = _sinks_pointer(sinks, _host_ok)
+    c.has_sinks, c.sinks = (0, None) if ptr is None else (1, ptr)
     return c
 
 
 def validate_cfg(**cfg) -> int:
     """Host-only configuration check (no CUDA call): returns the status code."""
-    c = make_cfg(**cfg)
+    c = make_cfg(_host_ok=True, **cfg)
     return int(lib().rpa_validate_cfg(ctypes.byref(c)))
 
 
@@ -154,11 +176,19 @@ class RaggedPagedAttention:
       kv_lens      [max_num_seqs] int32
       page_indices [max_num_seqs, pages_per_seq] int32
       cu_q_lens    [max_num_seqs + 1] int32
-    and returns o [num_q_tokens, Hq, D] bfloat16.
+    and returns o [num_q_tokens, Hq, D] bfloat16.  ``sinks`` (optional) is a
+    float32 [Hq] array or CUDA tensor of attention-sink logits.
     """
 
     def __init__(self, **cfg):
         self.cfg = dict(cfg)
+        sinks = cfg.get("sinks")
+        if isinstance(sinks, np.ndarray):
+            import torch
+
+            # the library reads the sinks on the device at every call: keep them there, alive
+            cfg["sinks"] = torch.from_numpy(np.ascontiguousarray(sinks, np.float32)).cuda()
+        self._sinks = cfg.get("sinks")
         self._c = make_cfg(**cfg)
         h = ctypes.c_void_p()
         r = lib().rpa_create(ctypes.byref(self._c), ctypes.byref(h))

@@ -315,7 +315,8 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
                 const int t = q_start + item.tok0 + r / G;
                 const int qh = h * G + r % G;
                 if (item.part < 0) {
-                    const float inv = l_r[ri] > 0.f ? p.v_scale / l_r[ri] : 0.f;
+                    const float l = add_sink(l_r[ri], p.sinks, qh, m_r[ri]);
+                    const float inv = l > 0.f ? p.v_scale / l : 0.f;
                     uint32_t* orow = reinterpret_cast<uint32_t*>(p.o + ((size_t)t * Hq + qh) * (D * 2));
 #pragma unroll
                     for (int nd = 0; nd < D / 8; ++nd)
@@ -368,7 +369,8 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
                 const int t = q_start + item.tok0 + r / G;
                 const int qh = h * G + r % G;
                 if (item.part < 0) {
-                    const float inv = L > 0.f ? p.v_scale / L : 0.f;
+                    const float Ls = add_sink(L, p.sinks, qh, M);
+                    const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;
                     *reinterpret_cast<uint32_t*>(p.o + (((size_t)t * Hq + qh) * D + c) * 2) =
                         pack2<false>(o0 * inv, o1 * inv);
                 } else {

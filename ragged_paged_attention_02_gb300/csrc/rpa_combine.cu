@@ -8,6 +8,9 @@
 //
 //   M = max_i m_i,   L = sum_i 2^{m_i - M} l_i,   o = v_scale * sum_i 2^{m_i - M} O_i / L
 //
+// With attention sinks the row's sink term 2^{s log2(e) - M} joins L here, once: the pieces
+// leave it out.
+//
 // Work goes out in units of a few rows of one entry (one group of four columns per thread).  An
 // entry of at most four pieces merges in registers; longer ones first reduce each row's m and l
 // (a warp per row) into shared-memory scale factors.  Entries hold at most `rows_max` rows (the
@@ -79,9 +82,10 @@ __global__ void __launch_bounds__(kCombThreads, 2) rpa_combine_kernel(const Comb
                         }
                     }
                 }
-                const float inv = L > 0.f ? p.v_scale / L : 0.f;
                 const int t = q0 + r / G;
                 const int qh = c.head * G + r % G;
+                L = add_sink(L, p.sinks, qh, M);  // the sink joins once, over all pieces
+                const float inv = L > 0.f ? p.v_scale / L : 0.f;
                 uint2 w;
                 w.x = pack2<false>(acc.x * inv, acc.y * inv);
                 w.y = pack2<false>(acc.z * inv, acc.w * inv);
@@ -107,6 +111,7 @@ __global__ void __launch_bounds__(kCombThreads, 2) rpa_combine_kernel(const Comb
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
             if (lane == 0) {
+                L = add_sink(L, p.sinks, c.head * G + r % G, M);  // the sink joins once, over all pieces
                 s_M[r] = M;
                 s_inv[r] = L > 0.f ? p.v_scale / L : 0.f;
             }

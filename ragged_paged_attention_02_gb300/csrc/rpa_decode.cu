@@ -512,9 +512,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     }
                 }
                 if (part < 0) {
-                    const float inv = L > 0.f ? a.v_scale / L : 0.f;
                     const int t = q_start + tok0 + r / G;
                     const int qh = head * G + r % G;
+                    L = add_sink(L, a.sinks, qh, M);
+                    const float inv = L > 0.f ? a.v_scale / L : 0.f;
                     *reinterpret_cast<uint32_t*>(a.o + (((size_t)t * Hq + qh) * D + c) * 2) =
                         pack2<false>(o0 * inv, o1 * inv);
                 } else {
@@ -764,9 +765,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     }
                 }
                 if (part < 0) {
-                    const float inv = L > 0.f ? a.v_scale / L : 0.f;
                     const int t = q_start + tok0 + r / G;
                     const int qh = head * G + r % G;
+                    L = add_sink(L, a.sinks, qh, M);
+                    const float inv = L > 0.f ? a.v_scale / L : 0.f;
                     *reinterpret_cast<uint32_t*>(a.o + (((size_t)t * Hq + qh) * D + c) * 2) =
                         pack2<false>(o0 * inv, o1 * inv);
                 } else {

@@ -170,6 +170,9 @@ int rpa_validate_cfg(const RpaCfg* c) {
     if (c->has_k_scale && !is_finite(c->k_scale)) return RPA_ERR_INVALID_ARG;
     if (c->has_v_scale && !is_finite(c->v_scale)) return RPA_ERR_INVALID_ARG;
     if (c->has_sliding_window && c->sliding_window < 1) return RPA_ERR_INVALID_ARG;
+    if (c->has_sinks && (!c->sinks || !aligned(c->sinks, 4))) return RPA_ERR_INVALID_ARG;
+    if (c->reserved != 0) return RPA_ERR_INVALID_ARG;
+    if (c->kv_layout != RPA_KV_SPLIT || c->v_head_dim != 0) return RPA_ERR_UNSUPPORTED;
     if (c->num_q_heads % c->num_kv_heads) return RPA_ERR_UNSUPPORTED;
     if (c->num_q_heads / c->num_kv_heads > kPfRows) return RPA_ERR_UNSUPPORTED;
     if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return RPA_ERR_UNSUPPORTED;
@@ -381,6 +384,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     ap.ctrl = h->ctrl;
     ap.part_o = h->part_o;
     ap.part_ml = h->part_ml;
+    ap.sinks = c.has_sinks ? c.sinks : nullptr;
 
     // With concurrent decode / prefill the decode kernel runs on the side stream, forked from st
     // after the planner.  Once forked, every return joins it back (st waits for whatever was
@@ -476,6 +480,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     cp.D = h->D;
     cp.rows_max = h->dec_rows;
     cp.v_scale = h->v_scale;
+    cp.sinks = c.has_sinks ? c.sinks : nullptr;
     cp.ctrl = h->ctrl;
     cp.comb = h->comb;
     cp.part_o = h->part_o;

@@ -115,6 +115,7 @@ struct AttnParams {
     int counter_word;      // ctrl index of the work counter
     float* part_o;         // [max_part, kDecRows, D]
     float* part_ml;        // [max_part, kDecRows, 2]
+    const float* sinks;    // [Hq] sink logits (natural-log domain), or nullptr
 };
 
 struct DecParams {
@@ -139,6 +140,7 @@ struct CombParams {
     int num_seqs, T, Hq, G, D;
     int rows_max;  // most rows of a combine entry (the decode tile's rows)
     float v_scale;
+    const float* sinks;  // [Hq] sink logits (natural-log domain), or nullptr
     const int* ctrl;
     const Comb* comb;
     const float* part_o;
@@ -247,6 +249,16 @@ __device__ __forceinline__ float rcp_approx(float x) {
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
     return y;
+}
+
+// The softmax denominator of a row whose logits (log2 domain) are relative to `base`, with the
+// row's attention sink added: l + 2^(sink log2(e) - base).  The sink starts the row's maximum in
+// the definition; any other common base gives the same quotient, and a sink far above the base
+// makes the denominator infinite and the row zero, its limit.  A row with no allowed key
+// (base -inf) stays zero: its O is zero whatever the denominator.
+__device__ __forceinline__ float add_sink(float l, const float* sinks, int qh, float base) {
+    if (sinks == nullptr || base == -INFINITY) return l;
+    return l + ex2(__ldg(sinks + qh) * 1.4426950408889634f - base);
 }
 
 // tanh(x) on the special-function unit (hardware approximation, relative error about 2^-11).

@@ -222,6 +222,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     ap.ctrl = ctrl;
     ap.part_o = part_o;
     ap.part_ml = part_ml;
+    ap.sinks = c.has_sinks ? c.sinks : nullptr;
     if (c.num_q_tokens > 0) {
         int BR = 64, br_shift = 0;
         while ((int)(c.page_size % BR)) BR >>= 1;
@@ -277,6 +278,7 @@ extern "C" int rpa_forward_noalloc(const RpaCfg* cfg, const void* q, const void*
     cp.D = D;
     cp.rows_max = dec_rows;
     cp.v_scale = ap.v_scale;
+    cp.sinks = ap.sinks;
     cp.ctrl = ctrl;
     cp.comb = comb;
     cp.part_o = part_o;

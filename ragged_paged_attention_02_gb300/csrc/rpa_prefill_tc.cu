@@ -531,9 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
             if (!mbar_wait(smem_u32(&o_full), items & 1u, ctrl, tmo)) break;
             tc_fence_after();
             const int rows_used = ntx * G;
-            const float inv = l_run > 0.f ? a.v_scale / l_run : 0.f;
             const int t_tok = q_start + ttok0 + r / G;
             const int qh = head * G + r % G;
+            const float l_fin = add_sink(l_run, a.sinks, qh, m_run);  // P was taken relative to m_run
+            const float inv = l_fin > 0.f ? a.v_scale / l_fin : 0.f;
             uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2);
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {

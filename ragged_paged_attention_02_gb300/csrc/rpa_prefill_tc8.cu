@@ -749,9 +749,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 ++items;
                 continue;
             }
-            const float inv = l_row > 0.f ? a.v_scale / l_row : 0.f;
             const int t_tok = q_start + tok0 + r / G;
             const int qh = head * G + r % G;
+            const float l_fin = add_sink(l_row, a.sinks, qh, m_run);  // P was taken relative to m_run
+            const float inv = l_fin > 0.f ? a.v_scale / l_fin : 0.f;
             uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2) + half * HO * 2;
 #pragma unroll 1
             for (int cc = 0; cc < HO / 32; ++cc) {

@@ -94,6 +94,19 @@ SMALL = [
               kv_dtype="fp8_e4m3", k_scale=0.07, v_scale=0.05, is_causal=False)),
     (75, dict(num_seqs=8, decode_only=True, max_kv=6000, num_q_heads=32, num_kv_heads=2, head_dim=256,
               page_size=16, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
+    # attention sinks on every kernel: 8-row decode tiles and the bf16 tensor-memory prefill; 16-row
+    # decode tiles with split pieces (the combine kernel adds the sink once); the fp8 tensor-memory
+    # kernel with split pieces, soft cap and window; the warp-MMA prefill (bf16 D 256, fp8 D 64)
+    (76, dict(num_seqs=10, max_q=200, max_kv=2500, num_q_heads=16, num_kv_heads=4, head_dim=128, sinks=True)),
+    (77, dict(num_seqs=8, max_q=2, max_kv=5000, num_q_heads=32, num_kv_heads=2, head_dim=128, sinks=True)),
+    (78, dict(num_seqs=12, max_q=40, max_kv=5000, num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0, sliding_window=1500,
+              sm_scale=1 / 16, sinks=True)),
+    (79, dict(num_seqs=5, max_q=70, max_kv=900, num_q_heads=8, num_kv_heads=2, head_dim=256, sinks=True)),
+    (80, dict(num_seqs=8, max_q=30, max_kv=3000, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, sinks=True)),
+    (81, dict(num_seqs=16, decode_only=True, max_kv=8000, num_q_heads=32, num_kv_heads=8, head_dim=128,
+              sinks=True)),
 ]
 
 

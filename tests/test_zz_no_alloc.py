@@ -34,7 +34,10 @@ def _built():
 def _noalloc(prob, t, out):
     import ragged_paged_attention_02_gb300 as rpa
 
-    c = rpa.make_cfg(**prob.cfg_dict())
+    cfg = prob.cfg_dict()
+    if cfg.get("sinks") is not None:
+        cfg["sinks"] = torch.from_numpy(cfg["sinks"]).cuda()  # kept alive in cfg until the call returns
+    c = rpa.make_cfg(**cfg)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     q, kv, kvl, pi, cu = t
     return rpa.lib().rpa_forward_noalloc(ctypes.byref(c), q.data_ptr(), kv.data_ptr(), kvl.data_ptr(),
@@ -56,6 +59,9 @@ CASES = {
                            soft_cap=30.0, sm_scale=1 / 16)),
     # bf16 with G = 16: 16-row decode tiles beside the bf16 tensor-memory prefill
     "bf16_g16": (63, dict(num_seqs=10, max_q=30, max_kv=3000, num_q_heads=32, num_kv_heads=2, head_dim=128)),
+    # attention sinks read through the cfg's device pointer
+    "sinks": (64, dict(num_seqs=9, max_q=60, max_kv=4000, num_q_heads=16, num_kv_heads=4, head_dim=128,
+                       sinks=True)),
 }
 
 

@@ -49,14 +49,19 @@ class OracleCfg(ctypes.Structure):
         ("num_kv_heads", ctypes.c_int64), ("head_dim", ctypes.c_int64),
         ("total_num_pages", ctypes.c_int64), ("page_size", ctypes.c_int64),
         ("max_num_seqs", ctypes.c_int64), ("pages_per_seq", ctypes.c_int64),
-        ("kv_is_fp8", ctypes.c_int32), ("is_causal", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32), ("is_causal", ctypes.c_int32),
         ("sm_scale", ctypes.c_double),
         ("has_soft_cap", ctypes.c_int32), ("has_k_scale", ctypes.c_int32),
         ("soft_cap", ctypes.c_double), ("k_scale", ctypes.c_double),
         ("has_v_scale", ctypes.c_int32), ("has_sliding_window", ctypes.c_int32),
         ("v_scale", ctypes.c_double), ("sliding_window", ctypes.c_int64),
         ("has_sinks", ctypes.c_int32), ("sinks", ctypes.c_void_p),
+        ("q_dtype", ctypes.c_int32),
     ]
+
+# the oracle's own type codes (rpa_oracle.c: OracleKv, OracleQ)
+KV_CODES = {"bf16": 0, "fp8_e4m3": 1, "f16": 2, "fp8_e5m2": 3, "int8": 4}
+Q_CODES = {"bf16": 0, "f16": 1, "f32": 2}
 
 
 def build(force: bool = False) -> str:
@@ -87,6 +92,10 @@ def _load():
         lib.oracle_bf16_to_f64.restype = ctypes.c_double
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+        lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e5m2_to_f64.restype = ctypes.c_double
+        lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f64.restype = ctypes.c_double
         _lib = lib
     return _lib
 
@@ -96,7 +105,8 @@ def make_cfg(cfg: dict) -> OracleCfg:
     for k in ("num_q_tokens", "num_q_heads", "num_kv_heads", "head_dim", "total_num_pages",
               "page_size", "max_num_seqs", "pages_per_seq"):
         setattr(c, k, int(cfg[k]))
-    c.kv_is_fp8 = 1 if cfg.get("kv_dtype", "bf16") == "fp8_e4m3" else 0
+    c.kv_dtype = KV_CODES[cfg.get("kv_dtype", "bf16")]
+    c.q_dtype = Q_CODES[cfg.get("q_dtype", "bf16")]
     c.is_causal = 1 if cfg.get("is_causal", True) else 0
     c.sm_scale = float(cfg["sm_scale"])
     for name in ("soft_cap", "k_scale", "v_scale"):
@@ -118,7 +128,8 @@ def make_cfg(cfg: dict) -> OracleCfg:
 
 
 def _arrays(prob):
-    q = np.ascontiguousarray(prob.q, dtype=np.uint16)
+    q = np.ascontiguousarray(prob.q)
+    assert q.dtype == (np.float32 if getattr(prob, "q_dtype", "bf16") == "f32" else np.uint16)
     kv = np.ascontiguousarray(prob.kv_pages)
     kvl = np.ascontiguousarray(prob.kv_lens, dtype=np.int32)
     pi = np.ascontiguousarray(prob.page_indices, dtype=np.int32)
@@ -178,3 +189,11 @@ def decode_bf16(bits: int) -> float:
 
 def decode_e4m3(byte: int) -> float:
     return float(_load().oracle_e4m3_to_f64(int(byte)))
+
+
+def decode_e5m2(byte: int) -> float:
+    return float(_load().oracle_e5m2_to_f64(int(byte)))
+
+
+def decode_f16(bits: int) -> float:
+    return float(_load().oracle_f16_to_f64(int(bits)))

@@ -36,9 +36,21 @@
  *  - dequant is exact fp64 x*scale (the page rounds it to the q dtype);
  *  - tokens not covered by [cu_q_lens[0], cu_q_lens[num_seqs]) are 0.
  *
- * Decoders follow the formats' definitions: bf16 is the top half of an IEEE
- * binary32; e4m3fn has bias 7, 3 mantissa bits, subnormals, no infinities,
- * S.1111.111 = NaN, max 448.
+ * Element types ("ragged_paged.zig", Cfg: q_dtype f32 / f16 / bf16; kv_dtype
+ * bf16 / f16 / f8e4m3fn / f8e5m2 / i8).  Every stored value is decoded exactly
+ * to fp64 from its format's definition and used as it is: the page's casts to
+ * the q dtype before its matmuls are not reproduced (the oracle is the exact
+ * definition; the GPU's operand rounding is within the tolerance).
+ *  - f32: IEEE-754 binary32;
+ *  - bf16: the upper half of an IEEE binary32;
+ *  - f16: IEEE-754 binary16: 1 sign, 5 exponent bits (bias 15), 10 mantissa
+ *    bits, subnormals, infinities and NaN at exponent 31;
+ *  - e4m3fn (OCP FP8): bias 7, 3 mantissa bits, subnormals, no infinities,
+ *    S.1111.111 = NaN, max 448;
+ *  - e5m2 (OCP FP8): bias 15, 2 mantissa bits, subnormals, infinities and NaN
+ *    at exponent 31 (the upper byte of a binary16), max 57344;
+ *  - i8: two's-complement integers -128..127.
+ * The k_scale / v_scale dequant factors multiply the decoded K / V values.
  */
 #include <math.h>
 #include <pthread.h>
@@ -50,7 +62,7 @@
 typedef struct {
     int64_t num_q_tokens, num_q_heads, num_kv_heads, head_dim;
     int64_t total_num_pages, page_size, max_num_seqs, pages_per_seq;
-    int32_t kv_is_fp8; /* 0: bf16 K/V bits, 1: fp8 e4m3fn bytes */
+    int32_t kv_dtype; /* OracleKv: element type of kv_pages */
     int32_t is_causal;
     double sm_scale;
     int32_t has_soft_cap;
@@ -63,9 +75,12 @@ typedef struct {
     int64_t sliding_window;
     int32_t has_sinks;
     const double* sinks; /* [num_q_heads] sink logits when has_sinks */
+    int32_t q_dtype;     /* OracleQ: element type of q */
 } OracleCfg;
 
 enum { OR_OK = 0, OR_INVALID_ARG = 1, OR_BAD_PAGE_INDEX = 4, OR_BAD_LENGTHS = 5 };
+typedef enum { OKV_BF16 = 0, OKV_E4M3 = 1, OKV_F16 = 2, OKV_E5M2 = 3, OKV_I8 = 4 } OracleKv;
+typedef enum { OQ_BF16 = 0, OQ_F16 = 1, OQ_F32 = 2 } OracleQ;
 
 /* bf16: the 16 stored bits are the upper half of an IEEE-754 binary32. */
 double oracle_bf16_to_f64(uint16_t b) {
@@ -89,6 +104,37 @@ double oracle_e4m3_to_f64(uint8_t b) {
     return sign ? -v : v;
 }
 
+/* f16 (IEEE binary16): 1 sign, 5 exponent (bias 15), 10 mantissa bits. */
+double oracle_f16_to_f64(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int e = (b >> 10) & 0x1F;
+    int m = b & 0x3FF;
+    double v;
+    if (e == 0x1F) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m / 1024.0, 1 - 15); /* subnormal */
+    else v = ldexp(1.0 + (double)m / 1024.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* fp8 e5m2 (OCP FP8): 1 sign, 5 exponent (bias 15), 2 mantissa bits. */
+double oracle_e5m2_to_f64(uint8_t b) {
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1F;
+    int m = b & 0x3;
+    double v;
+    if (e == 0x1F) v = m ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)m / 4.0, 1 - 15); /* subnormal */
+    else v = ldexp(1.0 + (double)m / 4.0, e - 15);
+    return sign ? -v : v;
+}
+
+/* f32 (IEEE binary32) */
+static double f32_to_f64(const void* p) {
+    float f;
+    memcpy(&f, p, sizeof f);
+    return (double)f;
+}
+
 /* Mask of the page (flashAttention): a key is dropped when it is past the
  * sequence, when causal and j > p, or when p - sliding_window >= j. */
 static int key_allowed(const OracleCfg* c, int64_t kv_len, int64_t p, int64_t j) {
@@ -101,8 +147,21 @@ static int key_allowed(const OracleCfg* c, int64_t kv_len, int64_t p, int64_t j)
 static double kv_elem(const OracleCfg* c, const void* kv, int64_t page, int64_t slot,
                       int64_t comb_head, int64_t d) {
     int64_t idx = ((page * c->page_size + slot) * (2 * c->num_kv_heads) + comb_head) * c->head_dim + d;
-    if (c->kv_is_fp8) return oracle_e4m3_to_f64(((const uint8_t*)kv)[idx]);
-    return oracle_bf16_to_f64(((const uint16_t*)kv)[idx]);
+    switch (c->kv_dtype) {
+        case OKV_E4M3: return oracle_e4m3_to_f64(((const uint8_t*)kv)[idx]);
+        case OKV_E5M2: return oracle_e5m2_to_f64(((const uint8_t*)kv)[idx]);
+        case OKV_I8: return (double)((const int8_t*)kv)[idx];
+        case OKV_F16: return oracle_f16_to_f64(((const uint16_t*)kv)[idx]);
+        default: return oracle_bf16_to_f64(((const uint16_t*)kv)[idx]);
+    }
+}
+
+static double q_elem(const OracleCfg* c, const void* q, int64_t idx) {
+    switch (c->q_dtype) {
+        case OQ_F32: return f32_to_f64((const float*)q + idx);
+        case OQ_F16: return oracle_f16_to_f64(((const uint16_t*)q)[idx]);
+        default: return oracle_bf16_to_f64(((const uint16_t*)q)[idx]);
+    }
 }
 
 /* Lengths / page-table validity, stated as the preconditions of the method.
@@ -131,7 +190,7 @@ int rpa_oracle_validate(const OracleCfg* c, const int32_t* kv_lens, const int32_
 
 /* One output row: query token t (of sequence s, local index i), query head qh.
  * scratch holds kv_len doubles. */
-static void one_row(const OracleCfg* c, const uint16_t* q, const void* kv, const int32_t* kv_lens,
+static void one_row(const OracleCfg* c, const void* q, const void* kv, const int32_t* kv_lens,
                     const int32_t* page_indices, const int32_t* cu_q_lens, int32_t s, int64_t t,
                     int64_t qh, double* out, double* x) {
     const int64_t D = c->head_dim;
@@ -143,7 +202,7 @@ static void one_row(const OracleCfg* c, const uint16_t* q, const void* kv, const
     const int64_t p = kv_len - q_len + i;
     const double ks = c->has_k_scale ? c->k_scale : 1.0;
     const double vs = c->has_v_scale ? c->v_scale : 1.0;
-    const uint16_t* qrow = q + (t * c->num_q_heads + qh) * D;
+    const int64_t qrow = (t * c->num_q_heads + qh) * D; /* element offset of the query row */
 
     for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
     double xmax = -INFINITY;
@@ -156,7 +215,7 @@ static void one_row(const OracleCfg* c, const uint16_t* q, const void* kv, const
         int64_t slot = j % c->page_size;
         double dot = 0.0;
         for (int64_t d = 0; d < D; ++d)
-            dot += oracle_bf16_to_f64(qrow[d]) * (kv_elem(c, kv, page, slot, 2 * h, d) * ks);
+            dot += q_elem(c, q, qrow + d) * (kv_elem(c, kv, page, slot, 2 * h, d) * ks);
         double xj = c->sm_scale * dot;
         if (c->has_soft_cap) xj = c->soft_cap * tanh(xj / c->soft_cap);
         x[j] = xj;
@@ -187,7 +246,7 @@ static int32_t seq_of_token(const int32_t* cu_q_lens, int32_t num_seqs, int64_t 
 
 typedef struct {
     const OracleCfg* c;
-    const uint16_t* q;
+    const void* q;
     const void* kv;
     const int32_t* kv_lens;
     const int32_t* page_indices;
@@ -248,7 +307,7 @@ static int run_job(Job* jb, int nthreads) {
 
 /* All rows: out[num_q_tokens, num_q_heads, head_dim] in fp64.
  * Returns the number of threads used, or -code on invalid input. */
-int rpa_oracle_forward(const OracleCfg* c, const uint16_t* q, const void* kv_pages,
+int rpa_oracle_forward(const OracleCfg* c, const void* q, const void* kv_pages,
                        const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
                        int32_t num_seqs, double* out, int nthreads) {
     if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return -OR_INVALID_ARG;
@@ -260,7 +319,7 @@ int rpa_oracle_forward(const OracleCfg* c, const uint16_t* q, const void* kv_pag
 }
 
 /* Selected rows only: rows = nrows (token, q head) int64 pairs; out[nrows, head_dim]. */
-int rpa_oracle_rows(const OracleCfg* c, const uint16_t* q, const void* kv_pages, const int32_t* kv_lens,
+int rpa_oracle_rows(const OracleCfg* c, const void* q, const void* kv_pages, const int32_t* kv_lens,
                     const int32_t* page_indices, const int32_t* cu_q_lens, int32_t num_seqs,
                     const int64_t* rows, int64_t nrows, double* out, int nthreads) {
     if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return -OR_INVALID_ARG;

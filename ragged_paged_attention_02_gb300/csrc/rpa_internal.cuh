@@ -43,6 +43,14 @@ struct Comb {
     int seq, head, part, pieces;
 };
 
+// K/V element types inside the kernels (template arguments): 16-bit types feed the MMAs as they
+// are; 8-bit types are converted exactly to f16 first.
+enum KvType : int { KT_BF16 = 0, KT_F16 = 1, KT_E4M3 = 2, KT_E5M2 = 3, KT_I8 = 4 };
+__host__ __device__ constexpr bool kt_8bit(int kt) { return kt >= KT_E4M3; }
+__host__ __device__ constexpr bool kt_f16_mma(int kt) { return kt != KT_BF16; }  // MMA operands in f16
+// Output element types (o has the q dtype)
+enum OutType : int { OT_BF16 = 0, OT_F16 = 1, OT_F32 = 2 };
+
 constexpr int kDecRows = 16;       // rows of a decode tile (one m16 MMA tile)
 constexpr int kPfRows = 64;        // rows of a prefill tile (4 warps x 16)
 constexpr int kDecWaves = 4;       // target decode items per resident CTA
@@ -116,6 +124,8 @@ struct AttnParams {
     float* part_o;         // [max_part, kDecRows, D]
     float* part_ml;        // [max_part, kDecRows, 2]
     const float* sinks;    // [Hq] sink logits (natural-log domain), or nullptr
+    int odt;               // OutType of o
+    int q_f16;             // 8-bit K/V: q holds f16 values (else bf16, rounded to f16 in the kernel)
 };
 
 struct DecParams {
@@ -141,6 +151,7 @@ struct CombParams {
     int rows_max;  // most rows of a combine entry (the decode tile's rows)
     float v_scale;
     const float* sinks;  // [Hq] sink logits (natural-log domain), or nullptr
+    int odt;             // OutType of o
     const int* ctrl;
     const Comb* comb;
     const float* part_o;
@@ -320,6 +331,81 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
     uint32_t r;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
     return r;
+}
+// Two e5m2 bytes -> f16x2 (exact: e5m2 is the upper byte of an IEEE binary16).
+__device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint16_t v) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e5m2x2 %0, %1;\n" : "=r"(r) : "h"(v));
+    return r;
+}
+// f16x2 subtraction
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// Four int8 values -> two f16x2 (exact).  Each byte x is placed, sign bit flipped, as the low
+// mantissa byte of the f16 0x6400 (1024): that is 1024 + (x + 128) exactly, and subtracting 1152
+// (0x6480) leaves x.  Every step is exact in f16 (11 significant bits).
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    lo = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4140), 0x64806480u);
+    hi = hsub2_u32(__byte_perm(u, 0x64646464u, 0x4342), 0x64806480u);
+}
+// Eight 8-bit K/V values (two words, in memory order) -> eight f16 (exact), for KT_E4M3,
+// KT_E5M2 or KT_I8.
+template <int KT>
+__device__ __forceinline__ uint4 cvt8x8_to_f16x8(uint32_t w0, uint32_t w1) {
+    uint4 r;
+    if constexpr (KT == KT_I8) {
+        i8x4_to_f16x4(w0, r.x, r.y);
+        i8x4_to_f16x4(w1, r.z, r.w);
+    } else if constexpr (KT == KT_E5M2) {
+        r = make_uint4(e5m2x2_to_f16x2((uint16_t)(w0 & 0xffff)), e5m2x2_to_f16x2((uint16_t)(w0 >> 16)),
+                       e5m2x2_to_f16x2((uint16_t)(w1 & 0xffff)), e5m2x2_to_f16x2((uint16_t)(w1 >> 16)));
+    } else {
+        r = make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
+                       e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
+    }
+    return r;
+}
+// Two bf16 (one word) -> f16x2, round to nearest even
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack2<true>(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+// Output stores in the OutType of o; `e` is the element offset of the first element.
+// Two adjacent elements (e even).
+__device__ __forceinline__ void store_o2(uint8_t* o, size_t e, float a, float b, int odt) {
+    if (odt == OT_F32) *reinterpret_cast<float2*>(o + e * 4) = make_float2(a, b);
+    else if (odt == OT_F16) *reinterpret_cast<uint32_t*>(o + e * 2) = pack2<true>(a, b);
+    else *reinterpret_cast<uint32_t*>(o + e * 2) = pack2<false>(a, b);
+}
+// Four consecutive elements (e a multiple of 4).
+__device__ __forceinline__ void store_o4(uint8_t* o, size_t e, float a, float b, float c, float d, int odt) {
+    if (odt == OT_F32) {
+        *reinterpret_cast<float4*>(o + e * 4) = make_float4(a, b, c, d);
+    } else if (odt == OT_F16) {
+        *reinterpret_cast<uint2*>(o + e * 2) = make_uint2(pack2<true>(a, b), pack2<true>(c, d));
+    } else {
+        *reinterpret_cast<uint2*>(o + e * 2) = make_uint2(pack2<false>(a, b), pack2<false>(c, d));
+    }
+}
+// Eight consecutive elements v[0..7] * s (e a multiple of 8).
+__device__ __forceinline__ void store_o8(uint8_t* o, size_t e, const uint32_t* v, float s, int odt) {
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[i]) * s;
+    if (odt == OT_F32) {
+        *reinterpret_cast<float4*>(o + e * 4) = make_float4(f[0], f[1], f[2], f[3]);
+        *reinterpret_cast<float4*>(o + e * 4 + 16) = make_float4(f[4], f[5], f[6], f[7]);
+    } else if (odt == OT_F16) {
+        *reinterpret_cast<uint4*>(o + e * 2) =
+            make_uint4(pack2<true>(f[0], f[1]), pack2<true>(f[2], f[3]), pack2<true>(f[4], f[5]), pack2<true>(f[6], f[7]));
+    } else {
+        *reinterpret_cast<uint4*>(o + e * 2) = make_uint4(pack2<false>(f[0], f[1]), pack2<false>(f[2], f[3]),
+                                                          pack2<false>(f[4], f[5]), pack2<false>(f[6], f[7]));
+    }
 }
 
 // Programmatic dependent launch: a kernel launched with the programmatic

@@ -6,10 +6,12 @@ so both the CUDA path and the CPU oracle can consume the same bytes.
 
 Layouts follow the "ragged_paged.zig" page (kernel arguments of ``run``):
 
-* ``q``            [num_q_tokens, num_q_heads, head_dim]   bf16 bits (uint16)
+* ``q``            [num_q_tokens, num_q_heads, head_dim]   bf16 or f16 bits
+                   (uint16), or float32
 * ``kv_pages``     [total_num_pages, page_size, 2*num_kv_heads, head_dim]
-                   bf16 bits (uint16) or fp8 e4m3fn bytes (uint8); combined
-                   head 2h is K of kv head h, 2h+1 is V of kv head h.
+                   bf16 or f16 bits (uint16), fp8 e4m3fn / e5m2 bytes (uint8)
+                   or int8; combined head 2h is K of kv head h, 2h+1 is V of
+                   kv head h.
 * ``kv_lens``      [max_num_seqs]                 int32
 * ``page_indices`` [max_num_seqs, pages_per_seq]  int32
 * ``cu_q_lens``    [max_num_seqs + 1]             int32
@@ -23,8 +25,11 @@ Recipe (fixed, so every run sees the same bytes):
 3. ``q`` and ``kv_pages`` are filled chunk by chunk (2**22 elements per chunk)
    from ``default_rng([seed, 1, chunk])`` and ``default_rng([seed, 2, chunk])``.
    Every element of ``kv_pages`` is drawn, tail slots and unused pages too.
-4. Values are N(0, 1) in float32, rounded to bf16 with round-to-nearest-even.
-   fp8 K/V values are ``clip(N(0,1) / 0.05, -448, 448)`` rounded to e4m3fn.
+4. Values are N(0, 1) in float32, rounded to bf16 (or f16) with
+   round-to-nearest-even, or kept as float32 for f32 q.  fp8 K/V values are
+   ``clip(N(0,1) / 0.05, -448, 448)`` rounded to e4m3fn, or
+   ``clip(N(0,1) / 0.05, -57344, 57344)`` rounded to e5m2; int8 K/V values are
+   ``clip(rint(N(0,1) / 0.04), -127, 127)`` (used with scales 0.05 / 0.04).
 5. Attention sinks, when asked for, are one float32 logit per query head drawn
    as N(0, 2^2) from ``default_rng([seed, 3])``.
 """
@@ -54,7 +59,7 @@ class Problem:
     page_size: int
     max_num_seqs: int
     pages_per_seq: int
-    kv_dtype: str  # "bf16" or "fp8_e4m3"
+    kv_dtype: str  # "bf16", "f16", "fp8_e4m3", "fp8_e5m2" or "int8"
     sm_scale: float
     soft_cap: float | None = None
     k_scale: float | None = None
@@ -63,6 +68,7 @@ class Problem:
     sliding_window: int | None = None
     mask_value: float = MASK_VALUE
     sinks: np.ndarray | None = field(default=None, repr=False)  # float32 [num_q_heads] sink logits
+    q_dtype: str = "bf16"  # "bf16", "f16" or "f32" (o has the same type)
     num_seqs: int = 0
     q: np.ndarray = field(default=None, repr=False)
     kv_pages: np.ndarray = field(default=None, repr=False)
@@ -80,7 +86,7 @@ class Problem:
             kv_dtype=self.kv_dtype, sm_scale=self.sm_scale,
             soft_cap=self.soft_cap, k_scale=self.k_scale, v_scale=self.v_scale,
             is_causal=self.is_causal, sliding_window=self.sliding_window,
-            mask_value=self.mask_value, sinks=self.sinks)
+            mask_value=self.mask_value, sinks=self.sinks, q_dtype=self.q_dtype)
 
     @property
     def q_lens(self) -> np.ndarray:
@@ -114,6 +120,38 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << 16).view(np.float32)
 
 
+def f32_to_e5m2_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 (already within +-57344) to fp8 e5m2 bytes via torch."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e5m2).view(torch.uint8).numpy().copy()
+
+
+# storage type of each element type of q and kv_pages
+Q_STORAGE = {"bf16": np.uint16, "f16": np.uint16, "f32": np.float32}
+KV_STORAGE = {"bf16": np.uint16, "f16": np.uint16, "fp8_e4m3": np.uint8, "fp8_e5m2": np.uint8, "int8": np.int8}
+KV_ELT = {"bf16": 2, "f16": 2, "fp8_e4m3": 1, "fp8_e5m2": 1, "int8": 1}
+# fill kinds (the names of the first two are the recipe's originals)
+_KV_FILL = {"bf16": "bf16", "f16": "f16", "fp8_e4m3": "fp8", "fp8_e5m2": "e5m2", "int8": "int8"}
+
+
+def values_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact values of stored q / o / K / V elements of type `dtype` (via numpy / torch casts)."""
+    if dtype == "bf16":
+        return bf16_bits_to_f32(bits).astype(np.float64)
+    if dtype == "f16":
+        return bits.view(np.float16).astype(np.float64)
+    if dtype == "f32":
+        return bits.astype(np.float64)
+    if dtype == "int8":
+        return bits.astype(np.float64)
+    import torch
+
+    tt = torch.float8_e4m3fn if dtype == "fp8_e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.ascontiguousarray(bits)).view(tt).double().numpy()
+
+
 # ---------------------------------------------------------------- fills
 def _fill(out_flat: np.ndarray, seed: int, stream: int, kind: str,
           threads: int | None = None) -> None:
@@ -127,9 +165,18 @@ def _fill(out_flat: np.ndarray, seed: int, stream: int, kind: str,
         x = rng.standard_normal(hi - lo, dtype=np.float32)
         if kind == "bf16":
             out_flat[lo:hi] = f32_to_bf16_bits(x)
-        else:
+        elif kind == "f16":
+            out_flat[lo:hi] = x.astype(np.float16).view(np.uint16)
+        elif kind == "f32":
+            out_flat[lo:hi] = x
+        elif kind == "fp8":
             np.clip(x / np.float32(0.05), -448.0, 448.0, out=x)
             out_flat[lo:hi] = f32_to_e4m3_bits(x)
+        elif kind == "e5m2":
+            np.clip(x / np.float32(0.05), -57344.0, 57344.0, out=x)
+            out_flat[lo:hi] = f32_to_e5m2_bits(x)
+        else:  # int8
+            out_flat[lo:hi] = np.clip(np.rint(x / np.float32(0.04)), -127, 127).astype(np.int8)
 
     threads = threads or min(32, os.cpu_count() or 1)
     if nchunks <= 1:
@@ -146,7 +193,7 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
           sm_scale: float | None = None, soft_cap=None, k_scale=None,
           v_scale=None, is_causal: bool = True, sliding_window=None,
           max_num_seqs: int | None = None, extra_tokens: int = 0,
-          extra_pages: int = 0, name: str = "custom", sinks=None,
+          extra_pages: int = 0, name: str = "custom", sinks=None, q_dtype: str = "bf16",
           rng_lengths: np.random.Generator | None = None) -> Problem:
     """Build a problem with the given lengths (already drawn by the caller).
 
@@ -183,11 +230,10 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
     kvl[:S] = kv_lens_a
 
     Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
-    q = np.empty((T, Hq, D), dtype=np.uint16)
-    _fill(q.reshape(-1), seed, 1, "bf16")
-    kv_np_dtype = np.uint16 if kv_dtype == "bf16" else np.uint8
-    kv = np.empty((total_num_pages, page_size, 2 * Hkv, D), dtype=kv_np_dtype)
-    _fill(kv.reshape(-1), seed, 2, "bf16" if kv_dtype == "bf16" else "fp8")
+    q = np.empty((T, Hq, D), dtype=Q_STORAGE[q_dtype])
+    _fill(q.reshape(-1), seed, 1, q_dtype)
+    kv = np.empty((total_num_pages, page_size, 2 * Hkv, D), dtype=KV_STORAGE[kv_dtype])
+    _fill(kv.reshape(-1), seed, 2, _KV_FILL[kv_dtype])
 
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
@@ -201,7 +247,7 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
         max_num_seqs=max_num_seqs, pages_per_seq=pages_per_seq,
         kv_dtype=kv_dtype, sm_scale=float(sm_scale), soft_cap=soft_cap,
         k_scale=k_scale, v_scale=v_scale, is_causal=is_causal,
-        sliding_window=sliding_window, sinks=sinks, num_seqs=S, q=q, kv_pages=kv,
+        sliding_window=sliding_window, sinks=sinks, q_dtype=q_dtype, num_seqs=S, q=q, kv_pages=kv,
         kv_lens=kvl, page_indices=page_indices, cu_q_lens=cu, name=name)
 
 
@@ -290,14 +336,15 @@ def random_small(seed: int, *, num_seqs: int = 3, max_q: int = 9, max_kv: int = 
 def algorithmic_work(p: Problem, decode_rows: int = 16) -> dict:
     """Algorithmic bytes and FLOPs of one call (keys in the allowed band only).
 
-    bytes = sum_s n_kv(s) * 2*Hkv*D*kv_elt + 2 * T_used*Hq*D*2 + 4*(pages used + 2S + 1)
+    bytes = sum_s n_kv(s) * 2*Hkv*D*kv_elt + 2 * T_used*Hq*D*q_elt + 4*(pages used + 2S + 1)
     flops = sum_s sum_i 4*Hq*D*n_allowed(s, i)
 
     The same sums split by sequence class are returned as ``decode`` and
     ``prefill`` (a sequence is decode-class when q_len * G <= decode_rows),
     so that each attention kernel is charged with the work it does.
     """
-    kv_elt = 2 if p.kv_dtype == "bf16" else 1
+    kv_elt = KV_ELT[p.kv_dtype]
+    q_elt = 4 if p.q_dtype == "f32" else 2  # q and o
     Hq, Hkv, D = p.num_q_heads, p.num_kv_heads, p.head_dim
     G = Hq // Hkv
     sw = p.sliding_window
@@ -313,7 +360,7 @@ def algorithmic_work(p: Problem, decode_rows: int = 16) -> dict:
         lo = np.maximum(pos - sw + 1, 0) if sw else np.zeros(ql, np.int64)
         n_allowed = np.maximum(hi - lo, 0)
         c = part["decode" if ql * G <= decode_rows else "prefill"]
-        c[0] += (int(hi.max()) - int(lo.min())) * 2 * Hkv * D * kv_elt + 2 * ql * Hq * D * 2
+        c[0] += (int(hi.max()) - int(lo.min())) * 2 * Hkv * D * kv_elt + 2 * ql * Hq * D * q_elt
         c[1] += int(n_allowed.sum())
         c[2] += (kl + p.page_size - 1) // p.page_size
         c[3] += ql

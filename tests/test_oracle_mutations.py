@@ -31,6 +31,14 @@ MUTATIONS = [
     ("slot off by one", "int64_t slot = j % c->page_size;", "int64_t slot = (j + 1) % c->page_size;"),
     ("e4m3 subnormal scale", "v = ldexp((double)m / 8.0, 1 - 7); /* subnormal */", "v = ldexp((double)m / 8.0, -7);"),
     ("e4m3 exponent bias", "v = ldexp(1.0 + (double)m / 8.0, e - 7);", "v = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("f16 exponent bias", "else v = ldexp(1.0 + (double)m / 1024.0, e - 15);",
+     "else v = ldexp(1.0 + (double)m / 1024.0, e - 14);"),
+    ("e5m2 mantissa width", "else v = ldexp(1.0 + (double)m / 4.0, e - 15);",
+     "else v = ldexp(1.0 + (double)m / 8.0, e - 15);"),
+    ("int8 read unsigned", "case OKV_I8: return (double)((const int8_t*)kv)[idx];",
+     "case OKV_I8: return (double)((const uint8_t*)kv)[idx];"),
+    ("f32 q read as bf16", "case OQ_F32: return f32_to_f64((const float*)q + idx);",
+     "case OQ_F32: return oracle_bf16_to_f64(((const uint16_t*)q)[idx]);"),
     ("sink left out of the denominator", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);", ""),
     ("sink of the wrong head", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);",
      "if (c->has_sinks) denom += exp(c->sinks[qh / G] - xmax);"),
@@ -41,7 +49,8 @@ MUTATIONS = [
 
 def _pin_calls():
     """Every pin of test_oracle_pins.py as a zero-argument call."""
-    calls = [pins.test_e4m3_decoder_all_codes, pins.test_bf16_decoder_matches_float32_view]
+    calls = [pins.test_e4m3_decoder_all_codes, pins.test_bf16_decoder_matches_float32_view,
+             pins.test_f16_decoder_all_codes, pins.test_e5m2_decoder_all_codes]
     calls += [lambda c=c: pins.test_oracle_equals_dense_brute_force(c) for c in range(len(pins.CASES))]
     calls += [lambda s=s: pins.test_oracle_random_configs_equal_brute_force(s) for s in range(24)]
     calls += [lambda a=a, w=w: pins.test_zero_query_averages_the_allowed_keys(a, w)
@@ -59,7 +68,7 @@ def _load_mutant(path):
     lib = ctypes.CDLL(path)
     ref = oracle._load()
     for name in ("rpa_oracle_forward", "rpa_oracle_rows", "rpa_oracle_validate", "oracle_bf16_to_f64",
-                 "oracle_e4m3_to_f64"):
+                 "oracle_e4m3_to_f64", "oracle_e5m2_to_f64", "oracle_f16_to_f64"):
         f, g = getattr(lib, name), getattr(ref, name)
         f.argtypes, f.restype = g.argtypes, g.restype
     return lib

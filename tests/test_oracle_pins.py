@@ -4,7 +4,9 @@ Each pin is chosen so that a plausible slip in the oracle (a dropped scale, an
 off-by-one in the query position, a swapped K/V head, a wrong window edge, a
 mis-decoded fp8 code) fails at least one of them:
 
-* format decoders against numpy / torch casts and the formats' fixed points;
+* format decoders (bf16, f16, e4m3fn, e5m2) against numpy / torch casts over
+  their codes and the formats' fixed points; f16 / f32 queries and f16, e5m2
+  and int8 K/V in the brute-force cases;
 * brute-force dense attention in numpy (explicit mask matrix, softmax over a
   dense score matrix) on tiny unpaged inputs scattered into shuffled pages;
 * closed forms: uniform V, a single allowed key, one-key sequences, zero-query
@@ -30,7 +32,7 @@ from rpa_inputs import Problem
 
 
 # ------------------------------------------------------------------ helpers
-def dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, kv_dtype="bf16", **knobs):
+def dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, kv_dtype="bf16", q_dtype="bf16", **knobs):
     """Dense per-sequence K/V/Q drawn here, then scattered into shuffled pages.
 
     Returns (problem, dense) where dense[s] = (Q [ql,Hq,D], K [kl,Hkv,D], V [kl,Hkv,D])
@@ -47,23 +49,30 @@ def dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, kv_dtype="bf16", **knobs
         page_indices[s, npages[s]:] = perm[-1]
         off += npages[s]
     T = int(sum(q_lens))
-    q = ri.f32_to_bf16_bits(rng.standard_normal((T, Hq, D)).astype(np.float32))
+    qx = rng.standard_normal((T, Hq, D)).astype(np.float32)
+    q = {"bf16": lambda: ri.f32_to_bf16_bits(qx), "f16": lambda: qx.astype(np.float16).view(np.uint16),
+         "f32": lambda: qx}[q_dtype]()
+    x = rng.standard_normal((N, ps, 2 * Hkv, D)).astype(np.float32)
     if kv_dtype == "bf16":
-        kv = ri.f32_to_bf16_bits(rng.standard_normal((N, ps, 2 * Hkv, D)).astype(np.float32))
-        dec = ri.bf16_bits_to_f32
+        kv = ri.f32_to_bf16_bits(x)
+    elif kv_dtype == "f16":
+        kv = x.astype(np.float16).view(np.uint16)
+    elif kv_dtype == "fp8_e4m3":
+        kv = ri.f32_to_e4m3_bits(np.clip(x / 0.05, -448, 448))
+    elif kv_dtype == "fp8_e5m2":
+        kv = ri.f32_to_e5m2_bits(np.clip(x / 0.05, -57344, 57344))
     else:
-        x = np.clip(rng.standard_normal((N, ps, 2 * Hkv, D)) / 0.05, -448, 448).astype(np.float32)
-        kv = ri.f32_to_e4m3_bits(x)
-        dec = lambda b: torch.from_numpy(b).view(torch.float8_e4m3fn).float().numpy()
+        kv = np.clip(np.rint(x / 0.04), -127, 127).astype(np.int8)
+    dec = lambda b: ri.values_f64(b, kv_dtype)
     cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
     if knobs.get("sinks") is not None:
         knobs["sinks"] = np.asarray(knobs["sinks"], np.float32)
     prob = Problem(num_q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
                    total_num_pages=N, page_size=ps, max_num_seqs=S, pages_per_seq=P,
-                   kv_dtype=kv_dtype, num_seqs=S, q=q, kv_pages=kv,
+                   kv_dtype=kv_dtype, q_dtype=q_dtype, num_seqs=S, q=q, kv_pages=kv,
                    kv_lens=np.asarray(kv_lens, np.int32), page_indices=page_indices,
                    cu_q_lens=cu, sm_scale=knobs.pop("sm_scale", 1.0 / math.sqrt(D)), **knobs)
-    qf = ri.bf16_bits_to_f32(q).astype(np.float64)
+    qf = ri.values_f64(q, q_dtype)
     kvf = dec(kv).astype(np.float64)
     dense = []
     for s in range(S):
@@ -136,6 +145,33 @@ def test_bf16_decoder_matches_float32_view():
         assert (math.isnan(ref) and math.isnan(got)) or ref == got, bits
 
 
+def test_f16_decoder_all_codes():
+    ref = np.arange(65536, dtype=np.uint32).astype(np.uint16).view(np.float16).astype(np.float64)
+    for code in range(65536):
+        got = oracle.decode_f16(code)
+        r = float(ref[code])
+        assert (math.isnan(r) and math.isnan(got)) or r == got, code
+    # fixed points: 1, -2, max normal, min subnormal, min normal, infinities
+    assert oracle.decode_f16(0x3C00) == 1.0 and oracle.decode_f16(0xC000) == -2.0
+    assert oracle.decode_f16(0x7BFF) == 65504.0
+    assert oracle.decode_f16(0x0001) == 2.0 ** -24 and oracle.decode_f16(0x0400) == 2.0 ** -14
+    assert oracle.decode_f16(0x7C00) == math.inf and oracle.decode_f16(0xFC00) == -math.inf
+
+
+def test_e5m2_decoder_all_codes():
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e5m2).double()
+    for code in range(256):
+        got = oracle.decode_e5m2(code)
+        r = float(ref[code])
+        assert (math.isnan(r) and math.isnan(got)) or r == got, code
+    # e5m2 is the upper byte of a binary16, and its fixed points: max 57344, min subnormal 2^-16
+    for code in range(256):
+        a, b = oracle.decode_e5m2(code), oracle.decode_f16(code << 8)
+        assert (math.isnan(a) and math.isnan(b)) or a == b, code
+    assert oracle.decode_e5m2(0x7B) == 57344.0 and oracle.decode_e5m2(0x01) == 2.0 ** -16
+    assert oracle.decode_e5m2(0x3C) == 1.0 and oracle.decode_e5m2(0x7C) == math.inf
+
+
 def test_e4m3_decoder_all_codes():
     ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double()
     for code in range(256):
@@ -168,6 +204,13 @@ CASES = [
     dict(q_lens=[6, 2], kv_lens=[20, 33], Hq=8, Hkv=2, D=16, ps=8, sliding_window=5, soft_cap=2.0,
          sinks=[3.0, -3.0, 0.1, 1.7, -0.4, 5.0, 0.0, 1.0]),
     dict(q_lens=[4, 4], kv_lens=[11, 4], Hq=2, Hkv=1, D=16, ps=4, is_causal=False, sinks=[40.0, -40.0]),
+    # element types: f16 q and K/V; f32 q over bf16 K/V; e5m2 and int8 K/V with scales
+    dict(q_lens=[1, 5, 16], kv_lens=[17, 40, 64], Hq=4, Hkv=2, D=64, ps=16, q_dtype="f16", kv_dtype="f16"),
+    dict(q_lens=[6, 2], kv_lens=[20, 33], Hq=8, Hkv=2, D=16, ps=8, q_dtype="f32", sliding_window=5, soft_cap=2.0),
+    dict(q_lens=[3, 8], kv_lens=[40, 21], Hq=4, Hkv=2, D=32, ps=8, kv_dtype="fp8_e5m2",
+         k_scale=0.05, v_scale=0.07, soft_cap=5.0, sm_scale=0.125),
+    dict(q_lens=[5, 3], kv_lens=[9, 30], Hq=4, Hkv=1, D=32, ps=4, q_dtype="f16", kv_dtype="int8",
+         k_scale=0.04, v_scale=0.03, is_causal=False, sm_scale=0.2),
 ]
 
 
@@ -197,8 +240,11 @@ def test_oracle_random_configs_equal_brute_force(seed):
         kw["sliding_window"] = int(rng.integers(1, 40))
     if rng.integers(0, 2):
         kw["soft_cap"] = float(rng.uniform(0.5, 30.0))
-    if rng.integers(0, 2):
-        kw.update(kv_dtype="fp8_e4m3", k_scale=float(rng.uniform(0.01, 0.1)), v_scale=float(rng.uniform(0.01, 0.1)))
+    kvd = str(rng.choice(["bf16", "f16", "fp8_e4m3", "fp8_e5m2", "int8"]))
+    kw["kv_dtype"] = kvd
+    kw["q_dtype"] = str(rng.choice(["bf16", "f16", "f32"]))
+    if kvd not in ("bf16", "f16"):
+        kw.update(k_scale=float(rng.uniform(0.01, 0.1)), v_scale=float(rng.uniform(0.01, 0.1)))
     if rng.integers(0, 2):
         kw["sinks"] = (rng.standard_normal(Hq) * 2).astype(np.float32)
     prob, dense = dense_problem(rng, q_lens, kv_lens, Hq, Hkv, D, ps, **kw)

@@ -36,14 +36,29 @@
 extern "C" {
 #endif
 
-/* Element types. q is bf16; K/V are bf16 or fp8 e4m3fn ("ragged_paged.zig",
- * Cfg.q_dtype / Cfg.kv_dtype). */
-typedef enum RpaDtype { RPA_DT_BF16 = 0, RPA_DT_FP8_E4M3 = 1 } RpaDtype;
+/* Element types ("ragged_paged.zig", Cfg.q_dtype / Cfg.kv_dtype).
+ *   q (and o, which has q's type): bf16, f16 or f32.
+ *   K/V: bf16, f16, fp8 e4m3fn, fp8 e5m2 or int8 (two's complement); the 8-bit
+ *        types are usually paired with k_scale / v_scale.
+ * The tensor cores take both operands of a product in one type: bf16 with bf16
+ * K/V, f16 with every other K/V type.  K/V values convert exactly; q values
+ * of another type are rounded to that type to nearest even (f32 q; f16 q with
+ * bf16 K/V; bf16 q with f16 or 8-bit K/V), which the tolerance of the results
+ * covers.  The page's other K/V types (f32, i32, i16) are not supported
+ * (RPA_ERR_UNSUPPORTED). */
+typedef enum RpaDtype {
+    RPA_DT_BF16 = 0,
+    RPA_DT_FP8_E4M3 = 1,
+    RPA_DT_F16 = 2,
+    RPA_DT_F32 = 3,       /* q only */
+    RPA_DT_FP8_E5M2 = 4,  /* K/V only */
+    RPA_DT_INT8 = 5       /* K/V only */
+} RpaDtype;
 
 typedef enum RpaStatus {
     RPA_OK = 0,
     RPA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad configuration value */
-    RPA_ERR_UNSUPPORTED = 2,    /* dtype, head_dim not in {64,128,256}, Hq % Hkv != 0, group > 64,
+    RPA_ERR_UNSUPPORTED = 2,    /* dtype (f32/i32/i16 K/V), head_dim not in {64,128,256}, Hq % Hkv != 0, group > 64,
                                    page_size not a multiple of 4, mask_value above -1e30 */
     RPA_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed */
     RPA_ERR_BAD_PAGE_INDEX = 4, /* device-detected: a used page id outside [0, total_num_pages) */
@@ -67,8 +82,8 @@ typedef struct RpaCfg {
     int64_t max_num_seqs;    /* rows of kv_lens / page_indices; cu_q_lens has max_num_seqs+1 */
     int64_t pages_per_seq;   /* columns of page_indices */
     int64_t sliding_window;  /* used when has_sliding_window; must be >= 1 */
-    int32_t q_dtype;         /* RpaDtype: RPA_DT_BF16 */
-    int32_t kv_dtype;        /* RpaDtype: RPA_DT_BF16 or RPA_DT_FP8_E4M3 */
+    int32_t q_dtype;         /* RpaDtype of q and o: BF16, F16 or F32 */
+    int32_t kv_dtype;        /* RpaDtype of kv_pages: BF16, F16, FP8_E4M3, FP8_E5M2 or INT8 */
     float sm_scale;          /* logit scale, finite */
     float mask_value;        /* additive mask of the page (default -2.38197633e38); must be
                                 <= -1e30 so that masked keys get weight exactly 0 */
@@ -115,14 +130,14 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out);
 
 /* One ragged paged attention call (the page's kernel call with inputs
  * kv_lens, page_indices, cu_q_lens, num_seqs, q, kv_pages and output o).
- *   q            device, [num_q_tokens, Hq, D] bf16, 16-byte aligned
+ *   q            device, [num_q_tokens, Hq, D] q_dtype, 16-byte aligned
  *   kv_pages     device, [total_num_pages, page_size, 2*Hkv, D] kv_dtype, 16-byte aligned
  *   kv_lens      device, int32 [max_num_seqs]
  *   page_indices device, int32 [max_num_seqs, pages_per_seq], row-major
  *   cu_q_lens    device, int32 [max_num_seqs + 1]
  *   num_seqs     host scalar, 0 <= num_seqs <= max_num_seqs (the page passes it
  *                as a one-element array)
- *   o            device, [num_q_tokens, Hq, D] bf16, 16-byte aligned, written in
+ *   o            device, [num_q_tokens, Hq, D] q_dtype, 16-byte aligned, written in
  *                full: rows of tokens outside [cu_q_lens[0], cu_q_lens[num_seqs])
  *                are written as 0
  *   stream       cudaStream_t as void*

@@ -10,7 +10,11 @@ from .binding import (  # noqa: F401
     EXPORTS,
     MASK_VALUE,
     RPA_DT_BF16,
+    RPA_DT_F16,
+    RPA_DT_F32,
     RPA_DT_FP8_E4M3,
+    RPA_DT_FP8_E5M2,
+    RPA_DT_INT8,
     RPA_ERR_BAD_LENGTHS,
     RPA_ERR_BAD_PAGE_INDEX,
     RPA_ERR_CUDA,

@@ -26,6 +26,14 @@ RPA_ERR_TIMEOUT = 6
 RPA_ERR_NO_ALLOC_LIMIT = 7
 RPA_DT_BF16 = 0
 RPA_DT_FP8_E4M3 = 1
+RPA_DT_F16 = 2
+RPA_DT_F32 = 3
+RPA_DT_FP8_E5M2 = 4
+RPA_DT_INT8 = 5
+# dtype names of the configuration (q / o, and kv_pages)
+Q_DTYPES = {"bf16": RPA_DT_BF16, "f16": RPA_DT_F16, "f32": RPA_DT_F32}
+KV_DTYPES = {"bf16": RPA_DT_BF16, "f16": RPA_DT_F16, "fp8_e4m3": RPA_DT_FP8_E4M3, "fp8_e5m2": RPA_DT_FP8_E5M2,
+             "int8": RPA_DT_INT8}
 
 # every entry point declared in include/rpa.h
 EXPORTS = ("rpa_cfg_init", "rpa_validate_cfg", "rpa_create", "rpa_forward", "rpa_forward_host",
@@ -133,13 +141,14 @@ def _sinks_pointer(sinks, host_ok):
 def make_cfg(*, num_q_tokens, num_q_heads, num_kv_heads, head_dim, total_num_pages, page_size,
              max_num_seqs, pages_per_seq, sm_scale, kv_dtype="bf16", soft_cap=None, k_scale=None,
              v_scale=None, is_causal=True, sliding_window=None, mask_value=MASK_VALUE, sinks=None,
-             _host_ok=False, **_ignored) -> RpaCfg:
+             q_dtype="bf16", _host_ok=False, **_ignored) -> RpaCfg:
     c = RpaCfg()
     c.num_q_tokens, c.num_q_heads, c.num_kv_heads = int(num_q_tokens), int(num_q_heads), int(num_kv_heads)
     c.head_dim, c.total_num_pages, c.page_size = int(head_dim), int(total_num_pages), int(page_size)
     c.max_num_seqs, c.pages_per_seq = int(max_num_seqs), int(pages_per_seq)
     lib().rpa_cfg_init(ctypes.byref(c))
-    c.kv_dtype = {"bf16": RPA_DT_BF16, "fp8_e4m3": RPA_DT_FP8_E4M3}[kv_dtype]
+    c.kv_dtype = KV_DTYPES[kv_dtype]
+    c.q_dtype = Q_DTYPES[q_dtype]
     c.sm_scale = float(sm_scale)
     c.mask_value = float(mask_value)
     c.has_soft_cap, c.soft_cap = (0, 0.0) if soft_cap is None else (1, float(soft_cap))
@@ -170,13 +179,13 @@ class RaggedPagedAttention:
     """One configuration (shapes and knobs); owns the library workspace.
 
     ``forward`` takes CUDA tensors:
-      q            [num_q_tokens, Hq, D] bfloat16
-      kv_pages     [total_num_pages, page_size, 2*Hkv, D] bfloat16, or uint8 /
-                   float8_e4m3fn bytes for fp8 K/V
+      q            [num_q_tokens, Hq, D] bfloat16, float16 or float32 (q_dtype)
+      kv_pages     [total_num_pages, page_size, 2*Hkv, D] bfloat16 / float16, or
+                   one-byte elements for fp8 (e4m3, e5m2) and int8 K/V
       kv_lens      [max_num_seqs] int32
       page_indices [max_num_seqs, pages_per_seq] int32
       cu_q_lens    [max_num_seqs + 1] int32
-    and returns o [num_q_tokens, Hq, D] bfloat16.  ``sinks`` (optional) is a
+    and returns o [num_q_tokens, Hq, D] of q's dtype.  ``sinks`` (optional) is a
     float32 [Hq] array or CUDA tensor of attention-sink logits.
     """
 
@@ -212,17 +221,20 @@ class RaggedPagedAttention:
 
         c = self._c
         T, Hq, D = c.num_q_tokens, c.num_q_heads, c.head_dim
-        if q.dtype != torch.bfloat16 or tuple(q.shape) != (T, Hq, D) or not q.is_contiguous():
-            raise ValueError("q must be a contiguous bfloat16 tensor [num_q_tokens, Hq, D]")
-        if out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or not out.is_contiguous():
-            raise ValueError("out must be a contiguous bfloat16 tensor [num_q_tokens, Hq, D]")
+        qt = {RPA_DT_BF16: torch.bfloat16, RPA_DT_F16: torch.float16, RPA_DT_F32: torch.float32}[c.q_dtype]
+        if q.dtype != qt or tuple(q.shape) != (T, Hq, D) or not q.is_contiguous():
+            raise ValueError(f"q must be a contiguous {qt} tensor [num_q_tokens, Hq, D]")
+        if out.dtype != qt or tuple(out.shape) != (T, Hq, D) or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous {qt} tensor [num_q_tokens, Hq, D]")
         want_kv = (c.total_num_pages, c.page_size, 2 * c.num_kv_heads, D)
         if tuple(kv_pages.shape) != want_kv or not kv_pages.is_contiguous():
             raise ValueError(f"kv_pages must be contiguous {want_kv}")
         if c.kv_dtype == RPA_DT_BF16 and kv_pages.dtype != torch.bfloat16:
             raise ValueError("kv_pages must be bfloat16")
-        if c.kv_dtype == RPA_DT_FP8_E4M3 and kv_pages.element_size() != 1:
-            raise ValueError("kv_pages must hold fp8 e4m3 bytes")
+        if c.kv_dtype == RPA_DT_F16 and kv_pages.dtype != torch.float16:
+            raise ValueError("kv_pages must be float16")
+        if c.kv_dtype in (RPA_DT_FP8_E4M3, RPA_DT_FP8_E5M2, RPA_DT_INT8) and kv_pages.element_size() != 1:
+            raise ValueError("kv_pages must hold one byte per element (fp8 / int8)")
         for name, t, shape in (("kv_lens", kv_lens, (c.max_num_seqs,)),
                                ("page_indices", page_indices, (c.max_num_seqs, c.pages_per_seq)),
                                ("cu_q_lens", cu_q_lens, (c.max_num_seqs + 1,))):

@@ -18,13 +18,14 @@
 //     cap*tanh(x/cap) = cap - 2cap/(1 + e^{2x/cap}), then masked (tail, causal
 //     p < j, window p - sw >= j) to -inf;
 //   * online softmax with running max / sum per row (row max by warp shuffle),
-//     P in bf16 (f16 for fp8 K/V), O += P V on mma.sync;
-//   * epilogue: O * v_scale / l in bf16, or the unnormalised fp32 partial and
-//     (max, sum) of a split-KV piece for the combine kernel.
+//     P in bf16 (f16 for f16 and 8-bit K/V), O += P V on mma.sync;
+//   * epilogue: O * v_scale / l in o's type, or the unnormalised fp32 partial
+//     and (max, sum) of a split-KV piece for the combine kernel.
 //
-// fp8 K/V: the e4m3 bytes are converted to f16 in shared memory (exact), Q is
-// taken to f16, and the MMAs run in f16; k_scale is folded into the logit
-// scale and v_scale into the epilogue.
+// 8-bit K/V (e4m3, e5m2, int8): the bytes are converted to f16 in shared
+// memory (exact), Q is taken to f16 (bf16 q rounded, f16 q as it is), and the
+// MMAs run in f16; k_scale is folded into the logit scale and v_scale into the
+// epilogue.  f16 K/V run the MMAs in f16 with f16 Q.
 //
 // The body is written for WM row-warps x WN key-warps; the prefill kernel
 // uses WM=4, WN=1: 64 rows, all warps share each stage of keys.  (WN > 1
@@ -35,8 +36,9 @@ namespace rpa {
 
 namespace {
 
-template <int D, bool FP8, int WM, int WN, int BK, int STAGES>
+template <int D, int KT, int WM, int WN, int BK, int STAGES>
 struct KCfg {
+    static constexpr bool FP8 = kt_8bit(KT);
     static constexpr int kThreads = 32 * WM * WN;
     static constexpr int kRows = 16 * WM;
     static constexpr int kKeys = WN * BK;          // keys per stage
@@ -55,10 +57,11 @@ struct KCfg {
 
 __device__ __forceinline__ uint32_t swz(int row, int ch) { return (uint32_t)((ch ^ (row & 7)) << 4); }
 
-template <int D, bool FP8, int WM, int WN, int BK, int STAGES>
+template <int D, int KT, int WM, int WN, int BK, int STAGES>
 __device__ __forceinline__ void attn_body(const AttnParams& p) {
-    using C = KCfg<D, FP8, WM, WN, BK, STAGES>;
-    constexpr bool F16 = FP8;
+    using C = KCfg<D, KT, WM, WN, BK, STAGES>;
+    constexpr bool FP8 = C::FP8;
+    constexpr bool F16 = kt_f16_mma(KT);
     constexpr int kThreads = C::kThreads;
     constexpr int kKeys = C::kKeys;
     constexpr int kCh = C::kCh;
@@ -104,15 +107,11 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
             if constexpr (FP8) {
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid) v = __ldg(reinterpret_cast<const uint4*>(src));
-                // bf16 -> f32 -> f16 for the f16 MMAs
+                // bf16 -> f16 for the f16 MMAs (f16 q as it is)
                 uint32_t w[4] = {v.x, v.y, v.z, v.w};
                 uint32_t o4[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float lo = __uint_as_float(w[k] << 16);
-                    const float hi = __uint_as_float(w[k] & 0xffff0000u);
-                    o4[k] = pack2<true>(lo, hi);
-                }
+                for (int k = 0; k < 4; ++k) o4[k] = p.q_f16 ? w[k] : bf16x2_to_f16x2(w[k]);
                 *reinterpret_cast<uint4*>(dst) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
             } else {
                 cp_async16(smem_u32(dst), valid ? (const void*)src : (const void*)p.q, valid);
@@ -182,7 +181,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
             }
             const uint8_t* kt;
             if constexpr (FP8) {
-                // e4m3 -> f16 (exact) into the single converted tile
+                // 8-bit -> f16 (exact) into the single converted tile
                 const uint8_t* raw = stage_s + (tile % STAGES) * C::kRawBytes;
                 uint8_t* conv = stage_s + STAGES * C::kRawBytes;
                 constexpr int U = 2 * D / 8;  // 8-element units per key (K then V)
@@ -191,11 +190,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
                     const int isv = w >= D / 8;
                     const int ch = w - isv * (D / 8);
                     const uint2 b = *reinterpret_cast<const uint2*>(raw + kk * (2 * D) + w * 8);
-                    uint4 o4;
-                    o4.x = e4m3x2_to_f16x2((uint16_t)(b.x & 0xffff));
-                    o4.y = e4m3x2_to_f16x2((uint16_t)(b.x >> 16));
-                    o4.z = e4m3x2_to_f16x2((uint16_t)(b.y & 0xffff));
-                    o4.w = e4m3x2_to_f16x2((uint16_t)(b.y >> 16));
+                    const uint4 o4 = cvt8x8_to_f16x8<KT>(b.x, b.y);
                     *reinterpret_cast<uint4*>(conv + isv * (kKeys * kRowB) + kk * kRowB + swz(kk, ch)) = o4;
                 }
                 __syncthreads();
@@ -317,11 +312,11 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
                 if (item.part < 0) {
                     const float l = add_sink(l_r[ri], p.sinks, qh, m_r[ri]);
                     const float inv = l > 0.f ? p.v_scale / l : 0.f;
-                    uint32_t* orow = reinterpret_cast<uint32_t*>(p.o + ((size_t)t * Hq + qh) * (D * 2));
+                    const size_t orow = ((size_t)t * Hq + qh) * D;  // element offset of the output row
 #pragma unroll
                     for (int nd = 0; nd < D / 8; ++nd)
-                        orow[nd * 4 + (lane & 3)] =
-                            pack2<false>(o_acc[nd][2 * ri] * inv, o_acc[nd][2 * ri + 1] * inv);
+                        store_o2(p.o, orow + nd * 8 + (lane & 3) * 2, o_acc[nd][2 * ri] * inv,
+                                 o_acc[nd][2 * ri + 1] * inv, p.odt);
                 } else {
                     float* prow = p.part_o + ((size_t)item.part * kDecRows + r) * D;
 #pragma unroll
@@ -371,8 +366,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
                 if (item.part < 0) {
                     const float Ls = add_sink(L, p.sinks, qh, M);
                     const float inv = Ls > 0.f ? p.v_scale / Ls : 0.f;
-                    *reinterpret_cast<uint32_t*>(p.o + (((size_t)t * Hq + qh) * D + c) * 2) =
-                        pack2<false>(o0 * inv, o1 * inv);
+                    store_o2(p.o, ((size_t)t * Hq + qh) * D + c, o0 * inv, o1 * inv, p.odt);
                 } else {
                     *reinterpret_cast<float2*>(p.part_o + ((size_t)item.part * kDecRows + r) * D + c) =
                         make_float2(o0, o1);
@@ -388,72 +382,56 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
 
 // ---------------------------------------------------------------- instantiations
 // prefill: 64 rows (4 warps), all warps share each stage
-template <int D, bool FP8>
+template <int D>
 struct PfShape {
     static constexpr int WM = 4, WN = 1, BK = (D >= 256 ? 32 : 64), STAGES = (D >= 256 ? 2 : 3);
 };
 
-template <int D, bool FP8>
+template <int D, int KT>
 __global__ void __launch_bounds__(128) rpa_prefill_attn(const AttnParams p) {
-    using S = PfShape<D, FP8>;
-    attn_body<D, FP8, S::WM, S::WN, S::BK, S::STAGES>(p);
+    using S = PfShape<D>;
+    attn_body<D, KT, S::WM, S::WN, S::BK, S::STAGES>(p);
 }
-template <template <int, bool> class Shape, int D, bool FP8>
-struct KernelOf;
-template <int D, bool FP8>
-struct KernelOf<PfShape, D, FP8> {
-    static constexpr auto fn = rpa_prefill_attn<D, FP8>;
-};
 
-template <int D, bool FP8, template <int, bool> class Shape>
+template <int D, int KT>
 struct Kern {
-    using S = Shape<D, FP8>;
-    using C = KCfg<D, FP8, S::WM, S::WN, S::BK, S::STAGES>;
+    using S = PfShape<D>;
+    using C = KCfg<D, KT, S::WM, S::WN, S::BK, S::STAGES>;
     static_assert(C::kThreads == 128, "launch bounds");
-    static constexpr auto fn = KernelOf<Shape, D, FP8>::fn;
     static cudaError_t prepare(int* blocks_per_sm) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaError_t e = cudaFuncSetAttribute(rpa_prefill_attn<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmem);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, fn, C::kThreads, C::kSmem);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, rpa_prefill_attn<D, KT>, C::kThreads,
+                                                             C::kSmem);
     }
     static cudaError_t launch(const AttnParams& p, const Launch& l) {
-        return launch_pdl(fn, l.grid, C::kThreads, C::kSmem, l.stream, p);
+        return launch_pdl(rpa_prefill_attn<D, KT>, l.grid, C::kThreads, C::kSmem, l.stream, p);
     }
 };
 
-template <template <int, bool> class Shape>
-cudaError_t dispatch_launch(int D, int fp8, const AttnParams& p, const Launch& l) {
-    if (fp8) {
-        if (D == 64) return Kern<64, true, Shape>::launch(p, l);
-        if (D == 128) return Kern<128, true, Shape>::launch(p, l);
-        if (D == 256) return Kern<256, true, Shape>::launch(p, l);
-    } else {
-        if (D == 64) return Kern<64, false, Shape>::launch(p, l);
-        if (D == 128) return Kern<128, false, Shape>::launch(p, l);
-        if (D == 256) return Kern<256, false, Shape>::launch(p, l);
-    }
-    return cudaErrorInvalidValue;
-}
-
-template <template <int, bool> class Shape>
-cudaError_t dispatch_prepare(int D, int fp8, int* bps) {
-    if (fp8) {
-        if (D == 64) return Kern<64, true, Shape>::prepare(bps);
-        if (D == 128) return Kern<128, true, Shape>::prepare(bps);
-        if (D == 256) return Kern<256, true, Shape>::prepare(bps);
-    } else {
-        if (D == 64) return Kern<64, false, Shape>::prepare(bps);
-        if (D == 128) return Kern<128, false, Shape>::prepare(bps);
-        if (D == 256) return Kern<256, false, Shape>::prepare(bps);
+// The configurations routed here: 2-byte K/V at D 256 (the tensor-memory prefill covers D 64 /
+// 128) and 8-bit K/V at D 64 (the 8-bit tensor-memory prefill covers D 128 / 256).
+template <typename Op>
+cudaError_t mma_dispatch(int D, int kt, Op op) {
+    if (D == 256) {
+        if (kt == KT_BF16) return op(Kern<256, KT_BF16>{});
+        if (kt == KT_F16) return op(Kern<256, KT_F16>{});
+    } else if (D == 64) {
+        if (kt == KT_E4M3) return op(Kern<64, KT_E4M3>{});
+        if (kt == KT_E5M2) return op(Kern<64, KT_E5M2>{});
+        if (kt == KT_I8) return op(Kern<64, KT_I8>{});
     }
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l) {
-    return dispatch_launch<PfShape>(p.D, fp8, p, l);
+cudaError_t launch_prefill(const AttnParams& p, int kt, const Launch& l) {
+    return mma_dispatch(p.D, kt, [&](auto k) { return decltype(k)::launch(p, l); });
 }
-cudaError_t attn_prepare(int D, int fp8, int* pf_bps) { return dispatch_prepare<PfShape>(D, fp8, pf_bps); }
+cudaError_t attn_prepare(int D, int kt, int* pf_bps) {
+    return mma_dispatch(D, kt, [&](auto k) { return decltype(k)::prepare(pf_bps); });
+}
 
 }  // namespace rpa

@@ -86,10 +86,8 @@ __global__ void __launch_bounds__(kCombThreads, 2) rpa_combine_kernel(const Comb
                 const int qh = c.head * G + r % G;
                 L = add_sink(L, p.sinks, qh, M);  // the sink joins once, over all pieces
                 const float inv = L > 0.f ? p.v_scale / L : 0.f;
-                uint2 w;
-                w.x = pack2<false>(acc.x * inv, acc.y * inv);
-                w.y = pack2<false>(acc.z * inv, acc.w * inv);
-                *reinterpret_cast<uint2*>(p.o + (((size_t)t * Hq + qh) * D + col) * 2) = w;
+                store_o4(p.o, ((size_t)t * Hq + qh) * D + col, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv,
+                         p.odt);
             }
             continue;  // the same for every thread of the block
         }
@@ -138,17 +136,14 @@ __global__ void __launch_bounds__(kCombThreads, 2) rpa_combine_kernel(const Comb
             const float inv = s_inv[r];
             const int t = q0 + r / G;
             const int qh = c.head * G + r % G;
-            uint2 w;
-            w.x = pack2<false>(acc.x * inv, acc.y * inv);
-            w.y = pack2<false>(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2*>(p.o + (((size_t)t * Hq + qh) * D + col) * 2) = w;
+            store_o4(p.o, ((size_t)t * Hq + qh) * D + col, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.odt);
         }
         __syncthreads();
     }
     // zero rows of uncovered tokens: [0, lo) and [hi, T)
     const int lo = min(max(p.ctrl[kCovLo], 0), p.T);
     const int hi = min(max(p.ctrl[kCovHi], lo), p.T);
-    const size_t row16 = (size_t)Hq * D * 2 / 16;  // 16-byte words per token row
+    const size_t row16 = (size_t)Hq * D * (p.odt == OT_F32 ? 4 : 2) / 16;  // 16-byte words per token row
     const size_t n_lo = (size_t)lo * row16;
     const size_t n_hi = (size_t)(p.T - hi) * row16;
     uint4* o16 = reinterpret_cast<uint4*>(p.o);

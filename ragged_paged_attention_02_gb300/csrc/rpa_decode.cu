@@ -26,9 +26,11 @@
 // keys on the MMA's M side instead: S^T = K Q^T and O^T += V^T P^T, half the
 // MMAs and accumulator registers of a 16-row tile, three CTAs per SM.
 //
-// fp8 e4m3 K/V: stages hold the raw bytes; each consumer warp converts its 16
-// keys to f16 (exact) in its own buffer and runs the MMAs in f16, with
-// k_scale folded into the logit scale and v_scale into the epilogue.
+// 8-bit K/V (e4m3, e5m2, int8): stages hold the raw bytes; each consumer warp
+// converts its 16 keys to f16 (exact) in its own buffer and runs the MMAs in
+// f16, with k_scale folded into the logit scale and v_scale into the epilogue.
+// f16 K/V run the MMAs in f16, bf16 K/V in bf16; Q arrives in that type (or,
+// with 8-bit K/V, as bf16 rounded to f16 when its fragments are loaded).
 //
 // Every wait is a bounded mbarrier wait (a global-timer deadline): on expiry
 // the status word gets RPA_ERR_TIMEOUT and the warp returns.
@@ -52,8 +54,9 @@ enum Meta : int {
     mKey0, mStop
 };
 
-template <int D, bool FP8, int ROWS>
+template <int D, int KT, int ROWS>
 struct DecGeom {
+    static constexpr bool FP8 = kt_8bit(KT);       // 8-bit K/V, converted to f16 by the consumers
     static constexpr int NS = ROWS == 8 ? 2 : 3;   // stages in the ring
     static constexpr int E = FP8 ? 1 : 2;          // bytes per K/V element
     static constexpr int DHQ = D * 2 / 128;        // 128-byte column blocks of a bf16 row
@@ -65,7 +68,7 @@ struct DecGeom {
     static constexpr int SMEM = NS * SB + kCW * CONV + 1024;  // + alignment slack
     static_assert(QB % 1024 == 0 && KVB % 1024 == 0, "stage alignment");
     static_assert(kCW * ROWS * D * 4 <= (FP8 ? kCW * CONV : KVB), "merge area");
-    static_assert(ROWS == 16 || !FP8, "8-row tiles are bf16 only");
+    static_assert(ROWS == 16 || !FP8, "8-row tiles are for 2-byte K/V only");
 };
 
 __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
@@ -77,12 +80,13 @@ __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
 template <int D, int ROWS>
 constexpr int dec_min_blocks() { return D > 128 ? 1 : ROWS == 8 ? 3 : 2; }
 
-template <int D, bool FP8, int ROWS>
+template <int D, int KT, int ROWS>
 __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_decode_attn(
     const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap, const DecParams p) {
-    using Gm = DecGeom<D, FP8, ROWS>;
+    using Gm = DecGeom<D, KT, ROWS>;
     constexpr int kNS = Gm::NS;
-    constexpr bool F16 = FP8;
+    constexpr bool FP8 = Gm::FP8;
+    constexpr bool F16 = kt_f16_mma(KT);  // MMA operands in f16 (else bf16)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kNS];
     __shared__ __align__(8) uint64_t empty_bar[kNS];
@@ -247,11 +251,11 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                 const int c = 2 * kd + (lane >> 4);
                 const uint32_t line = (uint32_t)((c >> 3) * 16 + r);
                 ldsm_x4(st_base + swz128(line, c & 7), qf[kd][0], qf[kd][1], qf[kd][2], qf[kd][3]);
-                if constexpr (F16) {
+                if constexpr (FP8) {
+                    // bf16 q rounded to f16 for the f16 MMAs (q already f16: as it is)
+                    if (!a.q_f16) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t v = qf[kd][k];
-                        qf[kd][k] = pack2<true>(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+                        for (int k = 0; k < 4; ++k) qf[kd][k] = bf16x2_to_f16x2(qf[kd][k]);
                     }
                 }
             }
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
             const bool partial = kw < kv_begin || kw + 16 > kv_end;
             uint32_t kb, vb;  // bases of row 0 for the ldmatrix address helpers below
             if constexpr (FP8) {
-                // e4m3 -> f16 into this warp's buffer: [K 16 rows][V 16 rows] of D f16, swizzled.
+                // 8-bit -> f16 into this warp's buffer: [K 16 rows][V 16 rows] of D f16, swizzled.
                 // A lane converts 16 consecutive bytes of one (row, K/V) unit; loads are issued
                 // in batches before any conversion so that shared-memory latency overlaps.
                 constexpr int LPR = D / 16, UPP = 32 / LPR, NPASS = 32 / UPP, BATCH = D == 256 ? 2 : 4;
@@ -300,10 +304,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                         const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
                         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
                         if (j >= kv_begin && j < kv_end) {
-                            o0 = make_uint4(e4m3x2_to_f16x2((uint16_t)(a0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(a0 >> 16)),
-                                            e4m3x2_to_f16x2((uint16_t)(a1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(a1 >> 16)));
-                            o1 = make_uint4(e4m3x2_to_f16x2((uint16_t)(b0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(b0 >> 16)),
-                                            e4m3x2_to_f16x2((uint16_t)(b1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(b1 >> 16)));
+                            o0 = cvt8x8_to_f16x8<KT>(a0, a1);
+                            o1 = cvt8x8_to_f16x8<KT>(b0, b1);
                         }
                         uint8_t* rowp = conv + kv * (16 * D * 2) + row * (D * 2);
                         const int c1 = 2 * e + (sw ? 1 : 0), c2 = 2 * e + (sw ? 0 : 1);
@@ -516,8 +518,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     const int qh = head * G + r % G;
                     L = add_sink(L, a.sinks, qh, M);
                     const float inv = L > 0.f ? a.v_scale / L : 0.f;
-                    *reinterpret_cast<uint32_t*>(a.o + (((size_t)t * Hq + qh) * D + c) * 2) =
-                        pack2<false>(o0 * inv, o1 * inv);
+                    store_o2(a.o, ((size_t)t * Hq + qh) * D + c, o0 * inv, o1 * inv, a.odt);
                 } else {
                     *reinterpret_cast<float2*>(a.part_o + ((size_t)part * kDecRows + r) * D + c) =
                         make_float2(o0, o1);
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     const uint32_t line = (uint32_t)((c >> 3) * BR + r);
                     uint32_t af[4];
                     ldsm_x4(kv_base + b * PBB + swz128(line, c & 7), af[0], af[1], af[2], af[3]);
-                    mma16816<false>((kd & 1) ? sodd : sacc, af, qt[kd][0], qt[kd][1]);
+                    mma16816<F16>((kd & 1) ? sodd : sacc, af, qt[kd][0], qt[kd][1]);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
@@ -682,8 +683,8 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
             // P[key k][row n] (k < 8) sits in lane 4k + n/2, element n % 2 (keys 8-15: elements 2, 3).
             uint32_t pb0, pb1;
             {
-                const uint32_t w01 = pack2<false>(sacc[0], sacc[1]);  // key g:     rows 2q, 2q + 1
-                const uint32_t w23 = pack2<false>(sacc[2], sacc[3]);  // key g + 8: rows 2q, 2q + 1
+                const uint32_t w01 = pack2<F16>(sacc[0], sacc[1]);  // key g:     rows 2q, 2q + 1
+                const uint32_t w23 = pack2<F16>(sacc[2], sacc[3]);  // key g + 8: rows 2q, 2q + 1
                 const int src0 = 8 * q + (g >> 1), src1 = src0 + 4;   // lanes of keys 2q, 2q + 1
                 const uint32_t x0 = __shfl_sync(0xffffffffu, w01, src0);
                 const uint32_t x1 = __shfl_sync(0xffffffffu, w01, src1);
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
                     uint32_t af[4];
                     ldsm_x4_t(kv_base + b * PBB + swz128(line, c & 7), af[0], af[1], af[2], af[3]);
-                    mma16816<false>(o_acc[mt], af, pb0, pb1);
+                    mma16816<F16>(o_acc[mt], af, pb0, pb1);
                 }
             }
         }
@@ -769,8 +770,7 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     const int qh = head * G + r % G;
                     L = add_sink(L, a.sinks, qh, M);
                     const float inv = L > 0.f ? a.v_scale / L : 0.f;
-                    *reinterpret_cast<uint32_t*>(a.o + (((size_t)t * Hq + qh) * D + c) * 2) =
-                        pack2<false>(o0 * inv, o1 * inv);
+                    store_o2(a.o, ((size_t)t * Hq + qh) * D + c, o0 * inv, o1 * inv, a.odt);
                 } else {
                     *reinterpret_cast<float2*>(a.part_o + ((size_t)part * kDecRows + r) * D + c) =
                         make_float2(o0, o1);
@@ -794,59 +794,56 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
     }
 }
 
-template <int D, bool FP8, int ROWS>
+template <int D, int KT, int ROWS>
 struct DecKern {
-    using Gm = DecGeom<D, FP8, ROWS>;
+    using Gm = DecGeom<D, KT, ROWS>;
     static cudaError_t prepare(int* bps) {
-        cudaError_t e = cudaFuncSetAttribute(rpa_decode_attn<D, FP8, ROWS>,
+        cudaError_t e = cudaFuncSetAttribute(rpa_decode_attn<D, KT, ROWS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_decode_attn<D, FP8, ROWS>, kDecThreads,
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_decode_attn<D, KT, ROWS>, kDecThreads,
                                                              Gm::SMEM);
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p,
                               const Launch& l) {
-        return launch_pdl(rpa_decode_attn<D, FP8, ROWS>, l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
+        return launch_pdl(rpa_decode_attn<D, KT, ROWS>, l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 
-}  // namespace
-
-cudaError_t decode_prepare(int D, int fp8, int rows, int* bps) {
-    if (fp8) {
-        if (rows != 16) return cudaErrorInvalidValue;
-        if (D == 64) return DecKern<64, true, 16>::prepare(bps);
-        if (D == 128) return DecKern<128, true, 16>::prepare(bps);
-        if (D == 256) return DecKern<256, true, 16>::prepare(bps);
-    } else if (rows == 8) {
-        if (D == 64) return DecKern<64, false, 8>::prepare(bps);
-        if (D == 128) return DecKern<128, false, 8>::prepare(bps);
-        if (D == 256) return DecKern<256, false, 8>::prepare(bps);
-    } else {
-        if (D == 64) return DecKern<64, false, 16>::prepare(bps);
-        if (D == 128) return DecKern<128, false, 16>::prepare(bps);
-        if (D == 256) return DecKern<256, false, 16>::prepare(bps);
+// The instantiations in use: 2-byte K/V at D 64 / 128 / 256 with 8- or 16-row tiles; 8-bit K/V
+// at D 64 with 16-row tiles (at D 128 / 256 the 8-bit tensor-memory prefill kernel takes the
+// decode rows).  `op` is called with the kernel type, or the result is cudaErrorInvalidValue.
+template <typename Op>
+cudaError_t dec_dispatch(int D, int kt, int rows, Op op) {
+    if (kt_8bit(kt)) {
+        if (rows != 16 || D != 64) return cudaErrorInvalidValue;
+        if (kt == KT_E4M3) return op(DecKern<64, KT_E4M3, 16>{});
+        if (kt == KT_E5M2) return op(DecKern<64, KT_E5M2, 16>{});
+        if (kt == KT_I8) return op(DecKern<64, KT_I8, 16>{});
+        return cudaErrorInvalidValue;
+    }
+    const bool f16 = kt == KT_F16;
+    if (rows == 8) {
+        if (D == 64) return f16 ? op(DecKern<64, KT_F16, 8>{}) : op(DecKern<64, KT_BF16, 8>{});
+        if (D == 128) return f16 ? op(DecKern<128, KT_F16, 8>{}) : op(DecKern<128, KT_BF16, 8>{});
+        if (D == 256) return f16 ? op(DecKern<256, KT_F16, 8>{}) : op(DecKern<256, KT_BF16, 8>{});
+    } else if (rows == 16) {
+        if (D == 64) return f16 ? op(DecKern<64, KT_F16, 16>{}) : op(DecKern<64, KT_BF16, 16>{});
+        if (D == 128) return f16 ? op(DecKern<128, KT_F16, 16>{}) : op(DecKern<128, KT_BF16, 16>{});
+        if (D == 256) return f16 ? op(DecKern<256, KT_F16, 16>{}) : op(DecKern<256, KT_BF16, 16>{});
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int fp8,
+}  // namespace
+
+cudaError_t decode_prepare(int D, int kt, int rows, int* bps) {
+    return dec_dispatch(D, kt, rows, [&](auto k) { return decltype(k)::prepare(bps); });
+}
+
+cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int kt,
                               int rows, const Launch& l) {
-    if (fp8) {
-        if (rows != 16) return cudaErrorInvalidValue;
-        if (p.a.D == 64) return DecKern<64, true, 16>::launch(kvm, qm, p, l);
-        if (p.a.D == 128) return DecKern<128, true, 16>::launch(kvm, qm, p, l);
-        if (p.a.D == 256) return DecKern<256, true, 16>::launch(kvm, qm, p, l);
-    } else if (rows == 8) {
-        if (p.a.D == 64) return DecKern<64, false, 8>::launch(kvm, qm, p, l);
-        if (p.a.D == 128) return DecKern<128, false, 8>::launch(kvm, qm, p, l);
-        if (p.a.D == 256) return DecKern<256, false, 8>::launch(kvm, qm, p, l);
-    } else {
-        if (p.a.D == 64) return DecKern<64, false, 16>::launch(kvm, qm, p, l);
-        if (p.a.D == 128) return DecKern<128, false, 16>::launch(kvm, qm, p, l);
-        if (p.a.D == 256) return DecKern<256, false, 16>::launch(kvm, qm, p, l);
-    }
-    return cudaErrorInvalidValue;
+    return dec_dispatch(p.a.D, kt, rows, [&](auto k) { return decltype(k)::launch(kvm, qm, p, l); });
 }
 
 }  // namespace rpa

@@ -179,26 +179,92 @@ cudaError_t launch_pdl(Kern k, int grid, int block, size_t smem, cudaStream_t st
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
-cudaError_t launch_prefill(const AttnParams& p, int fp8, const Launch& l);
+// kt: KvType of kv_pages
+cudaError_t launch_prefill(const AttnParams& p, int kt, const Launch& l);
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
-// rows: query rows of a decode tile, 16 (any) or 8 (bf16 K/V, G <= 8: keys on the MMA's M side)
-cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int fp8,
+// rows: query rows of a decode tile, 16 (any) or 8 (2-byte K/V, G <= 8: keys on the MMA's M side)
+cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int kt,
                               int rows, const Launch& l);
-cudaError_t decode_prepare(int D, int fp8, int rows, int* blocks_per_sm);
-cudaError_t launch_prefill_tc(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l);
-cudaError_t prefill_tc_prepare(int D, int* blocks_per_sm);
-cudaError_t launch_prefill_tc8(const CUtensorMap& kvm_runs, const CUtensorMap& qm, const TcParams& p,
+cudaError_t decode_prepare(int D, int kt, int rows, int* blocks_per_sm);
+cudaError_t launch_prefill_tc(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, int kt,
+                              const Launch& l);
+cudaError_t prefill_tc_prepare(int D, int kt, int* blocks_per_sm);
+cudaError_t launch_prefill_tc8(const CUtensorMap& kvm_runs, const CUtensorMap& qm, const TcParams& p, int kt,
                                const Launch& l);
-cudaError_t prefill_tc8_prepare(int D, int* blocks_per_sm);
+cudaError_t prefill_tc8_prepare(int D, int kt, int* blocks_per_sm);
+// q (n elements of RpaDtype q_dtype: f32, f16 or bf16) rounded to f16 (to_f16) or bf16 into out
+cudaError_t launch_q_convert(const void* q, int q_dtype, uint8_t* out, int to_f16, size_t n, const Launch& l);
 constexpr int kTcRows = 128;  // rows of a tensor-memory prefill tile
-// tensor maps for the decode gather (host; no allocation)
-int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR);
+// tensor maps for the gathers (host; no allocation); byte_elems: 1-byte K/V elements, else 2-byte
+int encode_kv_map(CUtensorMap* m, const void* kv, int byte_elems, long long N, int ps, int Hkv, int D, int BR);
 int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt);
-int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR);
+int encode_kv_map_runs(CUtensorMap* m, const void* kv, int byte_elems, long long N, int ps, int Hkv, int D, int BR);
 // occupancy / attributes (call once per device)
-cudaError_t attn_prepare(int D, int fp8, int* pf_blocks_per_sm);
+cudaError_t attn_prepare(int D, int kt, int* pf_blocks_per_sm);
 size_t plan_smem_bytes();
 cudaError_t plan_prepare();
+
+// ---------------------------------------------------------------- one call, host side (rpa_launch.cu)
+// The kernels and tiles a configuration uses, with their occupancy and the workspace capacities.
+struct KernelSet {
+    int G, D, kt, odt;
+    int q_conv;          // 1: q is first rounded into the workspace (its type is not the MMA operand type)
+    int q_conv_f16;      // ... to f16 (else bf16)
+    int q_f16;           // 8-bit K/V: the q the kernels read holds f16 values
+    int tc, tc8;         // prefill on the tensor-memory kernel for 2-byte / 8-bit K/V
+    int dec_rows, pf_tokens, Tt, BR, br_shift, window;
+    float qk_log2, cap_exp, cap_log2, v_scale;
+    int sms, dec_bps, pf_bps;
+    int max_dec_units, max_pf_units, max_units, max_part, max_comb;
+};
+struct Workspace {
+    int* ctrl;
+    int* seq_scratch;
+    int* units;
+    Item* dec_items;
+    Item* pf_items;
+    Comb* comb;
+    float* part_o;
+    float* part_ml;
+    uint8_t* qbuf;  // q in the MMA operand type (when KernelSet::q_conv)
+};
+// Tensor maps of the last call, re-encoded when the pointers change
+struct MapCache {
+    CUtensorMap kv, kv_pf, q, q_pf;
+    const void* kv_ptr;
+    const void* q_ptr;
+};
+// Profile events of one call: each kernel is timed from an event recorded on its own stream just
+// before its launch (after any cross-stream wait) to one recorded just after it.
+enum ProfEvent : int {
+    kEvStart = 0, kEvPlanEnd, kEvDecStart, kEvDecEnd, kEvPfStart, kEvPfEnd, kEvCombStart, kEvCombEnd,
+    kProfEvents
+};
+struct EnqueueOpts {
+    cudaStream_t st;                 // the caller's stream
+    int conc;                        // decode on `side` concurrently with prefill on st
+    cudaStream_t side;
+    cudaEvent_t ev_plan, ev_dec;     // fork / join events (conc)
+    cudaEvent_t ev[kProfEvents];     // profile events, or nullptr
+    int debug_stall;
+    unsigned long long timeout_ns;
+    int force_pf_sms, force_dec_sms;
+};
+// Host only: fill ks from a validated configuration (sms = the device's SM count).
+void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks);
+// Kernel attributes and occupancy on the current device (dec_bps, pf_bps); an error if a kernel
+// cannot be resident.
+cudaError_t kernels_occupancy(KernelSet* ks);
+// The workspace capacities of cfg (host only, after kernels_occupancy).
+void kernels_capacity(const RpaCfg& c, KernelSet* ks);
+// Both of the above.
+cudaError_t kernels_prepare(const RpaCfg& c, KernelSet* ks);
+size_t workspace_bytes(const RpaCfg& c, const KernelSet& ks);
+Workspace workspace_carve(const RpaCfg& c, const KernelSet& ks, void* base);
+// Enqueue one call; returns an RpaStatus.  Allocates nothing.
+int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, MapCache* maps, const void* q,
+                    const void* kv_pages, const int32_t* kv_lens, const int32_t* page_indices,
+                    const int32_t* cu_q_lens, int32_t num_seqs, void* o, const EnqueueOpts& eo);
 
 // ---------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
@@ -368,6 +434,14 @@ __device__ __forceinline__ uint4 cvt8x8_to_f16x8(uint32_t w0, uint32_t w1) {
                        e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
     }
     return r;
+}
+// f16x2 -> two floats (exact)
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
+    float lo, hi;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+        : "=f"(lo), "=f"(hi)
+        : "r"(v));
+    return make_float2(lo, hi);
 }
 // Two bf16 (one word) -> f16x2, round to nearest even
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {

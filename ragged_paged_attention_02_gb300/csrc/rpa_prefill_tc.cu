@@ -26,6 +26,9 @@
 //                   is unchanged).  At the item's end it normalises O by l and
 //                   stores bf16 o.
 //
+// K/V in f16 run both MMAs in f16 (P in f16); bf16 K/V in bf16.  Q arrives in
+// the same type.
+//
 // Keys of a tile outside the item's [kv_begin, kv_end) are masked in S and
 // their V rows are zeroed in shared memory (by group A, before PV_A) since
 // tail slots of a page may hold any bits; the page zeroes K/V past kv_len the
@@ -66,7 +69,8 @@ struct TcGeom {
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// p = 2^(x * mul - base) for the 32 logits of one S chunk: bf16 pairs into pk, sums into ls2
+// p = 2^(x * mul - base) for the 32 logits of one S chunk: bf16 (F16: f16) pairs into pk, sums into ls2
+template <bool F16>
 __device__ __forceinline__ void exp_chunk(const uint32_t* sv, uint64_t mul2, uint64_t nbase2, uint64_t* ls2,
                                           uint32_t* pk) {
 #pragma unroll
@@ -75,11 +79,11 @@ __device__ __forceinline__ void exp_chunk(const uint32_t* sv, uint64_t mul2, uin
         f32x2_split(ffma2(f32x2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), mul2, nbase2), x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
         ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
-        pk[i] = pack2<false>(p0, p1);
+        pk[i] = pack2<F16>(p0, p1);
     }
 }
 
-template <int D>
+template <int D, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_constant__ CUtensorMap kvmap,
                                                               const __grid_constant__ CUtensorMap qmap,
                                                               const TcParams p) {
@@ -253,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     } else if (warp == kMma) {
         // =============================== MMA issuer ===============================
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = umma_idesc_bf16(kM, kBN, 0, 0);
-            constexpr uint32_t idesc_pv = umma_idesc_bf16(kM, D, 0, 1);
+            constexpr uint32_t idesc_qk = F16 ? umma_idesc_f16(kM, kBN, 0, 0) : umma_idesc_bf16(kM, kBN, 0, 0);
+            constexpr uint32_t idesc_pv = F16 ? umma_idesc_f16(kM, D, 0, 1) : umma_idesc_bf16(kM, D, 0, 1);
             int s = 0;
             uint32_t qph = 0, ph = 0;
             uint32_t j_all = 0;   // key tiles issued so far (all items): phase of s_full / p_full
@@ -432,16 +436,16 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                     // chunks 2 and 3 reloaded while chunk 1 is exponentiated
                     const uint64_t mul2 = f32x2(a.qk_log2, a.qk_log2), nbase2 = f32x2(-base, -base);
                     uint32_t pk[16];
-                    exp_chunk(sa, mul2, nbase2, ls2, pk);
+                    exp_chunk<F16>(sa, mul2, nbase2, ls2, pk);
                     tmem_st16(lane_addr + scol, pk);
                     tmem_ld32(lane_addr + scol + 64, sa);
-                    exp_chunk(sb, mul2, nbase2, ls2, pk);
+                    exp_chunk<F16>(sb, mul2, nbase2, ls2, pk);
                     tmem_st16(lane_addr + scol + 16, pk);
                     tmem_ld32(lane_addr + scol + 96, sb);
                     tmem_ld_wait();
-                    exp_chunk(sa, mul2, nbase2, ls2, pk);
+                    exp_chunk<F16>(sa, mul2, nbase2, ls2, pk);
                     tmem_st16(lane_addr + scol + 32, pk);
-                    exp_chunk(sb, mul2, nbase2, ls2, pk);
+                    exp_chunk<F16>(sb, mul2, nbase2, ls2, pk);
                     tmem_st16(lane_addr + scol + 48, pk);
                 } else {
                     const bool cap = a.has_cap;
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                         uint32_t sv[32], pk[16];
                         tmem_ld32(lane_addr + scol + c * 32, sv);
                         tmem_ld_wait();
-                        exp_chunk(sv, mul2, nbase2, ls2, pk);
+                        exp_chunk<F16>(sv, mul2, nbase2, ls2, pk);
                         tmem_st16(lane_addr + scol + c * 16, pk);
                     }
                 }
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
             const int qh = head * G + r % G;
             const float l_fin = add_sink(l_run, a.sinks, qh, m_run);  // P was taken relative to m_run
             const float inv = l_fin > 0.f ? a.v_scale / l_fin : 0.f;
-            uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2);
+            const size_t orow = ((size_t)t_tok * Hq + qh) * D;  // element offset of the output row
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t ov[32];
@@ -543,14 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
                 tmem_ld_wait();
                 if (r < rows_used) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 w;
-                        w.x = pack2<false>(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
-                        w.y = pack2<false>(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
-                        w.z = pack2<false>(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
-                        w.w = pack2<false>(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
-                        put_u4(orow + c * 64 + i * 16, w);
-                    }
+                    for (int i = 0; i < 4; ++i) store_o8(a.o, orow + c * 32 + i * 8, ov + 8 * i, inv, a.odt);
                 }
             }
             tc_fence_before();
@@ -567,31 +564,38 @@ __global__ void __launch_bounds__(kThreads, 1) rpa_prefill_tc(const __grid_const
     }
 }
 
-template <int D>
+template <int D, bool F16>
 struct TcKern {
     using Gm = TcGeom<D>;
     static cudaError_t prepare(int* bps) {
-        cudaError_t e = cudaFuncSetAttribute(rpa_prefill_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(rpa_prefill_tc<D, F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_prefill_tc<D>, kThreads, Gm::SMEM);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_prefill_tc<D, F16>, kThreads, Gm::SMEM);
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
-        return launch_pdl(rpa_prefill_tc<D>, l.grid, kThreads, Gm::SMEM, l.stream, kvm, qm, p);
+        return launch_pdl(rpa_prefill_tc<D, F16>, l.grid, kThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 
-}  // namespace
-
-cudaError_t prefill_tc_prepare(int D, int* bps) {
-    if (D == 64) return TcKern<64>::prepare(bps);
-    if (D == 128) return TcKern<128>::prepare(bps);
+// 2-byte K/V at D 64 / 128: bf16 or f16 MMAs
+template <typename Op>
+cudaError_t tc_dispatch(int D, int kt, Op op) {
+    if (kt != KT_BF16 && kt != KT_F16) return cudaErrorInvalidValue;
+    const bool f16 = kt == KT_F16;
+    if (D == 64) return f16 ? op(TcKern<64, true>{}) : op(TcKern<64, false>{});
+    if (D == 128) return f16 ? op(TcKern<128, true>{}) : op(TcKern<128, false>{});
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_prefill_tc(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
-    if (p.a.D == 64) return TcKern<64>::launch(kvm, qm, p, l);
-    if (p.a.D == 128) return TcKern<128>::launch(kvm, qm, p, l);
-    return cudaErrorInvalidValue;
+}  // namespace
+
+cudaError_t prefill_tc_prepare(int D, int kt, int* bps) {
+    return tc_dispatch(D, kt, [&](auto k) { return decltype(k)::prepare(bps); });
+}
+
+cudaError_t launch_prefill_tc(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, int kt, const Launch& l) {
+    return tc_dispatch(p.a.D, kt, [&](auto k) { return decltype(k)::launch(kvm, qm, p, l); });
 }
 
 }  // namespace rpa

@@ -1,20 +1,22 @@
-// rpa_prefill_tc8.cu -- K1 prefill for fp8 e4m3 K/V on the tcgen05 tensor cores.
+// rpa_prefill_tc8.cu -- K1 prefill for 8-bit K/V (fp8 e4m3 / e5m2, int8) on the tcgen05 tensor cores.
 //
 // One persistent CTA per SM takes prefill work items of up to 128 query rows
 // of one kv head (Tq = 128 / G tokens x the G query heads of the group, packed
 // as the "ragged_paged.zig" page packs its q block into [Tq*G, D]) against a
 // key range of one sequence, in tiles of 64 keys.  The page dequantises with
-// k.astype(f32) * k_scale -> q dtype; here the e4m3 values are converted
-// exactly to f16, both MMAs run in f16 with fp32 accumulation, k_scale is
-// folded into the logit scale and v_scale into the epilogue.  Roles:
+// k.astype(f32) * k_scale -> q dtype; here the 8-bit values (e4m3, e5m2 or
+// int8) are converted exactly to f16, both MMAs run in f16 with fp32
+// accumulation, k_scale is folded into the logit scale and v_scale into the
+// epilogue.  Roles:
 //
 //   producer warp    Q tile (bf16) into a staging buffer, then per 64-key tile
 //                    the raw fp8 K/V rows of each page run (one bulk tensor
 //                    copy per run: K and V of the head) into a 2-slot ring.
-//   8 converter      Q (warps on lane quadrants 0-3): bf16 -> f16 into TMEM
-//   warps            (the A operand of S = Q K^T).  K and V: each warp takes 8
+//   8 converter      Q (warps on lane quadrants 0-3): bf16 -> f16 (f16 q as it
+//   warps            is) into TMEM (the A operand of S = Q K^T).  K and V: each
+//                    warp takes 8
 //                    key rows of a tile into registers (the ring slot goes
-//                    straight back to the producer), then e4m3 -> f16 into
+//                    straight back to the producer), then 8-bit -> f16 into
 //                    double-buffered, 128-byte swizzled tiles (K-major), keys
 //                    outside the item's [kv_begin, kv_end) written as zero
 //                    (the page zeroes K/V past kv_len; tail slots may hold any
@@ -74,12 +76,6 @@ struct G8 {
 
 __device__ __forceinline__ void put_u4(uint8_t* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
-// e4m3 x 8 -> f16 x 8 with the hardware conversion (exact values)
-__device__ __forceinline__ uint4 e4m3x8_to_f16x8_hw(uint32_t w0, uint32_t w1) {
-    return make_uint4(e4m3x2_to_f16x2((uint16_t)(w0 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w0 >> 16)),
-                      e4m3x2_to_f16x2((uint16_t)(w1 & 0xffff)), e4m3x2_to_f16x2((uint16_t)(w1 >> 16)));
-}
-
 // One converter warp's key rows (kConvRows cw .. + kConvRows - 1) of one half (K or V) of a raw
 // stage ([run][K | V][BR rows][D bytes]; `raw` points at the half's first run): a lane takes 16
 // consecutive bytes of a row (D / 16 lanes a row, RPP rows a pass, NP passes).
@@ -100,7 +96,7 @@ __device__ __forceinline__ void load_rows(const uint8_t* raw, int cw, int lane, 
 }
 // ... and those rows, converted exactly to f16, into a 128-byte swizzled tile [D / 64][64 rows]
 // [128 B]; keys outside [kv_begin, kv_end) become zero.
-template <int D>
+template <int D, int KT>
 __device__ __forceinline__ void store_rows(const uint4* v, uint8_t* dst, int cw, int lane, int k_lo, int kv_begin,
                                            int kv_end) {
     using C = ConvLanes<D>;
@@ -117,8 +113,8 @@ __device__ __forceinline__ void store_rows(const uint4* v, uint8_t* dst, int cw,
         const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
         uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
         if (j >= kv_begin && j < kv_end) {
-            o0 = e4m3x8_to_f16x8_hw(a0, a1);
-            o1 = e4m3x8_to_f16x8_hw(b0, b1);
+            o0 = cvt8x8_to_f16x8<KT>(a0, a1);
+            o1 = cvt8x8_to_f16x8<KT>(b0, b1);
         }
         const int line = cb * kBN + key;
         uint8_t* row = dst + line * 128;
@@ -180,7 +176,7 @@ __device__ __forceinline__ void add_copies(uint32_t* ov, int R) {
     }
 }
 
-template <int D>
+template <int D, int KT>
 __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __grid_constant__ CUtensorMap kvmap,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const TcParams p) {
@@ -382,8 +378,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const uint4 w = *reinterpret_cast<const uint4*>(row + (((c ^ r) & 7) << 4));
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            qv[4 * c + k] = pack2<true>(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xffff0000u));
+                        for (int k = 0; k < 4; ++k) qv[4 * c + k] = a.q_f16 ? ws[k] : bf16x2_to_f16x2(ws[k]);
                     }
                     tmem_st32(lane_addr + Gm::TM_Q + rd * 32, qv);
                 }
@@ -423,7 +418,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     ok = false;
                     break;
                 }
-                store_rows<D>(kr, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
+                store_rows<D, KT>(kr, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&k_full[b2]));
@@ -431,7 +426,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     ok = false;
                     break;
                 }
-                store_rows<D>(vr, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
+                store_rows<D, KT>(vr, smem + (v16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
@@ -569,7 +564,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
         constexpr int HC = kBN / 2;  // logits of a lane's row in this warp's half of a tile
         constexpr int HO = D / 2;    // O columns this warp owns
         const int G = a.G, Hq = a.Hq;
-        // K and V tiles hold the exact e4m3 values (the scales act on the logits and the output).
+        // K and V tiles hold the exact 8-bit values (the scales act on the logits and the output).
         // Soft cap: cap log2(e) tanh(s sm_scale k_scale / cap) with the hardware tanh (relative
         // error about 2^-11, the order of the f16 rounding of P); its argument factor is
         // cap_exp / (2 log2(e)).
@@ -753,7 +748,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             const int qh = head * G + r % G;
             const float l_fin = add_sink(l_row, a.sinks, qh, m_run);  // P was taken relative to m_run
             const float inv = l_fin > 0.f ? a.v_scale / l_fin : 0.f;
-            uint8_t* orow = a.o + ((size_t)t_tok * Hq + qh) * (D * 2) + half * HO * 2;
+            const size_t orow = ((size_t)t_tok * Hq + qh) * D + half * HO;  // element offset of this half row
 #pragma unroll 1
             for (int cc = 0; cc < HO / 32; ++cc) {
                 uint32_t ov[32];
@@ -762,14 +757,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 add_copies(ov, R);
                 if (store) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint4 w;
-                        w.x = pack2<false>(__uint_as_float(ov[8 * i + 0]) * inv, __uint_as_float(ov[8 * i + 1]) * inv);
-                        w.y = pack2<false>(__uint_as_float(ov[8 * i + 2]) * inv, __uint_as_float(ov[8 * i + 3]) * inv);
-                        w.z = pack2<false>(__uint_as_float(ov[8 * i + 4]) * inv, __uint_as_float(ov[8 * i + 5]) * inv);
-                        w.w = pack2<false>(__uint_as_float(ov[8 * i + 6]) * inv, __uint_as_float(ov[8 * i + 7]) * inv);
-                        put_u4(orow + cc * 64 + i * 16, w);
-                    }
+                    for (int i = 0; i < 4; ++i) store_o8(a.o, orow + cc * 32 + i * 8, ov + 8 * i, inv, a.odt);
                 }
             }
             tc_fence_before();
@@ -786,32 +774,44 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     }
 }
 
-template <int D>
+template <int D, int KT>
 struct Tc8Kern {
     using Gm = G8<D>;
     static cudaError_t prepare(int* bps) {
         cudaError_t e =
-            cudaFuncSetAttribute(rpa_prefill_tc8<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+            cudaFuncSetAttribute(rpa_prefill_tc8<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_prefill_tc8<D>, kThreads, Gm::SMEM);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_prefill_tc8<D, KT>, kThreads, Gm::SMEM);
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
-        return launch_pdl(rpa_prefill_tc8<D>, l.grid, kThreads, Gm::SMEM, l.stream, kvm, qm, p);
+        return launch_pdl(rpa_prefill_tc8<D, KT>, l.grid, kThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 
-}  // namespace
-
-cudaError_t prefill_tc8_prepare(int D, int* bps) {
-    if (D == 128) return Tc8Kern<128>::prepare(bps);
-    if (D == 256) return Tc8Kern<256>::prepare(bps);
+// 8-bit K/V (e4m3, e5m2, int8) at D 128 / 256
+template <int D, typename Op>
+cudaError_t tc8_dispatch_kt(int kt, Op op) {
+    if (kt == KT_E4M3) return op(Tc8Kern<D, KT_E4M3>{});
+    if (kt == KT_E5M2) return op(Tc8Kern<D, KT_E5M2>{});
+    if (kt == KT_I8) return op(Tc8Kern<D, KT_I8>{});
+    return cudaErrorInvalidValue;
+}
+template <typename Op>
+cudaError_t tc8_dispatch(int D, int kt, Op op) {
+    if (D == 128) return tc8_dispatch_kt<128>(kt, op);
+    if (D == 256) return tc8_dispatch_kt<256>(kt, op);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_prefill_tc8(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, const Launch& l) {
-    if (p.a.D == 128) return Tc8Kern<128>::launch(kvm, qm, p, l);
-    if (p.a.D == 256) return Tc8Kern<256>::launch(kvm, qm, p, l);
-    return cudaErrorInvalidValue;
+}  // namespace
+
+cudaError_t prefill_tc8_prepare(int D, int kt, int* bps) {
+    return tc8_dispatch(D, kt, [&](auto k) { return decltype(k)::prepare(bps); });
+}
+
+cudaError_t launch_prefill_tc8(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, int kt,
+                               const Launch& l) {
+    return tc8_dispatch(p.a.D, kt, [&](auto k) { return decltype(k)::launch(kvm, qm, p, l); });
 }
 
 }  // namespace rpa

@@ -39,8 +39,9 @@ EncodeTiledFn encoder() {
 
 // K/V pages viewed as a 2-D tensor: rows = N * page_size slots, each row the
 // 2 * Hkv * D elements of one slot (combined heads: K of head h at 2h, V at
-// 2h+1).  One box = BR slots x one 128-byte column block (bf16, 128-byte
-// swizzle) or BR slots x one whole D-byte row (fp8, no swizzle).
+// 2h+1).  One box = BR slots x one 128-byte column block (2-byte elements,
+// 128-byte swizzle) or BR slots x one whole D-byte row (1-byte elements, no
+// swizzle).  The copies move bits: a 2-byte map serves bf16 and f16 alike.
 int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR) {
     EncodeTiledFn fn = encoder();
     if (!fn) return -1;
@@ -58,8 +59,9 @@ int encode_kv_map(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, 
 // K/V pages viewed as a 3-D tensor for the decode gather: (row elements of one
 // 128-byte column block, slots, column blocks of a slot row).  One box = BR
 // slots of kv head h: its K column blocks then its V column blocks, landing in
-// shared memory as [2*D/64][BR][128 B] (bf16, 128-byte swizzle); for fp8 the
-// box is (D bytes, BR slots, K and V) landing as [2][BR][D] (no swizzle).
+// shared memory as [2*D/64][BR][128 B] (2-byte elements, 128-byte swizzle);
+// for 1-byte elements the box is (D bytes, BR slots, K and V) landing as
+// [2][BR][D] (no swizzle).
 // The slot dimension comes before the column-block dimension so that the BR
 // rows of one column block are consecutive 128-byte lines.
 int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int ps, int Hkv, int D, int BR) {
@@ -86,7 +88,8 @@ int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int
 }
 
 // q viewed as (D, Hq, T): one box = 64 elements x the G heads of a kv group x
-// Tt tokens, 128-byte swizzle; tokens past T read as zero.
+// Tt tokens, 128-byte swizzle; tokens past T read as zero.  q holds 2-byte
+// elements (bf16 or f16: the copy moves bits).
 int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt) {
     EncodeTiledFn fn = encoder();
     if (!fn) return -1;

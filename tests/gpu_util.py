@@ -4,17 +4,25 @@ import numpy as np
 
 import rpa_inputs as ri
 
-TOL = {"bf16": (2e-2, 2e-2), "fp8_e4m3": (6e-2, 6e-2)}  # (abs, rel)
+# (abs, rel) by K/V element type: the stated tolerance for bf16 K/V, and for fp8 K/V; f16 K/V
+# take the 16-bit one, e5m2 and int8 the 8-bit one
+TOL = {"bf16": (2e-2, 2e-2), "f16": (2e-2, 2e-2), "fp8_e4m3": (6e-2, 6e-2), "fp8_e5m2": (6e-2, 6e-2),
+       "int8": (6e-2, 6e-2)}
+
+
+def _torch_view(a, dtype):
+    import torch
+
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    if dtype == "f16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.float16)
+    return torch.from_numpy(a)  # float32, uint8 (fp8 bytes) or int8
 
 
 def to_dev(prob, dev="cuda:0"):
-    import torch
-
-    q = torch.from_numpy(prob.q.view(np.int16)).view(torch.bfloat16).to(dev)
-    if prob.kv_dtype == "bf16":
-        kv = torch.from_numpy(prob.kv_pages.view(np.int16)).view(torch.bfloat16).to(dev)
-    else:
-        kv = torch.from_numpy(prob.kv_pages).to(dev)
+    q = _torch_view(prob.q, getattr(prob, "q_dtype", "bf16")).to(dev)
+    kv = _torch_view(prob.kv_pages, prob.kv_dtype).to(dev)
     kvl = torch.from_numpy(np.ascontiguousarray(prob.kv_lens, np.int32)).to(dev)
     pi = torch.from_numpy(np.ascontiguousarray(prob.page_indices, np.int32)).to(dev)
     cu = torch.from_numpy(np.ascontiguousarray(prob.cu_q_lens, np.int32)).to(dev)
@@ -24,7 +32,10 @@ def to_dev(prob, dev="cuda:0"):
 def o_to_f64(o):
     import torch
 
-    return ri.bf16_bits_to_f32(o.view(torch.int16).cpu().numpy().view(np.uint16)).astype(np.float64)
+    if o.dtype == torch.float32:
+        return o.cpu().numpy().astype(np.float64)
+    bits = o.view(torch.int16).cpu().numpy().view(np.uint16)
+    return ri.values_f64(bits, "f16" if o.dtype == torch.float16 else "bf16")
 
 
 def run(prob, att=None, tensors=None, out=None):

@@ -119,6 +119,52 @@ def test_small_cases_all_rows(case):
     assert_close(got, oracle.forward(p), p.kv_dtype, f"small case {case}")
 
 
+# Element types (q / o, and K/V) on every kernel that serves them.  f16 K/V: f16 MMAs on the 8- and
+# 16-row decode tiles, the tensor-memory prefill (D 64, 128) and the warp-MMA prefill (D 256).
+# e5m2 and int8 K/V: the 8-bit tensor-memory prefill (D 128, 256; decode rows too, split pieces)
+# and the D 64 decode / warp-MMA prefill.  q of another type than the MMA operand type: rounded
+# into the workspace first (f32 q; f16 q with bf16 K/V; bf16 q with f16 K/V); f16 q with 8-bit K/V
+# read as it is.  o has q's type.
+DTYPE_CASES = [
+    (90, dict(num_seqs=10, max_q=150, max_kv=2500, num_q_heads=16, num_kv_heads=4, head_dim=128,
+              q_dtype="f16", kv_dtype="f16")),
+    (91, dict(num_seqs=8, max_q=60, max_kv=1500, num_q_heads=8, num_kv_heads=8, head_dim=64, page_size=32,
+              q_dtype="f16", kv_dtype="f16", soft_cap=20.0, sliding_window=300)),
+    (92, dict(num_seqs=9, max_q=3, max_kv=4000, num_q_heads=32, num_kv_heads=2, head_dim=128,
+              q_dtype="bf16", kv_dtype="f16")),
+    (93, dict(num_seqs=6, max_q=70, max_kv=900, num_q_heads=8, num_kv_heads=2, head_dim=256,
+              q_dtype="f16", kv_dtype="f16", sm_scale=1 / 16)),
+    (94, dict(num_seqs=10, max_q=120, max_kv=2000, num_q_heads=16, num_kv_heads=4, head_dim=128,
+              q_dtype="f16", kv_dtype="bf16", sinks=True)),
+    (95, dict(num_seqs=10, max_q=120, max_kv=2000, num_q_heads=16, num_kv_heads=4, head_dim=128,
+              q_dtype="f32", kv_dtype="bf16", sliding_window=500)),
+    (96, dict(num_seqs=12, max_q=40, max_kv=4000, num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+              kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.05, soft_cap=50.0, sm_scale=1 / 16)),
+    (97, dict(num_seqs=10, max_q=40, max_kv=3000, num_q_heads=16, num_kv_heads=4, head_dim=128, page_size=32,
+              q_dtype="f16", kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.06, sliding_window=700)),
+    (98, dict(num_seqs=12, max_q=40, max_kv=4000, num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+              kv_dtype="int8", k_scale=0.04, v_scale=0.04, sm_scale=1 / 16, sinks=True)),
+    (99, dict(num_seqs=10, max_q=40, max_kv=3000, num_q_heads=32, num_kv_heads=2, head_dim=128, page_size=16,
+              q_dtype="f32", kv_dtype="int8", k_scale=0.04, v_scale=0.03)),
+    (100, dict(num_seqs=8, max_q=30, max_kv=2500, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
+               kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.05, soft_cap=20.0)),
+    (101, dict(num_seqs=8, max_q=30, max_kv=2500, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
+               q_dtype="f16", kv_dtype="int8", k_scale=0.04, v_scale=0.04)),
+    (102, dict(num_seqs=8, max_q=30, max_kv=2500, num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+               q_dtype="f16", kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(DTYPE_CASES)), ids=[f"{c[1].get('q_dtype', 'bf16')}-"
+                                                               f"{c[1]['kv_dtype']}-seed{c[0]}" for c in DTYPE_CASES])
+def test_dtype_cases_all_rows(case):
+    seed, kw = DTYPE_CASES[case]
+    p = ri.random_small(seed, **kw)
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, f"dtype case {case}")
+
+
 def _sample_rows(p, n, seed, tile_tokens):
     """n random (token, q head) rows, plus, for every query tile of `tile_tokens` tokens of every
     sequence, its first and last token, each with the first and the last q head of a random kv
@@ -201,16 +247,19 @@ def test_page_placement_invariance_bit_identical():
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("kv_dtype,head_dim", [("bf16", 128), ("fp8_e4m3", 128), ("fp8_e4m3", 256)])
+@pytest.mark.parametrize("kv_dtype,head_dim", [("bf16", 128), ("fp8_e4m3", 128), ("fp8_e4m3", 256),
+                                               ("f16", 128), ("fp8_e5m2", 256), ("int8", 128)])
 def test_poisoned_tails_and_unused_pages(kv_dtype, head_dim):
-    extra = {} if kv_dtype == "bf16" else dict(k_scale=0.05, v_scale=0.05)
+    extra = {} if kv_dtype in ("bf16", "f16") else dict(k_scale=0.05, v_scale=0.05)
     p = ri.random_small(42, num_seqs=5, max_q=130, max_kv=500, num_q_heads=8, num_kv_heads=2,
                         head_dim=head_dim, extra_tokens=0, kv_dtype=kv_dtype, **extra)
     ref = oracle.forward(p)
     used = set()
     ps = p.page_size
-    # bf16: NaN in the tails, +inf in unused pages; e4m3fn has no inf, NaN is 0x7F
-    nan, inf = (0x7FC0, 0x7F80) if kv_dtype == "bf16" else (0x7F, 0x7F)
+    # NaN in the tails and +inf in the unused pages: bf16 0x7FC0 / 0x7F80, f16 0x7E00 / 0x7C00,
+    # e5m2 0x7F / 0x7C; e4m3fn has no inf (NaN 0x7F in both); int8 has neither (extremes)
+    nan, inf = {"bf16": (0x7FC0, 0x7F80), "f16": (0x7E00, 0x7C00), "fp8_e4m3": (0x7F, 0x7F),
+                "fp8_e5m2": (0x7F, 0x7C), "int8": (-128, 127)}[kv_dtype]
     for s in range(p.num_seqs):
         kl = int(p.kv_lens[s])
         used.update(int(x) for x in p.page_indices[s, : (kl + ps - 1) // ps])

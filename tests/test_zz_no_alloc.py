@@ -62,6 +62,9 @@ CASES = {
     # attention sinks read through the cfg's device pointer
     "sinks": (64, dict(num_seqs=9, max_q=60, max_kv=4000, num_q_heads=16, num_kv_heads=4, head_dim=128,
                        sinks=True)),
+    # f32 q rounded into the fixed array before the kernels read it; e5m2 K/V; f32 o
+    "f32_q_e5m2": (65, dict(num_seqs=8, max_q=40, max_kv=3000, num_q_heads=16, num_kv_heads=8, head_dim=256,
+                            q_dtype="f32", kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
 }
 
 

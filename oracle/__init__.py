@@ -13,7 +13,9 @@ walk, GQA head mapping, dequant); see the C file's header for the readings.
 
 Attention sinks follow the "from_qwen_ops.rs" page (flat_softmax_rows_at,
 ``sinks``): one extra logit per query head that starts the row maximum and
-joins the denominator with no value.
+joins the denominator with no value.  Latent attention (the same page, "The
+latent-attention family at whole-tile widths") reads a paged latent cache of
+one row per kv head: K is the row, V its first v_head_dim elements.
 
 Parity pins (tests/test_oracle_pins.py): brute-force dense attention on tiny
 unpaged inputs (fixed and random configurations, with and without sinks),
@@ -56,7 +58,7 @@ class OracleCfg(ctypes.Structure):
         ("has_v_scale", ctypes.c_int32), ("has_sliding_window", ctypes.c_int32),
         ("v_scale", ctypes.c_double), ("sliding_window", ctypes.c_int64),
         ("has_sinks", ctypes.c_int32), ("sinks", ctypes.c_void_p),
-        ("q_dtype", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32), ("latent", ctypes.c_int32), ("v_head_dim", ctypes.c_int64),
     ]
 
 # the oracle's own type codes (rpa_oracle.c: OracleKv, OracleQ)
@@ -107,6 +109,8 @@ def make_cfg(cfg: dict) -> OracleCfg:
         setattr(c, k, int(cfg[k]))
     c.kv_dtype = KV_CODES[cfg.get("kv_dtype", "bf16")]
     c.q_dtype = Q_CODES[cfg.get("q_dtype", "bf16")]
+    c.latent = 1 if cfg.get("kv_layout", "split") == "latent" else 0
+    c.v_head_dim = int(cfg.get("v_head_dim") or cfg["head_dim"])
     c.is_causal = 1 if cfg.get("is_causal", True) else 0
     c.sm_scale = float(cfg["sm_scale"])
     for name in ("soft_cap", "k_scale", "v_scale"):
@@ -148,11 +152,11 @@ class OracleError(RuntimeError):
 
 
 def forward(prob, nthreads: int = 0, return_threads: bool = False):
-    """All rows of ``o`` as float64 [num_q_tokens, num_q_heads, head_dim]."""
+    """All rows of ``o`` as float64 [num_q_tokens, num_q_heads, v_head_dim]."""
     lib = _load()
     c = make_cfg(prob.cfg_dict())
     q, kv, kvl, pi, cu = _arrays(prob)
-    out = np.zeros((prob.num_q_tokens, prob.num_q_heads, prob.head_dim), dtype=np.float64)
+    out = np.zeros((prob.num_q_tokens, prob.num_q_heads, prob.out_dim), dtype=np.float64)
     r = lib.rpa_oracle_forward(ctypes.byref(c), _ptr(q), _ptr(kv), _ptr(kvl), _ptr(pi), _ptr(cu),
                                int(prob.num_seqs), _ptr(out), int(nthreads))
     if r < 0:
@@ -161,12 +165,12 @@ def forward(prob, nthreads: int = 0, return_threads: bool = False):
 
 
 def rows(prob, rows_th: np.ndarray, nthreads: int = 0, return_threads: bool = False):
-    """Selected rows: ``rows_th`` int64 [n, 2] of (token, q head); returns [n, head_dim]."""
+    """Selected rows: ``rows_th`` int64 [n, 2] of (token, q head); returns [n, v_head_dim]."""
     lib = _load()
     c = make_cfg(prob.cfg_dict())
     q, kv, kvl, pi, cu = _arrays(prob)
     rr = np.ascontiguousarray(rows_th, dtype=np.int64).reshape(-1, 2)
-    out = np.zeros((rr.shape[0], prob.head_dim), dtype=np.float64)
+    out = np.zeros((rr.shape[0], prob.out_dim), dtype=np.float64)
     r = lib.rpa_oracle_rows(ctypes.byref(c), _ptr(q), _ptr(kv), _ptr(kvl), _ptr(pi), _ptr(cu),
                             int(prob.num_seqs), _ptr(rr), int(rr.shape[0]), _ptr(out), int(nthreads))
     if r < 0:

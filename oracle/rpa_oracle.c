@@ -36,6 +36,17 @@
  *  - dequant is exact fp64 x*scale (the page rounds it to the q dtype);
  *  - tokens not covered by [cu_q_lens[0], cu_q_lens[num_seqs]) are 0.
  *
+ * Latent attention over a paged latent cache (the "from_qwen_ops.rs" page,
+ * "The latent-attention family at whole-tile widths": a latent of 512 and a
+ * rope part of 64, sixteen or more heads of 576), when latent is set: every
+ * slot of a page holds one row of head_dim elements per kv head (kv_pages
+ * [total_num_pages, page_size, num_kv_heads, head_dim]); key j of kv head h is
+ * that whole row, and its value is the row's first v_head_dim elements:
+ *   K_j = dec(kv_pages[pg, sl, h, 0:head_dim]) * k_scale,
+ *   V_j = dec(kv_pages[pg, sl, h, 0:v_head_dim]) * v_scale,
+ * and o is [num_q_tokens, num_q_heads, v_head_dim].  Everything else (masks,
+ * soft cap, sinks, GQA grouping) is as above.
+ *
  * Element types ("ragged_paged.zig", Cfg: q_dtype f32 / f16 / bf16; kv_dtype
  * bf16 / f16 / f8e4m3fn / f8e5m2 / i8).  Every stored value is decoded exactly
  * to fp64 from its format's definition and used as it is: the page's casts to
@@ -76,6 +87,8 @@ typedef struct {
     int32_t has_sinks;
     const double* sinks; /* [num_q_heads] sink logits when has_sinks */
     int32_t q_dtype;     /* OracleQ: element type of q */
+    int32_t latent;      /* 1: latent cache layout (one row per kv head; V = its first v_head_dim) */
+    int64_t v_head_dim;  /* width of V and o (head_dim unless latent) */
 } OracleCfg;
 
 enum { OR_OK = 0, OR_INVALID_ARG = 1, OR_BAD_PAGE_INDEX = 4, OR_BAD_LENGTHS = 5 };
@@ -144,9 +157,14 @@ static int key_allowed(const OracleCfg* c, int64_t kv_len, int64_t p, int64_t j)
     return 1;
 }
 
-static double kv_elem(const OracleCfg* c, const void* kv, int64_t page, int64_t slot,
-                      int64_t comb_head, int64_t d) {
-    int64_t idx = ((page * c->page_size + slot) * (2 * c->num_kv_heads) + comb_head) * c->head_dim + d;
+/* Element d of the K row (is_v = 0) or V row (is_v = 1) of kv head h in a page slot. */
+static double kv_elem(const OracleCfg* c, const void* kv, int64_t page, int64_t slot, int64_t h, int is_v,
+                      int64_t d) {
+    int64_t idx;
+    if (c->latent) /* [N, ps, Hkv, D]: K and V share the row */
+        idx = ((page * c->page_size + slot) * c->num_kv_heads + h) * c->head_dim + d;
+    else /* [N, ps, 2 Hkv, D]: combined head 2h = K, 2h + 1 = V */
+        idx = ((page * c->page_size + slot) * (2 * c->num_kv_heads) + 2 * h + is_v) * c->head_dim + d;
     switch (c->kv_dtype) {
         case OKV_E4M3: return oracle_e4m3_to_f64(((const uint8_t*)kv)[idx]);
         case OKV_E5M2: return oracle_e5m2_to_f64(((const uint8_t*)kv)[idx]);
@@ -194,6 +212,7 @@ static void one_row(const OracleCfg* c, const void* q, const void* kv, const int
                     const int32_t* page_indices, const int32_t* cu_q_lens, int32_t s, int64_t t,
                     int64_t qh, double* out, double* x) {
     const int64_t D = c->head_dim;
+    const int64_t Dv = c->v_head_dim; /* width of V and of the output row */
     const int64_t G = c->num_q_heads / c->num_kv_heads;
     const int64_t h = qh / G;
     const int64_t q_len = (int64_t)cu_q_lens[s + 1] - cu_q_lens[s];
@@ -204,7 +223,7 @@ static void one_row(const OracleCfg* c, const void* q, const void* kv, const int
     const double vs = c->has_v_scale ? c->v_scale : 1.0;
     const int64_t qrow = (t * c->num_q_heads + qh) * D; /* element offset of the query row */
 
-    for (int64_t d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t d = 0; d < Dv; ++d) out[d] = 0.0;
     double xmax = -INFINITY;
     int any = 0;
     /* a sink logit starts the row maximum */
@@ -215,7 +234,7 @@ static void one_row(const OracleCfg* c, const void* q, const void* kv, const int
         int64_t slot = j % c->page_size;
         double dot = 0.0;
         for (int64_t d = 0; d < D; ++d)
-            dot += q_elem(c, q, qrow + d) * (kv_elem(c, kv, page, slot, 2 * h, d) * ks);
+            dot += q_elem(c, q, qrow + d) * (kv_elem(c, kv, page, slot, h, 0, d) * ks);
         double xj = c->sm_scale * dot;
         if (c->has_soft_cap) xj = c->soft_cap * tanh(xj / c->soft_cap);
         x[j] = xj;
@@ -232,9 +251,9 @@ static void one_row(const OracleCfg* c, const void* q, const void* kv, const int
         denom += w;
         int64_t page = page_indices[(int64_t)s * c->pages_per_seq + j / c->page_size];
         int64_t slot = j % c->page_size;
-        for (int64_t d = 0; d < D; ++d) out[d] += w * (kv_elem(c, kv, page, slot, 2 * h + 1, d) * vs);
+        for (int64_t d = 0; d < Dv; ++d) out[d] += w * (kv_elem(c, kv, page, slot, h, 1, d) * vs);
     }
-    for (int64_t d = 0; d < D; ++d) out[d] /= denom;
+    for (int64_t d = 0; d < Dv; ++d) out[d] /= denom;
 }
 
 static int32_t seq_of_token(const int32_t* cu_q_lens, int32_t num_seqs, int64_t t) {
@@ -262,7 +281,7 @@ typedef struct {
 static void* worker(void* arg) {
     Job* jb = (Job*)arg;
     const OracleCfg* c = jb->c;
-    const int64_t D = c->head_dim;
+    const int64_t D = c->v_head_dim; /* output row width */
     double* x = (double*)malloc(sizeof(double) * (size_t)(jb->max_kv > 0 ? jb->max_kv : 1));
     for (;;) {
         int64_t r = __atomic_fetch_add(&jb->next, 1, __ATOMIC_RELAXED);
@@ -305,12 +324,18 @@ static int run_job(Job* jb, int nthreads) {
     return started > 0 ? started : 1;
 }
 
-/* All rows: out[num_q_tokens, num_q_heads, head_dim] in fp64.
+/* All rows: out[num_q_tokens, num_q_heads, v_head_dim] in fp64.
  * Returns the number of threads used, or -code on invalid input. */
+static int cfg_ok(const OracleCfg* c) {
+    if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return 0;
+    if (c->v_head_dim < 1 || c->v_head_dim > c->head_dim || (!c->latent && c->v_head_dim != c->head_dim)) return 0;
+    return 1;
+}
+
 int rpa_oracle_forward(const OracleCfg* c, const void* q, const void* kv_pages,
                        const int32_t* kv_lens, const int32_t* page_indices, const int32_t* cu_q_lens,
                        int32_t num_seqs, double* out, int nthreads) {
-    if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return -OR_INVALID_ARG;
+    if (!cfg_ok(c)) return -OR_INVALID_ARG;
     int v = rpa_oracle_validate(c, kv_lens, page_indices, cu_q_lens, num_seqs);
     if (v) return -v;
     Job jb = {c, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, NULL,
@@ -318,11 +343,11 @@ int rpa_oracle_forward(const OracleCfg* c, const void* q, const void* kv_pages,
     return run_job(&jb, nthreads);
 }
 
-/* Selected rows only: rows = nrows (token, q head) int64 pairs; out[nrows, head_dim]. */
+/* Selected rows only: rows = nrows (token, q head) int64 pairs; out[nrows, v_head_dim]. */
 int rpa_oracle_rows(const OracleCfg* c, const void* q, const void* kv_pages, const int32_t* kv_lens,
                     const int32_t* page_indices, const int32_t* cu_q_lens, int32_t num_seqs,
                     const int64_t* rows, int64_t nrows, double* out, int nthreads) {
-    if (!c || c->num_kv_heads <= 0 || c->num_q_heads % c->num_kv_heads) return -OR_INVALID_ARG;
+    if (!cfg_ok(c)) return -OR_INVALID_ARG;
     int v = rpa_oracle_validate(c, kv_lens, page_indices, cu_q_lens, num_seqs);
     if (v) return -v;
     Job jb = {c, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, rows, nrows, out, 0, 0};

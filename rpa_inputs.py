@@ -12,6 +12,8 @@ Layouts follow the "ragged_paged.zig" page (kernel arguments of ``run``):
                    bf16 or f16 bits (uint16), fp8 e4m3fn / e5m2 bytes (uint8)
                    or int8; combined head 2h is K of kv head h, 2h+1 is V of
                    kv head h.
+                   Latent layout: [total_num_pages, page_size, num_kv_heads,
+                   head_dim], K = the row, V = its first v_head_dim elements.
 * ``kv_lens``      [max_num_seqs]                 int32
 * ``page_indices`` [max_num_seqs, pages_per_seq]  int32
 * ``cu_q_lens``    [max_num_seqs + 1]             int32
@@ -69,6 +71,8 @@ class Problem:
     mask_value: float = MASK_VALUE
     sinks: np.ndarray | None = field(default=None, repr=False)  # float32 [num_q_heads] sink logits
     q_dtype: str = "bf16"  # "bf16", "f16" or "f32" (o has the same type)
+    kv_layout: str = "split"  # "split" ([N, ps, 2*Hkv, D], K/V interleaved) or "latent" ([N, ps, Hkv, D])
+    v_head_dim: int | None = None  # latent layout: width of V and o (the first v_head_dim of each row)
     num_seqs: int = 0
     q: np.ndarray = field(default=None, repr=False)
     kv_pages: np.ndarray = field(default=None, repr=False)
@@ -86,7 +90,13 @@ class Problem:
             kv_dtype=self.kv_dtype, sm_scale=self.sm_scale,
             soft_cap=self.soft_cap, k_scale=self.k_scale, v_scale=self.v_scale,
             is_causal=self.is_causal, sliding_window=self.sliding_window,
-            mask_value=self.mask_value, sinks=self.sinks, q_dtype=self.q_dtype)
+            mask_value=self.mask_value, sinks=self.sinks, q_dtype=self.q_dtype,
+            kv_layout=self.kv_layout, v_head_dim=self.v_head_dim)
+
+    @property
+    def out_dim(self) -> int:
+        """Width of V and of the output rows."""
+        return self.v_head_dim if self.v_head_dim else self.head_dim
 
     @property
     def q_lens(self) -> np.ndarray:
@@ -194,6 +204,7 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
           v_scale=None, is_causal: bool = True, sliding_window=None,
           max_num_seqs: int | None = None, extra_tokens: int = 0,
           extra_pages: int = 0, name: str = "custom", sinks=None, q_dtype: str = "bf16",
+          kv_layout: str = "split", v_head_dim: int | None = None,
           rng_lengths: np.random.Generator | None = None) -> Problem:
     """Build a problem with the given lengths (already drawn by the caller).
 
@@ -232,7 +243,8 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
     Hq, Hkv, D = num_q_heads, num_kv_heads, head_dim
     q = np.empty((T, Hq, D), dtype=Q_STORAGE[q_dtype])
     _fill(q.reshape(-1), seed, 1, q_dtype)
-    kv = np.empty((total_num_pages, page_size, 2 * Hkv, D), dtype=KV_STORAGE[kv_dtype])
+    rows_per_slot = Hkv if kv_layout == "latent" else 2 * Hkv
+    kv = np.empty((total_num_pages, page_size, rows_per_slot, D), dtype=KV_STORAGE[kv_dtype])
     _fill(kv.reshape(-1), seed, 2, _KV_FILL[kv_dtype])
 
     if sm_scale is None:
@@ -247,7 +259,8 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
         max_num_seqs=max_num_seqs, pages_per_seq=pages_per_seq,
         kv_dtype=kv_dtype, sm_scale=float(sm_scale), soft_cap=soft_cap,
         k_scale=k_scale, v_scale=v_scale, is_causal=is_causal,
-        sliding_window=sliding_window, sinks=sinks, q_dtype=q_dtype, num_seqs=S, q=q, kv_pages=kv,
+        sliding_window=sliding_window, sinks=sinks, q_dtype=q_dtype, kv_layout=kv_layout,
+        v_head_dim=v_head_dim if kv_layout == "latent" else None, num_seqs=S, q=q, kv_pages=kv,
         kv_lens=kvl, page_indices=page_indices, cu_q_lens=cu, name=name)
 
 
@@ -336,16 +349,22 @@ def random_small(seed: int, *, num_seqs: int = 3, max_q: int = 9, max_kv: int = 
 def algorithmic_work(p: Problem, decode_rows: int = 16) -> dict:
     """Algorithmic bytes and FLOPs of one call (keys in the allowed band only).
 
-    bytes = sum_s n_kv(s) * 2*Hkv*D*kv_elt + 2 * T_used*Hq*D*q_elt + 4*(pages used + 2S + 1)
-    flops = sum_s sum_i 4*Hq*D*n_allowed(s, i)
+    bytes = sum_s n_kv(s) * row_bytes + T_used*Hq*(D + Dv)*q_elt + 4*(pages used + 2S + 1)
+    flops = sum_s sum_i 2*Hq*(D + Dv)*n_allowed(s, i)
+
+    row_bytes = 2*Hkv*D*kv_elt (K and V rows), or Hkv*D*kv_elt for the latent layout (K and V
+    share the row); Dv = v_head_dim (= D except for the latent layout).
 
     The same sums split by sequence class are returned as ``decode`` and
     ``prefill`` (a sequence is decode-class when q_len * G <= decode_rows),
     so that each attention kernel is charged with the work it does.
     """
+    Hq, Hkv, D = p.num_q_heads, p.num_kv_heads, p.head_dim
     kv_elt = KV_ELT[p.kv_dtype]
     q_elt = 4 if p.q_dtype == "f32" else 2  # q and o
-    Hq, Hkv, D = p.num_q_heads, p.num_kv_heads, p.head_dim
+    Dv = p.out_dim
+    # bytes of one key's cache rows: K and V rows of every kv head, or (latent) the one shared row
+    row_bytes = (Hkv * D if p.kv_layout == "latent" else 2 * Hkv * D) * kv_elt
     G = Hq // Hkv
     sw = p.sliding_window
     part = {"decode": [0, 0, 0, 0], "prefill": [0, 0, 0, 0]}  # bytes, pairs, pages, tokens
@@ -360,15 +379,16 @@ def algorithmic_work(p: Problem, decode_rows: int = 16) -> dict:
         lo = np.maximum(pos - sw + 1, 0) if sw else np.zeros(ql, np.int64)
         n_allowed = np.maximum(hi - lo, 0)
         c = part["decode" if ql * G <= decode_rows else "prefill"]
-        c[0] += (int(hi.max()) - int(lo.min())) * 2 * Hkv * D * kv_elt + 2 * ql * Hq * D * q_elt
+        c[0] += (int(hi.max()) - int(lo.min())) * row_bytes + ql * Hq * (D + Dv) * q_elt
         c[1] += int(n_allowed.sum())
         c[2] += (kl + p.page_size - 1) // p.page_size
         c[3] += ql
     out = {}
+    fpp = 2 * Hq * (D + Dv)  # FLOPs of one (query, key) pair over all q heads: QK^T and PV
     for k, (b, pairs, pages, toks) in part.items():
-        out[k] = dict(bytes=b + 4 * pages, flops=4 * Hq * D * pairs, q_tokens=toks)
+        out[k] = dict(bytes=b + 4 * pages, flops=fpp * pairs, q_tokens=toks)
     t_used = int(p.cu_q_lens[p.num_seqs])
     byts = out["decode"]["bytes"] + out["prefill"]["bytes"] + 4 * (2 * p.num_seqs + 1)
-    pairs = (out["decode"]["flops"] + out["prefill"]["flops"]) // (4 * Hq * D)
-    return dict(bytes=byts, flops=4 * Hq * D * pairs, exps=Hq * pairs, q_tokens=t_used,
+    pairs = (out["decode"]["flops"] + out["prefill"]["flops"]) // fpp
+    return dict(bytes=byts, flops=fpp * pairs, exps=Hq * pairs, q_tokens=t_used,
                 decode=out["decode"], prefill=out["prefill"])

@@ -21,7 +21,8 @@ MUTATIONS = [
     ("causal edge", "c->is_causal && j > p", "c->is_causal && j >= p"),
     ("query position", "const int64_t p = kv_len - q_len + i;", "const int64_t p = kv_len - q_len + i - 1;"),
     ("dropped sm_scale", "double xj = c->sm_scale * dot;", "double xj = dot;"),
-    ("K read from the V head", "kv_elem(c, kv, page, slot, 2 * h, d) * ks", "kv_elem(c, kv, page, slot, 2 * h + 1, d) * ks"),
+    ("K read from the V head", "kv_elem(c, kv, page, slot, h, 0, d) * ks", "kv_elem(c, kv, page, slot, h, 1, d) * ks"),
+    ("split V head off by one", "+ 2 * h + is_v) * c->head_dim + d;", "+ 2 * h + 2 * is_v) * c->head_dim + d;"),
     ("GQA map strided", "const int64_t h = qh / G;", "const int64_t h = qh % c->num_kv_heads;"),
     ("dropped k_scale", "const double ks = c->has_k_scale ? c->k_scale : 1.0;", "const double ks = 1.0;"),
     ("dropped v_scale", "const double vs = c->has_v_scale ? c->v_scale : 1.0;", "const double vs = 1.0;"),
@@ -39,6 +40,10 @@ MUTATIONS = [
      "case OKV_I8: return (double)((const uint8_t*)kv)[idx];"),
     ("f32 q read as bf16", "case OQ_F32: return f32_to_f64((const float*)q + idx);",
      "case OQ_F32: return oracle_bf16_to_f64(((const uint16_t*)q)[idx]);"),
+    ("latent V from the end of the row", "for (int64_t d = 0; d < Dv; ++d) out[d] += w * (kv_elem(c, kv, page, slot, h, 1, d) * vs);",
+     "for (int64_t d = 0; d < Dv; ++d) out[d] += w * (kv_elem(c, kv, page, slot, h, 1, d + D - Dv) * vs);"),
+    ("latent rows strided like the split layout", "idx = ((page * c->page_size + slot) * c->num_kv_heads + h) * c->head_dim + d;",
+     "idx = ((page * c->page_size + slot) * c->num_kv_heads + 2 * h) * c->head_dim + d;"),
     ("sink left out of the denominator", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);", ""),
     ("sink of the wrong head", "if (c->has_sinks) denom += exp(c->sinks[qh] - xmax);",
      "if (c->has_sinks) denom += exp(c->sinks[qh / G] - xmax);"),
@@ -57,6 +62,9 @@ def _pin_calls():
               for a, w in [(True, None), (True, 3), (True, 7), (False, None), (False, 4)]]
     calls += [lambda v=v: pins.test_zero_query_mean_shrunk_by_a_sink(v) for v in (0.0, math.log(3.0), -2.5)]
     calls += [pins.test_very_negative_sink_changes_nothing]
+    calls += [lambda c=c: pins.test_latent_oracle_equals_dense_brute_force(c) for c in range(len(pins.LATENT_CASES))]
+    calls += [pins.test_latent_equals_split_layout_with_padded_values,
+              pins.test_latent_zero_query_averages_the_value_part]
     calls += [pins.test_two_keys_closed_form_weights, pins.test_window_one_selects_own_position,
               pins.test_uniform_v_gives_v, pins.test_single_key_sequence,
               pins.test_decode_equals_last_prefill_row, pins.test_gqa_equals_mha_with_repeated_kv,

@@ -11,6 +11,9 @@ mis-decoded fp8 code) fails at least one of them:
   dense score matrix) on tiny unpaged inputs scattered into shuffled pages;
 * closed forms: uniform V, a single allowed key, one-key sequences, zero-query
   means, two-key weights, zero-query means shrunk by a sink (n / (n + e^s));
+* latent attention over a paged latent cache (the "from_qwen_ops.rs" page, "The
+  latent-attention family at whole-tile widths"): a dense brute force, the
+  split layout with zero-padded values, and zero-query means;
 * attention sinks (the "from_qwen_ops.rs" page, flat_softmax_rows_at): the
   brute force takes the sink as one more always-allowed column with a zero
   value row; a very negative sink changes nothing;
@@ -128,6 +131,76 @@ def brute(prob, dense, capped_form=False):
             # a row with no allowed key is zero (with a sink too: the sink carries no value)
             o[~allowed.any(axis=1)] = 0.0
             out[q0:q0 + ql, qh, :] = o
+    return out
+
+
+def dense_latent_problem(rng, q_lens, kv_lens, Hq, Hkv, D, Dv, ps, **knobs):
+    """A latent-layout problem: one row of D elements per kv head and slot, drawn here and
+    scattered into shuffled pages.  Returns (problem, dense) with dense[s] = (Q [ql,Hq,D],
+    R [kl,Hkv,D]) as float64 values of the stored bits."""
+    S = len(q_lens)
+    npages = [(k + ps - 1) // ps for k in kv_lens]
+    N = sum(npages) + 2
+    P = max(npages + [1])
+    perm = rng.permutation(N)
+    page_indices = np.zeros((S, P), np.int32)
+    off = 0
+    for s in range(S):
+        page_indices[s, :npages[s]] = perm[off:off + npages[s]]
+        page_indices[s, npages[s]:] = perm[-1]
+        off += npages[s]
+    T = int(sum(q_lens))
+    q = ri.f32_to_bf16_bits(rng.standard_normal((T, Hq, D)).astype(np.float32))
+    kv = ri.f32_to_bf16_bits(rng.standard_normal((N, ps, Hkv, D)).astype(np.float32))
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    if knobs.get("sinks") is not None:
+        knobs["sinks"] = np.asarray(knobs["sinks"], np.float32)
+    prob = Problem(num_q_tokens=T, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D,
+                   total_num_pages=N, page_size=ps, max_num_seqs=S, pages_per_seq=P,
+                   kv_dtype="bf16", kv_layout="latent", v_head_dim=Dv, num_seqs=S, q=q, kv_pages=kv,
+                   kv_lens=np.asarray(kv_lens, np.int32), page_indices=page_indices,
+                   cu_q_lens=cu, sm_scale=knobs.pop("sm_scale", 1.0 / math.sqrt(D)), **knobs)
+    qf = ri.bf16_bits_to_f32(q).astype(np.float64)
+    kvf = ri.bf16_bits_to_f32(kv).astype(np.float64)
+    dense = []
+    for s in range(S):
+        kl = kv_lens[s]
+        R = kvf[page_indices[s, np.arange(kl) // ps], np.arange(kl) % ps]
+        dense.append((qf[cu[s]:cu[s + 1]], R))
+    return prob, dense
+
+
+def brute_latent(prob, dense):
+    """Dense softmax attention over latent rows: K = the row, V = its first v_head_dim."""
+    Dv = prob.v_head_dim
+    split = [(Q, R, R[:, :, :Dv]) for Q, R in dense]
+    out = np.zeros((prob.num_q_tokens, prob.num_q_heads, Dv))
+    G = prob.num_q_heads // prob.num_kv_heads
+    for s, (Q, K, V) in enumerate(split):
+        ql, kl = Q.shape[0], K.shape[0]
+        q0 = prob.cu_q_lens[s]
+        pos = kl - ql + np.arange(ql)[:, None]
+        col = np.arange(kl)[None, :]
+        allowed = np.ones((ql, kl), bool)
+        if prob.is_causal:
+            allowed &= col <= pos
+        if prob.sliding_window is not None:
+            allowed &= ~(pos - prob.sliding_window >= col)
+        for qh in range(prob.num_q_heads):
+            h = qh // G
+            x = prob.sm_scale * (Q[:, qh, :] @ K[:, h, :].T)
+            if prob.soft_cap is not None:
+                x = prob.soft_cap * np.tanh(x / prob.soft_cap)
+            x = np.where(allowed, x, -np.inf)
+            Vh = V[:, h, :]
+            allowed_s = allowed
+            if prob.sinks is not None:
+                x = np.concatenate([x, np.full((ql, 1), float(prob.sinks[qh]))], axis=1)
+                allowed_s = np.concatenate([allowed, np.ones((ql, 1), bool)], axis=1)
+                Vh = np.concatenate([Vh, np.zeros((1, Dv))], axis=0)
+            m = x.max(axis=1, keepdims=True)
+            w = np.where(allowed_s, np.exp(x - m), 0.0)
+            out[q0:q0 + ql, qh, :] = (w @ Vh) / w.sum(axis=1, keepdims=True)
     return out
 
 
@@ -394,6 +467,55 @@ def test_single_key_sequence():
     for s, (Q, K, V) in enumerate(dense):
         for qh in range(4):
             close(o[s, qh], V[0, qh // 2], 1e-14)
+
+
+# ------------------------------------------------------------------ latent attention
+LATENT_CASES = [
+    dict(q_lens=[1, 5, 9], kv_lens=[17, 40, 30], Hq=8, Hkv=1, D=48, Dv=32, ps=8),
+    dict(q_lens=[3, 1], kv_lens=[20, 33], Hq=4, Hkv=2, D=40, Dv=24, ps=4, sliding_window=6, soft_cap=3.0,
+         sinks=[0.5, -1.0, 2.0, 0.0]),
+    dict(q_lens=[4, 2], kv_lens=[9, 13], Hq=16, Hkv=1, D=72, Dv=64, ps=16, is_causal=False, sm_scale=0.1),
+]
+
+
+@pytest.mark.parametrize("case", range(len(LATENT_CASES)))
+def test_latent_oracle_equals_dense_brute_force(case):
+    kw = dict(LATENT_CASES[case])
+    rng = np.random.default_rng(300 + case)
+    prob, dense = dense_latent_problem(rng, kw.pop("q_lens"), kw.pop("kv_lens"), kw.pop("Hq"), kw.pop("Hkv"),
+                                       kw.pop("D"), kw.pop("Dv"), kw.pop("ps"), **kw)
+    close(oracle.forward(prob), brute_latent(prob, dense))
+
+
+def test_latent_equals_split_layout_with_padded_values():
+    """The latent layout is the split layout whose K row is the latent row and whose V row is the
+    latent row's first v_head_dim elements followed by zeros: the split output's first v_head_dim
+    columns equal the latent output bit for bit, and its other columns are zero."""
+    rng = np.random.default_rng(310)
+    Dv = 24
+    lat, _ = dense_latent_problem(rng, [3, 6], [15, 26], 6, 2, 40, Dv, 4, soft_cap=4.0, sliding_window=9)
+    o_lat = oracle.forward(lat)
+    kvl = lat.kv_pages  # [N, ps, Hkv, D]
+    split_kv = np.zeros(kvl.shape[:2] + (2 * kvl.shape[2], kvl.shape[3]), kvl.dtype)
+    split_kv[:, :, 0::2] = kvl
+    split_kv[:, :, 1::2, :Dv] = kvl[:, :, :, :Dv]
+    sp = Problem(**{**lat.__dict__, "kv_layout": "split", "v_head_dim": None, "kv_pages": split_kv})
+    o_sp = oracle.forward(sp)
+    assert np.array_equal(o_sp[:, :, :Dv], o_lat)
+    assert (o_sp[:, :, Dv:] == 0).all()
+
+
+def test_latent_zero_query_averages_the_value_part():
+    """q = 0: every allowed key weighs 1, so o is the mean of the allowed rows' first v_head_dim."""
+    rng = np.random.default_rng(311)
+    prob, dense = dense_latent_problem(rng, [4], [11], 2, 1, 32, 16, 4)
+    prob.q = np.zeros_like(prob.q)
+    o = oracle.forward(prob)
+    Q, R = dense[0]
+    for i in range(4):
+        p = 11 - 4 + i
+        for qh in range(2):
+            close(o[i, qh], R[:p + 1, 0, :16].mean(axis=0), 1e-13)
 
 
 # ------------------------------------------------------------------ invariants

@@ -21,6 +21,8 @@ def _torch_view(a, dtype):
 
 
 def to_dev(prob, dev="cuda:0"):
+    import torch
+
     q = _torch_view(prob.q, getattr(prob, "q_dtype", "bf16")).to(dev)
     kv = _torch_view(prob.kv_pages, prob.kv_dtype).to(dev)
     kvl = torch.from_numpy(np.ascontiguousarray(prob.kv_lens, np.int32)).to(dev)

@@ -57,6 +57,8 @@ DESCR = {
     "decode_quarter": "64 seqs x q_len 1, kv_len~U[512,8192], Hq 32 / Hkv 8, D 128, page 16, bf16",
     "fp8_window_quarter": "the first 32 seqs of fp8_window (q_len~U{1..64} kv_len~U[256,16384]), "
                           "Hq 16 / Hkv 8, D 256, page 16, fp8 e4m3 K/V, softcap 50, window 4096",
+    "mla_decode": "latent attention decode: 128 seqs x q_len 1, kv_len~U[1024,8192], Hq 16 on one latent "
+                  "kv head, rows 576 (V 512), page 64, bf16",
 }
 
 
@@ -387,7 +389,7 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
     res = {
         "workload": f"{name}: {DESCR[name]}", "value": value, "unit": "tokens/s", "steps": K,
         "warmup": max(3, warmup), "ms_per_step": ms_step,
-        "dtype": "bf16" if prob.kv_dtype == "bf16" else "f16 (e4m3 K/V converted exactly)",
+        "dtype": "bf16" if prob.kv_dtype == "bf16" else "f16 (8-bit K/V converted exactly)",
         "config": {"workload": f"{name}: {DESCR[name]}", "num_seqs": prob.num_seqs, "q_tokens": tokens,
                    "kv_tokens": int(prob.kv_lens[: prob.num_seqs].sum()),
                    "l2": f"no flush: inputs larger than L2 (K/V cache {kv_gb:.2f} GB)"
@@ -436,7 +438,7 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
 
 # the other workloads of the default line: (name, timed steps); each K/V cache is far above L2
 # except long_prefill's (134 MB, about L2-sized)
-SIDE_WORKLOADS = (("mixed", 300), ("fp8_window", 300), ("long_prefill", 100))
+SIDE_WORKLOADS = (("mixed", 300), ("fp8_window", 300), ("long_prefill", 100), ("mla_decode", 300))
 
 
 def main():
@@ -496,7 +498,7 @@ def main():
 if __name__ == "__main__":
     a0 = parse()
     if a0.all and a0.impl == "ours":
-        for w in ("decode", "mixed", "fp8_window", "long_prefill"):
+        for w in ("decode", "mixed", "fp8_window", "long_prefill", "mla_decode"):
             sys.argv = [sys.argv[0], "--workload", w, "--steps", str(a0.steps), "--warmup",
                         str(a0.warmup), "--no-cpu-baseline", "--e2e-steps", "0", "--no-side-workloads"]
             main()

@@ -96,9 +96,9 @@ typedef struct RpaCfg {
     int32_t is_causal;       /* 1 = causal (default of the page) */
     int32_t has_sliding_window;
     int32_t has_sinks;       /* 1: attention sinks, read from `sinks` */
-    int32_t kv_layout;       /* RpaKvLayout: RPA_KV_SPLIT (the page's layout, default) */
+    int32_t kv_layout;       /* RpaKvLayout: RPA_KV_SPLIT (the page's layout, default) or RPA_KV_LATENT */
     int32_t reserved;        /* set to 0 */
-    int64_t v_head_dim;      /* 0 (V rows are head_dim wide, the page's layout) */
+    int64_t v_head_dim;      /* RPA_KV_SPLIT: 0 or head_dim.  RPA_KV_LATENT: the width of V and o */
     const float* sinks;      /* when has_sinks: device, [num_q_heads] fp32, 4-byte aligned; the
                                 sink logit of each query head (the "from_qwen_ops.rs" page,
                                 flat_softmax_rows_at, `sinks`): it starts the row maximum and
@@ -109,9 +109,20 @@ typedef struct RpaCfg {
                                 stay valid while those calls run. */
 } RpaCfg;
 
-/* K/V page layouts.  RPA_KV_SPLIT: kv_pages[total_num_pages, page_size,
- * 2*Hkv, D], combined head 2h = K of kv head h, 2h+1 = V (the page's). */
-typedef enum RpaKvLayout { RPA_KV_SPLIT = 0 } RpaKvLayout;
+/* K/V page layouts.
+ * RPA_KV_SPLIT:  kv_pages[total_num_pages, page_size, 2*Hkv, head_dim], combined
+ *                head 2h = K of kv head h, 2h+1 = its V ("ragged_paged.zig").
+ * RPA_KV_LATENT: latent attention over a paged latent cache (the
+ *                "from_qwen_ops.rs" page, "The latent-attention family at
+ *                whole-tile widths"): kv_pages[total_num_pages, page_size,
+ *                Hkv, head_dim], one latent row per kv head and slot; K is the
+ *                whole row and V its first v_head_dim elements, so q is
+ *                [num_q_tokens, Hq, head_dim] and o [num_q_tokens, Hq,
+ *                v_head_dim].  Supported: head_dim 576 with v_head_dim 512 (a
+ *                512-wide latent and a 64-wide rope part), bf16 or f16 rows,
+ *                page_size a multiple of 8, Hq/Hkv at most 16 or a multiple of
+ *                16; any other choice gives RPA_ERR_UNSUPPORTED. */
+typedef enum RpaKvLayout { RPA_KV_SPLIT = 0, RPA_KV_LATENT = 1 } RpaKvLayout;
 
 typedef struct RpaHandle RpaHandle;
 
@@ -132,12 +143,14 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out);
  * kv_lens, page_indices, cu_q_lens, num_seqs, q, kv_pages and output o).
  *   q            device, [num_q_tokens, Hq, D] q_dtype, 16-byte aligned
  *   kv_pages     device, [total_num_pages, page_size, 2*Hkv, D] kv_dtype, 16-byte aligned
+ *                ([total_num_pages, page_size, Hkv, D] for RPA_KV_LATENT)
  *   kv_lens      device, int32 [max_num_seqs]
  *   page_indices device, int32 [max_num_seqs, pages_per_seq], row-major
  *   cu_q_lens    device, int32 [max_num_seqs + 1]
  *   num_seqs     host scalar, 0 <= num_seqs <= max_num_seqs (the page passes it
  *                as a one-element array)
- *   o            device, [num_q_tokens, Hq, D] q_dtype, 16-byte aligned, written in
+ *   o            device, [num_q_tokens, Hq, Dv] q_dtype (Dv = D, or v_head_dim for
+ *                RPA_KV_LATENT), 16-byte aligned, written in
  *                full: rows of tokens outside [cu_q_lens[0], cu_q_lens[num_seqs])
  *                are written as 0
  *   stream       cudaStream_t as void*
@@ -175,7 +188,7 @@ int rpa_get_status(RpaHandle* h, void* stream);
  * units, [9] 1 if units were sorted by cost, [10] decode CTAs given work, [11]
  * prefill CTAs given work, [12] SMs, [13] / [14] resident decode / prefill
  * CTAs per SM, [15] bit 0: decode and prefill ran concurrently, bit 1: decode units were
- * items of the prefill kernel (fp8 K/V on tensor memory).  items (host, may be NULL)
+ * items of the prefill-side kernel (8-bit K/V on tensor memory, or the latent layout).  items (host, may be NULL)
  * receives up to max_items decode items followed by the prefill items, 8
  * int32 each: seq, kv head, first query token of the sequence's tile (local),
  * tokens in the tile, first key, end key, partial slot (-1 = direct write),

@@ -22,6 +22,8 @@ from .binding import (  # noqa: F401
     RPA_ERR_NO_ALLOC_LIMIT,
     RPA_ERR_TIMEOUT,
     RPA_ERR_UNSUPPORTED,
+    RPA_KV_LATENT,
+    RPA_KV_SPLIT,
     RPA_OK,
     RPA_OPT_DECODE_SMS,
     RPA_OPT_PREFILL_SMS,

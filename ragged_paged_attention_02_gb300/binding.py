@@ -30,6 +30,9 @@ RPA_DT_F16 = 2
 RPA_DT_F32 = 3
 RPA_DT_FP8_E5M2 = 4
 RPA_DT_INT8 = 5
+RPA_KV_SPLIT = 0
+RPA_KV_LATENT = 1
+KV_LAYOUTS = {"split": RPA_KV_SPLIT, "latent": RPA_KV_LATENT}
 # dtype names of the configuration (q / o, and kv_pages)
 Q_DTYPES = {"bf16": RPA_DT_BF16, "f16": RPA_DT_F16, "f32": RPA_DT_F32}
 KV_DTYPES = {"bf16": RPA_DT_BF16, "f16": RPA_DT_F16, "fp8_e4m3": RPA_DT_FP8_E4M3, "fp8_e5m2": RPA_DT_FP8_E5M2,
@@ -141,7 +144,7 @@ def _sinks_pointer(sinks, host_ok):
 def make_cfg(*, num_q_tokens, num_q_heads, num_kv_heads, head_dim, total_num_pages, page_size,
              max_num_seqs, pages_per_seq, sm_scale, kv_dtype="bf16", soft_cap=None, k_scale=None,
              v_scale=None, is_causal=True, sliding_window=None, mask_value=MASK_VALUE, sinks=None,
-             q_dtype="bf16", _host_ok=False, **_ignored) -> RpaCfg:
+             q_dtype="bf16", kv_layout="split", v_head_dim=None, _host_ok=False, **_ignored) -> RpaCfg:
     c = RpaCfg()
     c.num_q_tokens, c.num_q_heads, c.num_kv_heads = int(num_q_tokens), int(num_q_heads), int(num_kv_heads)
     c.head_dim, c.total_num_pages, c.page_size = int(head_dim), int(total_num_pages), int(page_size)
@@ -158,6 +161,8 @@ def make_cfg(*, num_q_tokens, num_q_heads, num_kv_heads, head_dim, total_num_pag
     c.has_sliding_window, c.sliding_window = (0, 0) if sliding_window is None else (1, int(sliding_window))
     ptr = _sinks_pointer(sinks, _host_ok)
     c.has_sinks, c.sinks = (0, None) if ptr is None else (1, ptr)
+    c.kv_layout = KV_LAYOUTS[kv_layout]
+    c.v_head_dim = 0 if v_head_dim is None else int(v_head_dim)
     return c
 
 
@@ -182,10 +187,12 @@ class RaggedPagedAttention:
       q            [num_q_tokens, Hq, D] bfloat16, float16 or float32 (q_dtype)
       kv_pages     [total_num_pages, page_size, 2*Hkv, D] bfloat16 / float16, or
                    one-byte elements for fp8 (e4m3, e5m2) and int8 K/V
+                   ([total_num_pages, page_size, Hkv, D] for kv_layout="latent")
       kv_lens      [max_num_seqs] int32
       page_indices [max_num_seqs, pages_per_seq] int32
       cu_q_lens    [max_num_seqs + 1] int32
-    and returns o [num_q_tokens, Hq, D] of q's dtype.  ``sinks`` (optional) is a
+    and returns o [num_q_tokens, Hq, Dv] of q's dtype (Dv = D, or v_head_dim for
+    kv_layout="latent").  ``sinks`` (optional) is a
     float32 [Hq] array or CUDA tensor of attention-sink logits.
     """
 
@@ -224,9 +231,11 @@ class RaggedPagedAttention:
         qt = {RPA_DT_BF16: torch.bfloat16, RPA_DT_F16: torch.float16, RPA_DT_F32: torch.float32}[c.q_dtype]
         if q.dtype != qt or tuple(q.shape) != (T, Hq, D) or not q.is_contiguous():
             raise ValueError(f"q must be a contiguous {qt} tensor [num_q_tokens, Hq, D]")
-        if out.dtype != qt or tuple(out.shape) != (T, Hq, D) or not out.is_contiguous():
-            raise ValueError(f"out must be a contiguous {qt} tensor [num_q_tokens, Hq, D]")
-        want_kv = (c.total_num_pages, c.page_size, 2 * c.num_kv_heads, D)
+        Dv = self.out_dim
+        if out.dtype != qt or tuple(out.shape) != (T, Hq, Dv) or not out.is_contiguous():
+            raise ValueError(f"out must be a contiguous {qt} tensor [num_q_tokens, Hq, {Dv}]")
+        rows = c.num_kv_heads if c.kv_layout == RPA_KV_LATENT else 2 * c.num_kv_heads
+        want_kv = (c.total_num_pages, c.page_size, rows, D)
         if tuple(kv_pages.shape) != want_kv or not kv_pages.is_contiguous():
             raise ValueError(f"kv_pages must be contiguous {want_kv}")
         if c.kv_dtype == RPA_DT_BF16 and kv_pages.dtype != torch.bfloat16:
@@ -241,11 +250,14 @@ class RaggedPagedAttention:
             if t.dtype != torch.int32 or tuple(t.shape) != shape or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous int32 tensor {shape}")
 
-    def forward(self, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, out=None, stream=None):
-        import torch
+    @property
+    def out_dim(self) -> int:
+        """Width of o: head_dim, or v_head_dim for the latent layout."""
+        return int(self._c.v_head_dim) if self._c.kv_layout == RPA_KV_LATENT else int(self._c.head_dim)
 
+    def forward(self, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs, out=None, stream=None):
         if out is None:
-            out = torch.empty_like(q)
+            out = q.new_empty((q.shape[0], q.shape[1], self.out_dim))
         self._check(q, kv_pages, kv_lens, page_indices, cu_q_lens, out)
         for t in (q, kv_pages, kv_lens, page_indices, cu_q_lens, out):
             if not t.is_cuda:

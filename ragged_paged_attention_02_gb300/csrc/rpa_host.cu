@@ -137,11 +137,22 @@ int rpa_validate_cfg(const RpaCfg* c) {
     if (c->has_sliding_window && c->sliding_window < 1) return RPA_ERR_INVALID_ARG;
     if (c->has_sinks && (!c->sinks || !aligned(c->sinks, 4))) return RPA_ERR_INVALID_ARG;
     if (c->reserved != 0) return RPA_ERR_INVALID_ARG;
-    if (c->kv_layout != RPA_KV_SPLIT || c->v_head_dim != 0) return RPA_ERR_UNSUPPORTED;
     if (c->num_q_heads % c->num_kv_heads) return RPA_ERR_UNSUPPORTED;
-    if (c->num_q_heads / c->num_kv_heads > kPfRows) return RPA_ERR_UNSUPPORTED;
-    if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return RPA_ERR_UNSUPPORTED;
-    if (c->page_size % 4) return RPA_ERR_UNSUPPORTED;  // page runs of the gather are >= 4 slots
+    const int64_t G = c->num_q_heads / c->num_kv_heads;
+    if (c->kv_layout == RPA_KV_LATENT) {
+        // latent rows of 576 with 512-wide values; 2-byte rows; page runs of >= 8 slots (so that
+        // every run lands on a 1 KB boundary); blocks of <= 16 query heads
+        if (c->head_dim != kMlaDqk || c->v_head_dim != kMlaDv) return RPA_ERR_UNSUPPORTED;
+        if (c->kv_dtype != RPA_DT_BF16 && c->kv_dtype != RPA_DT_F16) return RPA_ERR_UNSUPPORTED;
+        if (c->page_size % 8) return RPA_ERR_UNSUPPORTED;
+        if (G > kMlaRows && G % kMlaRows) return RPA_ERR_UNSUPPORTED;
+    } else {
+        if (c->kv_layout != RPA_KV_SPLIT) return RPA_ERR_UNSUPPORTED;
+        if (c->v_head_dim != 0 && c->v_head_dim != c->head_dim) return RPA_ERR_UNSUPPORTED;
+        if (G > kPfRows) return RPA_ERR_UNSUPPORTED;
+        if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return RPA_ERR_UNSUPPORTED;
+        if (c->page_size % 4) return RPA_ERR_UNSUPPORTED;  // page runs of the gather are >= 4 slots
+    }
     if (c->q_dtype != RPA_DT_BF16 && c->q_dtype != RPA_DT_F16 && c->q_dtype != RPA_DT_F32) return RPA_ERR_UNSUPPORTED;
     if (c->kv_dtype != RPA_DT_BF16 && c->kv_dtype != RPA_DT_F16 && c->kv_dtype != RPA_DT_FP8_E4M3 &&
         c->kv_dtype != RPA_DT_FP8_E5M2 && c->kv_dtype != RPA_DT_INT8)
@@ -317,11 +328,12 @@ int rpa_forward_host(RpaHandle* h, const void* q_host, const void* kv_pages, con
     if (num_seqs < 0 || num_seqs > c.max_num_seqs) return RPA_ERR_INVALID_ARG;
     DeviceGuard g(h->device);
     if (!g.ok) return RPA_ERR_CUDA;
-    const size_t qb = (size_t)c.num_q_tokens * c.num_q_heads * c.head_dim * q_elt_bytes(c.q_dtype);  // q and o
+    const size_t qb = (size_t)c.num_q_tokens * c.num_q_heads * c.head_dim * q_elt_bytes(c.q_dtype);
+    const size_t ob = (size_t)c.num_q_tokens * c.num_q_heads * h->ks.Dv * q_elt_bytes(c.q_dtype);
     const size_t kb = (size_t)c.max_num_seqs * sizeof(int32_t);
     const size_t pb = (size_t)c.max_num_seqs * c.pages_per_seq * sizeof(int32_t);
     const size_t cb = (size_t)(c.max_num_seqs + 1) * sizeof(int32_t);
-    const size_t o_q = 0, o_o = align256(qb), o_k = o_o + align256(qb), o_p = o_k + align256(kb),
+    const size_t o_q = 0, o_o = align256(qb), o_k = o_o + align256(ob), o_p = o_k + align256(kb),
                  o_c = o_p + align256(pb), total = o_c + align256(cb);
     if (!h->stage) {
         if (cudaMalloc(&h->stage, total) != cudaSuccess) {
@@ -341,7 +353,7 @@ int rpa_forward_host(RpaHandle* h, const void* q_host, const void* kv_pages, con
                         reinterpret_cast<const int32_t*>(s + o_p), reinterpret_cast<const int32_t*>(s + o_c),
                         num_seqs, qb ? s + o_o : nullptr, stream);
     if (r != RPA_OK) return r;
-    if (qb && cudaMemcpyAsync(o_host, s + o_o, qb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (ob && cudaMemcpyAsync(o_host, s + o_o, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return RPA_ERR_CUDA;
     return RPA_OK;
 }
@@ -383,7 +395,7 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[12] = h->ks.sms;
     info[13] = h->ks.dec_bps;
     info[14] = h->ks.pf_bps;
-    info[15] = h->concurrent | (h->ks.tc8 << 1);
+    info[15] = h->concurrent | ((h->ks.tc8 | h->ks.mla) << 1);
     if (items && max_items > 0) {
         const int64_t nd = ctrl[kNumDecItems] < max_items ? ctrl[kNumDecItems] : max_items;
         const int64_t np = ctrl[kNumPfItems] < max_items - nd ? ctrl[kNumPfItems] : max_items - nd;

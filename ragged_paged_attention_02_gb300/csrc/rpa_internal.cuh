@@ -52,6 +52,10 @@ __host__ __device__ constexpr bool kt_f16_mma(int kt) { return kt != KT_BF16; } 
 enum OutType : int { OT_BF16 = 0, OT_F16 = 1, OT_F32 = 2 };
 
 constexpr int kDecRows = 16;       // rows of a decode tile (one m16 MMA tile)
+// latent attention: row width, value width, query rows of a work item
+constexpr int kMlaDqk = 576;
+constexpr int kMlaDv = 512;
+constexpr int kMlaRows = 16;
 constexpr int kPfRows = 64;        // rows of a prefill tile (4 warps x 16)
 constexpr int kDecWaves = 4;       // target decode items per resident CTA
 constexpr int kMinChunk = 512;     // smallest split-KV piece (keys)
@@ -192,6 +196,9 @@ cudaError_t prefill_tc_prepare(int D, int kt, int* blocks_per_sm);
 cudaError_t launch_prefill_tc8(const CUtensorMap& kvm_runs, const CUtensorMap& qm, const TcParams& p, int kt,
                                const Launch& l);
 cudaError_t prefill_tc8_prepare(int D, int kt, int* blocks_per_sm);
+// latent attention (kt: KT_BF16 or KT_F16); items are tiles of kMlaRows query rows
+cudaError_t mla_prepare(int kt, int* blocks_per_sm);
+cudaError_t launch_mla(const CUtensorMap& kvm, const CUtensorMap& qm, const TcParams& p, int kt, const Launch& l);
 // q (n elements of RpaDtype q_dtype: f32, f16 or bf16) rounded to f16 (to_f16) or bf16 into out
 cudaError_t launch_q_convert(const void* q, int q_dtype, uint8_t* out, int to_f16, size_t n, const Launch& l);
 constexpr int kTcRows = 128;  // rows of a tensor-memory prefill tile
@@ -199,6 +206,8 @@ constexpr int kTcRows = 128;  // rows of a tensor-memory prefill tile
 int encode_kv_map(CUtensorMap* m, const void* kv, int byte_elems, long long N, int ps, int Hkv, int D, int BR);
 int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt);
 int encode_kv_map_runs(CUtensorMap* m, const void* kv, int byte_elems, long long N, int ps, int Hkv, int D, int BR);
+// latent cache [N, ps, Hkv, D] (2-byte elements): one box = BR slots of one kv head's row
+int encode_kv_map_latent(CUtensorMap* m, const void* kv, long long N, int ps, int Hkv, int D, int BR);
 // occupancy / attributes (call once per device)
 cudaError_t attn_prepare(int D, int kt, int* pf_blocks_per_sm);
 size_t plan_smem_bytes();
@@ -208,6 +217,9 @@ cudaError_t plan_prepare();
 // The kernels and tiles a configuration uses, with their occupancy and the workspace capacities.
 struct KernelSet {
     int G, D, kt, odt;
+    int Dv;              // width of V and o (D except for the latent layout)
+    int mla;             // latent layout: every item runs on the latent-attention kernel
+    int Gp, Hp;          // the planner's heads per kv head and kv heads (latent: blocks of <= 16 q heads)
     int q_conv;          // 1: q is first rounded into the workspace (its type is not the MMA operand type)
     int q_conv_f16;      // ... to f16 (else bf16)
     int q_f16;           // 8-bit K/V: the q the kernels read holds f16 values

@@ -10,7 +10,8 @@
 //   decode          (2-byte K/V: 8- or 16-row tiles; 8-bit K/V at D 64) -- on the side stream
 //                   when decode and prefill run concurrently
 //   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128, 8-bit K/V at D 128 / 256,
-//                   which also take the decode rows) or the warp-MMA kernel (the rest)
+//                   which also take the decode rows), the latent-attention kernel (latent layout,
+//                   every row) or the warp-MMA kernel (the rest)
 //   combine         split-KV merge, output of the uncovered rows
 //
 // Nothing here allocates: the caller owns the workspace.
@@ -44,7 +45,7 @@ struct Layout {
 };
 
 Layout layout(const RpaCfg& c, const KernelSet& ks) {
-    const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
+    const int64_t S = c.max_num_seqs, Hkv = ks.Hp;  // the planner's kv heads
     Layout L;
     size_t off = 0;
     L.ctrl = off; off = align256(off + kCtrlWords * sizeof(int));
@@ -69,6 +70,12 @@ void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks) {
     ks->D = (int)c.head_dim;
     ks->kt = kv_type(c.kv_dtype);
     ks->odt = out_type(c.q_dtype);
+    ks->mla = c.kv_layout == RPA_KV_LATENT;
+    ks->Dv = ks->mla ? (int)c.v_head_dim : ks->D;
+    // the planner's head grouping: latent items hold at most 16 query rows, so a kv head's query
+    // heads are planned as blocks of up to 16 ("kv heads" of the planner, reading one latent row)
+    ks->Gp = ks->mla && ks->G > kMlaRows ? kMlaRows : ks->G;
+    ks->Hp = (int)c.num_kv_heads * (ks->G / ks->Gp);
     const bool eight = kt_8bit(ks->kt);
     // the MMA operands of Q: bf16 with bf16 K/V, f16 otherwise; q of another type is rounded
     // into the workspace first, except bf16 q with 8-bit K/V, which the kernels round to f16 as
@@ -99,23 +106,32 @@ void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks) {
     // 8-row decode tiles (keys on the MMA's M side) whenever a group fits: 2-byte K/V, G <= 8
     ks->dec_rows = (!eight && ks->G <= 8) ? 8 : kDecRows;
     ks->Tt = ks->G <= ks->dec_rows ? ks->dec_rows / ks->G : 1;
-    ks->tc = (!eight && (ks->D == 64 || ks->D == 128)) ? 1 : 0;
-    ks->tc8 = (eight && (ks->D == 128 || ks->D == 256)) ? 1 : 0;
+    ks->tc = (!ks->mla && !eight && (ks->D == 64 || ks->D == 128)) ? 1 : 0;
+    ks->tc8 = (!ks->mla && eight && (ks->D == 128 || ks->D == 256)) ? 1 : 0;
     ks->pf_tokens = ks->tc    ? 2 * (kTcRows / ks->G)
                     : ks->tc8 ? kTcRows / ks->G
                               : (kPfRows / ks->G > 0 ? kPfRows / ks->G : 1);
+    if (ks->mla) {
+        // every sequence is planned in tiles of 16 query rows; the split-KV rule takes those with
+        // q_len * G' <= 16
+        ks->dec_rows = kMlaRows;
+        ks->Tt = kMlaRows / ks->Gp;
+        ks->pf_tokens = ks->Tt;
+    }
     ks->sms = sms;
 }
 
 cudaError_t kernels_occupancy(KernelSet* ks) {
     cudaError_t e = plan_prepare();
     if (e != cudaSuccess) return e;
-    e = ks->tc    ? prefill_tc_prepare(ks->D, ks->kt, &ks->pf_bps)
+    e = ks->mla   ? mla_prepare(ks->kt, &ks->pf_bps)
+        : ks->tc  ? prefill_tc_prepare(ks->D, ks->kt, &ks->pf_bps)
         : ks->tc8 ? prefill_tc8_prepare(ks->D, ks->kt, &ks->pf_bps)
                   : attn_prepare(ks->D, ks->kt, &ks->pf_bps);
     if (e != cudaSuccess) return e;
-    if (ks->tc8) {
-        // the fp8 tensor-memory kernel takes the decode rows too: the decode kernel never runs
+    if (ks->tc8 || ks->mla) {
+        // the 8-bit tensor-memory kernel (and the latent kernel) takes the decode rows too: the
+        // decode kernel never runs
         ks->dec_bps = ks->pf_bps;
     } else {
         e = decode_prepare(ks->D, ks->kt, ks->dec_rows, &ks->dec_bps);
@@ -128,14 +144,15 @@ cudaError_t kernels_occupancy(KernelSet* ks) {
 void kernels_capacity(const RpaCfg& c, KernelSet* ks) {
     // worst-case capacities (see the planner's chunk rule: at most kDecWaves pieces per CTA of
     // the kernel that runs the decode units, plus one per sequence)
-    const int64_t S = c.max_num_seqs, Hkv = c.num_kv_heads;
+    const int64_t S = c.max_num_seqs, Hkv = ks->Hp;  // the planner's kv heads
     const int64_t Tq = ks->pf_tokens;
     const int64_t dec_slots = (int64_t)ks->sms * ks->dec_bps;
     ks->max_dec_units = (int)(S + (kDecWaves * dec_slots + Hkv - 1) / Hkv + 1);
     const int pf_only_units = (int)((c.num_q_tokens + Tq - 1) / Tq + S + 1);
     ks->max_units = ks->max_dec_units + pf_only_units;
-    // with 8-bit K/V on tensor memory, decode units are items of the prefill kernel too
-    ks->max_pf_units = ks->tc8 ? ks->max_units : pf_only_units;
+    // with 8-bit K/V on tensor memory (or latent attention), decode units are items of the
+    // prefill-side kernel too
+    ks->max_pf_units = (ks->tc8 || ks->mla) ? ks->max_units : pf_only_units;
     ks->max_part = (int)(ks->max_dec_units * Hkv);
     ks->max_comb = (int)(S * Hkv);
 }
@@ -186,8 +203,8 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     pp.cu_q_lens = cu_q_lens;
     pp.num_seqs = num_seqs;
     pp.T = (int)c.num_q_tokens;
-    pp.Hkv = (int)c.num_kv_heads;
-    pp.G = ks.G;
+    pp.Hkv = ks.Hp;
+    pp.G = ks.Gp;
     pp.P = (int)c.pages_per_seq;
     pp.ps = (int)c.page_size;
     pp.causal = c.is_causal ? 1 : 0;
@@ -200,8 +217,8 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     pp.n_sms = ks.sms;
     pp.dec_bps = ks.dec_bps;
     pp.pf_bps = ks.pf_bps;
-    pp.pf_mma_rows = ks.tc ? 2 * kTcRows : ks.tc8 ? kTcRows : kPfRows;
-    pp.dec_on_pf = ks.tc8;
+    pp.pf_mma_rows = ks.tc ? 2 * kTcRows : ks.tc8 ? kTcRows : ks.mla ? kMlaRows : kPfRows;
+    pp.dec_on_pf = ks.tc8 || ks.mla;
     pp.D = ks.D;
     pp.kv_elt = kt_8bit(ks.kt) ? 1 : 2;
     pp.pf_sm_gflops = (ks.tc || ks.tc8) ? kPfSmGflopsTc : kPfSmGflopsMma;
@@ -234,7 +251,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     ap.T = (int)c.num_q_tokens;
     ap.Hq = (int)c.num_q_heads;
     ap.Hkv = (int)c.num_kv_heads;
-    ap.G = ks.G;
+    ap.G = ks.Gp;
     ap.D = ks.D;
     ap.ps = (int)c.page_size;
     ap.P = (int)c.pages_per_seq;
@@ -281,8 +298,10 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     const int byte_kv = kt_8bit(ks.kt) ? 1 : 0;
     if (has_q) {
         if (maps->kv_ptr != kv_pages) {
-            if (encode_kv_map_runs(&maps->kv, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
-                                   (int)c.num_kv_heads, ks.D, ks.BR) != 0 ||
+            if ((ks.mla ? encode_kv_map_latent(&maps->kv, kv_pages, c.total_num_pages, (int)c.page_size,
+                                               (int)c.num_kv_heads, ks.D, ks.BR)
+                        : encode_kv_map_runs(&maps->kv, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
+                                             (int)c.num_kv_heads, ks.D, ks.BR)) != 0 ||
                 (ks.tc && encode_kv_map(&maps->kv_pf, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
                                         (int)c.num_kv_heads, ks.D, ks.BR) != 0)) {
                 maps->kv_ptr = nullptr;
@@ -291,7 +310,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
             maps->kv_ptr = kv_pages;
         }
         if (maps->q_ptr != qk) {
-            if (encode_q_map(&maps->q, qk, c.num_q_tokens, (int)c.num_q_heads, ks.D, ks.G, ks.Tt) != 0 ||
+            if (encode_q_map(&maps->q, qk, c.num_q_tokens, (int)c.num_q_heads, ks.D, ks.Gp, ks.Tt) != 0 ||
                 ((ks.tc || ks.tc8) && encode_q_map(&maps->q_pf, qk, c.num_q_tokens, (int)c.num_q_heads, ks.D,
                                                    ks.G, kTcRows / ks.G) != 0)) {
                 maps->q_ptr = nullptr;
@@ -301,7 +320,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
         }
     }
     if (!rec(kEvDecStart, dst)) return fail(RPA_ERR_CUDA);
-    if (has_q && !ks.tc8) {
+    if (has_q && !ks.tc8 && !ks.mla) {
         DecParams dp;
         dp.a = ap;
         dp.a.items = ws.dec_items;
@@ -324,7 +343,14 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
         ap.item_count_word = kNumPfItems;
         ap.counter_word = kPfCounter;
         cudaError_t e;
-        if (ks.tc || ks.tc8) {
+        if (ks.mla) {
+            TcParams tp;
+            tp.a = ap;
+            tp.BR = ks.BR;
+            tp.Tq = ks.pf_tokens;
+            tp.timeout_ns = eo.timeout_ns;
+            e = launch_mla(maps->kv, maps->q, tp, ks.kt, Launch{ks.sms * ks.pf_bps, st});
+        } else if (ks.tc || ks.tc8) {
             TcParams tp;
             tp.a = ap;
             tp.BR = ks.BR;
@@ -347,8 +373,8 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     cp.num_seqs = num_seqs;
     cp.T = (int)c.num_q_tokens;
     cp.Hq = (int)c.num_q_heads;
-    cp.G = ks.G;
-    cp.D = ks.D;
+    cp.G = ks.Gp;
+    cp.D = ks.Dv;  // the width of o and of the split-KV partials
     cp.rows_max = ks.dec_rows;
     cp.v_scale = ks.v_scale;
     cp.sinks = ap.sinks;

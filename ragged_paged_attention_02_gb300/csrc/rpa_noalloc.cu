@@ -30,12 +30,12 @@ static __device__ __align__(256) unsigned char g_rpa_scratch[kNoAllocScratchByte
 
 std::mutex g_mu;
 void* g_scratch_dev[kMaxDevices];
-// occupancy per device and kernel choice: [device][D: 64, 128, 256][KvType][8-row decode tiles]
-int g_dec_bps[kMaxDevices][3][5][2];
-int g_pf_bps[kMaxDevices][3][5][2];
-bool g_ready[kMaxDevices][3][5][2];
+// occupancy per device and kernel choice: [device][D: 64, 128, 256, latent][KvType][8-row decode tiles]
+int g_dec_bps[kMaxDevices][4][5][2];
+int g_pf_bps[kMaxDevices][4][5][2];
+bool g_ready[kMaxDevices][4][5][2];
 
-int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+int d_index(const KernelSet& ks) { return ks.mla ? 3 : ks.D == 64 ? 0 : ks.D == 128 ? 1 : 2; }
 
 // Once per device (and per head size / K/V type for the kernel attributes), with that device
 // current: fetch the scratch array's device address and set the kernels' shared-memory limits.
@@ -52,7 +52,7 @@ int setup(int dev, KernelSet* ks, void** scratch) {
         }
         g_scratch_dev[dev] = ptr;
     }
-    const int di = d_index(ks->D), kt = ks->kt, r8 = ks->dec_rows == 8 ? 1 : 0;
+    const int di = d_index(*ks), kt = ks->kt, r8 = ks->dec_rows == 8 ? 1 : 0;
     if (!g_ready[dev][di][kt][r8]) {
         if (kernels_occupancy(ks) != cudaSuccess) {
             cudaGetLastError();

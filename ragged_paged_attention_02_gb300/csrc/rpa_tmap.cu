@@ -87,6 +87,22 @@ int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
+// Latent cache [N, ps, Hkv, D] viewed as (64 elements of a column block, slots, column blocks of
+// a slot: Hkv * D / 64).  One box = BR slots of one kv head's row, landing as [D/64][BR][128 B]
+// (2-byte elements, 128-byte swizzle).
+int encode_kv_map_latent(CUtensorMap* m, const void* kv, long long N, int ps, int Hkv, int D, int BR) {
+    EncodeTiledFn fn = encoder();
+    if (!fn) return -1;
+    const cuuint64_t dims[3] = {64u, (cuuint64_t)(N * ps), (cuuint64_t)(Hkv * D / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)(Hkv * D * 2), 128u};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)BR, (cuuint32_t)(D / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : (int)r;
+}
+
 // q viewed as (D, Hq, T): one box = 64 elements x the G heads of a kv group x
 // Tt tokens, 128-byte swizzle; tokens past T read as zero.  q holds 2-byte
 // elements (bf16 or f16: the copy moves bits).

@@ -266,7 +266,7 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
 
 # ---------------------------------------------------------------- the five workloads
 WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill", "decode_quarter",
-             "fp8_window_quarter")
+             "fp8_window_quarter", "mla_decode")
 
 
 def workload(name: str) -> Problem:
@@ -326,6 +326,16 @@ def workload(name: str) -> Problem:
         return build(seed=4, q_lens=[8192] * 4, kv_lens=[8192] * 4, num_q_heads=64,
                      num_kv_heads=8, head_dim=128, page_size=64, pages_per_seq=128,
                      total_num_pages=512, sm_scale=1.0 / math.sqrt(128), name=name,
+                     rng_lengths=rng)
+    if name == "mla_decode":
+        # latent attention decode, DeepSeek-V2-Lite-like: 128 x q_len 1, kv_len ~ U[1024, 8192],
+        # 16 q heads on one latent kv head, rows of 576 (512 latent + 64 rope), values of 512,
+        # page 64, bf16, softmax scale 1/sqrt(192) (the q.k width before the latent absorption)
+        rng = np.random.default_rng([5, 0])
+        kl = rng.integers(1024, 8192, size=128, endpoint=True)
+        return build(seed=5, q_lens=np.ones(128, np.int64), kv_lens=kl, num_q_heads=16,
+                     num_kv_heads=1, head_dim=576, page_size=64, pages_per_seq=128,
+                     kv_layout="latent", v_head_dim=512, sm_scale=1.0 / math.sqrt(192), name=name,
                      rng_lengths=rng)
     raise KeyError(name)
 

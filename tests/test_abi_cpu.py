@@ -60,6 +60,22 @@ BASE = dict(num_q_tokens=22, num_q_heads=4, num_kv_heads=2, head_dim=64, total_n
     (dict(page_size=6), rpa.RPA_ERR_UNSUPPORTED),  # page runs of the gather are >= 4 slots
     (dict(page_size=4, pages_per_seq=16), rpa.RPA_OK),
     (dict(head_dim=256, num_q_heads=16, num_kv_heads=8), rpa.RPA_OK),
+    # element types: f16 / f32 q, f16 / e5m2 / int8 K/V
+    (dict(q_dtype="f16", kv_dtype="f16"), rpa.RPA_OK),
+    (dict(q_dtype="f32", kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.05), rpa.RPA_OK),
+    (dict(q_dtype="f16", kv_dtype="int8", k_scale=0.04, v_scale=0.04), rpa.RPA_OK),
+    # latent layout: 576 / 512 rows only, 2-byte rows, pages of a multiple of 8, blocks of 16 heads
+    (dict(kv_layout="latent", head_dim=576, v_head_dim=512, num_q_heads=16, num_kv_heads=1, page_size=64), rpa.RPA_OK),
+    (dict(kv_layout="latent", head_dim=576, v_head_dim=512, num_q_heads=128, num_kv_heads=1, page_size=16), rpa.RPA_OK),
+    (dict(kv_layout="latent", head_dim=576, v_head_dim=512, num_q_heads=24, num_kv_heads=1, page_size=16),
+     rpa.RPA_ERR_UNSUPPORTED),
+    (dict(kv_layout="latent", head_dim=576, v_head_dim=512, num_q_heads=16, num_kv_heads=1, page_size=4),
+     rpa.RPA_ERR_UNSUPPORTED),
+    (dict(kv_layout="latent", head_dim=512, v_head_dim=512, num_q_heads=16, num_kv_heads=1, page_size=16),
+     rpa.RPA_ERR_UNSUPPORTED),
+    (dict(kv_layout="latent", head_dim=576, v_head_dim=512, num_q_heads=16, num_kv_heads=1, page_size=16,
+          kv_dtype="fp8_e4m3"), rpa.RPA_ERR_UNSUPPORTED),
+    (dict(v_head_dim=32), rpa.RPA_ERR_UNSUPPORTED),  # the split layout's V is head_dim wide
 ])
 def test_validate_cfg(L, change, code):
     cfg = dict(BASE)
@@ -102,3 +118,28 @@ def test_cfg_init_defaults_keep_the_shape(L):
     assert c.is_causal == 1 and c.reserved == 0
     assert (c.has_soft_cap, c.has_k_scale, c.has_v_scale, c.has_sliding_window) == (0, 0, 0, 0)
     assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_OK
+
+
+def test_dtypes_the_library_refuses(L):
+    """K/V in f32 / i32 / i16 (the page's other packings) and q in 8-bit types are refused."""
+    import ctypes
+
+    for kv, q in ((rpa.RPA_DT_F32, rpa.RPA_DT_BF16), (7, rpa.RPA_DT_BF16), (rpa.RPA_DT_BF16, rpa.RPA_DT_FP8_E4M3),
+                  (rpa.RPA_DT_BF16, rpa.RPA_DT_INT8)):
+        c = rpa.make_cfg(**BASE)
+        c.kv_dtype, c.q_dtype = kv, q
+        assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_ERR_UNSUPPORTED, (kv, q)
+
+
+def test_sinks_need_an_aligned_pointer(L):
+    import ctypes
+
+    c = rpa.make_cfg(**BASE)
+    c.has_sinks, c.sinks = 1, None
+    assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_ERR_INVALID_ARG
+    c.sinks = 4098  # not 4-byte aligned
+    assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_ERR_INVALID_ARG
+    c.sinks = 4096
+    assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_OK
+    c.reserved = 1
+    assert L.rpa_validate_cfg(ctypes.byref(c)) == rpa.RPA_ERR_INVALID_ARG

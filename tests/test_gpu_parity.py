@@ -165,6 +165,32 @@ def test_dtype_cases_all_rows(case):
     assert_close(got, oracle.forward(p), p.kv_dtype, f"dtype case {case}")
 
 
+# Latent attention over a paged latent cache (rows of 576: a 512-wide latent, whose part is the
+# value, and a 64-wide rope part): decode rows split into pieces (combine kernel), prefill tiles,
+# G = 16, 8 and 128 (blocks of 16 q heads per item), two kv heads, f16 rows, f32 q, sinks, soft cap
+# and window, page sizes 16 and 64.
+LATENT = dict(kv_layout="latent", head_dim=576, v_head_dim=512, sm_scale=1 / 24)
+MLA_CASES = [
+    (110, dict(num_seqs=10, decode_only=True, max_kv=4000, num_q_heads=16, num_kv_heads=1, page_size=64, **LATENT)),
+    (111, dict(num_seqs=6, max_q=40, max_kv=900, num_q_heads=16, num_kv_heads=1, page_size=16, **LATENT)),
+    (112, dict(num_seqs=8, max_q=9, max_kv=2000, num_q_heads=8, num_kv_heads=1, page_size=32, soft_cap=30.0,
+               sliding_window=700, sinks=True, **LATENT)),
+    (113, dict(num_seqs=5, max_q=3, max_kv=1500, num_q_heads=128, num_kv_heads=1, page_size=64, **LATENT)),
+    (114, dict(num_seqs=6, max_q=12, max_kv=1200, num_q_heads=32, num_kv_heads=2, page_size=16, kv_dtype="f16",
+               q_dtype="f32", is_causal=False, **LATENT)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(MLA_CASES)), ids=[f"seed{c[0]}" for c in MLA_CASES])
+def test_latent_cases_all_rows(case):
+    seed, kw = MLA_CASES[case]
+    p = ri.random_small(seed, **kw)
+    got, st = run(p)
+    assert st == 0
+    assert got.shape == (p.num_q_tokens, p.num_q_heads, 512)
+    assert_close(got, oracle.forward(p), p.kv_dtype, f"latent case {case}")
+
+
 def _sample_rows(p, n, seed, tile_tokens):
     """n random (token, q head) rows, plus, for every query tile of `tile_tokens` tokens of every
     sequence, its first and last token, each with the first and the last q head of a random kv

@@ -62,6 +62,9 @@ CASES = {
     # attention sinks read through the cfg's device pointer
     "sinks": (64, dict(num_seqs=9, max_q=60, max_kv=4000, num_q_heads=16, num_kv_heads=4, head_dim=128,
                        sinks=True)),
+    # latent attention: the latent kernel, split pieces of 512-wide partials
+    "latent": (66, dict(num_seqs=8, max_q=4, max_kv=3000, num_q_heads=16, num_kv_heads=1, page_size=64,
+                        kv_layout="latent", head_dim=576, v_head_dim=512, sm_scale=1 / 24)),
     # f32 q rounded into the fixed array before the kernels read it; e5m2 K/V; f32 o
     "f32_q_e5m2": (65, dict(num_seqs=8, max_q=40, max_kv=3000, num_q_heads=16, num_kv_heads=8, head_dim=256,
                             q_dtype="f32", kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
@@ -84,7 +87,7 @@ def test_noalloc_matches_oracle_and_rpa_forward_twice(name):
     assert att.status() == 0
     att.close()
     for _ in range(2):
-        out = torch.full_like(t[0], 9.0)
+        out = t[0].new_full((p.num_q_tokens, p.num_q_heads, p.out_dim), 9.0)
         assert _noalloc(p, t, out) == 0
         torch.cuda.synchronize()
         got = o_to_f64(out)

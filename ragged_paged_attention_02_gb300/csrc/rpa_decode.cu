@@ -80,9 +80,9 @@ __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
 template <int D, int ROWS>
 constexpr int dec_min_blocks() { return D > 128 ? 1 : ROWS == 8 ? 3 : 2; }
 
+// The kernel body; `kvmap` and `qmap` point at the kernel's grid-constant tensor-map parameters.
 template <int D, int KT, int ROWS>
-__global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_decode_attn(
-    const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap, const DecParams p) {
+__device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecParams& p) {
     using Gm = DecGeom<D, KT, ROWS>;
     constexpr int kNS = Gm::NS;
     constexpr bool FP8 = Gm::FP8;
@@ -338,7 +338,9 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
             }
 
             // ---- S = Q K^T  (16 rows x 16 keys); even and odd k-steps accumulate separately
-            // (two independent MMA chains per n-block), summed at the end
+            // (two independent MMA chains per n-block), summed at the end -- at D <= 128: at D 256
+            // the registers are spent on Q and O, and one chain per n-block keeps them unspilled
+            constexpr bool kTwo = D <= 128;
             float sacc[2][4], sodd[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
@@ -361,13 +363,15 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
                     }
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
-                    mma16816<F16>((kd & 1) ? sodd[0] : sacc[0], qf[kd], b0, b1);
-                    mma16816<F16>((kd & 1) ? sodd[1] : sacc[1], qf[kd], b2, b3);
+                    mma16816<F16>((kTwo && (kd & 1)) ? sodd[0] : sacc[0], qf[kd], b0, b1);
+                    mma16816<F16>((kTwo && (kd & 1)) ? sodd[1] : sacc[1], qf[kd], b2, b3);
                 }
+                if constexpr (kTwo) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                    for (int i = 0; i < 2; ++i)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[i][e] += sodd[i][e];
+                        for (int e = 0; e < 4; ++e) sacc[i][e] += sodd[i][e];
+                }
             }
             // ---- scale, softcap, masks (log2 domain)
             const bool need_mask = partial || (a.causal && kw + 15 > kl - ql + tok0) ||
@@ -795,18 +799,35 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
 }
 
 template <int D, int KT, int ROWS>
+__global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_decode_attn(
+    const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap, const DecParams p) {
+    decode_body<D, KT, ROWS>(kvmap, qmap, p);
+}
+
+// 16-row tiles at D 128 need more registers than the launch bound for two CTAs per SM lets the
+// compiler assume (it spilled at 168): 200 a thread still fits two CTAs (2 x 160 x 200 <= 65536).
+constexpr int kDec16Regs = 200;
+template <int D, int KT, int ROWS>
+__global__ void __maxnreg__(kDec16Regs) rpa_decode_attn_r(const __grid_constant__ CUtensorMap kvmap,
+                                                         const __grid_constant__ CUtensorMap qmap, const DecParams p) {
+    decode_body<D, KT, ROWS>(kvmap, qmap, p);
+}
+
+template <int D, int KT, int ROWS>
 struct DecKern {
     using Gm = DecGeom<D, KT, ROWS>;
+    static constexpr auto fn() {
+        if constexpr (D == 128 && ROWS == 16) return rpa_decode_attn_r<D, KT, ROWS>;
+        else return rpa_decode_attn<D, KT, ROWS>;
+    }
     static cudaError_t prepare(int* bps) {
-        cudaError_t e = cudaFuncSetAttribute(rpa_decode_attn<D, KT, ROWS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
         if (e != cudaSuccess) return e;
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, rpa_decode_attn<D, KT, ROWS>, kDecThreads,
-                                                             Gm::SMEM);
+        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, fn(), kDecThreads, Gm::SMEM);
     }
     static cudaError_t launch(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p,
                               const Launch& l) {
-        return launch_pdl(rpa_decode_attn<D, KT, ROWS>, l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
+        return launch_pdl(fn(), l.grid, kDecThreads, Gm::SMEM, l.stream, kvm, qm, p);
     }
 };
 

@@ -280,6 +280,12 @@ def upload(prob, dev):
     return q, kv, kvl, pi, cu
 
 
+def out_for(prob, like):
+    """An output tensor for prob, of like's dtype and device: [num_q_tokens, Hq, v_head_dim] (the
+    width of V: head_dim, or the latent layout's value width)."""
+    return like.new_empty((prob.num_q_tokens, prob.num_q_heads, prob.out_dim))
+
+
 def gpu_uuid(dev):
     import torch
 
@@ -301,7 +307,7 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
     prob = ri.workload(name)
     work = ri.algorithmic_work(prob)
     q, kv, kvl, pi, cu = upload(prob, dev)
-    out = torch.empty_like(q)
+    out = out_for(prob, q)
     att = RaggedPagedAttention(**prob.cfg_dict())
     stream = torch.cuda.current_stream()
 
@@ -413,7 +419,7 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
         hkvl = kvl.cpu().pin_memory()
         hpi = pi.cpu().pin_memory()
         hcu = cu.cpu().pin_memory()
-        hout = torch.empty_like(hq).pin_memory()
+        hout = out_for(prob, hq).pin_memory()
         for _ in range(3):
             att.forward_host(hq, kv, hkvl, hpi, hcu, prob.num_seqs, hout, stream=stream)
         torch.cuda.synchronize()

@@ -68,3 +68,17 @@ def test_recorded_traffic_needs_the_current_sources(tmp_path, monkeypatch):
     assert bench.recorded_traffic("decode_attention", "decode") == 123456.0
     assert bench.recorded_traffic("decode_attention", "fp8_window") is None
     assert bench.recorded_traffic("combine", "decode") is None
+
+
+def test_output_shape_follows_the_value_width():
+    """The bench allocates o with the value width: head_dim, or 512 for the latent workload."""
+    import torch
+
+    import bench
+    import rpa_inputs as ri
+
+    for name, width in (("tiny", 64), ("mla_decode", 512)):
+        p = ri.workload(name)
+        q = torch.zeros(p.q.shape, dtype=torch.bfloat16)
+        o = bench.out_for(p, q)
+        assert tuple(o.shape) == (p.num_q_tokens, p.num_q_heads, width) and o.dtype == torch.bfloat16

@@ -410,14 +410,11 @@ struct Kern {
     }
 };
 
-// The configurations routed here: 2-byte K/V at D 256 (the tensor-memory prefill covers D 64 /
-// 128) and 8-bit K/V at D 64 (the 8-bit tensor-memory prefill covers D 128 / 256).
+// The configurations routed here: 8-bit K/V at D 64 (the tensor-memory kernels cover 2-byte K/V
+// at every head size and 8-bit K/V at D 128 / 256).
 template <typename Op>
 cudaError_t mma_dispatch(int D, int kt, Op op) {
-    if (D == 256) {
-        if (kt == KT_BF16) return op(Kern<256, KT_BF16>{});
-        if (kt == KT_F16) return op(Kern<256, KT_F16>{});
-    } else if (D == 64) {
+    if (D == 64) {
         if (kt == KT_E4M3) return op(Kern<64, KT_E4M3>{});
         if (kt == KT_E5M2) return op(Kern<64, KT_E5M2>{});
         if (kt == KT_I8) return op(Kern<64, KT_I8>{});

@@ -9,9 +9,9 @@
 //   planner         work items, split-KV pieces, SM split
 //   decode          (2-byte K/V: 8- or 16-row tiles; 8-bit K/V at D 64) -- on the side stream
 //                   when decode and prefill run concurrently
-//   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128, 8-bit K/V at D 128 / 256,
-//                   which also take the decode rows), the latent-attention kernel (latent layout,
-//                   every row) or the warp-MMA kernel (the rest)
+//   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128; 8-bit K/V at D 128 / 256 and
+//                   2-byte K/V at D 256, which also take the decode rows), the latent-attention
+//                   kernel (latent layout, every row) or the warp-MMA kernel (8-bit K/V at D 64)
 //   combine         split-KV merge, output of the uncovered rows
 //
 // Nothing here allocates: the caller owns the workspace.
@@ -107,7 +107,9 @@ void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks) {
     ks->dec_rows = (!eight && ks->G <= 8) ? 8 : kDecRows;
     ks->Tt = ks->G <= ks->dec_rows ? ks->dec_rows / ks->G : 1;
     ks->tc = (!ks->mla && !eight && (ks->D == 64 || ks->D == 128)) ? 1 : 0;
-    ks->tc8 = (!ks->mla && eight && (ks->D == 128 || ks->D == 256)) ? 1 : 0;
+    // the 64-key-tile tensor-memory kernel: 8-bit K/V at D 128 / 256 (converted to f16), and 2-byte
+    // K/V at D 256 (copied straight into its tiles)
+    ks->tc8 = (!ks->mla && ((eight && (ks->D == 128 || ks->D == 256)) || (!eight && ks->D == 256))) ? 1 : 0;
     ks->pf_tokens = ks->tc    ? 2 * (kTcRows / ks->G)
                     : ks->tc8 ? kTcRows / ks->G
                               : (kPfRows / ks->G > 0 ? kPfRows / ks->G : 1);
@@ -302,8 +304,9 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
                                                (int)c.num_kv_heads, ks.D, ks.BR)
                         : encode_kv_map_runs(&maps->kv, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
                                              (int)c.num_kv_heads, ks.D, ks.BR)) != 0 ||
-                (ks.tc && encode_kv_map(&maps->kv_pf, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
-                                        (int)c.num_kv_heads, ks.D, ks.BR) != 0)) {
+                ((ks.tc || (ks.tc8 && !byte_kv)) &&
+                 encode_kv_map(&maps->kv_pf, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
+                               (int)c.num_kv_heads, ks.D, ks.BR) != 0)) {
                 maps->kv_ptr = nullptr;
                 return fail(RPA_ERR_INVALID_ARG);
             }
@@ -356,9 +359,11 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
             tp.BR = ks.BR;
             tp.Tq = ks.pf_tokens;
             tp.timeout_ns = eo.timeout_ns;
-            // the 8-bit kernel copies whole page runs (K and V of the head) with the decode gather's map
+            // the 64-key-tile kernel copies whole page runs (K and V of the head) with the decode
+            // gather's map for 8-bit K/V, and 128-byte column blocks with the slot x row map for 2-byte
             e = ks.tc ? launch_prefill_tc(maps->kv_pf, maps->q_pf, tp, ks.kt, Launch{ks.sms * ks.pf_bps, st})
-                      : launch_prefill_tc8(maps->kv, maps->q_pf, tp, ks.kt, Launch{ks.sms * ks.pf_bps, st});
+                      : launch_prefill_tc8(byte_kv ? maps->kv : maps->kv_pf, maps->q_pf, tp, ks.kt,
+                                           Launch{ks.sms * ks.pf_bps, st});
         } else {
             e = launch_prefill(ap, ks.kt, Launch{ks.sms * ks.pf_bps, st});
         }

@@ -29,9 +29,16 @@
 //                    2^8), epilogue.  Items of at most 64 rows hold each query
 //                    row in 2, 4 or 8 TMEM lanes that split the keys.
 //
-// TMEM: Q (D/2 columns of packed f16 pairs), S0, S1 (64 each), O (D) -- 512
-// columns at D = 256.  All waits are bounded; on expiry the status word gets
-// RPA_ERR_TIMEOUT.
+// 2-byte K/V (bf16 or f16) at D = 256 run on the same pipeline in direct mode:
+// the producer copies K and V page runs straight into the 128-byte-swizzled
+// tiles the MMAs read (K once the QK two tiles back is done, V once that
+// tile's PV is done), the MMAs run in the K/V type (P in it too), and the
+// converter warps only zero the V rows of keys outside [kv_begin, kv_end) on
+// a tile's edges before signalling V ready (K rows there are masked in S).
+//
+// TMEM: Q (D/2 columns of packed 16-bit pairs), S0, S1 (64 each), O (D) --
+// 512 columns at D = 256.  All waits are bounded; on expiry the status word
+// gets RPA_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include <type_traits>
@@ -58,12 +65,12 @@ constexpr uint32_t kIssueNapNs = 100;  // longest suspension of the MMA thread's
 
 enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, eNtok, eNt, eKey0, eStop, ePart };
 
-template <int D>
+template <int D, bool DIRECT>
 struct G8 {
     static constexpr int CB = D / 64;                  // 128-byte column blocks of a 16-bit row
     static constexpr int ROUNDS = D / 64;              // Q staging rounds (one column block each)
     static constexpr int QSTAGE = kM * 128;            // Q staging: one column block x 128 rows
-    static constexpr int RAW = kBN * 2 * D;            // one raw fp8 stage (K and V)
+    static constexpr int RAW = DIRECT ? 0 : kBN * 2 * D;  // one raw 8-bit stage (K and V); none in direct mode
     static constexpr int T16 = CB * kBN * 128;         // one f16 K (or V) tile
     static constexpr int DATA = QSTAGE + 2 * RAW + 4 * T16;
     static constexpr int SMEM = DATA + 1024;
@@ -180,7 +187,11 @@ template <int D, int KT>
 __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __grid_constant__ CUtensorMap kvmap,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const TcParams p) {
-    using Gm = G8<D>;
+    // DIRECT: 2-byte K/V copied straight into the MMA tiles (kvmap: the slot x row map with
+    // 128-byte swizzle); else 8-bit page runs through the raw ring (kvmap: the page-run map)
+    constexpr bool DIRECT = !kt_8bit(KT);
+    constexpr bool F16 = kt_f16_mma(KT);  // MMA operands (and P) in f16, else bf16
+    using Gm = G8<D, DIRECT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t meta_full[2], meta_free[2];
     __shared__ __align__(8) uint64_t q_full, q_empty, q_ready, qt_free;
@@ -188,6 +199,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     // per S / f16 buffer b: K converted; QK done (S ready, K buffer free); P and V ready (softmax
     // and converter warps); PV done (V buffer free, O holds the PV)
     __shared__ __align__(8) uint64_t k_full[2], qk_done[2], pv_ready[2], pv_done[2];
+    __shared__ __align__(8) uint64_t v_land[2];  // direct mode: V(t) copied
     __shared__ __align__(8) uint64_t o_full, o_free;
     __shared__ __align__(8) uint64_t xchg[4];  // per lane quadrant: the two softmax warps' row maxima / sums
     __shared__ float xm[2][2][kM];             // [tile parity][key half][row] partial row maxima
@@ -212,7 +224,9 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             mbar_init(smem_u32(&meta_free[i]), 17);  // 8 softmax + 8 converter warps + MMA thread
             mbar_init(smem_u32(&raw_full[i]), 1);
             mbar_init(smem_u32(&raw_empty[i]), kNConv);
-            mbar_init(smem_u32(&k_full[i]), kNConv);
+            // K(t) ready: the converters' arrivals, or in direct mode the copies themselves
+            mbar_init(smem_u32(&k_full[i]), DIRECT ? 1 : kNConv);
+            mbar_init(smem_u32(&v_land[i]), 1);
             mbar_init(smem_u32(&qk_done[i]), 1);
             mbar_init(smem_u32(&pv_ready[i]), 8 + kNConv);
             mbar_init(smem_u32(&pv_done[i]), 1);
@@ -245,6 +259,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
         const uint32_t q_round_bytes = (uint32_t)(G * Tq * 128);
         int s = 0, ms = 0;
         uint32_t ph = 0, mph = 0, qph = 0;
+        uint32_t tgp = 0;  // direct mode: tiles copied so far (all items): tile buffer and phase
         bool ok = true;
         int it = 0;
         if (lane == 0) it = atomicAdd(ctrl + a.counter_word, 1);
@@ -310,6 +325,53 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 if (lp_last - win0 >= 32) {
                     win0 = k_tile / ps;
                     win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
+                }
+                if constexpr (DIRECT) {
+                    // K(t) into K tile b2 once QK(t-2) is done, V(t) into V tile b2 once PV(t-2) is
+                    // done: one copy per (page run, 128-byte column block), BR rows each
+                    const int b2 = tgp & 1;
+                    const uint32_t par = (tgp >> 1) & 1u;
+                    ++tgp;
+                    const int tasks = runs * Gm::CB;
+#pragma unroll 1
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        if (!mbar_wait(smem_u32(kv ? &pv_done[b2] : &qk_done[b2]), par ^ 1u, ctrl, tmo)) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t dst0 = (kv ? v16_base : k16_base) + b2 * Gm::T16;
+                        auto task = [&](int tk, int& x, int& y, uint32_t& dst) -> int {
+                            const int b = tk / Gm::CB, cb = tk % Gm::CB;
+                            const int k0 = k_tile + b * BR;
+                            const int lp = k0 / ps;
+                            const int pg = __shfl_sync(0xffffffffu, win, (lp - win0) & 31);
+                            if (tk >= tasks || k0 >= item.kv_end || k0 + BR <= item.kv_begin) return 0;
+                            if ((unsigned)pg >= (unsigned)a.N) return 2;
+                            x = (2 * item.head + kv) * D + cb * 64;
+                            y = pg * ps + (k0 - lp * ps);
+                            dst = dst0 + (uint32_t)(cb * (kBN * 128) + b * BR * 128);
+                            return 1;
+                        };
+                        int n_mine = 0, bad = 0;
+                        for (int t0 = 0; t0 < tasks; t0 += 32) {
+                            int x, y;
+                            uint32_t dst;
+                            const int r = task(t0 + lane, x, y, dst);
+                            n_mine += r == 1;
+                            bad |= r == 2;
+                        }
+                        const int n_issue = __reduce_add_sync(0xffffffffu, n_mine);
+                        if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(ctrl, RPA_ERR_BAD_PAGE_INDEX);
+                        const uint32_t fb = smem_u32(kv ? &v_land[b2] : &k_full[b2]);
+                        if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)n_issue * (uint32_t)BR * 128u);
+                        __syncwarp();
+                        for (int t0 = 0; t0 < tasks; t0 += 32) {
+                            int x, y;
+                            uint32_t dst;
+                            if (task(t0 + lane, x, y, dst) == 1) tma_load_2d(dst, &kvmap, fb, x, y);
+                        }
+                    }
+                    continue;
                 }
                 if (!mbar_wait(smem_u32(&raw_empty[s]), ph ^ 1u, ctrl, tmo)) {
                     ok = false;
@@ -378,7 +440,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const uint4 w = *reinterpret_cast<const uint4*>(row + (((c ^ r) & 7) << 4));
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) qv[4 * c + k] = a.q_f16 ? ws[k] : bf16x2_to_f16x2(ws[k]);
+                        for (int k = 0; k < 4; ++k)
+                            qv[4 * c + k] = (DIRECT || a.q_f16) ? ws[k] : bf16x2_to_f16x2(ws[k]);
                     }
                     tmem_st32(lane_addr + Gm::TM_Q + rd * 32, qv);
                 }
@@ -396,6 +459,30 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             for (int t = 0; t < nt; ++t, ++tg) {
                 const int b2 = tg & 1;
                 const uint32_t par = (tg >> 1) & 1u;
+                if constexpr (DIRECT) {
+                    // the copies wrote V(t) into its tile: on the tile's edges, zero this warp's rows of
+                    // keys outside [kv_begin, kv_end) (page tails may hold any bits; runs outside the
+                    // range were not copied), then V is ready
+                    if (!mbar_wait(smem_u32(&v_land[b2]), par, ctrl, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    const int k_lo = key0 + t * kBN;
+                    if (k_lo < kv_begin || k_lo + kBN > kv_end) {
+                        uint8_t* vt = smem + (v16_base - smem0) + b2 * Gm::T16;
+                        for (int i = lane; i < kConvRows * Gm::CB * 8; i += 32) {
+                            const int key = kConvRows * cw + i / (Gm::CB * 8);
+                            const int rem = i % (Gm::CB * 8);
+                            const int j = k_lo + key;
+                            if (j >= kv_begin && j < kv_end) continue;
+                            put_u4(vt + ((rem >> 3) * kBN + key) * 128 + (rem & 7) * 16, make_uint4(0, 0, 0, 0));
+                        }
+                        fence_proxy_async_smem();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
+                    continue;
+                }
                 if (!mbar_wait(smem_u32(&raw_full[s]), ph, ctrl, tmo)) {
                     ok = false;
                     break;
@@ -437,8 +524,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     } else if (warp == kMma) {
         // =============================== MMA issuer ===============================
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = umma_idesc_f16(kM, kBN, 0, 0);
-            constexpr uint32_t idesc_pv = umma_idesc_f16(kM, D, 0, 1);
+            constexpr uint32_t idesc_qk = F16 ? umma_idesc_f16(kM, kBN, 0, 0) : umma_idesc_bf16(kM, kBN, 0, 0);
+            constexpr uint32_t idesc_pv = F16 ? umma_idesc_f16(kM, D, 0, 1) : umma_idesc_bf16(kM, D, 0, 1);
             int ms = 0;
             uint32_t mph = 0;
             uint32_t tg = 0, items = 0;
@@ -656,7 +743,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                                     x0, x1);
                         const float p0 = ex2(x0), p1 = ex2(x1);
                         ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
-                        own[i] = pack2<true>(p0, p1);
+                        own[i] = pack2<F16>(p0, p1);
                     }
                     // the half's 16 P columns (P[i] at column i / 2): the copy's own, zero elsewhere
                     uint32_t pk[HC / 2];
@@ -776,7 +863,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
 
 template <int D, int KT>
 struct Tc8Kern {
-    using Gm = G8<D>;
+    using Gm = G8<D, !kt_8bit(KT)>;
     static cudaError_t prepare(int* bps) {
         cudaError_t e =
             cudaFuncSetAttribute(rpa_prefill_tc8<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
@@ -788,12 +875,16 @@ struct Tc8Kern {
     }
 };
 
-// 8-bit K/V (e4m3, e5m2, int8) at D 128 / 256
+// 8-bit K/V (e4m3, e5m2, int8) at D 128 / 256; 2-byte K/V (bf16, f16) at D 256 in direct mode
 template <int D, typename Op>
 cudaError_t tc8_dispatch_kt(int kt, Op op) {
     if (kt == KT_E4M3) return op(Tc8Kern<D, KT_E4M3>{});
     if (kt == KT_E5M2) return op(Tc8Kern<D, KT_E5M2>{});
     if (kt == KT_I8) return op(Tc8Kern<D, KT_I8>{});
+    if constexpr (D == 256) {
+        if (kt == KT_BF16) return op(Tc8Kern<D, KT_BF16>{});
+        if (kt == KT_F16) return op(Tc8Kern<D, KT_F16>{});
+    }
     return cudaErrorInvalidValue;
 }
 template <typename Op>

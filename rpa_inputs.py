@@ -266,7 +266,7 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
 
 # ---------------------------------------------------------------- the five workloads
 WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill", "decode_quarter",
-             "fp8_window_quarter", "mla_decode")
+             "fp8_window_quarter", "mla_decode", "long_prefill_d256")
 
 
 def workload(name: str) -> Problem:
@@ -327,6 +327,13 @@ def workload(name: str) -> Problem:
                      num_kv_heads=8, head_dim=128, page_size=64, pages_per_seq=128,
                      total_num_pages=512, sm_scale=1.0 / math.sqrt(128), name=name,
                      rng_lengths=rng)
+    if name == "long_prefill_d256":
+        # long fresh prefill at head_dim 256 (Gemma-2-9B-like heads): 4 x 8192 tokens, 16 q heads /
+        # 8 kv heads, page 64, bf16, causal
+        rng = np.random.default_rng([6, 0])
+        return build(seed=6, q_lens=[8192] * 4, kv_lens=[8192] * 4, num_q_heads=16, num_kv_heads=8,
+                     head_dim=256, page_size=64, pages_per_seq=128, total_num_pages=512,
+                     sm_scale=1.0 / 16.0, name=name, rng_lengths=rng)
     if name == "mla_decode":
         # latent attention decode, DeepSeek-V2-Lite-like: 128 x q_len 1, kv_len ~ U[1024, 8192],
         # 16 q heads on one latent kv head, rows of 576 (512 latent + 64 rope), values of 512,

@@ -155,6 +155,28 @@ DTYPE_CASES = [
 ]
 
 
+# 2-byte K/V at D 256 on the 64-key-tile tensor-memory kernel (direct mode: K and V copied straight
+# into the MMA tiles): decode rows as split pieces, G = 16 with page runs of 8 keys, f16 with sinks
+# and no causal mask
+D256_CASES = [
+    (115, dict(num_seqs=10, decode_only=True, max_kv=6000, num_q_heads=16, num_kv_heads=8, head_dim=256,
+               sm_scale=1 / 16)),
+    (116, dict(num_seqs=8, max_q=20, max_kv=1500, num_q_heads=32, num_kv_heads=2, head_dim=256, page_size=8,
+               soft_cap=50.0, sliding_window=500, sm_scale=1 / 16)),
+    (117, dict(num_seqs=7, max_q=150, max_kv=1200, num_q_heads=8, num_kv_heads=2, head_dim=256, page_size=32,
+               q_dtype="f16", kv_dtype="f16", is_causal=False, sinks=True, sm_scale=1 / 16)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(D256_CASES)), ids=[f"seed{c[0]}" for c in D256_CASES])
+def test_d256_tensor_memory_cases_all_rows(case):
+    seed, kw = D256_CASES[case]
+    p = ri.random_small(seed, **kw)
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, f"D 256 case {case}")
+
+
 @pytest.mark.parametrize("case", range(len(DTYPE_CASES)), ids=[f"{c[1].get('q_dtype', 'bf16')}-"
                                                                f"{c[1]['kv_dtype']}-seed{c[0]}" for c in DTYPE_CASES])
 def test_dtype_cases_all_rows(case):
@@ -274,7 +296,8 @@ def test_page_placement_invariance_bit_identical():
 
 
 @pytest.mark.parametrize("kv_dtype,head_dim", [("bf16", 128), ("fp8_e4m3", 128), ("fp8_e4m3", 256),
-                                               ("f16", 128), ("fp8_e5m2", 256), ("int8", 128)])
+                                               ("f16", 128), ("fp8_e5m2", 256), ("int8", 128), ("bf16", 256),
+                                               ("f16", 256)])
 def test_poisoned_tails_and_unused_pages(kv_dtype, head_dim):
     extra = {} if kv_dtype in ("bf16", "f16") else dict(k_scale=0.05, v_scale=0.05)
     p = ri.random_small(42, num_seqs=5, max_q=130, max_kv=500, num_q_heads=8, num_kv_heads=2,

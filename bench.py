@@ -39,14 +39,26 @@ import rpa_inputs as ri  # noqa: E402
 
 METRIC = "ragged paged attn tokens/s; decode HBM GB/s & prefill TFLOP/s vs roofline"
 KERNEL_NAMES = ("planner", "decode_attention", "prefill_attention", "combine")
-KERNEL_SOURCES = {
-    "decode_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_decode.cu",
-                         "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
-    "prefill_attention": ["ragged_paged_attention_02_gb300/csrc/rpa_prefill_tc.cu",
-                          "ragged_paged_attention_02_gb300/csrc/rpa_prefill_tc8.cu",
-                          "ragged_paged_attention_02_gb300/csrc/rpa_attn_mma.cu",
-                          "ragged_paged_attention_02_gb300/csrc/rpa_internal.cuh"],
-}
+CSRC = "ragged_paged_attention_02_gb300/csrc/"
+
+
+def kernel_sources(prob, kernel):
+    """The source files of the kernel that runs `kernel` ("decode_attention" or
+    "prefill_attention") on this problem: its own .cu file and the shared header."""
+    eight = prob.kv_dtype in ("fp8_e4m3", "fp8_e5m2", "int8")
+    if kernel == "decode_attention":
+        f = "rpa_decode.cu"
+    elif prob.kv_layout == "latent":
+        f = "rpa_mla.cu"
+    elif (eight and prob.head_dim in (128, 256)) or (not eight and prob.head_dim == 256):
+        f = "rpa_prefill_tc8.cu"
+    elif not eight:
+        f = "rpa_prefill_tc.cu"
+    else:
+        f = "rpa_attn_mma.cu"
+    return [CSRC + f, CSRC + "rpa_internal.cuh"]
+
+
 DESCR = {
     "tiny": "3 seqs q_len {1,5,16} kv_len {17,40,64}, Hq 4 / Hkv 2, D 64, page 16, bf16",
     "decode": "256 seqs x q_len 1, kv_len~U[512,8192], Hq 32 / Hkv 8, D 128, page 16, bf16",
@@ -97,12 +109,13 @@ def sources_sha(names):
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """dram bytes per launch from profiles/kernel_traffic.txt, if taken on the current source."""
+def recorded_traffic(kernel: str, workload: str, sources):
+    """dram bytes per launch from profiles/kernel_traffic.txt, if taken on the current source of
+    the kernel (the hash of `sources`)."""
     path = os.path.join(ROOT, "profiles", "kernel_traffic.txt")
-    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
+    if not os.path.exists(path):
         return None
-    sha = sources_sha(KERNEL_SOURCES[kernel])
+    sha = sources_sha(sources)
     with open(path) as f:
         for line in f:
             parts = line.split()
@@ -371,7 +384,7 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
         else:
             bound, achieved, peak, unit, key = "hbm", w["bytes"] / (ms * 1e-3) / 1e9, hbm, "GB/s", "hbm_gbs"
         r = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-             "traffic": recorded_traffic(kname, name), "kernel": kname,
+             "traffic": recorded_traffic(kname, name, kernel_sources(prob, kname)), "kernel": kname,
              "peak_source": f"{src} ({key})", "kernel_ms": float(ms),
              "algorithmic": {"bytes": w["bytes"], "flops": w["flops"]}}
         if int(info[15]) & 1 and bound == "tensor" and all(has_work.values()):

@@ -12,7 +12,7 @@
 // leave it out.
 //
 // Work goes out in units of a few rows of one entry (one group of four columns per thread).  An
-// entry of at most four pieces merges in registers; longer ones first reduce each row's m and l
+// entry of at most eight pieces merges in registers; longer ones first reduce each row's m and l
 // (a warp per row) into shared-memory scale factors.  Entries hold at most `rows_max` rows (the
 // decode tile's rows: the planner classifies a sequence as decode only when q_len * G fits).
 //
@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kCombThreads = 256;
 constexpr int kCombCache = 64;  // pieces whose per-row scale factors are kept in shared memory
-constexpr int kDirect = 4;      // entries of at most this many pieces merge without shared memory
+constexpr int kDirect = 8;      // entries of at most this many pieces merge without shared memory
 
 __global__ void __launch_bounds__(kCombThreads, 2) rpa_combine_kernel(const CombParams p) {
     __shared__ float s_sc[kCombCache][kDecRows];  // 2^(m_i - M) of piece i and row r

@@ -14,10 +14,13 @@
 //                   then per 64-key stage one bulk tensor copy per page run of the latent rows
 //                   ("ragged_paged.zig": createKvAsyncCopyDescriptors, logical page ->
 //                   page_indices[s, page]) into a 2-stage mbarrier ring, crossing item boundaries.
-//   8 consumer      S = Q K^T: warp w takes keys 8w .. 8w+7 of the stage over the 576-wide
-//   warps           contraction (mma.sync, fp32); scale / soft cap / masks in the log2 domain; the
-//                   row maxima meet in shared memory, every warp forms the same running max, writes
-//                   its P (bf16 / f16) to shared memory and keeps its own partial row sum; then
+//   8 consumer      S = Q K^T: warp w takes k-steps [36w/8, 36(w+1)/8) of the 576-wide
+//   warps           contraction for all 64 keys of the stage (mma.sync, fp32; its Q slice stays in
+//                   registers for the item, eight independent accumulator chains), the partial
+//                   sums meet in shared memory and warp w adds up keys 8w .. 8w+7; scale / soft cap
+//                   / masks in the log2 domain; the row maxima meet in shared memory, every warp
+//                   forms the same running max, writes its P (bf16 / f16) to shared memory and
+//                   keeps its own partial row sum; then
 //                   O += P V: warp w owns value columns 64w .. 64w+63 of all 16 rows (V is the first
 //                   512 columns of the very rows of the stage).  Lazy rescale (the max grows by more
 //                   than 2^8).  At the item's end the row sums meet in shared memory and each warp
@@ -50,6 +53,9 @@ constexpr int kQBuf = kCBQ * kRows * 128;      // 18432 bytes: [9 column blocks]
 constexpr int kPBuf = kRows * kKS * 2;         // P: [16 rows][64 keys] 16-bit, 2048 bytes
 constexpr int kMlaSmem = kNS * kStage + 2 * kQBuf + kPBuf + 1024;
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kSPad = 72;                      // row stride (floats) of the partial-S exchange
+constexpr int kKSteps = kQK / 16;              // k-steps of the QK contraction (36)
+constexpr int kMaxWarpSteps = (kKSteps + kMlaCW - 1) / kMlaCW;  // 5
 
 enum MlaMeta : int { mSeq = 0, mHead, mQStart, mQl, mKl, mKvBegin, mKvEnd, mPart, mTok0, mNtok, mSt, mNst, mKey0,
                      mQb, mStop, mWords = 16 };
@@ -58,8 +64,11 @@ __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
     return line * 128u + (((chunk ^ line) & 7u) << 4);
 }
 
+// one CTA per SM: nine warps x 224 registers fit the register file (the launch bound alone lets the
+// compiler assume fewer, and it spilled)
+constexpr int kMlaRegs = 224;
 template <bool F16>
-__global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_constant__ CUtensorMap kvmap,
+__global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUtensorMap kvmap,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -67,10 +76,13 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
     // exchanges among the consumer warps (bounded mbarrier waits, so that a warp that gives up
     // cannot leave the others waiting on a hardware barrier): row maxima posted, P complete,
     // row sums posted
-    __shared__ __align__(8) uint64_t x_max, x_p, x_sum;
+    __shared__ __align__(8) uint64_t x_s, x_max, x_p, x_sum;
     __shared__ int meta[kNS][mWords];
     __shared__ float red_m[kMlaCW][kRows];  // per warp: its keys' row maxima (this stage)
     __shared__ float red_l[kMlaCW][kRows];  // per warp: its row sums (item end)
+    // per warp: its partial S over its k-steps, [row][key] with rows padded to 72 floats (the
+    // fragment stores and loads of a half warp then touch 32 distinct banks)
+    __shared__ __align__(16) float red_s[kMlaCW][kRows][kSPad];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const AttnParams& a = p.a;
@@ -91,6 +103,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
             mbar_init(smem_u32(&q_full[i]), 1);
             mbar_init(smem_u32(&q_empty[i]), kMlaCW);
         }
+        mbar_init(smem_u32(&x_s), kMlaCW);
         mbar_init(smem_u32(&x_max), kMlaCW);
         mbar_init(smem_u32(&x_p), kMlaCW);
         mbar_init(smem_u32(&x_sum), kMlaCW);
@@ -223,7 +236,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
     const int BR = p.BR, br_shift = __ffs(BR) - 1;
     const uint32_t run_bytes = (uint32_t)(kCBQ * BR * 128);
     int s = 0;
-    uint32_t ph = 0, xph_max = 0, xph_p = 0, xph_sum = 0;
+    uint32_t ph = 0, xph_s = 0, xph_max = 0, xph_p = 0, xph_sum = 0;
+    // this warp's k-steps of the QK contraction and its Q fragments for them (loaded per item)
+    const int kd0 = (kKSteps * w) / kMlaCW, nk = (kKSteps * (w + 1)) / kMlaCW - kd0;
+    uint32_t qf[kMaxWarpSteps][4];
     uint32_t qph[2] = {0u, 0u};
     // every consumer warp arrives, then waits (bounded) for the others
     auto exchange = [&](uint64_t& bar, uint32_t& xph) -> bool {
@@ -254,6 +270,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
             if (!mbar_wait(smem_u32(&q_full[qb]), qph[qb], ctrl, tmo)) return;
             qph[qb] ^= 1u;
 #pragma unroll
+            for (int i = 0; i < kMaxWarpSteps; ++i) {
+                if (i < nk) {
+                    const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int c = 2 * (kd0 + i) + (lane >> 4);
+                    ldsm_x4(qbase + swz128((uint32_t)((c >> 3) * kRows + qr), c & 7), qf[i][0], qf[i][1], qf[i][2],
+                            qf[i][3]);
+                }
+            }
+#pragma unroll
             for (int nd = 0; nd < 8; ++nd) o_acc[nd][0] = o_acc[nd][1] = o_acc[nd][2] = o_acc[nd][3] = 0.f;
             m_r[0] = m_r[1] = -INFINITY;
             l_r[0] = l_r[1] = 0.f;
@@ -276,31 +301,46 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
             __syncwarp();
         }
 
-        // ---- S = Q K^T for keys 8w .. 8w+7 (16 rows x 8 keys), even / odd k-steps in two chains
-        float sacc[4] = {0.f, 0.f, 0.f, 0.f}, sodd[4] = {0.f, 0.f, 0.f, 0.f};
+        // ---- S = Q K^T: this warp's k-steps for all 64 keys (eight n-tiles, independent chains),
+        // then the partial sums meet in shared memory and the warp adds up its keys 8w .. 8w+7
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            // B matrices (ldmatrix.x4): keys 8w + (lane & 7) of chunk 2 kd + (lane >> 3) for two
-            // k-steps kd, kd + 1
-            const int kk = 8 * w + (lane & 7);
-            const int b = kk >> br_shift, r = kk & (BR - 1);
-            const uint32_t kbase = stage + b * run_bytes;
-#pragma unroll 6
-            for (int kd = 0; kd < kQK / 16; kd += 2) {
-                uint32_t qa0[4], qa1[4];
-                {
-                    const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int c0 = 2 * kd + (lane >> 4), c1 = c0 + 2;
-                    ldsm_x4(qbase + swz128((uint32_t)((c0 >> 3) * kRows + qr), c0 & 7), qa0[0], qa0[1], qa0[2], qa0[3]);
-                    ldsm_x4(qbase + swz128((uint32_t)((c1 >> 3) * kRows + qr), c1 & 7), qa1[0], qa1[1], qa1[2], qa1[3]);
-                }
-                const int c = 2 * kd + (lane >> 3);  // chunk of this lane's matrix
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kbase + swz128((uint32_t)((c >> 3) * BR + r), c & 7), b0, b1, b2, b3);
-                mma16816<F16>(sacc, qa0, b0, b1);
-                mma16816<F16>(sodd, qa1, b2, b3);
-            }
+            float sp[8][4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[e] += sodd[e];
+            for (int nt = 0; nt < 8; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
+#pragma unroll
+            for (int i = 0; i < kMaxWarpSteps; ++i) {
+                if (i < nk) {
+                    const int c = 2 * (kd0 + i) + ((lane >> 3) & 1);  // chunk of this lane's matrix
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        // keys 16 np + (lane & 7) (+ 8 for lanes 16-31): b0, b1 the first n-tile,
+                        // b2, b3 the second
+                        const int kk = 16 * np + (lane & 7) + (lane >> 4) * 8;
+                        const int b = kk >> br_shift, r = kk & (BR - 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(stage + b * run_bytes + swz128((uint32_t)((c >> 3) * BR + r), c & 7), b0, b1, b2, b3);
+                        mma16816<F16>(sp[2 * np], qf[i], b0, b1);
+                        mma16816<F16>(sp[2 * np + 1], qf[i], b2, b3);
+                    }
+                }
+            }
+            const int r0 = lane >> 2, qq = 2 * (lane & 3);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                *reinterpret_cast<float2*>(&red_s[w][r0][8 * nt + qq]) = make_float2(sp[nt][0], sp[nt][1]);
+                *reinterpret_cast<float2*>(&red_s[w][r0 + 8][8 * nt + qq]) = make_float2(sp[nt][2], sp[nt][3]);
+            }
+            if (!exchange(x_s, xph_s)) return;
+#pragma unroll
+            for (int ww = 0; ww < kMlaCW; ++ww) {
+                const float2 u = *reinterpret_cast<const float2*>(&red_s[ww][r0][8 * w + qq]);
+                const float2 v = *reinterpret_cast<const float2*>(&red_s[ww][r0 + 8][8 * w + qq]);
+                sacc[0] += u.x;
+                sacc[1] += u.y;
+                sacc[2] += v.x;
+                sacc[3] += v.y;
+            }
         }
         // ---- scale, soft cap, masks (log2 domain); sacc[e]: row (lane / 4) + 8 (e >> 1), key
         // 8w + 2 (lane % 4) + (e & 1)
@@ -376,8 +416,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
             *reinterpret_cast<uint32_t*>(smem + (pbuf - smem0) + swz128((uint32_t)row, (uint32_t)w) + 4 * (lane & 3)) =
                 pack2<F16>(p0, p1);
         }
-        // P complete.  The next stage's P and maxima are written only after the next x_max
-        // exchange, which every warp reaches after its PV of this stage.
+        // P complete.  The next stage's partial S, maxima and P are written only after this
+        // warp's PV of this stage; every warp has read this stage's partial S and maxima before
+        // it arrives here.
         if (!exchange(x_p, xph_p)) return;
 
         // ---- O += P V: this warp's value columns 64w .. 64w+63 (column block w of the rows)

@@ -56,7 +56,10 @@ def test_peaks_fallback_and_measured(tmp_path, monkeypatch):
 
 
 def test_recorded_traffic_needs_the_current_sources(tmp_path, monkeypatch):
-    sha = bench.sources_sha(bench.KERNEL_SOURCES["decode_attention"])
+    import rpa_inputs as ri
+
+    src = bench.kernel_sources(ri.workload("tiny"), "decode_attention")
+    sha = bench.sources_sha(src)
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "kernel_traffic.txt").write_text(
         "# comment\n"
@@ -65,9 +68,36 @@ def test_recorded_traffic_needs_the_current_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     # sources_sha reads the kernel files relative to ROOT: keep them readable from the repo
     monkeypatch.setattr(bench, "sources_sha", lambda names: sha)
-    assert bench.recorded_traffic("decode_attention", "decode") == 123456.0
-    assert bench.recorded_traffic("decode_attention", "fp8_window") is None
-    assert bench.recorded_traffic("combine", "decode") is None
+    assert bench.recorded_traffic("decode_attention", "decode", src) == 123456.0
+    assert bench.recorded_traffic("decode_attention", "fp8_window", src) is None
+    assert bench.recorded_traffic("combine", "decode", src) is None
+
+
+def test_kernel_sources_follow_the_routing():
+    """Each workload's dominant kernel is charged to its own source file."""
+    import rpa_inputs as ri
+
+    want = {("decode", "decode_attention"): "rpa_decode.cu", ("long_prefill", "prefill_attention"): "rpa_prefill_tc.cu",
+            ("fp8_window", "prefill_attention"): "rpa_prefill_tc8.cu",
+            ("long_prefill_d256", "prefill_attention"): "rpa_prefill_tc8.cu",
+            ("mla_decode", "prefill_attention"): "rpa_mla.cu"}
+    for (w, k), f in want.items():
+        src = bench.kernel_sources(_shape_only(w), k)
+        assert src[0].endswith(f) and src[1].endswith("rpa_internal.cuh"), (w, src)
+
+
+def _shape_only(name):
+    """The configuration fields of a named workload without drawing its tensors."""
+    import types
+
+    import rpa_inputs as ri
+
+    shapes = {"decode": ("bf16", 128, "split"), "long_prefill": ("bf16", 128, "split"),
+              "fp8_window": ("fp8_e4m3", 256, "split"), "long_prefill_d256": ("bf16", 256, "split"),
+              "mla_decode": ("bf16", 576, "latent")}
+    kv, d, layout = shapes[name]
+    assert name in ri.WORKLOADS
+    return types.SimpleNamespace(kv_dtype=kv, head_dim=d, kv_layout=layout)
 
 
 def test_output_shape_follows_the_value_width():

@@ -14,10 +14,10 @@
 //                   then per 64-key stage one bulk tensor copy per page run of the latent rows
 //                   ("ragged_paged.zig": createKvAsyncCopyDescriptors, logical page ->
 //                   page_indices[s, page]) into a 2-stage mbarrier ring, crossing item boundaries.
-//   8 consumer      S = Q K^T: warp w takes k-steps [36w/8, 36(w+1)/8) of the 576-wide
-//   warps           contraction for all 64 keys of the stage (mma.sync, fp32; its Q slice stays in
-//                   registers for the item, eight independent accumulator chains), the partial
-//                   sums meet in shared memory and warp w adds up keys 8w .. 8w+7; scale / soft cap
+//   8 consumer      S = Q K^T: warp w takes k-steps [9 (w % 4), 9 (w % 4) + 9) of the 576-wide
+//   warps           contraction for keys 32 (w / 4) .. + 31 of the stage (mma.sync, fp32; its Q
+//                   slice stays in registers for the item, four independent accumulator chains),
+//                   the partial sums meet in shared memory and warp w adds up keys 8w .. 8w+7; scale / soft cap
 //                   / masks in the log2 domain; the row maxima meet in shared memory, every warp
 //                   forms the same running max, writes its P (bf16 / f16) to shared memory and
 //                   keeps its own partial row sum; then
@@ -55,7 +55,9 @@ constexpr int kMlaSmem = kNS * kStage + 2 * kQBuf + kPBuf + 1024;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kSPad = 72;                      // row stride (floats) of the partial-S exchange
 constexpr int kKSteps = kQK / 16;              // k-steps of the QK contraction (36)
-constexpr int kMaxWarpSteps = (kKSteps + kMlaCW - 1) / kMlaCW;  // 5
+constexpr int kKSlices = 4;                    // the contraction split four ways, the keys two ways
+constexpr int kSliceSteps = kKSteps / kKSlices;  // 9
+static_assert(kKSlices * 2 == kMlaCW && kKSteps % kKSlices == 0, "warp split of S");
 
 enum MlaMeta : int { mSeq = 0, mHead, mQStart, mQl, mKl, mKvBegin, mKvEnd, mPart, mTok0, mNtok, mSt, mNst, mKey0,
                      mQb, mStop, mWords = 16 };
@@ -80,9 +82,9 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
     __shared__ int meta[kNS][mWords];
     __shared__ float red_m[kMlaCW][kRows];  // per warp: its keys' row maxima (this stage)
     __shared__ float red_l[kMlaCW][kRows];  // per warp: its row sums (item end)
-    // per warp: its partial S over its k-steps, [row][key] with rows padded to 72 floats (the
-    // fragment stores and loads of a half warp then touch 32 distinct banks)
-    __shared__ __align__(16) float red_s[kMlaCW][kRows][kSPad];
+    // per k-slice: the partial S over its k-steps (both key halves), [row][key] with rows padded to
+    // 72 floats (the fragment stores and loads of a half warp then touch 32 distinct banks)
+    __shared__ __align__(16) float red_s[kKSlices][kRows][kSPad];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const AttnParams& a = p.a;
@@ -237,9 +239,11 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
     const uint32_t run_bytes = (uint32_t)(kCBQ * BR * 128);
     int s = 0;
     uint32_t ph = 0, xph_s = 0, xph_max = 0, xph_p = 0, xph_sum = 0;
-    // this warp's k-steps of the QK contraction and its Q fragments for them (loaded per item)
-    const int kd0 = (kKSteps * w) / kMlaCW, nk = (kKSteps * (w + 1)) / kMlaCW - kd0;
-    uint32_t qf[kMaxWarpSteps][4];
+    // this warp's k-slice of the QK contraction and key half of the stage, and its Q fragments for
+    // the slice (loaded per item)
+    const int kslice = w & (kKSlices - 1), khalf = w / kKSlices;
+    const int kd0 = kslice * kSliceSteps;
+    uint32_t qf[kSliceSteps][4];
     uint32_t qph[2] = {0u, 0u};
     // every consumer warp arrives, then waits (bounded) for the others
     auto exchange = [&](uint64_t& bar, uint32_t& xph) -> bool {
@@ -270,13 +274,10 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
             if (!mbar_wait(smem_u32(&q_full[qb]), qph[qb], ctrl, tmo)) return;
             qph[qb] ^= 1u;
 #pragma unroll
-            for (int i = 0; i < kMaxWarpSteps; ++i) {
-                if (i < nk) {
-                    const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int c = 2 * (kd0 + i) + (lane >> 4);
-                    ldsm_x4(qbase + swz128((uint32_t)((c >> 3) * kRows + qr), c & 7), qf[i][0], qf[i][1], qf[i][2],
-                            qf[i][3]);
-                }
+            for (int i = 0; i < kSliceSteps; ++i) {
+                const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int c = 2 * (kd0 + i) + (lane >> 4);
+                ldsm_x4(qbase + swz128((uint32_t)((c >> 3) * kRows + qr), c & 7), qf[i][0], qf[i][1], qf[i][2], qf[i][3]);
             }
 #pragma unroll
             for (int nd = 0; nd < 8; ++nd) o_acc[nd][0] = o_acc[nd][1] = o_acc[nd][2] = o_acc[nd][3] = 0.f;
@@ -301,41 +302,40 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
             __syncwarp();
         }
 
-        // ---- S = Q K^T: this warp's k-steps for all 64 keys (eight n-tiles, independent chains),
+        // ---- S = Q K^T: this warp's k-slice for its 32 keys (four n-tiles, independent chains),
         // then the partial sums meet in shared memory and the warp adds up its keys 8w .. 8w+7
         float sacc[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            float sp[8][4];
+            float sp[4][4];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
+            for (int nt = 0; nt < 4; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
 #pragma unroll
-            for (int i = 0; i < kMaxWarpSteps; ++i) {
-                if (i < nk) {
-                    const int c = 2 * (kd0 + i) + ((lane >> 3) & 1);  // chunk of this lane's matrix
+            for (int i = 0; i < kSliceSteps; ++i) {
+                const int c = 2 * (kd0 + i) + ((lane >> 3) & 1);  // chunk of this lane's matrix
 #pragma unroll
-                    for (int np = 0; np < 4; ++np) {
-                        // keys 16 np + (lane & 7) (+ 8 for lanes 16-31): b0, b1 the first n-tile,
-                        // b2, b3 the second
-                        const int kk = 16 * np + (lane & 7) + (lane >> 4) * 8;
-                        const int b = kk >> br_shift, r = kk & (BR - 1);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(stage + b * run_bytes + swz128((uint32_t)((c >> 3) * BR + r), c & 7), b0, b1, b2, b3);
-                        mma16816<F16>(sp[2 * np], qf[i], b0, b1);
-                        mma16816<F16>(sp[2 * np + 1], qf[i], b2, b3);
-                    }
+                for (int np = 0; np < 2; ++np) {
+                    // keys 32 khalf + 16 np + (lane & 7) (+ 8 for lanes 16-31): b0, b1 the first
+                    // n-tile, b2, b3 the second
+                    const int kk = 32 * khalf + 16 * np + (lane & 7) + (lane >> 4) * 8;
+                    const int b = kk >> br_shift, r = kk & (BR - 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(stage + b * run_bytes + swz128((uint32_t)((c >> 3) * BR + r), c & 7), b0, b1, b2, b3);
+                    mma16816<F16>(sp[2 * np], qf[i], b0, b1);
+                    mma16816<F16>(sp[2 * np + 1], qf[i], b2, b3);
                 }
             }
             const int r0 = lane >> 2, qq = 2 * (lane & 3);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                *reinterpret_cast<float2*>(&red_s[w][r0][8 * nt + qq]) = make_float2(sp[nt][0], sp[nt][1]);
-                *reinterpret_cast<float2*>(&red_s[w][r0 + 8][8 * nt + qq]) = make_float2(sp[nt][2], sp[nt][3]);
+            for (int nt = 0; nt < 4; ++nt) {
+                const int key = 32 * khalf + 8 * nt + qq;
+                *reinterpret_cast<float2*>(&red_s[kslice][r0][key]) = make_float2(sp[nt][0], sp[nt][1]);
+                *reinterpret_cast<float2*>(&red_s[kslice][r0 + 8][key]) = make_float2(sp[nt][2], sp[nt][3]);
             }
             if (!exchange(x_s, xph_s)) return;
 #pragma unroll
-            for (int ww = 0; ww < kMlaCW; ++ww) {
-                const float2 u = *reinterpret_cast<const float2*>(&red_s[ww][r0][8 * w + qq]);
-                const float2 v = *reinterpret_cast<const float2*>(&red_s[ww][r0 + 8][8 * w + qq]);
+            for (int ks = 0; ks < kKSlices; ++ks) {
+                const float2 u = *reinterpret_cast<const float2*>(&red_s[ks][r0][8 * w + qq]);
+                const float2 v = *reinterpret_cast<const float2*>(&red_s[ks][r0 + 8][8 * w + qq]);
                 sacc[0] += u.x;
                 sacc[1] += u.y;
                 sacc[2] += v.x;

@@ -338,9 +338,9 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
             }
 
             // ---- S = Q K^T  (16 rows x 16 keys); even and odd k-steps accumulate separately
-            // (two independent MMA chains per n-block), summed at the end -- at D <= 128: at D 256
+            // (two independent MMA chains per n-block), summed at the end -- at D 64: at D 128 and 256
             // the registers are spent on Q and O, and one chain per n-block keeps them unspilled
-            constexpr bool kTwo = D <= 128;
+            constexpr bool kTwo = D <= 64;
             float sacc[2][4], sodd[2][4];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
@@ -804,22 +804,10 @@ __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_de
     decode_body<D, KT, ROWS>(kvmap, qmap, p);
 }
 
-// 16-row tiles at D 128 need more registers than the launch bound for two CTAs per SM lets the
-// compiler assume (it spilled at 168): 200 a thread still fits two CTAs (2 x 160 x 200 <= 65536).
-constexpr int kDec16Regs = 200;
-template <int D, int KT, int ROWS>
-__global__ void __maxnreg__(kDec16Regs) rpa_decode_attn_r(const __grid_constant__ CUtensorMap kvmap,
-                                                         const __grid_constant__ CUtensorMap qmap, const DecParams p) {
-    decode_body<D, KT, ROWS>(kvmap, qmap, p);
-}
-
 template <int D, int KT, int ROWS>
 struct DecKern {
     using Gm = DecGeom<D, KT, ROWS>;
-    static constexpr auto fn() {
-        if constexpr (D == 128 && ROWS == 16) return rpa_decode_attn_r<D, KT, ROWS>;
-        else return rpa_decode_attn<D, KT, ROWS>;
-    }
+    static constexpr auto fn() { return rpa_decode_attn<D, KT, ROWS>; }
     static cudaError_t prepare(int* bps) {
         cudaError_t e = cudaFuncSetAttribute(fn(), cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
         if (e != cudaSuccess) return e;

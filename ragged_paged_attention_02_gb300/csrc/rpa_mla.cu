@@ -15,8 +15,8 @@
 //                   ("ragged_paged.zig": createKvAsyncCopyDescriptors, logical page ->
 //                   page_indices[s, page]) into a 2-stage mbarrier ring, crossing item boundaries.
 //   8 consumer      S = Q K^T: warp w takes k-steps [9 (w % 4), 9 (w % 4) + 9) of the 576-wide
-//   warps           contraction for keys 32 (w / 4) .. + 31 of the stage (mma.sync, fp32; its Q
-//                   slice stays in registers for the item, four independent accumulator chains),
+//   warps           contraction for keys 32 (w / 4) .. + 31 of the stage (mma.sync, fp32; four
+//                   independent accumulator chains; its Q fragments from the item's Q buffer),
 //                   the partial sums meet in shared memory and warp w adds up keys 8w .. 8w+7; scale / soft cap
 //                   / masks in the log2 domain; the row maxima meet in shared memory, every warp
 //                   forms the same running max, writes its P (bf16 / f16) to shared memory and
@@ -66,11 +66,8 @@ __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
     return line * 128u + (((chunk ^ line) & 7u) << 4);
 }
 
-// one CTA per SM: nine warps x 224 registers fit the register file (the launch bound alone lets the
-// compiler assume fewer, and it spilled)
-constexpr int kMlaRegs = 224;
 template <bool F16>
-__global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUtensorMap kvmap,
+__global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_constant__ CUtensorMap kvmap,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -239,11 +236,9 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
     const uint32_t run_bytes = (uint32_t)(kCBQ * BR * 128);
     int s = 0;
     uint32_t ph = 0, xph_s = 0, xph_max = 0, xph_p = 0, xph_sum = 0;
-    // this warp's k-slice of the QK contraction and key half of the stage, and its Q fragments for
-    // the slice (loaded per item)
+    // this warp's k-slice of the QK contraction and key half of the stage
     const int kslice = w & (kKSlices - 1), khalf = w / kKSlices;
     const int kd0 = kslice * kSliceSteps;
-    uint32_t qf[kSliceSteps][4];
     uint32_t qph[2] = {0u, 0u};
     // every consumer warp arrives, then waits (bounded) for the others
     auto exchange = [&](uint64_t& bar, uint32_t& xph) -> bool {
@@ -273,12 +268,7 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
         if (st == 0) {
             if (!mbar_wait(smem_u32(&q_full[qb]), qph[qb], ctrl, tmo)) return;
             qph[qb] ^= 1u;
-#pragma unroll
-            for (int i = 0; i < kSliceSteps; ++i) {
-                const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int c = 2 * (kd0 + i) + (lane >> 4);
-                ldsm_x4(qbase + swz128((uint32_t)((c >> 3) * kRows + qr), c & 7), qf[i][0], qf[i][1], qf[i][2], qf[i][3]);
-            }
+
 #pragma unroll
             for (int nd = 0; nd < 8; ++nd) o_acc[nd][0] = o_acc[nd][1] = o_acc[nd][2] = o_acc[nd][3] = 0.f;
             m_r[0] = m_r[1] = -INFINITY;
@@ -311,6 +301,13 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
             for (int nt = 0; nt < 4; ++nt) sp[nt][0] = sp[nt][1] = sp[nt][2] = sp[nt][3] = 0.f;
 #pragma unroll
             for (int i = 0; i < kSliceSteps; ++i) {
+                // the Q fragment of k-step kd0 + i (A, 16 rows x 16): read from the item's Q buffer
+                uint32_t qa[4];
+                {
+                    const int qr = (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int qc = 2 * (kd0 + i) + (lane >> 4);
+                    ldsm_x4(qbase + swz128((uint32_t)((qc >> 3) * kRows + qr), qc & 7), qa[0], qa[1], qa[2], qa[3]);
+                }
                 const int c = 2 * (kd0 + i) + ((lane >> 3) & 1);  // chunk of this lane's matrix
 #pragma unroll
                 for (int np = 0; np < 2; ++np) {
@@ -320,8 +317,8 @@ __global__ void __maxnreg__(kMlaRegs) rpa_mla_attn(const __grid_constant__ CUten
                     const int b = kk >> br_shift, r = kk & (BR - 1);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(stage + b * run_bytes + swz128((uint32_t)((c >> 3) * BR + r), c & 7), b0, b1, b2, b3);
-                    mma16816<F16>(sp[2 * np], qf[i], b0, b1);
-                    mma16816<F16>(sp[2 * np + 1], qf[i], b2, b3);
+                    mma16816<F16>(sp[2 * np], qa, b0, b1);
+                    mma16816<F16>(sp[2 * np + 1], qa, b2, b3);
                 }
             }
             const int r0 = lane >> 2, qq = 2 * (lane & 3);

@@ -255,6 +255,31 @@ def test_full_workloads(name):
         assert_close(got[rows[:, 0], rows[:, 1]], ref, p.kv_dtype, name)
 
 
+@pytest.mark.parametrize("kw,dec_bps,pf_bps", [
+    # 8-row decode tiles: three CTAs per SM at D 128; 16-row tiles: two; the tensor-memory and latent
+    # kernels: one
+    (dict(num_q_heads=32, num_kv_heads=8, head_dim=128), 3, 1),
+    (dict(num_q_heads=32, num_kv_heads=2, head_dim=128), 2, 1),
+    (dict(num_q_heads=16, num_kv_heads=1, kv_layout="latent", head_dim=576, v_head_dim=512, page_size=64,
+          sm_scale=1 / 24), None, 1),
+])
+def test_resident_ctas_per_sm_as_designed(kw, dec_bps, pf_bps):
+    """The kernels' register and shared-memory budgets give the occupancy they were designed for
+    (rpa_read_plan info[13], info[14]): a budget over by a few registers silently halves a decode
+    kernel's CTAs per SM."""
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    p = ri.random_small(51, num_seqs=4, max_q=3, max_kv=300, **kw)
+    att = RaggedPagedAttention(**p.cfg_dict())
+    att.forward(*to_dev(p), p.num_seqs)
+    info = att.plan(max_items=1)[0]
+    assert info[0] == 0
+    if dec_bps is not None:
+        assert int(info[13]) == dec_bps
+    assert int(info[14]) == pf_bps
+    att.close()
+
+
 def test_planner_matches_python_rederivation():
     from plan_model import plan
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention

@@ -72,7 +72,10 @@ struct G8 {
     static constexpr int QSTAGE = kM * 128;            // Q staging: one column block x 128 rows
     static constexpr int RAW = DIRECT ? 0 : kBN * 2 * D;  // one raw 8-bit stage (K and V); none in direct mode
     static constexpr int T16 = CB * kBN * 128;         // one f16 K (or V) tile
-    static constexpr int DATA = QSTAGE + 2 * RAW + 4 * T16;
+    // K and V tile buffers: 2 in 8-bit mode (behind the raw ring), 3 in direct mode (the copies land
+    // in them, so a third buffer starts each tile's copies a tile earlier)
+    static constexpr int NB = DIRECT ? 3 : 2;
+    static constexpr int DATA = QSTAGE + 2 * RAW + 2 * NB * T16;
     static constexpr int SMEM = DATA + 1024;
     static constexpr uint32_t TM_Q = 0;                // Q: D/2 columns
     static constexpr uint32_t TM_S0 = D / 2, TM_S1 = D / 2 + kBN;
@@ -198,8 +201,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     __shared__ __align__(8) uint64_t raw_full[2], raw_empty[2];
     // per S / f16 buffer b: K converted; QK done (S ready, K buffer free); P and V ready (softmax
     // and converter warps); PV done (V buffer free, O holds the PV)
-    __shared__ __align__(8) uint64_t k_full[2], qk_done[2], pv_ready[2], pv_done[2];
-    __shared__ __align__(8) uint64_t v_land[2];  // direct mode: V(t) copied
+    // per S buffer (t mod 2): QK done, P and V ready, PV done; per K/V buffer (t mod NB): K ready,
+    // and in direct mode V copied and the K / V buffer free again (the MMAs that read it are done)
+    __shared__ __align__(8) uint64_t qk_done[2], pv_ready[2], pv_done[2];
+    __shared__ __align__(8) uint64_t k_full[3], v_land[3], k_free[3], v_free[3];
     __shared__ __align__(8) uint64_t o_full, o_free;
     __shared__ __align__(8) uint64_t xchg[4];  // per lane quadrant: the two softmax warps' row maxima / sums
     __shared__ float xm[2][2][kM];             // [tile parity][key half][row] partial row maxima
@@ -215,8 +220,11 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     const uint32_t smem0 = smem_u32(smem);
     const uint32_t q_stage = smem0;                                 // Q staging (bf16)
     const uint32_t raw_base = q_stage + Gm::QSTAGE;                 // 2 raw fp8 stages
-    const uint32_t k16_base = raw_base + 2 * Gm::RAW;               // 2 f16 K tiles
-    const uint32_t v16_base = k16_base + 2 * Gm::T16;               // 2 f16 V tiles
+    const uint32_t k16_base = raw_base + 2 * Gm::RAW;               // NB 16-bit K tiles
+    const uint32_t v16_base = k16_base + Gm::NB * Gm::T16;          // NB 16-bit V tiles
+    // K/V buffer of global tile g and the parity of its use of that buffer
+    auto kvb = [](uint32_t g) -> int { return DIRECT ? (int)(g % 3u) : (int)(g & 1u); };
+    auto kvpar = [](uint32_t g) -> uint32_t { return DIRECT ? (g / 3u) & 1u : (g >> 1) & 1u; };
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -224,12 +232,16 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             mbar_init(smem_u32(&meta_free[i]), 17);  // 8 softmax + 8 converter warps + MMA thread
             mbar_init(smem_u32(&raw_full[i]), 1);
             mbar_init(smem_u32(&raw_empty[i]), kNConv);
-            // K(t) ready: the converters' arrivals, or in direct mode the copies themselves
-            mbar_init(smem_u32(&k_full[i]), DIRECT ? 1 : kNConv);
-            mbar_init(smem_u32(&v_land[i]), 1);
             mbar_init(smem_u32(&qk_done[i]), 1);
             mbar_init(smem_u32(&pv_ready[i]), 8 + kNConv);
             mbar_init(smem_u32(&pv_done[i]), 1);
+        }
+        for (int i = 0; i < 3; ++i) {
+            // K(t) ready: the converters' arrivals, or in direct mode the copies themselves
+            mbar_init(smem_u32(&k_full[i]), DIRECT ? 1 : kNConv);
+            mbar_init(smem_u32(&v_land[i]), 1);
+            mbar_init(smem_u32(&k_free[i]), 1);
+            mbar_init(smem_u32(&v_free[i]), 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 64);
         mbar_init(smem_u32(&q_full), 1);
@@ -327,15 +339,15 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     win = (win0 + lane < a.P) ? __ldg(ptab + win0 + lane) : 0;
                 }
                 if constexpr (DIRECT) {
-                    // K(t) into K tile b2 once QK(t-2) is done, V(t) into V tile b2 once PV(t-2) is
+                    // K(t) into K buffer b once QK(t-3) is done, V(t) into V buffer b once PV(t-3) is
                     // done: one copy per (page run, 128-byte column block), BR rows each
-                    const int b2 = tgp & 1;
-                    const uint32_t par = (tgp >> 1) & 1u;
+                    const int b2 = kvb(tgp);
+                    const uint32_t par = kvpar(tgp);
                     ++tgp;
                     const int tasks = runs * Gm::CB;
 #pragma unroll 1
                     for (int kv = 0; kv < 2 && ok; ++kv) {
-                        if (!mbar_wait(smem_u32(kv ? &pv_done[b2] : &qk_done[b2]), par ^ 1u, ctrl, tmo)) {
+                        if (!mbar_wait(smem_u32(kv ? &v_free[b2] : &k_free[b2]), par ^ 1u, ctrl, tmo)) {
                             ok = false;
                             break;
                         }
@@ -463,13 +475,14 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     // the copies wrote V(t) into its tile: on the tile's edges, zero this warp's rows of
                     // keys outside [kv_begin, kv_end) (page tails may hold any bits; runs outside the
                     // range were not copied), then V is ready
-                    if (!mbar_wait(smem_u32(&v_land[b2]), par, ctrl, tmo)) {
+                    const int vb = kvb(tg);
+                    if (!mbar_wait(smem_u32(&v_land[vb]), kvpar(tg), ctrl, tmo)) {
                         ok = false;
                         break;
                     }
                     const int k_lo = key0 + t * kBN;
                     if (k_lo < kv_begin || k_lo + kBN > kv_end) {
-                        uint8_t* vt = smem + (v16_base - smem0) + b2 * Gm::T16;
+                        uint8_t* vt = smem + (v16_base - smem0) + vb * Gm::T16;
                         for (int i = lane; i < kConvRows * Gm::CB * 8; i += 32) {
                             const int key = kConvRows * cw + i / (Gm::CB * 8);
                             const int rem = i % (Gm::CB * 8);
@@ -556,10 +569,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     bool did = false;
                     if (tq < nt && tq <= tp + 1) {
                         const uint32_t g = tg + tq;
-                        const int b2 = g & 1;
-                        if (mbar_test(smem_u32(&k_full[b2]), (g >> 1) & 1u)) {
+                        const int b2 = g & 1, kb = kvb(g);
+                        if (mbar_test(smem_u32(&k_full[kb]), kvpar(g))) {
                             tc_fence_after();
-                            const uint64_t kd = umma_sdesc(k16_base + b2 * Gm::T16, 16, 1024);
+                            const uint64_t kd = umma_sdesc(k16_base + kb * Gm::T16, 16, 1024);
                             const uint32_t kd_lo = (uint32_t)kd, kd_hi = (uint32_t)(kd >> 32);
                             const uint32_t sd = tmem + (b2 ? Gm::TM_S1 : Gm::TM_S0), qa = tmem + Gm::TM_Q;
                             umma_ts_c<0>(sd, qa, kd_lo, kd_hi, idesc_qk);
@@ -568,6 +581,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                                 umma_ts_c<1>(sd, qa + kk * 8, kd_lo + ((kk >> 2) * (kBN * 128) + (kk & 3) * 32) / 16, kd_hi,
                                              idesc_qk);
                             umma_commit(smem_u32(&qk_done[b2]));
+                            if constexpr (DIRECT) umma_commit(smem_u32(&k_free[kb]));
                             if (tq == nt - 1) umma_commit(smem_u32(&qt_free));
                             ++tq;
                             did = true;
@@ -581,7 +595,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         if (mbar_test(smem_u32(&pv_ready[b2]), par) &&
                             (!first || items == 0 || mbar_test(smem_u32(&o_free), (items - 1) & 1u))) {
                             tc_fence_after();
-                            const uint64_t vd = umma_sdesc(v16_base + b2 * Gm::T16, kBN * 128, 1024);
+                            const int vb = kvb(g);
+                            const uint64_t vd = umma_sdesc(v16_base + vb * Gm::T16, kBN * 128, 1024);
                             const uint32_t vd_lo = (uint32_t)vd, vd_hi = (uint32_t)(vd >> 32);
                             const uint32_t od = tmem + Gm::TM_O, pa = tmem + (b2 ? Gm::TM_S1 : Gm::TM_S0);
                             if (first)
@@ -592,6 +607,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                             for (int kk = 1; kk < kBN / 16; ++kk)
                                 umma_ts_c<1>(od, pa + kk * 8, vd_lo + kk * 16 * 128 / 16, vd_hi, idesc_pv);
                             umma_commit(smem_u32(&pv_done[b2]));
+                            if constexpr (DIRECT) umma_commit(smem_u32(&v_free[vb]));
                             ++tp;
                             did = true;
                         }
@@ -609,7 +625,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const uint32_t pp = (gp >> 1) & 1u;
                         const bool qk_next = tq < nt && tq <= tp + 1 && (tp >= tq || (idle & 1));
                         if (qk_next)
-                            mbar_try_wait_for(smem_u32(&k_full[gq & 1]), (gq >> 1) & 1u, kIssueNapNs);
+                            mbar_try_wait_for(smem_u32(&k_full[kvb(gq)]), kvpar(gq), kIssueNapNs);
                         else if (tp < tq)
                             mbar_try_wait_for(smem_u32(&pv_ready[gp & 1]), pp, kIssueNapNs);
                     }

@@ -206,8 +206,9 @@ constexpr int kTcRows = 128;  // rows of a tensor-memory prefill tile
 int encode_kv_map(CUtensorMap* m, const void* kv, int byte_elems, long long N, int ps, int Hkv, int D, int BR);
 int encode_q_map(CUtensorMap* m, const void* q, long long T, int Hq, int D, int G, int Tt);
 int encode_kv_map_runs(CUtensorMap* m, const void* kv, int byte_elems, long long N, int ps, int Hkv, int D, int BR);
-// latent cache [N, ps, Hkv, D] (2-byte elements): one box = BR slots of one kv head's row
-int encode_kv_map_latent(CUtensorMap* m, const void* kv, long long N, int ps, int Hkv, int D, int BR);
+// cache [N, ps, H, D] (2-byte elements; the split cache as H = 2 Hkv): one box = BR slots of one
+// row, all its column blocks
+int encode_kv_map_heads(CUtensorMap* m, const void* kv, long long N, int ps, int H, int D, int BR);
 // occupancy / attributes (call once per device)
 cudaError_t attn_prepare(int D, int kt, int* pf_blocks_per_sm);
 size_t plan_smem_bytes();
@@ -229,6 +230,11 @@ struct KernelSet {
     int sms, dec_bps, pf_bps;
     int max_dec_units, max_pf_units, max_units, max_part, max_comb;
 };
+// The 64-key-tile kernel in direct mode (2-byte K/V) copies a page run's whole K (or V) tile in
+// one box when a run is a whole tile (BR = 64, the map from encode_kv_map_heads); with smaller
+// page runs, one box per (run, column block) (the map from encode_kv_map)
+constexpr int kTc8Keys = 64;
+inline bool tc8_whole_tiles(const KernelSet& ks) { return ks.tc8 && !kt_8bit(ks.kt) && ks.BR == kTc8Keys; }
 struct Workspace {
     int* ctrl;
     int* seq_scratch;

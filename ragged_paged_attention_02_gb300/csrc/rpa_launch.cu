@@ -300,13 +300,16 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     const int byte_kv = kt_8bit(ks.kt) ? 1 : 0;
     if (has_q) {
         if (maps->kv_ptr != kv_pages) {
-            if ((ks.mla ? encode_kv_map_latent(&maps->kv, kv_pages, c.total_num_pages, (int)c.page_size,
-                                               (int)c.num_kv_heads, ks.D, ks.BR)
+            if ((ks.mla ? encode_kv_map_heads(&maps->kv, kv_pages, c.total_num_pages, (int)c.page_size,
+                                              (int)c.num_kv_heads, ks.D, ks.BR)
                         : encode_kv_map_runs(&maps->kv, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
                                              (int)c.num_kv_heads, ks.D, ks.BR)) != 0 ||
                 ((ks.tc || (ks.tc8 && !byte_kv)) &&
-                 encode_kv_map(&maps->kv_pf, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
-                               (int)c.num_kv_heads, ks.D, ks.BR) != 0)) {
+                 (tc8_whole_tiles(ks)
+                      ? encode_kv_map_heads(&maps->kv_pf, kv_pages, c.total_num_pages, (int)c.page_size,
+                                            2 * (int)c.num_kv_heads, ks.D, ks.BR)
+                      : encode_kv_map(&maps->kv_pf, kv_pages, byte_kv, c.total_num_pages, (int)c.page_size,
+                                      (int)c.num_kv_heads, ks.D, ks.BR)) != 0)) {
                 maps->kv_ptr = nullptr;
                 return fail(RPA_ERR_INVALID_ARG);
             }

@@ -31,8 +31,9 @@
 //
 // 2-byte K/V (bf16 or f16) at D = 256 run on the same pipeline in direct mode:
 // the producer copies K and V page runs straight into the 128-byte-swizzled
-// tiles the MMAs read (K once the QK two tiles back is done, V once that
-// tile's PV is done), the MMAs run in the K/V type (P in it too), and the
+// tiles the MMAs read (one copy per K or V tile when a page run spans the
+// 64 keys; K once the QK three tiles back is done, V once that tile's PV is
+// done), the MMAs run in the K/V type (P in it too), and the
 // converter warps only zero the V rows of keys outside [kv_begin, kv_end) on
 // a tile's edges before signalling V ready (K rows there are masked in S).
 //
@@ -50,7 +51,7 @@ namespace rpa {
 namespace {
 
 constexpr int kM = kTcRows;   // query rows per tile = TMEM lanes
-constexpr int kBN = 64;       // keys per K/V tile
+constexpr int kBN = kTc8Keys;  // keys per K/V tile
 // warps 0-7 softmax (two per TMEM lane quadrant, one per half of the key tile), 8-15 convert
 // (8 key rows of a tile each; 8-11 also convert Q, one TMEM lane quadrant each), 16 producer,
 // 17 MMA
@@ -190,8 +191,9 @@ template <int D, int KT>
 __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __grid_constant__ CUtensorMap kvmap,
                                                                const __grid_constant__ CUtensorMap qmap,
                                                                const TcParams p) {
-    // DIRECT: 2-byte K/V copied straight into the MMA tiles (kvmap: the slot x row map with
-    // 128-byte swizzle); else 8-bit page runs through the raw ring (kvmap: the page-run map)
+    // DIRECT: 2-byte K/V copied straight into the MMA tiles (kvmap, 128-byte swizzle: the slot x
+    // head-row x column-block map when BR = kBN, else the slot x row map); else 8-bit page runs
+    // through the raw ring (kvmap: the page-run map)
     constexpr bool DIRECT = !kt_8bit(KT);
     constexpr bool F16 = kt_f16_mma(KT);  // MMA operands (and P) in f16, else bf16
     using Gm = G8<D, DIRECT>;
@@ -199,12 +201,13 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     __shared__ __align__(8) uint64_t meta_full[2], meta_free[2];
     __shared__ __align__(8) uint64_t q_full, q_empty, q_ready, qt_free;
     __shared__ __align__(8) uint64_t raw_full[2], raw_empty[2];
-    // per S / f16 buffer b: K converted; QK done (S ready, K buffer free); P and V ready (softmax
-    // and converter warps); PV done (V buffer free, O holds the PV)
-    // per S buffer (t mod 2): QK done, P and V ready, PV done; per K/V buffer (t mod NB): K ready,
-    // and in direct mode V copied and the K / V buffer free again (the MMAs that read it are done)
+    // per S buffer (t mod 2): QK done, P ready (softmax warps; in 8-bit mode also V converted: the
+    // converter warps), PV done; per K/V buffer (t mod NB): K ready, and in direct mode V copied, V
+    // ready (its edge rows zeroed: converter warps) and the K / V buffer free again (the MMAs that
+    // read it are done).  Direct mode keeps V ready apart from P ready: V(t + 2) can be ready before
+    // P(t), and each barrier's arrivals must come from one tile at a time.
     __shared__ __align__(8) uint64_t qk_done[2], pv_ready[2], pv_done[2];
-    __shared__ __align__(8) uint64_t k_full[3], v_land[3], k_free[3], v_free[3];
+    __shared__ __align__(8) uint64_t k_full[3], v_land[3], v_ready[3], k_free[3], v_free[3];
     __shared__ __align__(8) uint64_t o_full, o_free;
     __shared__ __align__(8) uint64_t xchg[4];  // per lane quadrant: the two softmax warps' row maxima / sums
     __shared__ float xm[2][2][kM];             // [tile parity][key half][row] partial row maxima
@@ -233,13 +236,14 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             mbar_init(smem_u32(&raw_full[i]), 1);
             mbar_init(smem_u32(&raw_empty[i]), kNConv);
             mbar_init(smem_u32(&qk_done[i]), 1);
-            mbar_init(smem_u32(&pv_ready[i]), 8 + kNConv);
+            mbar_init(smem_u32(&pv_ready[i]), DIRECT ? 8 : 8 + kNConv);
             mbar_init(smem_u32(&pv_done[i]), 1);
         }
         for (int i = 0; i < 3; ++i) {
             // K(t) ready: the converters' arrivals, or in direct mode the copies themselves
             mbar_init(smem_u32(&k_full[i]), DIRECT ? 1 : kNConv);
             mbar_init(smem_u32(&v_land[i]), 1);
+            mbar_init(smem_u32(&v_ready[i]), kNConv);
             mbar_init(smem_u32(&k_free[i]), 1);
             mbar_init(smem_u32(&v_free[i]), 1);
         }
@@ -340,7 +344,9 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 }
                 if constexpr (DIRECT) {
                     // K(t) into K buffer b once QK(t-3) is done, V(t) into V buffer b once PV(t-3) is
-                    // done: one copy per (page run, 128-byte column block), BR rows each
+                    // done: with runs of a whole tile one copy of all column blocks (kvmap from
+                    // encode_kv_map_heads: K of head h is row 2h of a slot, V row 2h + 1), else one
+                    // copy per (page run, 128-byte column block), BR rows each
                     const int b2 = kvb(tgp);
                     const uint32_t par = kvpar(tgp);
                     ++tgp;
@@ -352,6 +358,22 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                             break;
                         }
                         const uint32_t dst0 = (kv ? v16_base : k16_base) + b2 * Gm::T16;
+                        if (BR == kBN) {
+                            const int lp = k_tile / ps;
+                            const int pg = __shfl_sync(0xffffffffu, win, (lp - win0) & 31);
+                            const bool want = k_tile < item.kv_end && k_tile + BR > item.kv_begin;
+                            const bool good = (unsigned)pg < (unsigned)a.N;
+                            const uint32_t fb = smem_u32(kv ? &v_land[b2] : &k_full[b2]);
+                            if (lane == 0) {
+                                if (want && !good) set_status(ctrl, RPA_ERR_BAD_PAGE_INDEX);
+                                mbar_arrive_expect_tx(fb, (want && good) ? (uint32_t)(kBN * D * 2) : 0u);
+                                if (want && good)
+                                    tma_load_3d(dst0, &kvmap, fb, 0, pg * ps + (k_tile - lp * ps),
+                                                (2 * item.head + kv) * Gm::CB);
+                            }
+                            __syncwarp();
+                            continue;
+                        }
                         auto task = [&](int tk, int& x, int& y, uint32_t& dst) -> int {
                             const int b = tk / Gm::CB, cb = tk % Gm::CB;
                             const int k0 = k_tile + b * BR;
@@ -493,7 +515,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         fence_proxy_async_smem();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&pv_ready[b2]));
+                    if (lane == 0) mbar_arrive(smem_u32(&v_ready[vb]));
                     continue;
                 }
                 if (!mbar_wait(smem_u32(&raw_full[s]), ph, ctrl, tmo)) {
@@ -593,6 +615,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const uint32_t par = (g >> 1) & 1u;
                         const bool first = tp == 0;
                         if (mbar_test(smem_u32(&pv_ready[b2]), par) &&
+                            (!DIRECT || mbar_test(smem_u32(&v_ready[kvb(g)]), kvpar(g))) &&
                             (!first || items == 0 || mbar_test(smem_u32(&o_free), (items - 1) & 1u))) {
                             tc_fence_after();
                             const int vb = kvb(g);

@@ -87,14 +87,16 @@ int encode_kv_map_runs(CUtensorMap* m, const void* kv, int fp8, long long N, int
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
-// Latent cache [N, ps, Hkv, D] viewed as (64 elements of a column block, slots, column blocks of
-// a slot: Hkv * D / 64).  One box = BR slots of one kv head's row, landing as [D/64][BR][128 B]
-// (2-byte elements, 128-byte swizzle).
-int encode_kv_map_latent(CUtensorMap* m, const void* kv, long long N, int ps, int Hkv, int D, int BR) {
+// A cache whose slots hold H rows of D 2-byte elements ([N, ps, H, D]) viewed as (64 elements of
+// a column block, slots, column blocks of a slot: H * D / 64).  One box = BR slots of one row,
+// landing as [D/64][BR][128 B] (128-byte swizzle): the MMA tile layout of BR keys.  Serves the
+// latent cache (H = Hkv) and the split K/V cache seen as 2 Hkv rows (K of head h at 2h, V at
+// 2h + 1), one box then being a page run's whole K (or V) tile.
+int encode_kv_map_heads(CUtensorMap* m, const void* kv, long long N, int ps, int H, int D, int BR) {
     EncodeTiledFn fn = encoder();
     if (!fn) return -1;
-    const cuuint64_t dims[3] = {64u, (cuuint64_t)(N * ps), (cuuint64_t)(Hkv * D / 64)};
-    const cuuint64_t strides[2] = {(cuuint64_t)(Hkv * D * 2), 128u};
+    const cuuint64_t dims[3] = {64u, (cuuint64_t)(N * ps), (cuuint64_t)(H * D / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)(H * D * 2), 128u};
     const cuuint32_t box[3] = {64u, (cuuint32_t)BR, (cuuint32_t)(D / 64)};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv), dims, strides, box, estr,

@@ -72,6 +72,8 @@ DESCR = {
     "mla_decode": "latent attention decode: 128 seqs x q_len 1, kv_len~U[1024,8192], Hq 16 on one latent "
                   "kv head, rows 576 (V 512), page 64, bf16",
     "long_prefill_d256": "4 seqs x 8192 fresh prefill, Hq 16 / Hkv 8, D 256, page 64, bf16",
+    "decode_g16": "256 seqs x q_len 1, kv_len~U[512,8192], Hq 32 / Hkv 2 (16 q heads a kv head), D 128, "
+                  "page 16, bf16",
 }
 
 
@@ -459,7 +461,7 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
 # the other workloads of the default line: (name, timed steps); each K/V cache is far above L2
 # except long_prefill's (134 MB, about L2-sized)
 SIDE_WORKLOADS = (("mixed", 300), ("fp8_window", 300), ("long_prefill", 100), ("mla_decode", 300),
-                  ("long_prefill_d256", 100))
+                  ("long_prefill_d256", 100), ("decode_g16", 300))
 
 
 def main():
@@ -519,7 +521,7 @@ def main():
 if __name__ == "__main__":
     a0 = parse()
     if a0.all and a0.impl == "ours":
-        for w in ("decode", "mixed", "fp8_window", "long_prefill", "mla_decode", "long_prefill_d256"):
+        for w in ("decode", "mixed", "fp8_window", "long_prefill", "mla_decode", "long_prefill_d256", "decode_g16"):
             sys.argv = [sys.argv[0], "--workload", w, "--steps", str(a0.steps), "--warmup",
                         str(a0.warmup), "--no-cpu-baseline", "--e2e-steps", "0", "--no-side-workloads"]
             main()

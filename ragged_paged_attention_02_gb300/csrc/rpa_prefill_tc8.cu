@@ -73,10 +73,16 @@ struct G8 {
     static constexpr int QSTAGE = kM * 128;            // Q staging: one column block x 128 rows
     static constexpr int RAW = DIRECT ? 0 : kBN * 2 * D;  // one raw 8-bit stage (K and V); none in direct mode
     static constexpr int T16 = CB * kBN * 128;         // one f16 K (or V) tile
-    // K and V tile buffers: 2 in 8-bit mode (behind the raw ring), 3 in direct mode (the copies land
-    // in them, so a third buffer starts each tile's copies a tile earlier)
-    static constexpr int NB = DIRECT ? 3 : 2;
-    static constexpr int DATA = QSTAGE + 2 * RAW + 2 * NB * T16;
+    // Ring depths.  Direct mode: 3 K and 3 V tiles (the copies land in them, so a third buffer
+    // starts each tile's copies a tile earlier).  8-bit mode: the raw stages hold the copies in
+    // flight (2 at D 256; 4 at D 128, whose stages are half the bytes), then 2 K tiles (K(t)
+    // converted once QK(t-2) is done) and 2 V tiles (V(t) once PV(t-2) is done).  A third raw
+    // stage at D 256 (in place of a K tile) measured no faster: there the converter and softmax
+    // warps, not the copies, set a tile's time
+    static constexpr int NRAW = DIRECT ? 0 : (D == 256 ? 2 : 4);
+    static constexpr int NBK = DIRECT ? 3 : 2;
+    static constexpr int NBV = DIRECT ? 3 : 2;
+    static constexpr int DATA = QSTAGE + NRAW * RAW + (NBK + NBV) * T16;
     static constexpr int SMEM = DATA + 1024;
     static constexpr uint32_t TM_Q = 0;                // Q: D/2 columns
     static constexpr uint32_t TM_S0 = D / 2, TM_S1 = D / 2 + kBN;
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t meta_full[2], meta_free[2];
     __shared__ __align__(8) uint64_t q_full, q_empty, q_ready, qt_free;
-    __shared__ __align__(8) uint64_t raw_full[2], raw_empty[2];
+    __shared__ __align__(8) uint64_t raw_full[4], raw_empty[4];
     // per S buffer (t mod 2): QK done, P ready (softmax warps; in 8-bit mode also V converted: the
     // converter warps), PV done; per K/V buffer (t mod NB): K ready, and in direct mode V copied, V
     // ready (its edge rows zeroed: converter warps) and the K / V buffer free again (the MMAs that
@@ -222,19 +228,23 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t smem0 = smem_u32(smem);
     const uint32_t q_stage = smem0;                                 // Q staging (bf16)
-    const uint32_t raw_base = q_stage + Gm::QSTAGE;                 // 2 raw fp8 stages
-    const uint32_t k16_base = raw_base + 2 * Gm::RAW;               // NB 16-bit K tiles
-    const uint32_t v16_base = k16_base + Gm::NB * Gm::T16;          // NB 16-bit V tiles
-    // K/V buffer of global tile g and the parity of its use of that buffer
-    auto kvb = [](uint32_t g) -> int { return DIRECT ? (int)(g % 3u) : (int)(g & 1u); };
-    auto kvpar = [](uint32_t g) -> uint32_t { return DIRECT ? (g / 3u) & 1u : (g >> 1) & 1u; };
+    const uint32_t raw_base = q_stage + Gm::QSTAGE;                 // NRAW raw 8-bit stages
+    const uint32_t k16_base = raw_base + Gm::NRAW * Gm::RAW;        // NBK 16-bit K tiles
+    const uint32_t v16_base = k16_base + Gm::NBK * Gm::T16;         // NBV 16-bit V tiles
+    // K (V) buffer of global tile g and the parity of its use of that buffer
+    auto kbuf = [](uint32_t g) -> int { return (int)(g % (uint32_t)Gm::NBK); };
+    auto kpar = [](uint32_t g) -> uint32_t { return (g / (uint32_t)Gm::NBK) & 1u; };
+    auto vbuf = [](uint32_t g) -> int { return (int)(g % (uint32_t)Gm::NBV); };
+    auto vpar = [](uint32_t g) -> uint32_t { return (g / (uint32_t)Gm::NBV) & 1u; };
 
     if (tid == 0) {
+        for (int i = 0; i < Gm::NRAW; ++i) {
+            mbar_init(smem_u32(&raw_full[i]), 1);
+            mbar_init(smem_u32(&raw_empty[i]), kNConv);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&meta_full[i]), 1);
             mbar_init(smem_u32(&meta_free[i]), 17);  // 8 softmax + 8 converter warps + MMA thread
-            mbar_init(smem_u32(&raw_full[i]), 1);
-            mbar_init(smem_u32(&raw_empty[i]), kNConv);
             mbar_init(smem_u32(&qk_done[i]), 1);
             mbar_init(smem_u32(&pv_ready[i]), DIRECT ? 8 : 8 + kNConv);
             mbar_init(smem_u32(&pv_done[i]), 1);
@@ -347,8 +357,9 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     // done: with runs of a whole tile one copy of all column blocks (kvmap from
                     // encode_kv_map_heads: K of head h is row 2h of a slot, V row 2h + 1), else one
                     // copy per (page run, 128-byte column block), BR rows each
-                    const int b2 = kvb(tgp);
-                    const uint32_t par = kvpar(tgp);
+                    static_assert(Gm::NBK == Gm::NBV, "direct mode: K and V rings alike");
+                    const int b2 = kbuf(tgp);
+                    const uint32_t par = kpar(tgp);
                     ++tgp;
                     const int tasks = runs * Gm::CB;
 #pragma unroll 1
@@ -425,7 +436,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 if (want && good)
                     tma_load_3d(stage + (uint32_t)lane * run_bytes, &kvmap, fb, 0, pg * ps + (k0 - lp * ps),
                                 2 * item.head);
-                if (++s == 2) {
+                if (++s == Gm::NRAW) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -497,8 +508,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     // the copies wrote V(t) into its tile: on the tile's edges, zero this warp's rows of
                     // keys outside [kv_begin, kv_end) (page tails may hold any bits; runs outside the
                     // range were not copied), then V is ready
-                    const int vb = kvb(tg);
-                    if (!mbar_wait(smem_u32(&v_land[vb]), kvpar(tg), ctrl, tmo)) {
+                    const int vb = vbuf(tg);
+                    if (!mbar_wait(smem_u32(&v_land[vb]), vpar(tg), ctrl, tmo)) {
                         ok = false;
                         break;
                     }
@@ -530,20 +541,25 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 load_rows<D>(raw + BR * D, cw, lane, brs, vr);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&raw_empty[s]));
-                if (++s == 2) {
+                if (++s == Gm::NRAW) {
                     s = 0;
                     ph ^= 1u;
                 }
                 const int k_lo = key0 + t * kBN;
-                // K, then V, both converted exactly by the hardware conversion
-                if (!mbar_wait(smem_u32(&qk_done[b2]), par ^ 1u, ctrl, tmo)) {
-                    ok = false;
-                    break;
+                // K, then V, both converted exactly by the hardware conversion: K(t) into its buffer
+                // once QK(t - NBK), the buffer's last reader, is done
+                if (tg >= (uint32_t)Gm::NBK) {
+                    const uint32_t gk = tg - Gm::NBK;
+                    if (!mbar_wait(smem_u32(&qk_done[gk & 1]), (gk >> 1) & 1u, ctrl, tmo)) {
+                        ok = false;
+                        break;
+                    }
                 }
-                store_rows<D, KT>(kr, smem + (k16_base - smem0) + b2 * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
+                const int kb = kbuf(tg);
+                store_rows<D, KT>(kr, smem + (k16_base - smem0) + kb * Gm::T16, cw, lane, k_lo, kv_begin, kv_end);
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&k_full[b2]));
+                if (lane == 0) mbar_arrive(smem_u32(&k_full[kb]));
                 if (!mbar_wait(smem_u32(&pv_done[b2]), par ^ 1u, ctrl, tmo)) {
                     ok = false;
                     break;
@@ -591,8 +607,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     bool did = false;
                     if (tq < nt && tq <= tp + 1) {
                         const uint32_t g = tg + tq;
-                        const int b2 = g & 1, kb = kvb(g);
-                        if (mbar_test(smem_u32(&k_full[kb]), kvpar(g))) {
+                        const int b2 = g & 1, kb = kbuf(g);
+                        if (mbar_test(smem_u32(&k_full[kb]), kpar(g))) {
                             tc_fence_after();
                             const uint64_t kd = umma_sdesc(k16_base + kb * Gm::T16, 16, 1024);
                             const uint32_t kd_lo = (uint32_t)kd, kd_hi = (uint32_t)(kd >> 32);
@@ -615,10 +631,10 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const uint32_t par = (g >> 1) & 1u;
                         const bool first = tp == 0;
                         if (mbar_test(smem_u32(&pv_ready[b2]), par) &&
-                            (!DIRECT || mbar_test(smem_u32(&v_ready[kvb(g)]), kvpar(g))) &&
+                            (!DIRECT || mbar_test(smem_u32(&v_ready[vbuf(g)]), vpar(g))) &&
                             (!first || items == 0 || mbar_test(smem_u32(&o_free), (items - 1) & 1u))) {
                             tc_fence_after();
-                            const int vb = kvb(g);
+                            const int vb = vbuf(g);
                             const uint64_t vd = umma_sdesc(v16_base + vb * Gm::T16, kBN * 128, 1024);
                             const uint32_t vd_lo = (uint32_t)vd, vd_hi = (uint32_t)(vd >> 32);
                             const uint32_t od = tmem + Gm::TM_O, pa = tmem + (b2 ? Gm::TM_S1 : Gm::TM_S0);
@@ -648,7 +664,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                         const uint32_t pp = (gp >> 1) & 1u;
                         const bool qk_next = tq < nt && tq <= tp + 1 && (tp >= tq || (idle & 1));
                         if (qk_next)
-                            mbar_try_wait_for(smem_u32(&k_full[kvb(gq)]), kvpar(gq), kIssueNapNs);
+                            mbar_try_wait_for(smem_u32(&k_full[kbuf(gq)]), kpar(gq), kIssueNapNs);
                         else if (tp < tq)
                             mbar_try_wait_for(smem_u32(&pv_ready[gp & 1]), pp, kIssueNapNs);
                     }

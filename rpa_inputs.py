@@ -266,11 +266,11 @@ def build(*, seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int,
 
 # ---------------------------------------------------------------- the five workloads
 WORKLOADS = ("tiny", "decode", "mixed", "fp8_window", "long_prefill", "decode_quarter",
-             "fp8_window_quarter", "mla_decode", "long_prefill_d256")
+             "fp8_window_quarter", "mla_decode", "long_prefill_d256", "decode_g16")
 
 
 def workload(name: str) -> Problem:
-    """The five named workloads (seeds 0..4)."""
+    """The named workloads (each with a seed of its own)."""
     if name == "tiny":
         # 3 sequences, q_lens {1,5,16}, kv_lens {17,40,64}, 16 physical pages.
         return build(seed=0, q_lens=[1, 5, 16], kv_lens=[17, 40, 64], num_q_heads=4,
@@ -344,6 +344,14 @@ def workload(name: str) -> Problem:
                      num_kv_heads=1, head_dim=576, page_size=64, pages_per_seq=128,
                      kv_layout="latent", v_head_dim=512, sm_scale=1.0 / math.sqrt(192), name=name,
                      rng_lengths=rng)
+    if name == "decode_g16":
+        # grouped decode with 16 q heads per kv head (the 16-row decode tiles): 256 x q_len 1,
+        # kv_len ~ U[512, 8192], Hq 32 / Hkv 2, D 128, page 16, bf16
+        rng = np.random.default_rng([7, 0])
+        kl = rng.integers(512, 8192, size=256, endpoint=True)
+        return build(seed=7, q_lens=np.ones(256, np.int64), kv_lens=kl, num_q_heads=32,
+                     num_kv_heads=2, head_dim=128, page_size=16, pages_per_seq=512,
+                     sm_scale=1.0 / math.sqrt(128), name=name, rng_lengths=rng)
     raise KeyError(name)
 
 

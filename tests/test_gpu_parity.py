@@ -263,10 +263,10 @@ SAMPLED = {"long_prefill": 8000, "long_prefill_d256": 4000, "mla_decode": 800}
 
 
 @pytest.mark.parametrize("name", ["decode", "mixed", "fp8_window", "long_prefill", "long_prefill_d256",
-                                  "mla_decode"])
+                                  "mla_decode", "decode_g16"])
 def test_full_workloads(name):
-    """The full-size workloads in the launch configuration the benchmark times.  decode, mixed and
-    fp8_window: every output row against the oracle.  long_prefill (2.1 M rows), long_prefill_d256
+    """The full-size workloads in the launch configuration the benchmark times.  decode, mixed,
+    fp8_window and decode_g16: every output row against the oracle.  long_prefill (2.1 M rows), long_prefill_d256
     (0.5 M rows) and mla_decode (2 k rows of 8 k keys): a seeded sample holding the first and last
     row of every 128-row query tile (every sequence's token for the decode batch) beside random
     rows."""

@@ -11,10 +11,12 @@
 // With attention sinks the row's sink term 2^{s log2(e) - M} joins L here, once: the pieces
 // leave it out.
 //
-// Work goes out in units of a few rows of one entry (one group of four columns per thread).  An
-// entry of at most eight pieces merges in registers; longer ones first reduce each row's m and l
-// (a warp per row) into shared-memory scale factors.  Entries hold at most `rows_max` rows (the
-// decode tile's rows: the planner classifies a sequence as decode only when q_len * G fits).
+// Each warp merges one row of one entry at a time (rows of an entry on consecutive warps): lanes
+// over the pieces reduce the row's m and l to M, the scale factors 2^(m_i - M) and 1 / L (shuffles),
+// then lanes over groups of four columns sum the pieces' partial O, the loads of up to eight pieces
+// in flight at once.  No block barrier: a row costs two dependent rounds of loads after its entry.
+// Entries hold at most `rows_max` rows (the decode tile's rows: the planner classifies a sequence as
+// decode only when q_len * G fits).
 //
 // The same kernel writes zeros into the rows of tokens that no sequence
 // covers (outside [cu_q_lens[0], cu_q_lens[num_seqs])), so that o is always
@@ -26,119 +28,75 @@ namespace rpa {
 namespace {
 
 constexpr int kCombThreads = 256;
-constexpr int kCombCache = 64;  // pieces whose per-row scale factors are kept in shared memory
-constexpr int kDirect = 8;      // entries of at most this many pieces merge without shared memory
+constexpr int kBatch = 8;  // pieces whose partial O loads a lane has in flight at once
 
-__global__ void __launch_bounds__(kCombThreads, 2) rpa_combine_kernel(const CombParams p) {
-    __shared__ float s_sc[kCombCache][kDecRows];  // 2^(m_i - M) of piece i and row r
-    __shared__ float s_M[kDecRows], s_inv[kDecRows];
+__global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kernel(const CombParams p) {
     pdl_wait();  // the attention kernels' partials are complete from here on
     const int n_comb = p.ctrl[kNumComb];
     const int D = p.D, G = p.G, Hq = p.Hq;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // a unit of work: rpu rows of one entry, so that each thread merges one group of four
-    // columns (more units than entries keep more SMs busy)
-    const int quads = D / 4;
+    const int lane = threadIdx.x & 31;
     const int rmax = max(1, min(p.rows_max, kDecRows));
-    const int rpu = max(1, min(rmax, kCombThreads / quads));
-    const int upe = (rmax + rpu - 1) / rpu;
-    for (int u = blockIdx.x; u < n_comb * upe; u += gridDim.x) {
-        const int e = u / upe, r0 = (u % upe) * rpu;
-        const Comb c = p.comb[e];
-        const int q0 = p.cu_q_lens[c.seq];
-        const int rows = (p.cu_q_lens[c.seq + 1] - q0) * G;
-        const int r1 = min(rows, r0 + rpu);
-        if (r0 >= rows) continue;  // the same for every thread of the block
-        const float* ml = p.part_ml + (size_t)c.part * kDecRows * 2;  // [pieces][kDecRows][2]
-        if (c.pieces <= kDirect) {
-            // few pieces: each thread merges its four columns of a row on its own (the row's m and
-            // l are re-read by the row's threads; all loads are issued before the sums)
-            for (int x = tid; x < (r1 - r0) * quads; x += kCombThreads) {
-                const int r = r0 + x / quads, col = (x % quads) * 4;
-                float2 mlk[kDirect];
-                float4 v[kDirect];
-                float M = -INFINITY;
+    const int quads = D / 4;
+    const int warps = gridDim.x * (kCombThreads / 32);
+    for (int task = blockIdx.x * (kCombThreads / 32) + (threadIdx.x >> 5); task < n_comb * rmax; task += warps) {
+        const int e = task / rmax, r = task - e * rmax;
+        const int4* cp = reinterpret_cast<const int4*>(p.comb + e);
+        const int4 c0 = cp[0], c1 = cp[1];
+        const int q0 = c0.x, rows = c0.y, head = c0.z, part = c0.w, pieces = c1.x;
+        if (r >= rows) continue;  // the same for every lane of the warp
+        const float* ml = p.part_ml + ((size_t)part * kDecRows + r) * 2;  // piece k at + k kDecRows 2
+        // the row's M, and L over all pieces (lanes over the pieces, 32 at a time)
+        float M = -INFINITY;
+        for (int k = lane; k < pieces; k += 32) M = fmaxf(M, ml[(size_t)k * kDecRows * 2]);
 #pragma unroll
-                for (int k = 0; k < kDirect; ++k) {
-                    if (k < c.pieces) {
-                        const size_t pr = (size_t)(c.part + k) * kDecRows + r;
-                        mlk[k] = *reinterpret_cast<const float2*>(p.part_ml + pr * 2);
-                        v[k] = *reinterpret_cast<const float4*>(p.part_o + pr * D + col);
-                        M = fmaxf(M, mlk[k].x);
-                    }
-                }
-                float L = 0.f;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (M != -INFINITY) {
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f, sc_mine = 0.f;  // sc_mine: 2^(m_lane - M) for piece `lane` (the first 32)
+        if (M != -INFINITY) {
+            for (int k = lane; k < pieces; k += 32) {
+                const float2 v = *reinterpret_cast<const float2*>(ml + (size_t)k * kDecRows * 2);
+                const float sc = ex2(v.x - M);
+                if (k < 32) sc_mine = sc;
+                L += sc * v.y;
+            }
+        }
 #pragma unroll
-                    for (int k = 0; k < kDirect; ++k) {
-                        if (k < c.pieces) {
-                            const float sc = ex2(mlk[k].x - M);
-                            L += sc * mlk[k].y;
-                            acc.x += sc * v[k].x;
-                            acc.y += sc * v[k].y;
-                            acc.z += sc * v[k].z;
-                            acc.w += sc * v[k].w;
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        const int qh = head * G + r % G;
+        L = add_sink(L, p.sinks, qh, M);  // the sink joins once, over all pieces
+        const float inv = L > 0.f ? p.v_scale / L : 0.f;
+        const float* po = p.part_o + ((size_t)part * kDecRows + r) * D;  // piece k at + k kDecRows D
+        const size_t orow = ((size_t)(q0 + r / G) * Hq + qh) * D;
+        // columns in groups of four, 32 groups a pass; every lane runs every pass (the scale factors
+        // travel by shuffles), lanes past the row's last group neither load nor store
+        for (int cb = 0; cb < quads; cb += 32) {
+            const int c4 = cb + lane;
+            const bool act = c4 < quads;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (M != -INFINITY) {
+                for (int k0 = 0; k0 < pieces; k0 += kBatch) {
+                    float4 v[kBatch];
+#pragma unroll
+                    for (int k = 0; k < kBatch; ++k)
+                        if (act && k0 + k < pieces)
+                            v[k] = *reinterpret_cast<const float4*>(po + (size_t)(k0 + k) * kDecRows * D + 4 * c4);
+#pragma unroll
+                    for (int k = 0; k < kBatch; ++k) {
+                        if (k0 + k < pieces) {
+                            const int kk = k0 + k;
+                            const float sc = kk < 32 ? __shfl_sync(0xffffffffu, sc_mine, kk)
+                                                     : ex2(ml[(size_t)kk * kDecRows * 2] - M);
+                            if (act) {
+                                acc.x += sc * v[k].x;
+                                acc.y += sc * v[k].y;
+                                acc.z += sc * v[k].z;
+                                acc.w += sc * v[k].w;
+                            }
                         }
                     }
                 }
-                const int t = q0 + r / G;
-                const int qh = c.head * G + r % G;
-                L = add_sink(L, p.sinks, qh, M);  // the sink joins once, over all pieces
-                const float inv = L > 0.f ? p.v_scale / L : 0.f;
-                store_o4(p.o, ((size_t)t * Hq + qh) * D + col, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv,
-                         p.odt);
             }
-            continue;  // the same for every thread of the block
+            if (act) store_o4(p.o, orow + 4 * c4, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.odt);
         }
-        // 1. per row (a warp per row, lanes over the pieces): M, the scale factors and 1 / L
-        for (int r = r0 + warp; r < r1; r += kCombThreads / 32) {
-            float M = -INFINITY;
-            for (int k = lane; k < c.pieces; k += 32) M = fmaxf(M, ml[((size_t)k * kDecRows + r) * 2]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float L = 0.f;
-            if (M != -INFINITY) {
-                for (int k = lane; k < c.pieces; k += 32) {
-                    const float2 v = *reinterpret_cast<const float2*>(ml + ((size_t)k * kDecRows + r) * 2);
-                    const float sc = ex2(v.x - M);
-                    if (k < kCombCache) s_sc[k][r] = sc;
-                    L += sc * v.y;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            if (lane == 0) {
-                L = add_sink(L, p.sinks, c.head * G + r % G, M);  // the sink joins once, over all pieces
-                s_M[r] = M;
-                s_inv[r] = L > 0.f ? p.v_scale / L : 0.f;
-            }
-        }
-        __syncthreads();
-        // 2. each thread: four columns of a row, summed over the pieces (loads of several pieces
-        // in flight at once)
-        for (int x = tid; x < (r1 - r0) * quads; x += kCombThreads) {
-            const int r = r0 + x / quads, col = (x % quads) * 4;
-            const float M = s_M[r];
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
-                const float* po = p.part_o + ((size_t)c.part * kDecRows + r) * D + col;
-#pragma unroll 4
-                for (int k = 0; k < c.pieces; ++k) {
-                    const float sc = k < kCombCache ? s_sc[k][r] : ex2(ml[((size_t)k * kDecRows + r) * 2] - M);
-                    const float4 v = *reinterpret_cast<const float4*>(po + (size_t)k * kDecRows * D);
-                    acc.x += sc * v.x;
-                    acc.y += sc * v.y;
-                    acc.z += sc * v.z;
-                    acc.w += sc * v.w;
-                }
-            }
-            const float inv = s_inv[r];
-            const int t = q0 + r / G;
-            const int qh = c.head * G + r % G;
-            store_o4(p.o, ((size_t)t * Hq + qh) * D + col, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.odt);
-        }
-        __syncthreads();
     }
     // zero rows of uncovered tokens: [0, lo) and [hi, T)
     const int lo = min(max(p.ctrl[kCovLo], 0), p.T);

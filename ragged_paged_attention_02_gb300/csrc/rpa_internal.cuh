@@ -37,10 +37,10 @@ struct Item {
     int seq, head, tok0, ntok, kv_begin, kv_end, part, piece;
 };
 
-// One split-KV combine entry: rows [0, rows) of (seq, head) merge `pieces`
-// partials starting at slot `part`.
-struct Comb {
-    int seq, head, part, pieces;
+// One split-KV combine entry: rows [0, rows) of the kv head `head` of the sequence whose first
+// query token is q0 merge `pieces` partials starting at slot `part` (32 bytes: two 16-byte loads)
+struct __align__(16) Comb {
+    int q0, rows, head, part, pieces, pad0, pad1, pad2;
 };
 
 // K/V element types inside the kernels (template arguments): 16-bit types feed the MMAs as they
@@ -62,6 +62,7 @@ constexpr int kMinChunk = 512;     // smallest split-KV piece (keys)
 constexpr int kChunkAlign = 64;    // pieces are multiples of this many keys
 constexpr int kMaxSort = 8192;     // units sorted by cost on the device
 constexpr int kSeqSmem = 4096;     // sequences whose plan scratch fits in shared memory
+constexpr int kSeqArrays = 7;      // per-sequence plan scratch arrays of S + 1 ints
 constexpr int kPlanThreads = 1024;
 // rates of the SM-split model (planner): FLOP/ns of one SM on prefill, B/ns one SM can
 // stream in the decode kernel, and HBM B/ns.  The first two are the rates measured with
@@ -185,6 +186,7 @@ cudaError_t launch_pdl(Kern k, int grid, int block, size_t smem, cudaStream_t st
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
 // kt: KvType of kv_pages
 cudaError_t launch_prefill(const AttnParams& p, int kt, const Launch& l);
+constexpr int kCombCtasPerSm = 3;  // combine CTAs resident per SM (its register budget)
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
 // rows: query rows of a decode tile, 16 (any) or 8 (2-byte K/V, G <= 8: keys on the MMA's M side)
 cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int kt,

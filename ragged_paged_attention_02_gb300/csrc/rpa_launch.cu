@@ -49,7 +49,7 @@ Layout layout(const RpaCfg& c, const KernelSet& ks) {
     Layout L;
     size_t off = 0;
     L.ctrl = off; off = align256(off + kCtrlWords * sizeof(int));
-    L.seq = off; off = align256(off + 6 * (size_t)(S + 1) * sizeof(int));
+    L.seq = off; off = align256(off + kSeqArrays * (size_t)(S + 1) * sizeof(int));
     L.units = off; off = align256(off + (size_t)ks.max_units * 8 * sizeof(int));
     L.dec = off; off = align256(off + (size_t)ks.max_dec_units * Hkv * sizeof(Item));
     L.pf = off; off = align256(off + (size_t)ks.max_pf_units * Hkv * sizeof(Item));
@@ -392,7 +392,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     cp.part_o = ws.part_o;
     cp.part_ml = ws.part_ml;
     if (!rec(kEvCombStart, st)) return RPA_ERR_CUDA;
-    if (launch_combine(cp, Launch{ks.sms * 2, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    if (launch_combine(cp, Launch{ks.sms * kCombCtasPerSm, st}) != cudaSuccess) return RPA_ERR_CUDA;
     if (!rec(kEvCombEnd, st)) return RPA_ERR_CUDA;
     return RPA_OK;
 }

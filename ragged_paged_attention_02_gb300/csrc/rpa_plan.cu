@@ -86,18 +86,28 @@ __device__ int4 block_scan4(int4 v, int4* s_warp, int4* total) {
     return r;
 }
 
-// Sum of one 64-bit value per thread over the block (all threads get it).  s_red holds 32.
-__device__ unsigned long long block_sum64(unsigned long long v, unsigned long long* s_red) {
+// Sums of two 64-bit values per thread over the block (all threads get them).  s_red holds 64.
+__device__ void block_sum64x2(unsigned long long& a, unsigned long long& b, unsigned long long* s_red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) s_red[warp] = v;
+    for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+    }
+    if (lane == 0) {
+        s_red[warp] = a;
+        s_red[32 + warp] = b;
+    }
     __syncthreads();
-    unsigned long long t = lane < nwarps ? s_red[lane] : 0ull;
+    unsigned long long x = lane < nwarps ? s_red[lane] : 0ull, y = lane < nwarps ? s_red[32 + lane] : 0ull;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    for (int o = 16; o > 0; o >>= 1) {
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+        y += __shfl_xor_sync(0xffffffffu, y, o);
+    }
     __syncthreads();
-    return t;
+    a = x;
+    b = y;
 }
 // Minimum of one 64-bit value per thread over the block (all threads get it).  s_red holds 32.
 __device__ unsigned long long block_min64(unsigned long long v, unsigned long long* s_red) {
@@ -130,10 +140,54 @@ __device__ __forceinline__ int upper_seq(const int* ends, int n, int u) {
     return lo;
 }
 
+// Bitonic sort (ascending) of keys[0, 32 E) by one warp, in registers: element i = lane + 32 r
+// sits in lane `lane`, register r, so strides of 32 and more pair registers of one lane and
+// shorter strides pair lanes (shuffles); no block barrier.
+template <int E>
+__device__ void warp_sort(unsigned long long* keys, int lane) {
+    unsigned long long v[E];
+#pragma unroll
+    for (int r = 0; r < E; ++r) v[r] = keys[lane + 32 * r];
+    for (int k = 2; k <= 32 * E; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            if (j >= 32) {
+                // partner register r ^ jr of the same lane (jr a power of two below E)
+                const int jr = j >> 5;
+#pragma unroll
+                for (int b = 1; b < E; b <<= 1) {
+                    if (b != jr) continue;
+#pragma unroll
+                    for (int r = 0; r < E; ++r) {
+                        if (r & b) continue;
+                        const int i = lane + 32 * r;
+                        const bool up = (i & k) == 0;
+                        const unsigned long long a = v[r], c = v[r | b];
+                        const bool sw = (a > c) == up;
+                        v[r] = sw ? c : a;
+                        v[r | b] = sw ? a : c;
+                    }
+                }
+            } else {
+                const bool lower = (lane & j) == 0;
+#pragma unroll
+                for (int r = 0; r < E; ++r) {
+                    const int i = lane + 32 * r;
+                    const bool up = (i & k) == 0;
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], j);
+                    const unsigned long long lo = v[r] < o ? v[r] : o, hi = v[r] < o ? o : v[r];
+                    v[r] = (lower == up) ? lo : hi;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < E; ++r) keys[lane + 32 * r] = v[r];
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p) {
     extern __shared__ __align__(16) unsigned long long s_keys[];  // kMaxSort keys, then sequence scratch
     __shared__ int4 s_warp[33];
-    __shared__ unsigned long long s_red[32];
+    __shared__ unsigned long long s_red[64];
     __shared__ int s_bad;
     __shared__ int s_split[2];                // prefill CTAs, decode CTAs
     const int tid = threadIdx.x;
@@ -141,7 +195,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     int* ctrl = p.ctrl;
     pdl_trigger();  // the attention kernels may start their prologue now
     // per-sequence scratch (shared memory when it fits): class, count, decode / prefill
-    // unit ends, partial offset, combine offset
+    // unit ends, partial offset, combine offset, decode sequences with a partial last piece before
+    // this one
     int* seq_base = S <= kSeqSmem ? reinterpret_cast<int*>(s_keys + kMaxSort) : p.seq_scratch;
     int* s_cls = seq_base;
     int* s_cnt = s_cls + S + 1;
@@ -149,6 +204,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     int* s_pend = s_dend + S + 1;
     int* s_part = s_pend + S + 1;
     int* s_comb = s_part + S + 1;
+    int* s_ppre = s_comb + S + 1;
     const int Tq = max(1, p.pf_tokens);  // query tokens per prefill tile
 
     if (tid == 0) s_bad = 0;
@@ -198,8 +254,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         return;
     }
 
-    const unsigned long long s_total = block_sum64(my_total, s_red);
-    const unsigned long long s_pf_keys = block_sum64(my_pf_keys, s_red);
+    block_sum64x2(my_total, my_pf_keys, s_red);
+    const unsigned long long s_total = my_total, s_pf_keys = my_pf_keys;
 
     // ---- 2. SMs for each kernel, then the split-KV chunk for decode units
     {
@@ -249,14 +305,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
 
     // ---- 3. prefix sums: unit ends per class, partial slots, combine entries
-    int carry_d = 0, carry_p = 0, carry_part = 0, carry_comb = 0;
+    int carry_d = 0, carry_p = 0, carry_part = 0, carry_comb = 0, carry_pp = 0;
     for (int base = 0; base < S; base += blockDim.x) {
         const int s = base + tid;
-        int du = 0, pu = 0, pa = 0, cb = 0;
+        int du = 0, pu = 0, pa = 0, cb = 0, pp = 0;
         if (s < S) {
             const int cls = s_cls[s], cnt = s_cnt[s];
             if (cls == 1) {
                 du = (cnt + chunk - 1) / chunk;
+                pp = cnt % chunk != 0 ? 1 : 0;  // a last piece shorter than the chunk
                 if (du > 1) {
                     pa = du * p.Hkv;
                     cb = p.Hkv;
@@ -265,9 +322,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 pu = cnt;
             }
         }
-        int4 tot;
+        int4 tot, tot2;
         const int4 off = block_scan4(make_int4(du, pu, pa, cb), s_warp, &tot);
+        const int4 off2 = block_scan4(make_int4(pp, 0, 0, 0), s_warp, &tot2);
         if (s < S) {
+            s_ppre[s] = carry_pp + off2.x;
             s_dend[s] = carry_d + off.x + du;
             s_pend[s] = carry_p + off.y + pu;
             if (s_cls[s] != 2) {  // partial and combine offsets are read for decode sequences only
@@ -279,8 +338,13 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         carry_p += tot.y;
         carry_part += tot.z;
         carry_comb += tot.w;
+        carry_pp += tot2.x;
     }
     const int n_dec = carry_d, n_pf = carry_p, n_units = n_dec + n_pf;
+    // decode pieces of a whole chunk (all of a sequence's but a shorter last one) share the highest
+    // decode cost, so their sorted order is unit order: they go straight to their ranks, and only
+    // the shorter pieces and the prefill units are sorted, after them
+    const int n_full = n_dec - carry_pp;
     if (n_units > p.max_units || n_dec > p.max_dec_units || (p.dec_on_pf ? n_units : n_pf) > p.max_pf_units ||
         carry_part > p.max_part || carry_comb > p.max_comb) {
         // cannot happen with the create-time sizing; refuse rather than overflow
@@ -298,6 +362,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         int d[8];
         int cost, wseq = 0;
         int cls_bit;
+        int pos;  // the key's slot: a whole-chunk piece at its rank, the others in the range sorted below
         if (u < n_dec) {
             const int s = upper_seq(s_dend, S, u);
             const int k = u - (s_dend[s] - (s_cnt[s] + chunk - 1) / chunk);  // piece index
@@ -312,6 +377,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             d[6] = k; d[7] = pieces;
             cost = ke - kb;
             cls_bit = 0;
+            pos = cost == chunk ? (s_dend[s] - pieces - s_ppre[s]) + k : n_full + s_ppre[s];
         } else {
             const int v = u - n_dec;
             const int s = upper_seq(s_pend, S, v);
@@ -326,6 +392,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             cost = hi - lo;
             wseq = s_comb[s];
             cls_bit = 1;
+            pos = u;
         }
         int4* dst = reinterpret_cast<int4*>(p.units + (size_t)u * 8);
         dst[0] = make_int4(d[0], d[1], d[2], d[3]);
@@ -335,7 +402,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         // cost descending; weights and costs in 16-key buckets.  Fields: class 1 | weight 16 |
         // sequence 18 | cost 16 | unit 13 (units < 8192, sequences < 65536 when sorting).
         if (do_sort)
-            s_keys[u] = cls_bit == 0
+            s_keys[pos] = cls_bit == 0
                             ? ((unsigned long long)(0x7FFFFFFF - cost) << 32) | (unsigned long long)u
                             : (1ull << 63) | ((unsigned long long)(0xFFFF - min(wseq >> 4, 0xFFFF)) << 47) |
                                   ((unsigned long long)d[0] << 29) |
@@ -343,11 +410,33 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                                   (unsigned long long)u;
     }
 
-    // ---- 5. bitonic sort of the keys (ascending: decode first, then cost descending)
+    // ---- 5. bitonic sort of the keys (ascending: decode first, then cost descending) in
+    // [n_full, n_units), or in all of [0, n_units) when that range's power-of-two span would not
+    // fit the key array (the same order either way)
+    int base = n_full, n_sort = n_units - n_full;
     int n2 = 32;
-    while (n2 < n_units) n2 <<= 1;
-    if (do_sort) {
-        for (int i = n_units + tid; i < n2; i += blockDim.x) s_keys[i] = ~0ull;
+    while (n2 < n_sort) n2 <<= 1;
+    if (base + n2 > kMaxSort) {
+        base = 0;
+        n_sort = n_units;
+        n2 = 32;
+        while (n2 < n_units) n2 <<= 1;
+    }
+    unsigned long long* keys = s_keys + base;
+    if (do_sort && n_sort > 1 && n2 <= 256) {
+        // up to 256 keys: one warp, in registers
+        for (int i = n_sort + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
+        __syncthreads();
+        if (tid < 32) {
+            switch (n2) {
+                case 32: warp_sort<1>(keys, tid); break;
+                case 64: warp_sort<2>(keys, tid); break;
+                case 128: warp_sort<4>(keys, tid); break;
+                default: warp_sort<8>(keys, tid); break;
+            }
+        }
+    } else if (do_sort && n_sort > 1) {
+        for (int i = n_sort + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
         __syncthreads();
         for (int k = 2; k <= n2; k <<= 1) {
             // strides >= 32: pairs in different warps, through shared memory
@@ -355,11 +444,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 for (int i = tid; i < n2; i += blockDim.x) {
                     const int ixj = i ^ j;
                     if (ixj > i) {
-                        const unsigned long long a = s_keys[i], b = s_keys[ixj];
+                        const unsigned long long a = keys[i], b = keys[ixj];
                         const bool up = (i & k) == 0;
                         if ((a > b) == up) {
-                            s_keys[i] = b;
-                            s_keys[ixj] = a;
+                            keys[i] = b;
+                            keys[ixj] = a;
                         }
                     }
                 }
@@ -367,7 +456,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             }
             // strides < 32: both keys of a pair sit in one warp, exchanged by shuffles
             for (int i = tid; i < n2; i += blockDim.x) {
-                unsigned long long v = s_keys[i];
+                unsigned long long v = keys[i];
                 const bool up = (i & k) == 0;
                 for (int j = min(k >> 1, 16); j > 0; j >>= 1) {
                     const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
@@ -375,7 +464,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                     const unsigned long long lo = v < o ? v : o, hi = v < o ? o : v;
                     v = (lower == up) ? lo : hi;
                 }
-                s_keys[i] = v;
+                keys[i] = v;
             }
             __syncthreads();
         }
@@ -405,12 +494,15 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         if (s_cls[s] != 1) continue;
         const int pieces = (s_cnt[s] + chunk - 1) / chunk;
         if (pieces <= 1) continue;
+        const int q0 = p.cu_q_lens[s], rows = (p.cu_q_lens[s + 1] - q0) * p.G;
         for (int h = 0; h < p.Hkv; ++h) {
             Comb c;
-            c.seq = s;
+            c.q0 = q0;
+            c.rows = rows;
             c.head = h;
             c.part = s_part[s] + h * pieces;
             c.pieces = pieces;
+            c.pad0 = c.pad1 = c.pad2 = 0;
             p.comb[s_comb[s] + h] = c;
         }
     }
@@ -434,7 +526,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
 
 }  // namespace
 
-size_t plan_smem_bytes() { return sizeof(unsigned long long) * kMaxSort + sizeof(int) * 6 * (kSeqSmem + 1); }
+size_t plan_smem_bytes() { return sizeof(unsigned long long) * kMaxSort + sizeof(int) * kSeqArrays * (kSeqSmem + 1); }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem) {
     rpa_plan_kernel<<<1, kPlanThreads, smem, st>>>(p);

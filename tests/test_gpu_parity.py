@@ -311,11 +311,14 @@ def test_resident_ctas_per_sm_as_designed(kw, dec_bps, pf_bps):
 
 
 def test_planner_matches_python_rederivation():
+    """The device planner's items, chunk, CTA split and sort flag equal a plain Python restatement.
+    The cases span the sort's paths: a few keys (one warp, in registers), a few thousand (the
+    block-wide network), and decode batches whose whole-chunk pieces skip the sort."""
     from plan_model import plan
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
-    for name in ("tiny", "mixed", "fp8"):
-        if name == "tiny":
+    for name in ("tiny", "mixed", "fp8", "decode", "long_prefill", "mla_decode", "decode_g16"):
+        if name in ("tiny", "decode", "long_prefill", "mla_decode", "decode_g16"):
             p = ri.workload(name)
         elif name == "mixed":
             p = ri.random_small(40, num_seqs=60, max_q=300, max_kv=5000, num_q_heads=32, num_kv_heads=8,

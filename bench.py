@@ -503,8 +503,8 @@ def main():
             r, _ = measure(name, min(k, max(1, args.steps)), args.warmup, dist, dev, world)
             side[name] = {key: r[key] for key in ("value", "unit", "ms_per_step", "steps", "dtype", "config",
                                                   "step_roofline_frac", "step_roofline_bound", "step_hbm_gbs",
-                                                  "step_tflops", "kernel_rooflines", "kernels_ms", "idle_kernels",
-                                                  "roofline", "clocks")}
+                                                  "step_tflops", "kernel_rooflines", "kernels_ms", "kernel_timing",
+                                                  "idle_kernels", "roofline", "clocks")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -519,7 +519,7 @@ def main():
             "step_hbm_gbs": res["step_hbm_gbs"], "step_tflops": res["step_tflops"],
             "step_roofline_frac": res["step_roofline_frac"],
             "kernel_rooflines": res["kernel_rooflines"], "kernels_ms": res["kernels_ms"],
-            "idle_kernels": res["idle_kernels"],
+            "kernel_timing": res["kernel_timing"], "idle_kernels": res["idle_kernels"],
             "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res.get("e2e"),
             "gpu_launches": res["gpu_launches"], "clocks": res["clocks"],
         }

@@ -11,12 +11,12 @@
 // With attention sinks the row's sink term 2^{s log2(e) - M} joins L here, once: the pieces
 // leave it out.
 //
-// Each warp merges one row of one entry at a time (rows of an entry on consecutive warps): lanes
-// over the pieces reduce the row's m and l to M, the scale factors 2^(m_i - M) and 1 / L (shuffles),
-// then lanes over groups of four columns sum the pieces' partial O, the loads of up to eight pieces
-// in flight at once.  No block barrier: a row costs two dependent rounds of loads after its entry.
-// Entries hold at most `rows_max` rows (the decode tile's rows: the planner classifies a sequence as
-// decode only when q_len * G fits).
+// Each warp merges 128 columns of one row of one entry at a time (the tasks of an entry on
+// consecutive warps).  Its partial O loads (up to eight pieces, all in flight at once) go out as soon
+// as the entry is read; beside them, lanes over the pieces reduce the row's m and l to M, the scale
+// factors 2^(m_i - M) and 1 / L (shuffles).  No block barrier: a task costs two dependent rounds of
+// loads.  Entries hold at most `rows_max` rows (the decode tile's rows: the planner classifies a
+// sequence as decode only when q_len * G fits).
 //
 // The same kernel writes zeros into the rows of tokens that no sequence
 // covers (outside [cu_q_lens[0], cu_q_lens[num_seqs])), so that o is always
@@ -37,14 +37,30 @@ __global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kern
     const int lane = threadIdx.x & 31;
     const int rmax = max(1, min(p.rows_max, kDecRows));
     const int quads = D / 4;
+    const int nchunk = (quads + 31) / 32;  // 128-column chunks of a row
+    const int per_entry = rmax * nchunk;
     const int warps = gridDim.x * (kCombThreads / 32);
-    for (int task = blockIdx.x * (kCombThreads / 32) + (threadIdx.x >> 5); task < n_comb * rmax; task += warps) {
-        const int e = task / rmax, r = task - e * rmax;
+    for (int task = blockIdx.x * (kCombThreads / 32) + (threadIdx.x >> 5); task < n_comb * per_entry;
+         task += warps) {
+        const int e = task / per_entry, rem = task - e * per_entry;
+        const int r = rem / nchunk, c4 = (rem - r * nchunk) * 32 + lane;
         const int4* cp = reinterpret_cast<const int4*>(p.comb + e);
         const int4 c0 = cp[0], c1 = cp[1];
         const int q0 = c0.x, rows = c0.y, head = c0.z, part = c0.w, pieces = c1.x;
         if (r >= rows) continue;  // the same for every lane of the warp
+        const bool act = c4 < quads;
         const float* ml = p.part_ml + ((size_t)part * kDecRows + r) * 2;  // piece k at + k kDecRows 2
+        // piece k's four columns at pv[k * kstride] (float4 units)
+        const float4* pv = reinterpret_cast<const float4*>(p.part_o + ((size_t)part * kDecRows + r) * D) + c4;
+        const int kstride = kDecRows * D / 4;
+        // few pieces: every partial O load in flight before the m / l reduction
+        const bool held = pieces <= kBatch;
+        float4 v[kBatch];
+        if (held) {
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+                if (act && k < pieces) v[k] = pv[k * kstride];
+        }
         // the row's M, and L over all pieces (lanes over the pieces, 32 at a time)
         float M = -INFINITY;
         for (int k = lane; k < pieces; k += 32) M = fmaxf(M, ml[(size_t)k * kDecRows * 2]);
@@ -53,10 +69,10 @@ __global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kern
         float L = 0.f, sc_mine = 0.f;  // sc_mine: 2^(m_lane - M) for piece `lane` (the first 32)
         if (M != -INFINITY) {
             for (int k = lane; k < pieces; k += 32) {
-                const float2 v = *reinterpret_cast<const float2*>(ml + (size_t)k * kDecRows * 2);
-                const float sc = ex2(v.x - M);
+                const float2 w = *reinterpret_cast<const float2*>(ml + (size_t)k * kDecRows * 2);
+                const float sc = ex2(w.x - M);
                 if (k < 32) sc_mine = sc;
-                L += sc * v.y;
+                L += sc * w.y;
             }
         }
 #pragma unroll
@@ -64,21 +80,27 @@ __global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kern
         const int qh = head * G + r % G;
         L = add_sink(L, p.sinks, qh, M);  // the sink joins once, over all pieces
         const float inv = L > 0.f ? p.v_scale / L : 0.f;
-        const float* po = p.part_o + ((size_t)part * kDecRows + r) * D;  // piece k at + k kDecRows D
-        const size_t orow = ((size_t)(q0 + r / G) * Hq + qh) * D;
-        // columns in groups of four, 32 groups a pass; every lane runs every pass (the scale factors
-        // travel by shuffles), lanes past the row's last group neither load nor store
-        for (int cb = 0; cb < quads; cb += 32) {
-            const int c4 = cb + lane;
-            const bool act = c4 < quads;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (M != -INFINITY) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY) {
+            if (held) {
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    if (k < pieces) {
+                        const float sc = __shfl_sync(0xffffffffu, sc_mine, k);
+                        if (act) {
+                            acc.x += sc * v[k].x;
+                            acc.y += sc * v[k].y;
+                            acc.z += sc * v[k].z;
+                            acc.w += sc * v[k].w;
+                        }
+                    }
+                }
+            } else {
+                // many pieces: batches of kBatch loads; every lane runs every step (shuffles)
                 for (int k0 = 0; k0 < pieces; k0 += kBatch) {
-                    float4 v[kBatch];
 #pragma unroll
                     for (int k = 0; k < kBatch; ++k)
-                        if (act && k0 + k < pieces)
-                            v[k] = *reinterpret_cast<const float4*>(po + (size_t)(k0 + k) * kDecRows * D + 4 * c4);
+                        if (act && k0 + k < pieces) v[k] = pv[(k0 + k) * kstride];
 #pragma unroll
                     for (int k = 0; k < kBatch; ++k) {
                         if (k0 + k < pieces) {
@@ -95,8 +117,10 @@ __global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kern
                     }
                 }
             }
-            if (act) store_o4(p.o, orow + 4 * c4, acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv, p.odt);
         }
+        if (act)
+            store_o4(p.o, ((size_t)(q0 + r / G) * Hq + qh) * D + 4 * c4, acc.x * inv, acc.y * inv, acc.z * inv,
+                     acc.w * inv, p.odt);
     }
     // zero rows of uncovered tokens: [0, lo) and [hi, T)
     const int lo = min(max(p.ctrl[kCovLo], 0), p.T);

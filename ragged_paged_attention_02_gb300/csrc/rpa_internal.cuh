@@ -63,7 +63,7 @@ constexpr int kChunkAlign = 64;    // pieces are multiples of this many keys
 constexpr int kMaxSort = 8192;     // units sorted by cost on the device
 constexpr int kSeqSmem = 4096;     // sequences whose plan scratch fits in shared memory
 constexpr int kSeqArrays = 7;      // per-sequence plan scratch arrays of S + 1 ints
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 512;
 // rates of the SM-split model (planner): FLOP/ns of one SM on prefill, B/ns one SM can
 // stream in the decode kernel, and HBM B/ns.  The first two are the rates measured with
 // both kernels running at once (chunked prefill of 512 tokens beside long decodes, D 128):
@@ -101,7 +101,7 @@ struct PlanParams {
     int max_part;    // capacity of partial slots
     int max_comb;    // capacity of combine entries
     int* ctrl;
-    int* seq_scratch;  // [4 * max_num_seqs]
+    int* seq_scratch;  // [kSeqArrays * (max_num_seqs + 1)], used when the sequences overflow shared memory
     int* units;        // [max_units * 8]
     unsigned long long* keys;  // [max_units] (only used if > kMaxSort)
     Item* dec_items;

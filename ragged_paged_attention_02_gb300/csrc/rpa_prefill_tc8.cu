@@ -10,13 +10,14 @@
 // epilogue.  Roles:
 //
 //   producer warp    Q tile (bf16) into a staging buffer, then per 64-key tile
-//                    the raw fp8 K/V rows of each page run (one bulk tensor
-//                    copy per run: K and V of the head) into a 2-slot ring.
+//                    the raw 8-bit K/V rows of each page run (one bulk tensor
+//                    copy per run: K and V of the head) into a ring of raw
+//                    stages (2 at D 256, 4 at D 128).
 //   8 converter      Q (warps on lane quadrants 0-3): bf16 -> f16 (f16 q as it
 //   warps            is) into TMEM (the A operand of S = Q K^T).  K and V: each
-//                    warp takes 8
-//                    key rows of a tile into registers (the ring slot goes
-//                    straight back to the producer), then 8-bit -> f16 into
+//                    warp takes 8 key rows of a tile into registers (the
+//                    ring slot goes straight back to the producer), then
+//                    8-bit -> f16 into
 //                    double-buffered, 128-byte swizzled tiles (K-major), keys
 //                    outside the item's [kv_begin, kv_end) written as zero
 //                    (the page zeroes K/V past kv_len; tail slots may hold any
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             mbar_init(smem_u32(&k_free[i]), 1);
             mbar_init(smem_u32(&v_free[i]), 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 64);
+        for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&xchg[i]), 2);  // one arrival per softmax warp
         mbar_init(smem_u32(&q_full), 1);
         mbar_init(smem_u32(&q_empty), 4);
         mbar_init(smem_u32(&q_ready), 4);
@@ -779,7 +780,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
 #pragma unroll
                     for (int x = 32 / F; x < 32; x <<= 1) mh = fmaxf(mh, __shfl_xor_sync(0xffffffffu, mh, x));
                     xm[tg & 1][half][L] = mh;
-                    mbar_arrive(xb);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xb);
                     if (!mbar_wait(xb, xph, ctrl, tmo)) return false;
                     xph ^= 1u;
                     const float mt = fmaxf(mh, xm[tg & 1][half ^ 1][L]);
@@ -849,7 +851,8 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
             // ---- epilogue: o = O * v_scale / l, this warp's half of the row, the copies added
             for (int x = R; x < 32; x <<= 1) l_run += __shfl_xor_sync(0xffffffffu, l_run, x);
             xl[half][L] = l_run;
-            mbar_arrive(xb);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(xb);
             if (!mbar_wait(xb, xph, ctrl, tmo)) break;
             xph ^= 1u;
             const float l_row = l_run + xl[half ^ 1][L];

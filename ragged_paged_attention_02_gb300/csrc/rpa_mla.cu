@@ -26,9 +26,12 @@
 //                   than 2^8).  At the item's end the row sums meet in shared memory and each warp
 //                   writes its 64 columns of o, or of an fp32 split-KV partial.
 //
-// Why not the tensor-memory MMAs here: an fp32 accumulator of 512 value columns fills all 512
-// columns of a tensor-memory lane, which leaves no room for S; the rows of a decode tile are few,
-// so the warp MMAs keep O in registers (32 floats a thread) and stream the cache at HBM rate.
+// Why not the tensor-memory MMAs here: with the query rows on the M side an fp32 accumulator of
+// 512 value columns fills all 512 columns of a tensor-memory lane, which leaves no room for S; with
+// the keys on the M side (S^T = K Q^T at M = 64, N = 16; O^T += V^T P^T at M = 128, N = 16) each
+// MMA of these shapes measured ~60-80 cycles whatever its size, ~3.5k cycles of tensor pipe a 64-key
+// stage for 52 of them, longer than this kernel's whole stage.  The rows of a decode tile are few
+// (the heads that share a latent row), so the warp MMAs keep O in registers (32 floats a thread).
 //
 // Every wait is a bounded mbarrier wait (a global-timer deadline): on expiry the status word gets
 // RPA_ERR_TIMEOUT and the warp returns.

@@ -224,6 +224,13 @@ MLA_CASES = [
     (113, dict(num_seqs=5, max_q=3, max_kv=1500, num_q_heads=128, num_kv_heads=1, page_size=64, **LATENT)),
     (114, dict(num_seqs=6, max_q=12, max_kv=1200, num_q_heads=32, num_kv_heads=2, page_size=16, kv_dtype="f16",
                q_dtype="f32", is_causal=False, **LATENT)),
+    # pages of whole 64-slot runs (one copy per stage), 12 q heads a latent kv head (rows past the tile's 12)
+    (120, dict(num_seqs=6, max_q=40, max_kv=900, num_q_heads=16, num_kv_heads=1, page_size=64, **LATENT)),
+    (121, dict(num_seqs=8, max_q=9, max_kv=2000, num_q_heads=8, num_kv_heads=1, page_size=128, soft_cap=30.0,
+               sliding_window=700, sinks=True, **LATENT)),
+    (122, dict(num_seqs=6, max_q=12, max_kv=1200, num_q_heads=32, num_kv_heads=2, page_size=64, kv_dtype="f16",
+               q_dtype="f32", is_causal=False, **LATENT)),
+    (123, dict(num_seqs=7, max_q=5, max_kv=3000, num_q_heads=12, num_kv_heads=1, page_size=64, **LATENT)),
 ]
 
 
@@ -235,6 +242,28 @@ def test_latent_cases_all_rows(case):
     assert st == 0
     assert got.shape == (p.num_q_tokens, p.num_q_heads, 512)
     assert_close(got, oracle.forward(p), p.kv_dtype, f"latent case {case}")
+
+
+@pytest.mark.parametrize("page_size", [16, 64])
+def test_latent_poisoned_tails_and_unused_pages(page_size):
+    """Latent rows past kv_len hold NaN and unused pages +inf, with page runs of 16 slots and of a
+    whole 64-key stage (the value rows outside the key range are zeroed before the PV)."""
+    p = ri.random_small(124, num_seqs=6, max_q=20, max_kv=700, num_q_heads=16, num_kv_heads=1,
+                        page_size=page_size, extra_tokens=0, **LATENT)
+    ref = oracle.forward(p)
+    used = set()
+    ps = p.page_size
+    for s in range(p.num_seqs):
+        kl = int(p.kv_lens[s])
+        used.update(int(x) for x in p.page_indices[s, : (kl + ps - 1) // ps])
+        if kl % ps:
+            p.kv_pages[p.page_indices[s, kl // ps], kl % ps:] = 0x7FC0
+    for pg in range(p.total_num_pages):
+        if pg not in used:
+            p.kv_pages[pg] = 0x7F80
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, ref, p.kv_dtype, "latent poisoned")
 
 
 def _sample_rows(p, n, seed, tile_tokens):

@@ -78,9 +78,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
     // exchanges among the consumer warps (bounded mbarrier waits, so that a warp that gives up
     // cannot leave the others waiting on a hardware barrier): row maxima posted, P complete,
     // row sums posted
-    __shared__ __align__(8) uint64_t x_s, x_max, x_p, x_sum;
+    __shared__ __align__(8) uint64_t x_s, x_p, x_p2, x_sum;
     __shared__ int meta[kNS][mWords];
-    __shared__ float red_m[kMlaCW][kRows];  // per warp: its keys' row maxima (this stage)
+    __shared__ float red_m[kNS][kMlaCW][kRows];  // [ring slot][warp]: its keys' row maxima (that stage)
+    __shared__ int red_f[kNS][kMlaCW];           // [ring slot][warp]: some row outgrew the running max
     __shared__ float red_l[kMlaCW][kRows];  // per warp: its row sums (item end)
     // per k-slice: the partial S over its k-steps (both key halves), [row][key] with rows padded to
     // 72 floats (the fragment stores and loads of a half warp then touch 32 distinct banks)
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
             mbar_init(smem_u32(&q_empty[i]), kMlaCW);
         }
         mbar_init(smem_u32(&x_s), kMlaCW);
-        mbar_init(smem_u32(&x_max), kMlaCW);
+        mbar_init(smem_u32(&x_p2), kMlaCW);
         mbar_init(smem_u32(&x_p), kMlaCW);
         mbar_init(smem_u32(&x_sum), kMlaCW);
         fence_mbar_init();
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
     const int BR = p.BR, br_shift = __ffs(BR) - 1;
     const uint32_t run_bytes = (uint32_t)(kCBQ * BR * 128);
     int s = 0;
-    uint32_t ph = 0, xph_s = 0, xph_max = 0, xph_p = 0, xph_sum = 0;
+    uint32_t ph = 0, xph_s = 0, xph_p = 0, xph_p2 = 0, xph_sum = 0;
     // this warp's k-slice of the QK contraction and key half of the stage
     const int kslice = w & (kKSlices - 1), khalf = w / kKSlices;
     const int kd0 = kslice * kSliceSteps;
@@ -372,26 +373,47 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
             mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 1));
             mx[ri] = fmaxf(mx[ri], __shfl_xor_sync(0xffffffffu, mx[ri], 2));
         }
-        // the rows' maxima over the whole stage: every warp reads all eight warps' and forms the
-        // same running max (no second exchange)
+        // Lazy maximum.  A row's exponent base is its running max, which moves only when some key
+        // outgrows it by more than 2^8 (always so on an item's first stage with a live key).  Each
+        // warp posts its keys' row maxima and whether any row of its keys grew, and writes P against
+        // the running max (all warps hold the same one); after the P exchange all read the flags.  If
+        // some row grew, the stage's row maxima form the new running max, O and the sums are rescaled
+        // and P is written again, behind one more exchange.
+        const bool grow = __any_sync(0xffffffffu, mx[0] > m_r[0] + kRescaleLog2 || mx[1] > m_r[1] + kRescaleLog2);
         if ((lane & 3) == 0) {
-            red_m[w][lane >> 2] = mx[0];
-            red_m[w][(lane >> 2) + 8] = mx[1];
+            red_m[s][w][lane >> 2] = mx[0];
+            red_m[s][w][(lane >> 2) + 8] = mx[1];
         }
-        if (!exchange(x_max, xph_max)) return;
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-            float mt = -INFINITY;
-#pragma unroll
-            for (int ww = 0; ww < kMlaCW; ++ww) mt = fmaxf(mt, red_m[ww][(lane >> 2) + 8 * ri]);
-            mx[ri] = mt;
-        }
-        // lazy rescale: the running max moves only when some row's max grows by more than 2^8
-        const bool need = __any_sync(0xffffffffu, mx[0] > m_r[0] + kRescaleLog2 || mx[1] > m_r[1] + kRescaleLog2);
-        if (need) {
+        if (lane == 0) red_f[s][w] = grow ? 1 : 0;
+        float lsum[2] = {0.f, 0.f};
+        // P of this warp's 8 keys into the shared P tile [16 rows][64 keys] (128-byte rows,
+        // swizzled): keys 8w + 2 (lane % 4), + 1 are word lane % 4 of chunk w of the row
+        auto write_p = [&]() {
 #pragma unroll
             for (int ri = 0; ri < 2; ++ri) {
-                const float m_new = fmaxf(m_r[ri], mx[ri]);
+                const float bse = m_r[ri] == -INFINITY ? 0.f : m_r[ri];
+                const float p0 = ex2(sacc[2 * ri] - bse), p1 = ex2(sacc[2 * ri + 1] - bse);
+                lsum[ri] = p0 + p1;
+                const int row = (lane >> 2) + 8 * ri;
+                *reinterpret_cast<uint32_t*>(smem + (pbuf - smem0) + swz128((uint32_t)row, (uint32_t)w) + 4 * (lane & 3)) =
+                    pack2<F16>(p0, p1);
+            }
+        };
+        if (!grow) write_p();
+        // P complete.  The next stage's partial S, maxima and P are written only after this
+        // warp's PV of this stage; every warp has read this stage's partial S before it arrives here.
+        if (!exchange(x_p, xph_p)) return;
+        bool need = false;
+#pragma unroll
+        for (int ww = 0; ww < kMlaCW; ++ww) need |= red_f[s][ww] != 0;
+        if (need) {
+            // (the same flags and maxima in every warp: the same new running max)
+#pragma unroll
+            for (int ri = 0; ri < 2; ++ri) {
+                float mt = -INFINITY;
+#pragma unroll
+                for (int ww = 0; ww < kMlaCW; ++ww) mt = fmaxf(mt, red_m[s][ww][(lane >> 2) + 8 * ri]);
+                const float m_new = fmaxf(m_r[ri], mt);
                 const float bse = m_new == -INFINITY ? 0.f : m_new;
                 const float alpha = m_r[ri] == -INFINITY ? 0.f : ex2(m_r[ri] - bse);
                 m_r[ri] = m_new;
@@ -402,24 +424,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
                     o_acc[nd][2 * ri + 1] *= alpha;
                 }
             }
+            write_p();
+            if (!exchange(x_p2, xph_p2)) return;
         }
-        float base[2];
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) base[ri] = m_r[ri] == -INFINITY ? 0.f : m_r[ri];
-        // P of this warp's 8 keys into the shared P tile [16 rows][64 keys] (128-byte rows,
-        // swizzled): keys 8w + 2 (lane % 4), + 1 are word lane % 4 of chunk w of the row
-#pragma unroll
-        for (int ri = 0; ri < 2; ++ri) {
-            const float p0 = ex2(sacc[2 * ri] - base[ri]), p1 = ex2(sacc[2 * ri + 1] - base[ri]);
-            l_r[ri] += p0 + p1;
-            const int row = (lane >> 2) + 8 * ri;
-            *reinterpret_cast<uint32_t*>(smem + (pbuf - smem0) + swz128((uint32_t)row, (uint32_t)w) + 4 * (lane & 3)) =
-                pack2<F16>(p0, p1);
-        }
-        // P complete.  The next stage's partial S, maxima and P are written only after this
-        // warp's PV of this stage; every warp has read this stage's partial S and maxima before
-        // it arrives here.
-        if (!exchange(x_p, xph_p)) return;
+        l_r[0] += lsum[0];
+        l_r[1] += lsum[1];
 
         // ---- O += P V: this warp's value columns 64w .. 64w+63 (column block w of the rows)
 #pragma unroll
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
                 red_l[w][lane >> 2] = lsum[0];
                 red_l[w][(lane >> 2) + 8] = lsum[1];
             }
-            // red_l is rewritten only at the next item's end, after its x_max and x_p exchanges
+            // red_l is rewritten only at the next item's end, after its x_s and x_p exchanges
             if (!exchange(x_sum, xph_sum)) return;
             const int rows_used = ntok * Gv;
 #pragma unroll

@@ -201,6 +201,41 @@ def test_d256_repeated_calls_identical_and_in_tolerance():
             assert np.array_equal(got, first)
 
 
+MANY_PIECES = [
+    # decode kernel (8-row tiles): three long decodes split into ~78 pieces each
+    ("decode-bf16", dict(q_lens=[1, 1, 1], kv_lens=[60000, 45000, 70000], num_q_heads=32, num_kv_heads=8,
+                         head_dim=128, page_size=16, sm_scale=1 / 11.3)),
+    # 64-key-tile kernel (8-bit K/V at D 256): one decode across every CTA (~76 pieces)
+    ("tc8-fp8", dict(q_lens=[1], kv_lens=[70000], num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+                     kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
+    # latent kernel: ~60-80 pieces a sequence, with sinks (added once, by the merge)
+    ("latent-sinks", dict(q_lens=[1, 1], kv_lens=[40000, 30000], num_q_heads=16, num_kv_heads=1, head_dim=576,
+                          v_head_dim=512, kv_layout="latent", page_size=64, sinks=True, sm_scale=1 / 24)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(MANY_PIECES)), ids=[c[0] for c in MANY_PIECES])
+def test_many_split_pieces_all_rows(case):
+    """Long decodes split into more than 32 pieces: the combine's streaming path (pieces beyond the
+    eight held in registers, scale factors beyond the first 32 recomputed), all rows vs the oracle."""
+    name, kw = MANY_PIECES[case]
+    p = ri.build(seed=130 + case, name=name, **kw)
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    att = RaggedPagedAttention(**p.cfg_dict())
+    o = att.forward(*to_dev(p), p.num_seqs)
+    assert att.status() == 0
+    info, items = att.plan()
+    pieces = {}
+    for it in items:
+        key = (int(it[0]), int(it[1]))
+        pieces[key] = pieces.get(key, 0) + 1
+    assert max(pieces.values()) > 32, pieces
+    got = o_to_f64(o)
+    att.close()
+    assert_close(got, oracle.forward(p), p.kv_dtype, f"many pieces {name}")
+
+
 @pytest.mark.parametrize("case", range(len(DTYPE_CASES)), ids=[f"{c[1].get('q_dtype', 'bf16')}-"
                                                                f"{c[1]['kv_dtype']}-seed{c[0]}" for c in DTYPE_CASES])
 def test_dtype_cases_all_rows(case):

@@ -87,7 +87,7 @@ __device__ __forceinline__ void attn_body(const AttnParams& p) {
         __syncthreads();
         const int it_idx = s_item;
         if (it_idx >= n_items) break;
-        const Item item = p.items[it_idx];
+        const Item item = item_at(p.units, it_idx, p.unit_heads);
         const int s = item.seq, h = item.head;
         const int q_start = p.cu_q_lens[s];
         const int ql = p.cu_q_lens[s + 1] - q_start;

@@ -129,7 +129,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
         it = __shfl_sync(0xffffffffu, it, 0);
         bool ok = true;
         while (ok && it < n_items) {
-            const Item item = a.items[it];
+            const Item item = item_at(a.units, it, a.unit_heads);
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(ctrl + a.counter_word, 1);
             const int q_start = a.cu_q_lens[item.seq];

@@ -282,7 +282,8 @@ int rpa_profile_read(RpaHandle* h, float* ms, int32_t max_calls, int32_t* n_call
     static const int to[4] = {kEvPlanEnd, kEvDecEnd, kEvPfEnd, kEvCombEnd};
     for (int c = 0; c < n; ++c) {
         cudaEvent_t* e = h->prof_ev + (size_t)c * kProfEvents;
-        if (cudaEventSynchronize(e[kEvCombEnd]) != cudaSuccess) return RPA_ERR_CUDA;
+        if (cudaEventSynchronize(e[kEvCombEnd]) != cudaSuccess || cudaEventSynchronize(e[kEvPfEnd]) != cudaSuccess)
+            return RPA_ERR_CUDA;
         for (int k = 0; k < 4; ++k) {
             float t = 0.f;
             if (cudaEventElapsedTime(&t, e[from[k]], e[to[k]]) != cudaSuccess) return RPA_ERR_CUDA;
@@ -397,11 +398,33 @@ int rpa_read_plan(RpaHandle* h, int32_t* info, int32_t* items, int64_t max_items
     info[14] = h->ks.pf_bps;
     info[15] = h->concurrent | ((h->ks.tc8 | h->ks.mla) << 1);
     if (items && max_items > 0) {
+        // the kernels' unit lists, each unit expanded to its items (one per kv head, as item_at)
+        const int64_t H = h->ks.Hp;
         const int64_t nd = ctrl[kNumDecItems] < max_items ? ctrl[kNumDecItems] : max_items;
         const int64_t np = ctrl[kNumPfItems] < max_items - nd ? ctrl[kNumPfItems] : max_items - nd;
-        if ((nd && cudaMemcpy(items, h->w.dec_items, nd * sizeof(Item), cudaMemcpyDeviceToHost) != cudaSuccess) ||
-            (np && cudaMemcpy(items + nd * 8, h->w.pf_items, np * sizeof(Item), cudaMemcpyDeviceToHost) != cudaSuccess))
+        const int64_t ud = (nd + H - 1) / H, up = (np + H - 1) / H;
+        Unit* u = static_cast<Unit*>(malloc((size_t)(ud + up + 1) * sizeof(Unit)));
+        if (!u) return RPA_ERR_INVALID_ARG;
+        if ((ud && cudaMemcpy(u, h->w.dec_units, ud * sizeof(Unit), cudaMemcpyDeviceToHost) != cudaSuccess) ||
+            (up && cudaMemcpy(u + ud, h->w.pf_units, up * sizeof(Unit), cudaMemcpyDeviceToHost) != cudaSuccess)) {
+            free(u);
             return RPA_ERR_CUDA;
+        }
+        for (int64_t i = 0; i < nd + np; ++i) {
+            const int64_t it = i < nd ? i : i - nd;
+            const Unit& x = u[(i < nd ? 0 : ud) + it / H];
+            const int hd = (int)(it % H);
+            int32_t* d = items + i * 8;
+            d[0] = x.seq;
+            d[1] = hd;
+            d[2] = x.tok0;
+            d[3] = x.ntok;
+            d[4] = x.kv_begin;
+            d[5] = x.kv_end;
+            d[6] = x.part >= 0 ? x.part + hd * x.pieces + x.piece : -1;
+            d[7] = x.piece;
+        }
+        free(u);
     }
     return RPA_OK;
 }

@@ -36,6 +36,29 @@ enum Ctrl : int {
 struct Item {
     int seq, head, tok0, ntok, kv_begin, kv_end, part, piece;
 };
+// One work unit (the planner's list): a sequence's query tokens [tok0, tok0 + ntok) against keys
+// [kv_begin, kv_end), piece `piece` of `pieces`; `part` is the first partial slot of its split
+// sequence (or -1).  Unit u stands for items u H .. u H + H - 1, one per kv head (H the planner's
+// kv heads), whose partial slot is part + head * pieces + piece.
+struct Unit {
+    int seq, tok0, ntok, kv_begin, kv_end, part, piece, pieces;
+};
+// Item `it` of a unit list of H kv heads
+__device__ __forceinline__ Item item_at(const Unit* units, int it, int H) {
+    const int u = it / H, h = it - u * H;
+    const int4* src = reinterpret_cast<const int4*>(units + u);
+    const int4 a = src[0], b = src[1];
+    Item r;
+    r.seq = a.x;
+    r.head = h;
+    r.tok0 = a.y;
+    r.ntok = a.z;
+    r.kv_begin = a.w;
+    r.kv_end = b.x;
+    r.part = b.y >= 0 ? b.y + h * b.w + b.z : -1;
+    r.piece = b.z;
+    return r;
+}
 
 // One split-KV combine entry: rows [0, rows) of the kv head `head` of the sequence whose first
 // query token is q0 merge `pieces` partials starting at slot `part` (32 bytes: two 16-byte loads)
@@ -62,7 +85,7 @@ constexpr int kMinChunk = 512;     // smallest split-KV piece (keys)
 constexpr int kChunkAlign = 64;    // pieces are multiples of this many keys
 constexpr int kMaxSort = 8192;     // units sorted by cost on the device
 constexpr int kSeqSmem = 4096;     // sequences whose plan scratch fits in shared memory
-constexpr int kSeqArrays = 7;      // per-sequence plan scratch arrays of S + 1 ints
+constexpr int kSeqArrays = 9;      // per-sequence plan scratch arrays of S + 1 ints
 constexpr int kPlanThreads = 512;
 // rates of the SM-split model (planner): FLOP/ns of one SM on prefill, B/ns one SM can
 // stream in the decode kernel, and HBM B/ns.  The first two are the rates measured with
@@ -97,15 +120,15 @@ struct PlanParams {
     int force_pf_sms;    // > 0: tuning hook, prefill SMs when both classes have work
     int force_dec_sms;   // > 0: tuning hook, decode SMs
     int max_units;   // capacity of the unit arrays
-    int max_dec_units, max_pf_units;  // capacities of the two item lists (in units)
+    int max_dec_units, max_pf_units;  // capacities of the two unit lists
     int max_part;    // capacity of partial slots
     int max_comb;    // capacity of combine entries
     int* ctrl;
     int* seq_scratch;  // [kSeqArrays * (max_num_seqs + 1)], used when the sequences overflow shared memory
     int* units;        // [max_units * 8]
     unsigned long long* keys;  // [max_units] (only used if > kMaxSort)
-    Item* dec_items;
-    Item* pf_items;
+    Unit* dec_units;   // the decode kernel's list, in order
+    Unit* pf_units;    // the prefill kernel's list, in order
     Comb* comb;
 };
 
@@ -123,7 +146,8 @@ struct AttnParams {
     float cap_log2;     // cap * log2(e)
     float v_scale;
     int* ctrl;
-    const Item* items;
+    const Unit* units;     // the kernel's unit list (item it: item_at(units, it, unit_heads))
+    int unit_heads;        // kv heads a unit stands for
     int item_count_word;   // ctrl index of the item count
     int counter_word;      // ctrl index of the work counter
     float* part_o;         // [max_part, kDecRows, D]
@@ -241,8 +265,8 @@ struct Workspace {
     int* ctrl;
     int* seq_scratch;
     int* units;
-    Item* dec_items;
-    Item* pf_items;
+    Unit* dec_units;
+    Unit* pf_units;
     Comb* comb;
     float* part_o;
     float* part_ml;

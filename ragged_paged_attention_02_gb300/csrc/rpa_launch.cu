@@ -12,7 +12,9 @@
 //   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128; 8-bit K/V at D 128 / 256 and
 //                   2-byte K/V at D 256, which also take the decode rows), the latent-attention
 //                   kernel (latent layout, every row) or the warp-MMA kernel (8-bit K/V at D 64)
-//   combine         split-KV merge, output of the uncovered rows
+//   combine         split-KV merge, output of the uncovered rows -- after the decode kernel on
+//                   its stream: it reads only the decode kernel's split-KV partials (prefill units
+//                   are never split) and writes rows no prefill unit writes
 //
 // Nothing here allocates: the caller owns the workspace.
 #include <string.h>
@@ -45,14 +47,14 @@ struct Layout {
 };
 
 Layout layout(const RpaCfg& c, const KernelSet& ks) {
-    const int64_t S = c.max_num_seqs, Hkv = ks.Hp;  // the planner's kv heads
+    const int64_t S = c.max_num_seqs;
     Layout L;
     size_t off = 0;
     L.ctrl = off; off = align256(off + kCtrlWords * sizeof(int));
     L.seq = off; off = align256(off + kSeqArrays * (size_t)(S + 1) * sizeof(int));
     L.units = off; off = align256(off + (size_t)ks.max_units * 8 * sizeof(int));
-    L.dec = off; off = align256(off + (size_t)ks.max_dec_units * Hkv * sizeof(Item));
-    L.pf = off; off = align256(off + (size_t)ks.max_pf_units * Hkv * sizeof(Item));
+    L.dec = off; off = align256(off + (size_t)ks.max_dec_units * sizeof(Unit));
+    L.pf = off; off = align256(off + (size_t)ks.max_pf_units * sizeof(Unit));
     L.comb = off; off = align256(off + (size_t)ks.max_comb * sizeof(Comb));
     L.po = off; off = align256(off + (size_t)ks.max_part * kDecRows * ks.D * sizeof(float));
     L.pml = off; off = align256(off + (size_t)ks.max_part * kDecRows * 2 * sizeof(float));
@@ -174,8 +176,8 @@ Workspace workspace_carve(const RpaCfg& c, const KernelSet& ks, void* base) {
     w.ctrl = reinterpret_cast<int*>(b + L.ctrl);
     w.seq_scratch = reinterpret_cast<int*>(b + L.seq);
     w.units = reinterpret_cast<int*>(b + L.units);
-    w.dec_items = reinterpret_cast<Item*>(b + L.dec);
-    w.pf_items = reinterpret_cast<Item*>(b + L.pf);
+    w.dec_units = reinterpret_cast<Unit*>(b + L.dec);
+    w.pf_units = reinterpret_cast<Unit*>(b + L.pf);
     w.comb = reinterpret_cast<Comb*>(b + L.comb);
     w.part_o = reinterpret_cast<float*>(b + L.po);
     w.part_ml = reinterpret_cast<float*>(b + L.pml);
@@ -237,8 +239,8 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     pp.seq_scratch = ws.seq_scratch;
     pp.units = ws.units;
     pp.keys = nullptr;
-    pp.dec_items = ws.dec_items;
-    pp.pf_items = ws.pf_items;
+    pp.dec_units = ws.dec_units;
+    pp.pf_units = ws.pf_units;
     pp.comb = ws.comb;
     if (launch_plan(pp, st, plan_smem_bytes()) != cudaSuccess) return RPA_ERR_CUDA;
     if (!rec(kEvPlanEnd, st)) return RPA_ERR_CUDA;
@@ -267,7 +269,8 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     ap.cap_log2 = ks.cap_log2;
     ap.v_scale = ks.v_scale;
     ap.ctrl = ws.ctrl;
-    ap.items = nullptr;
+    ap.units = nullptr;
+    ap.unit_heads = ks.Hp;
     ap.item_count_word = 0;
     ap.counter_word = 0;
     ap.part_o = ws.part_o;
@@ -276,10 +279,10 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     ap.odt = ks.odt;
     ap.q_f16 = ks.q_f16;
 
-    // With concurrent decode / prefill the decode kernel runs on the side stream, forked from st
-    // after the planner.  Once forked, every return joins it back (st waits for whatever was
-    // enqueued there), so that no kernel of this call is still writing the workspace when the
-    // caller's stream moves on.
+    // With concurrent decode / prefill the decode and combine kernels run on the side stream,
+    // forked from st after the planner.  Once forked, every return joins it back (st waits for
+    // whatever was enqueued there), so that no kernel of this call is still writing the workspace
+    // or o when the caller's stream moves on.
     cudaStream_t dst = st;  // stream of the decode kernel
     bool forked = false;
     auto join = [&]() -> bool {
@@ -329,7 +332,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     if (has_q && !ks.tc8 && !ks.mla) {
         DecParams dp;
         dp.a = ap;
-        dp.a.items = ws.dec_items;
+        dp.a.units = ws.dec_units;
         dp.a.item_count_word = kNumDecItems;
         dp.a.counter_word = kDecCounter;
         dp.BR = ks.BR;
@@ -345,7 +348,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
 
     if (!rec(kEvPfStart, st)) return fail(RPA_ERR_CUDA);
     if (has_q) {
-        ap.items = ws.pf_items;
+        ap.units = ws.pf_units;
         ap.item_count_word = kNumPfItems;
         ap.counter_word = kPfCounter;
         cudaError_t e;
@@ -373,7 +376,6 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
         if (e != cudaSuccess) return fail(RPA_ERR_CUDA);
     }
     if (!rec(kEvPfEnd, st)) return fail(RPA_ERR_CUDA);
-    if (!join()) return RPA_ERR_CUDA;
 
     CombParams cp;
     cp.o = static_cast<uint8_t*>(o);
@@ -391,10 +393,10 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     cp.comb = ws.comb;
     cp.part_o = ws.part_o;
     cp.part_ml = ws.part_ml;
-    if (!rec(kEvCombStart, st)) return RPA_ERR_CUDA;
-    if (launch_combine(cp, Launch{ks.sms * kCombCtasPerSm, st}) != cudaSuccess) return RPA_ERR_CUDA;
-    if (!rec(kEvCombEnd, st)) return RPA_ERR_CUDA;
-    return RPA_OK;
+    if (!rec(kEvCombStart, dst)) return fail(RPA_ERR_CUDA);
+    if (launch_combine(cp, Launch{ks.sms * kCombCtasPerSm, dst}) != cudaSuccess) return fail(RPA_ERR_CUDA);
+    if (!rec(kEvCombEnd, dst)) return fail(RPA_ERR_CUDA);
+    return join() ? RPA_OK : RPA_ERR_CUDA;
 }
 
 }  // namespace rpa

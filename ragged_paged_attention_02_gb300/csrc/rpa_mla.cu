@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1) rpa_mla_attn(const __grid_cons
         it = __shfl_sync(0xffffffffu, it, 0);
         bool ok = true;
         while (ok && it < n_items) {
-            const Item item = a.items[it];
+            const Item item = item_at(a.units, it, a.unit_heads);
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(ctrl + a.counter_word, 1);
             const int q_start = a.cu_q_lens[item.seq];

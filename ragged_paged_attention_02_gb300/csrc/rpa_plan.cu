@@ -27,6 +27,12 @@ namespace rpa {
 
 namespace {
 
+constexpr int kUnitSmem = 1024;    // unit descriptors kept in shared memory (else global)
+// with at most kUnitSmem units the sort touches keys [0, 3 kUnitSmem) (its range starts below
+// kUnitSmem and spans at most twice the keys), below the descriptors
+static_assert(3 * kUnitSmem <= kMaxSort / 2 && kUnitSmem * 8 * 4 <= kMaxSort / 2 * 8,
+              "unit descriptors share the key array's upper half");
+
 __device__ __forceinline__ void key_band(int kl, int ql, int i0, int i1, const PlanParams& p,
                                          int& lo, int& hi) {
     const int p_lo = kl - ql + i0;
@@ -36,54 +42,53 @@ __device__ __forceinline__ void key_band(int kl, int ql, int i0, int i1, const P
     if (hi < lo) hi = lo;
 }
 
-// Exclusive scan of four ints per thread over the whole block (one pass for
-// all four); *total gets the sums.  s_warp holds 33 int4.
-__device__ int4 block_scan4(int4 v, int4* s_warp, int4* total) {
+// Exclusive scan of N ints per thread over the whole block (one pass for all N): r gets the
+// thread's offsets, tot the block's sums.  s_scan holds 33 N ints.
+template <int N>
+__device__ void block_scan(const int (&v)[N], int (&r)[N], int (&tot)[N], int* s_scan) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = blockDim.x >> 5;
-    int4 x = v;
+    int x[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) x[i] = v[i];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int4 y;
-        y.x = __shfl_up_sync(0xffffffffu, x.x, o);
-        y.y = __shfl_up_sync(0xffffffffu, x.y, o);
-        y.z = __shfl_up_sync(0xffffffffu, x.z, o);
-        y.w = __shfl_up_sync(0xffffffffu, x.w, o);
-        if (lane >= o) {
-            x.x += y.x;
-            x.y += y.y;
-            x.z += y.z;
-            x.w += y.w;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const int y = __shfl_up_sync(0xffffffffu, x[i], o);
+            if (lane >= o) x[i] += y;
         }
     }
-    if (lane == 31) s_warp[warp] = x;
+    if (lane == 31) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) s_scan[warp * N + i] = x[i];
+    }
     __syncthreads();
     if (warp == 0) {
-        const int4 w = lane < nwarps ? s_warp[lane] : make_int4(0, 0, 0, 0);
-        int4 ww = w;
+        int w[N], ww[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) ww[i] = w[i] = lane < nwarps ? s_scan[lane * N + i] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int4 y;
-            y.x = __shfl_up_sync(0xffffffffu, ww.x, o);
-            y.y = __shfl_up_sync(0xffffffffu, ww.y, o);
-            y.z = __shfl_up_sync(0xffffffffu, ww.z, o);
-            y.w = __shfl_up_sync(0xffffffffu, ww.w, o);
-            if (lane >= o) {
-                ww.x += y.x;
-                ww.y += y.y;
-                ww.z += y.z;
-                ww.w += y.w;
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const int y = __shfl_up_sync(0xffffffffu, ww[i], o);
+                if (lane >= o) ww[i] += y;
             }
         }
-        s_warp[lane] = make_int4(ww.x - w.x, ww.y - w.y, ww.z - w.z, ww.w - w.w);
-        if (lane == 31) s_warp[32] = ww;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            s_scan[lane * N + i] = ww[i] - w[i];
+            if (lane == 31) s_scan[32 * N + i] = ww[i];
+        }
     }
     __syncthreads();
-    const int4 base = s_warp[warp];
-    const int4 r = make_int4(x.x - v.x + base.x, x.y - v.y + base.y, x.z - v.z + base.z, x.w - v.w + base.w);
-    *total = s_warp[32];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        r[i] = x[i] - v[i] + s_scan[warp * N + i];
+        tot[i] = s_scan[32 * N + i];
+    }
     __syncthreads();
-    return r;
 }
 
 // Sums of two 64-bit values per thread over the block (all threads get them).  s_red holds 64.
@@ -140,53 +145,9 @@ __device__ __forceinline__ int upper_seq(const int* ends, int n, int u) {
     return lo;
 }
 
-// Bitonic sort (ascending) of keys[0, 32 E) by one warp, in registers: element i = lane + 32 r
-// sits in lane `lane`, register r, so strides of 32 and more pair registers of one lane and
-// shorter strides pair lanes (shuffles); no block barrier.
-template <int E>
-__device__ void warp_sort(unsigned long long* keys, int lane) {
-    unsigned long long v[E];
-#pragma unroll
-    for (int r = 0; r < E; ++r) v[r] = keys[lane + 32 * r];
-    for (int k = 2; k <= 32 * E; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            if (j >= 32) {
-                // partner register r ^ jr of the same lane (jr a power of two below E)
-                const int jr = j >> 5;
-#pragma unroll
-                for (int b = 1; b < E; b <<= 1) {
-                    if (b != jr) continue;
-#pragma unroll
-                    for (int r = 0; r < E; ++r) {
-                        if (r & b) continue;
-                        const int i = lane + 32 * r;
-                        const bool up = (i & k) == 0;
-                        const unsigned long long a = v[r], c = v[r | b];
-                        const bool sw = (a > c) == up;
-                        v[r] = sw ? c : a;
-                        v[r | b] = sw ? a : c;
-                    }
-                }
-            } else {
-                const bool lower = (lane & j) == 0;
-#pragma unroll
-                for (int r = 0; r < E; ++r) {
-                    const int i = lane + 32 * r;
-                    const bool up = (i & k) == 0;
-                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v[r], j);
-                    const unsigned long long lo = v[r] < o ? v[r] : o, hi = v[r] < o ? o : v[r];
-                    v[r] = (lower == up) ? lo : hi;
-                }
-            }
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < E; ++r) keys[lane + 32 * r] = v[r];
-}
-
 __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p) {
     extern __shared__ __align__(16) unsigned long long s_keys[];  // kMaxSort keys, then sequence scratch
-    __shared__ int4 s_warp[33];
+    __shared__ int s_scan[33 * 5];
     __shared__ unsigned long long s_red[64];
     __shared__ int s_bad;
     __shared__ int s_split[2];                // prefill CTAs, decode CTAs
@@ -196,7 +157,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     pdl_trigger();  // the attention kernels may start their prologue now
     // per-sequence scratch (shared memory when it fits): class, count, decode / prefill
     // unit ends, partial offset, combine offset, decode sequences with a partial last piece before
-    // this one
+    // this one, first query token (S + 1 entries: cu_q_lens), kv_len
     int* seq_base = S <= kSeqSmem ? reinterpret_cast<int*>(s_keys + kMaxSort) : p.seq_scratch;
     int* s_cls = seq_base;
     int* s_cnt = s_cls + S + 1;
@@ -205,6 +166,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     int* s_part = s_pend + S + 1;
     int* s_comb = s_part + S + 1;
     int* s_ppre = s_comb + S + 1;
+    int* s_q0 = s_ppre + S + 1;
+    int* s_kl = s_q0 + S + 1;
     const int Tq = max(1, p.pf_tokens);  // query tokens per prefill tile
 
     if (tid == 0) s_bad = 0;
@@ -216,6 +179,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     for (int s = tid; s < S; s += blockDim.x) {
         const int q0 = p.cu_q_lens[s], q1 = p.cu_q_lens[s + 1], kl = p.kv_lens[s];
         const int ql = q1 - q0;
+        s_q0[s] = q0;
+        if (s == S - 1) s_q0[S] = q1;
+        s_kl[s] = kl;
         const bool bad = q0 < 0 || ql < 0 || kl < 0 || kl > p.P * p.ps || ql > kl || q1 > p.T;
         int cls = 0, cnt = 0;
         if (bad) {
@@ -322,23 +288,23 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 pu = cnt;
             }
         }
-        int4 tot, tot2;
-        const int4 off = block_scan4(make_int4(du, pu, pa, cb), s_warp, &tot);
-        const int4 off2 = block_scan4(make_int4(pp, 0, 0, 0), s_warp, &tot2);
+        const int v[5] = {du, pu, pa, cb, pp};
+        int off[5], tot[5];
+        block_scan<5>(v, off, tot, s_scan);
         if (s < S) {
-            s_ppre[s] = carry_pp + off2.x;
-            s_dend[s] = carry_d + off.x + du;
-            s_pend[s] = carry_p + off.y + pu;
+            s_ppre[s] = carry_pp + off[4];
+            s_dend[s] = carry_d + off[0] + du;
+            s_pend[s] = carry_p + off[1] + pu;
             if (s_cls[s] != 2) {  // partial and combine offsets are read for decode sequences only
-                s_part[s] = carry_part + off.z;
-                s_comb[s] = carry_comb + off.w;
+                s_part[s] = carry_part + off[2];
+                s_comb[s] = carry_comb + off[3];
             }
         }
-        carry_d += tot.x;
-        carry_p += tot.y;
-        carry_part += tot.z;
-        carry_comb += tot.w;
-        carry_pp += tot2.x;
+        carry_d += tot[0];
+        carry_p += tot[1];
+        carry_part += tot[2];
+        carry_comb += tot[3];
+        carry_pp += tot[4];
     }
     const int n_dec = carry_d, n_pf = carry_p, n_units = n_dec + n_pf;
     // decode pieces of a whole chunk (all of a sequence's but a shorter last one) share the highest
@@ -356,8 +322,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
     __syncthreads();
 
-    // ---- 4. unit descriptors and sort keys
+    // ---- 4. unit descriptors and sort keys.  Descriptors of up to kUnitSmem units sit in the
+    // upper half of the key array (the sort touches at most the first 2 kUnitSmem keys then)
     const bool do_sort = n_units <= kMaxSort && S < 65536;  // key fields: unit < 2^16, seq < 2^16
+    int* units = n_units <= kUnitSmem ? reinterpret_cast<int*>(s_keys + kMaxSort / 2) : p.units;
     for (int u = tid; u < n_units; u += blockDim.x) {
         int d[8];
         int cost, wseq = 0;
@@ -366,7 +334,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         if (u < n_dec) {
             const int s = upper_seq(s_dend, S, u);
             const int k = u - (s_dend[s] - (s_cnt[s] + chunk - 1) / chunk);  // piece index
-            const int q0 = p.cu_q_lens[s], ql = p.cu_q_lens[s + 1] - q0, kl = p.kv_lens[s];
+            const int ql = s_q0[s + 1] - s_q0[s], kl = s_kl[s];
             int lo, hi;
             key_band(kl, ql, 0, ql, p, lo, hi);
             const int pieces = (s_cnt[s] + chunk - 1) / chunk;
@@ -382,7 +350,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             const int v = u - n_dec;
             const int s = upper_seq(s_pend, S, v);
             const int k = v - (s_pend[s] - s_cnt[s]);  // tile index
-            const int q0 = p.cu_q_lens[s], ql = p.cu_q_lens[s + 1] - q0, kl = p.kv_lens[s];
+            const int ql = s_q0[s + 1] - s_q0[s], kl = s_kl[s];
             const int t0 = k * Tq;
             const int nt = min(Tq, ql - t0);
             int lo, hi;
@@ -394,7 +362,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             cls_bit = 1;
             pos = u;
         }
-        int4* dst = reinterpret_cast<int4*>(p.units + (size_t)u * 8);
+        int4* dst = reinterpret_cast<int4*>(units + (size_t)u * 8);
         dst[0] = make_int4(d[0], d[1], d[2], d[3]);
         dst[1] = make_int4(d[4], d[5], d[6], d[7]);
         // decode: cost descending.  Prefill: sequences by their heaviest unit descending (the
@@ -423,22 +391,27 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         while (n2 < n_units) n2 <<= 1;
     }
     unsigned long long* keys = s_keys + base;
-    if (do_sort && n_sort > 1 && n2 <= 256) {
-        // up to 256 keys: one warp, in registers
+    if (do_sort && n_sort > 1) {
         for (int i = n_sort + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
         __syncthreads();
-        if (tid < 32) {
-            switch (n2) {
-                case 32: warp_sort<1>(keys, tid); break;
-                case 64: warp_sort<2>(keys, tid); break;
-                case 128: warp_sort<4>(keys, tid); break;
-                default: warp_sort<8>(keys, tid); break;
+        // merge widths up to 32: every warp sorts its 32 keys in registers, by shuffles
+        for (int i = tid; i < n2; i += blockDim.x) {
+            unsigned long long v = keys[i];
+#pragma unroll
+            for (int k = 2; k <= 32; k <<= 1) {
+                const bool up = (i & k) == 0;
+#pragma unroll
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
+                    const bool lower = (i & j) == 0;
+                    const unsigned long long lo = v < o ? v : o, hi = v < o ? o : v;
+                    v = (lower == up) ? lo : hi;
+                }
             }
+            keys[i] = v;
         }
-    } else if (do_sort && n_sort > 1) {
-        for (int i = n_sort + tid; i < n2; i += blockDim.x) keys[i] = ~0ull;
         __syncthreads();
-        for (int k = 2; k <= n2; k <<= 1) {
+        for (int k = 64; k <= n2; k <<= 1) {
             // strides >= 32: pairs in different warps, through shared memory
             for (int j = k >> 1; j >= 32; j >>= 1) {
                 for (int i = tid; i < n2; i += blockDim.x) {
@@ -458,7 +431,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
             for (int i = tid; i < n2; i += blockDim.x) {
                 unsigned long long v = keys[i];
                 const bool up = (i & k) == 0;
-                for (int j = min(k >> 1, 16); j > 0; j >>= 1) {
+#pragma unroll
+                for (int j = 16; j > 0; j >>= 1) {
                     const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, j);
                     const bool lower = (i & j) == 0;
                     const unsigned long long lo = v < o ? v : o, hi = v < o ? o : v;
@@ -471,39 +445,39 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
     __syncthreads();
 
-    // ---- 6. items (one per kv head) in sorted unit order; consecutive threads write
-    // consecutive items (coalesced 16-byte stores)
-    for (int idx = tid; idx < n_units * p.Hkv; idx += blockDim.x) {
-        const int r = idx / p.Hkv, h = idx - r * p.Hkv;
+    // ---- 6. the unit lists in sorted order (each unit stands for one item per kv head); a
+    // thread writes one 16-byte half of a unit, consecutive threads consecutive halves
+    for (int c = tid; c < 2 * n_units; c += blockDim.x) {
+        const int r = c >> 1, hf = c & 1;
         // unit index: low 32 bits of a decode key, low 13 bits of a prefill key
         const unsigned long long key = do_sort ? s_keys[r] : 0ull;
         const int u = !do_sort ? r : (int)((key >> 63) ? (key & 0x1FFFull) : (key & 0xFFFFFFFFull));
-        const int4* src = reinterpret_cast<const int4*>(p.units + (size_t)u * 8);
-        const int4 a = src[0], b = src[1];
         // decode units come first; with dec_on_pf they lead the prefill kernel's list instead
         const bool is_dec = r < n_dec && !p.dec_on_pf;
-        Item* dst = is_dec ? p.dec_items + (size_t)r * p.Hkv
-                           : p.pf_items + (size_t)(p.dec_on_pf ? r : r - n_dec) * p.Hkv;
-        int4* d4 = reinterpret_cast<int4*>(dst + h);
-        // Item: seq, head, tok0, ntok | kv_begin, kv_end, part, piece
-        d4[0] = make_int4(a.x, h, a.y, a.z);
-        d4[1] = make_int4(a.w, b.x, b.y >= 0 ? b.y + h * b.w + b.z : -1, b.z);
+        Unit* dst = is_dec ? p.dec_units + r : p.pf_units + (p.dec_on_pf ? r : r - n_dec);
+        reinterpret_cast<int4*>(dst)[hf] = reinterpret_cast<const int4*>(units + (size_t)u * 8)[hf];
     }
-    // ---- 7. combine entries of split decode sequences
-    for (int s = tid; s < S; s += blockDim.x) {
-        if (s_cls[s] != 1) continue;
-        const int pieces = (s_cnt[s] + chunk - 1) / chunk;
-        if (pieces <= 1) continue;
-        const int q0 = p.cu_q_lens[s], rows = (p.cu_q_lens[s + 1] - q0) * p.G;
-        for (int h = 0; h < p.Hkv; ++h) {
-            Comb c;
-            c.q0 = q0;
-            c.rows = rows;
-            c.head = h;
-            c.part = s_part[s] + h * pieces;
-            c.pieces = pieces;
-            c.pad0 = c.pad1 = c.pad2 = 0;
-            p.comb[s_comb[s] + h] = c;
+    // ---- 7. combine entries of split decode sequences, a 16-byte half of one a thread: thread
+    // index c -> sequence c / 2H, half (c mod 2H) of its H entries, stepped without divisions
+    {
+        const int W = 2 * p.Hkv;
+        const int ds = (int)blockDim.x / W, dr = (int)blockDim.x - ds * W;
+        int s = tid / W, rem = tid - s * W;
+        for (; s < S; s += ds, rem += dr) {
+            if (rem >= W) {
+                rem -= W;
+                if (++s >= S) break;
+            }
+            if (s_cls[s] != 1) continue;
+            const int pieces = s_dend[s] - (s > 0 ? s_dend[s - 1] : 0);  // the sequence's decode units
+            if (pieces <= 1) continue;
+            const int h = rem >> 1;
+            // Comb: q0, rows, head, part | pieces, 0, 0, 0
+            int4* d4 = reinterpret_cast<int4*>(p.comb + s_comb[s] + h);
+            if ((rem & 1) == 0)
+                d4[0] = make_int4(s_q0[s], (s_q0[s + 1] - s_q0[s]) * p.G, h, s_part[s] + h * pieces);
+            else
+                d4[1] = make_int4(pieces, 0, 0, 0);
         }
     }
     if (tid == 0) {
@@ -516,8 +490,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         ctrl[kNumPart] = carry_part;
         ctrl[kNumUnits] = n_units;
         ctrl[kSorted] = do_sort ? 1 : 0;
-        ctrl[kCovLo] = S > 0 ? p.cu_q_lens[0] : 0;
-        ctrl[kCovHi] = S > 0 ? p.cu_q_lens[S] : 0;
+        ctrl[kCovLo] = S > 0 ? s_q0[0] : 0;
+        ctrl[kCovHi] = S > 0 ? s_q0[S] : 0;
         ctrl[kPfCtas] = s_split[0];
         ctrl[kDecCtas] = s_split[1];
         ctrl[kStatus] = 0;

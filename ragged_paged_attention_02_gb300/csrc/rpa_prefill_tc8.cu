@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                 }
                 break;
             }
-            const Item item = a.items[it];
+            const Item item = item_at(a.units, it, a.unit_heads);
             int nxt = 0;
             if (lane == 0) nxt = atomicAdd(ctrl + a.counter_word, 1);
             const int q_start = a.cu_q_lens[item.seq];

@@ -80,7 +80,11 @@ constexpr int kMlaDqk = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaRows = 16;
 constexpr int kPfRows = 64;        // rows of a prefill tile (4 warps x 16)
-constexpr int kDecWaves = 4;       // target decode items per resident CTA
+constexpr int kDecWaves = 4;       // target decode items per resident CTA (the most of any kernel)
+// ... on the 64-key-tile kernel, whose items pay a Q load into tensor memory and a pipeline ramp
+// each, and whose decode rows cost a full tile's tensor work: fewer, longer pieces (fp8_window
+// workload: 0.517 ms a step with 2 against 0.527 with 4)
+constexpr int kDecWavesTc8 = 2;
 constexpr int kMinChunk = 512;     // smallest split-KV piece (keys)
 constexpr int kChunkAlign = 64;    // pieces are multiples of this many keys
 constexpr int kMaxSort = 8192;     // units sorted by cost on the device
@@ -119,6 +123,7 @@ struct PlanParams {
     int hbm_gbs;         // HBM bandwidth (B/ns)
     int force_pf_sms;    // > 0: tuning hook, prefill SMs when both classes have work
     int force_dec_sms;   // > 0: tuning hook, decode SMs
+    int dec_waves;       // target decode items per CTA of the kernel that runs them
     int max_units;   // capacity of the unit arrays
     int max_dec_units, max_pf_units;  // capacities of the two unit lists
     int max_part;    // capacity of partial slots

@@ -8,7 +8,7 @@
 //
 //  * decode-class sequences (q_len * G <= decode tile rows) become units
 //    (sequence, key piece); their keys are split into pieces of `chunk` keys
-//    so that the decode kernel has about kDecWaves items per resident CTA
+//    so that the kernel that runs them has about dec_waves items per resident CTA
 //    (split-KV; partial results are merged by the combine kernel);
 //  * prefill-class sequences become units (sequence, query tile);
 //  * each unit expands to one item per kv head;
@@ -260,9 +260,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     __syncthreads();
     int chunk;
     {
-        // pieces for about kDecWaves items per CTA of the kernel that runs them
+        // pieces for about dec_waves items per CTA of the kernel that runs them
         const int dec_ctas = p.dec_on_pf ? s_split[0] : s_split[1];
-        const unsigned long long target = (unsigned long long)kDecWaves * (unsigned long long)max(1, dec_ctas);
+        const unsigned long long target = (unsigned long long)p.dec_waves * (unsigned long long)max(1, dec_ctas);
         unsigned long long c = (s_total + target - 1) / target;
         if (c < (unsigned long long)kMinChunk) c = kMinChunk;
         c = (c + kChunkAlign - 1) / kChunkAlign * kChunkAlign;

@@ -376,8 +376,8 @@ def test_resident_ctas_per_sm_as_designed(kw, dec_bps, pf_bps):
 
 def test_planner_matches_python_rederivation():
     """The device planner's items, chunk, CTA split and sort flag equal a plain Python restatement.
-    The cases span the sort's paths: a few keys (one warp, in registers), a few thousand (the
-    block-wide network), and decode batches whose whole-chunk pieces skip the sort."""
+    The cases span the sort's ranges: a few keys, a few thousand, and decode batches whose
+    whole-chunk pieces skip the sort."""
     from plan_model import plan
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
@@ -394,8 +394,10 @@ def test_planner_matches_python_rederivation():
         att = RaggedPagedAttention(**p.cfg_dict())
         att.forward(*to_dev(p), p.num_seqs)
         info, items = att.plan()
+        # the 64-key-tile kernel (8-bit K/V here) aims at 2 decode items a CTA, the others at 4
         ref = plan(p, dec_rows=int(info[5]), pf_tokens=int(info[6]), n_sms=int(info[12]), dec_bps=int(info[13]),
-                   pf_bps=int(info[14]), concurrent=bool(info[15] & 1), dec_on_pf=bool(info[15] & 2))
+                   pf_bps=int(info[14]), concurrent=bool(info[15] & 1), dec_on_pf=bool(info[15] & 2),
+                   waves=2 if name == "fp8" else 4)
         assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
         assert info[10] == ref["dec_ctas"] and info[11] == ref["pf_ctas"]
         assert info[9] == ref["sorted"] and info[7] == ref["n_part"]

@@ -31,7 +31,8 @@ constexpr int kCombThreads = 256;
 constexpr int kBatch = 8;  // pieces whose partial O loads a lane has in flight at once
 
 __global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kernel(const CombParams p) {
-    pdl_wait();  // the attention kernels' partials are complete from here on
+    pdl_trigger();  // the next call's planner may start its first phases now
+    pdl_wait();     // the attention kernels' partials are complete from here on
     const int n_comb = p.ctrl[kNumComb];
     const int D = p.D, G = p.G, Hq = p.Hq;
     const int lane = threadIdx.x & 31;

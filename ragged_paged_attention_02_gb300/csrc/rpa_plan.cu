@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
     __syncthreads();
     if (s_bad) {
+        pdl_wait();  // the previous call's kernels read the control words until they finish
         if (tid == 0) {
             for (int w = 1; w < kCtrlWords; ++w) ctrl[w] = 0;
             ctrl[kStatus] = RPA_ERR_BAD_LENGTHS;
@@ -314,6 +315,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     if (n_units > p.max_units || n_dec > p.max_dec_units || (p.dec_on_pf ? n_units : n_pf) > p.max_pf_units ||
         carry_part > p.max_part || carry_comb > p.max_comb) {
         // cannot happen with the create-time sizing; refuse rather than overflow
+        pdl_wait();
         if (tid == 0) {
             for (int w = 1; w < kCtrlWords; ++w) ctrl[w] = 0;
             ctrl[kStatus] = RPA_ERR_INVALID_ARG;
@@ -445,6 +447,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
     __syncthreads();
 
+    // Launched as a programmatic dependent of the previous call's combine kernel, the planner
+    // gets here while that call may still be merging: the phases above touch only the inputs,
+    // shared memory and scratch no earlier kernel reads; what follows rewrites what they read
+    pdl_wait();
+
     // ---- 6. the unit lists in sorted order (each unit stands for one item per kv head); a
     // thread writes one 16-byte half of a unit, consecutive threads consecutive halves
     for (int c = tid; c < 2 * n_units; c += blockDim.x) {
@@ -503,8 +510,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
 size_t plan_smem_bytes() { return sizeof(unsigned long long) * kMaxSort + sizeof(int) * kSeqArrays * (kSeqSmem + 1); }
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem) {
-    rpa_plan_kernel<<<1, kPlanThreads, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(rpa_plan_kernel, 1, kPlanThreads, smem, st, p);
 }
 
 cudaError_t plan_prepare() {

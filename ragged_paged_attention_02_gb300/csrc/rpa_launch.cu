@@ -12,9 +12,12 @@
 //   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128; 8-bit K/V at D 128 / 256 and
 //                   2-byte K/V at D 256, which also take the decode rows), the latent-attention
 //                   kernel (latent layout, every row) or the warp-MMA kernel (8-bit K/V at D 64)
-//   combine         split-KV merge, output of the uncovered rows -- after the decode kernel on
-//                   its stream: it reads only the decode kernel's split-KV partials (prefill units
-//                   are never split) and writes rows no prefill unit writes
+//   combine         split-KV merge, output of the uncovered rows
+//
+// Each kernel is a programmatic dependent of the one before it on the caller's stream (its
+// prologue overlaps the previous kernel's tail); the planner, of the previous call's combine
+// kernel when that is the stream's last work.  With concurrent decode / prefill, decode runs on
+// the side stream, forked after the planner and joined before the combine.
 //
 // Nothing here allocates: the caller owns the workspace.
 #include <string.h>
@@ -280,8 +283,8 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     ap.odt = ks.odt;
     ap.q_f16 = ks.q_f16;
 
-    // With concurrent decode / prefill the decode and combine kernels run on the side stream,
-    // forked from st after the planner.  Once forked, every return joins it back (st waits for
+    // With concurrent decode / prefill the decode kernel runs on the side stream, forked from st
+    // after the planner.  Once forked, every return joins it back (st waits for
     // whatever was enqueued there), so that no kernel of this call is still writing the workspace
     // or o when the caller's stream moves on.
     cudaStream_t dst = st;  // stream of the decode kernel
@@ -377,6 +380,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
         if (e != cudaSuccess) return fail(RPA_ERR_CUDA);
     }
     if (!rec(kEvPfEnd, st)) return fail(RPA_ERR_CUDA);
+    if (!join()) return RPA_ERR_CUDA;
 
     CombParams cp;
     cp.o = static_cast<uint8_t*>(o);
@@ -394,10 +398,10 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     cp.comb = ws.comb;
     cp.part_o = ws.part_o;
     cp.part_ml = ws.part_ml;
-    if (!rec(kEvCombStart, dst)) return fail(RPA_ERR_CUDA);
-    if (launch_combine(cp, Launch{ks.sms * kCombCtasPerSm, dst}) != cudaSuccess) return fail(RPA_ERR_CUDA);
-    if (!rec(kEvCombEnd, dst)) return fail(RPA_ERR_CUDA);
-    return join() ? RPA_OK : RPA_ERR_CUDA;
+    if (!rec(kEvCombStart, st)) return RPA_ERR_CUDA;
+    if (launch_combine(cp, Launch{ks.sms * kCombCtasPerSm, st}) != cudaSuccess) return RPA_ERR_CUDA;
+    if (!rec(kEvCombEnd, st)) return RPA_ERR_CUDA;
+    return RPA_OK;
 }
 
 }  // namespace rpa

@@ -782,51 +782,35 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
                     xm[tg & 1][half][L] = mh;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(xb);
-                    // P = 2^(x - base) in f16 into the S columns (the copy's own, zero elsewhere);
-                    // returns the row's sum of it (x - base and the sums on pairs, f32x2)
-                    auto make_p = [&](float base) -> float {
-                        const uint64_t nbase2 = f32x2(-base, -base);
-                        uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
-                        uint32_t own[NK / 2];
-#pragma unroll
-                        for (int i = 0; i < NK / 2; ++i) {
-                            float x0, x1;
-                            f32x2_split(fadd2(f32x2(__uint_as_float(kv[2 * i]), __uint_as_float(kv[2 * i + 1])), nbase2),
-                                        x0, x1);
-                            const float p0 = ex2(x0), p1 = ex2(x1);
-                            ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
-                            own[i] = pack2<F16>(p0, p1);
-                        }
-                        // the half's 16 P columns (P[i] at column i / 2)
-                        uint32_t pk[HC / 2];
-#pragma unroll
-                        for (int k = 0; k < HC / 2; ++k) pk[k] = (F == 1 || k / (NK / 2) == c) ? own[k % (NK / 2)] : 0u;
-                        tmem_st16(lane_addr + (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * (HC / 2), pk);
-                        float la, lb, lc, ld;
-                        f32x2_split(ls2[0], la, lb);
-                        f32x2_split(ls2[1], lc, ld);
-                        return (la + lb) + (lc + ld);
-                    };
-                    // 8-bit K/V: while the other half's maxima are on their way, P against the
-                    // running max, kept unless some row of either half outgrows it (the usual case
-                    // after the first tiles): fp8_window 0.516 -> 0.507 ms a step.  Not in direct
-                    // mode, where it measured slower (long_prefill_d256 1.977 -> 2.006 ms)
-                    const bool grow = DIRECT || __any_sync(0xffffffffu, mh > m_run + kRescaleLog2);
-                    float lt = 0.f;
-                    if (!grow) lt = make_p(m_run == -INFINITY ? 0.f : m_run);
                     if (!mbar_wait(xb, xph, ctrl, tmo)) return false;
                     xph ^= 1u;
                     const float mt = fmaxf(mh, xm[tg & 1][half ^ 1][L]);
                     const bool need = __any_sync(0xffffffffu, mt > m_run + kRescaleLog2);
                     const float m_new = need ? fmaxf(m_run, mt) : m_run;
                     const float alpha = !need ? 1.f : (m_run == -INFINITY ? 0.f : ex2(m_run - m_new));
-                    if (need || grow) {
-                        // not yet, or again: the early P's tensor-memory stores complete first (two
-                        // stores of one thread to a column are not ordered otherwise)
-                        if (!grow) tmem_st_wait();
-                        lt = make_p(m_new == -INFINITY ? 0.f : m_new);
+                    const float base = m_new == -INFINITY ? 0.f : m_new;
+                    // P = 2^(x - base) in f16; x - base and the running sums on pairs (f32x2)
+                    const uint64_t nbase2 = f32x2(-base, -base);
+                    uint64_t ls2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+                    uint32_t own[NK / 2];
+#pragma unroll
+                    for (int i = 0; i < NK / 2; ++i) {
+                        float x0, x1;
+                        f32x2_split(fadd2(f32x2(__uint_as_float(kv[2 * i]), __uint_as_float(kv[2 * i + 1])), nbase2),
+                                    x0, x1);
+                        const float p0 = ex2(x0), p1 = ex2(x1);
+                        ls2[i & 1] = fadd2(ls2[i & 1], f32x2(p0, p1));
+                        own[i] = pack2<F16>(p0, p1);
                     }
-                    l_run = l_run * alpha + lt;
+                    // the half's 16 P columns (P[i] at column i / 2): the copy's own, zero elsewhere
+                    uint32_t pk[HC / 2];
+#pragma unroll
+                    for (int k = 0; k < HC / 2; ++k) pk[k] = (F == 1 || k / (NK / 2) == c) ? own[k % (NK / 2)] : 0u;
+                    tmem_st16(lane_addr + (b2 ? Gm::TM_S1 : Gm::TM_S0) + half * (HC / 2), pk);
+                    float la, lb, lc, ld;
+                    f32x2_split(ls2[0], la, lb);
+                    f32x2_split(ls2[1], lc, ld);
+                    l_run = l_run * alpha + ((la + lb) + (lc + ld));
                     m_run = m_new;
                     if (need && t > 0) {
                         // this warp's half of the O row holds the item's PVs up to tile t-1

@@ -109,9 +109,18 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
         mbar_init(smem_u32(&merge_bar), kCW);
         fence_mbar_init();
     }
+    __shared__ int s_plan_ok;
     __syncthreads();
     pdl_trigger();
-    pdl_wait();  // the planner's items are complete from here on
+    if (p.plan_epoch >= 0) {
+        // behind the prefill kernel on one stream: the planner's items are complete once it has
+        // published this call's epoch
+        if (tid == 0) s_plan_ok = flag_wait(ctrl + kPlanEpoch, p.plan_epoch, ctrl, tmo) ? 1 : 0;
+        __syncthreads();
+        if (!s_plan_ok) return;
+    } else {
+        pdl_wait();  // the planner's items are complete from here on
+    }
     if ((int)blockIdx.x >= a.ctrl[kDecCtas]) return;  // SMs left to the prefill kernel
     const int n_items = a.ctrl[a.item_count_word];
 
@@ -802,6 +811,9 @@ template <int D, int KT, int ROWS>
 __global__ void __launch_bounds__(kDecThreads, dec_min_blocks<D, ROWS>()) rpa_decode_attn(
     const __grid_constant__ CUtensorMap kvmap, const __grid_constant__ CUtensorMap qmap, const DecParams p) {
     decode_body<D, KT, ROWS>(kvmap, qmap, p);
+    // behind the prefill kernel: this grid completes only after it (the combine kernel and the
+    // next call depend on this grid alone)
+    if (p.plan_epoch >= 0) pdl_wait();
 }
 
 template <int D, int KT, int ROWS>

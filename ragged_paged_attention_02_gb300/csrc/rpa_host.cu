@@ -41,6 +41,7 @@ struct RpaHandle {
     int debug_stall;                // RPA_OPT_TEST_STALL_PRODUCER
     unsigned long long timeout_ns;  // RPA_OPT_WAIT_TIMEOUT_MS
     int force_pf_sms, force_dec_sms;  // RPA_OPT_PREFILL_SMS / RPA_OPT_DECODE_SMS
+    int epoch;                        // calls so far (the planner publishes each call's number)
 };
 
 namespace {
@@ -246,6 +247,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     eo.timeout_ns = h->timeout_ns;
     eo.force_pf_sms = h->force_pf_sms;
     eo.force_dec_sms = h->force_dec_sms;
+    eo.epoch = h->epoch = (h->epoch + 1) & 0x7FFFFFFF;
     h->concurrent = eo.conc;
     const int r = enqueue_forward(c, h->ks, h->w, &h->maps, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs,
                                   o, eo);

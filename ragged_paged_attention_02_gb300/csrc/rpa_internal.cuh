@@ -29,6 +29,7 @@ enum Ctrl : int {
     kCovHi = 11,   // end of covered tokens
     kPfCtas = 12,  // prefill CTAs that take work (the rest exit at once)
     kDecCtas = 13, // decode CTAs that take work
+    kPlanEpoch = 14,  // the epoch of the call whose plan is complete (the planner writes it last)
     kCtrlWords = 32,
 };
 
@@ -124,6 +125,7 @@ struct PlanParams {
     int force_pf_sms;    // > 0: tuning hook, prefill SMs when both classes have work
     int force_dec_sms;   // > 0: tuning hook, decode SMs
     int dec_waves;       // target decode items per CTA of the kernel that runs them
+    int epoch;           // this call's number, published in ctrl[kPlanEpoch] once the plan is out
     int max_units;   // capacity of the unit arrays
     int max_dec_units, max_pf_units;  // capacities of the two unit lists
     int max_part;    // capacity of partial slots
@@ -169,6 +171,10 @@ struct DecParams {
     int Tt;                 // query tokens per Q copy: 16 / G
     int debug_stall;        // test hook: the producer issues nothing
     unsigned long long timeout_ns;  // bound of every mbarrier wait
+    // >= 0: launched behind the prefill kernel on the same stream (concurrent decode / prefill):
+    // the CTAs wait for ctrl[kPlanEpoch] to reach this call's epoch instead of the grid dependency
+    // (which is then the prefill kernel), and wait for that dependency only before they exit
+    int plan_epoch;
 };
 
 struct TcParams {
@@ -298,6 +304,7 @@ struct EnqueueOpts {
     int debug_stall;
     unsigned long long timeout_ns;
     int force_pf_sms, force_dec_sms;
+    int epoch;  // this call's number (concurrent decode / prefill on one stream)
 };
 // Host only: fill ks from a validated configuration (sms = the device's SM count).
 void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks);
@@ -607,6 +614,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* ct
             set_status(ctrl, RPA_ERR_TIMEOUT);
             return false;
         }
+    }
+}
+// Wait for *flag (written by another kernel, released with a fence) to equal v, giving up after
+// timeout_ns: then the status word gets RPA_ERR_TIMEOUT and false is returned.
+__device__ __forceinline__ bool flag_wait(const int* flag, int v, int* ctrl, uint64_t timeout_ns) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        int x;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(x) : "l"(flag) : "memory");
+        if (x == v) return true;
+        if (global_ns() - t0 > timeout_ns) {
+            set_status(ctrl, RPA_ERR_TIMEOUT);
+            return false;
+        }
+        __nanosleep(200);
     }
 }
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -234,6 +234,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     pp.force_pf_sms = eo.force_pf_sms;
     pp.force_dec_sms = eo.force_dec_sms;
     pp.dec_waves = ks.tc8 ? kDecWavesTc8 : kDecWaves;
+    pp.epoch = eo.epoch;
     pp.max_units = ks.max_units;
     pp.max_dec_units = ks.max_dec_units;
     pp.max_pf_units = ks.max_pf_units;
@@ -298,7 +299,13 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
         join();
         return code;
     };
-    if (eo.conc) {
+    // Concurrent decode / prefill on one stream: the decode kernel is launched behind the
+    // prefill kernel (both programmatic dependents, so its CTAs take the SMs the prefill kernel
+    // leaves) and waits for the planner's published epoch instead.  With the per-kernel profile
+    // events on, the events between kernels would serialise them: the decode kernel then runs on
+    // the side stream, forked after the planner.
+    const bool one_stream = eo.conc && !ev[kEvStart];
+    if (eo.conc && !one_stream) {
         if (cudaEventRecord(eo.ev_plan, st) != cudaSuccess || cudaStreamWaitEvent(eo.side, eo.ev_plan, 0) != cudaSuccess)
             return RPA_ERR_CUDA;
         dst = eo.side;
@@ -332,23 +339,28 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
             maps->q_ptr = qk;
         }
     }
-    if (!rec(kEvDecStart, dst)) return fail(RPA_ERR_CUDA);
-    if (has_q && !ks.tc8 && !ks.mla) {
-        DecParams dp;
-        dp.a = ap;
-        dp.a.units = ws.dec_units;
-        dp.a.item_count_word = kNumDecItems;
-        dp.a.counter_word = kDecCounter;
-        dp.BR = ks.BR;
-        dp.br_shift = ks.br_shift;
-        dp.Tt = ks.Tt;
-        dp.debug_stall = eo.debug_stall;
-        dp.timeout_ns = eo.timeout_ns;
-        if (launch_decode_tma(maps->kv, maps->q, dp, ks.kt, ks.dec_rows, Launch{ks.sms * ks.dec_bps, dst}) !=
-            cudaSuccess)
-            return fail(RPA_ERR_CUDA);
-    }
-    if (!rec(kEvDecEnd, dst)) return fail(RPA_ERR_CUDA);
+    const AttnParams ap_dec = ap;
+    auto launch_dec = [&](cudaStream_t on, int plan_epoch) -> bool {
+        if (!rec(kEvDecStart, on)) return false;
+        if (has_q && !ks.tc8 && !ks.mla) {
+            DecParams dp;
+            dp.a = ap_dec;
+            dp.a.units = ws.dec_units;
+            dp.a.item_count_word = kNumDecItems;
+            dp.a.counter_word = kDecCounter;
+            dp.BR = ks.BR;
+            dp.br_shift = ks.br_shift;
+            dp.Tt = ks.Tt;
+            dp.debug_stall = eo.debug_stall;
+            dp.timeout_ns = eo.timeout_ns;
+            dp.plan_epoch = plan_epoch;
+            if (launch_decode_tma(maps->kv, maps->q, dp, ks.kt, ks.dec_rows, Launch{ks.sms * ks.dec_bps, on}) !=
+                cudaSuccess)
+                return false;
+        }
+        return rec(kEvDecEnd, on);
+    };
+    if (!one_stream && !launch_dec(dst, -1)) return fail(RPA_ERR_CUDA);
 
     if (!rec(kEvPfStart, st)) return fail(RPA_ERR_CUDA);
     if (has_q) {
@@ -380,6 +392,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
         if (e != cudaSuccess) return fail(RPA_ERR_CUDA);
     }
     if (!rec(kEvPfEnd, st)) return fail(RPA_ERR_CUDA);
+    if (one_stream && !launch_dec(st, eo.epoch)) return RPA_ERR_CUDA;
     if (!join()) return RPA_ERR_CUDA;
 
     CombParams cp;

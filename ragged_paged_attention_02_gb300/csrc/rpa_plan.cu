@@ -33,6 +33,13 @@ constexpr int kUnitSmem = 1024;    // unit descriptors kept in shared memory (el
 static_assert(3 * kUnitSmem <= kMaxSort / 2 && kUnitSmem * 8 * 4 <= kMaxSort / 2 * 8,
               "unit descriptors share the key array's upper half");
 
+// The plan of call `epoch` is complete (control words included): a decode kernel launched behind
+// the prefill kernel waits for this word instead of the planner grid.
+__device__ __forceinline__ void publish_epoch(int* ctrl, int epoch) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ctrl + kPlanEpoch), "r"(epoch) : "memory");
+}
+
 __device__ __forceinline__ void key_band(int kl, int ql, int i0, int i1, const PlanParams& p,
                                          int& lo, int& hi) {
     const int p_lo = kl - ql + i0;
@@ -217,6 +224,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         if (tid == 0) {
             for (int w = 1; w < kCtrlWords; ++w) ctrl[w] = 0;
             ctrl[kStatus] = RPA_ERR_BAD_LENGTHS;
+            publish_epoch(ctrl, p.epoch);
         }
         return;
     }
@@ -319,6 +327,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         if (tid == 0) {
             for (int w = 1; w < kCtrlWords; ++w) ctrl[w] = 0;
             ctrl[kStatus] = RPA_ERR_INVALID_ARG;
+            publish_epoch(ctrl, p.epoch);
         }
         return;
     }
@@ -487,6 +496,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
                 d4[1] = make_int4(pieces, 0, 0, 0);
         }
     }
+    // every thread's unit-list and combine-entry stores, before the plan is published
+    __threadfence();
+    __syncthreads();
     if (tid == 0) {
         ctrl[kNumDecItems] = p.dec_on_pf ? 0 : n_dec * p.Hkv;
         ctrl[kNumPfItems] = (p.dec_on_pf ? n_units : n_pf) * p.Hkv;
@@ -502,6 +514,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
         ctrl[kPfCtas] = s_split[0];
         ctrl[kDecCtas] = s_split[1];
         ctrl[kStatus] = 0;
+        publish_epoch(ctrl, p.epoch);
     }
 }
 

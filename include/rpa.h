@@ -215,9 +215,9 @@ typedef enum RpaOption {
     RPA_OPT_WAIT_TIMEOUT_MS = 1,   /* bound of every device-side wait, in ms (1 .. 3600000; default
                                       1000); a wait that runs out sets RPA_ERR_TIMEOUT */
     RPA_OPT_SERIAL = 2,            /* 1: run decode and prefill attention one after the other on the
-                                      caller's stream instead of concurrently on two streams with an
-                                      SM split (default 0; configurations without the split always
-                                      run serially) */
+                                      caller's stream instead of concurrently with an SM split
+                                      (default 0; configurations without the split always run
+                                      serially) */
     RPA_OPT_PREFILL_SMS = 3,       /* > 0: SMs given to prefill attention when both kernels have
                                       work and run concurrently (0 = the planner's model; tuning) */
     RPA_OPT_DECODE_SMS = 4,        /* > 0: SMs given to decode attention (0 = the planner's model) */

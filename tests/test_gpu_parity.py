@@ -381,12 +381,19 @@ def test_planner_matches_python_rederivation():
     from plan_model import plan
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
 
-    for name in ("tiny", "mixed", "fp8", "decode", "long_prefill", "mla_decode", "decode_g16"):
+    for name in ("tiny", "mixed", "fp8", "decode", "long_prefill", "mla_decode", "decode_g16", "many_units",
+                 "many_seqs"):
         if name in ("tiny", "decode", "long_prefill", "mla_decode", "decode_g16"):
             p = ri.workload(name)
         elif name == "mixed":
             p = ri.random_small(40, num_seqs=60, max_q=300, max_kv=5000, num_q_heads=32, num_kv_heads=8,
                                 head_dim=128, sliding_window=777)
+        elif name == "many_units":  # more units than the planner keeps in shared memory (1024)
+            p = ri.random_small(42, num_seqs=300, max_q=250, max_kv=3000, num_q_heads=8, num_kv_heads=1,
+                                head_dim=64)
+        elif name == "many_seqs":  # more sequences than the planner's shared-memory scratch holds (4096)
+            p = ri.random_small(43, num_seqs=5000, decode_only=True, max_kv=100, num_q_heads=4,
+                                num_kv_heads=1, head_dim=64)
         else:  # fp8 K/V on tensor memory: decode units become prefill-kernel items
             p = ri.random_small(41, num_seqs=50, max_q=60, max_kv=6000, num_q_heads=16, num_kv_heads=8,
                                 head_dim=256, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05,
@@ -401,6 +408,9 @@ def test_planner_matches_python_rederivation():
         assert info[0] == 0 and info[4] == ref["chunk"] and info[8] == ref["n_units"]
         assert info[10] == ref["dec_ctas"] and info[11] == ref["pf_ctas"]
         assert info[9] == ref["sorted"] and info[7] == ref["n_part"]
+        if name == "many_units":
+            assert info[8] > 1024
+
         assert np.array_equal(items[: info[1]], ref["dec"])
         assert np.array_equal(items[info[1]:], ref["pf"])
         att.close()

@@ -32,8 +32,9 @@ struct RpaHandle {
     cudaEvent_t* prof_ev;   // [prof_cap][kProfEvents]
     int prof_cap;
     int prof_used;
-    // decode and prefill may run concurrently: decode on a second stream forked after the planner
-    int can_concurrent;   // the side stream and events exist (tensor-memory prefill of 2-byte K/V)
+    // decode and prefill may run concurrently (tensor-memory prefill of 2-byte K/V): on the caller's
+    // stream, or with the profile events on, decode on a second stream forked after the planner
+    int can_concurrent;   // and the side stream and events exist
     int serial;           // RPA_OPT_SERIAL: run the two one after the other on the caller's stream
     int concurrent;       // the mode of the last call
     cudaStream_t side;

@@ -7,8 +7,8 @@
 //   [q conversion]  only when q's type is not the MMA operand type the kernels read (f32 q, or a
 //                   16-bit q of the other 16-bit type): q rounded into the workspace
 //   planner         work items, split-KV pieces, SM split
-//   decode          (2-byte K/V: 8- or 16-row tiles; 8-bit K/V at D 64) -- on the side stream
-//                   when decode and prefill run concurrently
+//   decode          (2-byte K/V: 8- or 16-row tiles; 8-bit K/V at D 64) -- behind the prefill
+//                   kernel when decode and prefill run concurrently
 //   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128; 8-bit K/V at D 128 / 256 and
 //                   2-byte K/V at D 256, which also take the decode rows), the latent-attention
 //                   kernel (latent layout, every row) or the warp-MMA kernel (8-bit K/V at D 64)
@@ -16,8 +16,10 @@
 //
 // Each kernel is a programmatic dependent of the one before it on the caller's stream (its
 // prologue overlaps the previous kernel's tail); the planner, of the previous call's combine
-// kernel when that is the stream's last work.  With concurrent decode / prefill, decode runs on
-// the side stream, forked after the planner and joined before the combine.
+// kernel when that is the stream's last work.  With concurrent decode / prefill the decode
+// kernel follows the prefill kernel and waits for the planner's published epoch instead of its
+// grid dependency; while per-kernel profile events are on, it runs on the side stream instead,
+// forked after the planner and joined before the combine.
 //
 // Nothing here allocates: the caller owns the workspace.
 #include <string.h>
@@ -284,10 +286,9 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     ap.odt = ks.odt;
     ap.q_f16 = ks.q_f16;
 
-    // With concurrent decode / prefill the decode kernel runs on the side stream, forked from st
-    // after the planner.  Once forked, every return joins it back (st waits for
-    // whatever was enqueued there), so that no kernel of this call is still writing the workspace
-    // or o when the caller's stream moves on.
+    // With the side stream forked (concurrent decode / prefill while profiling), every return
+    // joins it back (st waits for whatever was enqueued there), so that no kernel of this call is
+    // still writing the workspace or o when the caller's stream moves on.
     cudaStream_t dst = st;  // stream of the decode kernel
     bool forked = false;
     auto join = [&]() -> bool {

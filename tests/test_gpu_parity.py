@@ -583,8 +583,9 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 
 def test_serial_option_matches_concurrent_bit_for_bit():
-    """RPA_OPT_SERIAL runs decode and prefill one after the other instead of on two streams at
-    once with an SM split; the work items are the same, so the outputs are identical."""
+    """RPA_OPT_SERIAL runs decode and prefill one after the other instead of at once with an SM
+    split (the decode kernel behind the prefill kernel, waiting for the planner's published
+    epoch); the work items are the same, so the outputs are identical."""
     from ragged_paged_attention_02_gb300 import RaggedPagedAttention
     from ragged_paged_attention_02_gb300.binding import RPA_OPT_SERIAL
 

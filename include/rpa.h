@@ -221,6 +221,12 @@ typedef enum RpaOption {
     RPA_OPT_PREFILL_SMS = 3,       /* > 0: SMs given to prefill attention when both kernels have
                                       work and run concurrently (0 = the planner's model; tuning) */
     RPA_OPT_DECODE_SMS = 4,        /* > 0: SMs given to decode attention (0 = the planner's model) */
+    RPA_OPT_PLAN_EARLY = 5,        /* 1: the caller guarantees that a call's kv_lens and cu_q_lens are
+                                      complete when the call is enqueued (no kernel still writing them
+                                      precedes it on the stream: host copies, or kernels that end before
+                                      the call, satisfy this); the planner then reads and orders them
+                                      while the kernel before it (typically the previous call's
+                                      combine) still runs.  Default 0: it first waits for that kernel */
     RPA_OPT_TEST_STALL_PRODUCER = 100  /* test hook, 1: the decode kernel's copy warp issues nothing, so
                                       that its consumers' bounded waits run out (status
                                       RPA_ERR_TIMEOUT); the kernel still returns */

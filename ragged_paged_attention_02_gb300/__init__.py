@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     RPA_KV_SPLIT,
     RPA_OK,
     RPA_OPT_DECODE_SMS,
+    RPA_OPT_PLAN_EARLY,
     RPA_OPT_PREFILL_SMS,
     RPA_OPT_SERIAL,
     RPA_OPT_TEST_STALL_PRODUCER,

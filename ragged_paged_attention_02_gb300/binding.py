@@ -47,6 +47,7 @@ RPA_OPT_WAIT_TIMEOUT_MS = 1
 RPA_OPT_SERIAL = 2
 RPA_OPT_PREFILL_SMS = 3
 RPA_OPT_DECODE_SMS = 4
+RPA_OPT_PLAN_EARLY = 5
 RPA_OPT_TEST_STALL_PRODUCER = 100
 
 

@@ -42,6 +42,7 @@ struct RpaHandle {
     int debug_stall;                // RPA_OPT_TEST_STALL_PRODUCER
     unsigned long long timeout_ns;  // RPA_OPT_WAIT_TIMEOUT_MS
     int force_pf_sms, force_dec_sms;  // RPA_OPT_PREFILL_SMS / RPA_OPT_DECODE_SMS
+    int plan_early;                   // RPA_OPT_PLAN_EARLY
     int epoch;                        // calls so far (the planner publishes each call's number)
 };
 
@@ -248,6 +249,7 @@ int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t
     eo.timeout_ns = h->timeout_ns;
     eo.force_pf_sms = h->force_pf_sms;
     eo.force_dec_sms = h->force_dec_sms;
+    eo.plan_early = h->plan_early;
     eo.epoch = h->epoch = (h->epoch + 1) & 0x7FFFFFFF;
     h->concurrent = eo.conc;
     const int r = enqueue_forward(c, h->ks, h->w, &h->maps, q, kv_pages, kv_lens, page_indices, cu_q_lens, num_seqs,
@@ -312,6 +314,10 @@ int rpa_set_option(RpaHandle* h, int32_t option, int64_t value) {
         case RPA_OPT_DECODE_SMS:
             if (value < 0 || value > h->ks.sms) return RPA_ERR_INVALID_ARG;
             (option == RPA_OPT_PREFILL_SMS ? h->force_pf_sms : h->force_dec_sms) = (int)value;
+            return RPA_OK;
+        case RPA_OPT_PLAN_EARLY:
+            if (value != 0 && value != 1) return RPA_ERR_INVALID_ARG;
+            h->plan_early = (int)value;
             return RPA_OK;
         case RPA_OPT_TEST_STALL_PRODUCER:
             if (value != 0 && value != 1) return RPA_ERR_INVALID_ARG;

@@ -126,6 +126,7 @@ struct PlanParams {
     int force_dec_sms;   // > 0: tuning hook, decode SMs
     int dec_waves;       // target decode items per CTA of the kernel that runs them
     int epoch;           // this call's number, published in ctrl[kPlanEpoch] once the plan is out
+    int early;           // the inputs are complete at launch: read them before the grid dependency
     int max_units;   // capacity of the unit arrays
     int max_dec_units, max_pf_units;  // capacities of the two unit lists
     int max_part;    // capacity of partial slots
@@ -305,6 +306,7 @@ struct EnqueueOpts {
     unsigned long long timeout_ns;
     int force_pf_sms, force_dec_sms;
     int epoch;  // this call's number (concurrent decode / prefill on one stream)
+    int plan_early;  // RPA_OPT_PLAN_EARLY
 };
 // Host only: fill ks from a validated configuration (sms = the device's SM count).
 void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks);

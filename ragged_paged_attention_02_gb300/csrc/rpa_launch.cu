@@ -237,6 +237,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     pp.force_dec_sms = eo.force_dec_sms;
     pp.dec_waves = ks.tc8 ? kDecWavesTc8 : kDecWaves;
     pp.epoch = eo.epoch;
+    pp.early = eo.plan_early;
     pp.max_units = ks.max_units;
     pp.max_dec_units = ks.max_dec_units;
     pp.max_pf_units = ks.max_pf_units;

@@ -162,6 +162,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     const int S = p.num_seqs;
     int* ctrl = p.ctrl;
     pdl_trigger();  // the attention kernels may start their prologue now
+    // Launched as a programmatic dependent of the kernel before it on the stream, the planner may
+    // run while that kernel does.  Unless the caller has said that the inputs are complete at
+    // launch (RPA_OPT_PLAN_EARLY), it waits for that kernel before reading them; either way it
+    // waits before rewriting what earlier kernels read (below)
+    if (!p.early) pdl_wait();
     // per-sequence scratch (shared memory when it fits): class, count, decode / prefill
     // unit ends, partial offset, combine offset, decode sequences with a partial last piece before
     // this one, first query token (S + 1 entries: cu_q_lens), kv_len
@@ -456,9 +461,9 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     }
     __syncthreads();
 
-    // Launched as a programmatic dependent of the previous call's combine kernel, the planner
-    // gets here while that call may still be merging: the phases above touch only the inputs,
-    // shared memory and scratch no earlier kernel reads; what follows rewrites what they read
+    // With RPA_OPT_PLAN_EARLY the planner may get here while the previous call is still merging:
+    // the phases above touch only the inputs, shared memory and scratch no earlier kernel reads;
+    // what follows rewrites what they read
     pdl_wait();
 
     // ---- 6. the unit lists in sorted order (each unit stands for one item per kv head); a

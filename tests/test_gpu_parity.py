@@ -602,3 +602,53 @@ def test_serial_option_matches_concurrent_bit_for_bit():
     assert (info_a[15] & 1) == 1 and (info_b[15] & 1) == 0
     assert np.array_equal(a, b)
     att.close()
+
+
+def _two_batches(kind):
+    """Two batches of one configuration (same token count, page table shape and page count) with
+    different lengths: consecutive calls rewrite what the previous call's kernels read."""
+    rng = np.random.default_rng([55, 0])
+    if kind == "concurrent":
+        S, qmax, kmax, kw = 24, 150, 4000, dict(num_q_heads=16, num_kv_heads=4, head_dim=128, page_size=16)
+    else:
+        S, qmax, kmax, kw = 12, 3, 3000, dict(num_q_heads=16, num_kv_heads=1, head_dim=576, page_size=64,
+                                               kv_layout="latent", v_head_dim=512, sm_scale=1 / 24)
+    qa = rng.integers(1, qmax, size=S, endpoint=True)
+    qb = qa[::-1].copy()
+    ka = np.maximum(rng.integers(1, kmax, size=S, endpoint=True), qa)
+    kb = np.maximum(rng.integers(1, kmax, size=S, endpoint=True), qb)
+    ps = kw["page_size"]
+    used = max(int(((ka + ps - 1) // ps).sum()), int(((kb + ps - 1) // ps).sum()))
+    common = dict(pages_per_seq=(kmax + ps - 1) // ps, total_num_pages=used + 3, **kw)
+    return [ri.build(seed=56, q_lens=qa, kv_lens=ka, **common), ri.build(seed=57, q_lens=qb, kv_lens=kb, **common)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["concurrent", "latent"])
+def test_plan_early_option_back_to_back_calls(kind):
+    """RPA_OPT_PLAN_EARLY lets each call's planner read its inputs while the previous call's last
+    kernel still runs.  Back-to-back calls on one stream, alternating between two batches, give
+    the same outputs as the default mode and the oracle."""
+    import torch
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+    from ragged_paged_attention_02_gb300.binding import RPA_OPT_PLAN_EARLY
+
+    ps = _two_batches(kind)
+    cfg = ps[0].cfg_dict()
+    assert ps[1].cfg_dict() == cfg
+    ts = [to_dev(p) for p in ps]
+    outs = {}
+    for early in (0, 1):
+        att = RaggedPagedAttention(**cfg)
+        att.set_option(RPA_OPT_PLAN_EARLY, early)
+        res = []
+        for i in range(6):  # no synchronisation between the calls
+            res.append(att.forward(*ts[i % 2], ps[i % 2].num_seqs))
+        torch.cuda.synchronize()
+        assert att.status() == 0
+        outs[early] = [o_to_f64(r) for r in res]
+        att.close()
+    for i in range(6):
+        assert np.array_equal(outs[0][i], outs[1][i]), f"call {i}"
+    for i in range(2):
+        assert_close(outs[1][i], oracle.forward(ps[i]), ps[i].kv_dtype, f"{kind} batch {i}")

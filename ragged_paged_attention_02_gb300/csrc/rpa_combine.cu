@@ -28,7 +28,7 @@ namespace rpa {
 namespace {
 
 constexpr int kCombThreads = 256;
-constexpr int kBatch = 8;  // pieces whose partial O loads a lane has in flight at once
+constexpr int kBatch = 6;  // pieces whose partial O loads a lane has in flight at once
 
 __global__ void __launch_bounds__(kCombThreads, kCombCtasPerSm) rpa_combine_kernel(const CombParams p) {
     pdl_trigger();  // the next call's planner may start its first phases now

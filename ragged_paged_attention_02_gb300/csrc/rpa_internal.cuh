@@ -222,7 +222,7 @@ cudaError_t launch_pdl(Kern k, int grid, int block, size_t smem, cudaStream_t st
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
 // kt: KvType of kv_pages
 cudaError_t launch_prefill(const AttnParams& p, int kt, const Launch& l);
-constexpr int kCombCtasPerSm = 3;  // combine CTAs resident per SM (its register budget)
+constexpr int kCombCtasPerSm = 4;  // combine CTAs resident per SM (its register budget: 64)
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
 // rows: query rows of a decode tile, 16 (any) or 8 (2-byte K/V, G <= 8: keys on the MMA's M side)
 cudaError_t launch_decode_tma(const CUtensorMap& kvm, const CUtensorMap& qm, const DecParams& p, int kt,

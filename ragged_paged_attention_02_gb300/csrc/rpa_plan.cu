@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) rpa_plan_kernel(PlanParams p)
     __syncthreads();
 
     // ---- 4. unit descriptors and sort keys.  Descriptors of up to kUnitSmem units sit in the
-    // upper half of the key array (the sort touches at most the first 2 kUnitSmem keys then)
+    // upper half of the key array (the sort then touches only keys below 3 kUnitSmem)
     const bool do_sort = n_units <= kMaxSort && S < 65536;  // key fields: unit < 2^16, seq < 2^16
     int* units = n_units <= kUnitSmem ? reinterpret_cast<int*>(s_keys + kMaxSort / 2) : p.units;
     for (int u = tid; u < n_units; u += blockDim.x) {

@@ -652,3 +652,53 @@ def test_plan_early_option_back_to_back_calls(kind):
         assert np.array_equal(outs[0][i], outs[1][i]), f"call {i}"
     for i in range(2):
         assert_close(outs[1][i], oracle.forward(ps[i]), ps[i].kv_dtype, f"{kind} batch {i}")
+
+
+def _three_batches(kind):
+    """Three batches of one configuration (rolled query lengths, fresh key lengths)."""
+    rng = np.random.default_rng([77, 0])
+    if kind == "concurrent":
+        S, qmax, kmax, kw = 32, 200, 6000, dict(num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=16)
+    elif kind == "fp8":
+        S, qmax, kmax, kw = 24, 64, 6000, dict(num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
+                                               kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0,
+                                               sliding_window=2000)
+    else:
+        S, qmax, kmax, kw = 24, 2, 6000, dict(num_q_heads=16, num_kv_heads=1, head_dim=576, page_size=64,
+                                              kv_layout="latent", v_head_dim=512, sm_scale=1 / 24)
+    base_q = rng.integers(1, qmax, size=S, endpoint=True)
+    qs = [np.roll(base_q, i) for i in range(3)]
+    ks = [np.maximum(rng.integers(1, kmax, size=S, endpoint=True), q) for q in qs]
+    ps = kw["page_size"]
+    used = max(int(((k + ps - 1) // ps).sum()) for k in ks)
+    common = dict(pages_per_seq=(kmax + ps - 1) // ps, total_num_pages=used + 3, **kw)
+    return [ri.build(seed=80 + i, q_lens=qs[i], kv_lens=ks[i], **common) for i in range(3)]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("kind", ["concurrent", "fp8", "latent"])
+def test_back_to_back_calls_bit_equal_to_synchronised_calls(kind):
+    """Forty calls in a seeded random order over three batches, with no synchronisation between
+    them (each call's planner, attention kernels and merge overlapping its neighbours as the launch
+    order allows, RPA_OPT_PLAN_EARLY on): every output bit-equal to a synchronised call on the same
+    batch.  A race between consecutive calls would show as a mismatch."""
+    import torch
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+    from ragged_paged_attention_02_gb300.binding import RPA_OPT_PLAN_EARLY
+
+    ps = _three_batches(kind)
+    ts = [to_dev(p) for p in ps]
+    att = RaggedPagedAttention(**ps[0].cfg_dict())
+    att.set_option(RPA_OPT_PLAN_EARLY, 1)
+    ref = []
+    for i, p in enumerate(ps):
+        ref.append(o_to_f64(att.forward(*ts[i], p.num_seqs)))
+        torch.cuda.synchronize()
+    order = [int(x) for x in np.random.default_rng([78, 0]).integers(0, 3, size=40)]
+    outs = [att.forward(*ts[i], ps[i].num_seqs) for i in order]
+    torch.cuda.synchronize()
+    assert att.status() == 0
+    for n, (o, i) in enumerate(zip(outs, order)):
+        assert np.array_equal(o_to_f64(o), ref[i]), f"call {n} (batch {i})"
+    att.close()
+    assert_close(ref[0], oracle.forward(ps[0]), ps[0].kv_dtype, kind)

@@ -441,7 +441,9 @@ def measure(name, steps, warmup, dist, dev, world, e2e_steps=0):
         # SMs (the other kernel may hold them all), not work, so it is listed as idle instead
         "kernels_ms": {n: float(v) for n, v in zip(KERNEL_NAMES, mean_k) if has_work.get(n, True)},
         "idle_kernels": [n for n in KERNEL_NAMES if not has_work.get(n, True)],
-        "roofline": roof, "gpu_launches": 4 * K, "clocks": clk,
+        # a call launches the planner, the prefill-side kernel, the combine and (unless the
+        # prefill-side kernel takes the decode units too) the decode kernel
+        "roofline": roof, "gpu_launches": (3 if int(info[15]) & 2 else 4) * K, "clocks": clk,
     }
 
     # end to end through the public host-buffer entry point

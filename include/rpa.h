@@ -159,7 +159,10 @@ int rpa_create(const RpaCfg* cfg, RpaHandle** out);
  * rpa_get_status: bad lengths leave every row of o zero; a bad page id is
  * never dereferenced (its keys read as zero) and leaves the rows of the
  * sequences that use it unspecified.  Calls on one handle must be serialised
- * on the GPU (one stream, or ordered streams): they share the workspace. */
+ * on the GPU (one stream, or ordered streams): they share the workspace.
+ * The call may be captured into a CUDA graph (after one eager call, which
+ * sets kernel attributes); the graph's replays read the buffers passed at
+ * capture and must be serialised like calls. */
 int rpa_forward(RpaHandle* h, const void* q, const void* kv_pages, const int32_t* kv_lens,
                 const int32_t* page_indices, const int32_t* cu_q_lens, int32_t num_seqs,
                 void* o, void* stream);

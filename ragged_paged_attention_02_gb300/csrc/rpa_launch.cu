@@ -304,9 +304,13 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     // Concurrent decode / prefill on one stream: the decode kernel is launched behind the
     // prefill kernel (both programmatic dependents, so its CTAs take the SMs the prefill kernel
     // leaves) and waits for the planner's published epoch instead.  With the per-kernel profile
-    // events on, the events between kernels would serialise them: the decode kernel then runs on
-    // the side stream, forked after the planner.
-    const bool one_stream = eo.conc && !ev[kEvStart];
+    // events on, the events between kernels would serialise them, and a captured graph would
+    // replay one epoch: the decode kernel then runs on the side stream, forked after the planner.
+    // Under stream capture (a CUDA graph replays the call's parameters, the epoch included) the
+    // fork and join become graph edges instead.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (eo.conc && cudaStreamIsCapturing(st, &cap) != cudaSuccess) return RPA_ERR_CUDA;
+    const bool one_stream = eo.conc && !ev[kEvStart] && cap == cudaStreamCaptureStatusNone;
     if (eo.conc && !one_stream) {
         if (cudaEventRecord(eo.ev_plan, st) != cudaSuccess || cudaStreamWaitEvent(eo.side, eo.ev_plan, 0) != cudaSuccess)
             return RPA_ERR_CUDA;

@@ -50,12 +50,10 @@ def kernel_sources(prob, kernel):
         f = "rpa_decode.cu"
     elif prob.kv_layout == "latent":
         f = "rpa_mla.cu"
-    elif (eight and prob.head_dim in (128, 256)) or (not eight and prob.head_dim == 256):
+    elif eight or prob.head_dim == 256:
         f = "rpa_prefill_tc8.cu"
-    elif not eight:
-        f = "rpa_prefill_tc.cu"
     else:
-        f = "rpa_attn_mma.cu"
+        f = "rpa_prefill_tc.cu"
     return [CSRC + f, CSRC + "rpa_internal.cuh"]
 
 

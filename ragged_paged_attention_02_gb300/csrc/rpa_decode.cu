@@ -26,11 +26,9 @@
 // keys on the MMA's M side instead: S^T = K Q^T and O^T += V^T P^T, half the
 // MMAs and accumulator registers of a 16-row tile, three CTAs per SM.
 //
-// 8-bit K/V (e4m3, e5m2, int8): stages hold the raw bytes; each consumer warp
-// converts its 16 keys to f16 (exact) in its own buffer and runs the MMAs in
-// f16, with k_scale folded into the logit scale and v_scale into the epilogue.
-// f16 K/V run the MMAs in f16, bf16 K/V in bf16; Q arrives in that type (or,
-// with 8-bit K/V, as bf16 rounded to f16 when its fragments are loaded).
+// 2-byte K/V only: f16 K/V run the MMAs in f16, bf16 K/V in bf16, and Q
+// arrives in that type.  (8-bit K/V take the 64-key-tile tensor-memory kernel,
+// decode rows included.)
 //
 // Every wait is a bounded mbarrier wait (a global-timer deadline): on expiry
 // the status word gets RPA_ERR_TIMEOUT and the warp returns.
@@ -56,19 +54,16 @@ enum Meta : int {
 
 template <int D, int KT, int ROWS>
 struct DecGeom {
-    static constexpr bool FP8 = kt_8bit(KT);       // 8-bit K/V, converted to f16 by the consumers
+    static_assert(!kt_8bit(KT), "2-byte K/V");
     static constexpr int NS = ROWS == 8 ? 2 : 3;   // stages in the ring
-    static constexpr int E = FP8 ? 1 : 2;          // bytes per K/V element
     static constexpr int DHQ = D * 2 / 128;        // 128-byte column blocks of a bf16 row
-    static constexpr int DH = FP8 ? 1 : DHQ;       // column blocks per K/V box
+    static constexpr int DH = DHQ;                 // column blocks per K/V box
     static constexpr int QB = DHQ * ROWS * 128;    // Q area: [DHQ][ROWS lines][128 B]
-    static constexpr int KVB = kKS * 2 * D * E;    // K/V area of one stage
+    static constexpr int KVB = kKS * 2 * D * 2;    // K/V area of one stage
     static constexpr int SB = QB + KVB;            // one stage
-    static constexpr int CONV = FP8 ? 16 * D * 4 : 0;  // per-warp f16 buffer (K and V, 16 keys)
-    static constexpr int SMEM = NS * SB + kCW * CONV + 1024;  // + alignment slack
+    static constexpr int SMEM = NS * SB + 1024;    // + alignment slack
     static_assert(QB % 1024 == 0 && KVB % 1024 == 0, "stage alignment");
-    static_assert(kCW * ROWS * D * 4 <= (FP8 ? kCW * CONV : KVB), "merge area");
-    static_assert(ROWS == 16 || !FP8, "8-row tiles are for 2-byte K/V only");
+    static_assert(kCW * ROWS * D * 4 <= KVB, "merge area");
 };
 
 __device__ __forceinline__ uint32_t swz128(uint32_t line, uint32_t chunk) {
@@ -85,7 +80,6 @@ template <int D, int KT, int ROWS>
 __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUtensorMap& qmap, const DecParams& p) {
     using Gm = DecGeom<D, KT, ROWS>;
     constexpr int kNS = Gm::NS;
-    constexpr bool FP8 = Gm::FP8;
     constexpr bool F16 = kt_f16_mma(KT);  // MMA operands in f16 (else bf16)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kNS];
@@ -129,7 +123,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
         if (p.debug_stall) return;  // test hook: consumers must time out
         const int BR = p.BR, ps = a.ps;
         const int runs = kKS / BR;  // page runs per stage, one bulk copy each (K and V of the head)
-        const uint32_t run_bytes = FP8 ? (uint32_t)(2 * BR * D) : (uint32_t)(2 * Gm::DH * BR * 128);
+        const uint32_t run_bytes = (uint32_t)(2 * Gm::DH * BR * 128);
         const uint64_t pol_stream = l2_policy_evict_first();
         int s = 0;
         uint32_t ph = 0;
@@ -209,7 +203,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
                 // K/V a concurrent prefill re-reads
                 if (want && good)
                     tma_load_3d_hint(kv_base + (uint32_t)lane * run_bytes, &kvmap, fb, 0, pg * ps + (k0 - lp * ps),
-                                     FP8 ? 2 * item.head : 2 * item.head * Gm::DH, pol_stream);
+                                     2 * item.head * Gm::DH, pol_stream);
                 if (++s == kNS) {
                     s = 0;
                     ph ^= 1u;
@@ -234,8 +228,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
     const int w = warp;
     const int G = a.G, Hq = a.Hq;
     const int BR = p.BR, br_shift = p.br_shift;
-    const uint32_t PBB = FP8 ? (uint32_t)(2 * BR * D) : (uint32_t)(2 * Gm::DH * BR * 128);
-    uint8_t* conv = smem + kNS * Gm::SB + w * Gm::CONV;  // fp8 only
+    const uint32_t PBB = (uint32_t)(2 * Gm::DH * BR * 128);
     int s = 0;
     uint32_t ph = 0, mph = 0;
     uint32_t qf[D / 16][4];
@@ -260,13 +253,6 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
                 const int c = 2 * kd + (lane >> 4);
                 const uint32_t line = (uint32_t)((c >> 3) * 16 + r);
                 ldsm_x4(st_base + swz128(line, c & 7), qf[kd][0], qf[kd][1], qf[kd][2], qf[kd][3]);
-                if constexpr (FP8) {
-                    // bf16 q rounded to f16 for the f16 MMAs (q already f16: as it is)
-                    if (!a.q_f16) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) qf[kd][k] = bf16x2_to_f16x2(qf[kd][k]);
-                    }
-                }
             }
 #pragma unroll
             for (int i = 0; i < D / 8; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
@@ -281,70 +267,24 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
         const bool any_in = kw < kv_end && kw + 16 > kv_begin;
         if (any_in) {
             const bool partial = kw < kv_begin || kw + 16 > kv_end;
-            uint32_t kb, vb;  // bases of row 0 for the ldmatrix address helpers below
-            if constexpr (FP8) {
-                // 8-bit -> f16 into this warp's buffer: [K 16 rows][V 16 rows] of D f16, swizzled.
-                // A lane converts 16 consecutive bytes of one (row, K/V) unit; loads are issued
-                // in batches before any conversion so that shared-memory latency overlaps.
-                constexpr int LPR = D / 16, UPP = 32 / LPR, NPASS = 32 / UPP, BATCH = D == 256 ? 2 : 4;
-                static_assert(NPASS % BATCH == 0, "conversion passes");
-                const int e = lane % LPR, u0 = lane / LPR;
-                // lanes of odd (e / 4) store their second 16-byte chunk first: each 8-lane store
-                // phase then covers all 32 banks
-                const bool sw = (e >> 2) & 1;
-#pragma unroll
-                for (int pb = 0; pb < NPASS; pb += BATCH) {
-                    uint4 v[BATCH];
-#pragma unroll
-                    for (int i = 0; i < BATCH; ++i) {
-                        const int u = u0 + (pb + i) * UPP;  // unit: K rows 0..15, then V rows 0..15
-                        const int kv = u >> 4, row = u & 15;
-                        const int kk = 16 * w + row;
-                        const int b = kk >> br_shift, r = kk & (BR - 1);
-                        v[i] = *reinterpret_cast<const uint4*>(smem + (kv_base - smem0) + b * PBB + kv * BR * D +
-                                                               r * D + e * 16);
-                    }
-#pragma unroll
-                    for (int i = 0; i < BATCH; ++i) {
-                        const int u = u0 + (pb + i) * UPP;
-                        const int kv = u >> 4, row = u & 15;
-                        const int j = kw + row;
-                        const uint32_t a0 = sw ? v[i].z : v[i].x, a1 = sw ? v[i].w : v[i].y;
-                        const uint32_t b0 = sw ? v[i].x : v[i].z, b1 = sw ? v[i].y : v[i].w;
-                        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-                        if (j >= kv_begin && j < kv_end) {
-                            o0 = cvt8x8_to_f16x8<KT>(a0, a1);
-                            o1 = cvt8x8_to_f16x8<KT>(b0, b1);
-                        }
-                        uint8_t* rowp = conv + kv * (16 * D * 2) + row * (D * 2);
-                        const int c1 = 2 * e + (sw ? 1 : 0), c2 = 2 * e + (sw ? 0 : 1);
-                        *reinterpret_cast<uint4*>(rowp + (((c1 ^ row) & 7) | (c1 & ~7)) * 16) = o0;
-                        *reinterpret_cast<uint4*>(rowp + (((c2 ^ row) & 7) | (c2 & ~7)) * 16) = o1;
-                    }
+            if (partial) {
+                // keys of this slice outside [kv_begin, kv_end): V rows to zero
+                for (int i = lane; i < 16 * Gm::DH * 8; i += 32) {
+                    const int row = i / (Gm::DH * 8);
+                    const int c = i % (Gm::DH * 8);
+                    const int j = kw + row;
+                    if (j >= kv_begin && j < kv_end) continue;
+                    const int kk = 16 * w + row;
+                    const int b = kk >> br_shift, r = kk & (BR - 1);
+                    const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
+                    *reinterpret_cast<uint4*>(smem + (kv_base - smem0) + b * PBB + swz128(line, c & 7)) =
+                        make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
                 __syncwarp();
-                kb = smem_u32(conv);
-                vb = kb + 16 * D * 2;
-            } else {
-                if (partial) {
-                    // keys of this slice outside [kv_begin, kv_end): V rows to zero
-                    for (int i = lane; i < 16 * Gm::DH * 8; i += 32) {
-                        const int row = i / (Gm::DH * 8);
-                        const int c = i % (Gm::DH * 8);
-                        const int j = kw + row;
-                        if (j >= kv_begin && j < kv_end) continue;
-                        const int kk = 16 * w + row;
-                        const int b = kk >> br_shift, r = kk & (BR - 1);
-                        const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
-                        *reinterpret_cast<uint4*>(smem + (kv_base - smem0) + b * PBB + swz128(line, c & 7)) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                kb = kv_base;
-                vb = kv_base;
             }
+            // bases of row 0 for the ldmatrix addresses below (K and V blocks of the stage's page runs)
+            const uint32_t kb = kv_base, vb = kv_base;
 
             // ---- S = Q K^T  (16 rows x 16 keys); even and odd k-steps accumulate separately
             // (two independent MMA chains per n-block), summed at the end -- at D 64: at D 128 and 256
@@ -361,15 +301,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
 #pragma unroll
                 for (int kd = 0; kd < D / 16; ++kd) {
                     const int c = 2 * kd + ((lane >> 3) & 1);
-                    uint32_t addr;
-                    if constexpr (FP8) {
-                        addr = kb + row * (D * 2) + ((((c ^ row) & 7) | (c & ~7)) * 16);
-                    } else {
-                        const int kk = 16 * w + row;
-                        const int b = kk >> br_shift, r = kk & (BR - 1);
-                        const uint32_t line = (uint32_t)((c >> 3) * BR + r);
-                        addr = kb + b * PBB + swz128(line, c & 7);
-                    }
+                    const int kk = 16 * w + row;
+                    const int b = kk >> br_shift, r = kk & (BR - 1);
+                    const uint32_t line = (uint32_t)((c >> 3) * BR + r);
+                    const uint32_t addr = kb + b * PBB + swz128(line, c & 7);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4(addr, b0, b1, b2, b3);
                     mma16816<F16>((kTwo && (kd & 1)) ? sodd[0] : sacc[0], qf[kd], b0, b1);
@@ -454,15 +389,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
 #pragma unroll
                 for (int nd2 = 0; nd2 < D / 16; ++nd2) {
                     const int c = 2 * nd2 + (lane >> 4);
-                    uint32_t addr;
-                    if constexpr (FP8) {
-                        addr = vb + row * (D * 2) + ((((c ^ row) & 7) | (c & ~7)) * 16);
-                    } else {
-                        const int kk = 16 * w + row;
-                        const int b = kk >> br_shift, r = kk & (BR - 1);
-                        const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
-                        addr = vb + b * PBB + swz128(line, c & 7);
-                    }
+                    const int kk = 16 * w + row;
+                    const int b = kk >> br_shift, r = kk & (BR - 1);
+                    const uint32_t line = (uint32_t)((Gm::DH + (c >> 3)) * BR + r);
+                    const uint32_t addr = vb + b * PBB + swz128(line, c & 7);
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(addr, b0, b1, b2, b3);
                     mma16816<F16>(o_acc[2 * nd2], pa, b0, b1);
@@ -474,8 +404,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& kvmap, const CUte
         const uint32_t eb = smem_u32(&empty_bar[s]);
         if (st == nst - 1) {
             // ---- merge the four warps' partials; the stage's own buffers hold them
-            float* red_o = FP8 ? reinterpret_cast<float*>(smem + kNS * Gm::SB)
-                               : reinterpret_cast<float*>(smem + (kv_base - smem0));  // [kCW][16][D]
+            float* red_o = reinterpret_cast<float*>(smem + (kv_base - smem0));  // [kCW][16][D]
             float* red_ml = reinterpret_cast<float*>(smem + (st_base - smem0));        // [kCW][16][2]
             float lsum[2];
 #pragma unroll
@@ -831,18 +760,12 @@ struct DecKern {
     }
 };
 
-// The instantiations in use: 2-byte K/V at D 64 / 128 / 256 with 8- or 16-row tiles; 8-bit K/V
-// at D 64 with 16-row tiles (at D 128 / 256 the 8-bit tensor-memory prefill kernel takes the
-// decode rows).  `op` is called with the kernel type, or the result is cudaErrorInvalidValue.
+// The instantiations: 2-byte K/V at D 64 / 128 / 256 with 8- or 16-row tiles (8-bit K/V take the
+// 64-key-tile tensor-memory kernel).  `op` is called with the kernel type, or the result is
+// cudaErrorInvalidValue.
 template <typename Op>
 cudaError_t dec_dispatch(int D, int kt, int rows, Op op) {
-    if (kt_8bit(kt)) {
-        if (rows != 16 || D != 64) return cudaErrorInvalidValue;
-        if (kt == KT_E4M3) return op(DecKern<64, KT_E4M3, 16>{});
-        if (kt == KT_E5M2) return op(DecKern<64, KT_E5M2, 16>{});
-        if (kt == KT_I8) return op(DecKern<64, KT_I8, 16>{});
-        return cudaErrorInvalidValue;
-    }
+    if (kt_8bit(kt)) return cudaErrorInvalidValue;
     const bool f16 = kt == KT_F16;
     if (rows == 8) {
         if (D == 64) return f16 ? op(DecKern<64, KT_F16, 8>{}) : op(DecKern<64, KT_BF16, 8>{});

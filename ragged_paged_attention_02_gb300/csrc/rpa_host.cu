@@ -152,7 +152,7 @@ int rpa_validate_cfg(const RpaCfg* c) {
     } else {
         if (c->kv_layout != RPA_KV_SPLIT) return RPA_ERR_UNSUPPORTED;
         if (c->v_head_dim != 0 && c->v_head_dim != c->head_dim) return RPA_ERR_UNSUPPORTED;
-        if (G > kPfRows) return RPA_ERR_UNSUPPORTED;
+        if (G > kMaxGroup) return RPA_ERR_UNSUPPORTED;
         if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return RPA_ERR_UNSUPPORTED;
         if (c->page_size % 4) return RPA_ERR_UNSUPPORTED;  // page runs of the gather are >= 4 slots
     }

@@ -80,7 +80,7 @@ constexpr int kDecRows = 16;       // rows of a decode tile (one m16 MMA tile)
 constexpr int kMlaDqk = 576;
 constexpr int kMlaDv = 512;
 constexpr int kMlaRows = 16;
-constexpr int kPfRows = 64;        // rows of a prefill tile (4 warps x 16)
+constexpr int kMaxGroup = 64;      // query heads per kv head (a prefill tile holds 128 / G tokens)
 constexpr int kDecWaves = 4;       // target decode items per resident CTA (the most of any kernel)
 // ... on the 64-key-tile kernel, whose items pay a Q load into tensor memory and a pipeline ramp
 // each, and whose decode rows cost a full tile's tensor work: fewer, longer pieces (fp8_window
@@ -97,7 +97,7 @@ constexpr int kPlanThreads = 512;
 // both kernels running at once (chunked prefill of 512 tokens beside long decodes, D 128):
 // lower than either kernel alone, which shares no SMs, L2 or HBM bandwidth.
 constexpr int kPfSmGflopsTc = 6500;
-constexpr int kPfSmGflopsMma = 800;
+constexpr int kPfSmGflopsMma = 800;  // the latent kernel (warp MMAs)
 constexpr int kDecSmGBs = 78;
 constexpr int kHbmGBs = 6700;
 
@@ -220,8 +220,6 @@ cudaError_t launch_pdl(Kern k, int grid, int block, size_t smem, cudaStream_t st
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t st, size_t smem);
-// kt: KvType of kv_pages
-cudaError_t launch_prefill(const AttnParams& p, int kt, const Launch& l);
 constexpr int kCombCtasPerSm = 4;  // combine CTAs resident per SM (its register budget: 64)
 cudaError_t launch_combine(const CombParams& p, const Launch& l);
 // rows: query rows of a decode tile, 16 (any) or 8 (2-byte K/V, G <= 8: keys on the MMA's M side)
@@ -248,7 +246,6 @@ int encode_kv_map_runs(CUtensorMap* m, const void* kv, int byte_elems, long long
 // row, all its column blocks
 int encode_kv_map_heads(CUtensorMap* m, const void* kv, long long N, int ps, int H, int D, int BR);
 // occupancy / attributes (call once per device)
-cudaError_t attn_prepare(int D, int kt, int* pf_blocks_per_sm);
 size_t plan_smem_bytes();
 cudaError_t plan_prepare();
 

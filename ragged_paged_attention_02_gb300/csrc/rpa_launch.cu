@@ -114,12 +114,10 @@ void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks) {
     ks->dec_rows = (!eight && ks->G <= 8) ? 8 : kDecRows;
     ks->Tt = ks->G <= ks->dec_rows ? ks->dec_rows / ks->G : 1;
     ks->tc = (!ks->mla && !eight && (ks->D == 64 || ks->D == 128)) ? 1 : 0;
-    // the 64-key-tile tensor-memory kernel: 8-bit K/V at D 128 / 256 (converted to f16), and 2-byte
-    // K/V at D 256 (copied straight into its tiles)
-    ks->tc8 = (!ks->mla && ((eight && (ks->D == 128 || ks->D == 256)) || (!eight && ks->D == 256))) ? 1 : 0;
-    ks->pf_tokens = ks->tc    ? 2 * (kTcRows / ks->G)
-                    : ks->tc8 ? kTcRows / ks->G
-                              : (kPfRows / ks->G > 0 ? kPfRows / ks->G : 1);
+    // the 64-key-tile tensor-memory kernel: 8-bit K/V (converted to f16), and 2-byte K/V at D 256
+    // (copied straight into its tiles)
+    ks->tc8 = (!ks->mla && (eight || ks->D == 256)) ? 1 : 0;
+    ks->pf_tokens = ks->tc ? 2 * (kTcRows / ks->G) : kTcRows / ks->G;
     if (ks->mla) {
         // every sequence is planned in tiles of 16 query rows; the split-KV rule takes those with
         // q_len * G' <= 16
@@ -133,10 +131,9 @@ void kernels_choose(const RpaCfg& c, int sms, KernelSet* ks) {
 cudaError_t kernels_occupancy(KernelSet* ks) {
     cudaError_t e = plan_prepare();
     if (e != cudaSuccess) return e;
-    e = ks->mla   ? mla_prepare(ks->kt, &ks->pf_bps)
-        : ks->tc  ? prefill_tc_prepare(ks->D, ks->kt, &ks->pf_bps)
-        : ks->tc8 ? prefill_tc8_prepare(ks->D, ks->kt, &ks->pf_bps)
-                  : attn_prepare(ks->D, ks->kt, &ks->pf_bps);
+    e = ks->mla  ? mla_prepare(ks->kt, &ks->pf_bps)
+        : ks->tc ? prefill_tc_prepare(ks->D, ks->kt, &ks->pf_bps)
+                 : prefill_tc8_prepare(ks->D, ks->kt, &ks->pf_bps);
     if (e != cudaSuccess) return e;
     if (ks->tc8 || ks->mla) {
         // the 8-bit tensor-memory kernel (and the latent kernel) takes the decode rows too: the
@@ -226,11 +223,11 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
     pp.n_sms = ks.sms;
     pp.dec_bps = ks.dec_bps;
     pp.pf_bps = ks.pf_bps;
-    pp.pf_mma_rows = ks.tc ? 2 * kTcRows : ks.tc8 ? kTcRows : ks.mla ? kMlaRows : kPfRows;
+    pp.pf_mma_rows = ks.tc ? 2 * kTcRows : ks.mla ? kMlaRows : kTcRows;
     pp.dec_on_pf = ks.tc8 || ks.mla;
     pp.D = ks.D;
     pp.kv_elt = kt_8bit(ks.kt) ? 1 : 2;
-    pp.pf_sm_gflops = (ks.tc || ks.tc8) ? kPfSmGflopsTc : kPfSmGflopsMma;
+    pp.pf_sm_gflops = ks.mla ? kPfSmGflopsMma : kPfSmGflopsTc;
     pp.dec_sm_gbs = kDecSmGBs;
     pp.hbm_gbs = kHbmGBs;
     pp.force_pf_sms = eo.force_pf_sms;
@@ -381,7 +378,7 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
             tp.Tq = ks.pf_tokens;
             tp.timeout_ns = eo.timeout_ns;
             e = launch_mla(maps->kv, maps->q, tp, ks.kt, Launch{ks.sms * ks.pf_bps, st});
-        } else if (ks.tc || ks.tc8) {
+        } else {
             TcParams tp;
             tp.a = ap;
             tp.BR = ks.BR;
@@ -392,8 +389,6 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
             e = ks.tc ? launch_prefill_tc(maps->kv_pf, maps->q_pf, tp, ks.kt, Launch{ks.sms * ks.pf_bps, st})
                       : launch_prefill_tc8(byte_kv ? maps->kv : maps->kv_pf, maps->q_pf, tp, ks.kt,
                                            Launch{ks.sms * ks.pf_bps, st});
-        } else {
-            e = launch_prefill(ap, ks.kt, Launch{ks.sms * ks.pf_bps, st});
         }
         if (e != cudaSuccess) return fail(RPA_ERR_CUDA);
     }

@@ -12,7 +12,7 @@
 //   producer warp    Q tile (bf16) into a staging buffer, then per 64-key tile
 //                    the raw 8-bit K/V rows of each page run (one bulk tensor
 //                    copy per run: K and V of the head) into a ring of raw
-//                    stages (2 at D 256, 4 at D 128).
+//                    stages (2 at D 256, 4 at D 128, 8 at D 64).
 //   8 converter      Q (warps on lane quadrants 0-3): bf16 -> f16 (f16 q as it
 //   warps            is) into TMEM (the A operand of S = Q K^T).  K and V: each
 //                    warp takes 8 key rows of a tile into registers (the
@@ -38,7 +38,7 @@
 // converter warps only zero the V rows of keys outside [kv_begin, kv_end) on
 // a tile's edges before signalling V ready (K rows there are masked in S).
 //
-// TMEM: Q (D/2 columns of packed 16-bit pairs), S0, S1 (64 each), O (D) --
+// TMEM: Q (D/2 columns of packed 16-bit pairs, 64 at least), S0, S1 (64 each), O (D) --
 // 512 columns at D = 256.  All waits are bounded; on expiry the status word
 // gets RPA_ERR_TIMEOUT.
 #include <cuda.h>
@@ -64,6 +64,7 @@ constexpr int kRegBoundThreads = 640;
 constexpr int kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
 constexpr uint32_t kIssueNapNs = 100;  // longest suspension of the MMA thread's idle wait
+constexpr int kMaxRaw = 8;             // raw 8-bit stages (the ring at D 64)
 
 enum Meta8 : int { eSeq = 0, eHead, eQStart, eQl, eKl, eKvBegin, eKvEnd, eTok0, eNtok, eNt, eKey0, eStop, ePart };
 
@@ -76,19 +77,22 @@ struct G8 {
     static constexpr int T16 = CB * kBN * 128;         // one f16 K (or V) tile
     // Ring depths.  Direct mode: 3 K and 3 V tiles (the copies land in them, so a third buffer
     // starts each tile's copies a tile earlier).  8-bit mode: the raw stages hold the copies in
-    // flight (2 at D 256; 4 at D 128, whose stages are half the bytes), then 2 K tiles (K(t)
+    // flight (2 at D 256; 4 at D 128 and 8 at D 64, the same bytes), then 2 K tiles (K(t)
     // converted once QK(t-2) is done) and 2 V tiles (V(t) once PV(t-2) is done).  A third raw
     // stage at D 256 (in place of a K tile) measured no faster: there the converter and softmax
     // warps, not the copies, set a tile's time
-    static constexpr int NRAW = DIRECT ? 0 : (D == 256 ? 2 : 4);
+    static constexpr int NRAW = DIRECT ? 0 : 512 / D;
     static constexpr int NBK = DIRECT ? 3 : 2;
     static constexpr int NBV = DIRECT ? 3 : 2;
     static constexpr int DATA = QSTAGE + NRAW * RAW + (NBK + NBV) * T16;
     static constexpr int SMEM = DATA + 1024;
-    static constexpr uint32_t TM_Q = 0;                // Q: D/2 columns
-    static constexpr uint32_t TM_S0 = D / 2, TM_S1 = D / 2 + kBN;
-    static constexpr uint32_t TM_O = D / 2 + 2 * kBN;  // O: D columns
-    static_assert(D / 2 + 2 * kBN + D <= kTmemCols, "TMEM budget");
+    // TMEM columns: Q (D/2 of packed 16-bit pairs, in a slot of at least 64), S0, S1, O (D)
+    static constexpr uint32_t QC = D / 2 < 64 ? 64 : D / 2;
+    static constexpr uint32_t TM_Q = 0;
+    static constexpr uint32_t TM_S0 = QC, TM_S1 = QC + kBN;
+    static constexpr uint32_t TM_O = QC + 2 * kBN;
+    static_assert(QC + 2 * kBN + D <= kTmemCols, "TMEM budget");
+    static_assert(NRAW <= kMaxRaw, "raw stage barriers");
     static_assert(DATA + 1024 + 4096 <= 227 * 1024, "shared memory budget (dynamic + static)");
 };
 
@@ -207,7 +211,7 @@ __global__ void __launch_bounds__(kRegBoundThreads, 1) rpa_prefill_tc8(const __g
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t meta_full[2], meta_free[2];
     __shared__ __align__(8) uint64_t q_full, q_empty, q_ready, qt_free;
-    __shared__ __align__(8) uint64_t raw_full[4], raw_empty[4];
+    __shared__ __align__(8) uint64_t raw_full[kMaxRaw], raw_empty[kMaxRaw];
     // per S buffer (t mod 2): QK done, P ready (softmax warps; in 8-bit mode also V converted: the
     // converter warps), PV done; per K/V buffer (t mod NB): K ready, and in direct mode V copied, V
     // ready (its edge rows zeroed: converter warps) and the K / V buffer free again (the MMAs that
@@ -933,7 +937,7 @@ struct Tc8Kern {
     }
 };
 
-// 8-bit K/V (e4m3, e5m2, int8) at D 128 / 256; 2-byte K/V (bf16, f16) at D 256 in direct mode
+// 8-bit K/V (e4m3, e5m2, int8) at D 64 / 128 / 256; 2-byte K/V (bf16, f16) at D 256 in direct mode
 template <int D, typename Op>
 cudaError_t tc8_dispatch_kt(int kt, Op op) {
     if (kt == KT_E4M3) return op(Tc8Kern<D, KT_E4M3>{});
@@ -947,6 +951,7 @@ cudaError_t tc8_dispatch_kt(int kt, Op op) {
 }
 template <typename Op>
 cudaError_t tc8_dispatch(int D, int kt, Op op) {
+    if (D == 64) return tc8_dispatch_kt<64>(kt, op);
     if (D == 128) return tc8_dispatch_kt<128>(kt, op);
     if (D == 256) return tc8_dispatch_kt<256>(kt, op);
     return cudaErrorInvalidValue;

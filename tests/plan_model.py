@@ -26,12 +26,12 @@ PF_SM_GFLOPS_TC, PF_SM_GFLOPS_MMA, DEC_SM_GBS, HBM_GBS = 6500, 800, 78, 6700
 def split(prob, dec_keyheads, pf_keys, n_sms, dec_bps, pf_bps, concurrent, force_pf=0, force_dec=0):
     """(prefill CTAs, decode CTAs): minimise max(prefill time, decode time) over the
     prefill SM count, integer nanoseconds, first minimum wins."""
-    tc = prob.kv_dtype == "bf16" and prob.head_dim in (64, 128)
+    latent = getattr(prob, "kv_layout", "split") == "latent"
+    kv_elt = 2 if prob.kv_dtype in ("bf16", "f16") else 1
+    tc = not latent and kv_elt == 2 and prob.head_dim in (64, 128)
     D, Hkv = prob.head_dim, prob.num_kv_heads
-    kv_elt = 2 if prob.kv_dtype == "bf16" else 1
-    tc8 = prob.kv_dtype != "bf16" and prob.head_dim in (128, 256)
-    pf_rows = 256 if tc else 128 if tc8 else 64
-    rate = PF_SM_GFLOPS_TC if (tc or tc8) else PF_SM_GFLOPS_MMA
+    pf_rows = 256 if tc else 16 if latent else 128
+    rate = PF_SM_GFLOPS_MMA if latent else PF_SM_GFLOPS_TC
     dec_bytes = dec_keyheads * 2 * D * kv_elt
     pf_flops = pf_keys * Hkv * pf_rows * 4 * D
     pf_sms = dec_sms = n_sms

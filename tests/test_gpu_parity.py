@@ -78,7 +78,7 @@ SMALL = [
               sliding_window=400, sm_scale=1 / 16)),
     (48, dict(num_seqs=10, max_q=40, max_kv=1200, num_q_heads=16, num_kv_heads=4, head_dim=128,
               page_size=32, kv_dtype="fp8_e4m3", k_scale=0.08, v_scale=0.1)),
-    # fp8 K/V at D 64: the mma.sync decode kernel and the warp-MMA prefill
+    # fp8 K/V at D 64 on the tensor-memory kernel (one 128-byte column block a row; decode rows too)
     (70, dict(num_seqs=8, max_q=40, max_kv=900, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
               kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, soft_cap=20.0, sliding_window=300)),
     (71, dict(num_seqs=10, decode_only=True, max_kv=3000, num_q_heads=8, num_kv_heads=2, head_dim=64,
@@ -96,7 +96,7 @@ SMALL = [
               page_size=16, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
     # attention sinks on every kernel: 8-row decode tiles and the bf16 tensor-memory prefill; 16-row
     # decode tiles with split pieces (the combine kernel adds the sink once); the fp8 tensor-memory
-    # kernel with split pieces, soft cap and window; the warp-MMA prefill (bf16 D 256, fp8 D 64)
+    # kernel with split pieces, soft cap and window; its direct mode (bf16 D 256) and D 64 (fp8)
     (76, dict(num_seqs=10, max_q=200, max_kv=2500, num_q_heads=16, num_kv_heads=4, head_dim=128, sinks=True)),
     (77, dict(num_seqs=8, max_q=2, max_kv=5000, num_q_heads=32, num_kv_heads=2, head_dim=128, sinks=True)),
     (78, dict(num_seqs=12, max_q=40, max_kv=5000, num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=16,
@@ -105,6 +105,12 @@ SMALL = [
     (79, dict(num_seqs=5, max_q=70, max_kv=900, num_q_heads=8, num_kv_heads=2, head_dim=256, sinks=True)),
     (80, dict(num_seqs=8, max_q=30, max_kv=3000, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=16,
               kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, sinks=True)),
+    # fp8 K/V at D 64 with G 32 (4-token query tiles) over page runs of 4 keys (16 copies a tile),
+    # non-causal; and G 16 decode rows over long keys (split pieces, sinks)
+    (82, dict(num_seqs=7, max_q=10, max_kv=2500, num_q_heads=32, num_kv_heads=1, head_dim=64, page_size=4,
+              kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, is_causal=False)),
+    (83, dict(num_seqs=6, decode_only=True, max_kv=7000, num_q_heads=16, num_kv_heads=1, head_dim=64,
+              page_size=64, kv_dtype="fp8_e4m3", k_scale=0.06, v_scale=0.05, sinks=True)),
     (81, dict(num_seqs=16, decode_only=True, max_kv=8000, num_q_heads=32, num_kv_heads=8, head_dim=128,
               sinks=True)),
 ]
@@ -120,9 +126,9 @@ def test_small_cases_all_rows(case):
 
 
 # Element types (q / o, and K/V) on every kernel that serves them.  f16 K/V: f16 MMAs on the 8- and
-# 16-row decode tiles, the tensor-memory prefill (D 64, 128) and the warp-MMA prefill (D 256).
-# e5m2 and int8 K/V: the 8-bit tensor-memory prefill (D 128, 256; decode rows too, split pieces)
-# and the D 64 decode / warp-MMA prefill.  q of another type than the MMA operand type: rounded
+# 16-row decode tiles, the tensor-memory prefill (D 64, 128) and the 64-key-tile kernel's direct
+# mode (D 256).  e5m2 and int8 K/V: the 8-bit tensor-memory kernel (D 64, 128, 256; decode rows
+# too, split pieces).  q of another type than the MMA operand type: rounded
 # into the workspace first (f32 q; f16 q with bf16 K/V; bf16 q with f16 K/V); f16 q with 8-bit K/V
 # read as it is.  o has q's type.
 DTYPE_CASES = [
@@ -356,6 +362,9 @@ def test_full_workloads(name):
     (dict(num_q_heads=32, num_kv_heads=2, head_dim=128), 2, 1),
     (dict(num_q_heads=16, num_kv_heads=1, kv_layout="latent", head_dim=576, v_head_dim=512, page_size=64,
           sm_scale=1 / 24), None, 1),
+    # 8-bit K/V: the 64-key-tile kernel takes the decode rows too (one CTA per SM), D 64 and 256
+    (dict(num_q_heads=8, num_kv_heads=2, head_dim=64, kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05), 1, 1),
+    (dict(num_q_heads=16, num_kv_heads=8, head_dim=256, kv_dtype="int8", k_scale=0.04, v_scale=0.04), 1, 1),
 ])
 def test_resident_ctas_per_sm_as_designed(kw, dec_bps, pf_bps):
     """The kernels' register and shared-memory budgets give the occupancy they were designed for

@@ -7,9 +7,9 @@ rpa_forward.  Its workspace is a fixed 32 MiB array inside the library.  This
 test calls it through the C ABI, twice in a row per case, and checks each
 output against the fp64 oracle and against the handle-based rpa_forward, at
 the tolerance of the other parity tests.  The cases reach every kernel branch
-of the entry point: the bf16 tensor-memory prefill, the warp-MMA prefill (bf16
-D 256), the fp8 tensor-memory prefill, 8- and 16-row decode tiles and split-KV
-pieces.  An oversized configuration is refused.
+of the entry point: the bf16 tensor-memory prefill, the 64-key-tile kernel
+(fp8, and bf16 at D 256), the latent kernel, 8- and 16-row decode tiles and
+split-KV pieces.  An oversized configuration is refused.
 """
 import ctypes
 
@@ -54,7 +54,7 @@ CASES = {
     "fp8_mixed": (61, dict(num_seqs=8, max_q=80, max_kv=900, num_q_heads=16, num_kv_heads=8, head_dim=256,
                            kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0,
                            sliding_window=300, sm_scale=1 / 16)),
-    # bf16 at D 256: the warp-MMA prefill
+    # bf16 at D 256: the 64-key-tile kernel in direct mode
     "bf16_d256": (62, dict(num_seqs=6, max_q=70, max_kv=800, num_q_heads=8, num_kv_heads=4, head_dim=256,
                            soft_cap=30.0, sm_scale=1 / 16)),
     # bf16 with G = 16: 16-row decode tiles beside the bf16 tensor-memory prefill

@@ -1,7 +1,7 @@
 // rpa_internal.cuh -- shared definitions of the CUDA side of librpa.
 //
-// Plan layout, kernel parameters and the small PTX helpers (cp.async,
-// ldmatrix, mma.sync, ex2) used by the attention kernels.
+// Plan layout, kernel parameters and the small PTX helpers (mbarrier, bulk
+// tensor copies, tcgen05, ldmatrix, mma.sync, ex2) used by the kernels.
 #pragma once
 
 #include <cuda.h>
@@ -325,17 +325,6 @@ int enqueue_forward(const RpaCfg& c, const KernelSet& ks, const Workspace& ws, M
 #ifdef __CUDACC__
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    // zero-fill when !valid (src-size 0): nothing is read from src
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
@@ -702,9 +691,6 @@ __host__ __device__ constexpr uint32_t umma_idesc_f16(int M, int N, int a_mn, in
     return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
-}
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem),
                  "r"(ncols)
@@ -720,23 +706,8 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, int acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// The same with the B descriptor as its two 32-bit halves and a compile-time accumulate flag:
+// D[tmem] (+)= A[tmem] * B[smem], the B descriptor as its two 32-bit halves and a compile-time
+// accumulate flag:
 // an issuing thread that shares its sub-partition with busy warps gets few issue slots, so the
 // per-MMA work is kept to an address add or two (the caller offsets the low half, which holds
 // the start address, by a constant per MMA).

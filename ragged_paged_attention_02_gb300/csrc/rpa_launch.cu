@@ -7,19 +7,19 @@
 //   [q conversion]  only when q's type is not the MMA operand type the kernels read (f32 q, or a
 //                   16-bit q of the other 16-bit type): q rounded into the workspace
 //   planner         work items, split-KV pieces, SM split
-//   decode          (2-byte K/V: 8- or 16-row tiles; 8-bit K/V at D 64) -- behind the prefill
+//   decode          (2-byte K/V at D 64 / 128 / 256: 8- or 16-row tiles) -- behind the prefill
 //                   kernel when decode and prefill run concurrently
-//   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128; 8-bit K/V at D 128 / 256 and
-//                   2-byte K/V at D 256, which also take the decode rows), the latent-attention
-//                   kernel (latent layout, every row) or the warp-MMA kernel (8-bit K/V at D 64)
+//   prefill         tensor-memory kernels (2-byte K/V at D 64 / 128; 8-bit K/V and 2-byte K/V at
+//                   D 256, which also take the decode rows) or the latent-attention kernel (latent
+//                   layout, every row)
 //   combine         split-KV merge, output of the uncovered rows
 //
 // Each kernel is a programmatic dependent of the one before it on the caller's stream (its
 // prologue overlaps the previous kernel's tail); the planner, of the previous call's combine
 // kernel when that is the stream's last work.  With concurrent decode / prefill the decode
 // kernel follows the prefill kernel and waits for the planner's published epoch instead of its
-// grid dependency; while per-kernel profile events are on, it runs on the side stream instead,
-// forked after the planner and joined before the combine.
+// grid dependency; while per-kernel profile events are on or the stream is being captured, it
+// runs on the side stream instead, forked after the planner and joined before the combine.
 //
 // Nothing here allocates: the caller owns the workspace.
 #include <string.h>

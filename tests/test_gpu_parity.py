@@ -757,3 +757,35 @@ def test_cuda_graph_replay_bit_equal_to_eager_calls(kind):
         assert np.array_equal(o_to_f64(o), ref[i]), f"replay {n} (batch {i})"
     del graph
     att.close()
+
+
+@pytest.mark.gpu
+def test_two_handles_on_two_streams_at_once():
+    """Two handles (one workspace each) called on two streams with no synchronisation between
+    them, each call's kernels free to share the GPU with the other handle's: every output bit-equal
+    to a synchronised call, and both statuses clean.  The concurrent decode / prefill split polls
+    a flag in its own handle's workspace only."""
+    import torch
+    from ragged_paged_attention_02_gb300 import RaggedPagedAttention
+
+    ps = _two_batches("concurrent")
+    ts = [to_dev(p) for p in ps]
+    atts = [RaggedPagedAttention(**p.cfg_dict()) for p in ps]
+    ref = []
+    for att, t, p in zip(atts, ts, ps):
+        ref.append(o_to_f64(att.forward(*t, p.num_seqs)))
+        torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [[], []]
+    for _ in range(8):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                outs[i].append(atts[i].forward(*ts[i], ps[i].num_seqs))
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert atts[i].status() == 0
+        for n, o in enumerate(outs[i]):
+            assert np.array_equal(o_to_f64(o), ref[i]), f"handle {i} call {n}"
+        atts[i].close()

@@ -111,6 +111,9 @@ SMALL = [
               kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, is_causal=False)),
     (83, dict(num_seqs=6, decode_only=True, max_kv=7000, num_q_heads=16, num_kv_heads=1, head_dim=64,
               page_size=64, kv_dtype="fp8_e4m3", k_scale=0.06, v_scale=0.05, sinks=True)),
+    # int8 K/V at D 64 with G 64 (2-token query tiles, 8 copies of each row), page runs of 8 keys, window
+    (84, dict(num_seqs=5, max_q=6, max_kv=1200, num_q_heads=64, num_kv_heads=1, head_dim=64, page_size=8,
+              kv_dtype="int8", k_scale=0.04, v_scale=0.04, sliding_window=500)),
     (81, dict(num_seqs=16, decode_only=True, max_kv=8000, num_q_heads=32, num_kv_heads=8, head_dim=128,
               sinks=True)),
 ]

@@ -119,6 +119,33 @@ SMALL = [
 ]
 
 
+# Page sizes that are not powers of two (multiples of 4, or of 8 for the latent layout): the gather's
+# page runs are the largest power of two dividing the page size (4, 8 or 16 slots), every run inside
+# one page, on each kernel: 8-row decode tiles with the bf16 128-key-tile prefill, 16-row decode
+# tiles, the 8-bit 64-key-tile kernel, its direct mode (bf16 D 256) and the latent kernel
+ODD_PAGES = [
+    (110, dict(num_seqs=8, max_q=150, max_kv=2500, num_q_heads=16, num_kv_heads=4, head_dim=128, page_size=48)),
+    (111, dict(num_seqs=10, max_q=2, max_kv=3000, num_q_heads=32, num_kv_heads=2, head_dim=128, page_size=12)),
+    (112, dict(num_seqs=8, max_q=60, max_kv=2500, num_q_heads=16, num_kv_heads=8, head_dim=256, page_size=24,
+               kv_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.05, soft_cap=50.0, sliding_window=900, sm_scale=1 / 16)),
+    (113, dict(num_seqs=6, max_q=80, max_kv=1500, num_q_heads=8, num_kv_heads=4, head_dim=256, page_size=80,
+               sm_scale=1 / 16)),
+    (114, dict(num_seqs=8, max_q=3, max_kv=3000, num_q_heads=16, num_kv_heads=1, head_dim=576, page_size=40,
+               kv_layout="latent", v_head_dim=512, sm_scale=1 / 24)),
+    (115, dict(num_seqs=7, max_q=40, max_kv=2000, num_q_heads=8, num_kv_heads=2, head_dim=64, page_size=20,
+               kv_dtype="int8", k_scale=0.04, v_scale=0.04)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(ODD_PAGES)))
+def test_page_sizes_not_powers_of_two(case):
+    seed, kw = ODD_PAGES[case]
+    p = ri.random_small(seed, **kw)
+    got, st = run(p)
+    assert st == 0
+    assert_close(got, oracle.forward(p), p.kv_dtype, f"page size {kw['page_size']}")
+
+
 @pytest.mark.parametrize("case", range(len(SMALL)))
 def test_small_cases_all_rows(case):
     seed, kw = SMALL[case]

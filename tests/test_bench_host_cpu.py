@@ -84,6 +84,18 @@ def test_kernel_sources_follow_the_routing():
     for (w, k), f in want.items():
         src = bench.kernel_sources(_shape_only(w), k)
         assert src[0].endswith(f) and src[1].endswith("rpa_internal.cuh"), (w, src)
+    # every 8-bit cache takes the 64-key-tile kernel, D 64 included; 2-byte K/V at D 64 / 128 the
+    # 128-key-tile kernel; every named file exists
+    import os
+    import types
+
+    for kv, d, f in (("fp8_e4m3", 64, "rpa_prefill_tc8.cu"), ("int8", 128, "rpa_prefill_tc8.cu"),
+                     ("fp8_e5m2", 256, "rpa_prefill_tc8.cu"), ("f16", 64, "rpa_prefill_tc.cu"),
+                     ("bf16", 128, "rpa_prefill_tc.cu"), ("f16", 256, "rpa_prefill_tc8.cu")):
+        src = bench.kernel_sources(types.SimpleNamespace(kv_dtype=kv, head_dim=d, kv_layout="split"),
+                                   "prefill_attention")
+        assert src[0].endswith(f), (kv, d, src)
+        assert all(os.path.isfile(os.path.join(bench.ROOT, x)) for x in src), src
 
 
 def _shape_only(name):

@@ -68,6 +68,9 @@ CASES = {
     # f32 q rounded into the fixed array before the kernels read it; e5m2 K/V; f32 o
     "f32_q_e5m2": (65, dict(num_seqs=8, max_q=40, max_kv=3000, num_q_heads=16, num_kv_heads=8, head_dim=256,
                             q_dtype="f32", kv_dtype="fp8_e5m2", k_scale=0.05, v_scale=0.05, sm_scale=1 / 16)),
+    # int8 K/V at D 64: the 64-key-tile kernel with one column block a row, decode rows split into pieces
+    "int8_d64": (67, dict(num_seqs=9, max_q=30, max_kv=4000, num_q_heads=8, num_kv_heads=2, head_dim=64,
+                          page_size=16, kv_dtype="int8", k_scale=0.04, v_scale=0.04)),
 }
 
 
